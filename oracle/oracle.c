@@ -1,0 +1,426 @@
+/*
+ * oracle.c -- plain, slow, obviously-correct CPU model of the decode-time
+ * Mixture-of-Experts layer with GPU expert slots.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark may load this file's library.  The CUDA path
+ * never calls it and shares no code, header, table or helper with it.
+ *
+ * Sources (page title, section):
+ *  - xinfer-ai docs/moe_offload.md, "How it works": per-layer GPU slots,
+ *    routed expert ids rewritten to slot ids, GEMMs over [num_slots, N, K]
+ *    slot tensors; "Placement never changes routing or precision".
+ *  - onnxruntime PR #33976 "hybrid GPU/CPU expert offload for MoEPacked",
+ *    "Key Changes": expert_to_slot map, slot < 0 = cold, cold routes are
+ *    skipped on the GPU and handled elsewhere.
+ *  - NInfer-Offload release notes v0.4.0 "expert cache": slots follow recent
+ *    routing, at most two refills per layer and call, replacing the least
+ *    used expert.
+ *  - tinyserve README, "How it works" 2-3: fused dequantise-and-multiply over
+ *    the native MXFP4 bytes (gate, up, down), frequency-recency eviction.
+ *  - MXFP4 itself (E2M1 elements, one E8M0 scale per 32 elements) is named by
+ *    the pages (xinfer "Supported": FusedMoeMxfp4; tinyserve README: native
+ *    MXFP4) but not defined there; the OCP Microscaling Formats (MX) v1.0
+ *    definition is used.
+ *  - The pages define no router or FFN formula.  The plain reading used here:
+ *    logits = x.Wr^T + b; the k largest logits (ties to the lower expert id);
+ *    softmax over the k selected logits; expert FFN
+ *    y = Wd . (SiLU(Wg . x) * (Wu . x)); output = sum of w * y over the
+ *    token's hot routes.
+ *
+ * Arithmetic: fp32 throughout with sums taken in ascending index order; the
+ * products bf16 x E2M1 x 2^k are exact in fp32.  Every function is written
+ * for a reader to check by eye, not for speed.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------- formats */
+
+/* E2M1 element (OCP MX v1.0): sign bit 3, exponent bits 2..1 (bias 1),
+ * mantissa bit 0.  Magnitudes of codes 0..7 are listed out in full. */
+static const float E2M1_MAGNITUDE[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+
+float oracle_e2m1(uint8_t code) {
+    float m = E2M1_MAGNITUDE[code & 7];
+    return (code & 8) ? -m : m;
+}
+
+/* E8M0 scale (OCP MX v1.0): 2^(e - 127); e = 255 is NaN. */
+float oracle_e8m0(uint8_t e) {
+    if (e == 255) return NAN;
+    return ldexpf(1.0f, (int)e - 127);
+}
+
+/* bf16 bit pattern -> fp32 (bf16 is the top half of an fp32). */
+float oracle_bf16_to_f32(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* fp32 -> bf16 bit pattern, round to nearest even (NaN kept quiet). */
+uint16_t oracle_f32_to_bf16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x40);
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7fffu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+/* One MXFP4 matrix [R, C]: codes [R, C/2] (column 2c in the low nibble of
+ * byte c, column 2c+1 in the high nibble), scales [R, C/32]. */
+float oracle_mxfp4_element(const uint8_t *codes, const uint8_t *scales, int C, int r, int c) {
+    uint8_t byte = codes[(size_t)r * (C / 2) + c / 2];
+    uint8_t code = (c & 1) ? (byte >> 4) : (byte & 15);
+    uint8_t sc = scales[(size_t)r * (C / 32) + c / 32];
+    return oracle_e2m1(code) * oracle_e8m0(sc);
+}
+
+void oracle_mxfp4_dequant(const uint8_t *codes, const uint8_t *scales, int R, int C, float *W) {
+    for (int r = 0; r < R; ++r)
+        for (int c = 0; c < C; ++c) W[(size_t)r * C + c] = oracle_mxfp4_element(codes, scales, C, r, c);
+}
+
+/* Expert record: [Wg codes, Wg scales, Wu codes, Wu scales, Wd codes, Wd scales]. */
+size_t oracle_expert_bytes(int H, int I) { return (size_t)3 * I * H * 17 / 32; }
+
+static void expert_sections(const uint8_t *rec, int H, int I, const uint8_t **gc, const uint8_t **gs,
+                            const uint8_t **uc, const uint8_t **us, const uint8_t **dc, const uint8_t **ds) {
+    size_t c = (size_t)I * H / 2, s = (size_t)I * H / 32;
+    *gc = rec;
+    *gs = rec + c;
+    *uc = rec + c + s;
+    *us = rec + 2 * c + s;
+    *dc = rec + 2 * c + 2 * s;
+    *ds = rec + 3 * c + 2 * s;
+}
+
+/* ----------------------------------------------------------------- router */
+
+/* logits[t, e] = sum_h x[t, h] * Wr[e, h] + b[e], fp32, ascending h. */
+void oracle_router_logits(const uint16_t *x, int M, int H, const float *Wr, const float *bias, int E,
+                          float *logits) {
+    for (int t = 0; t < M; ++t)
+        for (int e = 0; e < E; ++e) {
+            float acc = 0.0f;
+            for (int h = 0; h < H; ++h) acc = acc + oracle_bf16_to_f32(x[(size_t)t * H + h]) * Wr[(size_t)e * H + h];
+            logits[(size_t)t * E + e] = acc + (bias ? bias[e] : 0.0f);
+        }
+}
+
+/* The k largest logits of each token, largest first; equal logits go to the
+ * lower expert id.  Weights: softmax over the k selected logits (equal to the
+ * softmax over all E renormalised to the selected k), max-subtracted, fp32. */
+void oracle_topk_softmax(const float *logits, int M, int E, int k, int32_t *ids, float *w) {
+    char *taken = (char *)malloc((size_t)E);
+    for (int t = 0; t < M; ++t) {
+        const float *l = logits + (size_t)t * E;
+        memset(taken, 0, (size_t)E);
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || l[e] > l[best]) best = e; /* strict '>' keeps the lower id on ties */
+            }
+            taken[best] = 1;
+            ids[(size_t)t * k + j] = best;
+        }
+        float lmax = l[ids[(size_t)t * k]];
+        float den = 0.0f;
+        for (int j = 0; j < k; ++j) den = den + expf(l[ids[(size_t)t * k + j]] - lmax);
+        for (int j = 0; j < k; ++j) w[(size_t)t * k + j] = expf(l[ids[(size_t)t * k + j]] - lmax) / den;
+    }
+    free(taken);
+}
+
+/* ------------------------------------------------------------ compaction */
+
+/* Splits the routes by the expert_to_slot map (slot < 0 = cold).
+ *  hot:    (expert, slot, token, weight), ordered by (expert, token)
+ *  active: one entry per expert with at least one hot route, ascending expert,
+ *          with its slot, first hot index and hot count
+ *  cold:   (token, expert, weight), ordered by (token, expert)
+ *  hist:   all routes (hot and cold) per expert
+ * counts[0..2] = n_hot, n_cold, n_active. */
+void oracle_compact(const int32_t *ids, const float *w, int M, int k, const int32_t *e2s, int E,
+                    int32_t *hot_expert, int32_t *hot_slot, int32_t *hot_token, float *hot_w,
+                    int32_t *act_expert, int32_t *act_slot, int32_t *act_off, int32_t *act_cnt,
+                    int32_t *cold_token, int32_t *cold_expert, float *cold_w, int32_t *hist,
+                    int32_t *counts) {
+    int n_hot = 0, n_cold = 0, n_act = 0;
+    for (int e = 0; e < E; ++e) hist[e] = 0;
+    for (int i = 0; i < M * k; ++i) hist[ids[i]] += 1;
+    /* hot routes: experts ascending, tokens ascending inside an expert */
+    for (int e = 0; e < E; ++e) {
+        if (e2s[e] < 0) continue;
+        int first = n_hot;
+        for (int t = 0; t < M; ++t)
+            for (int j = 0; j < k; ++j)
+                if (ids[t * k + j] == e) {
+                    hot_expert[n_hot] = e;
+                    hot_slot[n_hot] = e2s[e];
+                    hot_token[n_hot] = t;
+                    hot_w[n_hot] = w[t * k + j];
+                    ++n_hot;
+                }
+        if (n_hot > first) {
+            act_expert[n_act] = e;
+            act_slot[n_act] = e2s[e];
+            act_off[n_act] = first;
+            act_cnt[n_act] = n_hot - first;
+            ++n_act;
+        }
+    }
+    /* cold routes: tokens ascending, experts ascending inside a token */
+    for (int t = 0; t < M; ++t)
+        for (int e = 0; e < E; ++e) {
+            if (e2s[e] >= 0) continue;
+            for (int j = 0; j < k; ++j)
+                if (ids[t * k + j] == e) {
+                    cold_token[n_cold] = t;
+                    cold_expert[n_cold] = e;
+                    cold_w[n_cold] = w[t * k + j];
+                    ++n_cold;
+                }
+        }
+    counts[0] = n_hot;
+    counts[1] = n_cold;
+    counts[2] = n_act;
+}
+
+/* ------------------------------------------------------------- expert FFN */
+
+static float silu(float g) { return g / (1.0f + expf(-g)); }
+
+/* h[i] = SiLU(sum_c Wg[i,c] x[c]) * (sum_c Wu[i,c] x[c]), fp32, ascending c. */
+void oracle_expert_gate_up(const uint8_t *rec, int H, int I, const uint16_t *x, float *h) {
+    const uint8_t *gc, *gs, *uc, *us, *dc, *ds;
+    expert_sections(rec, H, I, &gc, &gs, &uc, &us, &dc, &ds);
+    for (int i = 0; i < I; ++i) {
+        float g = 0.0f, u = 0.0f;
+        for (int c = 0; c < H; ++c) {
+            float xc = oracle_bf16_to_f32(x[c]);
+            g = g + oracle_mxfp4_element(gc, gs, H, i, c) * xc;
+            u = u + oracle_mxfp4_element(uc, us, H, i, c) * xc;
+        }
+        h[i] = silu(g) * u;
+    }
+}
+
+/* y[r] = sum_i Wd[r,i] h[i], fp32, ascending i. */
+void oracle_expert_down(const uint8_t *rec, int H, int I, const float *h, float *y) {
+    const uint8_t *gc, *gs, *uc, *us, *dc, *ds;
+    expert_sections(rec, H, I, &gc, &gs, &uc, &us, &dc, &ds);
+    for (int r = 0; r < H; ++r) {
+        float acc = 0.0f;
+        for (int i = 0; i < I; ++i) acc = acc + oracle_mxfp4_element(dc, ds, I, r, i) * h[i];
+        y[r] = acc;
+    }
+}
+
+void oracle_expert_ffn(const uint8_t *rec, int H, int I, const uint16_t *x, float *y) {
+    float *h = (float *)malloc(sizeof(float) * (size_t)I);
+    oracle_expert_gate_up(rec, H, I, x, h);
+    oracle_expert_down(rec, H, I, h, y);
+    free(h);
+}
+
+/* ------------------------------------------------------------ whole layer */
+
+/* One layer call: route, split by the map, run every hot route through its
+ * expert, combine.  `experts` holds the records of all E experts (indexed by
+ * expert id, so the result cannot depend on which slot holds an expert).
+ * out_f32[t, :] = sum over t's hot routes, ascending expert, of w * y;
+ * a token without hot routes gets zeros.  Also returns the routing and the
+ * compaction (arrays sized M*k, E, and 3 for counts). */
+void oracle_moe_layer(const uint16_t *x, int M, int H, int I, int E, int k, const float *Wr,
+                      const float *bias, const uint8_t *experts, const int32_t *e2s, float *out_f32,
+                      uint16_t *out_bf16, int32_t *ids, float *w, int32_t *hot_expert, int32_t *hot_slot,
+                      int32_t *hot_token, float *hot_w, int32_t *act_expert, int32_t *act_slot,
+                      int32_t *act_off, int32_t *act_cnt, int32_t *cold_token, int32_t *cold_expert,
+                      float *cold_w, int32_t *hist, int32_t *counts, float *logits_out) {
+    size_t eb = oracle_expert_bytes(H, I);
+    float *logits = (float *)malloc(sizeof(float) * (size_t)M * E);
+    oracle_router_logits(x, M, H, Wr, bias, E, logits);
+    if (logits_out) memcpy(logits_out, logits, sizeof(float) * (size_t)M * E);
+    oracle_topk_softmax(logits, M, E, k, ids, w);
+    oracle_compact(ids, w, M, k, e2s, E, hot_expert, hot_slot, hot_token, hot_w, act_expert, act_slot,
+                   act_off, act_cnt, cold_token, cold_expert, cold_w, hist, counts);
+    for (size_t i = 0; i < (size_t)M * H; ++i) out_f32[i] = 0.0f;
+    float *y = (float *)malloc(sizeof(float) * (size_t)H);
+    for (int r = 0; r < counts[0]; ++r) {
+        int t = hot_token[r];
+        oracle_expert_ffn(experts + (size_t)hot_expert[r] * eb, H, I, x + (size_t)t * H, y);
+        for (int c = 0; c < H; ++c) out_f32[(size_t)t * H + c] = out_f32[(size_t)t * H + c] + hot_w[r] * y[c];
+    }
+    if (out_bf16)
+        for (size_t i = 0; i < (size_t)M * H; ++i) out_bf16[i] = oracle_f32_to_bf16(out_f32[i]);
+    free(y);
+    free(logits);
+}
+
+/* --------------------------------------------------------------- slot cache */
+
+/* One step of the frequency/recency slot cache for one layer (NInfer v0.4.0
+ * "expert cache": experts the router keeps choosing are copied in, at most
+ * R per layer and call, replacing the least used; tinyserve "GPU LFRU
+ * cache": frequency with a recency component).
+ *
+ *  score[e] <- decay * score[e] + hist[e]          (decay = 1: plain LFU)
+ *  last[e]  <- step if hist[e] > 0
+ *  candidates: experts not resident and not in flight, with score above the
+ *              lowest resident score, highest score first, ties lower id
+ *  victims:    resident experts not in flight, lowest score first, ties to
+ *              the least recently routed (smaller last), then the lower slot
+ *  the i-th candidate replaces the i-th victim while its score is strictly
+ *  greater, at most R pairs.
+ *
+ * e2s/s2e are updated in place as if every chosen copy had completed (the
+ * deterministic visibility mode); in_flight (per expert, may be NULL) marks
+ * experts whose copy has not landed yet in the polled mode.
+ * Writes the chosen pairs to pair_expert/pair_slot/pair_victim and returns
+ * their number.  Double precision, no contraction, so that decay < 1 gives
+ * the same decisions on any host. */
+int oracle_cache_step(double *score, int64_t *last, int32_t *e2s, int32_t *s2e, int E, int S,
+                      const int32_t *hist, int64_t step, double decay, int R, const uint8_t *in_flight,
+                      int32_t *pair_expert, int32_t *pair_slot, int32_t *pair_victim) {
+    for (int e = 0; e < E; ++e) {
+        score[e] = decay * score[e] + (double)hist[e];
+        if (hist[e] > 0) last[e] = step;
+    }
+    char *used = (char *)calloc((size_t)E, 1);
+    int n = 0;
+    for (int p = 0; p < R; ++p) {
+        /* best candidate */
+        int cand = -1;
+        for (int e = 0; e < E; ++e) {
+            if (e2s[e] >= 0 || used[e] || (in_flight && in_flight[e])) continue;
+            if (cand < 0 || score[e] > score[cand]) cand = e;
+        }
+        if (cand < 0) break;
+        /* worst resident victim */
+        int vic = -1;
+        for (int s = 0; s < S; ++s) {
+            int e = s2e[s];
+            if (e < 0 || used[e] || (in_flight && in_flight[e])) continue;
+            if (vic < 0 || score[e] < score[vic] || (score[e] == score[vic] && last[e] < last[vic]) ||
+                (score[e] == score[vic] && last[e] == last[vic] && e2s[e] < e2s[vic]))
+                vic = e;
+        }
+        if (vic < 0 || !(score[cand] > score[vic])) break;
+        int slot = e2s[vic];
+        used[cand] = 1;
+        used[vic] = 1;
+        pair_expert[n] = cand;
+        pair_slot[n] = slot;
+        pair_victim[n] = vic;
+        ++n;
+    }
+    for (int i = 0; i < n; ++i) {
+        e2s[pair_victim[i]] = -1;
+        e2s[pair_expert[i]] = pair_slot[i];
+        s2e[pair_slot[i]] = pair_expert[i];
+    }
+    free(used);
+    return n;
+}
+
+/* ------------------------------------------------ prefill activation format */
+
+/* E4M3 element (OCP MX v1.0 / OFP8): sign bit 7, exponent bits 6..3 (bias 7),
+ * mantissa bits 2..0; exponent 0 is subnormal; S.1111.111 is NaN; max 448. */
+float oracle_e4m3(uint8_t code) {
+    int s = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    float v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexpf((float)m, -9); /* m/8 * 2^(1-7) */
+    else
+        v = ldexpf(1.0f + (float)m / 8.0f, e - 7);
+    return s ? -v : v;
+}
+
+/* Nearest E4M3 code to v (ties to an even mantissa), saturating at +-448.
+ * Brute force over the 254 finite codes. */
+uint8_t oracle_e4m3_encode(float v) {
+    uint8_t best = 0;
+    double bd = INFINITY;
+    for (int c = 0; c < 256; ++c) {
+        float q = oracle_e4m3((uint8_t)c);
+        if (isnan(q)) continue;
+        if (q == 0.0f && (c & 0x80)) continue; /* keep +0 for zero */
+        double d = fabs((double)q - (double)v);
+        if (d < bd || (d == bd && (c & 1) == 0 && (best & 1) == 1)) {
+            bd = d;
+            best = (uint8_t)c;
+        }
+    }
+    if (v > 448.0f) best = 0x7e;
+    if (v < -448.0f) best = 0xfe;
+    return best;
+}
+
+/* MXFP8 block (OCP MX v1.0 conversion rule): shared exponent
+ * X = floor(log2(max |v|)) - 8 (8 = largest E4M3 exponent), clamped to the
+ * E8M0 range; each element becomes E4M3(v / 2^X), rounding to nearest even,
+ * saturating.  A block of zeros gets X = -127.  Returns the E8M0 byte. */
+uint8_t oracle_mxfp8_block(const float *v, int n, uint8_t *codes) {
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i)
+        if (fabsf(v[i]) > amax) amax = fabsf(v[i]);
+    int X;
+    if (amax == 0.0f)
+        X = -127;
+    else {
+        int ex;
+        frexpf(amax, &ex); /* amax = f * 2^ex, f in [0.5, 1): floor(log2 amax) = ex - 1 */
+        X = (ex - 1) - 8;
+        if (X < -127) X = -127;
+        if (X > 127) X = 127;
+    }
+    for (int i = 0; i < n; ++i) codes[i] = oracle_e4m3_encode(ldexpf(v[i], -X));
+    return (uint8_t)(X + 127);
+}
+
+/* Prefill variant of the expert FFN: x and h pass through MXFP8 (32-element
+ * blocks along the contraction) before their products with the MXFP4 weights;
+ * the products of two decoded values are exact and summed in fp32. */
+void oracle_expert_ffn_mxfp8(const uint8_t *rec, int H, int I, const uint16_t *x, float *y) {
+    const uint8_t *gc, *gs, *uc, *us, *dc, *ds;
+    expert_sections(rec, H, I, &gc, &gs, &uc, &us, &dc, &ds);
+    float *xq = (float *)malloc(sizeof(float) * (size_t)H);
+    float *h = (float *)malloc(sizeof(float) * (size_t)I);
+    float *hq = (float *)malloc(sizeof(float) * (size_t)I);
+    float blk[32];
+    uint8_t codes[32];
+    for (int b = 0; b < H / 32; ++b) {
+        for (int i = 0; i < 32; ++i) blk[i] = oracle_bf16_to_f32(x[b * 32 + i]);
+        uint8_t sc = oracle_mxfp8_block(blk, 32, codes);
+        for (int i = 0; i < 32; ++i) xq[b * 32 + i] = oracle_e4m3(codes[i]) * oracle_e8m0(sc);
+    }
+    for (int i = 0; i < I; ++i) {
+        float g = 0.0f, u = 0.0f;
+        for (int c = 0; c < H; ++c) {
+            g = g + oracle_mxfp4_element(gc, gs, H, i, c) * xq[c];
+            u = u + oracle_mxfp4_element(uc, us, H, i, c) * xq[c];
+        }
+        h[i] = silu(g) * u;
+    }
+    for (int b = 0; b < I / 32; ++b) {
+        uint8_t sc = oracle_mxfp8_block(h + b * 32, 32, codes);
+        for (int i = 0; i < 32; ++i) hq[b * 32 + i] = oracle_e4m3(codes[i]) * oracle_e8m0(sc);
+    }
+    for (int r = 0; r < H; ++r) {
+        float acc = 0.0f;
+        for (int i = 0; i < I; ++i) acc = acc + oracle_mxfp4_element(dc, ds, I, r, i) * hq[i];
+        y[r] = acc;
+    }
+    free(xq);
+    free(h);
+    free(hq);
+}

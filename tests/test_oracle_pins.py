@@ -1,0 +1,451 @@
+"""Pins of the CPU oracle to facts outside itself (no GPU needed).
+
+Each test checks the oracle against something it cannot agree with by
+construction: a published format table, a bit-field definition, brute force
+over a tiny input, a library matmul in float64 with a rigorous fp32 error
+bound, a closed form, or a trace worked by hand.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+
+from expert_offload_moe_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+U32 = 2.0 ** -24  # fp32 unit roundoff
+
+
+# ----------------------------------------------------------- independent decoders
+
+
+def e2m1_from_bits(code):
+    """OCP MX v1.0 E2M1: sign bit 3, exponent bits 2..1 with bias 1, mantissa bit 0."""
+    s = -1.0 if code & 8 else 1.0
+    e = (code >> 1) & 3
+    m = code & 1
+    mag = m * 0.5 if e == 0 else 2.0 ** (e - 1) * (1.0 + m / 2.0)
+    return s * mag
+
+
+def decode_mxfp4_np(codes, scales, R, C):
+    """float64 decode of an MXFP4 matrix from bit fields (independent of the oracle's table)."""
+    codes = codes.reshape(R, C // 2)
+    lo = (codes & 15).astype(np.int64)
+    hi = (codes >> 4).astype(np.int64)
+    q = np.empty((R, C), dtype=np.int64)
+    q[:, 0::2] = lo
+    q[:, 1::2] = hi
+    sign = np.where(q & 8, -1.0, 1.0)
+    e = (q >> 1) & 3
+    m = q & 1
+    mag = np.where(e == 0, m * 0.5, np.ldexp(1.0 + m / 2.0, (e - 1)))
+    sc = np.ldexp(1.0, scales.reshape(R, C // 32).astype(np.int64) - 127)
+    return sign * mag * np.repeat(sc, 32, axis=1)
+
+
+def bf16_to_f64(bits):
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def sections(rec, H, I):
+    offs = synth.section_offsets(H, I)
+    return {k: rec[o:o + n] for k, (o, n) in offs.items()}
+
+
+# ------------------------------------------------------------------- formats
+
+
+def test_e2m1_table_matches_ocp_fixture_and_bit_fields(oracle_lib):
+    rows = [l.split() for l in open(os.path.join(GOLDEN, "e2m1_ocp_mx_v1.txt")) if l[0] != "#"]
+    assert len(rows) == 16
+    for code_s, val_s in rows:
+        code, val = int(code_s), float(val_s)
+        got = oracle_lib.e2m1(code)
+        assert got == val and math.copysign(1, got) == math.copysign(1, val), code
+        assert got == e2m1_from_bits(code)
+
+
+@pytest.mark.parametrize("e", [0, 1, 2, 100, 120, 121, 122, 123, 124, 125, 126, 127, 128, 200, 254])
+def test_e8m0_scales_exact(oracle_lib, e):
+    assert oracle_lib.e8m0(e) == math.ldexp(1.0, e - 127)
+
+
+def test_e8m0_nan(oracle_lib):
+    assert math.isnan(oracle_lib.e8m0(255))
+
+
+def test_mxfp4_exhaustive_codes_times_scales(oracle_lib):
+    # every code in every position of a 32-element block, under several scales
+    scales_list = [1, 120, 121, 122, 123, 124, 125, 126, 127, 200, 254]
+    R = len(scales_list)
+    C = 32
+    codes = np.zeros((R, C // 2), dtype=np.uint8)
+    vals = np.arange(C) % 16
+    codes[:] = (vals[0::2] | (vals[1::2] << 4)).astype(np.uint8)
+    scales = np.array(scales_list, dtype=np.uint8).reshape(R, 1)
+    W = oracle_lib.mxfp4_dequant(codes, scales, R, C)
+    ref = decode_mxfp4_np(codes, scales, R, C)
+    # every finite product is exact in fp32; 6 * 2^127 overflows to inf in fp32 as it must
+    with np.errstate(over="ignore"):
+        assert np.array_equal(W, ref.astype(np.float32))
+    assert W[-1, 4] == np.inf and W[-1, 15] == -np.inf and float(W[-1, 3]) == 1.5 * 2.0 ** 127
+
+
+def test_mxfp4_nibble_order_and_block_scales(oracle_lib):
+    # column 2c is the low nibble of byte c; scale b covers columns [32b, 32b+32)
+    R, C = 2, 64
+    codes = np.zeros((R, C // 2), dtype=np.uint8)
+    codes[0, 0] = 0x72  # col 0 -> code 2 (1.0), col 1 -> code 7 (6.0)
+    codes[1, 16] = 0x0B  # col 32 -> code 11 (-1.5), col 33 -> 0
+    scales = np.array([[127, 126], [127, 129]], dtype=np.uint8)
+    W = oracle_lib.mxfp4_dequant(codes, scales, R, C)
+    assert W[0, 0] == 1.0 and W[0, 1] == 6.0 and np.count_nonzero(W[0]) == 2
+    assert W[1, 32] == -1.5 * 4.0 and np.count_nonzero(W[1]) == 1
+
+
+def test_bf16_round_nearest_even(oracle_lib):
+    assert oracle_lib.f32_to_bf16(1.0) == 0x3F80
+    # 1 + 2^-8 is halfway between 1 and 1 + 2^-7: ties to even -> 1.0
+    assert oracle_lib.f32_to_bf16(1.0 + 2.0 ** -8) == 0x3F80
+    # 1 + 3*2^-8 is halfway between 1+2^-7 (odd) and 1+2^-6 (even) -> up
+    assert oracle_lib.f32_to_bf16(1.0 + 3 * 2.0 ** -8) == 0x3F82
+    assert oracle_lib.f32_to_bf16(-2.0) == 0xC000
+
+
+# -------------------------------------------------------------------- router
+
+
+def test_router_logits_within_fp32_bound(oracle_lib):
+    H, E, M = 256, 16, 5
+    x = synth.activations(0, 0, 0, M, H)
+    Wr = synth.router_weights(0, 0, E, H)
+    b = np.linspace(-1, 1, E).astype(np.float32)
+    got = oracle_lib.router_logits(x, Wr, b).astype(np.float64)
+    xf = bf16_to_f64(x)
+    exact = xf @ Wr.astype(np.float64).T + b.astype(np.float64)
+    bound = (H + 2) * U32 * (np.abs(xf) @ np.abs(Wr.astype(np.float64)).T + np.abs(b))
+    assert np.all(np.abs(got - exact) <= bound)
+    # a transposed or shifted operand is far outside the bound
+    assert np.max(np.abs(got - exact)) < 1e-4
+
+
+# --------------------------------------------------------------------- top-k
+
+
+def brute_topk(l, k):
+    E = len(l)
+    sols = []
+    for S in itertools.combinations(range(E), k):
+        inside = set(S)
+        ok = all(l[i] > l[j] or (l[i] == l[j] and i < j) for i in inside for j in range(E) if j not in inside)
+        if ok:
+            sols.append(S)
+    assert len(sols) == 1
+    return sorted(sols[0], key=lambda i: (-l[i], i))
+
+
+def test_topk_brute_force_with_ties(oracle_lib):
+    rng = np.random.default_rng(7)
+    E, k = 16, 2
+    logits = rng.standard_normal((64, E)).astype(np.float32)
+    logits[32:] = np.round(logits[32:] * 2) / 2  # many exact ties
+    logits[40] = 0.0  # all equal -> experts 0, 1
+    ids, _ = oracle_lib.topk_softmax(logits, k)
+    for t in range(logits.shape[0]):
+        assert list(ids[t]) == brute_topk([float(v) for v in logits[t]], k), t
+    assert list(ids[40]) == [0, 1]
+
+
+@pytest.mark.parametrize("k", [1, 2, 4, 10])
+def test_softmax_weights(oracle_lib, k):
+    rng = np.random.default_rng(k)
+    E = 32
+    logits = (rng.standard_normal((16, E)) * 3).astype(np.float32)
+    ids, w = oracle_lib.topk_softmax(logits, k)
+    assert np.all(np.abs(w.astype(np.float64).sum(1) - 1.0) <= 4 * k * U32)
+    if k == 1:
+        assert np.all(w == 1.0)
+    # closed form against float64 on the selected logits
+    sel = np.take_along_axis(logits, ids, 1).astype(np.float64)
+    ref = np.exp(sel - sel.max(1, keepdims=True))
+    ref /= ref.sum(1, keepdims=True)
+    assert np.allclose(w, ref, rtol=1e-6, atol=1e-7)
+    # weights follow the logit order
+    assert np.all(np.diff(w, axis=1) <= 0)
+
+
+def test_softmax_equal_logits(oracle_lib):
+    logits = np.zeros((1, 8), dtype=np.float32)
+    _, w = oracle_lib.topk_softmax(logits, 4)
+    assert np.all(w == np.float32(0.25))
+
+
+# ---------------------------------------------------------------- compaction
+
+
+def test_compaction_against_brute_force_filter(oracle_lib):
+    rng = np.random.default_rng(3)
+    M, E, k = 8, 32, 4
+    ids = np.array([rng.choice(E, k, replace=False) for _ in range(M)], dtype=np.int32)
+    w = rng.random((M, k)).astype(np.float32)
+    e2s = np.full(E, -1, dtype=np.int32)
+    resident = rng.choice(E, 12, replace=False)
+    e2s[resident] = rng.permutation(12)
+    r = oracle_lib.compact(ids, w, e2s)
+    routes = [(t, int(ids[t, j]), float(w[t, j])) for t in range(M) for j in range(k)]
+    hot = sorted([(e, t, wt) for t, e, wt in routes if e2s[e] >= 0])
+    cold = sorted([(t, e, wt) for t, e, wt in routes if e2s[e] < 0])
+    assert r["n_hot"] == len(hot) and r["n_cold"] == len(cold) and r["n_hot"] + r["n_cold"] == M * k
+    assert [(int(a), int(b), float(c)) for a, b, c in zip(r["hot_expert"], r["hot_token"], r["hot_w"])] == hot
+    assert list(r["hot_slot"]) == [int(e2s[e]) for e, _, _ in hot]
+    assert [(int(a), int(b), float(c)) for a, b, c in zip(r["cold_token"], r["cold_expert"], r["cold_w"])] == cold
+    act = sorted(set(e for e, _, _ in hot))
+    assert list(r["act_expert"]) == act
+    assert list(r["act_cnt"]) == [sum(1 for e2, _, _ in hot if e2 == e) for e in act]
+    assert list(r["act_off"]) == list(np.concatenate([[0], np.cumsum(r["act_cnt"])[:-1]]))
+    assert np.array_equal(r["hist"], np.bincount(ids.ravel(), minlength=E))
+
+
+def test_compaction_all_cold_and_all_hot(oracle_lib):
+    ids = np.array([[1, 0], [2, 3]], dtype=np.int32)
+    w = np.full((2, 2), 0.5, dtype=np.float32)
+    r = oracle_lib.compact(ids, w, np.full(4, -1, dtype=np.int32))
+    assert r["n_hot"] == 0 and r["n_active"] == 0 and r["n_cold"] == 4
+    assert list(r["cold_expert"]) == [0, 1, 2, 3] and list(r["cold_token"]) == [0, 0, 1, 1]
+    r = oracle_lib.compact(ids, w, np.array([3, 2, 1, 0], dtype=np.int32))
+    assert r["n_cold"] == 0 and list(r["hot_expert"]) == [0, 1, 2, 3] and list(r["hot_slot"]) == [3, 2, 1, 0]
+
+
+# ---------------------------------------------------------------- expert FFN
+
+
+def _expert_f64(rec, H, I):
+    s = sections(rec, H, I)
+    Wg = decode_mxfp4_np(s["wg_codes"], s["wg_scales"], I, H)
+    Wu = decode_mxfp4_np(s["wu_codes"], s["wu_scales"], I, H)
+    Wd = decode_mxfp4_np(s["wd_codes"], s["wd_scales"], H, I)
+    return Wg, Wu, Wd
+
+
+def test_gate_up_within_fp32_bound(oracle_lib):
+    H, I = 256, 128  # H != I: a transposed operand cannot pass
+    rec = synth.expert_records(0, 0, 16, H, I, experts=[5])[0]
+    x = synth.activations(0, 0, 1, 1, H)[0]
+    h = oracle_lib.expert_gate_up(rec, H, I, x).astype(np.float64)
+    Wg, Wu, _ = _expert_f64(rec, H, I)
+    xf = bf16_to_f64(x)
+    g, u = Wg @ xf, Wu @ xf  # products are exact in float64; the sum nearly so
+    dg = (H + 1) * U32 * (np.abs(Wg) @ np.abs(xf))
+    du = (H + 1) * U32 * (np.abs(Wu) @ np.abs(xf))
+    silu = g / (1.0 + np.exp(-g))
+    ref = silu * u
+    bound = 1.1 * dg * np.abs(u) + np.abs(silu) * du + 16 * U32 * np.abs(ref) + 1e-30
+    assert np.all(np.abs(h - ref) <= bound)
+
+
+def test_down_within_fp32_bound(oracle_lib):
+    H, I = 256, 128
+    rec = synth.expert_records(0, 0, 16, H, I, experts=[3])[0]
+    h = np.random.default_rng(1).standard_normal(I).astype(np.float32)
+    y = oracle_lib.expert_down(rec, H, I, h).astype(np.float64)
+    _, _, Wd = _expert_f64(rec, H, I)
+    exact = Wd @ h.astype(np.float64)
+    bound = (I + 1) * U32 * (np.abs(Wd) @ np.abs(h.astype(np.float64)))
+    assert np.all(np.abs(y - exact) <= bound)
+
+
+def test_ffn_permutation_weights_pick_columns(oracle_lib):
+    # Wg = Wu = 1.0 * P (a permutation): g_i = u_i = x[p(i)], so h_i = SiLU(x)x;
+    # Wd = identity-like on the first I rows picks h back out.
+    H, I = 64, 32
+    perm = np.random.default_rng(0).permutation(H)[:I]
+    rec = np.zeros(synth.expert_bytes(H, I), dtype=np.uint8)
+    s = sections(rec, H, I)
+    for name in ("wg", "wu"):
+        codes = s[name + "_codes"].reshape(I, H // 2)
+        for i, c in enumerate(perm):
+            codes[i, c // 2] = 2 << (4 * (c & 1))  # code 2 = 1.0
+        s[name + "_scales"][:] = 127
+    dcodes = s["wd_codes"].reshape(H, I // 2)
+    for r in range(I):
+        dcodes[r, r // 2] = 2 << (4 * (r & 1))
+    s["wd_scales"][:] = 128  # 2.0
+    x = synth.activations(0, 0, 2, 1, H)[0]
+    xf = bf16_to_f64(x).astype(np.float32)
+    h = oracle_lib.expert_gate_up(rec, H, I, x)
+    xp = xf[perm]
+    ref_h = (xp / (np.float32(1) + np.exp(-xp))) * xp
+    assert np.allclose(h, ref_h, rtol=4e-7, atol=0)
+    y = oracle_lib.expert_ffn(rec, H, I, x)
+    assert np.array_equal(y[:I], 2 * h) and np.all(y[I:] == 0)
+
+
+def test_silu_closed_forms(oracle_lib):
+    # SiLU(0) = 0; SiLU(g) -> g for large g; SiLU(g) -> 0 for very negative g
+    H, I = 32, 32
+    rec = np.zeros(synth.expert_bytes(H, I), dtype=np.uint8)
+    s = sections(rec, H, I)
+    s["wg_scales"][:] = 127
+    s["wu_scales"][:] = 127
+    gc = s["wg_codes"].reshape(I, H // 2)
+    uc = s["wu_codes"].reshape(I, H // 2)
+    uc[:, 0] = 2  # u_i = x_0
+    gc[1, 0] = 7  # g_1 = 6 x_0
+    gc[2, 0] = 15  # g_2 = -6 x_0
+    x = np.zeros(H, dtype=np.uint16)
+    x[0] = 0x4120  # 10.0
+    h = oracle_lib.expert_gate_up(rec, H, I, x)
+    assert h[0] == 0.0  # g = 0
+    assert abs(h[1] - 60.0 * 10.0) <= 1e-4 * 600  # SiLU(60) ~ 60
+    assert abs(h[2]) < 1e-20  # SiLU(-60) ~ 0
+
+
+# ------------------------------------------------------- whole-layer invariants
+
+
+def _tiny_layer(seed=0, M=3, tau=0.0):
+    w = synth.WORKLOADS["tiny_h256_i128_e16k2"]
+    H, I, E, k = w.hidden, w.inter, w.experts, w.top_k
+    x = synth.activations(seed, 0, 0, M, H)
+    Wr = synth.router_weights(seed, 0, E, H)
+    b = synth.router_bias(seed, 0, E, tau)
+    ex = synth.expert_records(seed, 0, E, H, I)
+    return x, Wr, b, ex, H, I, E, k
+
+
+def test_hot_plus_cold_equals_all_resident(oracle_lib):
+    x, Wr, b, ex, H, I, E, k = _tiny_layer(M=6)
+    full = oracle_lib.moe_layer(x, Wr, b, ex, np.arange(E, dtype=np.int32), k, H, I)
+    e2s = np.full(E, -1, dtype=np.int32)
+    e2s[::3] = np.arange(len(e2s[::3]))
+    part = oracle_lib.moe_layer(x, Wr, b, ex, e2s, k, H, I)
+    assert part["n_cold"] > 0 and part["n_hot"] > 0
+    assert np.array_equal(part["ids"], full["ids"]) and np.array_equal(part["w"], full["w"])
+    recon = part["out_f32"].astype(np.float64).copy()
+    mag = np.zeros_like(recon)
+    for t, e, wt in zip(part["cold_token"], part["cold_expert"], part["cold_w"]):
+        y = oracle_lib.expert_ffn(ex[e], H, I, x[t]).astype(np.float64)
+        recon[t] += wt * y
+        mag[t] += np.abs(wt * y)
+    for t, e, wt in zip(part["hot_token"], part["hot_expert"], part["hot_w"]):
+        mag[t] += np.abs(wt * oracle_lib.expert_ffn(ex[e], H, I, x[t]).astype(np.float64))
+    assert np.all(np.abs(recon - full["out_f32"]) <= 4 * (k + 1) * U32 * mag + 1e-30)
+
+
+def test_single_route_output_is_expert_output(oracle_lib):
+    # top_k = 1: the weight is exactly 1, the output is y of the chosen expert
+    x, Wr, b, ex, H, I, E, _ = _tiny_layer(M=2)
+    r = oracle_lib.moe_layer(x, Wr, b, ex, np.arange(E, dtype=np.int32), 1, H, I)
+    for t in range(2):
+        y = oracle_lib.expert_ffn(ex[r["ids"][t, 0]], H, I, x[t])
+        assert np.array_equal(r["out_f32"][t], y)
+
+
+def test_all_cold_layer_outputs_zero(oracle_lib):
+    x, Wr, b, ex, H, I, E, k = _tiny_layer(M=2)
+    r = oracle_lib.moe_layer(x, Wr, b, ex, np.full(E, -1, dtype=np.int32), k, H, I)
+    assert r["n_hot"] == 0 and np.all(r["out_f32"] == 0) and r["n_cold"] == 2 * k
+
+
+# ------------------------------------------------------------------ slot cache
+
+
+def _read_trace(name):
+    lines = [l.split() for l in open(os.path.join(GOLDEN, name)) if l.strip() and l[0] != "#"]
+    hdr = lines[0]
+    E, S, R, decay = int(hdr[1]), int(hdr[3]), int(hdr[5]), float(hdr[7])
+    init = [int(v) for v in lines[1][1:]]
+    steps = []
+    for l in lines[2:]:
+        st = int(l[1])
+        i_p, i_m = l.index("pairs"), l.index("map")
+        hist = [int(v) for v in l[3:i_p]]
+        pairs = [tuple(int(q) for q in p.split(":")) for p in l[i_p + 1:i_m]]
+        mp = [int(v) for v in l[i_m + 1:]]
+        steps.append((st, hist, pairs, mp))
+    return E, S, R, decay, init, steps
+
+
+@pytest.mark.parametrize("trace", ["cache_lfu_trace.txt", "cache_lfru_trace.txt"])
+def test_cache_policy_hand_worked_trace(oracle_lib, trace):
+    E, S, R, decay, init, steps = _read_trace(trace)
+    rp = oracle_lib.CacheReplay(np.array(init, dtype=np.int32), S, decay=decay, R=R)
+    for st, hist, pairs, mp in steps:
+        got = rp.step(np.array(hist, dtype=np.int32), st)
+        assert got == pairs, (trace, st)
+        assert list(rp.e2s) == mp, (trace, st)
+
+
+def test_cache_policy_never_exceeds_budget_and_keeps_map_injective(oracle_lib):
+    rng = np.random.default_rng(11)
+    E, S, R = 32, 16, 2
+    rp = oracle_lib.CacheReplay(np.where(np.arange(E) < S, np.arange(E), -1).astype(np.int32), S, R=R)
+    for st in range(200):
+        hist = np.bincount(rng.choice(E, 4, replace=False, p=None), minlength=E).astype(np.int32)
+        pairs = rp.step(hist, st)
+        assert len(pairs) <= R
+        res = rp.e2s[rp.e2s >= 0]
+        assert len(res) == S and len(set(res.tolist())) == S
+        assert all(rp.s2e[rp.e2s[e]] == e for e in range(E) if rp.e2s[e] >= 0)
+
+
+def test_cache_in_flight_experts_are_skipped(oracle_lib):
+    rp = oracle_lib.CacheReplay(np.array([0, 1, -1, -1], dtype=np.int32), 2, R=2)
+    fl = np.array([0, 0, 1, 0], dtype=np.uint8)  # expert 2's copy has not landed
+    pairs = rp.step(np.array([0, 0, 5, 3], dtype=np.int32), 0, in_flight=fl)
+    assert pairs == [(3, 0, 0)]
+
+
+# ------------------------------------------------------- prefill activation format
+
+
+def e4m3_from_bits(code):
+    s = -1.0 if code & 0x80 else 1.0
+    e = (code >> 3) & 15
+    m = code & 7
+    if e == 15 and m == 7:
+        return float("nan")
+    if e == 0:
+        return s * m / 8.0 * 2.0 ** -6
+    return s * (1 + m / 8.0) * 2.0 ** (e - 7)
+
+
+def test_e4m3_exhaustive_and_fixture(oracle_lib):
+    for c in range(256):
+        a, b = oracle_lib.e4m3(c), e4m3_from_bits(c)
+        assert (math.isnan(a) and math.isnan(b)) or a == b, c
+    for l in open(os.path.join(GOLDEN, "e4m3_points.txt")):
+        if l[0] == "#":
+            continue
+        c, v = l.split()
+        assert oracle_lib.e4m3(int(c, 16)) == float(v)
+
+
+def test_e4m3_encode_round_trip_rne_and_saturation(oracle_lib):
+    for c in range(256):
+        v = e4m3_from_bits(c)
+        if math.isnan(v) or v == 0:
+            continue
+        assert oracle_lib.e4m3(oracle_lib.e4m3_encode(v)) == v
+    assert oracle_lib.e4m3(oracle_lib.e4m3_encode(1.0625)) == 1.0  # tie -> even mantissa
+    assert oracle_lib.e4m3(oracle_lib.e4m3_encode(1.1875)) == 1.25
+    assert oracle_lib.e4m3(oracle_lib.e4m3_encode(500.0)) == 448.0
+    assert oracle_lib.e4m3(oracle_lib.e4m3_encode(-1e9)) == -448.0
+
+
+def test_mxfp8_block_rule(oracle_lib):
+    # powers of two within the block's range come back exactly
+    v = np.array([2.0 ** j for j in range(-6, 2)] * 4, dtype=np.float32)
+    sc, codes = oracle_lib.mxfp8_block(v)
+    assert sc == 127 + (1 - 8)  # floor(log2 2) - 8 = -7
+    back = np.array([oracle_lib.e4m3(c) for c in codes]) * 2.0 ** (sc - 127)
+    assert np.array_equal(back, v)
+    # an all-equal block
+    sc, codes = oracle_lib.mxfp8_block(np.full(32, 1.5, dtype=np.float32))
+    assert sc == 127 - 8 and all(oracle_lib.e4m3(c) * 2.0 ** (sc - 127) == 1.5 for c in codes)
+    # zeros
+    sc, codes = oracle_lib.mxfp8_block(np.zeros(32, dtype=np.float32))
+    assert sc == 0 and np.all(codes == 0)
