@@ -1,0 +1,320 @@
+#!/usr/bin/env python3
+"""Decode-time MoE layer with GPU expert slots: throughput on one GB300.
+
+Workload (default): the gpt-oss-20B-shaped stack -- 24 independent layers,
+hidden 2880, expert intermediate 2880, 32 experts, top-4, every expert in a
+GPU slot, M=1 decode, each layer with its own fresh N(0,1) bf16 input every
+step, MXFP4 experts (~10 GB).  A step = route + forward of all 24 layers for
+one token (one CUDA-graph replay), so tokens/s = steps / time.
+
+Printed (rank 0, one JSON line): value (tokens/s with inputs resident in HBM),
+e2e (host inputs copied in and outputs copied back each step), roofline of
+the dominant kernel (gate/up GEMV, HBM-bound), the oracle as a CPU baseline,
+clocks sampled during the timed region, and the kernel launch count.
+
+`--impl reference` times the CPU oracle instead (the slow, plain reference),
+on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "gptoss20b_h2880_e32k4_resident_m1"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+METRIC = "MoE-layer decode tokens/s (M=1)"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=512)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--layers", type=int, default=None, help="fewer layers (debug only; not a valid result)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-layers", type=int, default=1, help="layers per oracle step (reference arm sample)")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return json.load(open(p)), "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out = ""
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_token_seconds(w, n_layers, seed=0):
+    """The oracle, as it stands, on one host core: seconds for one token through n_layers layers."""
+    import oracle
+    from expert_offload_moe_gb300 import synth
+
+    oracle.build()
+    t_total = 0.0
+    for l in range(n_layers):
+        Wr = synth.router_weights(seed, l, w.experts, w.hidden)
+        b = synth.router_bias(seed, l, w.experts, w.bias_tau)
+        ex = synth.expert_records(seed, l, w.experts, w.hidden, w.inter)
+        e2s = synth.expert_to_slot_by_rank(seed, l, w.experts, w.slots)
+        x = synth.activations(seed, l, 0, 1, w.hidden)
+        t0 = time.perf_counter()
+        oracle.moe_layer(x, Wr, b, ex, e2s, w.top_k, w.hidden, w.inter)
+        t_total += time.perf_counter() - t0
+        del ex
+    return t_total
+
+
+def cpu_baseline(w, n_layers):
+    t = oracle_token_seconds(w, n_layers)
+    per_token = t / n_layers * w.layers
+    return {"value": 1.0 / per_token, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"1 token through {n_layers} of {w.layers} layers (single-threaded C oracle, "
+                      f"{t:.1f} s), time scaled to the {w.layers}-layer stack"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from expert_offload_moe_gb300 import synth
+
+    w = synth.WORKLOADS[args.workload]
+    total = 0.0
+    for i in range(args.warmup + args.steps):
+        t = oracle_token_seconds(w, args.ref_layers) / args.ref_layers * w.layers
+        if i >= args.warmup:
+            total += t
+    val = args.steps / total
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "layers": w.layers, "tokens_per_step": 1},
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"each step: 1 token through {args.ref_layers} of {w.layers} layers on one "
+                                       f"core, time scaled to {w.layers} layers"},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def traffic_for(kernel_src):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
+    summ = os.path.join(ROOT, "profiles", "gateup_gptoss20b_traffic.txt")
+    if not os.path.exists(summ):
+        return None
+    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+    kv = {}
+    for line in open(summ):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("source_sha256") != sha:
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch_full_workload"])
+    except (KeyError, ValueError):
+        return None
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    from expert_offload_moe_gb300 import build as moe_build
+    from expert_offload_moe_gb300 import moe, stack, synth
+
+    moe_build.build()
+    moe.lib()
+    w = synth.WORKLOADS[args.workload]
+    M = w.tokens[0]
+    n_inputs = 64
+    st = stack.DecodeStack(w, M=M, n_layers=args.layers, seed=rank, n_inputs=n_inputs)
+    L = st.L
+    st.capture()
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        tt = torch.tensor([v], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        return float(tt.item())
+
+    # ---------------- timed region: graph replay, inputs resident in HBM -------
+    for i in range(args.warmup):
+        st.replay(i)
+    barrier()
+    clk = Clocks(local)
+    clk.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        st.replay(i)
+    e1.record(stream)
+    barrier()
+    clocks = clk.stop()
+    t_ms = max_over_ranks(e0.elapsed_time(e1))
+    tokens = args.steps * M * world
+    value = tokens / (t_ms / 1e3)
+
+    # expert bytes actually read (the routing of every input is fixed, so one pass gives the mix)
+    n_act = []
+    for i in range(n_inputs):
+        st.step(i)
+        torch.cuda.synchronize()
+        for l in range(L):
+            n_act.append(int(stack.host_counts(st.layers[l].res)[2]))
+    mean_act = float(np.mean(n_act))
+    gateup_bytes = mean_act * 2 * w.inter * w.hidden * 17 / 32
+    expert_bytes_step = mean_act * w.expert_bytes * L
+    router_bytes_step = w.experts * w.hidden * 4 * L
+
+    # ---------------- kernel timing pass (events on the launching stream) -------
+    for lay in st.layers:
+        lay.profile(True)
+    kt_steps = min(args.steps, 128)
+    for i in range(kt_steps):
+        st.step(i)
+    torch.cuda.synchronize()
+    prof = np.zeros(4)
+    for lay in st.layers:
+        prof += lay.profile_read()
+        lay.profile(False)
+    launches = max(prof[3], 1)
+    route_us, gateup_us, down_us = (1e3 * prof[i] / launches for i in range(3))
+    pk, pk_src = peaks()
+    hbm_peak = pk.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"])
+    achieved = gateup_bytes / (gateup_us * 1e-6) / 1e9
+    traffic = traffic_for(os.path.join(ROOT, "expert_offload_moe_gb300", "csrc", "moe_decode.cu"))
+
+    # ---------------- e2e: host inputs in, outputs back, every step ------------
+    x_host = torch.empty((n_inputs, L, M, w.hidden), dtype=torch.bfloat16, pin_memory=True)
+    x_host.copy_(st.x_all.cpu())
+    out_host = torch.empty(st.out.shape, dtype=st.out.dtype, pin_memory=True)
+    for i in range(args.warmup):
+        st.x_cur.copy_(x_host[i % n_inputs], non_blocking=True)
+        st.graph.replay()
+        out_host.copy_(st.out, non_blocking=True)
+    barrier()
+    e0.record(stream)
+    for i in range(args.steps):
+        st.x_cur.copy_(x_host[i % n_inputs], non_blocking=True)
+        st.graph.replay()
+        out_host.copy_(st.out, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    t_e2e = max_over_ranks(e0.elapsed_time(e1))
+    e2e = {"value": tokens / (t_e2e / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": L * M * w.hidden * 2,
+           "d2h_bytes_per_step": int(st.out.numel() * st.out.element_size())}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "layers": L, "hidden": w.hidden, "inter": w.inter, "experts": w.experts,
+                   "top_k": w.top_k, "slots": w.slots, "tokens_per_step": M, "parallelism": f"replicas{world}",
+                   "weights": "mxfp4 experts, fp32 router, fp32 accumulation",
+                   "l2": "inputs larger than L2: each step reads %.2f GB of distinct expert weights"
+                         % (expert_bytes_step / 1e9),
+                   "expert_gbs": expert_bytes_step / (t_ms / args.steps * 1e-3) / 1e9,
+                   "router_gbs": router_bytes_step / (t_ms / args.steps * 1e-3) / 1e9,
+                   "mean_active_experts": mean_act,
+                   "kernel_us": {"route": route_us, "gateup": gateup_us, "down": down_us}},
+        "roofline": {"bound": "hbm", "kernel": "gateup_kernel", "achieved": achieved, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
+                     "bytes_per_launch": gateup_bytes, "avg_launch_us": gateup_us,
+                     "peak_source": "measured hbm_gbs (MEASURED_PEAKS.json)" if pk_src == "measured"
+                     else "fallback 6.8 TB/s"},
+        "clocks": clocks,
+        "gpu_launches": int(args.steps * L * 3),
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w, 1)
+    st.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,210 @@
+// Decode expert FFN (M <= 8 tokens) straight from the MXFP4 slot bytes.
+//
+// gateup_kernel: for every active slot and every row i of its intermediate
+//   dimension, one warp streams row i of Wg and Wu (16-byte loads = one
+//   32-element MXFP4 block per lane), decodes the E2M1 codes in registers,
+//   multiplies by the bf16 activations of every token routed to the slot
+//   (fp32, exact products), applies the E8M0 block scale to each 32-element
+//   partial, sums across the warp, and writes h = SiLU(g) * u in fp32.
+// down_kernel: one warp per output row r: for every active slot in ascending
+//   expert order and every route of it, y = Wd[r, :] . h, and the weighted
+//   sum over the token's routes is formed in the same order and stored.
+//   Combining in expert order (not slot order) keeps the output independent
+//   of where an expert sits (xinfer docs: placement never changes precision).
+//
+// The work lists and counts come from the route kernel in device memory; the
+// grids are fixed (persistent, sized by the SM count), so the launches are
+// the same for every routing (xinfer docs "How it works").
+#include <cuda_bf16.h>
+
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kM = kDecodeMaxTokens;
+
+__device__ __forceinline__ float e8m0_to_f32(uint32_t e) {
+    return e ? __uint_as_float(e << 23) : __uint_as_float(0x00400000u);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ void fill_e2m1_lut(float *lut) {
+    if (threadIdx.x < 16) {
+        const float mag[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
+        const float m = mag[threadIdx.x & 7];
+        lut[threadIdx.x] = (threadIdx.x & 8) ? -m : m;
+    }
+}
+
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.f + expf(-g)); }
+
+__global__ void __launch_bounds__(kThreads) gateup_kernel(DecodeParams p, int M) {
+    extern __shared__ float sx[];  // [M][H] activations as fp32
+    __shared__ float lut[16];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int H = p.geo.H, I = p.geo.I, nb = H / 32;
+    fill_e2m1_lut(lut);
+    for (int i = threadIdx.x; i < M * H; i += kThreads) sx[i] = __uint_as_float((uint32_t)p.x[i] << 16);
+    __syncthreads();
+
+    const int n_act = p.counts[2];
+    const int total = n_act * I;
+    for (int task = blockIdx.x * kWarps + warp; task < total; task += gridDim.x * kWarps) {
+        const int a = task / I, i = task - a * I;
+        const int slot = p.act_slot[a], off = p.act_off[a], cnt = p.act_cnt[a];
+        const uint8_t *base = p.bank + (size_t)slot * p.geo.expert_bytes;
+        const uint8_t *gq = base + p.geo.off_wg_codes + (size_t)i * (H / 2);
+        const uint8_t *gs = base + p.geo.off_wg_scales + (size_t)i * nb;
+        const uint8_t *uq = base + p.geo.off_wu_codes + (size_t)i * (H / 2);
+        const uint8_t *us = base + p.geo.off_wu_scales + (size_t)i * nb;
+        int tok[kM];
+#pragma unroll
+        for (int t = 0; t < kM; ++t) tok[t] = t < cnt ? p.hot_token[off + t] : 0;
+        float g[kM], u[kM];
+#pragma unroll
+        for (int t = 0; t < kM; ++t) g[t] = u[t] = 0.f;
+
+        for (int b = lane; b < nb; b += 32) {
+            const uint4 qg4 = ld_stream(gq + (size_t)b * 16);
+            const uint4 qu4 = ld_stream(uq + (size_t)b * 16);
+            const float sg = e8m0_to_f32(__ldg(gs + b)), su = e8m0_to_f32(__ldg(us + b));
+            const uint32_t qg[4] = {qg4.x, qg4.y, qg4.z, qg4.w};
+            const uint32_t qu[4] = {qu4.x, qu4.y, qu4.z, qu4.w};
+            float pg[kM], pu[kM];
+#pragma unroll
+            for (int t = 0; t < kM; ++t) pg[t] = pu[t] = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+#pragma unroll
+                for (int n = 0; n < 8; ++n) {
+                    const float vg = lut[(qg[q] >> (4 * n)) & 15u];
+                    const float vu = lut[(qu[q] >> (4 * n)) & 15u];
+                    const int col = b * 32 + q * 8 + n;
+#pragma unroll
+                    for (int t = 0; t < kM; ++t) {
+                        if (t < cnt) {
+                            const float xv = sx[tok[t] * H + col];
+                            pg[t] = fmaf(vg, xv, pg[t]);
+                            pu[t] = fmaf(vu, xv, pu[t]);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < kM; ++t) {
+                g[t] = fmaf(pg[t], sg, g[t]);
+                u[t] = fmaf(pu[t], su, u[t]);
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < kM; ++t) {
+            if (t < cnt) {
+                const float gt = warp_sum(g[t]), ut = warp_sum(u[t]);
+                if (lane == 0) p.h[(size_t)(off + t) * I + i] = silu(gt) * ut;
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) down_kernel(DecodeParams p, int M) {
+    __shared__ float lut[16];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int H = p.geo.H, I = p.geo.I, nb = I / 32;
+    fill_e2m1_lut(lut);
+    __syncthreads();
+    const int n_act = p.counts[2];
+
+    for (int r = blockIdx.x * kWarps + warp; r < H; r += gridDim.x * kWarps) {
+        float acc[kM];
+#pragma unroll
+        for (int t = 0; t < kM; ++t) acc[t] = 0.f;
+        for (int a = 0; a < n_act; ++a) {
+            const int slot = p.act_slot[a], off = p.act_off[a], cnt = p.act_cnt[a];
+            const uint8_t *base = p.bank + (size_t)slot * p.geo.expert_bytes;
+            const uint8_t *dq = base + p.geo.off_wd_codes + (size_t)r * (I / 2);
+            const uint8_t *ds = base + p.geo.off_wd_scales + (size_t)r * nb;
+            float y[kM];
+#pragma unroll
+            for (int t = 0; t < kM; ++t) y[t] = 0.f;
+            for (int b = lane; b < nb; b += 32) {
+                const uint4 q4 = ld_stream(dq + (size_t)b * 16);
+                const float s = e8m0_to_f32(__ldg(ds + b));
+                const uint32_t q[4] = {q4.x, q4.y, q4.z, q4.w};
+                float py[kM];
+#pragma unroll
+                for (int t = 0; t < kM; ++t) py[t] = 0.f;
+#pragma unroll
+                for (int t = 0; t < kM; ++t) {
+                    if (t < cnt) {
+                        const float4 *hp = reinterpret_cast<const float4 *>(p.h + (size_t)(off + t) * I + b * 32);
+#pragma unroll
+                        for (int qq = 0; qq < 4; ++qq) {
+                            const float4 h0 = hp[2 * qq], h1 = hp[2 * qq + 1];
+                            const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+                            for (int n = 0; n < 8; ++n) py[t] = fmaf(lut[(q[qq] >> (4 * n)) & 15u], hv[n], py[t]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < kM; ++t) y[t] = fmaf(py[t], s, y[t]);
+            }
+#pragma unroll
+            for (int t = 0; t < kM; ++t) {
+                if (t < cnt) {
+                    const float yt = warp_sum(y[t]);
+                    const int tok = p.hot_token[off + t];
+                    const float wt = p.hot_w[off + t];
+#pragma unroll
+                    for (int tt = 0; tt < kM; ++tt)
+                        if (tt == tok) acc[tt] = fmaf(wt, yt, acc[tt]);
+                }
+            }
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int t = 0; t < kM; ++t) {
+                if (t < M) {
+                    if (p.out_f32)
+                        reinterpret_cast<float *>(p.out)[(size_t)t * H + r] = acc[t];
+                    else
+                        reinterpret_cast<__nv_bfloat16 *>(p.out)[(size_t)t * H + r] = __float2bfloat16_rn(acc[t]);
+                }
+            }
+        }
+    }
+}
+
+}  // namespace
+
+void launch_gateup(const DecodeParams &p, int M, cudaStream_t s, int num_sms) {
+    const size_t smem = (size_t)M * p.geo.H * sizeof(float);
+    static bool configured = false;
+    if (!configured) {
+        cudaFuncSetAttribute(gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmemLimit);
+        configured = true;
+    }
+    gateup_kernel<<<num_sms * 4, kThreads, smem, s>>>(p, M);
+}
+
+void launch_down(const DecodeParams &p, int M, cudaStream_t s, int num_sms) {
+    down_kernel<<<num_sms * 4, kThreads, 0, s>>>(p, M);
+}
+
+}  // namespace moe

@@ -1,0 +1,88 @@
+// Internal declarations shared by the layer's host code and its kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kMaxTopK = 16;
+constexpr int kMaxExperts = 512;
+constexpr int kMaxTokens = 4096;
+constexpr int kDecodeMaxTokens = 8;            // M <= 8 takes the decode kernels
+constexpr int kRouteChunk = 256;               // router columns per warp task
+constexpr int kDecodeSmemLimit = 200 * 1024;   // decode activations staged in shared memory
+
+// Device scratch written by the route kernel.
+struct RouteBuffers {
+    float *logit_part;    // [nchunk][max_tokens][E]
+    int32_t *topk_ids;    // [max_tokens][k]
+    float *topk_w;        // [max_tokens][k]
+    int32_t *hot_expert;  // [max_tokens * k]
+    int32_t *hot_token;
+    float *hot_w;
+    int32_t *act_expert;  // [max_tokens * k]
+    int32_t *act_slot;
+    int32_t *act_off;
+    int32_t *act_cnt;
+    int32_t *cold_token;  // [max_tokens * k]
+    int32_t *cold_expert;
+    float *cold_w;
+    int32_t *hist;        // [E]
+    int32_t *counts;      // [4] n_hot, n_cold, n_active, M
+    unsigned *arrive;     // [1] grid arrival counter (reset by the last block)
+};
+
+struct RouteParams {
+    const uint16_t *x;   // bf16 bits [M, H]
+    const float *Wr;     // [E, H]
+    const float *bias;   // [E] or nullptr
+    const int32_t *e2s;  // [E]; ignored when all_hot
+    int M, H, E, k, nchunk;
+    int all_hot;         // prefill: every expert is hot, slot = expert id
+    RouteBuffers b;
+};
+
+struct ExpertGeometry {
+    int H, I;
+    size_t expert_bytes;
+    size_t off_wg_codes, off_wg_scales, off_wu_codes, off_wu_scales, off_wd_codes, off_wd_scales;
+};
+
+inline ExpertGeometry make_geometry(int H, int I) {
+    ExpertGeometry g;
+    g.H = H;
+    g.I = I;
+    size_t c = (size_t)I * H / 2, s = (size_t)I * H / 32;
+    g.off_wg_codes = 0;
+    g.off_wg_scales = c;
+    g.off_wu_codes = c + s;
+    g.off_wu_scales = 2 * c + s;
+    g.off_wd_codes = 2 * c + 2 * s;
+    g.off_wd_scales = 3 * c + 2 * s;
+    g.expert_bytes = 3 * c + 3 * s;
+    return g;
+}
+
+struct DecodeParams {
+    const uint8_t *bank;    // slot bank (decode) or staging bank (prefill)
+    ExpertGeometry geo;
+    const uint16_t *x;      // bf16 [M, H]
+    const int32_t *counts;  // device counts from the route kernel
+    const int32_t *act_slot, *act_off, *act_cnt;
+    const int32_t *hot_token;
+    const float *hot_w;
+    float *h;               // [max_hot, I] fp32 scratch
+    void *out;              // [M, H]
+    int out_f32;
+};
+
+void launch_route(const RouteParams &p, cudaStream_t s, int num_sms);
+void launch_gateup(const DecodeParams &p, int M, cudaStream_t s, int num_sms);
+void launch_down(const DecodeParams &p, int M, cudaStream_t s, int num_sms);
+void launch_map_update(int32_t *e2s, int n, const int32_t *experts, const int32_t *slots, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,596 @@
+// The layer object and the C ABI calls (declared in include/moe.h).
+//
+// Streams: every compute kernel runs on the caller's stream.  Two internal
+// non-blocking streams carry copies: `d2h` mirrors the cold-route list to
+// page-locked host memory (forked from the caller's stream after routing,
+// joined back by moe_forward_slots), and `h2d` carries slot refills from the
+// page-locked host bank (onnxruntime PR #33976: pinned staging with
+// CUDA_EVENT_DISABLE_TIMING events for overlap; NInfer-Offload v0.4.0: refills
+// run in the background without stalling decode).
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "moe_internal.h"
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+#define CUDA_TRY(call)                                                                          \
+    do {                                                                                        \
+        cudaError_t _e = (call);                                                                \
+        if (_e != cudaSuccess) return fail(MOE_ECUDA, "%s: %s", #call, cudaGetErrorString(_e)); \
+    } while (0)
+
+struct PendingCopy {
+    int32_t expert, slot;
+    cudaEvent_t ev;
+};
+
+}  // namespace
+
+struct moe_layer {
+    moe_layer_desc d{};
+    int device = 0;
+    int num_sms = 0;
+    moe::ExpertGeometry geo{};
+    int nchunk = 0;
+    int max_hot = 0;
+
+    uint8_t *slots = nullptr;  // [S][expert_bytes]
+    float *Wr = nullptr;       // [E][H]
+    float *bias = nullptr;     // [E]
+    int32_t *e2s_dev = nullptr;
+    const uint8_t *host_bank = nullptr;
+    uint8_t *staging = nullptr;
+    size_t staging_bytes = 0;
+    bool staged = false;
+
+    moe::RouteBuffers rb{};
+    float *h = nullptr;  // [max_hot][I]
+    void *dev_block = nullptr;
+
+    // page-locked mirror
+    int32_t *m_counts = nullptr, *m_cold_token = nullptr, *m_cold_expert = nullptr, *m_hist = nullptr;
+    float *m_cold_w = nullptr;
+    void *pinned_block = nullptr;
+
+    cudaStream_t d2h = nullptr, h2d = nullptr;
+    cudaEvent_t ev_fork = nullptr, ev_route = nullptr, ev_fence = nullptr;
+    std::vector<cudaEvent_t> ev_copy;  // deterministic mode, one per pair
+    std::vector<cudaEvent_t> ev_pool;  // polled mode
+    std::vector<PendingCopy> pending;
+
+    // host policy state
+    std::vector<int32_t> e2s, s2e, e2s_visible;
+    std::vector<double> score;
+    std::vector<int64_t> last;
+    std::vector<uint8_t> in_flight;
+    int64_t step = 0;
+
+    // call-order state
+    const void *routed_x = nullptr;
+    int32_t routed_M = 0;
+    int64_t route_seq = 0, policy_seq = 0;
+    int fault = MOE_FAULT_NONE;
+    int64_t stats[4] = {0, 0, 0, 0};
+
+    // optional per-kernel timing: event pairs around route, gate/up and down launches
+    bool prof = false;
+    std::vector<cudaEvent_t> prof_ev[3];
+    size_t prof_n[3] = {0, 0, 0};
+};
+
+namespace {
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+void release(moe_layer *L) {
+    if (!L) return;
+    if (L->h2d) cudaStreamSynchronize(L->h2d);
+    if (L->d2h) cudaStreamSynchronize(L->d2h);
+    cudaFree(L->slots);
+    cudaFree(L->Wr);
+    cudaFree(L->bias);
+    cudaFree(L->e2s_dev);
+    cudaFree(L->dev_block);
+    cudaFree(L->h);
+    if (L->pinned_block) cudaFreeHost(L->pinned_block);
+    for (auto e : {L->ev_fork, L->ev_route, L->ev_fence})
+        if (e) cudaEventDestroy(e);
+    for (auto e : L->ev_copy) cudaEventDestroy(e);
+    for (auto e : L->ev_pool) cudaEventDestroy(e);
+    for (auto &p : L->pending) cudaEventDestroy(p.ev);
+    for (auto &v : L->prof_ev)
+        for (auto e : v) cudaEventDestroy(e);
+    if (L->d2h) cudaStreamDestroy(L->d2h);
+    if (L->h2d) cudaStreamDestroy(L->h2d);
+    delete L;
+}
+
+int enqueue_map(moe_layer *L, const std::vector<int32_t> &ex, const std::vector<int32_t> &sl, cudaStream_t s) {
+    if (ex.empty()) return MOE_OK;
+    moe::launch_map_update(L->e2s_dev, (int)ex.size(), ex.data(), sl.data(), s);
+    CUDA_TRY(cudaGetLastError());
+    for (size_t i = 0; i < ex.size(); ++i) L->e2s_visible[ex[i]] = sl[i];
+    return MOE_OK;
+}
+
+// Records the opening or closing event of timed kernel `which` (0 route, 1 gate/up, 2 down).
+cudaError_t prof_mark(moe_layer *L, int which, cudaStream_t s) {
+    if (!L->prof) return cudaSuccess;
+    auto &v = L->prof_ev[which];
+    size_t &n = L->prof_n[which];
+    if (n == v.size()) {
+        cudaEvent_t e;
+        cudaError_t rc = cudaEventCreate(&e);
+        if (rc != cudaSuccess) return rc;
+        v.push_back(e);
+    }
+    return cudaEventRecord(v[n++], s);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_last_error(void) { return g_err.c_str(); }
+
+int moe_layer_create(const moe_layer_desc *desc, const float *router_w_dev, const float *router_bias_dev,
+                     const uint8_t *host_bank, const int32_t *expert_to_slot_host, void *stream,
+                     moe_layer **out) {
+    g_err.clear();
+    if (!out) return fail(MOE_EINVAL, "out is NULL");
+    *out = nullptr;
+    if (!desc || !router_w_dev || !host_bank || !expert_to_slot_host)
+        return fail(MOE_EINVAL, "desc, router_w_dev, host_bank and expert_to_slot_host are required");
+    const moe_layer_desc d = *desc;
+    if (d.hidden <= 0 || d.hidden % 64 || d.inter <= 0 || d.inter % 64)
+        return fail(MOE_EINVAL, "hidden and inter must be positive multiples of 64 (got %d, %d)", d.hidden, d.inter);
+    if (d.top_k < 1 || d.top_k > moe::kMaxTopK || d.num_experts < d.top_k || d.num_experts > moe::kMaxExperts)
+        return fail(MOE_EINVAL, "need 1 <= top_k <= %d and top_k <= num_experts <= %d", moe::kMaxTopK,
+                    moe::kMaxExperts);
+    if (d.num_slots < d.top_k || d.num_slots > d.num_experts)
+        return fail(MOE_EINVAL, "need top_k <= num_slots <= num_experts (got %d)", d.num_slots);
+    if (d.max_tokens < 1 || d.max_tokens > moe::kMaxTokens)
+        return fail(MOE_EINVAL, "max_tokens must be in [1, %d]", moe::kMaxTokens);
+    if (d.out_dtype != MOE_OUT_BF16 && d.out_dtype != MOE_OUT_F32) return fail(MOE_EINVAL, "bad out_dtype");
+    if (d.max_refills_per_step < 0 || d.max_refills_per_step > 16)
+        return fail(MOE_EINVAL, "max_refills_per_step must be in [0, 16]");
+    if (!(d.score_decay > 0.f && d.score_decay <= 1.f)) return fail(MOE_EINVAL, "score_decay must be in (0, 1]");
+    if (d.visibility != MOE_VIS_DETERMINISTIC && d.visibility != MOE_VIS_POLLED)
+        return fail(MOE_EINVAL, "bad visibility");
+    const int dec_tokens = d.max_tokens < moe::kDecodeMaxTokens ? d.max_tokens : moe::kDecodeMaxTokens;
+    if ((size_t)dec_tokens * d.hidden * sizeof(float) > (size_t)moe::kDecodeSmemLimit)
+        return fail(MOE_EINVAL, "hidden %d too large for the decode kernels", d.hidden);
+
+    cudaPointerAttributes pa{};
+    if (cudaPointerGetAttributes(&pa, host_bank) != cudaSuccess || pa.type != cudaMemoryTypeHost) {
+        cudaGetLastError();
+        return fail(MOE_EINVAL, "host_bank must be page-locked host memory (cudaHostAlloc / cudaHostRegister)");
+    }
+    std::vector<int32_t> e2s(expert_to_slot_host, expert_to_slot_host + d.num_experts);
+    std::vector<int32_t> s2e(d.num_slots, -1);
+    for (int e = 0; e < d.num_experts; ++e) {
+        const int s = e2s[e];
+        if (s < -1 || s >= d.num_slots) return fail(MOE_EINVAL, "expert_to_slot[%d] = %d out of range", e, s);
+        if (s >= 0) {
+            if (s2e[s] >= 0) return fail(MOE_EINVAL, "slot %d given to experts %d and %d", s, s2e[s], e);
+            s2e[s] = e;
+        }
+    }
+
+    moe_layer *L = new moe_layer();
+    L->d = d;
+    L->host_bank = host_bank;
+    L->geo = moe::make_geometry(d.hidden, d.inter);
+    L->nchunk = (d.hidden + moe::kRouteChunk - 1) / moe::kRouteChunk;
+    L->max_hot = d.max_tokens * d.top_k;
+    L->e2s = e2s;
+    L->e2s_visible = e2s;
+    L->s2e = s2e;
+    L->score.assign(d.num_experts, 0.0);
+    L->last.assign(d.num_experts, -1);
+    L->in_flight.assign(d.num_experts, 0);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    auto bail = [&](int code) {
+        release(L);
+        return code;
+    };
+#define CREATE_TRY(call)                                                         \
+    do {                                                                         \
+        cudaError_t _e = (call);                                                 \
+        if (_e != cudaSuccess) {                                                 \
+            int _c = (_e == cudaErrorMemoryAllocation) ? MOE_ENOMEM : MOE_ECUDA; \
+            fail(_c, "%s: %s", #call, cudaGetErrorString(_e));                   \
+            cudaGetLastError();                                                  \
+            return bail(_c);                                                     \
+        }                                                                        \
+    } while (0)
+
+    CREATE_TRY(cudaGetDevice(&L->device));
+    CREATE_TRY(cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, L->device));
+    const int E = d.num_experts, H = d.hidden, I = d.inter, k = d.top_k, mt = d.max_tokens;
+    const size_t eb = L->geo.expert_bytes;
+    CREATE_TRY(cudaMalloc(&L->slots, (size_t)d.num_slots * eb));
+    CREATE_TRY(cudaMalloc(&L->Wr, (size_t)E * H * sizeof(float)));
+    CREATE_TRY(cudaMalloc(&L->bias, (size_t)E * sizeof(float)));
+    CREATE_TRY(cudaMalloc(&L->e2s_dev, (size_t)E * sizeof(int32_t)));
+    CREATE_TRY(cudaMalloc(&L->h, (size_t)L->max_hot * I * sizeof(float)));
+
+    // route scratch in one block
+    const size_t nh = (size_t)L->max_hot;
+    const size_t sizes[] = {
+        (size_t)L->nchunk * mt * E * 4,          // logit_part
+        (size_t)mt * k * 4, (size_t)mt * k * 4,  // topk ids, w
+        nh * 4, nh * 4, nh * 4,                  // hot expert/token/w
+        nh * 4, nh * 4, nh * 4, nh * 4,          // act expert/slot/off/cnt
+        nh * 4, nh * 4, nh * 4,                  // cold token/expert/w
+        (size_t)E * 4, 16, 16};                  // hist, counts, arrive
+    size_t total = 0;
+    for (size_t s : sizes) total += align_up(s, 256);
+    CREATE_TRY(cudaMalloc(&L->dev_block, total));
+    {
+        char *p = static_cast<char *>(L->dev_block);
+        void **dst[] = {(void **)&L->rb.logit_part, (void **)&L->rb.topk_ids, (void **)&L->rb.topk_w,
+                        (void **)&L->rb.hot_expert, (void **)&L->rb.hot_token, (void **)&L->rb.hot_w,
+                        (void **)&L->rb.act_expert, (void **)&L->rb.act_slot, (void **)&L->rb.act_off,
+                        (void **)&L->rb.act_cnt, (void **)&L->rb.cold_token, (void **)&L->rb.cold_expert,
+                        (void **)&L->rb.cold_w, (void **)&L->rb.hist, (void **)&L->rb.counts,
+                        (void **)&L->rb.arrive};
+        for (size_t i = 0; i < sizeof(sizes) / sizeof(sizes[0]); ++i) {
+            *dst[i] = p;
+            p += align_up(sizes[i], 256);
+        }
+    }
+    CREATE_TRY(cudaMemsetAsync(L->dev_block, 0, total, st));
+
+    // page-locked mirror: counts[4], hist[E], cold token/expert/w [max_hot]
+    const size_t psz = align_up(16, 64) + align_up((size_t)E * 4, 64) + 3 * align_up(nh * 4, 64);
+    CREATE_TRY(cudaHostAlloc(&L->pinned_block, psz, cudaHostAllocDefault));
+    memset(L->pinned_block, 0, psz);
+    {
+        char *p = static_cast<char *>(L->pinned_block);
+        L->m_counts = (int32_t *)p;
+        p += align_up(16, 64);
+        L->m_hist = (int32_t *)p;
+        p += align_up((size_t)E * 4, 64);
+        L->m_cold_token = (int32_t *)p;
+        p += align_up(nh * 4, 64);
+        L->m_cold_expert = (int32_t *)p;
+        p += align_up(nh * 4, 64);
+        L->m_cold_w = (float *)p;
+    }
+
+    CREATE_TRY(cudaStreamCreateWithFlags(&L->d2h, cudaStreamNonBlocking));
+    CREATE_TRY(cudaStreamCreateWithFlags(&L->h2d, cudaStreamNonBlocking));
+    for (cudaEvent_t *e : {&L->ev_fork, &L->ev_route, &L->ev_fence})
+        CREATE_TRY(cudaEventCreateWithFlags(e, cudaEventDisableTiming));
+    L->ev_copy.resize(d.max_refills_per_step);
+    for (auto &e : L->ev_copy) CREATE_TRY(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+
+    CREATE_TRY(cudaMemcpyAsync(L->Wr, router_w_dev, (size_t)E * H * sizeof(float), cudaMemcpyDeviceToDevice, st));
+    if (router_bias_dev)
+        CREATE_TRY(cudaMemcpyAsync(L->bias, router_bias_dev, (size_t)E * sizeof(float), cudaMemcpyDeviceToDevice, st));
+    else
+        CREATE_TRY(cudaMemsetAsync(L->bias, 0, (size_t)E * sizeof(float), st));
+    CREATE_TRY(cudaMemcpyAsync(L->e2s_dev, e2s.data(), (size_t)E * sizeof(int32_t), cudaMemcpyHostToDevice, st));
+    for (int e = 0; e < E; ++e)
+        if (e2s[e] >= 0)
+            CREATE_TRY(cudaMemcpyAsync(L->slots + (size_t)e2s[e] * eb, host_bank + (size_t)e * eb, eb,
+                                       cudaMemcpyHostToDevice, st));
+    CREATE_TRY(cudaStreamSynchronize(st));
+#undef CREATE_TRY
+    *out = L;
+    return MOE_OK;
+}
+
+int moe_route(moe_layer *L, const void *x_dev, int32_t M, void *stream, moe_route_result *res) {
+    g_err.clear();
+    if (!L || !x_dev) return fail(MOE_EINVAL, "layer and x_dev are required");
+    if (M < 1 || M > L->d.max_tokens) return fail(MOE_EINVAL, "M = %d outside [1, max_tokens=%d]", M, L->d.max_tokens);
+    if (reinterpret_cast<uintptr_t>(x_dev) % 16) return fail(MOE_EINVAL, "x_dev must be 16-byte aligned");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int E = L->d.num_experts, k = L->d.top_k;
+    moe::RouteParams p{};
+    p.x = static_cast<const uint16_t *>(x_dev);
+    p.Wr = L->Wr;
+    p.bias = L->bias;
+    p.e2s = L->e2s_dev;
+    p.M = M;
+    p.H = L->d.hidden;
+    p.E = E;
+    p.k = k;
+    p.nchunk = L->nchunk;
+    p.all_hot = M > moe::kDecodeMaxTokens;
+    p.b = L->rb;
+    CUDA_TRY(prof_mark(L, 0, st));
+    moe::launch_route(p, st, L->num_sms);
+    CUDA_TRY(cudaGetLastError());
+    CUDA_TRY(prof_mark(L, 0, st));
+
+    // mirror counts, histogram and cold triples to page-locked memory off the compute chain
+    const size_t n = (size_t)M * k;
+    CUDA_TRY(cudaEventRecord(L->ev_fork, st));
+    CUDA_TRY(cudaStreamWaitEvent(L->d2h, L->ev_fork, 0));
+    CUDA_TRY(cudaMemcpyAsync(L->m_counts, L->rb.counts, 16, cudaMemcpyDeviceToHost, L->d2h));
+    CUDA_TRY(cudaMemcpyAsync(L->m_hist, L->rb.hist, (size_t)E * 4, cudaMemcpyDeviceToHost, L->d2h));
+    CUDA_TRY(cudaMemcpyAsync(L->m_cold_token, L->rb.cold_token, n * 4, cudaMemcpyDeviceToHost, L->d2h));
+    CUDA_TRY(cudaMemcpyAsync(L->m_cold_expert, L->rb.cold_expert, n * 4, cudaMemcpyDeviceToHost, L->d2h));
+    CUDA_TRY(cudaMemcpyAsync(L->m_cold_w, L->rb.cold_w, n * 4, cudaMemcpyDeviceToHost, L->d2h));
+    CUDA_TRY(cudaEventRecord(L->ev_route, L->d2h));
+
+    L->routed_x = x_dev;
+    L->routed_M = M;
+    L->route_seq++;
+    if (res) {
+        res->M = M;
+        res->topk_ids = L->rb.topk_ids;
+        res->topk_w = L->rb.topk_w;
+        res->hot_expert = L->rb.hot_expert;
+        res->hot_token = L->rb.hot_token;
+        res->hot_w = L->rb.hot_w;
+        res->act_expert = L->rb.act_expert;
+        res->act_slot = L->rb.act_slot;
+        res->act_off = L->rb.act_off;
+        res->act_cnt = L->rb.act_cnt;
+        res->cold_token = L->rb.cold_token;
+        res->cold_expert = L->rb.cold_expert;
+        res->cold_w = L->rb.cold_w;
+        res->hist = L->rb.hist;
+        res->counts = L->rb.counts;
+        res->h_counts = L->m_counts;
+        res->h_cold_token = L->m_cold_token;
+        res->h_cold_expert = L->m_cold_expert;
+        res->h_cold_w = L->m_cold_w;
+        res->h_hist = L->m_hist;
+        res->done = L->ev_route;
+    }
+    return MOE_OK;
+}
+
+int moe_forward_slots(moe_layer *L, const void *x_dev, void *out_dev, int32_t M, void *stream) {
+    g_err.clear();
+    if (!L || !x_dev || !out_dev) return fail(MOE_EINVAL, "layer, x_dev and out_dev are required");
+    if (L->routed_M == 0 || L->routed_x != x_dev || L->routed_M != M)
+        return fail(MOE_ESTATE, "moe_forward_slots needs the x_dev and M of the last moe_route");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    moe::DecodeParams p{};
+    p.geo = L->geo;
+    p.x = static_cast<const uint16_t *>(x_dev);
+    p.counts = L->rb.counts;
+    p.act_slot = L->rb.act_slot;
+    p.act_off = L->rb.act_off;
+    p.act_cnt = L->rb.act_cnt;
+    p.hot_token = L->rb.hot_token;
+    p.hot_w = L->rb.hot_w;
+    p.h = L->h;
+    p.out = out_dev;
+    p.out_f32 = L->d.out_dtype == MOE_OUT_F32;
+    if (M <= moe::kDecodeMaxTokens) {
+        p.bank = L->slots;
+        CUDA_TRY(prof_mark(L, 1, st));
+        moe::launch_gateup(p, M, st, L->num_sms);
+        CUDA_TRY(cudaGetLastError());
+        CUDA_TRY(prof_mark(L, 1, st));
+        CUDA_TRY(prof_mark(L, 2, st));
+        moe::launch_down(p, M, st, L->num_sms);
+        CUDA_TRY(cudaGetLastError());
+        CUDA_TRY(prof_mark(L, 2, st));
+    } else {
+        return fail(MOE_ESTATE, "prefill (M > %d) needs the prefill kernels, which this build does not have",
+                    moe::kDecodeMaxTokens);
+    }
+    CUDA_TRY(cudaStreamWaitEvent(st, L->ev_route, 0));  // join the mirror copies
+    return MOE_OK;
+}
+
+int moe_cache_update(moe_layer *L, void *stream, int32_t *n_refills_out) {
+    g_err.clear();
+    if (n_refills_out) *n_refills_out = 0;
+    if (!L) return fail(MOE_EINVAL, "layer is NULL");
+    const int E = L->d.num_experts, S = L->d.num_slots;
+    if (S >= E) return MOE_OK;  // every expert resident: nothing to refill
+    if (L->route_seq == L->policy_seq)
+        return fail(MOE_ESTATE, "moe_cache_update needs a moe_route since the last update");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    CUDA_TRY(cudaEventSynchronize(L->ev_route));
+    L->policy_seq = L->route_seq;
+
+    // polled mode: map the experts whose copies have landed
+    if (L->d.visibility == MOE_VIS_POLLED && !L->pending.empty()) {
+        std::vector<int32_t> ex, sl;
+        std::vector<PendingCopy> still;
+        for (auto &pc : L->pending) {
+            cudaError_t q = cudaEventQuery(pc.ev);
+            if (q == cudaSuccess) {
+                ex.push_back(pc.expert);
+                sl.push_back(pc.slot);
+                L->in_flight[pc.expert] = 0;
+                L->ev_pool.push_back(pc.ev);
+            } else if (q == cudaErrorNotReady) {
+                still.push_back(pc);
+            } else {
+                return fail(MOE_ECUDA, "refill copy failed: %s", cudaGetErrorString(q));
+            }
+        }
+        L->pending.swap(still);
+        int rc = enqueue_map(L, ex, sl, st);
+        if (rc) return rc;
+    }
+
+    const int R = L->d.max_refills_per_step;
+    std::vector<int32_t> pe(R > 0 ? R : 1), ps(pe.size()), pv(pe.size());
+    // the decision runs on copies so that an injected fault leaves the state unchanged
+    std::vector<double> score = L->score;
+    std::vector<int64_t> last = L->last;
+    std::vector<int32_t> e2s = L->e2s, s2e = L->s2e;
+    const int n = moe_policy_step(score.data(), last.data(), e2s.data(), s2e.data(), E, S, L->m_hist, L->step,
+                                  (double)L->d.score_decay, R, L->in_flight.data(), pe.data(), ps.data(), pv.data());
+    if (n < 0) return fail(MOE_EINVAL, "policy rejected its arguments");
+    if (n > 0 && L->fault == MOE_FAULT_COPY) {
+        L->fault = MOE_FAULT_NONE;
+        return fail(MOE_ECUDA, "injected refill copy failure (no copy issued, map unchanged)");
+    }
+    L->score.swap(score);
+    L->last.swap(last);
+    L->e2s.swap(e2s);
+    L->s2e.swap(s2e);
+    L->step++;
+    L->stats[2] += (int64_t)L->routed_M * L->d.top_k;
+    L->stats[3] += L->m_counts[0];
+
+    if (n == 0) return MOE_OK;
+    const size_t eb = L->geo.expert_bytes;
+    std::vector<int32_t> unmap_e, unmap_s, map_e, map_s;
+    for (int i = 0; i < n; ++i) {
+        unmap_e.push_back(pv[i]);
+        unmap_s.push_back(-1);
+    }
+    if (L->d.visibility == MOE_VIS_POLLED) {
+        // victims leave the map in stream order before their slots are overwritten
+        int rc = enqueue_map(L, unmap_e, unmap_s, st);
+        if (rc) return rc;
+    }
+    // everything already on the compute stream (including reads of the victims' slots) precedes the copies
+    CUDA_TRY(cudaEventRecord(L->ev_fence, st));
+    CUDA_TRY(cudaStreamWaitEvent(L->h2d, L->ev_fence, 0));
+    for (int i = 0; i < n; ++i) {
+        CUDA_TRY(cudaMemcpyAsync(L->slots + (size_t)ps[i] * eb, L->host_bank + (size_t)pe[i] * eb, eb,
+                                 cudaMemcpyHostToDevice, L->h2d));
+        L->stats[0] += 1;
+        L->stats[1] += (int64_t)eb;
+        if (L->d.visibility == MOE_VIS_DETERMINISTIC) {
+            CUDA_TRY(cudaEventRecord(L->ev_copy[i], L->h2d));
+            CUDA_TRY(cudaStreamWaitEvent(st, L->ev_copy[i], 0));
+        } else {
+            cudaEvent_t ev;
+            if (L->ev_pool.empty()) {
+                CUDA_TRY(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+            } else {
+                ev = L->ev_pool.back();
+                L->ev_pool.pop_back();
+            }
+            CUDA_TRY(cudaEventRecord(ev, L->h2d));
+            L->pending.push_back({pe[i], ps[i], ev});
+            L->in_flight[pe[i]] = 1;
+        }
+    }
+    if (L->d.visibility == MOE_VIS_DETERMINISTIC) {
+        map_e = unmap_e;
+        map_s = unmap_s;
+        for (int i = 0; i < n; ++i) {
+            map_e.push_back(pe[i]);
+            map_s.push_back(ps[i]);
+        }
+        int rc = enqueue_map(L, map_e, map_s, st);
+        if (rc) return rc;
+    }
+    if (n_refills_out) *n_refills_out = n;
+    return MOE_OK;
+}
+
+int moe_destroy(moe_layer *L) {
+    g_err.clear();
+    release(L);
+    return MOE_OK;
+}
+
+int moe_layer_set_bias(moe_layer *L, const float *bias_dev, void *stream) {
+    g_err.clear();
+    if (!L) return fail(MOE_EINVAL, "layer is NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t n = (size_t)L->d.num_experts * sizeof(float);
+    if (bias_dev)
+        CUDA_TRY(cudaMemcpyAsync(L->bias, bias_dev, n, cudaMemcpyDeviceToDevice, st));
+    else
+        CUDA_TRY(cudaMemsetAsync(L->bias, 0, n, st));
+    return MOE_OK;
+}
+
+int moe_layer_attach_staging(moe_layer *L, void *staging_dev, size_t bytes) {
+    g_err.clear();
+    if (!L) return fail(MOE_EINVAL, "layer is NULL");
+    if (staging_dev && bytes < (size_t)L->d.num_experts * L->geo.expert_bytes)
+        return fail(MOE_EINVAL, "staging buffer needs %zu bytes, got %zu",
+                    (size_t)L->d.num_experts * L->geo.expert_bytes, bytes);
+    L->staging = static_cast<uint8_t *>(staging_dev);
+    L->staging_bytes = staging_dev ? bytes : 0;
+    L->staged = false;
+    return MOE_OK;
+}
+
+int moe_layer_stage_all(moe_layer *L, void *stream) {
+    g_err.clear();
+    if (!L) return fail(MOE_EINVAL, "layer is NULL");
+    if (!L->staging) return fail(MOE_ESTATE, "no staging buffer attached");
+    CUDA_TRY(cudaMemcpyAsync(L->staging, L->host_bank, (size_t)L->d.num_experts * L->geo.expert_bytes,
+                             cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream)));
+    L->staged = true;
+    return MOE_OK;
+}
+
+int moe_debug_get_map(const moe_layer *L, int32_t *out) {
+    if (!L || !out) return fail(MOE_EINVAL, "layer and out are required");
+    memcpy(out, L->e2s_visible.data(), L->e2s_visible.size() * sizeof(int32_t));
+    return MOE_OK;
+}
+
+int moe_debug_slot_ptr(const moe_layer *L, int32_t slot, const void **ptr) {
+    if (!L || !ptr || slot < 0 || slot >= L->d.num_slots) return fail(MOE_EINVAL, "bad slot");
+    *ptr = L->slots + (size_t)slot * L->geo.expert_bytes;
+    return MOE_OK;
+}
+
+int moe_debug_inject_fault(moe_layer *L, int32_t fault) {
+    if (!L || (fault != MOE_FAULT_NONE && fault != MOE_FAULT_COPY)) return fail(MOE_EINVAL, "bad fault");
+    L->fault = fault;
+    return MOE_OK;
+}
+
+int moe_debug_stats(const moe_layer *L, int64_t stats[4]) {
+    if (!L || !stats) return fail(MOE_EINVAL, "layer and stats are required");
+    for (int i = 0; i < 4; ++i) stats[i] = L->stats[i];
+    return MOE_OK;
+}
+
+int moe_debug_profile(moe_layer *L, int32_t enable) {
+    if (!L) return fail(MOE_EINVAL, "layer is NULL");
+    CUDA_TRY(cudaDeviceSynchronize());
+    L->prof = enable != 0;
+    for (auto &n : L->prof_n) n = 0;
+    return MOE_OK;
+}
+
+int moe_debug_profile_read(moe_layer *L, double out[4]) {
+    if (!L || !out) return fail(MOE_EINVAL, "layer and out are required");
+    for (int i = 0; i < 4; ++i) out[i] = 0.0;
+    for (int w = 0; w < 3; ++w) {
+        for (size_t i = 0; i + 1 < L->prof_n[w]; i += 2) {
+            CUDA_TRY(cudaEventSynchronize(L->prof_ev[w][i + 1]));
+            float ms = 0.f;
+            CUDA_TRY(cudaEventElapsedTime(&ms, L->prof_ev[w][i], L->prof_ev[w][i + 1]));
+            out[w] += ms;
+        }
+    }
+    out[3] = (double)(L->prof_n[1] / 2);
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,67 @@
+// Slot-cache decision for one layer and one step, on the host.
+//
+// NInfer-Offload v0.4.0 "expert cache": slots follow recent routing; experts
+// the router keeps choosing are copied to the GPU in the background, at most
+// two per layer and call, replacing the least used.  tinyserve README "How it
+// works" 3: frequency-recency eviction keyed by (layer, expert).
+//
+// Score: score = decay * score + routes this step (decay 1 = LFU).
+// Candidates: experts neither resident nor in flight, best score first (ties:
+// lower id).  Victims: resident experts not in flight, lowest score first
+// (ties: least recently routed, then lower slot).  Pair i is taken while the
+// candidate's score is strictly greater than the victim's; at most R pairs.
+#include <cstdint>
+#include <vector>
+
+#include "../../include/moe.h"
+
+extern "C" int moe_policy_step(double *score, int64_t *last, int32_t *e2s, int32_t *s2e, int32_t E, int32_t S,
+                               const int32_t *hist, int64_t step, double decay, int32_t R,
+                               const uint8_t *in_flight, int32_t *pair_expert, int32_t *pair_slot,
+                               int32_t *pair_victim) {
+    if (!score || !last || !e2s || !s2e || !hist || E <= 0 || S <= 0 || S > E || R < 0 ||
+        (R > 0 && (!pair_expert || !pair_slot || !pair_victim)))
+        return -1;
+    for (int32_t e = 0; e < E; ++e) {
+        // a separate multiply and add, so every host compiler gives the same doubles
+        const double decayed = decay * score[e];
+        score[e] = decayed + static_cast<double>(hist[e]);
+        if (hist[e] > 0) last[e] = step;
+    }
+    std::vector<char> taken(static_cast<size_t>(E), 0);
+    auto busy = [&](int32_t e) { return taken[e] || (in_flight && in_flight[e]); };
+
+    int32_t n = 0;
+    for (int32_t p = 0; p < R; ++p) {
+        int32_t cand = -1;
+        for (int32_t e = 0; e < E; ++e) {
+            if (e2s[e] >= 0 || busy(e)) continue;
+            if (cand < 0 || score[e] > score[cand]) cand = e;
+        }
+        if (cand < 0) break;
+        int32_t vic = -1;
+        for (int32_t s = 0; s < S; ++s) {
+            const int32_t e = s2e[s];
+            if (e < 0 || busy(e)) continue;
+            if (vic < 0) {
+                vic = e;
+                continue;
+            }
+            const bool lower = score[e] < score[vic];
+            const bool same = score[e] == score[vic];
+            if (lower || (same && last[e] < last[vic]) || (same && last[e] == last[vic] && s < e2s[vic])) vic = e;
+        }
+        if (vic < 0 || !(score[cand] > score[vic])) break;
+        taken[cand] = taken[vic] = 1;
+        pair_expert[n] = cand;
+        pair_slot[n] = e2s[vic];
+        pair_victim[n] = vic;
+        ++n;
+    }
+    for (int32_t i = 0; i < n; ++i) {
+        e2s[pair_victim[i]] = -1;
+        e2s[pair_expert[i]] = pair_slot[i];
+        s2e[pair_slot[i]] = pair_expert[i];
+    }
+    return n;
+}

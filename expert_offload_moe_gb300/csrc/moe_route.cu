@@ -1,0 +1,304 @@
+// Router GEMV, top-k + softmax, and slot compaction in one launch.
+//
+// Phase 1 (every block): one warp per (expert row, 256-column chunk) of the
+// router: 128-bit loads of Wr and x, fp32 products, warp-shuffle sum, partial
+// logits written to scratch.  The grid spans E x ceil(H/256) warp tasks, so
+// the router is read by many thread blocks at once (NInfer-Offload v0.4.0:
+// routing no longer runs in a single thread block).
+//
+// Phase 2 (the last block to arrive, found with a grid arrival counter; no
+// block ever waits for another): per token, the partials are summed in chunk
+// order, the bias added, the top-k taken by warp-shuffle arg-max rounds (ties
+// to the lower expert id), and the softmax taken over the selected logits.
+// Then the routes are split by expert_to_slot (onnxruntime PR #33976:
+// slot < 0 is cold) and compacted with block-level prefix scans:
+//   hot routes  ordered by (expert, token), grouped per active expert
+//   cold routes ordered by (token, expert)
+// All counts stay in device memory so the launch shape never depends on the
+// routing (xinfer docs "How it works": fixed launch shapes, miss count in
+// device memory, decode inside CUDA graphs).
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Exclusive scan of one int per thread across the block; returns the
+// exclusive prefix and writes the block total to *total.
+__device__ int block_scan_exclusive(int v, int *total) {
+    __shared__ int warp_tot[kWarps];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int t = lane < kWarps ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < kWarps; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        if (lane < kWarps) warp_tot[lane] = t;
+    }
+    __syncthreads();
+    const int base = w ? warp_tot[w - 1] : 0;
+    *total = warp_tot[kWarps - 1];
+    __syncthreads();
+    return base + x - v;
+}
+
+// Exclusive scan in place over a[0..n) (shared memory), chunked per thread.
+__device__ int block_scan_array(int *a, int n) {
+    const int per = (n + kThreads - 1) / kThreads;
+    const int lo = min((int)threadIdx.x * per, n), hi = min(lo + per, n);
+    int s = 0;
+    for (int i = lo; i < hi; ++i) s += a[i];
+    int total;
+    int run = block_scan_exclusive(s, &total);
+    for (int i = lo; i < hi; ++i) {
+        int v = a[i];
+        a[i] = run;
+        run += v;
+    }
+    __syncthreads();
+    return total;
+}
+
+__global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int H = p.H, E = p.E, M = p.M, k = p.k;
+
+    // ---------------- phase 1: partial logits -----------------------------
+    const int ntask = E * p.nchunk;
+    for (int task = blockIdx.x * kWarps + warp; task < ntask; task += gridDim.x * kWarps) {
+        const int e = task / p.nchunk, c = task - e * p.nchunk;
+        const int col = c * kRouteChunk + lane * 8;
+        const bool valid = col < H;  // H % 64 == 0, so a valid lane has all 8 columns
+        float w8[8];
+        if (valid) {
+            const float4 a = __ldg(reinterpret_cast<const float4 *>(p.Wr + (size_t)e * H + col));
+            const float4 b = __ldg(reinterpret_cast<const float4 *>(p.Wr + (size_t)e * H + col + 4));
+            w8[0] = a.x; w8[1] = a.y; w8[2] = a.z; w8[3] = a.w;
+            w8[4] = b.x; w8[5] = b.y; w8[6] = b.z; w8[7] = b.w;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w8[i] = 0.f;
+        }
+        for (int t = 0; t < M; ++t) {
+            float acc = 0.f;
+            if (valid) {
+                const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)t * H + col));
+                acc = fmaf(bf16_lo(xv.x), w8[0], acc);
+                acc = fmaf(bf16_hi(xv.x), w8[1], acc);
+                acc = fmaf(bf16_lo(xv.y), w8[2], acc);
+                acc = fmaf(bf16_hi(xv.y), w8[3], acc);
+                acc = fmaf(bf16_lo(xv.z), w8[4], acc);
+                acc = fmaf(bf16_hi(xv.z), w8[5], acc);
+                acc = fmaf(bf16_lo(xv.w), w8[6], acc);
+                acc = fmaf(bf16_hi(xv.w), w8[7], acc);
+            }
+            acc = warp_sum(acc);
+            if (lane == 0) p.b.logit_part[((size_t)c * M + t) * E + e] = acc;
+        }
+    }
+
+    // ---------------- arrival: the last block continues --------------------
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(p.b.arrive, 1u) == gridDim.x - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (threadIdx.x == 0) *p.b.arrive = 0u;  // every block has arrived: ready for the next launch
+
+    // ---------------- phase 2a: top-k + softmax per token -------------------
+    __shared__ float s_l[kWarps][kMaxExperts];
+    __shared__ int s_hist[kMaxExperts];
+    __shared__ int s_hot_off[kMaxExperts];
+    __shared__ int s_act_pos[kMaxExperts];
+    __shared__ int s_cold[kMaxTokens];
+
+    for (int e = threadIdx.x; e < E; e += kThreads) s_hist[e] = 0;
+    __syncthreads();
+
+    for (int t = warp; t < M; t += kWarps) {
+        for (int e = lane; e < E; e += 32) {
+            float v = 0.f;
+            for (int c = 0; c < p.nchunk; ++c) v += __ldcg(p.b.logit_part + ((size_t)c * M + t) * E + e);
+            v += p.bias ? p.bias[e] : 0.f;
+            s_l[warp][e] = (v != v) ? -INFINITY : v;  // NaN marks a taken expert below
+        }
+        __syncwarp();
+        int sel_id[kMaxTopK];
+        float sel_l[kMaxTopK];
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j) {
+            sel_id[j] = 0;
+            sel_l[j] = 0.f;
+            if (j < k) {
+                float bv = -INFINITY;
+                int be = 0x7fffffff;
+                for (int e = lane; e < E; e += 32) {
+                    const float v = s_l[warp][e];
+                    if (v != v) continue;  // taken
+                    if (v > bv || (v == bv && e < be)) {
+                        bv = v;
+                        be = e;
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                    const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                    if (ov > bv || (ov == bv && oe < be)) {
+                        bv = ov;
+                        be = oe;
+                    }
+                }
+                // E >= k and no stored value is NaN, so a candidate always exists: be < E
+                sel_id[j] = be;
+                sel_l[j] = bv;
+                if (lane == (be & 31)) s_l[warp][be] = __int_as_float(0x7fc00000);
+                __syncwarp();
+            }
+        }
+        const float lmax = sel_l[0];
+        float den = 0.f;
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j)
+            if (j < k) den += expf(sel_l[j] - lmax);
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j) {
+            if (j < k && lane == j) {
+                p.b.topk_ids[(size_t)t * k + j] = sel_id[j];
+                p.b.topk_w[(size_t)t * k + j] = expf(sel_l[j] - lmax) / den;
+                atomicAdd(&s_hist[sel_id[j]], 1);
+            }
+        }
+        __syncwarp();
+    }
+    __syncthreads();
+
+    // ---------------- phase 2b: compaction ----------------------------------
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+        const bool hot = p.all_hot || p.e2s[e] >= 0;
+        s_hot_off[e] = hot ? s_hist[e] : 0;
+        s_act_pos[e] = (hot && s_hist[e] > 0) ? 1 : 0;
+    }
+    __syncthreads();
+    const int n_hot = block_scan_array(s_hot_off, E);
+    const int n_act = block_scan_array(s_act_pos, E);
+
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+        p.b.hist[e] = s_hist[e];
+        const bool hot = p.all_hot || p.e2s[e] >= 0;
+        if (!hot || s_hist[e] == 0) continue;
+        const int a = s_act_pos[e];
+        int pos = s_hot_off[e];
+        p.b.act_expert[a] = e;
+        p.b.act_slot[a] = p.all_hot ? e : p.e2s[e];
+        p.b.act_off[a] = pos;
+        p.b.act_cnt[a] = s_hist[e];
+        for (int t = 0; t < M; ++t)
+            for (int j = 0; j < k; ++j)
+                if (p.b.topk_ids[(size_t)t * k + j] == e) {
+                    p.b.hot_expert[pos] = e;
+                    p.b.hot_token[pos] = t;
+                    p.b.hot_w[pos] = p.b.topk_w[(size_t)t * k + j];
+                    ++pos;
+                }
+    }
+
+    // cold routes: per token, ascending expert
+    for (int t = threadIdx.x; t < M; t += kThreads) {
+        int n = 0;
+        if (!p.all_hot)
+            for (int j = 0; j < k; ++j) n += p.e2s[p.b.topk_ids[(size_t)t * k + j]] < 0;
+        s_cold[t] = n;
+    }
+    __syncthreads();
+    const int n_cold = block_scan_array(s_cold, M);
+    if (!p.all_hot) {
+        for (int t = threadIdx.x; t < M; t += kThreads) {
+            int ce[kMaxTopK];
+            float cw[kMaxTopK];
+            int n = 0;
+            for (int j = 0; j < k; ++j) {
+                const int e = p.b.topk_ids[(size_t)t * k + j];
+                if (p.e2s[e] >= 0) continue;
+                const float wt = p.b.topk_w[(size_t)t * k + j];
+                int q = n++;  // insertion by expert id
+                while (q > 0 && ce[q - 1] > e) {
+                    ce[q] = ce[q - 1];
+                    cw[q] = cw[q - 1];
+                    --q;
+                }
+                ce[q] = e;
+                cw[q] = wt;
+            }
+            const int base = s_cold[t];
+            for (int q = 0; q < n; ++q) {
+                p.b.cold_token[base + q] = t;
+                p.b.cold_expert[base + q] = ce[q];
+                p.b.cold_w[base + q] = cw[q];
+            }
+        }
+    }
+    if (threadIdx.x == 0) {
+        p.b.counts[0] = n_hot;
+        p.b.counts[1] = n_cold;
+        p.b.counts[2] = n_act;
+        p.b.counts[3] = M;
+    }
+}
+
+constexpr int kMaxMapUpdates = 64;
+
+struct MapUpdate {
+    int n;
+    int32_t expert[kMaxMapUpdates];
+    int32_t slot[kMaxMapUpdates];
+};
+
+__global__ void map_update_kernel(int32_t *e2s, MapUpdate u) {
+    if (threadIdx.x == 0)
+        for (int i = 0; i < u.n; ++i) e2s[u.expert[i]] = u.slot[i];
+}
+
+}  // namespace
+
+void launch_route(const RouteParams &p, cudaStream_t s, int num_sms) {
+    const int ntask = p.E * p.nchunk;
+    int grid = (ntask + kWarps - 1) / kWarps;
+    grid = grid < 1 ? 1 : (grid > 8 * num_sms ? 8 * num_sms : grid);
+    route_kernel<<<grid, kThreads, 0, s>>>(p);
+}
+
+void launch_map_update(int32_t *e2s, int n, const int32_t *experts, const int32_t *slots, cudaStream_t s) {
+    MapUpdate u;
+    u.n = n < kMaxMapUpdates ? n : kMaxMapUpdates;
+    for (int i = 0; i < u.n; ++i) {
+        u.expert[i] = experts[i];
+        u.slot[i] = slots[i];
+    }
+    map_update_kernel<<<1, 32, 0, s>>>(e2s, u);
+}
+
+}  // namespace moe

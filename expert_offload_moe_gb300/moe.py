@@ -1,0 +1,205 @@
+"""ctypes binding of ``libmoe.so`` (include/moe.h), same call names.
+
+Argument marshalling only: every step of the layer runs in the library's
+CUDA kernels.  PyTorch provides device memory and streams.  If the library
+has not been built, ``lib()`` raises; there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmoe.so")
+
+MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_ETIMEOUT, MOE_ESTATE = range(6)
+MOE_OUT_BF16, MOE_OUT_F32 = 0, 1
+MOE_VIS_DETERMINISTIC, MOE_VIS_POLLED = 0, 1
+MOE_FAULT_NONE, MOE_FAULT_COPY = 0, 1
+
+EXPORTED = [
+    "moe_layer_create", "moe_route", "moe_forward_slots", "moe_cache_update", "moe_destroy", "moe_last_error",
+    "moe_layer_set_bias", "moe_layer_attach_staging", "moe_layer_stage_all", "moe_debug_get_map",
+    "moe_debug_slot_ptr", "moe_debug_inject_fault", "moe_debug_stats", "moe_debug_profile",
+    "moe_debug_profile_read", "moe_policy_step",
+]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"moe status {code}: {msg}")
+        self.code = code
+
+
+class LayerDesc(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("inter", ctypes.c_int32), ("num_experts", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("num_slots", ctypes.c_int32), ("max_tokens", ctypes.c_int32),
+                ("out_dtype", ctypes.c_int32), ("max_refills_per_step", ctypes.c_int32),
+                ("score_decay", ctypes.c_float), ("visibility", ctypes.c_int32)]
+
+
+_P = ctypes.c_void_p
+
+
+class RouteResult(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int32)] + [(n, _P) for n in (
+        "topk_ids", "topk_w", "hot_expert", "hot_token", "hot_w", "act_expert", "act_slot", "act_off",
+        "act_cnt", "cold_token", "cold_expert", "cold_w", "hist", "counts", "h_counts", "h_cold_token",
+        "h_cold_expert", "h_cold_w", "h_hist", "done")]
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m expert_offload_moe_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        i32, p = ctypes.c_int32, _P
+        L.moe_layer_create.argtypes = [ctypes.POINTER(LayerDesc), p, p, p, p, p, ctypes.POINTER(p)]
+        L.moe_route.argtypes = [p, p, i32, p, ctypes.POINTER(RouteResult)]
+        L.moe_forward_slots.argtypes = [p, p, p, i32, p]
+        L.moe_cache_update.argtypes = [p, p, ctypes.POINTER(i32)]
+        L.moe_destroy.argtypes = [p]
+        L.moe_last_error.argtypes = []
+        L.moe_last_error.restype = ctypes.c_char_p
+        L.moe_layer_set_bias.argtypes = [p, p, p]
+        L.moe_layer_attach_staging.argtypes = [p, p, ctypes.c_size_t]
+        L.moe_layer_stage_all.argtypes = [p, p]
+        L.moe_debug_get_map.argtypes = [p, p]
+        L.moe_debug_slot_ptr.argtypes = [p, i32, ctypes.POINTER(p)]
+        L.moe_debug_inject_fault.argtypes = [p, i32]
+        L.moe_debug_stats.argtypes = [p, p]
+        L.moe_debug_profile.argtypes = [p, i32]
+        L.moe_debug_profile_read.argtypes = [p, p]
+        L.moe_policy_step.argtypes = [p, p, p, p, i32, i32, p, ctypes.c_int64, ctypes.c_double, i32, p, p, p, p]
+        for name in EXPORTED:
+            if name != "moe_last_error":
+                getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def check(rc):
+    if rc != MOE_OK:
+        raise MoeError(rc, lib().moe_last_error().decode())
+    return rc
+
+
+def stream_ptr(stream):
+    if stream is None:
+        import torch
+
+        stream = torch.cuda.current_stream()
+    return _P(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+class Layer:
+    """One MoE layer: owns the slot bank, router copy, map and scratch on the GPU.
+
+    ``router_w`` / ``router_bias``: fp32 CUDA tensors [E, H] / [E] (copied);
+    ``host_bank``: page-locked uint8 CPU tensor [E, expert_bytes] (borrowed);
+    ``expert_to_slot``: int32 sequence [E].
+    """
+
+    def __init__(self, hidden, inter, num_experts, top_k, num_slots, max_tokens, router_w, router_bias,
+                 host_bank, expert_to_slot, out_f32=False, max_refills=2, score_decay=1.0,
+                 visibility=MOE_VIS_DETERMINISTIC, stream=None):
+        import numpy as np
+
+        self.h = None
+        self.desc = LayerDesc(hidden, inter, num_experts, top_k, num_slots, max_tokens,
+                              MOE_OUT_F32 if out_f32 else MOE_OUT_BF16, max_refills, score_decay, visibility)
+        self._host_bank = host_bank  # keep the borrowed bank alive
+        self._e2s = np.ascontiguousarray(np.asarray(expert_to_slot, dtype=np.int32))
+        h = _P()
+        bias_ptr = None if router_bias is None else _P(router_bias.data_ptr())
+        check(lib().moe_layer_create(ctypes.byref(self.desc), _P(router_w.data_ptr()), bias_ptr,
+                                     _P(host_bank.data_ptr()), self._e2s.ctypes.data_as(_P), stream_ptr(stream),
+                                     ctypes.byref(h)))
+        self.h = h
+        self.res = RouteResult()
+
+    def route(self, x, M, stream=None):
+        check(lib().moe_route(self.h, _P(x.data_ptr()), M, stream_ptr(stream), ctypes.byref(self.res)))
+        return self.res
+
+    def forward_slots(self, x, out, M, stream=None):
+        check(lib().moe_forward_slots(self.h, _P(x.data_ptr()), _P(out.data_ptr()), M, stream_ptr(stream)))
+
+    def cache_update(self, stream=None):
+        n = ctypes.c_int32(0)
+        check(lib().moe_cache_update(self.h, stream_ptr(stream), ctypes.byref(n)))
+        return n.value
+
+    def set_bias(self, bias, stream=None):
+        check(lib().moe_layer_set_bias(self.h, None if bias is None else _P(bias.data_ptr()), stream_ptr(stream)))
+
+    def attach_staging(self, buf):
+        check(lib().moe_layer_attach_staging(self.h, None if buf is None else _P(buf.data_ptr()),
+                                             0 if buf is None else buf.numel() * buf.element_size()))
+
+    def stage_all(self, stream=None):
+        check(lib().moe_layer_stage_all(self.h, stream_ptr(stream)))
+
+    def get_map(self):
+        import numpy as np
+
+        out = np.empty(self.desc.num_experts, dtype=np.int32)
+        check(lib().moe_debug_get_map(self.h, out.ctypes.data_as(_P)))
+        return out
+
+    def slot_ptr(self, slot):
+        p = _P()
+        check(lib().moe_debug_slot_ptr(self.h, slot, ctypes.byref(p)))
+        return p.value
+
+    def inject_fault(self, fault):
+        check(lib().moe_debug_inject_fault(self.h, fault))
+
+    def stats(self):
+        import numpy as np
+
+        s = np.zeros(4, dtype=np.int64)
+        check(lib().moe_debug_stats(self.h, s.ctypes.data_as(_P)))
+        return s
+
+    def profile(self, enable):
+        check(lib().moe_debug_profile(self.h, 1 if enable else 0))
+
+    def profile_read(self):
+        import numpy as np
+
+        out = np.zeros(4, dtype=np.float64)
+        check(lib().moe_debug_profile_read(self.h, out.ctypes.data_as(_P)))
+        return out
+
+    def close(self):
+        if getattr(self, "h", None):
+            lib().moe_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def policy_step(score, last, e2s, s2e, hist, step, decay, R, in_flight=None):
+    """The library's slot-cache decision on numpy arrays (updated in place)."""
+    import numpy as np
+
+    E, S = e2s.shape[0], s2e.shape[0]
+    pe, ps, pv = (np.zeros(max(R, 1), dtype=np.int32) for _ in range(3))
+    fl = None if in_flight is None else np.ascontiguousarray(in_flight, dtype=np.uint8)
+    hist = np.ascontiguousarray(hist, dtype=np.int32)
+    n = lib().moe_policy_step(score.ctypes.data_as(_P), last.ctypes.data_as(_P), e2s.ctypes.data_as(_P),
+                              s2e.ctypes.data_as(_P), E, S, hist.ctypes.data_as(_P),
+                              int(step), float(decay), int(R), None if fl is None else fl.ctypes.data_as(_P),
+                              pe.ctypes.data_as(_P), ps.ctypes.data_as(_P), pv.ctypes.data_as(_P))
+    if n < 0:
+        raise MoeError(MOE_EINVAL, "moe_policy_step rejected its arguments")
+    return [(int(pe[i]), int(ps[i]), int(pv[i])) for i in range(n)]

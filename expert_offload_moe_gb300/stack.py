@@ -1,0 +1,111 @@
+"""A stack of independent MoE layers built from the seeded workloads, and the
+decode step over it (route + forward for every layer), optionally captured
+as one CUDA graph.
+
+Layers are independent instances with their own fresh N(0,1) input each step
+(chaining them without attention and norms would overflow); this is how the
+workloads are timed and checked.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import torch
+
+from . import moe, synth
+
+
+def bf16_tensor(bits: np.ndarray, device="cuda") -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    return t.to(device) if device != "cpu" else t
+
+
+def pinned_bank(seed: int, layer: int, E: int, H: int, I: int) -> torch.Tensor:
+    eb = synth.expert_bytes(H, I)
+    bank = torch.empty((E, eb), dtype=torch.uint8, pin_memory=True)
+    synth.fill_expert_records(bank.numpy(), seed, layer, H, I, first=0)
+    return bank
+
+
+def host_counts(res) -> np.ndarray:
+    """The page-locked mirror of (n_hot, n_cold, n_active, M) of a route result."""
+    return np.ctypeslib.as_array(ctypes.cast(res.h_counts, ctypes.POINTER(ctypes.c_int32)), (4,)).copy()
+
+
+class LayerInputs:
+    """Everything one layer of a workload needs (host copies kept for the oracle)."""
+
+    def __init__(self, w: synth.Workload, layer: int, seed: int = 0, e2s=None, bias_order=0):
+        self.w, self.layer, self.seed = w, layer, seed
+        H, I, E = w.hidden, w.inter, w.experts
+        self.Wr = synth.router_weights(seed, layer, E, H)
+        self.bias = synth.router_bias(seed, layer, E, w.bias_tau, bias_order)
+        self.e2s = synth.expert_to_slot_by_rank(seed, layer, E, w.slots) if e2s is None else np.asarray(e2s, np.int32)
+        self.bank = pinned_bank(seed, layer, E, H, I)
+
+    def make_layer(self, max_tokens=8, out_f32=False, **kw) -> moe.Layer:
+        w = self.w
+        return moe.Layer(w.hidden, w.inter, w.experts, w.top_k, w.slots, max_tokens,
+                         torch.from_numpy(self.Wr).cuda(), torch.from_numpy(self.bias).cuda(), self.bank,
+                         self.e2s, out_f32=out_f32, **kw)
+
+
+class DecodeStack:
+    """L layers of one workload with M-token decode steps over resident inputs."""
+
+    def __init__(self, w: synth.Workload, M: int = 1, n_layers: int | None = None, seed: int = 0,
+                 n_inputs: int = 1, out_f32: bool = False, max_tokens: int = 8):
+        self.w, self.M, self.seed = w, M, seed
+        self.L = w.layers if n_layers is None else n_layers
+        self.inputs = [LayerInputs(w, l, seed) for l in range(self.L)]
+        self.layers = [li.make_layer(max_tokens=max_tokens, out_f32=out_f32) for li in self.inputs]
+        H = w.hidden
+        # n_inputs steps of fresh activations per layer, resident in HBM: [n_inputs, L, M, H]
+        xs = np.stack([np.stack([synth.activations(seed, l, s, M, H) for l in range(self.L)])
+                       for s in range(n_inputs)])
+        self.x_host = xs
+        self.x_all = bf16_tensor(xs)
+        self.x_cur = torch.empty((self.L, M, H), dtype=torch.bfloat16, device="cuda")
+        dt = torch.float32 if out_f32 else torch.bfloat16
+        self.out = torch.empty((self.L, M, H), dtype=dt, device="cuda")
+        self.graph = None
+        self.graph_stream = None
+
+    def _body(self, stream):
+        for l, layer in enumerate(self.layers):
+            layer.route(self.x_cur[l], self.M, stream)
+            layer.forward_slots(self.x_cur[l], self.out[l], self.M, stream)
+
+    def load_inputs(self, i: int):
+        self.x_cur.copy_(self.x_all[i % self.x_all.shape[0]], non_blocking=True)
+
+    def step(self, i: int = 0):
+        """One decode step over every layer (eager launches on the current stream)."""
+        self.load_inputs(i)
+        self._body(torch.cuda.current_stream())
+
+    def capture(self):
+        """Captures the step body (all layers) as one CUDA graph."""
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for _ in range(2):
+                self._body(s)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            self._body(s)
+        torch.cuda.synchronize()
+        self.graph, self.graph_stream = g, s
+        return g
+
+    def replay(self, i: int = 0):
+        self.load_inputs(i)
+        self.graph.replay()
+
+    def close(self):
+        for l in self.layers:
+            l.close()
+        self.layers = []

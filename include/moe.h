@@ -1,0 +1,243 @@
+/*
+ * moe.h -- C ABI of the decode-time Mixture-of-Experts layer with GPU expert
+ * slots, for one GB300 GPU (sm_103a).
+ *
+ * What the layer computes, per call, for M tokens x[M, H]:
+ *   1. router: logits[t, e] = x[t, :] . Wr[e, :] + b[e]; the top_k largest
+ *      logits of each token (ties go to the lower expert id); weights =
+ *      softmax over the selected logits (onnxruntime PR #33976 "Key Changes":
+ *      router, then hot experts on the GPU; NInfer-Offload v0.4.0: routing on
+ *      the GPU across many thread blocks).
+ *   2. expert_to_slot indirection: a route to expert e is hot when
+ *      expert_to_slot[e] >= 0 (the slot holding e), cold otherwise
+ *      (onnxruntime PR #33976 "Slot-Compacted GPU Hot Experts +
+ *      expert_to_slot Indirection": slot < 0 is skipped on the GPU).
+ *   3. hot routes run the expert FFN straight from the slot's MXFP4 bytes:
+ *      y = Wd . (SiLU(Wg . x) * (Wu . x)) (tinyserve README "How it works" 2:
+ *      fused dequantise-and-multiply, gate, up, down; xinfer docs
+ *      "How it works": GEMMs over [num_slots, N, K] slot tensors).
+ *   4. out[t, :] = sum of w * y over t's hot routes; cold routes are returned
+ *      as (token, expert, weight) triples for the caller to handle.
+ *   5. the slot cache refills slots from a page-locked host bank with async
+ *      copies, at most max_refills_per_step experts per call, replacing the
+ *      least used (NInfer-Offload v0.4.0 "expert cache"; tinyserve README
+ *      "How it works" 3: frequency-recency eviction; xinfer docs "Supported":
+ *      host RAM holds every expert, pinned).
+ *
+ * Formats (MXFP4 as defined by the OCP Microscaling Formats v1.0 spec; the
+ * pages name MXFP4 but do not define it):
+ *   x        bf16 [M, H], row-major, device memory, 16-byte aligned
+ *   out      bf16 or fp32 [M, H] (moe_layer_desc.out_dtype), row-major, device
+ *   Wr       fp32 [E, H], row-major;  b: fp32 [E] (may be NULL = zeros)
+ *   expert record, expert_bytes = 3 * I * H * 17 / 32 bytes:
+ *     [Wg codes I x H/2][Wg scales I x H/32][Wu codes I x H/2][Wu scales I x H/32]
+ *     [Wd codes H x I/2][Wd scales H x I/32]
+ *   codes: E2M1, row-major, byte c of a row holds column 2c in its low nibble
+ *   and column 2c+1 in its high nibble; scales: E8M0 (2^(s-127)), byte b of a
+ *   row covers columns [32b, 32b+32); 255 (NaN) is not allowed.
+ *   The host bank is [E][expert_bytes], indexed by expert id; a slot holds a
+ *   byte-identical copy of one record.
+ *
+ * Requirements: H and I multiples of 64; 1 <= top_k <= 16; top_k <= E <= 512;
+ * top_k <= num_slots <= E; 1 <= max_tokens <= 4096.  Decode calls use
+ * M <= 8 tokens; a call with M > 8 runs the prefill path (every expert of the
+ * layer staged on the GPU, see moe_layer_attach_staging).
+ *
+ * Threading: a layer is not thread-safe; calls on one layer must be
+ * serialised by the caller.  Every call returns a status code; on failure
+ * moe_last_error() gives a message (thread-local, valid until the next call
+ * on the same thread).  No call throws.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum moe_status {
+    MOE_OK = 0,
+    MOE_EINVAL = 1,   /* bad argument (sizes, NULL, non-pinned host bank, ...) */
+    MOE_ENOMEM = 2,   /* device or pinned host allocation failed */
+    MOE_ECUDA = 3,    /* a CUDA runtime call failed (message says which) */
+    MOE_ETIMEOUT = 4, /* a bounded device wait gave up */
+    MOE_ESTATE = 5    /* call order violated (e.g. forward without route) */
+};
+
+enum { MOE_OUT_BF16 = 0, MOE_OUT_F32 = 1 };
+
+/* Slot-cache visibility of a refill:
+ *  DETERMINISTIC: a refill chosen by moe_cache_update after step t is mapped
+ *                 before any work enqueued after that call (step t+1 sees it);
+ *                 the compute stream waits for the copy.
+ *  POLLED:        the victim is unmapped at once, the copy runs on a side
+ *                 stream, and the new expert is mapped by a later
+ *                 moe_cache_update once its copy has landed; decode never
+ *                 waits for a copy, so which routes are hot can depend on
+ *                 timing (the NInfer-Offload v0.4.0 behaviour). */
+enum { MOE_VIS_DETERMINISTIC = 0, MOE_VIS_POLLED = 1 };
+
+typedef struct moe_layer moe_layer;
+
+typedef struct {
+    int32_t hidden;               /* H */
+    int32_t inter;                /* I, expert intermediate size */
+    int32_t num_experts;          /* E */
+    int32_t top_k;                /* k */
+    int32_t num_slots;            /* S, GPU slots of this layer */
+    int32_t max_tokens;           /* largest M of any call (sizes the scratch) */
+    int32_t out_dtype;            /* MOE_OUT_BF16 or MOE_OUT_F32 */
+    int32_t max_refills_per_step; /* R, refills per moe_cache_update (NInfer: 2) */
+    float score_decay;            /* 1.0 = LFU; in (0,1) = decayed frequency (LFRU) */
+    int32_t visibility;           /* MOE_VIS_DETERMINISTIC or MOE_VIS_POLLED */
+} moe_layer_desc;
+
+/* Result of moe_route.  Device arrays are owned by the layer and stay valid
+ * until the next moe_route on the same layer; host arrays are a page-locked
+ * mirror, valid once `done` (a cudaEvent_t) has completed. */
+typedef struct {
+    int32_t M;
+    /* device */
+    const int32_t *topk_ids;   /* [M, k] experts of each token, largest logit first */
+    const float *topk_w;       /* [M, k] renormalised weights, same order */
+    const int32_t *hot_expert; /* [<= M*k] hot routes ordered by (expert, token) */
+    const int32_t *hot_token;
+    const float *hot_w;
+    const int32_t *act_expert; /* [<= min(S, M*k)] experts with hot routes, ascending */
+    const int32_t *act_slot;   /* their slots */
+    const int32_t *act_off;    /* first index of each in the hot arrays */
+    const int32_t *act_cnt;    /* number of hot routes of each */
+    const int32_t *cold_token; /* [<= M*k] cold routes ordered by (token, expert) */
+    const int32_t *cold_expert;
+    const float *cold_w;
+    const int32_t *hist;       /* [E] routes (hot and cold) per expert */
+    const int32_t *counts;     /* [4] n_hot, n_cold, n_active, M */
+    /* page-locked host mirror of counts, cold triples and hist */
+    const int32_t *h_counts;
+    const int32_t *h_cold_token;
+    const int32_t *h_cold_expert;
+    const float *h_cold_w;
+    const int32_t *h_hist;
+    void *done; /* cudaEvent_t recorded after the mirror copies */
+} moe_route_result;
+
+/* Creates a layer on the current CUDA device.
+ *  router_w_dev    fp32 [E, H] device, copied (the caller may free it after)
+ *  router_bias_dev fp32 [E] device or NULL, copied
+ *  host_bank       [E, expert_bytes] page-locked host memory (cudaHostAlloc or
+ *                  cudaHostRegister), borrowed: it must outlive the layer.
+ *                  Pageable memory is rejected with MOE_EINVAL.
+ *  expert_to_slot_host int32 [E]: -1 = cold, else a slot in [0, S); no slot
+ *                  twice.  The named experts are copied into their slots
+ *                  before this call returns (on `stream`, then synchronised).
+ *  stream          cudaStream_t for the initial copies (NULL = default)
+ * Allocates the slot bank (S * expert_bytes), router copy, map and scratch.
+ * Errors: MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA; *out is NULL on failure. */
+int moe_layer_create(const moe_layer_desc *desc, const float *router_w_dev, const float *router_bias_dev,
+                     const uint8_t *host_bank, const int32_t *expert_to_slot_host, void *stream,
+                     moe_layer **out);
+
+/* Routes M tokens: router GEMV, top-k + softmax, slot lookup and compaction,
+ * all on `stream` (asynchronous, no host synchronisation, fixed launch
+ * shapes: capturable in a CUDA graph).  The mirror copies run on an internal
+ * stream forked from `stream`; moe_forward_slots joins it back.
+ *  x_dev  bf16 [M, H] device;  1 <= M <= max_tokens
+ *  res    filled with the pointers above (may be NULL)
+ * With M > 8 (prefill) every expert is treated as resident in the staging
+ * bank, so every route is hot and the cold list is empty.
+ * Errors: MOE_EINVAL, MOE_ECUDA. */
+int moe_route(moe_layer *layer, const void *x_dev, int32_t M, void *stream, moe_route_result *res);
+
+/* Runs the hot routes of the last moe_route and combines them:
+ *   out[t, :] = sum over t's hot routes, in ascending expert order, of w * y
+ * where y is the expert FFN read from the expert's slot (fp32 accumulation);
+ * tokens without hot routes get zeros.  x_dev and M must be those of the last
+ * moe_route (MOE_ESTATE otherwise).  M <= 8: decode kernels over the slot
+ * bank.  M > 8: prefill on the staging bank (MOE_ESTATE if none is attached
+ * or it was not staged with moe_layer_stage_all).
+ *  out_dev  [M, H] out_dtype, device, caller-owned
+ * Asynchronous, capturable.  Errors: MOE_EINVAL, MOE_ESTATE, MOE_ECUDA. */
+int moe_forward_slots(moe_layer *layer, const void *x_dev, void *out_dev, int32_t M, void *stream);
+
+/* Host-side slot-cache step after a moe_route (waits for its `done` event).
+ * Scores every expert (score = decay * score + routes this step), picks at
+ * most R (candidate, victim) pairs, copies each candidate from the host bank
+ * into the victim's slot with cudaMemcpyAsync on the layer's side stream
+ * (after the work already on `stream`, so a slot is never overwritten while
+ * read), and updates expert_to_slot on `stream` per the visibility mode.
+ * Does nothing when every expert is resident (S == E).
+ *  n_refills_out  copies issued by this call (may be NULL)
+ * Not capturable (host decisions).  Errors: MOE_ESTATE, MOE_ECUDA. */
+int moe_cache_update(moe_layer *layer, void *stream, int32_t *n_refills_out);
+
+/* Waits for the layer's copies, frees everything the layer owns.  NULL is OK. */
+int moe_destroy(moe_layer *layer);
+
+/* Thread-local message of the last failed call on this thread ("" if none). */
+const char *moe_last_error(void);
+
+/* Replaces the router bias with bias_dev (fp32 [E], device; NULL = zeros),
+ * copied on `stream` in stream order (capturable).  Used when the bias moves
+ * between steps.  Errors: MOE_EINVAL, MOE_ECUDA. */
+int moe_layer_set_bias(moe_layer *layer, const float *bias_dev, void *stream);
+
+/* ------------------------------------------------------------ prefill */
+
+/* Attaches a caller-owned device buffer of at least E * expert_bytes bytes
+ * used to stage all experts of the layer for prefill (xinfer docs "How it
+ * works", Prefill: the whole expert layer is copied to a staging buffer and
+ * the unmodified GEMM runs on it).  Several layers may share one buffer if
+ * their calls are serialised on one stream.  NULL detaches.
+ * Errors: MOE_EINVAL. */
+int moe_layer_attach_staging(moe_layer *layer, void *staging_dev, size_t bytes);
+
+/* Copies all E experts of the layer from the host bank into the attached
+ * staging buffer on `stream` (asynchronous).  Errors: MOE_ESTATE, MOE_ECUDA. */
+int moe_layer_stage_all(moe_layer *layer, void *stream);
+
+/* ------------------------------------------------------- introspection */
+
+/* expert_to_slot as last enqueued to the device (what the next moe_route on
+ * the same stream sees): int32 [E]. */
+int moe_debug_get_map(const moe_layer *layer, int32_t *expert_to_slot_host);
+
+/* Device address of slot s (expert_bytes bytes), for byte comparisons. */
+int moe_debug_slot_ptr(const moe_layer *layer, int32_t slot, const void **ptr);
+
+/* Fault injection on the host: MOE_FAULT_COPY makes the next refill fail
+ * before any copy is issued (the call returns MOE_ECUDA and leaves the map
+ * unchanged); MOE_FAULT_NONE clears it. */
+enum { MOE_FAULT_NONE = 0, MOE_FAULT_COPY = 1 };
+int moe_debug_inject_fault(moe_layer *layer, int32_t fault);
+
+/* Cumulative counters of the layer: [0] refills issued, [1] refill bytes,
+ * [2] routes seen, [3] hot routes seen (updated by moe_cache_update). */
+int moe_debug_stats(const moe_layer *layer, int64_t stats[4]);
+
+/* Kernel timing for benchmarks: with enable != 0, later route and forward
+ * calls record timing events around the router, gate/up and down kernels on
+ * the caller's stream (synchronises the device; resets the sums). */
+int moe_debug_profile(moe_layer *layer, int32_t enable);
+
+/* Sums of the timed kernels since moe_debug_profile: out[0] route ms,
+ * out[1] gate/up ms, out[2] down ms, out[3] forward calls (waits for the events). */
+int moe_debug_profile_read(moe_layer *layer, double out[4]);
+
+/* The slot-cache decision on host arrays, as moe_cache_update runs it
+ * (exported so that the policy can be checked without a GPU).
+ *  score[E], last[E], e2s[E], s2e[S] are updated in place; in_flight[E]
+ *  (may be NULL) marks experts whose copy has not landed; hist[E] are this
+ *  step's routes per expert.  Writes up to R (expert, slot, victim) triples
+ *  and returns their number, or -1 on bad arguments. */
+int moe_policy_step(double *score, int64_t *last, int32_t *e2s, int32_t *s2e, int32_t E, int32_t S,
+                    const int32_t *hist, int64_t step, double decay, int32_t R, const uint8_t *in_flight,
+                    int32_t *pair_expert, int32_t *pair_slot, int32_t *pair_victim);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */
