@@ -24,7 +24,6 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kM = kDecodeMaxTokens;
 
 __device__ __forceinline__ float e8m0_to_f32(uint32_t e) {
     return e ? __uint_as_float(e << 23) : __uint_as_float(0x00400000u);
@@ -54,6 +53,7 @@ __device__ __forceinline__ uint4 ld_stream(const void *p) {
 
 __device__ __forceinline__ float silu(float g) { return g / (1.f + expf(-g)); }
 
+template <int kM>
 __global__ void __launch_bounds__(kThreads) gateup_kernel(DecodeParams p, int M) {
     extern __shared__ float sx[];  // [M][H] activations as fp32
     __shared__ float lut[16];
@@ -122,6 +122,7 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(DecodeParams p, int M)
     }
 }
 
+template <int kM>
 __global__ void __launch_bounds__(kThreads) down_kernel(DecodeParams p, int M) {
     __shared__ float lut[16];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -193,18 +194,30 @@ __global__ void __launch_bounds__(kThreads) down_kernel(DecodeParams p, int M) {
 
 }  // namespace
 
-void launch_gateup(const DecodeParams &p, int M, cudaStream_t s, int num_sms) {
-    const size_t smem = (size_t)M * p.geo.H * sizeof(float);
+// The token loops are unrolled for kM tokens per slot, the smallest of
+// 1, 2, 4, 8 that covers M (a slot never serves more tokens than M).
+template <int kM>
+void gateup_launch(const DecodeParams &p, int M, cudaStream_t s, int num_sms) {
     static bool configured = false;
     if (!configured) {
-        cudaFuncSetAttribute(gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmemLimit);
+        cudaFuncSetAttribute(gateup_kernel<kM>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmemLimit);
         configured = true;
     }
-    gateup_kernel<<<num_sms * 4, kThreads, smem, s>>>(p, M);
+    gateup_kernel<kM><<<num_sms * 4, kThreads, (size_t)M * p.geo.H * sizeof(float), s>>>(p, M);
+}
+
+void launch_gateup(const DecodeParams &p, int M, cudaStream_t s, int num_sms) {
+    if (M <= 1) gateup_launch<1>(p, M, s, num_sms);
+    else if (M <= 2) gateup_launch<2>(p, M, s, num_sms);
+    else if (M <= 4) gateup_launch<4>(p, M, s, num_sms);
+    else gateup_launch<8>(p, M, s, num_sms);
 }
 
 void launch_down(const DecodeParams &p, int M, cudaStream_t s, int num_sms) {
-    down_kernel<<<num_sms * 4, kThreads, 0, s>>>(p, M);
+    if (M <= 1) down_kernel<1><<<num_sms * 4, kThreads, 0, s>>>(p, M);
+    else if (M <= 2) down_kernel<2><<<num_sms * 4, kThreads, 0, s>>>(p, M);
+    else if (M <= 4) down_kernel<4><<<num_sms * 4, kThreads, 0, s>>>(p, M);
+    else down_kernel<8><<<num_sms * 4, kThreads, 0, s>>>(p, M);
 }
 
 }  // namespace moe

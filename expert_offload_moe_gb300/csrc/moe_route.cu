@@ -24,6 +24,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kSmemRoutes = 1024;
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -134,6 +135,11 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
     __shared__ int s_hot_off[kMaxExperts];
     __shared__ int s_act_pos[kMaxExperts];
     __shared__ int s_cold[kMaxTokens];
+    __shared__ int s_ids[kSmemRoutes];  // copy of the routes for the compaction when they fit
+    __shared__ float s_w[kSmemRoutes];
+    const bool routes_in_smem = M * k <= kSmemRoutes;
+    int *ids = routes_in_smem ? s_ids : p.b.topk_ids;
+    float *wts = routes_in_smem ? s_w : p.b.topk_w;
 
     for (int e = threadIdx.x; e < E; e += kThreads) s_hist[e] = 0;
     __syncthreads();
@@ -187,8 +193,13 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
 #pragma unroll
         for (int j = 0; j < kMaxTopK; ++j) {
             if (j < k && lane == j) {
+                const float wj = expf(sel_l[j] - lmax) / den;
                 p.b.topk_ids[(size_t)t * k + j] = sel_id[j];
-                p.b.topk_w[(size_t)t * k + j] = expf(sel_l[j] - lmax) / den;
+                p.b.topk_w[(size_t)t * k + j] = wj;
+                if (routes_in_smem) {
+                    s_ids[t * k + j] = sel_id[j];
+                    s_w[t * k + j] = wj;
+                }
                 atomicAdd(&s_hist[sel_id[j]], 1);
             }
         }
@@ -218,10 +229,10 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
         p.b.act_cnt[a] = s_hist[e];
         for (int t = 0; t < M; ++t)
             for (int j = 0; j < k; ++j)
-                if (p.b.topk_ids[(size_t)t * k + j] == e) {
+                if (ids[t * k + j] == e) {
                     p.b.hot_expert[pos] = e;
                     p.b.hot_token[pos] = t;
-                    p.b.hot_w[pos] = p.b.topk_w[(size_t)t * k + j];
+                    p.b.hot_w[pos] = wts[t * k + j];
                     ++pos;
                 }
     }
@@ -230,7 +241,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
     for (int t = threadIdx.x; t < M; t += kThreads) {
         int n = 0;
         if (!p.all_hot)
-            for (int j = 0; j < k; ++j) n += p.e2s[p.b.topk_ids[(size_t)t * k + j]] < 0;
+            for (int j = 0; j < k; ++j) n += p.e2s[ids[t * k + j]] < 0;
         s_cold[t] = n;
     }
     __syncthreads();
@@ -241,9 +252,9 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
             float cw[kMaxTopK];
             int n = 0;
             for (int j = 0; j < k; ++j) {
-                const int e = p.b.topk_ids[(size_t)t * k + j];
+                const int e = ids[t * k + j];
                 if (p.e2s[e] >= 0) continue;
-                const float wt = p.b.topk_w[(size_t)t * k + j];
+                const float wt = wts[t * k + j];
                 int q = n++;  // insertion by expert id
                 while (q > 0 && ce[q - 1] > e) {
                     ce[q] = ce[q - 1];

@@ -14,7 +14,7 @@ class _DevArray:
     """Exposes a raw device pointer to torch through __cuda_array_interface__."""
 
     def __init__(self, ptr, n, typestr):
-        self.__cuda_array_interface__ = {"shape": (n,), "typestr": typestr, "data": (int(ptr), True),
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": typestr, "data": (int(ptr), False),
                                          "version": 3, "strides": None}
 
 
