@@ -60,7 +60,12 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(DecodeParams p, int M)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int H = p.geo.H, I = p.geo.I, nb = H / 32;
     fill_e2m1_lut(lut);
-    for (int i = threadIdx.x; i < M * H; i += kThreads) sx[i] = __uint_as_float((uint32_t)p.x[i] << 16);
+    // block-transposed: sx[t][j][b] = x[t][32 b + j], so that lane b of a warp reading element j of its
+    // block hits consecutive words (no bank conflicts)
+    for (int i = threadIdx.x; i < M * H; i += kThreads) {
+        const int t = i / H, c = i - t * H;
+        sx[t * H + (c & 31) * nb + (c >> 5)] = __uint_as_float((uint32_t)p.x[i] << 16);
+    }
     __syncthreads();
 
     const int n_act = p.counts[2];
@@ -95,11 +100,10 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(DecodeParams p, int M)
                 for (int n = 0; n < 8; ++n) {
                     const float vg = lut[(qg[q] >> (4 * n)) & 15u];
                     const float vu = lut[(qu[q] >> (4 * n)) & 15u];
-                    const int col = b * 32 + q * 8 + n;
 #pragma unroll
                     for (int t = 0; t < kM; ++t) {
                         if (t < cnt) {
-                            const float xv = sx[tok[t] * H + col];
+                            const float xv = sx[tok[t] * H + (q * 8 + n) * nb + b];
                             pg[t] = fmaf(vg, xv, pg[t]);
                             pu[t] = fmaf(vu, xv, pu[t]);
                         }
@@ -116,7 +120,8 @@ __global__ void __launch_bounds__(kThreads) gateup_kernel(DecodeParams p, int M)
         for (int t = 0; t < kM; ++t) {
             if (t < cnt) {
                 const float gt = warp_sum(g[t]), ut = warp_sum(u[t]);
-                if (lane == 0) p.h[(size_t)(off + t) * I + i] = silu(gt) * ut;
+                // h is stored block-transposed like x: h[route][i % 32][i / 32]
+                if (lane == 0) p.h[(size_t)(off + t) * I + (i & 31) * (I / 32) + (i >> 5)] = silu(gt) * ut;
             }
         }
     }
@@ -153,13 +158,12 @@ __global__ void __launch_bounds__(kThreads) down_kernel(DecodeParams p, int M) {
 #pragma unroll
                 for (int t = 0; t < kM; ++t) {
                     if (t < cnt) {
-                        const float4 *hp = reinterpret_cast<const float4 *>(p.h + (size_t)(off + t) * I + b * 32);
+                        const float *hp = p.h + (size_t)(off + t) * I + b;  // block-transposed h
 #pragma unroll
                         for (int qq = 0; qq < 4; ++qq) {
-                            const float4 h0 = hp[2 * qq], h1 = hp[2 * qq + 1];
-                            const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
 #pragma unroll
-                            for (int n = 0; n < 8; ++n) py[t] = fmaf(lut[(q[qq] >> (4 * n)) & 15u], hv[n], py[t]);
+                            for (int n = 0; n < 8; ++n)
+                                py[t] = fmaf(lut[(q[qq] >> (4 * n)) & 15u], hp[(qq * 8 + n) * nb], py[t]);
                         }
                     }
                 }

@@ -6,6 +6,9 @@ import ctypes
 import numpy as np
 
 NEAR_TIE = 1e-4  # k-th vs (k+1)-th logit gap below which a token's routing is not compared exactly
+# fp32 logits summed in another order differ by ~1e-6..1e-5 (far inside NEAR_TIE); the softmax carries
+# that into the weights as a relative difference of the same size
+W_RTOL, W_ATOL = 1e-5, 1e-8
 REL_TOL = 2e-3
 RHO = 1e-2  # per-token floor: RHO * RMS of the token's oracle row
 
@@ -95,7 +98,7 @@ def compare_routing(g, o, logits, k, e2s):
         gw = dict(zip(g["ids"][t].tolist(), g["w"][t].tolist()))
         ow = dict(zip(o["ids"][t].tolist(), o["w"][t].tolist()))
         for e in ow:
-            assert abs(gw[e] - ow[e]) <= 2e-6 * max(1.0, abs(ow[e])), (t, e, gw[e], ow[e])
+            assert abs(gw[e] - ow[e]) <= W_ATOL + W_RTOL * abs(ow[e]), (t, e, gw[e], ow[e])
 
     def keep(tokens):
         return np.array([t not in excluded for t in tokens], dtype=bool)
@@ -108,11 +111,11 @@ def compare_routing(g, o, logits, k, e2s):
     kg, ko = keep(g["hot_token"]), keep(o["hot_token"])
     assert np.array_equal(g["hot_expert"][kg], o["hot_expert"][ko])
     assert np.array_equal(g["hot_token"][kg], o["hot_token"][ko])
-    assert np.allclose(g["hot_w"][kg], o["hot_w"][ko], rtol=2e-6, atol=1e-7)
+    assert np.allclose(g["hot_w"][kg], o["hot_w"][ko], rtol=W_RTOL, atol=W_ATOL)
     kg, ko = keep(g["cold_token"]), keep(o["cold_token"])
     assert np.array_equal(g["cold_token"][kg], o["cold_token"][ko])
     assert np.array_equal(g["cold_expert"][kg], o["cold_expert"][ko])
-    assert np.allclose(g["cold_w"][kg], o["cold_w"][ko], rtol=2e-6, atol=1e-7)
+    assert np.allclose(g["cold_w"][kg], o["cold_w"][ko], rtol=W_RTOL, atol=W_ATOL)
     assert all(e2s[e] < 0 for e in g["cold_expert"]) and all(e2s[e] >= 0 for e in g["hot_expert"])
     return excluded
 

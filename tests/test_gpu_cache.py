@@ -32,9 +32,15 @@ def slots_match_bank(lay, li, e2s):
             assert np.array_equal(got, li.bank.numpy()[e]), (e, s)
 
 
+def least_popular_placement(seed, E, S):
+    """Start from the S least popular experts so that routing misses and refills happen."""
+    rank = synth.popularity_rank(seed, 0, E)
+    return np.where(rank >= E - S, rank - (E - S), -1).astype(np.int32)
+
+
 def drive(visibility, decay, steps, M, R=2, seed=0):
     w = SMALL
-    li = stack.LayerInputs(w, 0, seed=seed)
+    li = stack.LayerInputs(w, 0, seed=seed, e2s=least_popular_placement(seed, w.experts, w.slots))
     lay = li.make_layer(max_tokens=8, out_f32=True, max_refills=R, score_decay=decay, visibility=visibility)
     replay = oracle.CacheReplay(li.e2s, w.slots, decay=decay, R=R)
     refills = 0
@@ -91,7 +97,7 @@ def test_polled_refills_keep_map_consistent():
 
 def test_injected_copy_fault_leaves_map_unchanged():
     w = SMALL
-    li = stack.LayerInputs(w, 0)
+    li = stack.LayerInputs(w, 0, e2s=least_popular_placement(0, w.experts, w.slots))
     lay = li.make_layer(max_tokens=8, out_f32=True)
     out = torch.empty((1, w.hidden), dtype=torch.float32, device="cuda")
     hit = False
