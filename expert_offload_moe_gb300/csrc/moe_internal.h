@@ -85,4 +85,7 @@ void launch_gateup(const DecodeParams &p, int M, cudaStream_t s, int num_sms);
 void launch_down(const DecodeParams &p, int M, cudaStream_t s, int num_sms);
 void launch_map_update(int32_t *e2s, int n, const int32_t *experts, const int32_t *slots, cudaStream_t s);
 
+// Sets the thread-local message returned by moe_last_error().
+void set_last_error(const char *msg);
+
 }  // namespace moe

@@ -147,6 +147,8 @@ cudaError_t prof_mark(moe_layer *L, int which, cudaStream_t s) {
 
 }  // namespace
 
+void moe::set_last_error(const char *msg) { g_err = msg ? msg : ""; }
+
 extern "C" {
 
 const char *moe_last_error(void) { return g_err.c_str(); }

@@ -21,7 +21,7 @@ EXPORTED = [
     "moe_layer_create", "moe_route", "moe_forward_slots", "moe_cache_update", "moe_destroy", "moe_last_error",
     "moe_layer_set_bias", "moe_layer_attach_staging", "moe_layer_stage_all", "moe_debug_get_map",
     "moe_debug_slot_ptr", "moe_debug_inject_fault", "moe_debug_stats", "moe_debug_profile",
-    "moe_debug_profile_read", "moe_policy_step",
+    "moe_debug_profile_read", "moe_policy_step", "moe_route_noalloc",
 ]
 
 
@@ -39,6 +39,14 @@ class LayerDesc(ctypes.Structure):
 
 
 _P = ctypes.c_void_p
+
+
+class RouteBuffers(ctypes.Structure):
+    """Caller-owned device buffers for moe_route_noalloc (device pointers)."""
+
+    _fields_ = [(n, _P) for n in (
+        "topk_ids", "topk_w", "hot_expert", "hot_token", "hot_w", "act_expert", "act_slot", "act_off",
+        "act_cnt", "cold_token", "cold_expert", "cold_w", "hist", "counts")]
 
 
 class RouteResult(ctypes.Structure):
@@ -74,6 +82,7 @@ def lib():
         L.moe_debug_stats.argtypes = [p, p]
         L.moe_debug_profile.argtypes = [p, i32]
         L.moe_debug_profile_read.argtypes = [p, p]
+        L.moe_route_noalloc.argtypes = [p, i32, i32, p, p, i32, i32, p, ctypes.POINTER(RouteBuffers), p]
         L.moe_policy_step.argtypes = [p, p, p, p, i32, i32, p, ctypes.c_int64, ctypes.c_double, i32, p, p, p, p]
         for name in EXPORTED:
             if name != "moe_last_error":
@@ -186,6 +195,15 @@ class Layer:
             self.close()
         except Exception:
             pass
+
+
+def route_noalloc(x, M, router_w, router_bias, E, top_k, expert_to_slot_dev, bufs: dict, stream=None):
+    """moe_route_noalloc: routes into the caller's device tensors in ``bufs`` (keys as RouteBuffers)."""
+    rb = RouteBuffers(*[_P(bufs[n].data_ptr()) for n, _ in RouteBuffers._fields_])
+    H = x.shape[-1]
+    check(lib().moe_route_noalloc(_P(x.data_ptr()), M, H, _P(router_w.data_ptr()),
+                                  None if router_bias is None else _P(router_bias.data_ptr()), E, top_k,
+                                  _P(expert_to_slot_dev.data_ptr()), ctypes.byref(rb), stream_ptr(stream)))
 
 
 def policy_step(score, last, e2s, s2e, hist, step, decay, R, in_flight=None):

@@ -184,6 +184,54 @@ const char *moe_last_error(void);
  * between steps.  Errors: MOE_EINVAL, MOE_ECUDA. */
 int moe_layer_set_bias(moe_layer *layer, const float *bias_dev, void *stream);
 
+/* ------------------------------------------------ routing without allocation */
+
+/* Caller-owned device buffers that receive a routing result; sizes as in
+ * moe_route_result: [M*k] for the route lists, [E] for hist, [4] for counts. */
+typedef struct {
+    int32_t *topk_ids;
+    float *topk_w;
+    int32_t *hot_expert;
+    int32_t *hot_token;
+    float *hot_w;
+    int32_t *act_expert;
+    int32_t *act_slot;
+    int32_t *act_off;
+    int32_t *act_cnt;
+    int32_t *cold_token;
+    int32_t *cold_expert;
+    float *cold_w;
+    int32_t *hist;
+    int32_t *counts;
+} moe_route_buffers;
+
+/* The pages have no counterpart to this call.  It routes M tokens exactly as
+ * moe_route does (router GEMV, top-k + softmax, split and compaction by
+ * expert_to_slot), but it never allocates: no cudaMalloc, no cudaFree, no
+ * host allocation, no layer object.  It is meant for callers that cannot
+ * allocate device memory where they route -- e.g. a serving process whose
+ * device memory is all reserved up front by its own pool allocator, or a
+ * latency-critical loop that must not take the implicit synchronisation of
+ * cudaMalloc/cudaFree.
+ *  x_dev, M, H          bf16 [M, H] device, 16-byte aligned; H % 64 == 0
+ *  router_w_dev         fp32 [E, H] device, 16-byte aligned (read in place)
+ *  router_bias_dev      fp32 [E] device, or NULL (zeros)
+ *  E, top_k             1 <= top_k <= 16, top_k <= E <= 512
+ *  expert_to_slot_dev   int32 [E] device; < 0 = cold (no prefill mode here)
+ *  out                  caller-owned device buffers (all required)
+ * Scratch: a built-in device array of 1 MiB (held by every GPU that loads the
+ * library until exit) holds the partial logits, so ceil(H/256) * M * E * 4
+ * must not exceed 1 MiB - 256 bytes; larger sizes return MOE_EINVAL with a
+ * message saying so.  The first call on each device looks up the array's
+ * device address (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  All calls share the array: calls that overlap on the GPU
+ * (unordered streams) race and give wrong results; calls ordered on one
+ * stream are fine (each clears the arrival counter it needs).
+ * Errors: MOE_EINVAL, MOE_ECUDA (message in moe_last_error()). */
+int moe_route_noalloc(const void *x_dev, int32_t M, int32_t H, const float *router_w_dev,
+                      const float *router_bias_dev, int32_t E, int32_t top_k, const int32_t *expert_to_slot_dev,
+                      const moe_route_buffers *out, void *stream);
+
 /* ------------------------------------------------------------ prefill */
 
 /* Attaches a caller-owned device buffer of at least E * expert_bytes bytes
