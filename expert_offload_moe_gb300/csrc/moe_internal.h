@@ -1,6 +1,7 @@
 // Internal declarations shared by the layer's host code and its kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -79,6 +80,35 @@ struct DecodeParams {
     void *out;              // [M, H]
     int out_f32;
 };
+
+// Tensor-core decode path (moe_decode_tc.cu).
+struct TcLaunch {
+    const uint8_t *bank;
+    ExpertGeometry geo;
+    int M, n_act_max, ks_gateup, ks_down;
+    const int32_t *counts, *act_slot, *act_off, *act_cnt, *hot_token;
+    const float *hot_w;
+    const uint8_t *xs;  // x-term scales [16][SPH]
+    int SPH;
+    uint8_t *hq, *hs;   // w*h terms [n_act_max][32][Ipad], scales [n_act_max][32][SPI]
+    int Ipad, SPI;
+    float *part, *part_down;
+    unsigned *tile_ctr_gateup, *tile_ctr_down;
+    int *err;
+    void *out;
+    int out_f32;
+    const CUtensorMap *mapG, *mapU, *mapX, *mapD, *mapH;
+};
+
+constexpr int kTcMaxSteps = 16;     // k-steps of 128 per CTA (tensor memory budget)
+constexpr int kTcXRows = 16;        // rows of the x-term operand
+constexpr int kTcHRows = 32;        // rows of the w*h-term operand
+constexpr int kTcPartGateup = 2 * 2 * kDecodeMaxTokens * 128;  // floats per gate/up split partial
+constexpr int kTcPartDown = kDecodeMaxTokens * 3 * 128;         // floats per down split partial
+
+void launch_quantize_x(const uint16_t *x, int M, int H, uint8_t *xq, int Hpad, uint8_t *xs, int SP, cudaStream_t s);
+void launch_gateup_tc(const TcLaunch &L, cudaStream_t s);
+void launch_down_tc(const TcLaunch &L, cudaStream_t s);
 
 void launch_route(const RouteParams &p, cudaStream_t s, int num_sms);
 void launch_gateup(const DecodeParams &p, int M, cudaStream_t s, int num_sms);

@@ -7,6 +7,8 @@
 // page-locked host bank (onnxruntime PR #33976: pinned staging with
 // CUDA_EVENT_DISABLE_TIMING events for overlap; NInfer-Offload v0.4.0: refills
 // run in the background without stalling decode).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cstdarg>
@@ -90,6 +92,17 @@ struct moe_layer {
     int fault = MOE_FAULT_NONE;
     int64_t stats[4] = {0, 0, 0, 0};
 
+    // tensor-core decode path: operand buffers, split-K scratch, tensor maps
+    bool tc = false;
+    int n_act_cap = 0;  // most active experts a decode call can have: min(S, 8 k)
+    int Hpad = 0, Ipad = 0, SPH = 0, SPI = 0;
+    uint8_t *xq = nullptr, *xs = nullptr, *hq = nullptr, *hs = nullptr;
+    float *part = nullptr, *part_down = nullptr;
+    unsigned *ctr_gateup = nullptr, *ctr_down = nullptr;
+    int *err = nullptr;
+    void *tc_block = nullptr;
+    CUtensorMap mapG{}, mapU{}, mapD{}, mapX{}, mapH{};
+
     // optional per-kernel timing: event pairs around route, gate/up and down launches
     bool prof = false;
     std::vector<cudaEvent_t> prof_ev[3];
@@ -110,6 +123,7 @@ void release(moe_layer *L) {
     cudaFree(L->e2s_dev);
     cudaFree(L->dev_block);
     cudaFree(L->h);
+    cudaFree(L->tc_block);
     if (L->pinned_block) cudaFreeHost(L->pinned_block);
     for (auto e : {L->ev_fork, L->ev_route, L->ev_fence})
         if (e) cudaEventDestroy(e);
@@ -143,6 +157,125 @@ cudaError_t prof_mark(moe_layer *L, int which, cudaStream_t s) {
         v.push_back(e);
     }
     return cudaEventRecord(v[n++], s);
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link against libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 3-D tiled map with a 128-byte swizzle: dims {d0 (elements), d1, d2}, byte strides {s1, s2}, box {b0, b1, 1}.
+int encode_map(CUtensorMap *m, CUtensorMapDataType type, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+               uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, const char *what) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return fail(MOE_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {s1, s2};
+    const cuuint32_t box[3] = {b0, b1, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, type, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MOE_ECUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, (int)r);
+    return MOE_OK;
+}
+
+// K splits: the largest split that keeps one wave of CTAs, at least enough splits that no CTA
+// takes more than kTcMaxSteps k-steps of 128.
+int choose_splits(int base_units, int steps, int num_sms) {
+    const int ks_min = (steps + moe::kTcMaxSteps - 1) / moe::kTcMaxSteps;
+    int ks = ks_min;
+    for (int k = ks_min; k <= steps; ++k)
+        if ((long)base_units * k <= num_sms) ks = k;
+    return ks < 1 ? 1 : ks;
+}
+
+int act_cap(const moe_layer *L, int M) {
+    const int a = M * L->d.top_k;
+    return a < L->d.num_slots ? a : L->d.num_slots;
+}
+
+int tc_splits_gateup(const moe_layer *L, int M) {
+    return choose_splits(act_cap(L, M) * ((L->d.inter + 127) / 128), (L->d.hidden + 127) / 128, L->num_sms);
+}
+
+int tc_splits_down(const moe_layer *L, int M) {
+    return choose_splits((L->d.hidden + 127) / 128, act_cap(L, M) * ((L->d.inter + 127) / 128), L->num_sms);
+}
+
+// Buffers and tensor maps of the tensor-core decode path.
+int tc_setup(moe_layer *L, cudaStream_t st) {
+    const int H = L->d.hidden, I = L->d.inter;
+    L->n_act_cap = act_cap(L, moe::kDecodeMaxTokens);
+    L->Hpad = (H + 127) / 128 * 128;
+    L->Ipad = (I + 127) / 128 * 128;
+    L->SPH = (H / 32 + 15) / 16 * 16;
+    L->SPI = (I / 32 + 15) / 16 * 16;
+    const int ntI = (I + 127) / 128, ntH = (H + 127) / 128;
+    size_t units_g = 0, units_d = 0;
+    for (int M = 1; M <= moe::kDecodeMaxTokens; ++M) {
+        const size_t ug = (size_t)act_cap(L, M) * ntI * tc_splits_gateup(L, M);
+        const size_t ud = (size_t)ntH * tc_splits_down(L, M);
+        units_g = ug > units_g ? ug : units_g;
+        units_d = ud > units_d ? ud : units_d;
+    }
+    const size_t sz[] = {(size_t)moe::kTcXRows * L->Hpad,
+                         (size_t)moe::kTcXRows * L->SPH,
+                         (size_t)L->n_act_cap * moe::kTcHRows * L->Ipad,
+                         (size_t)L->n_act_cap * moe::kTcHRows * L->SPI,
+                         units_g * moe::kTcPartGateup * sizeof(float),
+                         units_d * moe::kTcPartDown * sizeof(float),
+                         (size_t)L->n_act_cap * ntI * sizeof(unsigned),
+                         (size_t)ntH * sizeof(unsigned),
+                         sizeof(int)};
+    size_t total = 0;
+    for (size_t s : sz) total += align_up(s, 256);
+    cudaError_t e = cudaMalloc(&L->tc_block, total);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(e == cudaErrorMemoryAllocation ? MOE_ENOMEM : MOE_ECUDA, "tensor-core scratch: %s",
+                    cudaGetErrorString(e));
+    }
+    char *p = static_cast<char *>(L->tc_block);
+    void **dst[] = {(void **)&L->xq, (void **)&L->xs, (void **)&L->hq, (void **)&L->hs, (void **)&L->part,
+                    (void **)&L->part_down, (void **)&L->ctr_gateup, (void **)&L->ctr_down, (void **)&L->err};
+    for (size_t i = 0; i < sizeof(sz) / sizeof(sz[0]); ++i) {
+        *dst[i] = p;
+        p += align_up(sz[i], 256);
+    }
+    // operands start at zero; their scale padding (k-blocks past K) must stay finite: 2^0
+    CUDA_TRY(cudaMemsetAsync(L->tc_block, 0, total, st));
+    CUDA_TRY(cudaMemsetAsync(L->xs, 0x7f, sz[1], st));
+    CUDA_TRY(cudaMemsetAsync(L->hs, 0x7f, sz[3], st));
+
+    const moe::ExpertGeometry &g = L->geo;
+    const int S = L->d.num_slots;
+    int rc;
+    if ((rc = encode_map(&L->mapG, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, L->slots + g.off_wg_codes, H / 128 * 128,
+                         I, S, H / 2, g.expert_bytes, 128, 128, "gate codes")))
+        return rc;
+    if ((rc = encode_map(&L->mapU, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, L->slots + g.off_wu_codes, H / 128 * 128,
+                         I, S, H / 2, g.expert_bytes, 128, 128, "up codes")))
+        return rc;
+    if ((rc = encode_map(&L->mapD, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, L->slots + g.off_wd_codes, I / 128 * 128,
+                         H, S, I / 2, g.expert_bytes, 128, 128, "down codes")))
+        return rc;
+    if ((rc = encode_map(&L->mapX, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->xq, L->Hpad, moe::kTcXRows, 1, L->Hpad,
+                         (uint64_t)moe::kTcXRows * L->Hpad, 128, moe::kTcXRows, "x terms")))
+        return rc;
+    if ((rc = encode_map(&L->mapH, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->hq, L->Ipad, moe::kTcHRows, L->n_act_cap,
+                         L->Ipad, (uint64_t)moe::kTcHRows * L->Ipad, 128, moe::kTcHRows, "h terms")))
+        return rc;
+    L->tc = true;
+    return MOE_OK;
 }
 
 }  // namespace
@@ -262,6 +395,14 @@ int moe_layer_create(const moe_layer_desc *desc, const float *router_w_dev, cons
         }
     }
     CREATE_TRY(cudaMemsetAsync(L->dev_block, 0, total, st));
+    // decode on the tensor cores wherever a full 128-column tile exists along H and I
+    if (d.hidden >= 128 && d.inter >= 128) {
+        const int rc = tc_setup(L, st);
+        if (rc) {
+            release(L);
+            return rc;
+        }
+    }
 
     // page-locked mirror: counts[4], hist[E], cold token/expert/w [max_hot]
     const size_t psz = align_up(16, 64) + align_up((size_t)E * 4, 64) + 3 * align_up(nh * 4, 64);
@@ -385,7 +526,48 @@ int moe_forward_slots(moe_layer *L, const void *x_dev, void *out_dev, int32_t M,
     p.h = L->h;
     p.out = out_dev;
     p.out_f32 = L->d.out_dtype == MOE_OUT_F32;
-    if (M <= moe::kDecodeMaxTokens) {
+    if (M <= moe::kDecodeMaxTokens && L->tc) {
+        moe::TcLaunch t{};
+        t.bank = L->slots;
+        t.geo = L->geo;
+        t.M = M;
+        t.n_act_max = act_cap(L, M);
+        t.ks_gateup = tc_splits_gateup(L, M);
+        t.ks_down = tc_splits_down(L, M);
+        t.counts = L->rb.counts;
+        t.act_slot = L->rb.act_slot;
+        t.act_off = L->rb.act_off;
+        t.act_cnt = L->rb.act_cnt;
+        t.hot_token = L->rb.hot_token;
+        t.hot_w = L->rb.hot_w;
+        t.xs = L->xs;
+        t.SPH = L->SPH;
+        t.hq = L->hq;
+        t.hs = L->hs;
+        t.Ipad = L->Ipad;
+        t.SPI = L->SPI;
+        t.part = L->part;
+        t.part_down = L->part_down;
+        t.tile_ctr_gateup = L->ctr_gateup;
+        t.tile_ctr_down = L->ctr_down;
+        t.err = L->err;
+        t.out = out_dev;
+        t.out_f32 = p.out_f32;
+        t.mapG = &L->mapG;
+        t.mapU = &L->mapU;
+        t.mapX = &L->mapX;
+        t.mapD = &L->mapD;
+        t.mapH = &L->mapH;
+        CUDA_TRY(prof_mark(L, 1, st));
+        moe::launch_quantize_x(p.x, M, L->d.hidden, L->xq, L->Hpad, L->xs, L->SPH, st);
+        moe::launch_gateup_tc(t, st);
+        CUDA_TRY(cudaGetLastError());
+        CUDA_TRY(prof_mark(L, 1, st));
+        CUDA_TRY(prof_mark(L, 2, st));
+        moe::launch_down_tc(t, st);
+        CUDA_TRY(cudaGetLastError());
+        CUDA_TRY(prof_mark(L, 2, st));
+    } else if (M <= moe::kDecodeMaxTokens) {
         p.bank = L->slots;
         CUDA_TRY(prof_mark(L, 1, st));
         moe::launch_gateup(p, M, st, L->num_sms);
@@ -570,6 +752,18 @@ int moe_debug_stats(const moe_layer *L, int64_t stats[4]) {
     if (!L || !stats) return fail(MOE_EINVAL, "layer and stats are required");
     for (int i = 0; i < 4; ++i) stats[i] = L->stats[i];
     return MOE_OK;
+}
+
+int moe_debug_check_error(moe_layer *L, int32_t *code) {
+    if (!L) return fail(MOE_EINVAL, "layer is NULL");
+    int32_t v = 0;
+    if (L->err) {
+        CUDA_TRY(cudaDeviceSynchronize());
+        CUDA_TRY(cudaMemcpy(&v, L->err, sizeof(int32_t), cudaMemcpyDeviceToHost));
+        CUDA_TRY(cudaMemset(L->err, 0, sizeof(int32_t)));
+    }
+    if (code) *code = v;
+    return v ? fail(MOE_ETIMEOUT, "a tensor-core kernel gave up a bounded wait (code %d)", v) : MOE_OK;
 }
 
 int moe_debug_profile(moe_layer *L, int32_t enable) {

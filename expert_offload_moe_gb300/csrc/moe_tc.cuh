@@ -1,0 +1,188 @@
+// Device helpers for the Blackwell (sm_103a) tensor-core path: mbarriers,
+// TMA tensor copies, tcgen05 MMA / TMEM, and the exact splitting of fp32 /
+// bf16 values into E4M3 terms with E8M0 block scales.
+//
+// Layouts used with tcgen05.mma .kind::mxf8f6f4 .block_scale.scale_vec::1X
+// (M = 128, cta_group::1), as verified on the GPU with exact integer data:
+//  * A and B tiles are K-major, 128 bytes per row, 128-byte swizzle (16-byte
+//    chunk c of row r stored at chunk c ^ (r % 8)), 8-row groups 1024 bytes
+//    apart; the K step of one MMA (32 elements) advances the start address by
+//    32 bytes.  E2M1 operands sit in smem as 16 codes in 8 bytes (low nibble
+//    first) followed by 8 bytes of padding, i.e. one byte of smem per element.
+//  * The accumulator D[m][n] is TMEM lane m, column base + n (fp32).
+//  * Block scales (E8M0) of a 4-k-block step of an M=128 operand: TMEM lane
+//    (32 q + m0) for every quadrant q, column base + (m / 32), byte k-block % 4
+//    of row m = 32 (m / 32) + m0; the instruction's scale id picks the byte.
+//    Scale addresses are 4-column aligned.  B (N <= 32) uses the same atom with
+//    lane = column n.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace moe {
+namespace tc {
+
+// Bounded waits: a spin that runs out sets an error word and returns false.
+constexpr uint32_t kSpinLimit = 1u << 26;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_barrier_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for the phase with the given parity; gives up after kWaitLimitNs, sets *err and returns false.
+constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err, int code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 0; it < kSpinLimit; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63) == 63 && global_ns() - t0 > kWaitLimitNs) break;
+    }
+    if (err) atomicExch(err, code);
+    return false;
+}
+
+// 3-D tiled TMA load into shared memory, completing on an mbarrier.
+__device__ __forceinline__ void tma_load_3d(const CUtensorMap *map, uint64_t *bar, void *dst, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
+            "r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot_smem)),
+                 "r"(ncols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// K-major, 128-byte swizzle, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)(16 >> 4) << 16;    // leading byte offset (unused with swizzle)
+    d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: next 8-row group
+    d |= (uint64_t)1 << 46;            // descriptor version
+    d |= (uint64_t)2 << 61;            // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, block-scaled kinds: formats (E4M3 = 0, E2M1 = 5), UE8M0 scales, M = 128.
+__host__ __device__ constexpr uint32_t mx_idesc(uint32_t afmt, uint32_t bfmt, uint32_t N) {
+    return (afmt << 7) | (bfmt << 10) | ((N >> 3) << 17) | (1u << 23) | ((128u >> 4) << 24);
+}
+
+constexpr uint32_t kFmtE4M3 = 0, kFmtE2M1 = 5;
+
+__device__ __forceinline__ void mma_mx(uint32_t tD, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t sfid,
+                                       uint32_t tSFA, uint32_t tSFB, uint32_t accumulate) {
+    const uint32_t id = idesc | (sfid << 4) | (sfid << 29);
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p; }" ::"r"(tD),
+        "l"(adesc), "l"(bdesc), "r"(id), "r"(tSFA), "r"(tSFB), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ------------------------------------------------ E4M3 terms of a 32-value block
+
+// E8M0 byte of 2^e (e clamped to the E8M0 range).
+__device__ __forceinline__ uint32_t e8m0_byte(int e) { return (uint32_t)min(max(e + 127, 0), 254); }
+
+__device__ __forceinline__ float e8m0_value(uint32_t b) {
+    return b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);
+}
+
+// Two fp32 values to packed E4M3 (round to nearest even, saturating).
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Packed E4M3 pair back to fp32 (exact).
+__device__ __forceinline__ void e4m3x2_to_f32x2(uint16_t v, float &lo, float &hi) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+    __half2 h = *reinterpret_cast<__half2 *>(&h2);
+    lo = __low2float(h);
+    hi = __high2float(h);
+}
+
+}  // namespace tc
+}  // namespace moe

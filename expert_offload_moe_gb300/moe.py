@@ -21,7 +21,7 @@ EXPORTED = [
     "moe_layer_create", "moe_route", "moe_forward_slots", "moe_cache_update", "moe_destroy", "moe_last_error",
     "moe_layer_set_bias", "moe_layer_attach_staging", "moe_layer_stage_all", "moe_debug_get_map",
     "moe_debug_slot_ptr", "moe_debug_inject_fault", "moe_debug_stats", "moe_debug_profile",
-    "moe_debug_profile_read", "moe_policy_step", "moe_route_noalloc",
+    "moe_debug_profile_read", "moe_debug_check_error", "moe_policy_step", "moe_route_noalloc",
 ]
 
 
@@ -82,6 +82,7 @@ def lib():
         L.moe_debug_stats.argtypes = [p, p]
         L.moe_debug_profile.argtypes = [p, i32]
         L.moe_debug_profile_read.argtypes = [p, p]
+        L.moe_debug_check_error.argtypes = [p, ctypes.POINTER(i32)]
         L.moe_route_noalloc.argtypes = [p, i32, i32, p, p, i32, i32, p, ctypes.POINTER(RouteBuffers), p]
         L.moe_policy_step.argtypes = [p, p, p, p, i32, i32, p, ctypes.c_int64, ctypes.c_double, i32, p, p, p, p]
         for name in EXPORTED:
@@ -174,6 +175,11 @@ class Layer:
         s = np.zeros(4, dtype=np.int64)
         check(lib().moe_debug_stats(self.h, s.ctypes.data_as(_P)))
         return s
+
+    def check_error(self):
+        """Raises MoeError(MOE_ETIMEOUT) if a tensor-core kernel gave up a bounded wait since the last check."""
+        code = ctypes.c_int32(0)
+        check(lib().moe_debug_check_error(self.h, ctypes.byref(code)))
 
     def profile(self, enable):
         check(lib().moe_debug_profile(self.h, 1 if enable else 0))

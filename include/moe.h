@@ -265,6 +265,12 @@ int moe_debug_inject_fault(moe_layer *layer, int32_t fault);
  * [2] routes seen, [3] hot routes seen (updated by moe_cache_update). */
 int moe_debug_stats(const moe_layer *layer, int64_t stats[4]);
 
+/* Reads and clears the layer's device error word (synchronises the device):
+ * 0 = no error; otherwise a tensor-core kernel gave up a bounded wait
+ * (1: operand copy, 2: stage release, 3: accumulator) and its output is not
+ * valid.  Returns MOE_ETIMEOUT when the word was set, MOE_OK otherwise. */
+int moe_debug_check_error(moe_layer *layer, int32_t *code);
+
 /* Kernel timing for benchmarks: with enable != 0, later route and forward
  * calls record timing events around the router, gate/up and down kernels on
  * the caller's stream (synchronises the device; resets the sums). */

@@ -36,6 +36,7 @@ def run_layer(li, x_bits, M, out_f32=False, layer=None):
     res = lay.route(x, M)
     lay.forward_slots(x, out, M)
     torch.cuda.synchronize()
+    lay.check_error()
     g = route_arrays(res, w.experts, w.top_k)
     o = out.float().cpu().numpy()
     if layer is None:
@@ -80,6 +81,15 @@ def test_tiny_partial_map_returns_cold_routes(M):
     g, o, out, _, excl = check_case(li, x, True, e2s)
     if M > 1:
         assert g["counts"][1] > 0  # some routes are cold
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_narrow_expert_takes_the_cuda_core_kernels(M):
+    # I = 64 has no full 128-column tile, so this shape runs the CUDA-core decode kernels
+    w = synth.Workload("tiny_i64", 1, 256, 64, 16, 2, 16, (M,), 1)
+    li = stack.LayerInputs(w, 0)
+    x = synth.activations(0, 0, 70 + M, M, w.hidden)
+    check_case(li, x, M == 8)
 
 
 def test_tiny_all_cold_outputs_zero():
