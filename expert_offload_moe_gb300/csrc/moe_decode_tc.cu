@@ -12,7 +12,7 @@
 // The activation operand must be 8-bit, so each value is split exactly into
 // E4M3 terms with one E8M0 scale per 32-element block along K: x (bf16, 8-bit
 // significand) = 2 terms, reproduced exactly for every element within 2^14 of
-// its block's largest magnitude; h (fp32) = 3 terms (12 significant bits).
+// its block's largest magnitude; h (fp32) = 4 terms (16 significant bits).
 // Each term is one more column of the B operand, and the columns of a token
 // are summed after the MMA.  The routing weight is folded into the down
 // operand (w * h), so the down MMA accumulates sum over experts of w * Wd h
@@ -36,13 +36,15 @@ namespace {
 using namespace tc;
 
 constexpr int kStages = 4;
-constexpr int kTileA = 128 * 128;  // one 128 x 128 E2M1 tile, one byte per code in smem
+constexpr int kTileA = 128 * 128;       // one 128 x 128 E2M1 tile, one byte per code in smem
+constexpr int kTileATx = 128 * 128 / 2;  // bytes a TMA copy of that tile moves (the packed codes)
 constexpr uint32_t kTmemCols = 256;  // a CTA handles at most kMaxSteps k-steps
 constexpr int kMaxSteps = 16;
 constexpr int NBX = 16;  // B columns of gate/up: 2 x terms x <= 8 tokens
-constexpr int NBH = 32;  // B columns of down: 3 h terms x <= 8 tokens
+constexpr int kHTerms = 4;  // E4M3 terms of w * h: 16 significant bits
+constexpr int NBH = 32;      // B columns of down: 4 h terms x <= 8 tokens
 // error codes written to the error word
-constexpr int kErrFull = 1, kErrEmpty = 2, kErrDone = 3;
+constexpr int kErrFull = 1, kErrEmpty = 2, kErrDone = 3, kErrScales = 4, kErrSteps = 5;
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -192,8 +194,8 @@ __global__ void __launch_bounds__(kRoleThreads, 1)
     gateup_tc_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ CUtensorMap mapU,
                      const __grid_constant__ CUtensorMap mapX, GateUpArgs a) {
     constexpr int kB = NBX * 128;
-    constexpr uint32_t kTx = 2 * kTileA + kB;
-    constexpr int T = 3;  // terms of w * h in the down operand
+    constexpr uint32_t kTx = 2 * kTileATx + kB;
+    constexpr int T = kHTerms;  // terms of w * h in the down operand
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     uint32_t *s_scg = reinterpret_cast<uint32_t *>(smem + kStages * kGateStage);  // [kMaxSteps][128]
@@ -212,6 +214,10 @@ __global__ void __launch_bounds__(kRoleThreads, 1)
     const int nks = (a.H + 127) / 128;
     const int k0 = ks * nks / a.KS, k1 = (ks + 1) * nks / a.KS, nsteps = k1 - k0;
     const bool ragged = (a.H % 128) != 0;
+    if (nsteps > kMaxSteps) {  // the host always splits K finely enough; refuse rather than overrun
+        if (threadIdx.x == 0) atomicExch(a.err, kErrSteps);
+        return;
+    }
     const int slot = a.act_slot[aidx];
     const uint8_t *expert = a.bank + (size_t)slot * a.expert_bytes;
     const int row0 = tile * 128;
@@ -264,7 +270,7 @@ __global__ void __launch_bounds__(kRoleThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = mx_idesc(kFmtE2M1, kFmtE4M3, NBX);
-            ok = mbar_wait(&scales_ready, 0, a.err, kErrFull);
+            ok = mbar_wait(&scales_ready, 0, a.err, kErrScales);
             tc_fence_after();
             for (int i = 0; i < nsteps && ok; ++i) {
                 const int st = i % kStages;
@@ -432,8 +438,8 @@ __global__ void __launch_bounds__(kRoleThreads, 1)
     down_tc_kernel(const __grid_constant__ CUtensorMap mapD, const __grid_constant__ CUtensorMap mapH, DownArgs a) {
     constexpr int NB = NBH;
     constexpr int kB = NB * 128;
-    constexpr uint32_t kTx = kTileA + kB;
-    constexpr int T = 3;
+    constexpr uint32_t kTx = kTileATx + kB;
+    constexpr int T = kHTerms;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     uint32_t *s_sc = reinterpret_cast<uint32_t *>(smem + kStages * kDownStage);  // [kMaxSteps][128]
@@ -450,6 +456,10 @@ __global__ void __launch_bounds__(kRoleThreads, 1)
     const int g0 = ks * total / a.KS, g1 = (ks + 1) * total / a.KS, nsteps = g1 - g0;
     const bool ragged = (a.I % 128) != 0;
     const int row0 = tile * 128;
+    if (nsteps > kMaxSteps) {
+        if (threadIdx.x == 0) atomicExch(a.err, kErrSteps);
+        return;
+    }
     for (int i = threadIdx.x; i < n_act; i += kRoleThreads) s_slot[i] = a.act_slot[i];
 
     if (warp == 1) tmem_alloc(&tslot, kTmemCols);
@@ -492,7 +502,7 @@ __global__ void __launch_bounds__(kRoleThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = mx_idesc(kFmtE2M1, kFmtE4M3, NB);
-            ok = mbar_wait(&scales_ready, 0, a.err, kErrFull);
+            ok = mbar_wait(&scales_ready, 0, a.err, kErrScales);
             tc_fence_after();
             for (int i = 0; i < nsteps && ok; ++i) {
                 const int st = i % kStages;

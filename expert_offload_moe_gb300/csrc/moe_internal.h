@@ -104,7 +104,7 @@ constexpr int kTcMaxSteps = 16;     // k-steps of 128 per CTA (tensor memory bud
 constexpr int kTcXRows = 16;        // rows of the x-term operand
 constexpr int kTcHRows = 32;        // rows of the w*h-term operand
 constexpr int kTcPartGateup = 2 * 2 * kDecodeMaxTokens * 128;  // floats per gate/up split partial
-constexpr int kTcPartDown = kDecodeMaxTokens * 3 * 128;         // floats per down split partial
+constexpr int kTcPartDown = kDecodeMaxTokens * 4 * 128;         // floats per down split partial
 
 void launch_quantize_x(const uint16_t *x, int M, int H, uint8_t *xq, int Hpad, uint8_t *xs, int SP, cudaStream_t s);
 void launch_gateup_tc(const TcLaunch &L, cudaStream_t s);
