@@ -159,14 +159,23 @@ __device__ __forceinline__ void store_operand_scales(uint32_t tcol, const uint8_
 // 16-byte chunk u ^ (r % 8)).
 __device__ __forceinline__ void load_tail_tile(uint8_t *dst, const uint8_t *codes, int rows, int row0, int K,
                                                int kstep) {
+    // K is a multiple of 64, so a ragged step holds 64 codes: 4 units per row, 16 per lane; every load is
+    // issued before the first store so the warp waits for memory once
     const int lane = threadIdx.x & 31;
-    const int units = (K - kstep * 128) / 16;
-    for (int i = lane; i < 128 * units; i += 32) {
-        const int r = i / units, u = i - r * units;
-        uint2 v = make_uint2(0u, 0u);
+    constexpr int kUnits = 4, kPerLane = 128 * kUnits / 32;
+    (void)K;
+    uint2 v[kPerLane];
+#pragma unroll
+    for (int j = 0; j < kPerLane; ++j) {
+        const int i = lane + 32 * j, r = i / kUnits, u = i % kUnits;
+        v[j] = make_uint2(0u, 0u);
         if (row0 + r < rows)
-            v = *reinterpret_cast<const uint2 *>(codes + (size_t)(row0 + r) * (K / 2) + kstep * 64 + u * 8);
-        *reinterpret_cast<uint4 *>(dst + r * 128 + ((u ^ (r & 7)) * 16)) = make_uint4(v.x, v.y, 0u, 0u);
+            v[j] = __ldg(reinterpret_cast<const uint2 *>(codes + (size_t)(row0 + r) * (K / 2) + kstep * 64 + u * 8));
+    }
+#pragma unroll
+    for (int j = 0; j < kPerLane; ++j) {
+        const int i = lane + 32 * j, r = i / kUnits, u = i % kUnits;
+        *reinterpret_cast<uint4 *>(dst + r * 128 + ((u ^ (r & 7)) * 16)) = make_uint4(v[j].x, v[j].y, 0u, 0u);
     }
     fence_proxy_async();
     __syncwarp();

@@ -25,6 +25,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kSmemRoutes = 1024;
+constexpr int kMaxChunks = 16;  // router chunks summed with all loads in flight (H <= 4096)
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -144,12 +145,34 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
     for (int e = threadIdx.x; e < E; e += kThreads) s_hist[e] = 0;
     __syncthreads();
 
-    for (int t = warp; t < M; t += kWarps) {
-        for (int e = lane; e < E; e += 32) {
+    // Decode (M <= 8): every thread sums chunk partials for some (token, expert) pairs, all loads of a
+    // pair issued before the sum (in chunk order), into row t of s_l; warp t then selects from its row.
+    const bool rows_by_block = M <= kWarps && p.nchunk <= kMaxChunks;
+    if (rows_by_block) {
+        for (int q = threadIdx.x; q < M * E; q += kThreads) {
+            const int t = q / E, e = q - t * E;
+            float pv[kMaxChunks];
+#pragma unroll
+            for (int c = 0; c < kMaxChunks; ++c)
+                pv[c] = c < p.nchunk ? __ldcg(p.b.logit_part + ((size_t)c * M + t) * E + e) : 0.f;
             float v = 0.f;
-            for (int c = 0; c < p.nchunk; ++c) v += __ldcg(p.b.logit_part + ((size_t)c * M + t) * E + e);
+#pragma unroll
+            for (int c = 0; c < kMaxChunks; ++c)
+                if (c < p.nchunk) v += pv[c];
             v += p.bias ? p.bias[e] : 0.f;
-            s_l[warp][e] = (v != v) ? -INFINITY : v;  // NaN marks a taken expert below
+            s_l[t][e] = (v != v) ? -INFINITY : v;  // NaN marks a taken expert below
+        }
+        __syncthreads();
+    }
+
+    for (int t = warp; t < M; t += kWarps) {
+        if (!rows_by_block) {
+            for (int e = lane; e < E; e += 32) {
+                float v = 0.f;
+                for (int c = 0; c < p.nchunk; ++c) v += __ldcg(p.b.logit_part + ((size_t)c * M + t) * E + e);
+                v += p.bias ? p.bias[e] : 0.f;
+                s_l[warp][e] = (v != v) ? -INFINITY : v;
+            }
         }
         __syncwarp();
         int sel_id[kMaxTopK];
