@@ -9,16 +9,24 @@
 // dequantise-and-multiply, gate / up / down; xinfer docs "How it works":
 // GEMMs over [num_slots, N, K] slot tensors).
 //
+// Block scales travel as 512-byte atoms, one per (128-row tile, 128-column
+// k-step): byte m0*16 + m1*4 + kb holds the scale of row 32 m1 + m0 and
+// k-block 4 step + kb.  An atom is bulk-copied with its operand tile and moved
+// into tensor memory by tcgen05.cp (32x128b, replicated to the four lane
+// quadrants) right before the MMAs that use it.  Weight atoms are built once
+// when an expert lands in a slot (build_weight_atoms); activation atoms are
+// written by the kernels that produce the activation terms.
+//
 // The activation operand must be 8-bit, so each value is split exactly into
 // E4M3 terms with one E8M0 scale per 32-element block along K: x (bf16, 8-bit
 // significand) = 2 terms, reproduced exactly for every element within 2^14 of
-// its block's largest magnitude; h (fp32) = 4 terms (16 significant bits).
+// its block's largest magnitude; w h (fp32) = 4 terms (16 significant bits).
 // Each term is one more column of the B operand, and the columns of a token
 // are summed after the MMA.  The routing weight is folded into the down
-// operand (w * h), so the down MMA accumulates sum over experts of w * Wd h
-// directly: the combine happens in tensor memory, in ascending expert order.
+// operand (w h), so the down MMA accumulates the sum over experts of w Wd h in
+// tensor memory, in ascending expert order: the combine happens there.
 //
-// quantize_x_kernel  x -> x terms (B operand of gate/up)
+// quantize_x_kernel  x -> x terms + x atoms (B operand of gate/up)
 // gateup_tc_kernel   one CTA per (active expert, 128-row tile of I, K split):
 //                    Dg = Wg x, Du = Wu x; then h = SiLU(g) u, w h -> h terms
 // down_tc_kernel     one CTA per (128-row tile of H, K split over the
@@ -35,16 +43,20 @@ namespace {
 
 using namespace tc;
 
-constexpr int kStages = 4;
+constexpr int kThreads = 128;           // warp 0: copies; warp 1 lane 0: MMAs; all 4 warps: epilogue
 constexpr int kTileA = 128 * 128;       // one 128 x 128 E2M1 tile, one byte per code in smem
-constexpr int kTileATx = 128 * 128 / 2;  // bytes a TMA copy of that tile moves (the packed codes)
-constexpr uint32_t kTmemCols = 256;  // a CTA handles at most kMaxSteps k-steps
-constexpr int kMaxSteps = 16;
-constexpr int NBX = 16;  // B columns of gate/up: 2 x terms x <= 8 tokens
-constexpr int kHTerms = 4;  // E4M3 terms of w * h: 16 significant bits
-constexpr int NBH = 32;      // B columns of down: 4 h terms x <= 8 tokens
-// error codes written to the error word
-constexpr int kErrFull = 1, kErrEmpty = 2, kErrDone = 3, kErrScales = 4, kErrSteps = 5;
+constexpr int kTileATx = 128 * 128 / 2; // bytes a TMA copy of that tile moves (the packed codes)
+constexpr int kAtom = kTcAtomBytes;
+constexpr int NBX = kTcXRows;           // B columns of gate/up: 2 x terms x <= 8 tokens
+constexpr int NBH = kTcHRows;           // B columns of down: 4 w*h terms x <= 8 tokens
+constexpr int kHTerms = 4;
+constexpr int kGateStages = 3, kDownStages = 4;
+// stage layout: [A tiles][B tile][atoms], 1024-aligned for the 128-byte swizzle
+constexpr int kGateStage = 2 * kTileA + NBX * 128 + 3 * kAtom + 512;   // 36 KB
+constexpr int kDownStage = kTileA + NBH * 128 + 2 * kAtom + 1024;       // 22 KB
+static_assert(kGateStage % 1024 == 0 && kDownStage % 1024 == 0, "stage alignment");
+constexpr uint32_t kGateTmem = 128, kDownTmem = 64;
+constexpr int kErrFull = 1, kErrEmpty = 2, kErrDone = 3;
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -70,11 +82,9 @@ __device__ __forceinline__ int floor_log2(float a) {
 // returns this lane's code, updates the residual, and gives the block's E8M0 byte.
 __device__ __forceinline__ uint8_t split_term(float &res, uint32_t &scale_byte) {
     const float amax = warp_max(fabsf(res));
-    int X = amax > 0.f ? floor_log2(amax) - 7 : -127;  // |res| / 2^X < 256: no saturation
-    X = max(X, -127);
+    const int X = amax > 0.f ? max(floor_log2(amax) - 7, -127) : -127;  // |res| / 2^X < 256: no saturation
     scale_byte = e8m0_byte(X);
-    const float inv = e8m0_value(e8m0_byte(-X) < 255 ? e8m0_byte(-X) : 254);
-    // pair lanes so one cvt packs two values; each lane keeps its own byte
+    const float inv = e8m0_value(e8m0_byte(-X));
     const float mine = res * inv;
     const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
     const int lane = threadIdx.x & 31;
@@ -82,88 +92,34 @@ __device__ __forceinline__ uint8_t split_term(float &res, uint32_t &scale_byte) 
     const uint8_t code = (lane & 1) ? (uint8_t)(pk >> 8) : (uint8_t)(pk & 0xff);
     float lo, hi;
     e4m3x2_to_f32x2(pk, lo, hi);
-    const float q = (lane & 1) ? hi : lo;
-    res = res - q * e8m0_value(scale_byte);
+    res = res - ((lane & 1) ? hi : lo) * e8m0_value(scale_byte);
     return code;
 }
 
-}  // namespace
-
-// ------------------------------------------------------------------ x terms
-
-// xq[t * 2 + term][Hpad] E4M3 codes, xs[t * 2 + term][SP] E8M0 scales; one warp per 32-block.
-__global__ void __launch_bounds__(256) quantize_x_kernel(const uint16_t *x, int M, int H, uint8_t *xq, int Hpad,
-                                                         uint8_t *xs, int SP) {
-    const int lane = threadIdx.x & 31;
-    const int nb = H / 32;
-    const int task = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (task >= M * nb) return;
-    const int t = task / nb, b = task - t * nb;
-    float res = __uint_as_float((uint32_t)x[(size_t)t * H + b * 32 + lane] << 16);
-#pragma unroll
-    for (int term = 0; term < 2; ++term) {
-        uint32_t sb;
-        const uint8_t code = split_term(res, sb);
-        xq[(size_t)(t * 2 + term) * Hpad + b * 32 + lane] = code;
-        if (lane == 0) xs[(size_t)(t * 2 + term) * SP + b] = (uint8_t)sb;
-    }
+// 1-D bulk copy global -> shared completing on an mbarrier (16-byte aligned, multiple of 16 bytes).
+__device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
 }
 
-namespace {
-
-// ---------------------------------------------------------------- warp roles
-// 192 threads: warp 0 issues TMA copies (its lanes also copy a ragged last k-step), warp 1 lane 0 issues the
-// MMAs and warp 1 owns the tensor memory, warps 2..5 load the block scales into tensor memory while the
-// first copies are in flight, then read the accumulators (warp w reads TMEM lane quadrant w % 4).
-constexpr int kRoleThreads = 192;
-constexpr int kScaleWarp0 = 2;
-
-__device__ __forceinline__ void named_sync_scale_warps() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-// Weight scales of one k-step for row r of a 128-row tile: 4 E8M0 bytes (k-blocks 4 kstep .. +3) as one word;
-// 2^0 for rows or k-blocks outside the matrix.  nkb is even, so the byte pairs never straddle the end.
-__device__ __forceinline__ uint32_t weight_scale_word(const uint8_t *scales, int rows, int nkb, int row, int kstep) {
-    uint32_t v = 0x7f7f7f7fu;
-    if (row < rows) {
-        const int c = kstep * 4;
-        const uint16_t *p = reinterpret_cast<const uint16_t *>(scales + (size_t)row * nkb + c);
-        const uint32_t lo = c < nkb ? (uint32_t)__ldg(p) : 0x7f7fu;
-        const uint32_t hi = c + 2 < nkb ? (uint32_t)__ldg(p + 1) : 0x7f7fu;
-        v = lo | (hi << 16);
-    }
-    return v;
+// Scale atom (512 bytes in smem, 32 rows of 16 bytes) -> 4 TMEM columns in every lane quadrant.
+__device__ __forceinline__ void atom_to_tmem(uint32_t tcol, const void *atom) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_u32(atom) >> 4) & 0x3FFF);
+    d |= (uint64_t)(16 >> 4) << 16;
+    d |= (uint64_t)(128 >> 4) << 32;  // next 8 rows
+    d |= (uint64_t)1 << 46;
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tcol), "l"(d) : "memory");
 }
 
-// Writes the scale atoms of n k-steps from s_sc[step][row] into this warp's TMEM lane quadrant:
-// column base + 4 s + m1, byte kb, of row 32 m1 + lane.
-__device__ __forceinline__ void store_weight_scales(uint32_t tcol, const uint32_t *s_sc, int n) {
-    const int lane = threadIdx.x & 31, quad = (threadIdx.x >> 5) & 3;
-    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    for (int s = 0; s < n; ++s)
-        tmem_st4(tcol + lane_off + 4 * s, s_sc[s * 128 + lane], s_sc[s * 128 + 32 + lane], s_sc[s * 128 + 64 + lane],
-                 s_sc[s * 128 + 96 + lane]);
-}
-
-// Scales of the B operand (N <= 32 columns, one row of SP bytes each, padded with 2^0 past K); column n is
-// TMEM lane n of every quadrant.
-__device__ __forceinline__ void store_operand_scales(uint32_t tcol, const uint8_t *scales, int SP, int NB, int kstep) {
-    const int lane = threadIdx.x & 31, quad = (threadIdx.x >> 5) & 3;
-    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    uint32_t v = 0x7f7f7f7fu;
-    if (lane < NB) v = *reinterpret_cast<const uint32_t *>(scales + (size_t)lane * SP + kstep * 4);
-    tmem_st1(tcol + lane_off, v);
-}
-
-// The last k-step of a row tile when K is not a multiple of 128: the codes of each row (K - 128 kstep of
-// them, 8 bytes per 16) copied by the whole warp into the padded, swizzled smem layout (unit u of row r at
-// 16-byte chunk u ^ (r % 8)).
+// The last k-step of a row tile when K % 128 == 64: 64 codes per row copied by the whole warp into the
+// padded, swizzled smem layout (unit u of row r at 16-byte chunk u ^ (r % 8)); all loads before any store.
 __device__ __forceinline__ void load_tail_tile(uint8_t *dst, const uint8_t *codes, int rows, int row0, int K,
                                                int kstep) {
-    // K is a multiple of 64, so a ragged step holds 64 codes: 4 units per row, 16 per lane; every load is
-    // issued before the first store so the warp waits for memory once
     const int lane = threadIdx.x & 31;
     constexpr int kUnits = 4, kPerLane = 128 * kUnits / 32;
-    (void)K;
     uint2 v[kPerLane];
 #pragma unroll
     for (int j = 0; j < kPerLane; ++j) {
@@ -181,35 +137,79 @@ __device__ __forceinline__ void load_tail_tile(uint8_t *dst, const uint8_t *code
     __syncwarp();
 }
 
+}  // namespace
+
+// ------------------------------------------------------------------ atoms
+
+// Weight scale atoms of one slot: for each (row tile, k-step), byte m0*16 + m1*4 + kb = scale of row
+// 128 tile + 32 m1 + m0 and k-block 4 step + kb (2^0 outside the matrix).  One warp per atom.
+__global__ void __launch_bounds__(256) build_weight_atoms_kernel(const uint8_t *scales, int rows, int nkb,
+                                                                 uint8_t *atoms, int ntile, int nsteps) {
+    const int atom = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (atom >= ntile * nsteps) return;
+    const int tile = atom / nsteps, step = atom - tile * nsteps, m0 = threadIdx.x & 31;
+    uint32_t w[4];
+#pragma unroll
+    for (int m1 = 0; m1 < 4; ++m1) {
+        const int row = tile * 128 + 32 * m1 + m0;
+        uint32_t v = 0;
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) {
+            const int c = step * 4 + kb;
+            const uint32_t b = (row < rows && c < nkb) ? scales[(size_t)row * nkb + c] : 127u;
+            v |= b << (8 * kb);
+        }
+        w[m1] = v;
+    }
+    *reinterpret_cast<uint4 *>(atoms + (size_t)atom * kAtom + m0 * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// x terms: xq[t * 2 + term][Hpad] E4M3 codes and their scales in atoms xat[step][512] (row n = t*2+term
+// at byte n*16 + kb); one warp per 32-element block.
+__global__ void __launch_bounds__(256) quantize_x_kernel(const uint16_t *x, int M, int H, uint8_t *xq, int Hpad,
+                                                         uint8_t *xat) {
+    const int lane = threadIdx.x & 31;
+    const int nb = H / 32;
+    const int task = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (task >= M * nb) return;
+    const int t = task / nb, b = task - t * nb;
+    float res = __uint_as_float((uint32_t)x[(size_t)t * H + b * 32 + lane] << 16);
+#pragma unroll
+    for (int term = 0; term < 2; ++term) {
+        uint32_t sb;
+        const uint8_t code = split_term(res, sb);
+        const int n = t * 2 + term;
+        xq[(size_t)n * Hpad + b * 32 + lane] = code;
+        if (lane == 0) xat[(size_t)(b / 4) * kAtom + n * 16 + (b % 4)] = (uint8_t)sb;
+    }
+}
+
+namespace {
+
 struct GateUpArgs {
-    const uint8_t *bank;
-    size_t expert_bytes, off_g_codes, off_g_scales, off_u_codes, off_u_scales;
+    const uint8_t *bank, *atoms;  // slot bank; weight atoms of each slot
+    size_t expert_bytes, atom_slot_bytes, off_g_codes, off_u_codes, atom_off_g, atom_off_u;
     int H, I, M, KS;
     const int32_t *counts, *act_slot, *act_off, *act_cnt, *hot_token;
     const float *hot_w;
-    const uint8_t *xs;  // x-term scales [16][SPH]
-    int SPH;
-    uint8_t *hq, *hs;   // w*h terms [n_act_max][32][Ipad], scales [n_act_max][32][SPI]
-    int Ipad, SPI;
-    float *part;        // split-K partials
+    const uint8_t *xat;  // x atoms [nks][512]
+    uint8_t *hq, *hat;   // w*h terms [n_act_cap][32][Ipad], atoms [n_act_cap][nksI][512]
+    int Ipad;
+    float *part;
     unsigned *tile_ctr;
     int *err;
 };
 
-constexpr int kGateStage = 2 * kTileA + ((NBX * 128 + 1023) / 1024) * 1024;
-constexpr int kDownStage = kTileA + ((NBH * 128 + 1023) / 1024) * 1024;
-
-__global__ void __launch_bounds__(kRoleThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     gateup_tc_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ CUtensorMap mapU,
                      const __grid_constant__ CUtensorMap mapX, GateUpArgs a) {
+    constexpr int S = kGateStages;
     constexpr int kB = NBX * 128;
-    constexpr uint32_t kTx = 2 * kTileATx + kB;
-    constexpr int T = kHTerms;  // terms of w * h in the down operand
+    constexpr uint32_t kTxFull = 2 * kTileATx + kB + 3 * kAtom, kTxTail = kB + 3 * kAtom;
+    constexpr int T = kHTerms;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
-    uint32_t *s_scg = reinterpret_cast<uint32_t *>(smem + kStages * kGateStage);  // [kMaxSteps][128]
-    uint32_t *s_scu = s_scg + kMaxSteps * 128;
-    __shared__ __align__(8) uint64_t full[kStages], empty[kStages], done, scales_ready;
+    __shared__ __align__(8) uint64_t full[S], empty[S], done;
     __shared__ uint32_t tslot;
     __shared__ int s_last;
 
@@ -223,22 +223,19 @@ __global__ void __launch_bounds__(kRoleThreads, 1)
     const int nks = (a.H + 127) / 128;
     const int k0 = ks * nks / a.KS, k1 = (ks + 1) * nks / a.KS, nsteps = k1 - k0;
     const bool ragged = (a.H % 128) != 0;
-    if (nsteps > kMaxSteps) {  // the host always splits K finely enough; refuse rather than overrun
-        if (threadIdx.x == 0) atomicExch(a.err, kErrSteps);
-        return;
-    }
     const int slot = a.act_slot[aidx];
     const uint8_t *expert = a.bank + (size_t)slot * a.expert_bytes;
+    const uint8_t *gat = a.atoms + (size_t)slot * a.atom_slot_bytes + a.atom_off_g + (size_t)tile * nks * kAtom;
+    const uint8_t *uat = a.atoms + (size_t)slot * a.atom_slot_bytes + a.atom_off_u + (size_t)tile * nks * kAtom;
     const int row0 = tile * 128;
 
-    if (warp == 1) tmem_alloc(&tslot, kTmemCols);
+    if (warp == 1) tmem_alloc(&tslot, kGateTmem);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         mbar_init(&done, 1);
-        mbar_init(&scales_ready, 128);
         fence_barrier_init();
         tma_prefetch_desc(&mapG);
         tma_prefetch_desc(&mapU);
@@ -248,121 +245,92 @@ __global__ void __launch_bounds__(kRoleThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = tslot;
-    const uint32_t tDg = tbase, tDu = tbase + 16, tSFg = tbase + 32, tSFu = tbase + 32 + 4 * kMaxSteps,
-                   tSFb = tbase + 32 + 8 * kMaxSteps;
+    const uint32_t tDg = tbase, tDu = tbase + 16, tSF = tbase + 32;  // per stage: 12 scale columns
 
-    bool ok = true;
     if (warp == 0) {
-        // producer
+        bool ok = true;
         for (int i = 0; i < nsteps && ok; ++i) {
-            const int st = i % kStages;
-            const int kstep = k0 + i;
-            if (lane == 0) ok = mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1, a.err, kErrEmpty);
+            const int st = i % S, kstep = k0 + i;
+            if (lane == 0) ok = mbar_wait(&empty[st], ((i / S) & 1) ^ 1, a.err, kErrEmpty);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             uint8_t *sA = smem + st * kGateStage;
+            uint8_t *sAt = sA + 2 * kTileA + kB;
             const bool tail = ragged && kstep == nks - 1;
             if (tail) {
                 load_tail_tile(sA, expert + a.off_g_codes, a.I, row0, a.H, kstep);
                 load_tail_tile(sA + kTileA, expert + a.off_u_codes, a.I, row0, a.H, kstep);
             }
             if (lane == 0) {
-                mbar_expect_tx(&full[st], tail ? (uint32_t)kB : kTx);
+                mbar_expect_tx(&full[st], tail ? kTxTail : kTxFull);
                 if (!tail) {
                     tma_load_3d(&mapG, &full[st], sA, kstep * 128, row0, slot);
                     tma_load_3d(&mapU, &full[st], sA + kTileA, kstep * 128, row0, slot);
                 }
                 tma_load_3d(&mapX, &full[st], sA + 2 * kTileA, kstep * 128, 0, 0);
+                bulk_copy(sAt, gat + (size_t)kstep * kAtom, kAtom, &full[st]);
+                bulk_copy(sAt + kAtom, uat + (size_t)kstep * kAtom, kAtom, &full[st]);
+                bulk_copy(sAt + 2 * kAtom, a.xat + (size_t)kstep * kAtom, kAtom, &full[st]);
             }
             __syncwarp();
         }
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = mx_idesc(kFmtE2M1, kFmtE4M3, NBX);
-            ok = mbar_wait(&scales_ready, 0, a.err, kErrScales);
-            tc_fence_after();
+            bool ok = true;
             for (int i = 0; i < nsteps && ok; ++i) {
-                const int st = i % kStages;
-                ok = mbar_wait(&full[st], (i / kStages) & 1, a.err, kErrFull);
+                const int st = i % S;
+                ok = mbar_wait(&full[st], (i / S) & 1, a.err, kErrFull);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t aG = smem_u32(smem + st * kGateStage), aU = aG + kTileA, aB = aG + 2 * kTileA;
+                uint8_t *sA = smem + st * kGateStage;
+                uint8_t *sAt = sA + 2 * kTileA + kB;
+                const uint32_t sfg = tSF + 12 * st, sfu = sfg + 4, sfb = sfg + 8;
+                atom_to_tmem(sfg, sAt);
+                atom_to_tmem(sfu, sAt + kAtom);
+                atom_to_tmem(sfb, sAt + 2 * kAtom);
+                const uint32_t aG = smem_u32(sA), aU = aG + kTileA, aB = aG + 2 * kTileA;
                 const bool tail = ragged && (k0 + i) == nks - 1;
-                const int nk = tail ? ((a.H - (k0 + i) * 128) / 32) : 4;
+                const int nk = tail ? 2 : 4;
                 for (int kk = 0; kk < nk; ++kk) {
                     const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-                    mma_mx(tDg, sw128_desc(aG + kk * 32), sw128_desc(aB + kk * 32), idesc, kk, tSFg + 4 * i,
-                           tSFb + 4 * i, acc);
-                    mma_mx(tDu, sw128_desc(aU + kk * 32), sw128_desc(aB + kk * 32), idesc, kk, tSFu + 4 * i,
-                           tSFb + 4 * i, acc);
+                    mma_mx(tDg, sw128_desc(aG + kk * 32), sw128_desc(aB + kk * 32), idesc, kk, sfg, sfb, acc);
+                    mma_mx(tDu, sw128_desc(aU + kk * 32), sw128_desc(aB + kk * 32), idesc, kk, sfu, sfb, acc);
                 }
                 mma_commit(&empty[st]);
             }
             mma_commit(&done);
         }
         __syncwarp();
-    } else {
-        // scale warps: thread r loads row r's scale words of every step, regrouped through shared memory
-        const int r = threadIdx.x - kScaleWarp0 * 32;
-        const uint8_t *gsc = expert + a.off_g_scales, *usc = expert + a.off_u_scales;
-        const int nkb = a.H / 32;
-        uint32_t wg[kMaxSteps], wu[kMaxSteps];
-#pragma unroll
-        for (int s = 0; s < kMaxSteps; ++s) {
-            if (s < nsteps) {
-                wg[s] = weight_scale_word(gsc, a.I, nkb, row0 + r, k0 + s);
-                wu[s] = weight_scale_word(usc, a.I, nkb, row0 + r, k0 + s);
-            }
-        }
-#pragma unroll
-        for (int s = 0; s < kMaxSteps; ++s) {
-            if (s < nsteps) {
-                s_scg[s * 128 + r] = wg[s];
-                s_scu[s * 128 + r] = wu[s];
-            }
-        }
-        named_sync_scale_warps();
-        store_weight_scales(tSFg, s_scg, nsteps);
-        store_weight_scales(tSFu, s_scu, nsteps);
-        for (int s = 0; s < nsteps; ++s) store_operand_scales(tSFb + 4 * s, a.xs, a.SPH, NBX, k0 + s);
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&scales_ready);
     }
 
-    // ---------------- epilogue (scale warps): every thread owns one row of the tile ----------------
-    const bool epi = warp >= kScaleWarp0;
-    const int quad = warp & 3;
-    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const int row = row0 + quad * 32 + lane;
+    // ---------------- epilogue: every thread owns one row of the tile ----------------
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const int rloc = warp * 32 + lane, row = row0 + rloc;
     const int M = a.M;
     float g[2 * kDecodeMaxTokens], u[2 * kDecodeMaxTokens];
 #pragma unroll
     for (int c = 0; c < 2 * kDecodeMaxTokens; ++c) g[c] = u[c] = 0.f;
-    if (epi) {
-        const bool got = mbar_wait(&done, 0, a.err, kErrDone);
-        tc_fence_after();
-        if (got) {
-            uint32_t rr[8];
+    const bool got = mbar_wait(&done, 0, a.err, kErrDone);
+    tc_fence_after();
+    if (got) {
+        uint32_t rr[8];
 #pragma unroll
-            for (int c8 = 0; c8 < 2; ++c8) {
-                tmem_ld8(tDg + lane_off + 8 * c8, rr);
-                tmem_ld_wait();
+        for (int c8 = 0; c8 < 2; ++c8) {
+            tmem_ld8(tDg + lane_off + 8 * c8, rr);
+            tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 8; ++j) g[8 * c8 + j] = __uint_as_float(rr[j]);
-                tmem_ld8(tDu + lane_off + 8 * c8, rr);
-                tmem_ld_wait();
+            for (int j = 0; j < 8; ++j) g[8 * c8 + j] = __uint_as_float(rr[j]);
+            tmem_ld8(tDu + lane_off + 8 * c8, rr);
+            tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 8; ++j) u[8 * c8 + j] = __uint_as_float(rr[j]);
-            }
+            for (int j = 0; j < 8; ++j) u[8 * c8 + j] = __uint_as_float(rr[j]);
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) tmem_dealloc(tbase, kTmemCols);
-    if (!epi) return;
+    if (warp == 1) tmem_dealloc(tbase, kGateTmem);
 
-    const int rloc = quad * 32 + lane;  // row within the tile
     if (a.KS > 1) {
         // partials [unit][2][2 kDecodeMaxTokens][128], summed by the last CTA of the tile in split order
         const int tile_id = aidx * ntile + tile;
@@ -375,12 +343,12 @@ __global__ void __launch_bounds__(kRoleThreads, 1)
             }
         }
         __threadfence();
-        named_sync_scale_warps();
-        if (threadIdx.x == kScaleWarp0 * 32) s_last = atomicAdd(&a.tile_ctr[tile_id], 1u) == (unsigned)(a.KS - 1);
-        named_sync_scale_warps();
+        __syncthreads();
+        if (threadIdx.x == 0) s_last = atomicAdd(&a.tile_ctr[tile_id], 1u) == (unsigned)(a.KS - 1);
+        __syncthreads();
         if (!s_last) return;
         __threadfence();
-        if (threadIdx.x == kScaleWarp0 * 32) a.tile_ctr[tile_id] = 0u;
+        if (threadIdx.x == 0) a.tile_ctr[tile_id] = 0u;
 #pragma unroll
         for (int c = 0; c < 2 * kDecodeMaxTokens; ++c) g[c] = u[c] = 0.f;
         for (int k = 0; k < a.KS; ++k) {
@@ -397,8 +365,9 @@ __global__ void __launch_bounds__(kRoleThreads, 1)
 
     // h = SiLU(g) u for the tokens routed to this expert; w h split into T E4M3 terms per 32-row block
     const int off = a.act_off[aidx], cnt = a.act_cnt[aidx];
+    const int nksI = (a.I + 127) / 128;
     uint8_t *hq = a.hq + (size_t)aidx * NBH * a.Ipad;
-    uint8_t *hs = a.hs + (size_t)aidx * NBH * a.SPI;
+    uint8_t *hat = a.hat + (size_t)aidx * nksI * kAtom;
     float vt[kDecodeMaxTokens];
 #pragma unroll
     for (int t = 0; t < kDecodeMaxTokens; ++t) vt[t] = 0.f;
@@ -414,6 +383,7 @@ __global__ void __launch_bounds__(kRoleThreads, 1)
         }
     }
     if (row < a.I) {  // whole 32-row blocks are in or out (I % 64 == 0)
+        const int kblock = row / 32;
 #pragma unroll
         for (int t = 0; t < kDecodeMaxTokens; ++t) {
             if (t >= M) break;
@@ -422,20 +392,20 @@ __global__ void __launch_bounds__(kRoleThreads, 1)
             for (int term = 0; term < T; ++term) {
                 uint32_t sb;
                 const uint8_t code = split_term(res, sb);
-                hq[(size_t)(t * T + term) * a.Ipad + row] = code;
-                if (lane == 0) hs[(size_t)(t * T + term) * a.SPI + row / 32] = (uint8_t)sb;
+                const int n = t * T + term;
+                hq[(size_t)n * a.Ipad + row] = code;
+                if (lane == 0) hat[(size_t)(kblock / 4) * kAtom + n * 16 + (kblock % 4)] = (uint8_t)sb;
             }
         }
     }
 }
 
 struct DownArgs {
-    const uint8_t *bank;
-    size_t expert_bytes, off_d_codes, off_d_scales;
+    const uint8_t *bank, *atoms;
+    size_t expert_bytes, atom_slot_bytes, off_d_codes, atom_off_d;
     int H, I, M, KS;
     const int32_t *counts, *act_slot;
-    const uint8_t *hs;  // [n_act_max][32][SPI]
-    int Ipad, SPI;
+    const uint8_t *hat;  // [n_act_cap][nksI][512]
     void *out;
     int out_f32;
     float *part;
@@ -443,16 +413,16 @@ struct DownArgs {
     int *err;
 };
 
-__global__ void __launch_bounds__(kRoleThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     down_tc_kernel(const __grid_constant__ CUtensorMap mapD, const __grid_constant__ CUtensorMap mapH, DownArgs a) {
+    constexpr int S = kDownStages;
     constexpr int NB = NBH;
     constexpr int kB = NB * 128;
-    constexpr uint32_t kTx = kTileATx + kB;
+    constexpr uint32_t kTxFull = kTileATx + kB + 2 * kAtom, kTxTail = kB + 2 * kAtom;
     constexpr int T = kHTerms;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
-    uint32_t *s_sc = reinterpret_cast<uint32_t *>(smem + kStages * kDownStage);  // [kMaxSteps][128]
-    __shared__ __align__(8) uint64_t full[kStages], empty[kStages], done, scales_ready;
+    __shared__ __align__(8) uint64_t full[S], empty[S], done;
     __shared__ uint32_t tslot;
     __shared__ int s_last;
     __shared__ int s_slot[kMaxExperts];
@@ -460,25 +430,20 @@ __global__ void __launch_bounds__(kRoleThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_act = a.counts[2];
     const int tile = blockIdx.x / a.KS, ks = blockIdx.x - tile * a.KS;
-    const int nksI = (a.I + 127) / 128;
+    const int nksI = (a.I + 127) / 128, ntH = (a.H + 127) / 128;
     const int total = n_act * nksI;
     const int g0 = ks * total / a.KS, g1 = (ks + 1) * total / a.KS, nsteps = g1 - g0;
     const bool ragged = (a.I % 128) != 0;
     const int row0 = tile * 128;
-    if (nsteps > kMaxSteps) {
-        if (threadIdx.x == 0) atomicExch(a.err, kErrSteps);
-        return;
-    }
-    for (int i = threadIdx.x; i < n_act; i += kRoleThreads) s_slot[i] = a.act_slot[i];
+    for (int i = threadIdx.x; i < n_act; i += kThreads) s_slot[i] = a.act_slot[i];
 
-    if (warp == 1) tmem_alloc(&tslot, kTmemCols);
+    if (warp == 1) tmem_alloc(&tslot, kDownTmem);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         mbar_init(&done, 1);
-        mbar_init(&scales_ready, 128);
         fence_barrier_init();
         tma_prefetch_desc(&mapD);
         tma_prefetch_desc(&mapH);
@@ -487,106 +452,83 @@ __global__ void __launch_bounds__(kRoleThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = tslot;
-    const uint32_t tD = tbase, tSFa = tbase + 32, tSFb = tbase + 32 + 4 * kMaxSteps;
+    const uint32_t tD = tbase, tSF = tbase + 32;  // per stage: 8 scale columns
 
-    bool ok = true;
     if (warp == 0) {
+        bool ok = true;
         for (int i = 0; i < nsteps && ok; ++i) {
-            const int st = i % kStages;
+            const int st = i % S;
             const int g = g0 + i, e = g / nksI, s = g - e * nksI;
-            if (lane == 0) ok = mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1, a.err, kErrEmpty);
+            if (lane == 0) ok = mbar_wait(&empty[st], ((i / S) & 1) ^ 1, a.err, kErrEmpty);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             uint8_t *sA = smem + st * kDownStage;
+            uint8_t *sAt = sA + kTileA + kB;
+            const int slot = s_slot[e];
             const bool tail = ragged && s == nksI - 1;
-            if (tail)
-                load_tail_tile(sA, a.bank + (size_t)s_slot[e] * a.expert_bytes + a.off_d_codes, a.H, row0, a.I, s);
+            if (tail) load_tail_tile(sA, a.bank + (size_t)slot * a.expert_bytes + a.off_d_codes, a.H, row0, a.I, s);
             if (lane == 0) {
-                mbar_expect_tx(&full[st], tail ? (uint32_t)kB : kTx);
-                if (!tail) tma_load_3d(&mapD, &full[st], sA, s * 128, row0, s_slot[e]);
+                mbar_expect_tx(&full[st], tail ? kTxTail : kTxFull);
+                if (!tail) tma_load_3d(&mapD, &full[st], sA, s * 128, row0, slot);
                 tma_load_3d(&mapH, &full[st], sA + kTileA, s * 128, 0, e);
+                const uint8_t *dat = a.atoms + (size_t)slot * a.atom_slot_bytes + a.atom_off_d +
+                                     ((size_t)tile * nksI + s) * kAtom;
+                bulk_copy(sAt, dat, kAtom, &full[st]);
+                bulk_copy(sAt + kAtom, a.hat + ((size_t)e * nksI + s) * kAtom, kAtom, &full[st]);
             }
             __syncwarp();
         }
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = mx_idesc(kFmtE2M1, kFmtE4M3, NB);
-            ok = mbar_wait(&scales_ready, 0, a.err, kErrScales);
-            tc_fence_after();
+            bool ok = true;
             for (int i = 0; i < nsteps && ok; ++i) {
-                const int st = i % kStages;
-                ok = mbar_wait(&full[st], (i / kStages) & 1, a.err, kErrFull);
+                const int st = i % S;
+                ok = mbar_wait(&full[st], (i / S) & 1, a.err, kErrFull);
                 if (!ok) break;
                 tc_fence_after();
+                uint8_t *sA = smem + st * kDownStage;
+                uint8_t *sAt = sA + kTileA + kB;
+                const uint32_t sfa = tSF + 8 * st, sfb = sfa + 4;
+                atom_to_tmem(sfa, sAt);
+                atom_to_tmem(sfb, sAt + kAtom);
                 const int s = (g0 + i) % nksI;
-                const uint32_t aA = smem_u32(smem + st * kDownStage), aB = aA + kTileA;
-                const bool tail = ragged && s == nksI - 1;
-                const int nk = tail ? ((a.I - s * 128) / 32) : 4;
+                const uint32_t aA = smem_u32(sA), aB = aA + kTileA;
+                const int nk = (ragged && s == nksI - 1) ? 2 : 4;
                 for (int kk = 0; kk < nk; ++kk) {
                     const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-                    mma_mx(tD, sw128_desc(aA + kk * 32), sw128_desc(aB + kk * 32), idesc, kk, tSFa + 4 * i,
-                           tSFb + 4 * i, acc);
+                    mma_mx(tD, sw128_desc(aA + kk * 32), sw128_desc(aB + kk * 32), idesc, kk, sfa, sfb, acc);
                 }
                 mma_commit(&empty[st]);
             }
             mma_commit(&done);
         }
         __syncwarp();
-    } else {
-        const int r = threadIdx.x - kScaleWarp0 * 32;
-        uint32_t w[kMaxSteps];
-#pragma unroll
-        for (int i = 0; i < kMaxSteps; ++i) {
-            if (i < nsteps) {
-                const int g = g0 + i, e = g / nksI, s = g - e * nksI;
-                const uint8_t *expert = a.bank + (size_t)s_slot[e] * a.expert_bytes;
-                w[i] = weight_scale_word(expert + a.off_d_scales, a.H, a.I / 32, row0 + r, s);
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < kMaxSteps; ++i)
-            if (i < nsteps) s_sc[i * 128 + r] = w[i];
-        named_sync_scale_warps();
-        store_weight_scales(tSFa, s_sc, nsteps);
-        for (int i = 0; i < nsteps; ++i) {
-            const int g = g0 + i, e = g / nksI, s = g - e * nksI;
-            store_operand_scales(tSFb + 4 * i, a.hs + (size_t)e * NB * a.SPI, a.SPI, NB, s);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&scales_ready);
     }
 
-    const bool epi = warp >= kScaleWarp0;
-    const int quad = warp & 3;
-    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const int rloc = quad * 32 + lane;
-    const int row = row0 + rloc;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const int rloc = warp * 32 + lane, row = row0 + rloc;
     const int M = a.M;
     float d[kDecodeMaxTokens * T];
 #pragma unroll
     for (int c = 0; c < kDecodeMaxTokens * T; ++c) d[c] = 0.f;
-    if (epi) {
-        const bool got = mbar_wait(&done, 0, a.err, kErrDone);
-        tc_fence_after();
-        if (got && nsteps > 0) {
-            uint32_t rr[8];
+    const bool got = mbar_wait(&done, 0, a.err, kErrDone);
+    tc_fence_after();
+    if (got && nsteps > 0) {
+        uint32_t rr[8];
 #pragma unroll
-            for (int c8 = 0; c8 < (kDecodeMaxTokens * T + 7) / 8; ++c8) {
-                if (8 * c8 < M * T) {
-                    tmem_ld8(tD + lane_off + 8 * c8, rr);
-                    tmem_ld_wait();
+        for (int c8 = 0; c8 < kDecodeMaxTokens * T / 8; ++c8) {
+            if (8 * c8 < M * T) {
+                tmem_ld8(tD + lane_off + 8 * c8, rr);
+                tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        if (8 * c8 + j < kDecodeMaxTokens * T) d[8 * c8 + j] = __uint_as_float(rr[j]);
-                }
+                for (int j = 0; j < 8; ++j) d[8 * c8 + j] = __uint_as_float(rr[j]);
             }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) tmem_dealloc(tbase, kTmemCols);
-    if (!epi) return;
+    if (warp == 1) tmem_dealloc(tbase, kDownTmem);
 
     if (a.KS > 1) {
         float *mine = a.part + ((size_t)tile * a.KS + ks) * kTcPartDown;
@@ -594,12 +536,12 @@ __global__ void __launch_bounds__(kRoleThreads, 1)
         for (int c = 0; c < kDecodeMaxTokens * T; ++c)
             if (c < M * T) mine[c * 128 + rloc] = d[c];
         __threadfence();
-        named_sync_scale_warps();
-        if (threadIdx.x == kScaleWarp0 * 32) s_last = atomicAdd(&a.tile_ctr[tile], 1u) == (unsigned)(a.KS - 1);
-        named_sync_scale_warps();
+        __syncthreads();
+        if (threadIdx.x == 0) s_last = atomicAdd(&a.tile_ctr[tile], 1u) == (unsigned)(a.KS - 1);
+        __syncthreads();
         if (!s_last) return;
         __threadfence();
-        if (threadIdx.x == kScaleWarp0 * 32) a.tile_ctr[tile] = 0u;
+        if (threadIdx.x == 0) a.tile_ctr[tile] = 0u;
 #pragma unroll
         for (int c = 0; c < kDecodeMaxTokens * T; ++c) d[c] = 0.f;
         for (int k = 0; k < a.KS; ++k) {
@@ -609,6 +551,7 @@ __global__ void __launch_bounds__(kRoleThreads, 1)
                 if (c < M * T) d[c] += __ldcg(p + c * 128 + rloc);
         }
     }
+    (void)ntH;
     if (row < a.H) {
 #pragma unroll
         for (int t = 0; t < kDecodeMaxTokens; ++t) {
@@ -631,23 +574,49 @@ void set_smem(K kernel, int bytes) {
 
 }  // namespace
 
-// stages + the regrouped weight scales (one [kMaxSteps][128] word table per weight matrix) + alignment slack
-int tc_gateup_smem() { return kStages * kGateStage + 2 * kMaxSteps * 128 * 4 + 1024; }
-int tc_down_smem() { return kStages * kDownStage + kMaxSteps * 128 * 4 + 1024; }
+int tc_gateup_smem() { return kGateStages * kGateStage + 1024; }
+int tc_down_smem() { return kDownStages * kDownStage + 1024; }
 
-void launch_quantize_x(const uint16_t *x, int M, int H, uint8_t *xq, int Hpad, uint8_t *xs, int SP, cudaStream_t s) {
+TcAtomLayout tc_atom_layout(int H, int I) {
+    TcAtomLayout l;
+    l.ntI = (I + 127) / 128;
+    l.ntH = (H + 127) / 128;
+    l.nks = (H + 127) / 128;
+    l.nksI = (I + 127) / 128;
+    l.off_g = 0;
+    l.off_u = (size_t)l.ntI * l.nks * kAtom;
+    l.off_d = 2 * l.off_u;
+    l.slot_bytes = l.off_d + (size_t)l.ntH * l.nksI * kAtom;
+    return l;
+}
+
+void launch_build_weight_atoms(const uint8_t *expert, const ExpertGeometry &g, uint8_t *atoms, cudaStream_t s) {
+    const TcAtomLayout l = tc_atom_layout(g.H, g.I);
+    const int na = l.ntI * l.nks, nd = l.ntH * l.nksI;
+    build_weight_atoms_kernel<<<(na + 7) / 8, 256, 0, s>>>(expert + g.off_wg_scales, g.I, g.H / 32, atoms + l.off_g,
+                                                           l.ntI, l.nks);
+    build_weight_atoms_kernel<<<(na + 7) / 8, 256, 0, s>>>(expert + g.off_wu_scales, g.I, g.H / 32, atoms + l.off_u,
+                                                           l.ntI, l.nks);
+    build_weight_atoms_kernel<<<(nd + 7) / 8, 256, 0, s>>>(expert + g.off_wd_scales, g.H, g.I / 32, atoms + l.off_d,
+                                                           l.ntH, l.nksI);
+}
+
+void launch_quantize_x(const uint16_t *x, int M, int H, uint8_t *xq, int Hpad, uint8_t *xat, cudaStream_t s) {
     const int tasks = M * (H / 32);
-    quantize_x_kernel<<<(tasks + 7) / 8, 256, 0, s>>>(x, M, H, xq, Hpad, xs, SP);
+    quantize_x_kernel<<<(tasks + 7) / 8, 256, 0, s>>>(x, M, H, xq, Hpad, xat);
 }
 
 void launch_gateup_tc(const TcLaunch &L, cudaStream_t s) {
+    const TcAtomLayout l = tc_atom_layout(L.geo.H, L.geo.I);
     GateUpArgs a{};
     a.bank = L.bank;
+    a.atoms = L.atoms;
     a.expert_bytes = L.geo.expert_bytes;
+    a.atom_slot_bytes = l.slot_bytes;
     a.off_g_codes = L.geo.off_wg_codes;
-    a.off_g_scales = L.geo.off_wg_scales;
     a.off_u_codes = L.geo.off_wu_codes;
-    a.off_u_scales = L.geo.off_wu_scales;
+    a.atom_off_g = l.off_g;
+    a.atom_off_u = l.off_u;
     a.H = L.geo.H;
     a.I = L.geo.I;
     a.M = L.M;
@@ -658,46 +627,44 @@ void launch_gateup_tc(const TcLaunch &L, cudaStream_t s) {
     a.act_cnt = L.act_cnt;
     a.hot_token = L.hot_token;
     a.hot_w = L.hot_w;
-    a.xs = L.xs;
-    a.SPH = L.SPH;
+    a.xat = L.xat;
     a.hq = L.hq;
-    a.hs = L.hs;
+    a.hat = L.hat;
     a.Ipad = L.Ipad;
-    a.SPI = L.SPI;
     a.part = L.part;
     a.tile_ctr = L.tile_ctr_gateup;
     a.err = L.err;
-    const int ntile = (L.geo.I + 127) / 128;
-    const int grid = L.n_act_max * ntile * L.ks_gateup;
+    const int grid = L.n_act_max * l.ntI * L.ks_gateup;
     static bool cfg = false;
     if (!cfg) set_smem(gateup_tc_kernel, tc_gateup_smem()), cfg = true;
-    gateup_tc_kernel<<<grid, kRoleThreads, tc_gateup_smem(), s>>>(*L.mapG, *L.mapU, *L.mapX, a);
+    gateup_tc_kernel<<<grid, kThreads, tc_gateup_smem(), s>>>(*L.mapG, *L.mapU, *L.mapX, a);
 }
 
 void launch_down_tc(const TcLaunch &L, cudaStream_t s) {
+    const TcAtomLayout l = tc_atom_layout(L.geo.H, L.geo.I);
     DownArgs a{};
     a.bank = L.bank;
+    a.atoms = L.atoms;
     a.expert_bytes = L.geo.expert_bytes;
+    a.atom_slot_bytes = l.slot_bytes;
     a.off_d_codes = L.geo.off_wd_codes;
-    a.off_d_scales = L.geo.off_wd_scales;
+    a.atom_off_d = l.off_d;
     a.H = L.geo.H;
     a.I = L.geo.I;
     a.M = L.M;
     a.KS = L.ks_down;
     a.counts = L.counts;
     a.act_slot = L.act_slot;
-    a.hs = L.hs;
-    a.Ipad = L.Ipad;
-    a.SPI = L.SPI;
+    a.hat = L.hat;
     a.out = L.out;
     a.out_f32 = L.out_f32;
     a.part = L.part_down;
     a.tile_ctr = L.tile_ctr_down;
     a.err = L.err;
-    const int grid = ((L.geo.H + 127) / 128) * L.ks_down;
+    const int grid = l.ntH * L.ks_down;
     static bool cfg = false;
     if (!cfg) set_smem(down_tc_kernel, tc_down_smem()), cfg = true;
-    down_tc_kernel<<<grid, kRoleThreads, tc_down_smem(), s>>>(*L.mapD, *L.mapH, a);
+    down_tc_kernel<<<grid, kThreads, tc_down_smem(), s>>>(*L.mapD, *L.mapH, a);
 }
 
 }  // namespace moe

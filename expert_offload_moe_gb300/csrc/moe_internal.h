@@ -82,16 +82,28 @@ struct DecodeParams {
 };
 
 // Tensor-core decode path (moe_decode_tc.cu).
+constexpr int kTcAtomBytes = 512;   // block scales of a 128-row tile x 128-column k-step
+constexpr int kTcXRows = 16;        // rows of the x-term operand: 2 terms x 8 tokens
+constexpr int kTcHRows = 32;        // rows of the w*h-term operand: 4 terms x 8 tokens
+constexpr int kTcPartGateup = 2 * 2 * kDecodeMaxTokens * 128;  // floats per gate/up split partial
+constexpr int kTcPartDown = kDecodeMaxTokens * 4 * 128;         // floats per down split partial
+
+// Weight scale atoms of one slot: gate [ntI][nks], up [ntI][nks], down [ntH][nksI], 512 bytes each.
+struct TcAtomLayout {
+    int ntI, ntH, nks, nksI;
+    size_t off_g, off_u, off_d, slot_bytes;
+};
+TcAtomLayout tc_atom_layout(int H, int I);
+
 struct TcLaunch {
-    const uint8_t *bank;
+    const uint8_t *bank, *atoms;  // slot (or staging) bank and its weight atoms
     ExpertGeometry geo;
     int M, n_act_max, ks_gateup, ks_down;
     const int32_t *counts, *act_slot, *act_off, *act_cnt, *hot_token;
     const float *hot_w;
-    const uint8_t *xs;  // x-term scales [16][SPH]
-    int SPH;
-    uint8_t *hq, *hs;   // w*h terms [n_act_max][32][Ipad], scales [n_act_max][32][SPI]
-    int Ipad, SPI;
+    const uint8_t *xat;           // x-term atoms [nks][512]
+    uint8_t *hq, *hat;            // w*h terms [n_act_cap][32][Ipad], atoms [n_act_cap][nksI][512]
+    int Ipad;
     float *part, *part_down;
     unsigned *tile_ctr_gateup, *tile_ctr_down;
     int *err;
@@ -100,13 +112,8 @@ struct TcLaunch {
     const CUtensorMap *mapG, *mapU, *mapX, *mapD, *mapH;
 };
 
-constexpr int kTcMaxSteps = 16;     // k-steps of 128 per CTA (tensor memory budget)
-constexpr int kTcXRows = 16;        // rows of the x-term operand
-constexpr int kTcHRows = 32;        // rows of the w*h-term operand
-constexpr int kTcPartGateup = 2 * 2 * kDecodeMaxTokens * 128;  // floats per gate/up split partial
-constexpr int kTcPartDown = kDecodeMaxTokens * 4 * 128;         // floats per down split partial
-
-void launch_quantize_x(const uint16_t *x, int M, int H, uint8_t *xq, int Hpad, uint8_t *xs, int SP, cudaStream_t s);
+void launch_build_weight_atoms(const uint8_t *expert, const ExpertGeometry &g, uint8_t *atoms, cudaStream_t s);
+void launch_quantize_x(const uint16_t *x, int M, int H, uint8_t *xq, int Hpad, uint8_t *xat, cudaStream_t s);
 void launch_gateup_tc(const TcLaunch &L, cudaStream_t s);
 void launch_down_tc(const TcLaunch &L, cudaStream_t s);
 

@@ -95,8 +95,10 @@ struct moe_layer {
     // tensor-core decode path: operand buffers, split-K scratch, tensor maps
     bool tc = false;
     int n_act_cap = 0;  // most active experts a decode call can have: min(S, 8 k)
-    int Hpad = 0, Ipad = 0, SPH = 0, SPI = 0;
-    uint8_t *xq = nullptr, *xs = nullptr, *hq = nullptr, *hs = nullptr;
+    int Hpad = 0, Ipad = 0;
+    moe::TcAtomLayout atl{};
+    uint8_t *atoms = nullptr;  // weight scale atoms of every slot [S][atl.slot_bytes]
+    uint8_t *xq = nullptr, *xat = nullptr, *hq = nullptr, *hat = nullptr;
     float *part = nullptr, *part_down = nullptr;
     unsigned *ctr_gateup = nullptr, *ctr_down = nullptr;
     int *err = nullptr;
@@ -124,6 +126,7 @@ void release(moe_layer *L) {
     cudaFree(L->dev_block);
     cudaFree(L->h);
     cudaFree(L->tc_block);
+    cudaFree(L->atoms);
     if (L->pinned_block) cudaFreeHost(L->pinned_block);
     for (auto e : {L->ev_fork, L->ev_route, L->ev_fence})
         if (e) cudaEventDestroy(e);
@@ -188,13 +191,12 @@ int encode_map(CUtensorMap *m, CUtensorMapDataType type, const void *base, uint6
     return MOE_OK;
 }
 
-// K splits: the largest split that keeps one wave of CTAs, at least enough splits that no CTA
-// takes more than kTcMaxSteps k-steps of 128.
+// K splits: enough CTAs for about two per SM (the kernels are sized to fit two), but at least
+// 4 k-steps of 128 per CTA so the pipeline has something to overlap.
 int choose_splits(int base_units, int steps, int num_sms) {
-    const int ks_min = (steps + moe::kTcMaxSteps - 1) / moe::kTcMaxSteps;
-    int ks = ks_min;
-    for (int k = ks_min; k <= steps; ++k)
-        if ((long)base_units * k <= num_sms) ks = k;
+    int ks = (2 * num_sms) / (base_units > 0 ? base_units : 1);
+    const int ks_max = steps / 4 > 1 ? steps / 4 : 1;
+    if (ks > ks_max) ks = ks_max;
     return ks < 1 ? 1 : ks;
 }
 
@@ -211,15 +213,23 @@ int tc_splits_down(const moe_layer *L, int M) {
     return choose_splits((L->d.hidden + 127) / 128, act_cap(L, M) * ((L->d.inter + 127) / 128), L->num_sms);
 }
 
+// Weight scale atoms of one slot, rebuilt whenever an expert lands in it (stream-ordered after the copy).
+int build_slot_atoms(moe_layer *L, int slot, cudaStream_t st) {
+    if (!L->tc) return MOE_OK;
+    moe::launch_build_weight_atoms(L->slots + (size_t)slot * L->geo.expert_bytes, L->geo,
+                                   L->atoms + (size_t)slot * L->atl.slot_bytes, st);
+    CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+}
+
 // Buffers and tensor maps of the tensor-core decode path.
 int tc_setup(moe_layer *L, cudaStream_t st) {
     const int H = L->d.hidden, I = L->d.inter;
     L->n_act_cap = act_cap(L, moe::kDecodeMaxTokens);
     L->Hpad = (H + 127) / 128 * 128;
     L->Ipad = (I + 127) / 128 * 128;
-    L->SPH = (H / 32 + 15) / 16 * 16;
-    L->SPI = (I / 32 + 15) / 16 * 16;
-    const int ntI = (I + 127) / 128, ntH = (H + 127) / 128;
+    L->atl = moe::tc_atom_layout(H, I);
+    const int ntI = L->atl.ntI, ntH = L->atl.ntH;
     size_t units_g = 0, units_d = 0;
     for (int M = 1; M <= moe::kDecodeMaxTokens; ++M) {
         const size_t ug = (size_t)act_cap(L, M) * ntI * tc_splits_gateup(L, M);
@@ -228,9 +238,9 @@ int tc_setup(moe_layer *L, cudaStream_t st) {
         units_d = ud > units_d ? ud : units_d;
     }
     const size_t sz[] = {(size_t)moe::kTcXRows * L->Hpad,
-                         (size_t)moe::kTcXRows * L->SPH,
+                         (size_t)L->atl.nks * moe::kTcAtomBytes,
                          (size_t)L->n_act_cap * moe::kTcHRows * L->Ipad,
-                         (size_t)L->n_act_cap * moe::kTcHRows * L->SPI,
+                         (size_t)L->n_act_cap * L->atl.nksI * moe::kTcAtomBytes,
                          units_g * moe::kTcPartGateup * sizeof(float),
                          units_d * moe::kTcPartDown * sizeof(float),
                          (size_t)L->n_act_cap * ntI * sizeof(unsigned),
@@ -239,22 +249,24 @@ int tc_setup(moe_layer *L, cudaStream_t st) {
     size_t total = 0;
     for (size_t s : sz) total += align_up(s, 256);
     cudaError_t e = cudaMalloc(&L->tc_block, total);
+    if (e == cudaSuccess) e = cudaMalloc(&L->atoms, (size_t)L->d.num_slots * L->atl.slot_bytes);
     if (e != cudaSuccess) {
         cudaGetLastError();
-        return fail(e == cudaErrorMemoryAllocation ? MOE_ENOMEM : MOE_ECUDA, "tensor-core scratch: %s",
+        return fail(e == cudaErrorMemoryAllocation ? MOE_ENOMEM : MOE_ECUDA, "tensor-core buffers: %s",
                     cudaGetErrorString(e));
     }
     char *p = static_cast<char *>(L->tc_block);
-    void **dst[] = {(void **)&L->xq, (void **)&L->xs, (void **)&L->hq, (void **)&L->hs, (void **)&L->part,
+    void **dst[] = {(void **)&L->xq, (void **)&L->xat, (void **)&L->hq, (void **)&L->hat, (void **)&L->part,
                     (void **)&L->part_down, (void **)&L->ctr_gateup, (void **)&L->ctr_down, (void **)&L->err};
     for (size_t i = 0; i < sizeof(sz) / sizeof(sz[0]); ++i) {
         *dst[i] = p;
         p += align_up(sz[i], 256);
     }
-    // operands start at zero; their scale padding (k-blocks past K) must stay finite: 2^0
+    // operands start at zero; scale bytes never written (rows or k-blocks past the data) stay finite: 2^0
     CUDA_TRY(cudaMemsetAsync(L->tc_block, 0, total, st));
-    CUDA_TRY(cudaMemsetAsync(L->xs, 0x7f, sz[1], st));
-    CUDA_TRY(cudaMemsetAsync(L->hs, 0x7f, sz[3], st));
+    CUDA_TRY(cudaMemsetAsync(L->xat, 0x7f, sz[1], st));
+    CUDA_TRY(cudaMemsetAsync(L->hat, 0x7f, sz[3], st));
+    CUDA_TRY(cudaMemsetAsync(L->atoms, 0x7f, (size_t)L->d.num_slots * L->atl.slot_bytes, st));
 
     const moe::ExpertGeometry &g = L->geo;
     const int S = L->d.num_slots;
@@ -438,6 +450,15 @@ int moe_layer_create(const moe_layer_desc *desc, const float *router_w_dev, cons
         if (e2s[e] >= 0)
             CREATE_TRY(cudaMemcpyAsync(L->slots + (size_t)e2s[e] * eb, host_bank + (size_t)e * eb, eb,
                                        cudaMemcpyHostToDevice, st));
+    for (int e = 0; e < E; ++e)
+        if (e2s[e] >= 0) {
+            const int rc = build_slot_atoms(L, e2s[e], st);
+            if (rc) {
+                cudaStreamSynchronize(st);
+                release(L);
+                return rc;
+            }
+        }
     CREATE_TRY(cudaStreamSynchronize(st));
 #undef CREATE_TRY
     *out = L;
@@ -540,12 +561,11 @@ int moe_forward_slots(moe_layer *L, const void *x_dev, void *out_dev, int32_t M,
         t.act_cnt = L->rb.act_cnt;
         t.hot_token = L->rb.hot_token;
         t.hot_w = L->rb.hot_w;
-        t.xs = L->xs;
-        t.SPH = L->SPH;
+        t.atoms = L->atoms;
+        t.xat = L->xat;
         t.hq = L->hq;
-        t.hs = L->hs;
+        t.hat = L->hat;
         t.Ipad = L->Ipad;
-        t.SPI = L->SPI;
         t.part = L->part;
         t.part_down = L->part_down;
         t.tile_ctr_gateup = L->ctr_gateup;
@@ -559,7 +579,7 @@ int moe_forward_slots(moe_layer *L, const void *x_dev, void *out_dev, int32_t M,
         t.mapD = &L->mapD;
         t.mapH = &L->mapH;
         CUDA_TRY(prof_mark(L, 1, st));
-        moe::launch_quantize_x(p.x, M, L->d.hidden, L->xq, L->Hpad, L->xs, L->SPH, st);
+        moe::launch_quantize_x(p.x, M, L->d.hidden, L->xq, L->Hpad, L->xat, st);
         moe::launch_gateup_tc(t, st);
         CUDA_TRY(cudaGetLastError());
         CUDA_TRY(prof_mark(L, 1, st));
@@ -658,6 +678,7 @@ int moe_cache_update(moe_layer *L, void *stream, int32_t *n_refills_out) {
     for (int i = 0; i < n; ++i) {
         CUDA_TRY(cudaMemcpyAsync(L->slots + (size_t)ps[i] * eb, L->host_bank + (size_t)pe[i] * eb, eb,
                                  cudaMemcpyHostToDevice, L->h2d));
+        if (int rc = build_slot_atoms(L, ps[i], L->h2d)) return rc;
         L->stats[0] += 1;
         L->stats[1] += (int64_t)eb;
         if (L->d.visibility == MOE_VIS_DETERMINISTIC) {
