@@ -64,46 +64,6 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
 
 __device__ __forceinline__ float silu(float g) { return g / (1.f + expf(-g)); }
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-
-// floor(log2(a)) for a finite a > 0
-__device__ __forceinline__ int floor_log2(float a) {
-    const uint32_t u = __float_as_uint(a);
-    const int e = (int)((u >> 23) & 0xff);
-    if (e) return e - 127;
-    return -127 - (__clz(u & 0x7fffff) - 9);  // subnormal
-}
-
-// One term of the exact E4M3 split of a 32-value block held one value per lane:
-// returns this lane's code, updates the residual, and gives the block's E8M0 byte.
-__device__ __forceinline__ uint8_t split_term(float &res, uint32_t &scale_byte) {
-    const float amax = warp_max(fabsf(res));
-    const int X = amax > 0.f ? max(floor_log2(amax) - 7, -127) : -127;  // |res| / 2^X < 256: no saturation
-    scale_byte = e8m0_byte(X);
-    const float inv = e8m0_value(e8m0_byte(-X));
-    const float mine = res * inv;
-    const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
-    const int lane = threadIdx.x & 31;
-    const uint16_t pk = (lane & 1) ? f32x2_to_e4m3x2(other, mine) : f32x2_to_e4m3x2(mine, other);
-    const uint8_t code = (lane & 1) ? (uint8_t)(pk >> 8) : (uint8_t)(pk & 0xff);
-    float lo, hi;
-    e4m3x2_to_f32x2(pk, lo, hi);
-    res = res - ((lane & 1) ? hi : lo) * e8m0_value(scale_byte);
-    return code;
-}
-
-// 1-D bulk copy global -> shared completing on an mbarrier (16-byte aligned, multiple of 16 bytes).
-__device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-
 // Scale atom (512 bytes in smem, 32 rows of 16 bytes) -> 4 TMEM columns in every lane quadrant.
 __device__ __forceinline__ void atom_to_tmem(uint32_t tcol, const void *atom) {
     uint64_t d = 0;
@@ -126,7 +86,7 @@ __device__ __forceinline__ void load_tail_tile(uint8_t *dst, const uint8_t *code
         const int i = lane + 32 * j, r = i / kUnits, u = i % kUnits;
         v[j] = make_uint2(0u, 0u);
         if (row0 + r < rows)
-            v[j] = __ldg(reinterpret_cast<const uint2 *>(codes + (size_t)(row0 + r) * (K / 2) + kstep * 64 + u * 8));
+            v[j] = __ldcs(reinterpret_cast<const uint2 *>(codes + (size_t)(row0 + r) * (K / 2) + kstep * 64 + u * 8));
     }
 #pragma unroll
     for (int j = 0; j < kPerLane; ++j) {
@@ -164,27 +124,9 @@ __global__ void __launch_bounds__(256) build_weight_atoms_kernel(const uint8_t *
     *reinterpret_cast<uint4 *>(atoms + (size_t)atom * kAtom + m0 * 16) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// x terms: xq[t * 2 + term][Hpad] E4M3 codes and their scales in atoms xat[step][512] (row n = t*2+term
-// at byte n*16 + kb); one warp per 32-element block.
-__global__ void __launch_bounds__(256) quantize_x_kernel(const uint16_t *x, int M, int H, uint8_t *xq, int Hpad,
-                                                         uint8_t *xat) {
-    const int lane = threadIdx.x & 31;
-    const int nb = H / 32;
-    const int task = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (task >= M * nb) return;
-    const int t = task / nb, b = task - t * nb;
-    float res = __uint_as_float((uint32_t)x[(size_t)t * H + b * 32 + lane] << 16);
-#pragma unroll
-    for (int term = 0; term < 2; ++term) {
-        uint32_t sb;
-        const uint8_t code = split_term(res, sb);
-        const int n = t * 2 + term;
-        xq[(size_t)n * Hpad + b * 32 + lane] = code;
-        if (lane == 0) xat[(size_t)(b / 4) * kAtom + n * 16 + (b % 4)] = (uint8_t)sb;
-    }
-}
-
 namespace {
+
+constexpr int kMaxCluster = 8;  // K splits of one tile form a cluster (portable size)
 
 struct GateUpArgs {
     const uint8_t *bank, *atoms;  // slot bank; weight atoms of each slot
@@ -195,11 +137,10 @@ struct GateUpArgs {
     const uint8_t *xat;  // x atoms [nks][512]
     uint8_t *hq, *hat;   // w*h terms [n_act_cap][32][Ipad], atoms [n_act_cap][nksI][512]
     int Ipad;
-    float *part;
-    unsigned *tile_ctr;
     int *err;
 };
 
+// grid: (active expert, 128-row tile of I, K split), the K splits of a tile being one cluster.
 __global__ void __launch_bounds__(kThreads, 1)
     gateup_tc_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ CUtensorMap mapU,
                      const __grid_constant__ CUtensorMap mapX, GateUpArgs a) {
@@ -207,28 +148,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kB = NBX * 128;
     constexpr uint32_t kTxFull = 2 * kTileATx + kB + 3 * kAtom, kTxTail = kB + 3 * kAtom;
     constexpr int T = kHTerms;
+    constexpr int C = 2 * kDecodeMaxTokens;  // accumulator columns: 2 x terms per token
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     __shared__ __align__(8) uint64_t full[S], empty[S], done;
     __shared__ uint32_t tslot;
-    __shared__ int s_last;
+    __shared__ float s_wtok[kDecodeMaxTokens];  // routing weight of each token routed to this expert, else 0
+    __shared__ unsigned s_routed;               // bit t: token t is routed to this expert
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_act = a.counts[2];
     const int ntile = (a.I + 127) / 128;
-    const int aidx = blockIdx.x / (ntile * a.KS);
-    if (aidx >= n_act) return;
-    const int rem = blockIdx.x - aidx * ntile * a.KS;
-    const int tile = rem / a.KS, ks = rem - tile * a.KS;
+    const int KS = a.KS;
+    const int unit = blockIdx.x / KS, ks = blockIdx.x - unit * KS;
+    const int aidx = unit / ntile, tile = unit - aidx * ntile;
     const int nks = (a.H + 127) / 128;
-    const int k0 = ks * nks / a.KS, k1 = (ks + 1) * nks / a.KS, nsteps = k1 - k0;
+    const int k0 = ks * nks / KS, k1 = (ks + 1) * nks / KS, nsteps = k1 - k0;
     const bool ragged = (a.H % 128) != 0;
-    const int slot = a.act_slot[aidx];
-    const uint8_t *expert = a.bank + (size_t)slot * a.expert_bytes;
-    const uint8_t *gat = a.atoms + (size_t)slot * a.atom_slot_bytes + a.atom_off_g + (size_t)tile * nks * kAtom;
-    const uint8_t *uat = a.atoms + (size_t)slot * a.atom_slot_bytes + a.atom_off_u + (size_t)tile * nks * kAtom;
     const int row0 = tile * 128;
 
+    // setup that does not read the route kernel's results overlaps its tail
     if (warp == 1) tmem_alloc(&tslot, kGateTmem);
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -245,9 +183,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = tslot;
+    pdl_wait();  // routing and x terms are complete
+    pdl_trigger();
+    const int n_act = a.counts[2];
+    if (aidx >= n_act) {  // the whole cluster (one tile) leaves together
+        if (warp == 1) tmem_dealloc(tbase, kGateTmem);
+        return;
+    }
+    const int slot = a.act_slot[aidx];
+    const uint8_t *expert = a.bank + (size_t)slot * a.expert_bytes;
+    const uint8_t *gat = a.atoms + (size_t)slot * a.atom_slot_bytes + a.atom_off_g + (size_t)tile * nks * kAtom;
+    const uint8_t *uat = a.atoms + (size_t)slot * a.atom_slot_bytes + a.atom_off_u + (size_t)tile * nks * kAtom;
     const uint32_t tDg = tbase, tDu = tbase + 16, tSF = tbase + 32;  // per stage: 12 scale columns
 
     if (warp == 0) {
+        const uint64_t pol = l2_evict_first();
         bool ok = true;
         for (int i = 0; i < nsteps && ok; ++i) {
             const int st = i % S, kstep = k0 + i;
@@ -264,12 +214,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 mbar_expect_tx(&full[st], tail ? kTxTail : kTxFull);
                 if (!tail) {
-                    tma_load_3d(&mapG, &full[st], sA, kstep * 128, row0, slot);
-                    tma_load_3d(&mapU, &full[st], sA + kTileA, kstep * 128, row0, slot);
+                    tma_load_3d_hint(&mapG, &full[st], sA, kstep * 128, row0, slot, pol);
+                    tma_load_3d_hint(&mapU, &full[st], sA + kTileA, kstep * 128, row0, slot, pol);
                 }
                 tma_load_3d(&mapX, &full[st], sA + 2 * kTileA, kstep * 128, 0, 0);
-                bulk_copy(sAt, gat + (size_t)kstep * kAtom, kAtom, &full[st]);
-                bulk_copy(sAt + kAtom, uat + (size_t)kstep * kAtom, kAtom, &full[st]);
+                bulk_copy_hint(sAt, gat + (size_t)kstep * kAtom, kAtom, &full[st], pol);
+                bulk_copy_hint(sAt + kAtom, uat + (size_t)kstep * kAtom, kAtom, &full[st], pol);
                 bulk_copy(sAt + 2 * kAtom, a.xat + (size_t)kstep * kAtom, kAtom, &full[st]);
             }
             __syncwarp();
@@ -302,102 +252,119 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(&done);
         }
         __syncwarp();
+    } else if (warp == 2) {
+        // the epilogue's routing data, fetched while the weights stream
+        if (lane < kDecodeMaxTokens) s_wtok[lane] = 0.f;
+        const int off = a.act_off[aidx], cnt = a.act_cnt[aidx];
+        int t = -1;
+        float w = 0.f;
+        if (lane < cnt) {
+            t = a.hot_token[off + lane];
+            w = a.hot_w[off + lane];
+        }
+        __syncwarp();
+        if (t >= 0) s_wtok[t] = w;
+        const unsigned bits = __reduce_or_sync(0xffffffffu, t >= 0 ? 1u << t : 0u);
+        if (lane == 0) s_routed = bits;
     }
 
-    // ---------------- epilogue: every thread owns one row of the tile ----------------
+    // ---------------- epilogue: every thread owns one row of its CTA's partial ----------------
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const int rloc = warp * 32 + lane, row = row0 + rloc;
     const int M = a.M;
-    float g[2 * kDecodeMaxTokens], u[2 * kDecodeMaxTokens];
+    float g[C], u[C];
 #pragma unroll
-    for (int c = 0; c < 2 * kDecodeMaxTokens; ++c) g[c] = u[c] = 0.f;
+    for (int c = 0; c < C; ++c) g[c] = u[c] = 0.f;
     const bool got = mbar_wait(&done, 0, a.err, kErrDone);
     tc_fence_after();
     if (got) {
         uint32_t rr[8];
 #pragma unroll
-        for (int c8 = 0; c8 < 2; ++c8) {
-            tmem_ld8(tDg + lane_off + 8 * c8, rr);
-            tmem_ld_wait();
+        for (int c8 = 0; c8 < C / 8; ++c8) {
+            if (8 * c8 < 2 * M) {
+                tmem_ld8(tDg + lane_off + 8 * c8, rr);
+                tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 8; ++j) g[8 * c8 + j] = __uint_as_float(rr[j]);
-            tmem_ld8(tDu + lane_off + 8 * c8, rr);
-            tmem_ld_wait();
+                for (int j = 0; j < 8; ++j) g[8 * c8 + j] = __uint_as_float(rr[j]);
+                tmem_ld8(tDu + lane_off + 8 * c8, rr);
+                tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 8; ++j) u[8 * c8 + j] = __uint_as_float(rr[j]);
+                for (int j = 0; j < 8; ++j) u[8 * c8 + j] = __uint_as_float(rr[j]);
+            }
         }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) tmem_dealloc(tbase, kGateTmem);
 
-    if (a.KS > 1) {
-        // partials [unit][2][2 kDecodeMaxTokens][128], summed by the last CTA of the tile in split order
-        const int tile_id = aidx * ntile + tile;
-        float *mine = a.part + ((size_t)tile_id * a.KS + ks) * kTcPartGateup;
+    // K splits: partials meet in the cluster's shared memory; rank r finishes the 32-row groups
+    // r, r + KS, ... and sums the ranks in order 0..KS-1, so the result does not depend on timing.
+    int grp = warp;
+    float *red = reinterpret_cast<float *>(smem);  // [2][C][128], over the drained pipeline stages
+    if (KS > 1) {
+        const int rloc = warp * 32 + lane;
 #pragma unroll
-        for (int c = 0; c < 2 * kDecodeMaxTokens; ++c) {
+        for (int c = 0; c < C; ++c)
             if (c < 2 * M) {
-                mine[(0 * 2 * kDecodeMaxTokens + c) * 128 + rloc] = g[c];
-                mine[(1 * 2 * kDecodeMaxTokens + c) * 128 + rloc] = u[c];
+                red[c * 128 + rloc] = g[c];
+                red[(C + c) * 128 + rloc] = u[c];
             }
-        }
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0) s_last = atomicAdd(&a.tile_ctr[tile_id], 1u) == (unsigned)(a.KS - 1);
-        __syncthreads();
-        if (!s_last) return;
-        __threadfence();
-        if (threadIdx.x == 0) a.tile_ctr[tile_id] = 0u;
+        cluster_sync();
+        grp = ks + KS * warp;
+        if (grp < 4) {
+            const int rl = grp * 32 + lane;
 #pragma unroll
-        for (int c = 0; c < 2 * kDecodeMaxTokens; ++c) g[c] = u[c] = 0.f;
-        for (int k = 0; k < a.KS; ++k) {
-            const float *p = a.part + ((size_t)tile_id * a.KS + k) * kTcPartGateup;
+            for (int c = 0; c < C; ++c) g[c] = u[c] = 0.f;
+            for (int r = 0; r < KS; ++r) {
+                const uint32_t base = dsmem_addr(red, (uint32_t)r);
+                float gv[C], uv[C];
 #pragma unroll
-            for (int c = 0; c < 2 * kDecodeMaxTokens; ++c) {
-                if (c < 2 * M) {
-                    g[c] += __ldcg(p + (0 * 2 * kDecodeMaxTokens + c) * 128 + rloc);
-                    u[c] += __ldcg(p + (1 * 2 * kDecodeMaxTokens + c) * 128 + rloc);
+                for (int c = 0; c < C; ++c) {
+                    gv[c] = uv[c] = 0.f;
+                    if (c < 2 * M) {
+                        gv[c] = ld_dsmem(base + 4u * (c * 128 + rl));
+                        uv[c] = ld_dsmem(base + 4u * ((C + c) * 128 + rl));
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < C; ++c) {
+                    g[c] += gv[c];
+                    u[c] += uv[c];
                 }
             }
         }
     }
 
     // h = SiLU(g) u for the tokens routed to this expert; w h split into T E4M3 terms per 32-row block
-    const int off = a.act_off[aidx], cnt = a.act_cnt[aidx];
-    const int nksI = (a.I + 127) / 128;
-    uint8_t *hq = a.hq + (size_t)aidx * NBH * a.Ipad;
-    uint8_t *hat = a.hat + (size_t)aidx * nksI * kAtom;
-    float vt[kDecodeMaxTokens];
-#pragma unroll
-    for (int t = 0; t < kDecodeMaxTokens; ++t) vt[t] = 0.f;
-    for (int j = 0; j < cnt; ++j) {
-        const int t = a.hot_token[off + j];
-        const float w = a.hot_w[off + j];
-#pragma unroll
-        for (int tt = 0; tt < kDecodeMaxTokens; ++tt) {
-            if (tt == t) {
-                const float gg = g[2 * tt] + g[2 * tt + 1], uu = u[2 * tt] + u[2 * tt + 1];
-                vt[tt] = w * (silu(gg) * uu);
-            }
-        }
-    }
-    if (row < a.I) {  // whole 32-row blocks are in or out (I % 64 == 0)
-        const int kblock = row / 32;
+    if (grp < 4) {
+        const int row = row0 + grp * 32 + lane;
+        const int nksI = (a.I + 127) / 128;
+        uint8_t *hq = a.hq + (size_t)aidx * NBH * a.Ipad;
+        uint8_t *hat = a.hat + (size_t)aidx * nksI * kAtom;
+        const unsigned routed = s_routed;
+        float vt[kDecodeMaxTokens];
 #pragma unroll
         for (int t = 0; t < kDecodeMaxTokens; ++t) {
-            if (t >= M) break;
-            float res = vt[t];
+            const float gg = g[2 * t] + g[2 * t + 1], uu = u[2 * t] + u[2 * t + 1];
+            vt[t] = (routed >> t) & 1u ? s_wtok[t] * (silu(gg) * uu) : 0.f;
+        }
+        if (row < a.I) {  // whole 32-row groups are in or out (I % 64 == 0)
+            const int kblock = row / 32;
 #pragma unroll
-            for (int term = 0; term < T; ++term) {
-                uint32_t sb;
-                const uint8_t code = split_term(res, sb);
-                const int n = t * T + term;
-                hq[(size_t)n * a.Ipad + row] = code;
-                if (lane == 0) hat[(size_t)(kblock / 4) * kAtom + n * 16 + (kblock % 4)] = (uint8_t)sb;
+            for (int t = 0; t < kDecodeMaxTokens; ++t) {
+                if (t >= M) break;
+                float res = vt[t];
+#pragma unroll
+                for (int term = 0; term < T; ++term) {
+                    uint32_t sb;
+                    const uint8_t code = split_term(res, sb);
+                    const int n = t * T + term;
+                    hq[(size_t)n * a.Ipad + row] = code;
+                    if (lane == 0) hat[(size_t)(kblock / 4) * kAtom + n * 16 + (kblock % 4)] = (uint8_t)sb;
+                }
             }
         }
     }
+    if (KS > 1) cluster_sync();  // no CTA leaves while another still reads its shared memory
 }
 
 struct DownArgs {
@@ -408,11 +375,11 @@ struct DownArgs {
     const uint8_t *hat;  // [n_act_cap][nksI][512]
     void *out;
     int out_f32;
-    float *part;
-    unsigned *tile_ctr;
     int *err;
 };
 
+// grid: (128-row tile of H, K split over the concatenated (active expert, k-step) sequence), the K
+// splits of a tile being one cluster.
 __global__ void __launch_bounds__(kThreads, 1)
     down_tc_kernel(const __grid_constant__ CUtensorMap mapD, const __grid_constant__ CUtensorMap mapH, DownArgs a) {
     constexpr int S = kDownStages;
@@ -420,21 +387,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kB = NB * 128;
     constexpr uint32_t kTxFull = kTileATx + kB + 2 * kAtom, kTxTail = kB + 2 * kAtom;
     constexpr int T = kHTerms;
+    constexpr int C = kDecodeMaxTokens * T;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     __shared__ __align__(8) uint64_t full[S], empty[S], done;
     __shared__ uint32_t tslot;
-    __shared__ int s_last;
     __shared__ int s_slot[kMaxExperts];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_act = a.counts[2];
-    const int tile = blockIdx.x / a.KS, ks = blockIdx.x - tile * a.KS;
-    const int nksI = (a.I + 127) / 128, ntH = (a.H + 127) / 128;
-    const int total = n_act * nksI;
-    const int g0 = ks * total / a.KS, g1 = (ks + 1) * total / a.KS, nsteps = g1 - g0;
+    const int KS = a.KS;
+    const int tile = blockIdx.x / KS, ks = blockIdx.x - tile * KS;
+    const int nksI = (a.I + 127) / 128;
     const bool ragged = (a.I % 128) != 0;
     const int row0 = tile * 128;
+    // The routing (counts, slots) is complete: the gate/up grid waited for it before letting this grid
+    // launch.  Only the w*h terms come from the grid right before this one.
+    const int n_act = a.counts[2];
+    const int total = n_act * nksI;
+    const int g0 = ks * total / KS, g1 = (ks + 1) * total / KS, nsteps = g1 - g0;
     for (int i = threadIdx.x; i < n_act; i += kThreads) s_slot[i] = a.act_slot[i];
 
     if (warp == 1) tmem_alloc(&tslot, kDownTmem);
@@ -455,8 +425,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tD = tbase, tSF = tbase + 32;  // per stage: 8 scale columns
 
     if (warp == 0) {
+        // weights of the first stages are fetched before the gate/up grid has finished
+        const uint64_t pol = l2_evict_first();
+        const int npre = nsteps < S ? nsteps : S;
+        for (int i = 0; i < npre; ++i) {
+            const int g = g0 + i, e = g / nksI, s = g - e * nksI;
+            uint8_t *sA = smem + i * kDownStage;
+            const int slot = s_slot[e];
+            const bool tail = ragged && s == nksI - 1;
+            if (tail) load_tail_tile(sA, a.bank + (size_t)slot * a.expert_bytes + a.off_d_codes, a.H, row0, a.I, s);
+            if (lane == 0) {
+                mbar_expect_tx(&full[i], tail ? kTxTail : kTxFull);
+                if (!tail) tma_load_3d_hint(&mapD, &full[i], sA, s * 128, row0, slot, pol);
+                bulk_copy_hint(sA + kTileA + kB,
+                               a.atoms + (size_t)slot * a.atom_slot_bytes + a.atom_off_d +
+                                   ((size_t)tile * nksI + s) * kAtom,
+                               kAtom, &full[i], pol);
+            }
+            __syncwarp();
+        }
+        pdl_wait();
+        pdl_trigger();
+        if (lane == 0)
+            for (int i = 0; i < npre; ++i) {
+                const int g = g0 + i, e = g / nksI, s = g - e * nksI;
+                uint8_t *sA = smem + i * kDownStage;
+                tma_load_3d(&mapH, &full[i], sA + kTileA, s * 128, 0, e);
+                bulk_copy(sA + kTileA + kB + kAtom, a.hat + ((size_t)e * nksI + s) * kAtom, kAtom, &full[i]);
+            }
+        __syncwarp();
         bool ok = true;
-        for (int i = 0; i < nsteps && ok; ++i) {
+        for (int i = npre; i < nsteps && ok; ++i) {
             const int st = i % S;
             const int g = g0 + i, e = g / nksI, s = g - e * nksI;
             if (lane == 0) ok = mbar_wait(&empty[st], ((i / S) & 1) ^ 1, a.err, kErrEmpty);
@@ -469,55 +468,59 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tail) load_tail_tile(sA, a.bank + (size_t)slot * a.expert_bytes + a.off_d_codes, a.H, row0, a.I, s);
             if (lane == 0) {
                 mbar_expect_tx(&full[st], tail ? kTxTail : kTxFull);
-                if (!tail) tma_load_3d(&mapD, &full[st], sA, s * 128, row0, slot);
+                if (!tail) tma_load_3d_hint(&mapD, &full[st], sA, s * 128, row0, slot, pol);
                 tma_load_3d(&mapH, &full[st], sA + kTileA, s * 128, 0, e);
-                const uint8_t *dat = a.atoms + (size_t)slot * a.atom_slot_bytes + a.atom_off_d +
-                                     ((size_t)tile * nksI + s) * kAtom;
-                bulk_copy(sAt, dat, kAtom, &full[st]);
+                bulk_copy_hint(sAt, a.atoms + (size_t)slot * a.atom_slot_bytes + a.atom_off_d +
+                                        ((size_t)tile * nksI + s) * kAtom,
+                               kAtom, &full[st], pol);
                 bulk_copy(sAt + kAtom, a.hat + ((size_t)e * nksI + s) * kAtom, kAtom, &full[st]);
             }
             __syncwarp();
         }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t idesc = mx_idesc(kFmtE2M1, kFmtE4M3, NB);
-            bool ok = true;
-            for (int i = 0; i < nsteps && ok; ++i) {
-                const int st = i % S;
-                ok = mbar_wait(&full[st], (i / S) & 1, a.err, kErrFull);
-                if (!ok) break;
-                tc_fence_after();
-                uint8_t *sA = smem + st * kDownStage;
-                uint8_t *sAt = sA + kTileA + kB;
-                const uint32_t sfa = tSF + 8 * st, sfb = sfa + 4;
-                atom_to_tmem(sfa, sAt);
-                atom_to_tmem(sfb, sAt + kAtom);
-                const int s = (g0 + i) % nksI;
-                const uint32_t aA = smem_u32(sA), aB = aA + kTileA;
-                const int nk = (ragged && s == nksI - 1) ? 2 : 4;
-                for (int kk = 0; kk < nk; ++kk) {
-                    const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-                    mma_mx(tD, sw128_desc(aA + kk * 32), sw128_desc(aB + kk * 32), idesc, kk, sfa, sfb, acc);
+    } else {
+        pdl_wait();  // out may still be read by earlier work in the stream
+        pdl_trigger();
+        if (warp == 1) {
+            if (lane == 0) {
+                const uint32_t idesc = mx_idesc(kFmtE2M1, kFmtE4M3, NB);
+                bool ok = true;
+                for (int i = 0; i < nsteps && ok; ++i) {
+                    const int st = i % S;
+                    ok = mbar_wait(&full[st], (i / S) & 1, a.err, kErrFull);
+                    if (!ok) break;
+                    tc_fence_after();
+                    uint8_t *sA = smem + st * kDownStage;
+                    uint8_t *sAt = sA + kTileA + kB;
+                    const uint32_t sfa = tSF + 8 * st, sfb = sfa + 4;
+                    atom_to_tmem(sfa, sAt);
+                    atom_to_tmem(sfb, sAt + kAtom);
+                    const int s = (g0 + i) % nksI;
+                    const uint32_t aA = smem_u32(sA), aB = aA + kTileA;
+                    const int nk = (ragged && s == nksI - 1) ? 2 : 4;
+                    for (int kk = 0; kk < nk; ++kk) {
+                        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                        mma_mx(tD, sw128_desc(aA + kk * 32), sw128_desc(aB + kk * 32), idesc, kk, sfa, sfb, acc);
+                    }
+                    mma_commit(&empty[st]);
                 }
-                mma_commit(&empty[st]);
+                mma_commit(&done);
             }
-            mma_commit(&done);
+            __syncwarp();
         }
-        __syncwarp();
     }
 
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const int rloc = warp * 32 + lane, row = row0 + rloc;
+    const int rloc = warp * 32 + lane;
     const int M = a.M;
-    float d[kDecodeMaxTokens * T];
+    float d[C];
 #pragma unroll
-    for (int c = 0; c < kDecodeMaxTokens * T; ++c) d[c] = 0.f;
+    for (int c = 0; c < C; ++c) d[c] = 0.f;
     const bool got = mbar_wait(&done, 0, a.err, kErrDone);
     tc_fence_after();
     if (got && nsteps > 0) {
         uint32_t rr[8];
 #pragma unroll
-        for (int c8 = 0; c8 < kDecodeMaxTokens * T / 8; ++c8) {
+        for (int c8 = 0; c8 < C / 8; ++c8) {
             if (8 * c8 < M * T) {
                 tmem_ld8(tD + lane_off + 8 * c8, rr);
                 tmem_ld_wait();
@@ -530,41 +533,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 1) tmem_dealloc(tbase, kDownTmem);
 
-    if (a.KS > 1) {
-        float *mine = a.part + ((size_t)tile * a.KS + ks) * kTcPartDown;
+    if (KS == 1) {
+        const int row = row0 + rloc;
+        if (row < a.H) {
 #pragma unroll
-        for (int c = 0; c < kDecodeMaxTokens * T; ++c)
-            if (c < M * T) mine[c * 128 + rloc] = d[c];
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0) s_last = atomicAdd(&a.tile_ctr[tile], 1u) == (unsigned)(a.KS - 1);
-        __syncthreads();
-        if (!s_last) return;
-        __threadfence();
-        if (threadIdx.x == 0) a.tile_ctr[tile] = 0u;
+            for (int t = 0; t < kDecodeMaxTokens; ++t) {
+                if (t >= M) break;
+                float v = 0.f;
 #pragma unroll
-        for (int c = 0; c < kDecodeMaxTokens * T; ++c) d[c] = 0.f;
-        for (int k = 0; k < a.KS; ++k) {
-            const float *p = a.part + ((size_t)tile * a.KS + k) * kTcPartDown;
-#pragma unroll
-            for (int c = 0; c < kDecodeMaxTokens * T; ++c)
-                if (c < M * T) d[c] += __ldcg(p + c * 128 + rloc);
+                for (int term = 0; term < T; ++term) v += d[t * T + term];
+                if (a.out_f32)
+                    reinterpret_cast<float *>(a.out)[(size_t)t * a.H + row] = v;
+                else
+                    reinterpret_cast<__nv_bfloat16 *>(a.out)[(size_t)t * a.H + row] = __float2bfloat16_rn(v);
+            }
         }
+        return;
     }
-    (void)ntH;
-    if (row < a.H) {
+    // K splits: partials meet in the cluster's shared memory; rank r finishes rows [128 r / KS, 128 (r+1) / KS)
+    // of every token, summing ranks 0..KS-1 in order (then the terms), so the result does not depend on timing.
+    float *red = reinterpret_cast<float *>(smem);  // [C][128], over the drained pipeline stages
 #pragma unroll
-        for (int t = 0; t < kDecodeMaxTokens; ++t) {
-            if (t >= M) break;
-            float v = 0.f;
+    for (int c = 0; c < C; ++c)
+        if (c < M * T) red[c * 128 + rloc] = d[c];
+    cluster_sync();
+    const int r0 = ks * 128 / KS, nrows = (ks + 1) * 128 / KS - r0;
+    for (int it = threadIdx.x; it < nrows * M; it += kThreads) {
+        const int t = it / nrows, rl = r0 + (it - t * nrows);
+        float pv[kMaxCluster][T];
 #pragma unroll
-            for (int term = 0; term < T; ++term) v += d[t * T + term];
+        for (int r = 0; r < kMaxCluster; ++r) {
+            if (r < KS) {
+                const uint32_t base = dsmem_addr(red, (uint32_t)r);
+#pragma unroll
+                for (int term = 0; term < T; ++term) pv[r][term] = ld_dsmem(base + 4u * ((t * T + term) * 128 + rl));
+            }
+        }
+        float v = 0.f;
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r)
+            if (r < KS)
+#pragma unroll
+                for (int term = 0; term < T; ++term) v += pv[r][term];
+        const int row = row0 + rl;
+        if (row < a.H) {
             if (a.out_f32)
                 reinterpret_cast<float *>(a.out)[(size_t)t * a.H + row] = v;
             else
                 reinterpret_cast<__nv_bfloat16 *>(a.out)[(size_t)t * a.H + row] = __float2bfloat16_rn(v);
         }
     }
+    cluster_sync();  // no CTA leaves while another still reads its shared memory
 }
 
 template <typename K>
@@ -572,10 +591,36 @@ void set_smem(K kernel, int bytes) {
     cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
+// Launch with the K splits of a tile as one cluster and programmatic serialization after the previous grid.
+template <typename K, typename... Args>
+cudaError_t launch_ex(K kernel, int grid, int cluster, int smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[2];
+    int n = 0;
+    at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster > 1) {
+        at[n].id = cudaLaunchAttributeClusterDimension;
+        at[n].val.clusterDim.x = cluster;
+        at[n].val.clusterDim.y = 1;
+        at[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = at;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace
 
 int tc_gateup_smem() { return kGateStages * kGateStage + 1024; }
 int tc_down_smem() { return kDownStages * kDownStage + 1024; }
+int tc_max_splits() { return kMaxCluster; }
 
 TcAtomLayout tc_atom_layout(int H, int I) {
     TcAtomLayout l;
@@ -601,12 +646,7 @@ void launch_build_weight_atoms(const uint8_t *expert, const ExpertGeometry &g, u
                                                            l.ntH, l.nksI);
 }
 
-void launch_quantize_x(const uint16_t *x, int M, int H, uint8_t *xq, int Hpad, uint8_t *xat, cudaStream_t s) {
-    const int tasks = M * (H / 32);
-    quantize_x_kernel<<<(tasks + 7) / 8, 256, 0, s>>>(x, M, H, xq, Hpad, xat);
-}
-
-void launch_gateup_tc(const TcLaunch &L, cudaStream_t s) {
+cudaError_t launch_gateup_tc(const TcLaunch &L, cudaStream_t s) {
     const TcAtomLayout l = tc_atom_layout(L.geo.H, L.geo.I);
     GateUpArgs a{};
     a.bank = L.bank;
@@ -631,16 +671,15 @@ void launch_gateup_tc(const TcLaunch &L, cudaStream_t s) {
     a.hq = L.hq;
     a.hat = L.hat;
     a.Ipad = L.Ipad;
-    a.part = L.part;
-    a.tile_ctr = L.tile_ctr_gateup;
     a.err = L.err;
-    const int grid = L.n_act_max * l.ntI * L.ks_gateup;
+    if (a.KS < 1 || a.KS > kMaxCluster) return cudaErrorInvalidValue;
+    const int grid = L.n_act_max * l.ntI * a.KS;
     static bool cfg = false;
     if (!cfg) set_smem(gateup_tc_kernel, tc_gateup_smem()), cfg = true;
-    gateup_tc_kernel<<<grid, kThreads, tc_gateup_smem(), s>>>(*L.mapG, *L.mapU, *L.mapX, a);
+    return launch_ex(gateup_tc_kernel, grid, a.KS, tc_gateup_smem(), s, *L.mapG, *L.mapU, *L.mapX, a);
 }
 
-void launch_down_tc(const TcLaunch &L, cudaStream_t s) {
+cudaError_t launch_down_tc(const TcLaunch &L, cudaStream_t s) {
     const TcAtomLayout l = tc_atom_layout(L.geo.H, L.geo.I);
     DownArgs a{};
     a.bank = L.bank;
@@ -658,13 +697,12 @@ void launch_down_tc(const TcLaunch &L, cudaStream_t s) {
     a.hat = L.hat;
     a.out = L.out;
     a.out_f32 = L.out_f32;
-    a.part = L.part_down;
-    a.tile_ctr = L.tile_ctr_down;
     a.err = L.err;
-    const int grid = l.ntH * L.ks_down;
+    if (a.KS < 1 || a.KS > kMaxCluster) return cudaErrorInvalidValue;
+    const int grid = l.ntH * a.KS;
     static bool cfg = false;
     if (!cfg) set_smem(down_tc_kernel, tc_down_smem()), cfg = true;
-    down_tc_kernel<<<grid, kThreads, tc_down_smem(), s>>>(*L.mapD, *L.mapH, a);
+    return launch_ex(down_tc_kernel, grid, a.KS, tc_down_smem(), s, *L.mapD, *L.mapH, a);
 }
 
 }  // namespace moe

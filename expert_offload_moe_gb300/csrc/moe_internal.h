@@ -45,6 +45,9 @@ struct RouteParams {
     int M, H, E, k, nchunk;
     int all_hot;         // prefill: every expert is hot, slot = expert id
     RouteBuffers b;
+    uint8_t *xq;         // tensor-core decode: x terms [16][Hpad] and their atoms, or nullptr
+    uint8_t *xat;
+    int Hpad;
 };
 
 struct ExpertGeometry {
@@ -85,8 +88,6 @@ struct DecodeParams {
 constexpr int kTcAtomBytes = 512;   // block scales of a 128-row tile x 128-column k-step
 constexpr int kTcXRows = 16;        // rows of the x-term operand: 2 terms x 8 tokens
 constexpr int kTcHRows = 32;        // rows of the w*h-term operand: 4 terms x 8 tokens
-constexpr int kTcPartGateup = 2 * 2 * kDecodeMaxTokens * 128;  // floats per gate/up split partial
-constexpr int kTcPartDown = kDecodeMaxTokens * 4 * 128;         // floats per down split partial
 
 // Weight scale atoms of one slot: gate [ntI][nks], up [ntI][nks], down [ntH][nksI], 512 bytes each.
 struct TcAtomLayout {
@@ -104,20 +105,19 @@ struct TcLaunch {
     const uint8_t *xat;           // x-term atoms [nks][512]
     uint8_t *hq, *hat;            // w*h terms [n_act_cap][32][Ipad], atoms [n_act_cap][nksI][512]
     int Ipad;
-    float *part, *part_down;
-    unsigned *tile_ctr_gateup, *tile_ctr_down;
     int *err;
     void *out;
     int out_f32;
     const CUtensorMap *mapG, *mapU, *mapX, *mapD, *mapH;
 };
 
+int tc_max_splits();  // K splits of a tile run as one thread-block cluster: at most this many
 void launch_build_weight_atoms(const uint8_t *expert, const ExpertGeometry &g, uint8_t *atoms, cudaStream_t s);
-void launch_quantize_x(const uint16_t *x, int M, int H, uint8_t *xq, int Hpad, uint8_t *xat, cudaStream_t s);
-void launch_gateup_tc(const TcLaunch &L, cudaStream_t s);
-void launch_down_tc(const TcLaunch &L, cudaStream_t s);
+// Both launched with programmatic serialization after the previous grid in the stream.
+cudaError_t launch_gateup_tc(const TcLaunch &L, cudaStream_t s);
+cudaError_t launch_down_tc(const TcLaunch &L, cudaStream_t s);
 
-void launch_route(const RouteParams &p, cudaStream_t s, int num_sms);
+cudaError_t launch_route(const RouteParams &p, cudaStream_t s, int num_sms);
 void launch_gateup(const DecodeParams &p, int M, cudaStream_t s, int num_sms);
 void launch_down(const DecodeParams &p, int M, cudaStream_t s, int num_sms);
 void launch_map_update(int32_t *e2s, int n, const int32_t *experts, const int32_t *slots, cudaStream_t s);

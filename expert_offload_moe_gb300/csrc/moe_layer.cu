@@ -99,8 +99,6 @@ struct moe_layer {
     moe::TcAtomLayout atl{};
     uint8_t *atoms = nullptr;  // weight scale atoms of every slot [S][atl.slot_bytes]
     uint8_t *xq = nullptr, *xat = nullptr, *hq = nullptr, *hat = nullptr;
-    float *part = nullptr, *part_down = nullptr;
-    unsigned *ctr_gateup = nullptr, *ctr_down = nullptr;
     int *err = nullptr;
     void *tc_block = nullptr;
     CUtensorMap mapG{}, mapU{}, mapD{}, mapX{}, mapH{};
@@ -192,11 +190,12 @@ int encode_map(CUtensorMap *m, CUtensorMapDataType type, const void *base, uint6
 }
 
 // K splits: enough CTAs for about two per SM (the kernels are sized to fit two), but at least
-// 4 k-steps of 128 per CTA so the pipeline has something to overlap.
+// 4 k-steps of 128 per CTA so the pipeline has something to overlap, and at most one cluster's worth.
 int choose_splits(int base_units, int steps, int num_sms) {
     int ks = (2 * num_sms) / (base_units > 0 ? base_units : 1);
     const int ks_max = steps / 4 > 1 ? steps / 4 : 1;
     if (ks > ks_max) ks = ks_max;
+    if (ks > moe::tc_max_splits()) ks = moe::tc_max_splits();
     return ks < 1 ? 1 : ks;
 }
 
@@ -229,22 +228,10 @@ int tc_setup(moe_layer *L, cudaStream_t st) {
     L->Hpad = (H + 127) / 128 * 128;
     L->Ipad = (I + 127) / 128 * 128;
     L->atl = moe::tc_atom_layout(H, I);
-    const int ntI = L->atl.ntI, ntH = L->atl.ntH;
-    size_t units_g = 0, units_d = 0;
-    for (int M = 1; M <= moe::kDecodeMaxTokens; ++M) {
-        const size_t ug = (size_t)act_cap(L, M) * ntI * tc_splits_gateup(L, M);
-        const size_t ud = (size_t)ntH * tc_splits_down(L, M);
-        units_g = ug > units_g ? ug : units_g;
-        units_d = ud > units_d ? ud : units_d;
-    }
     const size_t sz[] = {(size_t)moe::kTcXRows * L->Hpad,
                          (size_t)L->atl.nks * moe::kTcAtomBytes,
                          (size_t)L->n_act_cap * moe::kTcHRows * L->Ipad,
                          (size_t)L->n_act_cap * L->atl.nksI * moe::kTcAtomBytes,
-                         units_g * moe::kTcPartGateup * sizeof(float),
-                         units_d * moe::kTcPartDown * sizeof(float),
-                         (size_t)L->n_act_cap * ntI * sizeof(unsigned),
-                         (size_t)ntH * sizeof(unsigned),
                          sizeof(int)};
     size_t total = 0;
     for (size_t s : sz) total += align_up(s, 256);
@@ -256,8 +243,7 @@ int tc_setup(moe_layer *L, cudaStream_t st) {
                     cudaGetErrorString(e));
     }
     char *p = static_cast<char *>(L->tc_block);
-    void **dst[] = {(void **)&L->xq, (void **)&L->xat, (void **)&L->hq, (void **)&L->hat, (void **)&L->part,
-                    (void **)&L->part_down, (void **)&L->ctr_gateup, (void **)&L->ctr_down, (void **)&L->err};
+    void **dst[] = {(void **)&L->xq, (void **)&L->xat, (void **)&L->hq, (void **)&L->hat, (void **)&L->err};
     for (size_t i = 0; i < sizeof(sz) / sizeof(sz[0]); ++i) {
         *dst[i] = p;
         p += align_up(sz[i], 256);
@@ -484,9 +470,13 @@ int moe_route(moe_layer *L, const void *x_dev, int32_t M, void *stream, moe_rout
     p.nchunk = L->nchunk;
     p.all_hot = M > moe::kDecodeMaxTokens;
     p.b = L->rb;
+    if (L->tc && M <= moe::kDecodeMaxTokens) {  // the route launch also writes the gate/up B operand
+        p.xq = L->xq;
+        p.xat = L->xat;
+        p.Hpad = L->Hpad;
+    }
     CUDA_TRY(prof_mark(L, 0, st));
-    moe::launch_route(p, st, L->num_sms);
-    CUDA_TRY(cudaGetLastError());
+    CUDA_TRY(moe::launch_route(p, st, L->num_sms));
     CUDA_TRY(prof_mark(L, 0, st));
 
     // mirror counts, histogram and cold triples to page-locked memory off the compute chain
@@ -566,10 +556,6 @@ int moe_forward_slots(moe_layer *L, const void *x_dev, void *out_dev, int32_t M,
         t.hq = L->hq;
         t.hat = L->hat;
         t.Ipad = L->Ipad;
-        t.part = L->part;
-        t.part_down = L->part_down;
-        t.tile_ctr_gateup = L->ctr_gateup;
-        t.tile_ctr_down = L->ctr_down;
         t.err = L->err;
         t.out = out_dev;
         t.out_f32 = p.out_f32;
@@ -579,13 +565,10 @@ int moe_forward_slots(moe_layer *L, const void *x_dev, void *out_dev, int32_t M,
         t.mapD = &L->mapD;
         t.mapH = &L->mapH;
         CUDA_TRY(prof_mark(L, 1, st));
-        moe::launch_quantize_x(p.x, M, L->d.hidden, L->xq, L->Hpad, L->xat, st);
-        moe::launch_gateup_tc(t, st);
-        CUDA_TRY(cudaGetLastError());
+        CUDA_TRY(moe::launch_gateup_tc(t, st));
         CUDA_TRY(prof_mark(L, 1, st));
         CUDA_TRY(prof_mark(L, 2, st));
-        moe::launch_down_tc(t, st);
-        CUDA_TRY(cudaGetLastError());
+        CUDA_TRY(moe::launch_down_tc(t, st));
         CUDA_TRY(prof_mark(L, 2, st));
     } else if (M <= moe::kDecodeMaxTokens) {
         p.bank = L->slots;

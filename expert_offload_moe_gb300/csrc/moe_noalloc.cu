@@ -137,8 +137,7 @@ extern "C" int moe_route_noalloc(const void *x_dev, int32_t M, int32_t H, const 
     p.b.cold_w = out->cold_w;
     p.b.hist = out->hist;
     p.b.counts = out->counts;
-    moe::launch_route(p, st, s.num_sms);
-    e = cudaGetLastError();
+    e = moe::launch_route(p, st, s.num_sms);
     if (e != cudaSuccess) return noalloc_fail(MOE_ECUDA, "route kernel launch: %s", cudaGetErrorString(e));
     return MOE_OK;
 }

@@ -17,7 +17,16 @@
 // All counts stay in device memory so the launch shape never depends on the
 // routing (xinfer docs "How it works": fixed launch shapes, miss count in
 // device memory, decode inside CUDA graphs).
+//
+// For the tensor-core decode path the same launch also writes the x terms:
+// extra warp tasks split each 32-element block of x exactly into two E4M3
+// terms with one E8M0 scale (the B operand of the gate/up MMAs).
+//
+// The kernel is launched with programmatic serialization: the router weights,
+// bias and expert_to_slot map are read before it waits for the previous grid
+// in the stream, x and all outputs after.
 #include "moe_internal.h"
+#include "moe_tc.cuh"
 
 namespace moe {
 namespace {
@@ -82,26 +91,58 @@ __device__ int block_scan_array(int *a, int n) {
     return total;
 }
 
+__device__ __forceinline__ void load_router_row(const RouteParams &p, int task, int lane, float (&w8)[8]) {
+    const int e = task / p.nchunk, c = task - e * p.nchunk;
+    const int col = c * kRouteChunk + lane * 8;
+    if (task < p.E * p.nchunk && col < p.H) {  // H % 64 == 0, so a valid lane has all 8 columns
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(p.Wr + (size_t)e * p.H + col));
+        const float4 b = __ldg(reinterpret_cast<const float4 *>(p.Wr + (size_t)e * p.H + col + 4));
+        w8[0] = a.x; w8[1] = a.y; w8[2] = a.z; w8[3] = a.w;
+        w8[4] = b.x; w8[5] = b.y; w8[6] = b.z; w8[7] = b.w;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w8[i] = 0.f;
+    }
+}
+
 __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int H = p.H, E = p.E, M = p.M, k = p.k;
+    __shared__ int s_e2s[kMaxExperts];
+    __shared__ float s_bias[kMaxExperts];
 
-    // ---------------- phase 1: partial logits -----------------------------
+    // ---------------- before the previous grid has finished: constant inputs ----
     const int ntask = E * p.nchunk;
-    for (int task = blockIdx.x * kWarps + warp; task < ntask; task += gridDim.x * kWarps) {
+    const int nq = p.xq ? M * (H / 32) : 0;  // x-term tasks, one 32-element block each
+    int task = blockIdx.x * kWarps + warp;
+    float w8[8];
+    load_router_row(p, task, lane, w8);
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+        s_e2s[e] = p.all_hot ? e : p.e2s[e];
+        s_bias[e] = p.bias ? p.bias[e] : 0.f;
+    }
+    tc::pdl_wait();
+    tc::pdl_trigger();
+
+    // ---------------- phase 1: partial logits; x terms -----------------------
+    for (bool first = true; task < ntask + nq; task += gridDim.x * kWarps, first = false) {
+        if (task >= ntask) {
+            const int q = task - ntask, nb = H / 32, t = q / nb, b = q - t * nb;
+            float res = __uint_as_float((uint32_t)p.x[(size_t)t * H + b * 32 + lane] << 16);
+#pragma unroll
+            for (int term = 0; term < 2; ++term) {
+                uint32_t sb;
+                const uint8_t code = tc::split_term(res, sb);
+                const int n = t * 2 + term;
+                p.xq[(size_t)n * p.Hpad + b * 32 + lane] = code;
+                if (lane == 0) p.xat[(size_t)(b / 4) * kTcAtomBytes + n * 16 + (b % 4)] = (uint8_t)sb;
+            }
+            continue;
+        }
+        if (!first) load_router_row(p, task, lane, w8);
         const int e = task / p.nchunk, c = task - e * p.nchunk;
         const int col = c * kRouteChunk + lane * 8;
-        const bool valid = col < H;  // H % 64 == 0, so a valid lane has all 8 columns
-        float w8[8];
-        if (valid) {
-            const float4 a = __ldg(reinterpret_cast<const float4 *>(p.Wr + (size_t)e * H + col));
-            const float4 b = __ldg(reinterpret_cast<const float4 *>(p.Wr + (size_t)e * H + col + 4));
-            w8[0] = a.x; w8[1] = a.y; w8[2] = a.z; w8[3] = a.w;
-            w8[4] = b.x; w8[5] = b.y; w8[6] = b.z; w8[7] = b.w;
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) w8[i] = 0.f;
-        }
+        const bool valid = col < H;
         for (int t = 0; t < M; ++t) {
             float acc = 0.f;
             if (valid) {
@@ -121,23 +162,31 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
     }
 
     // ---------------- arrival: the last block continues --------------------
+    // bar.sync orders the block's writes before thread 0's release; its acquire orders the
+    // finishing block's reads after every other block's writes.
     __shared__ int s_last;
-    __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) s_last = (atomicAdd(p.b.arrive, 1u) == gridDim.x - 1);
+    if (threadIdx.x == 0) {
+        unsigned prev;
+        asm volatile("atom.acq_rel.gpu.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(p.b.arrive) : "memory");
+        s_last = prev == gridDim.x - 1;
+        if (s_last) *p.b.arrive = 0u;  // every block has arrived: ready for the next launch
+    }
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
-    if (threadIdx.x == 0) *p.b.arrive = 0u;  // every block has arrived: ready for the next launch
 
     // ---------------- phase 2a: top-k + softmax per token -------------------
-    __shared__ float s_l[kWarps][kMaxExperts];
+    // logits rows (top-k) and the per-token cold counts (compaction) are never live together
+    __shared__ __align__(16) float s_union[kWarps * kMaxExperts > kMaxTokens ? kWarps * kMaxExperts : kMaxTokens];
+    float(*s_l)[kMaxExperts] = reinterpret_cast<float(*)[kMaxExperts]>(s_union);
+    int *s_cold = reinterpret_cast<int *>(s_union);
     __shared__ int s_hist[kMaxExperts];
     __shared__ int s_hot_off[kMaxExperts];
     __shared__ int s_act_pos[kMaxExperts];
-    __shared__ int s_cold[kMaxTokens];
     __shared__ int s_ids[kSmemRoutes];  // copy of the routes for the compaction when they fit
     __shared__ float s_w[kSmemRoutes];
+    __shared__ int s_sel_id[kWarps][kMaxTopK];
+    __shared__ float s_sel_l[kWarps][kMaxTopK];
     const bool routes_in_smem = M * k <= kSmemRoutes;
     int *ids = routes_in_smem ? s_ids : p.b.topk_ids;
     float *wts = routes_in_smem ? s_w : p.b.topk_w;
@@ -159,7 +208,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
 #pragma unroll
             for (int c = 0; c < kMaxChunks; ++c)
                 if (c < p.nchunk) v += pv[c];
-            v += p.bias ? p.bias[e] : 0.f;
+            v += s_bias[e];
             s_l[t][e] = (v != v) ? -INFINITY : v;  // NaN marks a taken expert below
         }
         __syncthreads();
@@ -170,69 +219,156 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
             for (int e = lane; e < E; e += 32) {
                 float v = 0.f;
                 for (int c = 0; c < p.nchunk; ++c) v += __ldcg(p.b.logit_part + ((size_t)c * M + t) * E + e);
-                v += p.bias ? p.bias[e] : 0.f;
+                v += s_bias[e];
                 s_l[warp][e] = (v != v) ? -INFINITY : v;
             }
         }
         __syncwarp();
-        int sel_id[kMaxTopK];
-        float sel_l[kMaxTopK];
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) {
-            sel_id[j] = 0;
-            sel_l[j] = 0.f;
-            if (j < k) {
-                float bv = -INFINITY;
-                int be = 0x7fffffff;
-                for (int e = lane; e < E; e += 32) {
-                    const float v = s_l[warp][e];
-                    if (v != v) continue;  // taken
-                    if (v > bv || (v == bv && e < be)) {
-                        bv = v;
-                        be = e;
-                    }
+        // k arg-max rounds (ties to the lower id); the taken expert is marked NaN in the row
+        for (int j = 0; j < k; ++j) {
+            float bv = -INFINITY;
+            int be = 0x7fffffff;
+            for (int e = lane; e < E; e += 32) {
+                const float v = s_l[warp][e];
+                if (v != v) continue;  // taken
+                if (v > bv || (v == bv && e < be)) {
+                    bv = v;
+                    be = e;
                 }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                    const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                    if (ov > bv || (ov == bv && oe < be)) {
-                        bv = ov;
-                        be = oe;
-                    }
-                }
-                // E >= k and no stored value is NaN, so a candidate always exists: be < E
-                sel_id[j] = be;
-                sel_l[j] = bv;
-                if (lane == (be & 31)) s_l[warp][be] = __int_as_float(0x7fc00000);
-                __syncwarp();
             }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                if (ov > bv || (ov == bv && oe < be)) {
+                    bv = ov;
+                    be = oe;
+                }
+            }
+            // E >= k and no stored value is NaN, so a candidate always exists: be < E
+            if (lane == 0) {
+                s_sel_id[warp][j] = be;
+                s_sel_l[warp][j] = bv;
+            }
+            if (lane == (be & 31)) s_l[warp][be] = __int_as_float(0x7fc00000);
+            __syncwarp();
         }
-        const float lmax = sel_l[0];
-        float den = 0.f;
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j)
-            if (j < k) den += expf(sel_l[j] - lmax);
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) {
-            if (j < k && lane == j) {
-                const float wj = expf(sel_l[j] - lmax) / den;
-                p.b.topk_ids[(size_t)t * k + j] = sel_id[j];
-                p.b.topk_w[(size_t)t * k + j] = wj;
-                if (routes_in_smem) {
-                    s_ids[t * k + j] = sel_id[j];
-                    s_w[t * k + j] = wj;
-                }
-                atomicAdd(&s_hist[sel_id[j]], 1);
+        // softmax over the k selected logits, the denominator summed in selection order
+        if (lane < k) {
+            const float lmax = s_sel_l[warp][0];
+            float den = 0.f;
+            for (int j = 0; j < k; ++j) den += expf(s_sel_l[warp][j] - lmax);
+            const int id = s_sel_id[warp][lane];
+            const float wj = expf(s_sel_l[warp][lane] - lmax) / den;
+            p.b.topk_ids[(size_t)t * k + lane] = id;
+            p.b.topk_w[(size_t)t * k + lane] = wj;
+            if (routes_in_smem) {
+                s_ids[t * k + lane] = id;
+                s_w[t * k + lane] = wj;
             }
+            atomicAdd(&s_hist[id], 1);
         }
         __syncwarp();
     }
     __syncthreads();
 
+    if (M <= kWarps) {
+        // Decode: warp 0 scans the experts (each lane a run of consecutive ids), warp 1 the tokens.
+        __shared__ int s_n[3];
+        if (warp == 0) {
+            const int per = (E + 31) / 32, e0 = min(lane * per, E), e1 = min(e0 + per, E);
+            int nh = 0, na = 0;
+            for (int e = e0; e < e1; ++e) {
+                const int h = s_e2s[e] >= 0 ? s_hist[e] : 0;
+                nh += h;
+                na += h > 0;
+            }
+            int xh = nh, xa = na;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int yh = __shfl_up_sync(0xffffffffu, xh, o), ya = __shfl_up_sync(0xffffffffu, xa, o);
+                if (lane >= o) {
+                    xh += yh;
+                    xa += ya;
+                }
+            }
+            int oh = xh - nh, oa = xa - na;
+            for (int e = e0; e < e1; ++e) {
+                p.b.hist[e] = s_hist[e];
+                const int h = s_e2s[e] >= 0 ? s_hist[e] : 0;
+                s_hot_off[e] = oh;
+                if (h > 0) {
+                    p.b.act_expert[oa] = e;
+                    p.b.act_slot[oa] = s_e2s[e];
+                    p.b.act_off[oa] = oh;
+                    p.b.act_cnt[oa] = h;
+                    ++oa;
+                }
+                oh += h;
+            }
+            if (lane == 31) {
+                s_n[0] = xh;
+                s_n[1] = xa;
+            }
+        } else if (warp == 1) {
+            // cold routes of token `lane`, ascending expert id
+            int ce[kMaxTopK];
+            float cw[kMaxTopK];
+            int n = 0;
+            if (lane < M)
+                for (int j = 0; j < k; ++j) {
+                    const int e = ids[lane * k + j];
+                    if (s_e2s[e] >= 0) continue;
+                    const float wt = wts[lane * k + j];
+                    int q = n++;  // insertion by expert id
+                    while (q > 0 && ce[q - 1] > e) {
+                        ce[q] = ce[q - 1];
+                        cw[q] = cw[q - 1];
+                        --q;
+                    }
+                    ce[q] = e;
+                    cw[q] = wt;
+                }
+            int x = n;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            const int base = x - n;
+            for (int q = 0; q < n; ++q) {
+                p.b.cold_token[base + q] = lane;
+                p.b.cold_expert[base + q] = ce[q];
+                p.b.cold_w[base + q] = cw[q];
+            }
+            if (lane == 31) s_n[2] = x;
+        }
+        __syncthreads();
+        // hot routes of each active expert in token order
+        for (int e = threadIdx.x; e < E; e += kThreads) {
+            if (s_e2s[e] < 0 || s_hist[e] == 0) continue;
+            int pos = s_hot_off[e];
+            for (int t = 0; t < M; ++t)
+                for (int j = 0; j < k; ++j)
+                    if (ids[t * k + j] == e) {
+                        p.b.hot_expert[pos] = e;
+                        p.b.hot_token[pos] = t;
+                        p.b.hot_w[pos] = wts[t * k + j];
+                        ++pos;
+                    }
+        }
+        if (threadIdx.x == 0) {
+            p.b.counts[0] = s_n[0];
+            p.b.counts[1] = s_n[2];
+            p.b.counts[2] = s_n[1];
+            p.b.counts[3] = M;
+        }
+        return;
+    }
+
     // ---------------- phase 2b: compaction ----------------------------------
     for (int e = threadIdx.x; e < E; e += kThreads) {
-        const bool hot = p.all_hot || p.e2s[e] >= 0;
+        const bool hot = s_e2s[e] >= 0;
         s_hot_off[e] = hot ? s_hist[e] : 0;
         s_act_pos[e] = (hot && s_hist[e] > 0) ? 1 : 0;
     }
@@ -242,12 +378,12 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
 
     for (int e = threadIdx.x; e < E; e += kThreads) {
         p.b.hist[e] = s_hist[e];
-        const bool hot = p.all_hot || p.e2s[e] >= 0;
+        const bool hot = s_e2s[e] >= 0;
         if (!hot || s_hist[e] == 0) continue;
         const int a = s_act_pos[e];
         int pos = s_hot_off[e];
         p.b.act_expert[a] = e;
-        p.b.act_slot[a] = p.all_hot ? e : p.e2s[e];
+        p.b.act_slot[a] = s_e2s[e];
         p.b.act_off[a] = pos;
         p.b.act_cnt[a] = s_hist[e];
         for (int t = 0; t < M; ++t)
@@ -264,7 +400,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
     for (int t = threadIdx.x; t < M; t += kThreads) {
         int n = 0;
         if (!p.all_hot)
-            for (int j = 0; j < k; ++j) n += p.e2s[ids[t * k + j]] < 0;
+            for (int j = 0; j < k; ++j) n += s_e2s[ids[t * k + j]] < 0;
         s_cold[t] = n;
     }
     __syncthreads();
@@ -276,7 +412,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
             int n = 0;
             for (int j = 0; j < k; ++j) {
                 const int e = ids[t * k + j];
-                if (p.e2s[e] >= 0) continue;
+                if (s_e2s[e] >= 0) continue;
                 const float wt = wts[t * k + j];
                 int q = n++;  // insertion by expert id
                 while (q > 0 && ce[q - 1] > e) {
@@ -318,11 +454,20 @@ __global__ void map_update_kernel(int32_t *e2s, MapUpdate u) {
 
 }  // namespace
 
-void launch_route(const RouteParams &p, cudaStream_t s, int num_sms) {
-    const int ntask = p.E * p.nchunk;
+cudaError_t launch_route(const RouteParams &p, cudaStream_t s, int num_sms) {
+    const int ntask = p.E * p.nchunk + (p.xq ? p.M * (p.H / 32) : 0);
     int grid = (ntask + kWarps - 1) / kWarps;
     grid = grid < 1 ? 1 : (grid > 8 * num_sms ? 8 * num_sms : grid);
-    route_kernel<<<grid, kThreads, 0, s>>>(p);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, route_kernel, p);
 }
 
 void launch_map_update(int32_t *e2s, int n, const int32_t *experts, const int32_t *slots, cudaStream_t s) {

@@ -87,9 +87,76 @@ __device__ __forceinline__ void tma_load_3d(const CUtensorMap *map, uint64_t *ba
         : "memory");
 }
 
+// L2 policy for data read once per step (expert weights): evicted first, so that streaming them
+// does not push code, router weights and activations out of L2.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void tma_load_3d_hint(const CUtensorMap *map, uint64_t *bar, void *dst, int x, int y, int z,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
+
+// 1-D bulk copy global -> shared completing on an mbarrier (16-byte aligned, multiple of 16 bytes).
+__device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_copy_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                               uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// ------------------------------------------------ thread-block clusters
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster; release / acquire orders shared-memory writes and reads.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(const void *p, uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+    return a;
+}
+
+__device__ __forceinline__ float ld_dsmem(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// ------------------------------------------------ programmatic dependent launch
+// wait: the grid launched before this one in the stream has completed and its writes are visible
+// (no-op when this grid was launched without the programmatic-serialization attribute).
+// trigger: the next grid may start launching once every CTA of this grid has triggered or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ---------------------------------------------------------------- tcgen05
 
@@ -182,6 +249,38 @@ __device__ __forceinline__ void e4m3x2_to_f32x2(uint16_t v, float &lo, float &hi
     __half2 h = *reinterpret_cast<__half2 *>(&h2);
     lo = __low2float(h);
     hi = __high2float(h);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// floor(log2(a)) for a finite a > 0
+__device__ __forceinline__ int floor_log2(float a) {
+    const uint32_t u = __float_as_uint(a);
+    const int e = (int)((u >> 23) & 0xff);
+    if (e) return e - 127;
+    return -127 - (__clz(u & 0x7fffff) - 9);  // subnormal
+}
+
+// One term of the exact E4M3 split of a 32-value block held one value per lane:
+// returns this lane's code, updates the residual, and gives the block's E8M0 byte.
+__device__ __forceinline__ uint8_t split_term(float &res, uint32_t &scale_byte) {
+    const float amax = warp_max(fabsf(res));
+    const int X = amax > 0.f ? max(floor_log2(amax) - 7, -127) : -127;  // |res| / 2^X < 256: no saturation
+    scale_byte = e8m0_byte(X);
+    const float inv = e8m0_value(e8m0_byte(-X));
+    const float mine = res * inv;
+    const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+    const int lane = threadIdx.x & 31;
+    const uint16_t pk = (lane & 1) ? f32x2_to_e4m3x2(other, mine) : f32x2_to_e4m3x2(mine, other);
+    const uint8_t code = (lane & 1) ? (uint8_t)(pk >> 8) : (uint8_t)(pk & 0xff);
+    float lo, hi;
+    e4m3x2_to_f32x2(pk, lo, hi);
+    res = res - ((lane & 1) ? hi : lo) * e8m0_value(scale_byte);
+    return code;
 }
 
 }  // namespace tc
