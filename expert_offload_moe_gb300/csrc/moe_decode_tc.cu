@@ -55,7 +55,12 @@ constexpr int kGateStages = 3, kDownStages = 4;
 constexpr int kGateStage = 2 * kTileA + NBX * 128 + 3 * kAtom + 512;   // 36 KB
 constexpr int kDownStage = kTileA + NBH * 128 + 2 * kAtom + 1024;       // 22 KB
 static_assert(kGateStage % 1024 == 0 && kDownStage % 1024 == 0, "stage alignment");
-constexpr uint32_t kGateTmem = 128, kDownTmem = 64;
+// Accumulators per operand: MMA slice kk of a k-step accumulates into kk % kAcc (summed in the epilogue).
+// More than one did not shorten a k-step on GB300 (the MMA chain is not the bottleneck), so one.
+constexpr int kAcc = 1;
+constexpr uint32_t tmem_cols(uint32_t need) { return need <= 32 ? 32 : need <= 64 ? 64 : need <= 128 ? 128 : need <= 256 ? 256 : 512; }
+constexpr uint32_t kGateTmem = tmem_cols(2 * kAcc * kTcXRows + 12 * kGateStages);
+constexpr uint32_t kDownTmem = tmem_cols(kAcc * kTcHRows + 8 * kDownStages);
 constexpr int kErrFull = 1, kErrEmpty = 2, kErrDone = 3;
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
@@ -86,7 +91,7 @@ __device__ __forceinline__ void load_tail_tile(uint8_t *dst, const uint8_t *code
         const int i = lane + 32 * j, r = i / kUnits, u = i % kUnits;
         v[j] = make_uint2(0u, 0u);
         if (row0 + r < rows)
-            v[j] = __ldcs(reinterpret_cast<const uint2 *>(codes + (size_t)(row0 + r) * (K / 2) + kstep * 64 + u * 8));
+            v[j] = __ldg(reinterpret_cast<const uint2 *>(codes + (size_t)(row0 + r) * (K / 2) + kstep * 64 + u * 8));
     }
 #pragma unroll
     for (int j = 0; j < kPerLane; ++j) {
@@ -194,10 +199,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint8_t *expert = a.bank + (size_t)slot * a.expert_bytes;
     const uint8_t *gat = a.atoms + (size_t)slot * a.atom_slot_bytes + a.atom_off_g + (size_t)tile * nks * kAtom;
     const uint8_t *uat = a.atoms + (size_t)slot * a.atom_slot_bytes + a.atom_off_u + (size_t)tile * nks * kAtom;
-    const uint32_t tDg = tbase, tDu = tbase + 16, tSF = tbase + 32;  // per stage: 12 scale columns
+    // columns: gate accumulators [kAcc][16], up accumulators [kAcc][16], then 12 scale columns per stage
+    const uint32_t tDg = tbase, tDu = tbase + kAcc * NBX, tSF = tbase + 2 * kAcc * NBX;
 
     if (warp == 0) {
-        const uint64_t pol = l2_evict_first();
         bool ok = true;
         for (int i = 0; i < nsteps && ok; ++i) {
             const int st = i % S, kstep = k0 + i;
@@ -214,12 +219,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 mbar_expect_tx(&full[st], tail ? kTxTail : kTxFull);
                 if (!tail) {
-                    tma_load_3d_hint(&mapG, &full[st], sA, kstep * 128, row0, slot, pol);
-                    tma_load_3d_hint(&mapU, &full[st], sA + kTileA, kstep * 128, row0, slot, pol);
+                    tma_load_3d(&mapG, &full[st], sA, kstep * 128, row0, slot);
+                    tma_load_3d(&mapU, &full[st], sA + kTileA, kstep * 128, row0, slot);
                 }
                 tma_load_3d(&mapX, &full[st], sA + 2 * kTileA, kstep * 128, 0, 0);
-                bulk_copy_hint(sAt, gat + (size_t)kstep * kAtom, kAtom, &full[st], pol);
-                bulk_copy_hint(sAt + kAtom, uat + (size_t)kstep * kAtom, kAtom, &full[st], pol);
+                bulk_copy(sAt, gat + (size_t)kstep * kAtom, kAtom, &full[st]);
+                bulk_copy(sAt + kAtom, uat + (size_t)kstep * kAtom, kAtom, &full[st]);
                 bulk_copy(sAt + 2 * kAtom, a.xat + (size_t)kstep * kAtom, kAtom, &full[st]);
             }
             __syncwarp();
@@ -227,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = mx_idesc(kFmtE2M1, kFmtE4M3, NBX);
+            unsigned init = 0;  // bit kk: accumulator kk holds a sum
             bool ok = true;
             for (int i = 0; i < nsteps && ok; ++i) {
                 const int st = i % S;
@@ -243,9 +249,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool tail = ragged && (k0 + i) == nks - 1;
                 const int nk = tail ? 2 : 4;
                 for (int kk = 0; kk < nk; ++kk) {
-                    const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-                    mma_mx(tDg, sw128_desc(aG + kk * 32), sw128_desc(aB + kk * 32), idesc, kk, sfg, sfb, acc);
-                    mma_mx(tDu, sw128_desc(aU + kk * 32), sw128_desc(aB + kk * 32), idesc, kk, sfu, sfb, acc);
+                    const int q = kk % kAcc;
+                    const uint32_t acc = (init >> q) & 1u;
+                    mma_mx(tDg + q * NBX, sw128_desc(aG + kk * 32), sw128_desc(aB + kk * 32), idesc, kk, sfg, sfb,
+                           acc);
+                    mma_mx(tDu + q * NBX, sw128_desc(aU + kk * 32), sw128_desc(aB + kk * 32), idesc, kk, sfu, sfb,
+                           acc);
+                    init |= 1u << q;
                 }
                 mma_commit(&empty[st]);
             }
@@ -277,18 +287,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool got = mbar_wait(&done, 0, a.err, kErrDone);
     tc_fence_after();
     if (got) {
+        // a CTA whose single k-step is a 64-column tail touches only the first two MMA slices
+        const int nacc = min(kAcc, (nsteps == 1 && ragged && k0 == nks - 1) ? 2 : 4);
         uint32_t rr[8];
+        for (int q = 0; q < nacc; ++q) {
 #pragma unroll
-        for (int c8 = 0; c8 < C / 8; ++c8) {
-            if (8 * c8 < 2 * M) {
-                tmem_ld8(tDg + lane_off + 8 * c8, rr);
-                tmem_ld_wait();
+            for (int c8 = 0; c8 < C / 8; ++c8) {
+                if (8 * c8 < 2 * M) {
+                    tmem_ld8(tDg + q * NBX + lane_off + 8 * c8, rr);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 8; ++j) g[8 * c8 + j] = __uint_as_float(rr[j]);
-                tmem_ld8(tDu + lane_off + 8 * c8, rr);
-                tmem_ld_wait();
+                    for (int j = 0; j < 8; ++j) g[8 * c8 + j] += __uint_as_float(rr[j]);
+                    tmem_ld8(tDu + q * NBX + lane_off + 8 * c8, rr);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 8; ++j) u[8 * c8 + j] = __uint_as_float(rr[j]);
+                    for (int j = 0; j < 8; ++j) u[8 * c8 + j] += __uint_as_float(rr[j]);
+                }
             }
         }
     }
@@ -422,11 +436,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = tslot;
-    const uint32_t tD = tbase, tSF = tbase + 32;  // per stage: 8 scale columns
+    // columns: accumulators [kAcc][32], then 8 scale columns per stage
+    const uint32_t tD = tbase, tSF = tbase + kAcc * NB;
 
     if (warp == 0) {
         // weights of the first stages are fetched before the gate/up grid has finished
-        const uint64_t pol = l2_evict_first();
         const int npre = nsteps < S ? nsteps : S;
         for (int i = 0; i < npre; ++i) {
             const int g = g0 + i, e = g / nksI, s = g - e * nksI;
@@ -436,11 +450,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tail) load_tail_tile(sA, a.bank + (size_t)slot * a.expert_bytes + a.off_d_codes, a.H, row0, a.I, s);
             if (lane == 0) {
                 mbar_expect_tx(&full[i], tail ? kTxTail : kTxFull);
-                if (!tail) tma_load_3d_hint(&mapD, &full[i], sA, s * 128, row0, slot, pol);
-                bulk_copy_hint(sA + kTileA + kB,
-                               a.atoms + (size_t)slot * a.atom_slot_bytes + a.atom_off_d +
-                                   ((size_t)tile * nksI + s) * kAtom,
-                               kAtom, &full[i], pol);
+                if (!tail) tma_load_3d(&mapD, &full[i], sA, s * 128, row0, slot);
+                bulk_copy(sA + kTileA + kB,
+                          a.atoms + (size_t)slot * a.atom_slot_bytes + a.atom_off_d + ((size_t)tile * nksI + s) * kAtom,
+                          kAtom, &full[i]);
             }
             __syncwarp();
         }
@@ -468,11 +481,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tail) load_tail_tile(sA, a.bank + (size_t)slot * a.expert_bytes + a.off_d_codes, a.H, row0, a.I, s);
             if (lane == 0) {
                 mbar_expect_tx(&full[st], tail ? kTxTail : kTxFull);
-                if (!tail) tma_load_3d_hint(&mapD, &full[st], sA, s * 128, row0, slot, pol);
+                if (!tail) tma_load_3d(&mapD, &full[st], sA, s * 128, row0, slot);
                 tma_load_3d(&mapH, &full[st], sA + kTileA, s * 128, 0, e);
-                bulk_copy_hint(sAt, a.atoms + (size_t)slot * a.atom_slot_bytes + a.atom_off_d +
-                                        ((size_t)tile * nksI + s) * kAtom,
-                               kAtom, &full[st], pol);
+                bulk_copy(sAt, a.atoms + (size_t)slot * a.atom_slot_bytes + a.atom_off_d +
+                                   ((size_t)tile * nksI + s) * kAtom,
+                          kAtom, &full[st]);
                 bulk_copy(sAt + kAtom, a.hat + ((size_t)e * nksI + s) * kAtom, kAtom, &full[st]);
             }
             __syncwarp();
@@ -483,6 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == 1) {
             if (lane == 0) {
                 const uint32_t idesc = mx_idesc(kFmtE2M1, kFmtE4M3, NB);
+                unsigned init = 0;  // bit kk: accumulator kk holds a sum
                 bool ok = true;
                 for (int i = 0; i < nsteps && ok; ++i) {
                     const int st = i % S;
@@ -498,8 +512,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t aA = smem_u32(sA), aB = aA + kTileA;
                     const int nk = (ragged && s == nksI - 1) ? 2 : 4;
                     for (int kk = 0; kk < nk; ++kk) {
-                        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-                        mma_mx(tD, sw128_desc(aA + kk * 32), sw128_desc(aB + kk * 32), idesc, kk, sfa, sfb, acc);
+                        const int q = kk % kAcc;
+                        mma_mx(tD + q * NB, sw128_desc(aA + kk * 32), sw128_desc(aB + kk * 32), idesc, kk, sfa, sfb,
+                               (init >> q) & 1u);
+                        init |= 1u << q;
                     }
                     mma_commit(&empty[st]);
                 }
@@ -518,14 +534,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool got = mbar_wait(&done, 0, a.err, kErrDone);
     tc_fence_after();
     if (got && nsteps > 0) {
+        // a CTA whose single k-step is a 64-column tail touches only the first two MMA slices
+        const int nacc = min(kAcc, (nsteps == 1 && ragged && g0 % nksI == nksI - 1) ? 2 : 4);
         uint32_t rr[8];
+        for (int q = 0; q < nacc; ++q) {
 #pragma unroll
-        for (int c8 = 0; c8 < C / 8; ++c8) {
-            if (8 * c8 < M * T) {
-                tmem_ld8(tD + lane_off + 8 * c8, rr);
-                tmem_ld_wait();
+            for (int c8 = 0; c8 < C / 8; ++c8) {
+                if (8 * c8 < M * T) {
+                    tmem_ld8(tD + q * NB + lane_off + 8 * c8, rr);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 8; ++j) d[8 * c8 + j] = __uint_as_float(rr[j]);
+                    for (int j = 0; j < 8; ++j) d[8 * c8 + j] += __uint_as_float(rr[j]);
+                }
             }
         }
     }
