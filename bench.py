@@ -159,7 +159,7 @@ def run_reference(args):
 
 def traffic_for(kernel_src):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
-    summ = os.path.join(ROOT, "profiles", "gateup_gptoss20b_traffic.txt")
+    summ = os.path.join(ROOT, "profiles", "gateup_tc_gptoss20b_traffic.txt")
     if not os.path.exists(summ):
         return None
     sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
@@ -255,7 +255,7 @@ def run_ours(args):
     pk, pk_src = peaks()
     hbm_peak = pk.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"])
     achieved = gateup_bytes / (gateup_us * 1e-6) / 1e9
-    traffic = traffic_for(os.path.join(ROOT, "expert_offload_moe_gb300", "csrc", "moe_decode.cu"))
+    traffic = traffic_for(os.path.join(ROOT, "expert_offload_moe_gb300", "csrc", "moe_decode_tc.cu"))
 
     # ---------------- e2e: host inputs in, outputs back, every step ------------
     x_host = torch.empty((n_inputs, L, M, w.hidden), dtype=torch.bfloat16, pin_memory=True)
@@ -280,7 +280,7 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4*e4m3->f32", "data": "synthetic",
         "config": {"workload": w.name, "layers": L, "hidden": w.hidden, "inter": w.inter, "experts": w.experts,
                    "top_k": w.top_k, "slots": w.slots, "tokens_per_step": M, "parallelism": f"replicas{world}",
                    "weights": "mxfp4 experts, fp32 router, fp32 accumulation",
@@ -290,7 +290,7 @@ def run_ours(args):
                    "router_gbs": router_bytes_step / (t_ms / args.steps * 1e-3) / 1e9,
                    "mean_active_experts": mean_act,
                    "kernel_us": {"route": route_us, "gateup": gateup_us, "down": down_us}},
-        "roofline": {"bound": "hbm", "kernel": "gateup_kernel", "achieved": achieved, "peak": hbm_peak,
+        "roofline": {"bound": "hbm", "kernel": "gateup_tc_kernel", "achieved": achieved, "peak": hbm_peak,
                      "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
                      "bytes_per_launch": gateup_bytes, "avg_launch_us": gateup_us,
                      "peak_source": "measured hbm_gbs (MEASURED_PEAKS.json)" if pk_src == "measured"
