@@ -284,7 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float g[C], u[C];
 #pragma unroll
     for (int c = 0; c < C; ++c) g[c] = u[c] = 0.f;
-    const bool got = mbar_wait(&done, 0, a.err, kErrDone);
+    // every lane leaves the wait at its own time: reconverge before the warp-aligned tensor-memory loads
+    const bool got = __all_sync(0xffffffffu, mbar_wait(&done, 0, a.err, kErrDone));
     tc_fence_after();
     if (got) {
         // a CTA whose single k-step is a 64-column tail touches only the first two MMA slices
@@ -294,12 +295,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c8 = 0; c8 < C / 8; ++c8) {
                 if (8 * c8 < 2 * M) {
-                    tmem_ld8(tDg + q * NBX + lane_off + 8 * c8, rr);
-                    tmem_ld_wait();
+                    tmem_ld8_sync(tDg + q * NBX + lane_off + 8 * c8, rr);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) g[8 * c8 + j] += __uint_as_float(rr[j]);
-                    tmem_ld8(tDu + q * NBX + lane_off + 8 * c8, rr);
-                    tmem_ld_wait();
+                    tmem_ld8_sync(tDu + q * NBX + lane_off + 8 * c8, rr);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) u[8 * c8 + j] += __uint_as_float(rr[j]);
                 }
@@ -322,6 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 red[c * 128 + rloc] = g[c];
                 red[(C + c) * 128 + rloc] = u[c];
             }
+        __syncwarp();
         cluster_sync();
         grp = ks + KS * warp;
         if (grp < 4) {
@@ -378,6 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     }
+    __syncwarp();
     if (KS > 1) cluster_sync();  // no CTA leaves while another still reads its shared memory
 }
 
@@ -531,7 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float d[C];
 #pragma unroll
     for (int c = 0; c < C; ++c) d[c] = 0.f;
-    const bool got = mbar_wait(&done, 0, a.err, kErrDone);
+    // every lane leaves the wait at its own time: reconverge before the warp-aligned tensor-memory loads
+    const bool got = __all_sync(0xffffffffu, mbar_wait(&done, 0, a.err, kErrDone));
     tc_fence_after();
     if (got && nsteps > 0) {
         // a CTA whose single k-step is a 64-column tail touches only the first two MMA slices
@@ -541,8 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c8 = 0; c8 < C / 8; ++c8) {
                 if (8 * c8 < M * T) {
-                    tmem_ld8(tD + q * NB + lane_off + 8 * c8, rr);
-                    tmem_ld_wait();
+                    tmem_ld8_sync(tD + q * NB + lane_off + 8 * c8, rr);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) d[8 * c8 + j] += __uint_as_float(rr[j]);
                 }
@@ -576,6 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int c = 0; c < C; ++c)
         if (c < M * T) red[c * 128 + rloc] = d[c];
+    __syncwarp();
     cluster_sync();
     const int r0 = ks * 128 / KS, nrows = (ks + 1) * 128 / KS - r0;
     for (int it = threadIdx.x; it < nrows * M; it += kThreads) {
@@ -603,6 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 reinterpret_cast<__nv_bfloat16 *>(a.out)[(size_t)t * a.H + row] = __float2bfloat16_rn(v);
         }
     }
+    __syncwarp();
     cluster_sync();  // no CTA leaves while another still reads its shared memory
 }
 

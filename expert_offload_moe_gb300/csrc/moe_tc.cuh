@@ -99,6 +99,15 @@ __device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t b
                  : "memory");
 }
 
+// Shared-memory stores that the tensor cores read through a descriptor: nothing in the program loads these
+// bytes with an ordinary instruction, so they are issued as volatile stores that are never dropped or sunk.
+__device__ __forceinline__ void st_shared_u8(void *p, uint32_t v) {
+    asm volatile("st.shared.u8 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_shared_zero16(void *p) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(smem_u32(p)), "r"(0u) : "memory");
+}
+
 // ------------------------------------------------ thread-block clusters
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -110,6 +119,26 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 // Every thread of every CTA of the cluster; release / acquire orders shared-memory writes and reads.
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The two halves of cluster_sync, for warps that reach a cluster barrier phase at different points:
+// a thread arrives once per phase and waits for that phase before arriving at the next.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// Barrier `id` (1..15) among `n` threads of the CTA (whole warps).
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// fetch-and-add with acquire-release semantics at GPU scope
+__device__ __forceinline__ unsigned atomic_add_acq_rel(unsigned *p, unsigned v) {
+    unsigned prev;
+    asm volatile("atom.acq_rel.gpu.add.u32 %0, [%1], %2;" : "=r"(prev) : "l"(p), "r"(v) : "memory");
+    return prev;
 }
 
 // Address of the same shared-memory variable in CTA `rank` of the cluster.
@@ -200,6 +229,29 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// Load and wait in one statement: the registers exist for the compiler only once the load has completed
+// (with a separate wait, uses of the outputs may be scheduled above it).
+__device__ __forceinline__ void tmem_ld8_sync(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Two 8-column loads in flight, then the wait.
+__device__ __forceinline__ void tmem_ld8x2_sync(uint32_t ta, uint32_t (&a)[8], uint32_t tb, uint32_t (&b)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%16];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%17];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
+          "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7])
+        : "r"(ta), "r"(tb)
+        : "memory");
+}
+
 // ------------------------------------------------ E4M3 terms of a 32-value block
 
 // E8M0 byte of 2^e (e clamped to the E8M0 range).
@@ -216,13 +268,15 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
     return r;
 }
 
-// Packed E4M3 pair back to fp32 (exact).
+// Packed E4M3 pair back to fp32 (exact): low byte -> lo, high byte -> hi.  One asm block, no type punning.
 __device__ __forceinline__ void e4m3x2_to_f32x2(uint16_t v, float &lo, float &hi) {
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
-    __half2 h = *reinterpret_cast<__half2 *>(&h2);
-    lo = __low2float(h);
-    hi = __high2float(h);
+    asm("{\n\t.reg .b32 t;\n\t.reg .b16 a, b;\n\t"
+        "cvt.rn.f16x2.e4m3x2 t, %2;\n\t"
+        "mov.b32 {a, b}, t;\n\t"
+        "cvt.f32.f16 %0, a;\n\t"
+        "cvt.f32.f16 %1, b;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "h"(v));
 }
 
 __device__ __forceinline__ float warp_max(float v) {
