@@ -117,6 +117,27 @@ void launch_build_weight_atoms(const uint8_t *expert, const ExpertGeometry &g, u
 cudaError_t launch_gateup_tc(const TcLaunch &L, cudaStream_t s);
 cudaError_t launch_down_tc(const TcLaunch &L, cudaStream_t s);
 
+// Prefill (M > 8) on the tensor cores over the staged bank (moe_prefill_tc.cu).
+struct PrefillLaunch {
+    const uint8_t *bank, *atoms;  // staged experts (slot = expert id) and their weight atoms
+    ExpertGeometry geo;
+    int E, k, M, max_routes, tiles_cap, Hpad, Ipad;
+    const uint16_t *x;
+    const int32_t *counts, *act_expert, *act_off, *act_cnt, *hot_expert, *hot_token, *topk_ids;
+    const float *hot_w;
+    int32_t *poff, *e2a, *tile_aidx, *tile_nrows, *ntiles;  // plan: [E], [E], [tiles_cap] x 2, [1]
+    uint8_t *XP, *XA, *HP, *HA;  // MXFP8 x / h in route order (rows_cap x Hpad / Ipad) and their atoms
+    float *YP;                   // weighted expert outputs in route order [rows_cap][H]
+    int *err;
+    void *out;
+    int out_f32;
+    const CUtensorMap *mapXP, *mapHP, *mapG, *mapU, *mapD;
+};
+int prefill_tiles_cap(int max_routes, int E);  // 128-row route tiles the buffers must hold
+cudaError_t launch_prefill(const PrefillLaunch &P, cudaStream_t s);
+void launch_build_weight_atoms_bank(const uint8_t *bank, int E, const ExpertGeometry &g, uint8_t *atoms,
+                                    cudaStream_t s);
+
 cudaError_t launch_route(const RouteParams &p, cudaStream_t s, int num_sms);
 void launch_gateup(const DecodeParams &p, int M, cudaStream_t s, int num_sms);
 void launch_down(const DecodeParams &p, int M, cudaStream_t s, int num_sms);

@@ -103,6 +103,16 @@ struct moe_layer {
     void *tc_block = nullptr;
     CUtensorMap mapG{}, mapU{}, mapD{}, mapX{}, mapH{};
 
+    // tensor-core prefill over the staged bank: scratch allocated when staging is attached
+    bool pf = false;
+    int tiles_cap = 0, rows_cap = 0;
+    uint8_t *stage_atoms = nullptr;  // weight atoms of every staged expert [E][atl.slot_bytes]
+    void *pf_block = nullptr;
+    uint8_t *XP = nullptr, *XA = nullptr, *HP = nullptr, *HA = nullptr;
+    float *YP = nullptr;
+    int32_t *pf_poff = nullptr, *pf_e2a = nullptr, *pf_tile_aidx = nullptr, *pf_tile_nrows = nullptr, *pf_ntiles = nullptr;
+    CUtensorMap mapXP{}, mapHP{}, mapSG{}, mapSU{}, mapSD{};
+
     // optional per-kernel timing: event pairs around route, gate/up and down launches
     bool prof = false;
     std::vector<cudaEvent_t> prof_ev[3];
@@ -125,6 +135,8 @@ void release(moe_layer *L) {
     cudaFree(L->h);
     cudaFree(L->tc_block);
     cudaFree(L->atoms);
+    cudaFree(L->pf_block);
+    cudaFree(L->stage_atoms);
     if (L->pinned_block) cudaFreeHost(L->pinned_block);
     for (auto e : {L->ev_fork, L->ev_route, L->ev_fence})
         if (e) cudaEventDestroy(e);
@@ -273,6 +285,70 @@ int tc_setup(moe_layer *L, cudaStream_t st) {
                          L->Ipad, (uint64_t)moe::kTcHRows * L->Ipad, 128, moe::kTcHRows, "h terms")))
         return rc;
     L->tc = true;
+    return MOE_OK;
+}
+
+// Scratch and tensor maps of the tensor-core prefill over the staging buffer `stg` (E experts).
+int prefill_setup(moe_layer *L, uint8_t *stg) {
+    cudaFree(L->pf_block);
+    cudaFree(L->stage_atoms);
+    L->pf_block = nullptr;
+    L->stage_atoms = nullptr;
+    L->pf = false;
+    if (!L->tc || !stg) return MOE_OK;
+    const int E = L->d.num_experts, H = L->d.hidden, I = L->d.inter;
+    const int max_routes = L->d.max_tokens * L->d.top_k;
+    L->tiles_cap = moe::prefill_tiles_cap(max_routes, E);
+    L->rows_cap = L->tiles_cap * 128;
+    L->Ipad = (I + 127) / 128 * 128;
+    const size_t sz[] = {(size_t)L->rows_cap * L->Hpad,
+                         (size_t)L->tiles_cap * L->atl.nks * moe::kTcAtomBytes,
+                         (size_t)L->rows_cap * L->Ipad,
+                         (size_t)L->tiles_cap * L->atl.nksI * moe::kTcAtomBytes,
+                         (size_t)L->rows_cap * H * sizeof(float),
+                         (size_t)E * 4, (size_t)E * 4, (size_t)L->tiles_cap * 4, (size_t)L->tiles_cap * 4, 4};
+    size_t total = 0;
+    for (size_t v : sz) total += align_up(v, 256);
+    cudaError_t e = cudaMalloc(&L->pf_block, total);
+    if (e == cudaSuccess) e = cudaMalloc(&L->stage_atoms, (size_t)E * L->atl.slot_bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(L->pf_block);
+        L->pf_block = nullptr;
+        return fail(e == cudaErrorMemoryAllocation ? MOE_ENOMEM : MOE_ECUDA, "prefill buffers: %s",
+                    cudaGetErrorString(e));
+    }
+    char *p = static_cast<char *>(L->pf_block);
+    void **dst[] = {(void **)&L->XP, (void **)&L->XA, (void **)&L->HP, (void **)&L->HA, (void **)&L->YP,
+                    (void **)&L->pf_poff, (void **)&L->pf_e2a, (void **)&L->pf_tile_aidx, (void **)&L->pf_tile_nrows,
+                    (void **)&L->pf_ntiles};
+    for (size_t i = 0; i < sizeof(sz) / sizeof(sz[0]); ++i) {
+        *dst[i] = p;
+        p += align_up(sz[i], 256);
+    }
+    // activation operands start at zero (columns past H or I are never written); unwritten scales are 2^0
+    CUDA_TRY(cudaMemset(L->pf_block, 0, total));
+    CUDA_TRY(cudaMemset(L->XA, 0x7f, sz[1]));
+    CUDA_TRY(cudaMemset(L->HA, 0x7f, sz[3]));
+    CUDA_TRY(cudaMemset(L->stage_atoms, 0x7f, (size_t)E * L->atl.slot_bytes));
+    const moe::ExpertGeometry &g = L->geo;
+    int rc;
+    if ((rc = encode_map(&L->mapSG, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, stg + g.off_wg_codes, H / 128 * 128, I, E,
+                         H / 2, g.expert_bytes, 128, 128, "staged gate codes")))
+        return rc;
+    if ((rc = encode_map(&L->mapSU, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, stg + g.off_wu_codes, H / 128 * 128, I, E,
+                         H / 2, g.expert_bytes, 128, 128, "staged up codes")))
+        return rc;
+    if ((rc = encode_map(&L->mapSD, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, stg + g.off_wd_codes, I / 128 * 128, H, E,
+                         I / 2, g.expert_bytes, 128, 128, "staged down codes")))
+        return rc;
+    if ((rc = encode_map(&L->mapXP, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->XP, L->Hpad, L->rows_cap, 1, L->Hpad,
+                         (uint64_t)L->rows_cap * L->Hpad, 128, 128, "prefill x")))
+        return rc;
+    if ((rc = encode_map(&L->mapHP, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->HP, L->Ipad, L->rows_cap, 1, L->Ipad,
+                         (uint64_t)L->rows_cap * L->Ipad, 128, 128, "prefill h")))
+        return rc;
+    L->pf = true;
     return MOE_OK;
 }
 
@@ -581,8 +657,52 @@ int moe_forward_slots(moe_layer *L, const void *x_dev, void *out_dev, int32_t M,
         CUDA_TRY(cudaGetLastError());
         CUDA_TRY(prof_mark(L, 2, st));
     } else {
-        return fail(MOE_ESTATE, "prefill (M > %d) needs the prefill kernels, which this build does not have",
-                    moe::kDecodeMaxTokens);
+        if (!L->staging || !L->staged)
+            return fail(MOE_ESTATE, "prefill (M > %d) needs a staging buffer filled by moe_layer_stage_all",
+                        moe::kDecodeMaxTokens);
+        if (!L->pf)
+            return fail(MOE_ESTATE, "prefill needs hidden and inter of at least 128 (tensor-core tiles)");
+        moe::PrefillLaunch P{};
+        P.bank = L->staging;
+        P.atoms = L->stage_atoms;
+        P.geo = L->geo;
+        P.E = L->d.num_experts;
+        P.k = L->d.top_k;
+        P.M = M;
+        P.max_routes = M * L->d.top_k;
+        P.tiles_cap = moe::prefill_tiles_cap(P.max_routes, P.E);
+        P.Hpad = L->Hpad;
+        P.Ipad = L->Ipad;
+        P.x = p.x;
+        P.counts = L->rb.counts;
+        P.act_expert = L->rb.act_expert;
+        P.act_off = L->rb.act_off;
+        P.act_cnt = L->rb.act_cnt;
+        P.hot_expert = L->rb.hot_expert;
+        P.hot_token = L->rb.hot_token;
+        P.topk_ids = L->rb.topk_ids;
+        P.hot_w = L->rb.hot_w;
+        P.poff = L->pf_poff;
+        P.e2a = L->pf_e2a;
+        P.tile_aidx = L->pf_tile_aidx;
+        P.tile_nrows = L->pf_tile_nrows;
+        P.ntiles = L->pf_ntiles;
+        P.XP = L->XP;
+        P.XA = L->XA;
+        P.HP = L->HP;
+        P.HA = L->HA;
+        P.YP = L->YP;
+        P.err = L->err;
+        P.out = out_dev;
+        P.out_f32 = p.out_f32;
+        P.mapXP = &L->mapXP;
+        P.mapHP = &L->mapHP;
+        P.mapG = &L->mapSG;
+        P.mapU = &L->mapSU;
+        P.mapD = &L->mapSD;
+        CUDA_TRY(prof_mark(L, 1, st));
+        CUDA_TRY(moe::launch_prefill(P, st));
+        CUDA_TRY(prof_mark(L, 1, st));
     }
     CUDA_TRY(cudaStreamWaitEvent(st, L->ev_route, 0));  // join the mirror copies
     return MOE_OK;
@@ -721,15 +841,20 @@ int moe_layer_attach_staging(moe_layer *L, void *staging_dev, size_t bytes) {
     L->staging = static_cast<uint8_t *>(staging_dev);
     L->staging_bytes = staging_dev ? bytes : 0;
     L->staged = false;
-    return MOE_OK;
+    return prefill_setup(L, L->staging);
 }
 
 int moe_layer_stage_all(moe_layer *L, void *stream) {
     g_err.clear();
     if (!L) return fail(MOE_EINVAL, "layer is NULL");
     if (!L->staging) return fail(MOE_ESTATE, "no staging buffer attached");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
     CUDA_TRY(cudaMemcpyAsync(L->staging, L->host_bank, (size_t)L->d.num_experts * L->geo.expert_bytes,
-                             cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream)));
+                             cudaMemcpyHostToDevice, st));
+    if (L->pf) {  // block scales of every staged expert, as the prefill kernels read them
+        moe::launch_build_weight_atoms_bank(L->staging, L->d.num_experts, L->geo, L->stage_atoms, st);
+        CUDA_TRY(cudaGetLastError());
+    }
     L->staged = true;
     return MOE_OK;
 }

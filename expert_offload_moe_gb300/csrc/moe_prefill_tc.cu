@@ -1,0 +1,429 @@
+// Prefill expert FFN (M > 8 tokens) on the 5th-generation tensor cores: a grouped, block-scaled GEMM over
+// every expert of the layer staged in one device buffer (xinfer docs "How it works", Prefill: the whole
+// expert layer is staged and the GEMM runs on it; tinyserve README, batched prefill: routes are grouped by
+// expert so that each expert's weights are read once per batch).
+//
+// The route launch has already ordered the hot routes by (expert, token).  Then, on one stream:
+//   prefill_plan_kernel      pads each active expert's routes to whole 128-row tiles (a tile never mixes
+//                            experts) and records the tile list and the expert -> active-index map
+//   prefill_quant_kernel     x of every route -> MXFP8 (E4M3 codes, one E8M0 scale per 32 columns, the
+//                            OCP MX v1.0 conversion rule), gathered into route order with scale atoms
+//   prefill_gemm_kernel<1>   per (route tile, 128 rows of I): Dg = x Wg^T, Du = x Wu^T on tcgen05
+//                            (A = E4M3 routes, B = E2M1 weights, both block-scaled), h = SiLU(g) u,
+//                            h -> MXFP8 in route order (the down GEMM's A operand)
+//   prefill_gemm_kernel<0>   per (route tile, 256 rows of H): y = h Wd^T, times the route's weight
+//   prefill_combine_kernel   out[t] = sum over t's routes in ascending expert order of w y
+// Every result is computed in a fixed order, so it does not depend on timing.
+#include <cuda_bf16.h>
+
+#include "moe_internal.h"
+#include "moe_tc.cuh"
+
+namespace moe {
+namespace {
+
+using namespace tc;
+
+constexpr int kThreads = 128;             // warp 0: copies; warp 1 lane 0: MMAs; all 4 warps: epilogue
+constexpr int kTileA = 128 * 128;         // one 128 x 128 operand tile in smem (one byte per element)
+constexpr int kTileActTx = 128 * 128;     // TMA bytes of an E4M3 activation tile
+constexpr int kTileWTx = 128 * 128 / 2;   // TMA bytes of an E2M1 weight tile (packed codes)
+constexpr int kAtom = kTcAtomBytes;
+constexpr int kStages = 4;
+// stage: [A (128 routes)][B0 (128 weight rows)][B1 (128 weight rows)][atom A][atom B0][atom B1]
+constexpr int kOffB0 = kTileA, kOffB1 = 2 * kTileA, kOffAtA = 3 * kTileA, kOffAtB0 = kOffAtA + kAtom,
+              kOffAtB1 = kOffAtB0 + kAtom;
+constexpr int kStage = 3 * kTileA + 3 * kAtom + 512;  // 50 KB
+static_assert(kStage % 1024 == 0, "stage alignment");
+constexpr int kSmemBytes = 1024 + kStages * kStage;
+// tensor memory: two 128-column accumulators (gate, up) or one 256-column accumulator (down), then
+// 12 scale columns per stage
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColSF = 256;
+static_assert(kColSF + 12 * kStages <= kTmemCols, "tensor memory layout");
+constexpr int kErrFull = 1, kErrEmpty = 2, kErrDone = 3;
+
+// Byte of the 512-byte scale atom that holds row m (of a 128-row tile), k-block kb (of a 128-column step).
+__device__ __forceinline__ int atom_byte(int m, int kb) { return (m & 31) * 16 + (m >> 5) * 4 + kb; }
+
+// MXFP8 shared exponent of a block whose largest magnitude is amax (OCP MX v1.0: floor(log2 amax) minus the
+// largest E4M3 exponent, 8; clamped to the E8M0 range; a block of zeros gets -127).
+__device__ __forceinline__ int mxfp8_exponent(float amax) {
+    if (!(amax > 0.f)) return -127;
+    return min(max(floor_log2(amax) - 8, -127), 127);
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ plan
+
+__global__ void __launch_bounds__(256) prefill_plan_kernel(const int32_t *counts, const int32_t *act_expert,
+                                                           const int32_t *act_cnt, int E, int32_t *poff,
+                                                           int32_t *e2a, int32_t *tile_aidx, int32_t *tile_nrows,
+                                                           int32_t *ntiles, int tiles_cap) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) e2a[e] = -1;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const int n_act = counts[2];
+        int pr = 0, nt = 0;
+        for (int a = 0; a < n_act; ++a) {
+            const int cnt = act_cnt[a];
+            poff[a] = pr;
+            e2a[act_expert[a]] = a;
+            for (int r = 0; r < cnt; r += 128) {
+                if (nt < tiles_cap) {
+                    tile_aidx[nt] = a;
+                    tile_nrows[nt] = min(128, cnt - r);
+                }
+                ++nt;
+            }
+            pr += (cnt + 127) / 128 * 128;
+        }
+        *ntiles = min(nt, tiles_cap);
+    }
+}
+
+// ------------------------------------------------------------------ x -> MXFP8, route order
+
+// One warp per (route, 32-column block): XP[pr][Hpad] codes, XA[tile][kstep][512] scales, pr = padded row.
+__global__ void __launch_bounds__(256) prefill_quant_kernel(const uint16_t *x, int H, const int32_t *counts,
+                                                            const int32_t *hot_expert, const int32_t *hot_token,
+                                                            const int32_t *act_off, const int32_t *e2a,
+                                                            const int32_t *poff, uint8_t *XP, int Hpad,
+                                                            uint8_t *XA, int nks) {
+    const int lane = threadIdx.x & 31;
+    const int nb = H / 32;
+    const int task = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (task >= counts[0] * nb) return;
+    const int p = task / nb, b = task - p * nb;
+    const int a = e2a[hot_expert[p]];
+    const int pr = poff[a] + (p - act_off[a]);
+    const float v = __uint_as_float((uint32_t)x[(size_t)hot_token[p] * H + b * 32 + lane] << 16);
+    const int X = mxfp8_exponent(warp_max(fabsf(v)));
+    const float sv = v * e8m0_value(e8m0_byte(-X));  // exact: a power of two
+    const float other = __shfl_xor_sync(0xffffffffu, sv, 1);
+    const uint16_t pk = (lane & 1) ? f32x2_to_e4m3x2(other, sv) : f32x2_to_e4m3x2(sv, other);
+    XP[(size_t)pr * Hpad + b * 32 + lane] = (lane & 1) ? (uint8_t)(pk >> 8) : (uint8_t)(pk & 0xff);
+    if (lane == 0) XA[((size_t)(pr >> 7) * nks + (b >> 2)) * kAtom + atom_byte(pr & 127, b & 3)] = (uint8_t)(X + 127);
+}
+
+// ------------------------------------------------------------------ grouped GEMM
+
+namespace {
+
+struct GemmArgs {
+    const uint8_t *bank, *atoms;  // staged experts (slot = expert id) and their weight atoms
+    size_t expert_bytes, atom_slot_bytes;
+    size_t off_b0_codes, off_b1_codes;  // gate/up: Wg, Wu codes; down: Wd codes (both halves)
+    size_t atom_off_b0, atom_off_b1;    // gate/up: gate, up atoms; down: down atoms
+    int K, Nrows;                       // contraction length; rows of the weight matrix (I or H)
+    int nN;                             // weight-row tiles per route tile (128 rows gate/up, 256 rows down)
+    const int32_t *ntiles, *tile_aidx, *tile_nrows, *act_expert, *act_off, *poff;
+    const float *hot_w;
+    const uint8_t *Aat;  // atoms of the A operand [tile][kstep][512]
+    // gate/up epilogue: h in route order (A operand of down)
+    uint8_t *HP, *HA;
+    int Ipad, nksI;
+    // down epilogue: weighted y in route order
+    float *YP;
+    int H;
+    int *err;
+};
+
+template <int kGateUp>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB0,
+                        const __grid_constant__ CUtensorMap mapB1, GemmArgs g) {
+    constexpr int S = kStages;
+    constexpr int NB = kGateUp ? 128 : 256;  // MMA N
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    __shared__ __align__(8) uint64_t full[S], empty[S], done;
+    __shared__ uint32_t tslot;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tile = blockIdx.x / g.nN, jn = blockIdx.x - tile * g.nN;
+    if (tile >= *g.ntiles) return;
+    const int aidx = g.tile_aidx[tile], nrows = g.tile_nrows[tile];
+    const int expert = g.act_expert[aidx];
+    const int nks = (g.K + 127) / 128;
+    const bool ragged = (g.K % 128) != 0;
+    const int wrow0 = jn * NB;  // first weight row of this CTA
+    // the second 128-row weight half exists (down: rows 128..255 of the 256-row tile; gate/up: always)
+    const bool b1 = kGateUp || wrow0 + 128 < g.Nrows;
+    const int ntW = (g.Nrows + 127) / 128;  // 128-row weight tiles (atoms)
+    const uint8_t *ex = g.bank + (size_t)expert * g.expert_bytes;
+    const uint8_t *exat = g.atoms + (size_t)expert * g.atom_slot_bytes;
+
+    if (warp == 1) tmem_alloc(&tslot, kTmemCols);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(&done, 1);
+        fence_barrier_init();
+        tma_prefetch_desc(&mapA);
+        tma_prefetch_desc(&mapB0);
+        tma_prefetch_desc(&mapB1);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = tslot;
+
+    if (warp == 0) {
+        bool ok = true;
+        for (int i = 0; i < nks && ok; ++i) {
+            const int st = i % S;
+            if (lane == 0) ok = mbar_wait(&empty[st], ((i / S) & 1) ^ 1, g.err, kErrEmpty);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            uint8_t *sS = smem + st * kStage;
+            const bool tail = ragged && i == nks - 1;
+            // weight tile halves: gate/up -> (Wg rows, Wu rows) of one 128-row tile; down -> two 128-row tiles
+            const int r0 = kGateUp ? wrow0 : wrow0, r1 = kGateUp ? wrow0 : wrow0 + 128;
+            const size_t atom0 = g.atom_off_b0 + ((size_t)(r0 >> 7) * nks + i) * kAtom;
+            const size_t atom1 = g.atom_off_b1 + ((size_t)(r1 >> 7) * nks + i) * kAtom;
+            if (tail) {
+                load_tail_tile(sS + kOffB0, ex + g.off_b0_codes, g.Nrows, r0, g.K, i);
+                if (b1) load_tail_tile(sS + kOffB1, ex + g.off_b1_codes, g.Nrows, r1, g.K, i);
+            }
+            if (lane == 0) {
+                const uint32_t wtx = tail ? 0u : (uint32_t)kTileWTx;
+                mbar_expect_tx(&full[st], kTileActTx + wtx * (b1 ? 2u : 1u) + kAtom * (b1 ? 3u : 2u));
+                tma_load_3d(&mapA, &full[st], sS, i * 128, tile * 128, 0);
+                if (!tail) {
+                    tma_load_3d(&mapB0, &full[st], sS + kOffB0, i * 128, r0, expert);
+                    if (b1) tma_load_3d(&mapB1, &full[st], sS + kOffB1, i * 128, r1, expert);
+                }
+                bulk_copy(sS + kOffAtA, g.Aat + ((size_t)tile * nks + i) * kAtom, kAtom, &full[st]);
+                bulk_copy(sS + kOffAtB0, exat + atom0, kAtom, &full[st]);
+                if (b1 && (kGateUp || (r1 >> 7) < ntW)) bulk_copy(sS + kOffAtB1, exat + atom1, kAtom, &full[st]);
+            }
+            __syncwarp();
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = mx_idesc(kFmtE4M3, kFmtE2M1, NB);
+            bool ok = true;
+            for (int i = 0; i < nks && ok; ++i) {
+                const int st = i % S;
+                ok = mbar_wait(&full[st], (i / S) & 1, g.err, kErrFull);
+                if (!ok) break;
+                tc_fence_after();
+                uint8_t *sS = smem + st * kStage;
+                const uint32_t sfa = tbase + kColSF + 12 * st, sfb0 = sfa + 4, sfb1 = sfa + 8;
+                atom_to_tmem(sfa, sS + kOffAtA);
+                atom_to_tmem(sfb0, sS + kOffAtB0);
+                if (b1) atom_to_tmem(sfb1, sS + kOffAtB1);
+                const uint32_t aA = smem_u32(sS), aB0 = aA + kOffB0, aB1 = aA + kOffB1;
+                const int nk = (ragged && i == nks - 1) ? 2 : 4;
+                for (int kk = 0; kk < nk; ++kk) {
+                    const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                    if (kGateUp) {
+                        mma_mx(tbase, sw128_desc(aA + kk * 32), sw128_desc(aB0 + kk * 32), idesc, kk, sfa, sfb0, acc);
+                        mma_mx(tbase + 128, sw128_desc(aA + kk * 32), sw128_desc(aB1 + kk * 32), idesc, kk, sfa, sfb1,
+                               acc);
+                    } else {
+                        // one N = 256 MMA over both halves (contiguous in smem); B scales in two atoms
+                        mma_mx(tbase, sw128_desc(aA + kk * 32), sw128_desc(aB0 + kk * 32), idesc, kk, sfa, sfb0, acc);
+                    }
+                }
+                mma_commit(&empty[st]);
+            }
+            mma_commit(&done);
+        }
+        __syncwarp();
+    }
+
+    // ---------------- epilogue: thread r owns route row r of the tile ----------------
+    const int r = warp * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const bool valid = r < nrows;
+    const bool got = __all_sync(0xffffffffu, mbar_wait(&done, 0, g.err, kErrDone));
+    tc_fence_after();
+    const int pr = tile * 128 + r;  // padded route row
+    if (kGateUp) {
+        // h = SiLU(g) u for 128 columns of I, one 32-column MXFP8 block at a time
+        for (int c = 0; c < 4; ++c) {
+            float h[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) h[j] = 0.f;
+            if (got) {
+                uint32_t gg[8], uu[8];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    tmem_ld8x2_sync(tbase + lane_off + 32 * c + 8 * q, gg, tbase + 128 + lane_off + 32 * c + 8 * q, uu);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        h[8 * q + j] = valid ? silu(__uint_as_float(gg[j])) * __uint_as_float(uu[j]) : 0.f;
+                }
+            }
+            float amax = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(h[j]));
+            const int X = mxfp8_exponent(amax);
+            const float inv = e8m0_value(e8m0_byte(-X));
+            uint32_t w[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t lo = f32x2_to_e4m3x2(h[4 * j] * inv, h[4 * j + 1] * inv);
+                const uint32_t hi = f32x2_to_e4m3x2(h[4 * j + 2] * inv, h[4 * j + 3] * inv);
+                w[j] = lo | (hi << 16);
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(g.HP + (size_t)pr * g.Ipad + jn * 128 + 32 * c);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            g.HA[((size_t)tile * g.nksI + jn) * kAtom + atom_byte(r, c)] = (uint8_t)(X + 127);
+        }
+    } else {
+        // y * w for 256 columns of H.  The tensor-memory loads are warp-aligned: every lane issues them,
+        // rows past the tile's routes only skip the stores.
+        const float w = valid ? g.hot_w[g.act_off[aidx] + (pr - g.poff[aidx])] : 0.f;
+        for (int c = 0; c < 8; ++c) {
+            const int col = wrow0 + 32 * c;
+            if (col >= g.H) break;  // H % 32 == 0; the same for every lane
+            float y[32];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t rr[8];
+                if (got)
+                    tmem_ld8_sync(tbase + lane_off + 32 * c + 8 * q, rr);
+                else
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) rr[j] = 0u;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) y[8 * q + j] = w * __uint_as_float(rr[j]);
+            }
+            if (valid) {
+                float4 *dst = reinterpret_cast<float4 *>(g.YP + (size_t)pr * g.H + col);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) dst[j] = make_float4(y[4 * j], y[4 * j + 1], y[4 * j + 2], y[4 * j + 3]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncwarp();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tbase, kTmemCols);
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ combine
+
+// One block per token: its routes in ascending expert order, each found by binary search among the
+// expert's tokens (ascending), summed into out.
+__global__ void __launch_bounds__(256) prefill_combine_kernel(const int32_t *topk_ids, int k, const int32_t *e2a,
+                                                              const int32_t *act_off, const int32_t *act_cnt,
+                                                              const int32_t *hot_token, const int32_t *poff,
+                                                              const float *YP, int H, void *out, int out_f32) {
+    __shared__ int s_pr[kMaxTopK];
+    const int t = blockIdx.x;
+    if (threadIdx.x == 0) {
+        int ids[kMaxTopK];
+        for (int j = 0; j < k; ++j) {
+            const int e = topk_ids[(size_t)t * k + j];
+            int q = j;
+            while (q > 0 && ids[q - 1] > e) {
+                ids[q] = ids[q - 1];
+                --q;
+            }
+            ids[q] = e;
+        }
+        for (int j = 0; j < k; ++j) {
+            const int a = e2a[ids[j]];
+            int lo = act_off[a], hi = act_off[a] + act_cnt[a];  // hot_token ascending in [lo, hi)
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (hot_token[mid] < t) lo = mid + 1;
+                else hi = mid;
+            }
+            s_pr[j] = poff[a] + (lo - act_off[a]);
+        }
+    }
+    __syncthreads();
+    for (int h = threadIdx.x; h < H; h += blockDim.x) {
+        float acc = 0.f;
+        for (int j = 0; j < k; ++j) acc += YP[(size_t)s_pr[j] * H + h];
+        if (out_f32)
+            reinterpret_cast<float *>(out)[(size_t)t * H + h] = acc;
+        else
+            reinterpret_cast<__nv_bfloat16 *>(out)[(size_t)t * H + h] = __float2bfloat16_rn(acc);
+    }
+}
+
+// ------------------------------------------------------------------ launchers
+
+int prefill_tiles_cap(int max_routes, int E) { return (max_routes + 127) / 128 + (E < max_routes ? E : max_routes); }
+
+cudaError_t launch_prefill(const PrefillLaunch &P, cudaStream_t s) {
+    const ExpertGeometry &geo = P.geo;
+    const TcAtomLayout l = tc_atom_layout(geo.H, geo.I);
+    prefill_plan_kernel<<<1, 256, 0, s>>>(P.counts, P.act_expert, P.act_cnt, P.E, P.poff, P.e2a, P.tile_aidx,
+                                          P.tile_nrows, P.ntiles, P.tiles_cap);
+    const int nb = geo.H / 32;
+    const long tasks = (long)P.max_routes * nb;
+    prefill_quant_kernel<<<(unsigned)((tasks + 7) / 8), 256, 0, s>>>(P.x, geo.H, P.counts, P.hot_expert, P.hot_token,
+                                                                      P.act_off, P.e2a, P.poff, P.XP, P.Hpad, P.XA,
+                                                                      l.nks);
+    static bool cfg = false;
+    if (!cfg) {
+        cudaFuncSetAttribute(prefill_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaFuncSetAttribute(prefill_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cfg = true;
+    }
+    GemmArgs g{};
+    g.bank = P.bank;
+    g.atoms = P.atoms;
+    g.expert_bytes = geo.expert_bytes;
+    g.atom_slot_bytes = l.slot_bytes;
+    g.ntiles = P.ntiles;
+    g.tile_aidx = P.tile_aidx;
+    g.tile_nrows = P.tile_nrows;
+    g.act_expert = P.act_expert;
+    g.act_off = P.act_off;
+    g.poff = P.poff;
+    g.hot_w = P.hot_w;
+    g.HP = P.HP;
+    g.HA = P.HA;
+    g.Ipad = P.Ipad;
+    g.nksI = l.nksI;
+    g.YP = P.YP;
+    g.H = geo.H;
+    g.err = P.err;
+    // gate/up: A = x (route order), B = Wg / Wu tiles of 128 rows of I
+    g.off_b0_codes = geo.off_wg_codes;
+    g.off_b1_codes = geo.off_wu_codes;
+    g.atom_off_b0 = l.off_g;
+    g.atom_off_b1 = l.off_u;
+    g.K = geo.H;
+    g.Nrows = geo.I;
+    g.nN = l.ntI;
+    g.Aat = P.XA;
+    prefill_gemm_kernel<1><<<P.tiles_cap * g.nN, kThreads, kSmemBytes, s>>>(*P.mapXP, *P.mapG, *P.mapU, g);
+    // down: A = h (route order), B = Wd tiles of 256 rows of H
+    g.off_b0_codes = geo.off_wd_codes;
+    g.off_b1_codes = geo.off_wd_codes;
+    g.atom_off_b0 = l.off_d;
+    g.atom_off_b1 = l.off_d;
+    g.K = geo.I;
+    g.Nrows = geo.H;
+    g.nN = (geo.H + 255) / 256;
+    g.Aat = P.HA;
+    prefill_gemm_kernel<0><<<P.tiles_cap * g.nN, kThreads, kSmemBytes, s>>>(*P.mapHP, *P.mapD, *P.mapD, g);
+    prefill_combine_kernel<<<P.M, 256, 0, s>>>(P.topk_ids, P.k, P.e2a, P.act_off, P.act_cnt, P.hot_token, P.poff,
+                                               P.YP, geo.H, P.out, P.out_f32);
+    return cudaGetLastError();
+}
+
+void launch_build_weight_atoms_bank(const uint8_t *bank, int E, const ExpertGeometry &g, uint8_t *atoms,
+                                    cudaStream_t s) {
+    const TcAtomLayout l = tc_atom_layout(g.H, g.I);
+    for (int e = 0; e < E; ++e)
+        launch_build_weight_atoms(bank + (size_t)e * g.expert_bytes, g, atoms + (size_t)e * l.slot_bytes, s);
+}
+
+}  // namespace moe

@@ -311,5 +311,46 @@ __device__ __forceinline__ uint8_t split_term(float &res, uint32_t &scale_byte) 
     return code;
 }
 
+// ------------------------------------------------ operand tiles shared by the decode and prefill kernels
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.f + expf(-g)); }
+
+// Scale atom (512 bytes in smem, 32 rows of 16 bytes) -> 4 TMEM columns in every lane quadrant.
+__device__ __forceinline__ void atom_to_tmem(uint32_t tcol, const void *atom) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_u32(atom) >> 4) & 0x3FFF);
+    d |= (uint64_t)(16 >> 4) << 16;
+    d |= (uint64_t)(128 >> 4) << 32;  // next 8 rows
+    d |= (uint64_t)1 << 46;
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tcol), "l"(d) : "memory");
+}
+
+// The last k-step of a row tile when K % 128 == 64: 64 codes per row copied by the whole warp into the
+// padded, swizzled smem layout (unit u of row r at 16-byte chunk u ^ (r % 8)); all loads before any store.
+__device__ __forceinline__ void load_tail_tile(uint8_t *dst, const uint8_t *codes, int rows, int row0, int K,
+                                               int kstep) {
+    const int lane = threadIdx.x & 31;
+    constexpr int kUnits = 4, kPerLane = 128 * kUnits / 32;
+    uint2 v[kPerLane];
+#pragma unroll
+    for (int j = 0; j < kPerLane; ++j) {
+        const int i = lane + 32 * j, r = i / kUnits, u = i % kUnits;
+        v[j] = make_uint2(0u, 0u);
+        if (row0 + r < rows)
+            v[j] = __ldg(reinterpret_cast<const uint2 *>(codes + (size_t)(row0 + r) * (K / 2) + kstep * 64 + u * 8));
+    }
+#pragma unroll
+    for (int j = 0; j < kPerLane; ++j) {
+        const int i = lane + 32 * j, r = i / kUnits, u = i % kUnits;
+        *reinterpret_cast<uint4 *>(dst + r * 128 + ((u ^ (r & 7)) * 16)) = make_uint4(v[j].x, v[j].y, 0u, 0u);
+    }
+    fence_proxy_async();
+    __syncwarp();
+}
+
 }  // namespace tc
 }  // namespace moe

@@ -1,0 +1,109 @@
+"""Prefill (M > 8) on the tensor cores over the staged expert bank, against the oracle's prefill reading.
+
+With every expert staged, every route is hot and the output is
+  out[t] = sum over t's top-k experts in ascending expert order of w * y_e(x_t),
+where y_e is the expert FFN with x and h passed through MXFP8 (32-element
+E4M3 blocks, OCP MX v1.0 conversion rule) before their products with the
+MXFP4 weights (oracle.expert_ffn_mxfp8).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from expert_offload_moe_gb300 import stack, synth
+
+from parity import compare_values, near_tie_tokens
+
+pytestmark = pytest.mark.gpu
+
+
+def prefill_reference(li, x_bits, k, H, I, tokens):
+    """The oracle's prefill output for the listed tokens: fp32, experts summed in ascending order."""
+    logits = oracle.router_logits(x_bits, li.Wr, li.bias)
+    ids, w = oracle.topk_softmax(logits, k)
+    bank = li.bank.numpy()
+    out = np.zeros((len(tokens), H), dtype=np.float32)
+    for i, t in enumerate(tokens):
+        acc = np.zeros(H, dtype=np.float32)
+        for j in np.argsort(ids[t], kind="stable"):
+            y = oracle.expert_ffn_mxfp8(bank[ids[t][j]], H, I, x_bits[t])
+            acc = (acc + np.float32(w[t][j]) * y).astype(np.float32)
+        out[i] = acc
+    return out, logits
+
+
+def run_prefill(li, x_bits, M, out_f32=True, max_tokens=None):
+    w = li.w
+    lay = li.make_layer(max_tokens=max_tokens or M, out_f32=out_f32)
+    try:
+        staging = torch.empty(w.experts * w.expert_bytes, dtype=torch.uint8, device="cuda")
+        lay.attach_staging(staging)
+        lay.stage_all()
+        x = stack.bf16_tensor(x_bits)
+        out = torch.empty((M, w.hidden), dtype=torch.float32 if out_f32 else torch.bfloat16, device="cuda")
+        lay.route(x, M)
+        lay.forward_slots(x, out, M)
+        torch.cuda.synchronize()
+        lay.check_error()
+        got = out.float().cpu().numpy()
+    finally:
+        lay.close()
+    return got
+
+
+def _tiny():
+    base = synth.WORKLOADS["tiny_h256_i128_e16k2"]
+    return synth.Workload("tiny_prefill", 1, base.hidden, base.inter, base.experts, base.top_k, base.experts,
+                          (16,), 1, bias_tau=0.25)
+
+
+@pytest.mark.parametrize("M", [9, 40, 300])
+def test_prefill_tiny_all_tokens(M):
+    """Every token and column: M spans one and several 128-route tiles per expert (ragged last tiles)."""
+    w = _tiny()
+    li = stack.LayerInputs(w, 0)
+    x_bits = synth.activations(0, 0, 11, M, w.hidden)
+    got = run_prefill(li, x_bits, M)
+    ref, logits = prefill_reference(li, x_bits, w.top_k, w.hidden, w.inter, range(M))
+    compare_values(got, ref, True, exclude=np.where(near_tie_tokens(logits, w.top_k))[0])
+
+
+def test_prefill_tiny_bf16_out():
+    w = _tiny()
+    li = stack.LayerInputs(w, 0)
+    M = 64
+    x_bits = synth.activations(0, 0, 12, M, w.hidden)
+    got = run_prefill(li, x_bits, M, out_f32=False)
+    ref, logits = prefill_reference(li, x_bits, w.top_k, w.hidden, w.inter, range(M))
+    compare_values(got, ref, False, exclude=np.where(near_tie_tokens(logits, w.top_k))[0])
+
+
+def test_prefill_gptoss_shape_sampled():
+    """The gpt-oss-20B-shaped prefill batch (2048 tokens, 32 experts, k = 4; ragged H = I = 2880), checked
+    on sampled tokens the oracle computes one by one."""
+    w = synth.WORKLOADS["gptoss20b_prefill2048_s16_lfu_drift"]
+    li = stack.LayerInputs(w, 0)
+    M = w.prefill_tokens
+    x_bits = synth.activations(0, 0, 0, M, w.hidden)
+    got = run_prefill(li, x_bits, M)
+    tokens = [0, 1, 777, 1500, M - 1]
+    ref, logits = prefill_reference(li, x_bits, w.top_k, w.hidden, w.inter, tokens)
+    tie = near_tie_tokens(logits, w.top_k)
+    keep = [i for i, t in enumerate(tokens) if not tie[t]]
+    compare_values(got[tokens][keep], ref[keep], True)
+
+
+def test_prefill_needs_staging():
+    w = _tiny()
+    li = stack.LayerInputs(w, 0)
+    lay = li.make_layer(max_tokens=16, out_f32=True)
+    try:
+        M = 12
+        x = stack.bf16_tensor(synth.activations(0, 0, 13, M, w.hidden))
+        out = torch.empty((M, w.hidden), dtype=torch.float32, device="cuda")
+        lay.route(x, M)
+        with pytest.raises(Exception):
+            lay.forward_slots(x, out, M)
+    finally:
+        lay.close()
