@@ -133,7 +133,7 @@ def cpu_baseline(w, n_layers):
                       f"{t:.1f} s), time scaled to the {w.layers}-layer stack"}
 
 
-def run_reference(args):
+def run_reference(args, prefill=False):
     rank, world, _ = dist_env()
     if rank != 0:
         return
@@ -141,18 +141,23 @@ def run_reference(args):
 
     w = synth.WORKLOADS[args.workload]
     total = 0.0
+    n_tok = 2 if prefill else 1
     for i in range(args.warmup + args.steps):
-        t = oracle_token_seconds(w, args.ref_layers) / args.ref_layers * w.layers
+        if prefill:
+            t = oracle_prefill_seconds(w, n_tok) * w.layers
+        else:
+            t = oracle_token_seconds(w, args.ref_layers) / args.ref_layers * w.layers
         if i >= args.warmup:
             total += t
-    val = args.steps / total
-    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
+    val = args.steps * n_tok / total
+    what = (f"{n_tok} prompt tokens through 1 of {w.layers} layers" if prefill
+            else f"1 token through {args.ref_layers} of {w.layers} layers")
+    line = {"impl": "reference", "metric": PREFILL_METRIC if prefill else METRIC, "value": val, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": w.name, "layers": w.layers, "tokens_per_step": 1},
+            "config": {"workload": w.name, "layers": w.layers, "tokens_per_step": n_tok},
             "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": f"each step: 1 token through {args.ref_layers} of {w.layers} layers on one "
-                                       f"core, time scaled to {w.layers} layers"},
+                             "sample": f"each step: {what} on one core, time scaled to {w.layers} layers"},
             "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -308,12 +313,150 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+PREFILL_METRIC = "MoE-layer prefill tokens/s (M=2048)"
+FP8_OVER_BF16 = 2.0  # nominal dense ratio of the 8-bit block-scaled tensor rate to bf16 (4.5 / 2.25 PFLOP/s)
+
+
+def run_prefill(args):
+    """The prompt phase of the prefill-then-decode workload: every layer routes and runs a batch of
+    M = prefill_tokens on the tensor cores over its staged expert bank.  A step = all layers, eager launches."""
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    from expert_offload_moe_gb300 import build as moe_build
+    from expert_offload_moe_gb300 import moe, stack, synth
+
+    moe_build.build()
+    moe.lib()
+    w = synth.WORKLOADS[args.workload]
+    st = stack.PrefillStack(w, n_layers=args.layers, seed=rank, n_inputs=2)
+    L, M = st.L, st.M
+    stream = torch.cuda.current_stream()
+    for i in range(args.warmup):
+        st.step(i)
+    torch.cuda.synchronize()
+    clk = Clocks(local)
+    clk.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        st.step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = clk.stop()
+    t_ms = e0.elapsed_time(e1)
+    value = args.steps * M / (t_ms / 1e3)
+
+    # per-GEMM device time (events on the launching stream, around each launch)
+    for lay in st.layers:
+        lay.profile(True)
+    kt_steps = min(args.steps, 8)
+    for i in range(kt_steps):
+        st.step(i)
+    torch.cuda.synchronize()
+    prof = np.zeros(4)
+    for lay in st.layers:
+        prof += lay.profile_read()
+        lay.profile(False)
+    launches = max(prof[3], 1)
+    route_us, gateup_us, down_us = (1e3 * prof[i] / launches for i in range(3))
+    routes = M * w.top_k
+    gateup_flop = 2.0 * routes * 2 * w.inter * w.hidden
+    down_flop = 2.0 * routes * w.hidden * w.inter
+    pk, pk_src = peaks()
+    bf16 = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops", PEAKS_FALLBACK["bf16_tflops"]))
+    peak = bf16 * FP8_OVER_BF16
+    achieved = gateup_flop / (gateup_us * 1e-6) / 1e12
+
+    # e2e: the step's activations copied in from pinned host memory and the outputs read back, every step
+    x_host = torch.empty(st.x_all.shape[1:], dtype=torch.bfloat16, pin_memory=True)
+    x_host.copy_(st.x_all[0].cpu())
+    out_host = torch.empty(st.out.shape, dtype=st.out.dtype, pin_memory=True)
+    for i in range(args.warmup):
+        st.x_all[0].copy_(x_host, non_blocking=True)
+        st.step(0)
+        out_host.copy_(st.out, non_blocking=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(args.steps):
+        st.x_all[0].copy_(x_host, non_blocking=True)
+        st.step(0)
+        out_host.copy_(st.out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_e2e = e0.elapsed_time(e1)
+    e2e = {"value": args.steps * M / (t_e2e / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": int(x_host.numel() * 2), "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size())}
+    step_s = t_ms / args.steps * 1e-3
+    line = {
+        "metric": PREFILL_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8*mxfp4->f32", "data": "synthetic",
+        "config": {"workload": w.name, "phase": "prefill", "layers": L, "hidden": w.hidden, "inter": w.inter,
+                   "experts": w.experts, "top_k": w.top_k, "tokens_per_step": M, "parallelism": f"replicas{world}",
+                   "weights": "mxfp4 experts (whole bank staged on the device), fp32 router, fp32 accumulation",
+                   "l2": "inputs larger than L2: each step reads %.2f GB of expert weights and %.2f GB of activations"
+                         % (L * w.experts * w.expert_bytes / 1e9, L * M * w.hidden * 2 / 1e9),
+                   "tensor_tflops_step": L * (gateup_flop + down_flop) / step_s / 1e12,
+                   "kernel_us": {"route": route_us, "gateup_gemm": gateup_us, "down_gemm": down_us}},
+        "roofline": {"bound": "tensor", "kernel": "prefill_gemm_kernel<1> (gate/up)", "achieved": achieved,
+                     "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                     "flop_per_launch": gateup_flop, "avg_launch_us": gateup_us,
+                     "peak_source": ("measured bf16_tflops_sustained (MEASURED_PEAKS.json)" if pk_src == "measured"
+                                     else "fallback 1.9 PFLOP/s bf16") + " x 2 (nominal 8-bit / bf16 ratio)"},
+        "clocks": clocks,
+        "gpu_launches": int(args.steps * L * 6),
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_prefill_baseline(w)
+    st.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def oracle_prefill_seconds(w, n_tokens, seed=0):
+    """The oracle, as it stands, on one host core: seconds for n_tokens prompt tokens through one layer."""
+    import oracle
+    from expert_offload_moe_gb300 import synth
+
+    oracle.build()
+    Wr = synth.router_weights(seed, 0, w.experts, w.hidden)
+    b = synth.router_bias(seed, 0, w.experts, w.bias_tau)
+    ex = synth.expert_records(seed, 0, w.experts, w.hidden, w.inter)
+    x = synth.activations(seed, 0, 0, n_tokens, w.hidden)
+    t0 = time.perf_counter()
+    ids, wt = oracle.topk_softmax(oracle.router_logits(x, Wr, b), w.top_k)
+    for t in range(n_tokens):
+        for j in range(w.top_k):
+            oracle.expert_ffn_mxfp8(ex[ids[t][j]], w.hidden, w.inter, x[t])
+    return time.perf_counter() - t0
+
+
+def cpu_prefill_baseline(w, n_tokens=4):
+    t = oracle_prefill_seconds(w, n_tokens)
+    return {"value": n_tokens / (t * w.layers), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n_tokens} prompt tokens through 1 of {w.layers} layers (single-threaded C oracle, "
+                      f"{t:.1f} s), time scaled to the {w.layers}-layer stack"}
+
+
 def main():
     args = parse()
+    prefill = synth_workload(args.workload).prefill_tokens > 0
     if args.impl == "reference":
-        run_reference(args)
+        run_reference(args, prefill)
+    elif prefill:
+        run_prefill(args)
     else:
         run_ours(args)
+
+
+def synth_workload(name):
+    from expert_offload_moe_gb300 import synth
+
+    return synth.WORKLOADS[name]
 
 
 if __name__ == "__main__":

@@ -15,6 +15,7 @@ constexpr int kMaxExperts = 512;
 constexpr int kMaxTokens = 4096;
 constexpr int kDecodeMaxTokens = 8;            // M <= 8 takes the decode kernels
 constexpr int kRouteChunk = 256;               // router columns per warp task
+constexpr int kPfRouteTok = 16;                // prefill routing: tokens per thread block
 constexpr int kDecodeSmemLimit = 200 * 1024;   // decode activations staged in shared memory
 
 // Device scratch written by the route kernel.
@@ -35,6 +36,8 @@ struct RouteBuffers {
     int32_t *hist;        // [E]
     int32_t *counts;      // [4] n_hot, n_cold, n_active, M
     unsigned *arrive;     // [1] grid arrival counter (reset by the last block)
+    int32_t *blk_cnt;     // prefill: [ceil(max_tokens / kPfRouteTok)][E] routes per (token tile, expert)
+    int32_t *route_rank;  // prefill: [max_tokens * k] rank of a route among its tile's routes to its expert
 };
 
 struct RouteParams {
@@ -132,6 +135,7 @@ struct PrefillLaunch {
     void *out;
     int out_f32;
     const CUtensorMap *mapXP, *mapHP, *mapG, *mapU, *mapD;
+    cudaEvent_t ev[4];  // optional (nullptr = none): recorded before/after the gate/up and the down GEMM
 };
 int prefill_tiles_cap(int max_routes, int E);  // 128-row route tiles the buffers must hold
 cudaError_t launch_prefill(const PrefillLaunch &P, cudaStream_t s);

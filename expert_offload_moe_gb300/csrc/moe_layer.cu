@@ -172,6 +172,19 @@ cudaError_t prof_mark(moe_layer *L, int which, cudaStream_t s) {
     return cudaEventRecord(v[n++], s);
 }
 
+// The next event of timed kernel `which` for a caller that records it itself (nullptr when not profiling).
+cudaEvent_t prof_next(moe_layer *L, int which) {
+    if (!L->prof) return nullptr;
+    auto &v = L->prof_ev[which];
+    size_t &n = L->prof_n[which];
+    if (n == v.size()) {
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+        v.push_back(e);
+    }
+    return v[n++];
+}
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link against libcuda).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -451,7 +464,9 @@ int moe_layer_create(const moe_layer_desc *desc, const float *router_w_dev, cons
         nh * 4, nh * 4, nh * 4,                  // hot expert/token/w
         nh * 4, nh * 4, nh * 4, nh * 4,          // act expert/slot/off/cnt
         nh * 4, nh * 4, nh * 4,                  // cold token/expert/w
-        (size_t)E * 4, 16, 16};                  // hist, counts, arrive
+        (size_t)E * 4, 16, 16,                   // hist, counts, arrive
+        (size_t)((mt + moe::kPfRouteTok - 1) / moe::kPfRouteTok) * E * 4,  // blk_cnt
+        (size_t)mt * k * 4};                     // route_rank
     size_t total = 0;
     for (size_t s : sizes) total += align_up(s, 256);
     CREATE_TRY(cudaMalloc(&L->dev_block, total));
@@ -462,7 +477,7 @@ int moe_layer_create(const moe_layer_desc *desc, const float *router_w_dev, cons
                         (void **)&L->rb.act_expert, (void **)&L->rb.act_slot, (void **)&L->rb.act_off,
                         (void **)&L->rb.act_cnt, (void **)&L->rb.cold_token, (void **)&L->rb.cold_expert,
                         (void **)&L->rb.cold_w, (void **)&L->rb.hist, (void **)&L->rb.counts,
-                        (void **)&L->rb.arrive};
+                        (void **)&L->rb.arrive, (void **)&L->rb.blk_cnt, (void **)&L->rb.route_rank};
         for (size_t i = 0; i < sizeof(sizes) / sizeof(sizes[0]); ++i) {
             *dst[i] = p;
             p += align_up(sizes[i], 256);
@@ -700,9 +715,11 @@ int moe_forward_slots(moe_layer *L, const void *x_dev, void *out_dev, int32_t M,
         P.mapG = &L->mapSG;
         P.mapU = &L->mapSU;
         P.mapD = &L->mapSD;
-        CUDA_TRY(prof_mark(L, 1, st));
+        P.ev[0] = prof_next(L, 1);  // gate/up GEMM
+        P.ev[1] = prof_next(L, 1);
+        P.ev[2] = prof_next(L, 2);  // down GEMM
+        P.ev[3] = prof_next(L, 2);
         CUDA_TRY(moe::launch_prefill(P, st));
-        CUDA_TRY(prof_mark(L, 1, st));
     }
     CUDA_TRY(cudaStreamWaitEvent(st, L->ev_route, 0));  // join the mirror copies
     return MOE_OK;

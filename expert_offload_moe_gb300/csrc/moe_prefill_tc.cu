@@ -403,7 +403,9 @@ cudaError_t launch_prefill(const PrefillLaunch &P, cudaStream_t s) {
     g.Nrows = geo.I;
     g.nN = l.ntI;
     g.Aat = P.XA;
+    if (P.ev[0]) cudaEventRecord(P.ev[0], s);
     prefill_gemm_kernel<1><<<P.tiles_cap * g.nN, kThreads, kSmemBytes, s>>>(*P.mapXP, *P.mapG, *P.mapU, g);
+    if (P.ev[1]) cudaEventRecord(P.ev[1], s);
     // down: A = h (route order), B = Wd tiles of 256 rows of H
     g.off_b0_codes = geo.off_wd_codes;
     g.off_b1_codes = geo.off_wd_codes;
@@ -413,7 +415,9 @@ cudaError_t launch_prefill(const PrefillLaunch &P, cudaStream_t s) {
     g.Nrows = geo.H;
     g.nN = (geo.H + 255) / 256;
     g.Aat = P.HA;
+    if (P.ev[2]) cudaEventRecord(P.ev[2], s);
     prefill_gemm_kernel<0><<<P.tiles_cap * g.nN, kThreads, kSmemBytes, s>>>(*P.mapHP, *P.mapD, *P.mapD, g);
+    if (P.ev[3]) cudaEventRecord(P.ev[3], s);
     prefill_combine_kernel<<<P.M, 256, 0, s>>>(P.topk_ids, P.k, P.e2a, P.act_off, P.act_cnt, P.hot_token, P.poff,
                                                P.YP, geo.H, P.out, P.out_f32);
     return cudaGetLastError();

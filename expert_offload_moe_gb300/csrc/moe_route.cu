@@ -439,6 +439,273 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// Prefill routing (M > 8; every expert is hot, slot = expert id).
+//
+// Block b owns tokens [16 b, 16 b + 16).  It stages its 16 rows of x in shared
+// memory and streams the router through shared memory 128 columns x 32
+// experts at a time (transposed so lane e reads expert e without bank
+// conflicts); warp w accumulates 4 tokens x 32 experts over one half of each
+// 128-column chunk, and the two halves are added at the end.  Each block then
+// takes top-k + softmax for its tokens (ties to the lower id, as in decode),
+// counts its routes per expert and ranks each route among the block's routes
+// to the same expert (token order).  The last block to arrive turns the
+// per-block counts into offsets and scatters every route to
+//   hot position = offset(expert) + routes to that expert in earlier blocks + rank,
+// i.e. the hot list ordered by (expert, token) -- a counting sort with no
+// serial pass over the routes.
+constexpr int kPfWc = 128;  // router columns per staged chunk
+constexpr int kPfTokWarp = 4;
+
+struct PfSmem {
+    static size_t bytes(int H, int E) {
+        return (size_t)kPfRouteTok * H * 2 + 2 * kPfWc * 32 * 4 + kPfRouteTok * 32 * 4 + (size_t)kPfRouteTok * E * 4;
+    }
+};
+
+__device__ __forceinline__ void pf_load_w(const RouteParams &p, int eg, int c, float4 (&r)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int idx = threadIdx.x + i * kThreads, el = idx & 31, cg = idx >> 5;
+        const int e = eg * 32 + el, col = c * kPfWc + cg * 4;
+        r[i] = (e < p.E && col < p.H) ? __ldg(reinterpret_cast<const float4 *>(p.Wr + (size_t)e * p.H + col))
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+__device__ __forceinline__ void pf_store_w(float *sW, const float4 (&r)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int idx = threadIdx.x + i * kThreads, el = idx & 31, cg = idx >> 5;
+        sW[(cg * 4 + 0) * 32 + el] = r[i].x;
+        sW[(cg * 4 + 1) * 32 + el] = r[i].y;
+        sW[(cg * 4 + 2) * 32 + el] = r[i].z;
+        sW[(cg * 4 + 3) * 32 + el] = r[i].w;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) route_prefill_kernel(RouteParams p) {
+    extern __shared__ __align__(16) unsigned char pf_smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int H = p.H, E = p.E, M = p.M, k = p.k;
+    const int t0 = blockIdx.x * kPfRouteTok;
+    uint16_t *sX = reinterpret_cast<uint16_t *>(pf_smem);                       // [16][H]
+    float *sW = reinterpret_cast<float *>(pf_smem + (size_t)kPfRouteTok * H * 2);  // [2][128][32]
+    float *sRed = sW + 2 * kPfWc * 32;                                           // [16][32]
+    float *sL = sRed + kPfRouteTok * 32;                                         // [16][E]
+    __shared__ float s_bias[kMaxExperts];
+    __shared__ int s_cnt[kMaxExperts];
+    __shared__ int s_off[kMaxExperts];
+    __shared__ int s_act[kMaxExperts];
+    __shared__ int s_ids[kPfRouteTok][kMaxTopK];
+    __shared__ int s_sel_id[kWarps][kMaxTopK];
+    __shared__ float s_sel_l[kWarps][kMaxTopK];
+
+    const int nc = (H + kPfWc - 1) / kPfWc;
+    float4 wr[4];
+    pf_load_w(p, 0, 0, wr);  // the router is constant: read before waiting for the previous grid
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+        s_bias[e] = p.bias ? p.bias[e] : 0.f;
+        s_cnt[e] = 0;
+    }
+    tc::pdl_wait();
+    tc::pdl_trigger();
+
+    // x rows of the block (zeros past M)
+    const int hv = H / 8;
+    for (int q = threadIdx.x; q < kPfRouteTok * hv; q += kThreads) {
+        const int t = q / hv, c8 = q - t * hv;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (t0 + t < M) v = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)(t0 + t) * H) + c8);
+        reinterpret_cast<uint4 *>(sX + (size_t)t * H)[c8] = v;
+    }
+
+    // ---------------- logits: 32 experts at a time --------------------------
+    const int g = warp & 3, hh = warp >> 2;
+    const int neg = (E + 31) / 32;
+    for (int eg = 0; eg < neg; ++eg) {
+        if (eg > 0) pf_load_w(p, eg, 0, wr);
+        pf_store_w(sW, wr);
+        __syncthreads();
+        float acc[kPfTokWarp] = {0.f, 0.f, 0.f, 0.f};
+        for (int c = 0; c < nc; ++c) {
+            if (c + 1 < nc) pf_load_w(p, eg, c + 1, wr);
+            const float *w = sW + (c & 1) * kPfWc * 32;
+            const int col0 = c * kPfWc + hh * (kPfWc / 2);
+            if (col0 < H) {  // H % 64 == 0: a half chunk is all valid or all past H
+#pragma unroll 2
+                for (int j = 0; j < kPfWc / 2; j += 8) {
+                    float wv[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) wv[q] = w[(hh * (kPfWc / 2) + j + q) * 32 + lane];
+#pragma unroll
+                    for (int t = 0; t < kPfTokWarp; ++t) {
+                        const uint4 xv = *reinterpret_cast<const uint4 *>(sX + (size_t)(g * kPfTokWarp + t) * H + col0 + j);
+                        float a = acc[t];
+                        a = fmaf(bf16_lo(xv.x), wv[0], a);
+                        a = fmaf(bf16_hi(xv.x), wv[1], a);
+                        a = fmaf(bf16_lo(xv.y), wv[2], a);
+                        a = fmaf(bf16_hi(xv.y), wv[3], a);
+                        a = fmaf(bf16_lo(xv.z), wv[4], a);
+                        a = fmaf(bf16_hi(xv.z), wv[5], a);
+                        a = fmaf(bf16_lo(xv.w), wv[6], a);
+                        a = fmaf(bf16_hi(xv.w), wv[7], a);
+                        acc[t] = a;
+                    }
+                }
+            }
+            if (c + 1 < nc) pf_store_w(sW + ((c + 1) & 1) * kPfWc * 32, wr);
+            __syncthreads();
+        }
+        if (hh == 1)
+#pragma unroll
+            for (int t = 0; t < kPfTokWarp; ++t) sRed[(g * kPfTokWarp + t) * 32 + lane] = acc[t];
+        __syncthreads();
+        const int e = eg * 32 + lane;
+        if (hh == 0 && e < E)
+#pragma unroll
+            for (int t = 0; t < kPfTokWarp; ++t) {
+                const float v = acc[t] + sRed[(g * kPfTokWarp + t) * 32 + lane] + s_bias[e];
+                sL[(size_t)(g * kPfTokWarp + t) * E + e] = (v != v) ? -INFINITY : v;  // NaN marks a taken expert
+            }
+        __syncthreads();
+    }
+
+    // ---------------- top-k + softmax: two tokens per warp -------------------
+    for (int tl = warp; tl < kPfRouteTok; tl += kWarps) {
+        const int t = t0 + tl;
+        if (t >= M) continue;  // warp-uniform
+        float *row = sL + (size_t)tl * E;
+        for (int j = 0; j < k; ++j) {
+            float bv = -INFINITY;
+            int be = 0x7fffffff;
+            for (int e = lane; e < E; e += 32) {
+                const float v = row[e];
+                if (v != v) continue;
+                if (v > bv || (v == bv && e < be)) {
+                    bv = v;
+                    be = e;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                if (ov > bv || (ov == bv && oe < be)) {
+                    bv = ov;
+                    be = oe;
+                }
+            }
+            if (lane == 0) {
+                s_sel_id[warp][j] = be;
+                s_sel_l[warp][j] = bv;
+            }
+            if (lane == (be & 31)) row[be] = __int_as_float(0x7fc00000);
+            __syncwarp();
+        }
+        if (lane < k) {
+            const float lmax = s_sel_l[warp][0];
+            float den = 0.f;
+            for (int j = 0; j < k; ++j) den += expf(s_sel_l[warp][j] - lmax);
+            const int id = s_sel_id[warp][lane];
+            p.b.topk_ids[(size_t)t * k + lane] = id;
+            p.b.topk_w[(size_t)t * k + lane] = expf(s_sel_l[warp][lane] - lmax) / den;
+            s_ids[tl][lane] = id;
+            atomicAdd(&s_cnt[id], 1);
+        }
+        __syncwarp();
+    }
+    __syncthreads();
+    // rank of each route among the block's earlier tokens routed to the same expert
+    for (int r = threadIdx.x; r < kPfRouteTok * k; r += kThreads) {
+        const int tl = r / k, j = r - tl * k;
+        if (t0 + tl >= M) continue;
+        const int e = s_ids[tl][j];
+        int n = 0;
+        for (int u = 0; u < tl; ++u)
+            for (int i = 0; i < k; ++i) n += s_ids[u][i] == e;
+        p.b.route_rank[(size_t)(t0 + tl) * k + j] = n;
+    }
+    for (int e = threadIdx.x; e < E; e += kThreads) p.b.blk_cnt[(size_t)blockIdx.x * E + e] = s_cnt[e];
+
+    // ---------------- arrival: the last block scatters ----------------------
+    __shared__ int s_last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned prev;
+        asm volatile("atom.acq_rel.gpu.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(p.b.arrive) : "memory");
+        s_last = prev == gridDim.x - 1;
+        if (s_last) *p.b.arrive = 0u;
+    }
+    __syncthreads();
+    if (!s_last) return;
+
+    // per expert: exclusive prefix of the block counts (in place), tpe lanes per expert
+    const int nblk = gridDim.x;
+    int tpe = 1;  // a power of two <= 32, so an expert's lanes never straddle a warp
+    while (tpe < 32 && E * tpe * 2 <= kThreads) tpe *= 2;
+    for (int base = 0; base < E * tpe; base += kThreads) {
+        const int q = base + threadIdx.x;
+        const int e = q / tpe, part = q - e * tpe;  // tpe consecutive lanes share an expert
+        const int per = (nblk + tpe - 1) / tpe, b0 = min(part * per, nblk), b1 = min(b0 + per, nblk);
+        int sum = 0;
+        if (e < E) {
+#pragma unroll 4
+            for (int b = b0; b < b1; ++b) sum += __ldcg(p.b.blk_cnt + (size_t)b * E + e);
+        }
+        int x = sum;  // inclusive scan over the tpe lanes of this expert
+        for (int o = 1; o < tpe; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (part >= o) x += y;
+        }
+        const int total = __shfl_sync(0xffffffffu, x, (lane | (tpe - 1)));
+        int run = x - sum;
+        if (e < E) {
+            for (int b = b0; b < b1; ++b) {
+                const int v = __ldcg(p.b.blk_cnt + (size_t)b * E + e);
+                p.b.blk_cnt[(size_t)b * E + e] = run;
+                run += v;
+            }
+            if (part == 0) {
+                p.b.hist[e] = total;
+                s_cnt[e] = total;
+            }
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+        s_off[e] = s_cnt[e];
+        s_act[e] = s_cnt[e] > 0;
+    }
+    __syncthreads();
+    block_scan_array(s_off, E);
+    const int n_act = block_scan_array(s_act, E);
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+        if (s_cnt[e] == 0) continue;
+        const int a = s_act[e];
+        p.b.act_expert[a] = e;
+        p.b.act_slot[a] = e;
+        p.b.act_off[a] = s_off[e];
+        p.b.act_cnt[a] = s_cnt[e];
+    }
+    const int nr = M * k;
+#pragma unroll 4
+    for (int r = threadIdx.x; r < nr; r += kThreads) {
+        const int t = r / k;
+        const int e = __ldcg(p.b.topk_ids + r);
+        const int pos = s_off[e] + __ldcg(p.b.blk_cnt + (size_t)(t / kPfRouteTok) * E + e) + __ldcg(p.b.route_rank + r);
+        p.b.hot_expert[pos] = e;
+        p.b.hot_token[pos] = t;
+        p.b.hot_w[pos] = __ldcg(p.b.topk_w + r);
+    }
+    if (threadIdx.x == 0) {
+        p.b.counts[0] = nr;
+        p.b.counts[1] = 0;
+        p.b.counts[2] = n_act;
+        p.b.counts[3] = M;
+    }
+}
+
 constexpr int kMaxMapUpdates = 64;
 
 struct MapUpdate {
@@ -455,6 +722,27 @@ __global__ void map_update_kernel(int32_t *e2s, MapUpdate u) {
 }  // namespace
 
 cudaError_t launch_route(const RouteParams &p, cudaStream_t s, int num_sms) {
+    const size_t smem = PfSmem::bytes(p.H, p.E);
+    if (p.all_hot && p.M > kDecodeMaxTokens && p.b.blk_cnt && p.b.route_rank && smem <= 200 * 1024) {
+        static size_t smem_set = 0;  // the kernel's dynamic shared memory limit raised so far
+        if (smem > smem_set) {
+            cudaError_t e = cudaFuncSetAttribute(route_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
+            if (e != cudaSuccess) return e;
+            smem_set = smem;
+        }
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3((p.M + kPfRouteTok - 1) / kPfRouteTok);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, route_prefill_kernel, p);
+    }
     const int ntask = p.E * p.nchunk + (p.xq ? p.M * (p.H / 32) : 0);
     int grid = (ntask + kWarps - 1) / kWarps;
     grid = grid < 1 ? 1 : (grid > 8 * num_sms ? 8 * num_sms : grid);

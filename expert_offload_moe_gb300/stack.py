@@ -109,3 +109,45 @@ class DecodeStack:
         for l in self.layers:
             l.close()
         self.layers = []
+
+
+class PrefillStack:
+    """L layers of one workload with the whole expert bank staged on the device, and the M-token prefill
+    step over it (route + forward of every layer on the tensor cores)."""
+
+    def __init__(self, w: synth.Workload, M: int | None = None, n_layers: int | None = None, seed: int = 0,
+                 n_inputs: int = 2, out_f32: bool = False):
+        self.w, self.seed = w, seed
+        self.M = w.prefill_tokens if M is None else M
+        self.L = w.layers if n_layers is None else n_layers
+        self.layers, self.staging = [], []
+        H, M = w.hidden, self.M
+        for l in range(self.L):
+            li = LayerInputs(w, l, seed)
+            lay = li.make_layer(max_tokens=M, out_f32=out_f32)
+            buf = torch.empty(w.experts * w.expert_bytes, dtype=torch.uint8, device="cuda")
+            lay.attach_staging(buf)
+            lay.stage_all()
+            self.layers.append(lay)
+            self.staging.append(buf)
+            del li  # the pinned host bank is only needed until staged
+        torch.cuda.synchronize()
+        # n_inputs fresh activation batches per layer, resident in HBM: [n_inputs, L, M, H]
+        self.x_all = torch.empty((n_inputs, self.L, M, H), dtype=torch.bfloat16, device="cuda")
+        for s in range(n_inputs):
+            for l in range(self.L):
+                self.x_all[s, l].copy_(bf16_tensor(synth.activations(seed, l, s, M, H), device="cpu"))
+        dt = torch.float32 if out_f32 else torch.bfloat16
+        self.out = torch.empty((self.L, M, H), dtype=dt, device="cuda")
+
+    def step(self, i: int = 0, stream=None):
+        """One prefill step: every layer routes and runs its own batch i (eager launches)."""
+        x = self.x_all[i % self.x_all.shape[0]]
+        for l, layer in enumerate(self.layers):
+            layer.route(x[l], self.M, stream)
+            layer.forward_slots(x[l], self.out[l], self.M, stream)
+
+    def close(self):
+        for l in self.layers:
+            l.close()
+        self.layers, self.staging = [], []

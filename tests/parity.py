@@ -6,9 +6,11 @@ import ctypes
 import numpy as np
 
 NEAR_TIE = 1e-4  # k-th vs (k+1)-th logit gap below which a token's routing is not compared exactly
-# fp32 logits summed in another order differ by ~1e-6..1e-5 (far inside NEAR_TIE); the softmax carries
-# that into the weights as a relative difference of the same size
-W_RTOL, W_ATOL = 1e-5, 1e-8
+# fp32 logits summed in another order differ by a random walk of roundings: about u * 0.02 * H / sqrt(2)
+# ~ 2.4e-6 per side for H = 2880 (router rows ~N(0, 0.02^2), x ~N(0, 1), u = 2^-24), so up to ~1.5e-5
+# at 4 sigma over thousands of tokens (far inside NEAR_TIE).  The softmax turns logit differences d
+# into relative weight differences of at most 2 max|d|: 5e-5 covers that with margin.
+W_RTOL, W_ATOL = 5e-5, 1e-8
 REL_TOL = 2e-3
 RHO = 1e-2  # per-token floor: RHO * RMS of the token's oracle row
 

@@ -13,7 +13,7 @@ import torch
 import oracle
 from expert_offload_moe_gb300 import stack, synth
 
-from parity import compare_values, near_tie_tokens
+from parity import compare_routing, compare_values, near_tie_tokens, route_arrays
 
 pytestmark = pytest.mark.gpu
 
@@ -92,6 +92,45 @@ def test_prefill_gptoss_shape_sampled():
     tie = near_tie_tokens(logits, w.top_k)
     keep = [i for i, t in enumerate(tokens) if not tie[t]]
     compare_values(got[tokens][keep], ref[keep], True)
+
+
+def _route_case(w, M, seed_step, layer=0):
+    """Prefill routing of M tokens against the oracle: every expert hot (slot = expert id), hot routes in
+    (expert, token) order, no cold routes."""
+    li = stack.LayerInputs(w, layer)
+    x_bits = synth.activations(0, layer, seed_step, M, w.hidden)
+    lay = li.make_layer(max_tokens=M)
+    try:
+        res = lay.route(stack.bf16_tensor(x_bits), M)
+        g = route_arrays(res, w.experts, w.top_k)
+    finally:
+        lay.close()
+    logits = oracle.router_logits(x_bits, li.Wr, li.bias)
+    ids, wt = oracle.topk_softmax(logits, w.top_k)
+    all_hot = np.arange(w.experts, dtype=np.int32)
+    o = oracle.compact(ids, wt, all_hot)
+    o.update(ids=ids, w=wt)
+    assert g["mirror_ok"]
+    assert g["counts"][1] == 0 and g["counts"][3] == M
+    excl = compare_routing(g, o, logits, w.top_k, all_hot)
+    return g, excl
+
+
+@pytest.mark.parametrize("M", [9, 16, 17, 40, 300, 4096])
+def test_prefill_routing_tiny(M):
+    """Token tiles of 16: a partial first tile, exactly one, one plus one token, several, the maximum."""
+    _route_case(_tiny(), M, 21)
+
+
+def test_prefill_routing_gptoss_2048():
+    w = synth.WORKLOADS["gptoss20b_prefill2048_s16_lfu_drift"]
+    g, _ = _route_case(w, w.prefill_tokens, 0, layer=3)
+    assert g["counts"][0] == w.prefill_tokens * w.top_k
+
+
+def test_prefill_routing_e512_k10():
+    """512 experts (sixteen 32-expert groups of router rows), k = 10, skewed popularity."""
+    _route_case(synth.WORKLOADS["e512k10_h2048_i512_s256_m1"], 100, 5)
 
 
 def test_prefill_needs_staging():
