@@ -24,7 +24,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 128;             // warp 0: copies; warp 1 lane 0: MMAs; all 4 warps: epilogue
+constexpr int kThreads = 256;             // warp 0: copies; warp 1 lane 0: MMAs; all 8 warps: epilogue
 constexpr int kTileA = 128 * 128;         // one 128 x 128 operand tile in smem (one byte per element)
 constexpr int kTileActTx = 128 * 128;     // TMA bytes of an E4M3 activation tile
 constexpr int kTileWTx = 128 * 128 / 2;   // TMA bytes of an E2M1 weight tile (packed codes)
@@ -36,8 +36,7 @@ constexpr int kOffB0 = kTileA, kOffB1 = 2 * kTileA, kOffAtA = 3 * kTileA, kOffAt
 constexpr int kStage = 3 * kTileA + 3 * kAtom + 512;  // 50 KB
 static_assert(kStage % 1024 == 0, "stage alignment");
 constexpr int kSmemBytes = 1024 + kStages * kStage;
-// tensor memory: two 128-column accumulators (gate, up) or one 256-column accumulator (down), then
-// 12 scale columns per stage
+// tensor memory: one 256-column accumulator (gate | up, or 256 rows of down), then 12 scale columns per stage
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColSF = 256;
 static_assert(kColSF + 12 * kStages <= kTmemCols, "tensor memory layout");
@@ -52,6 +51,11 @@ __device__ __forceinline__ int mxfp8_exponent(float amax) {
     if (!(amax > 0.f)) return -127;
     return min(max(floor_log2(amax) - 8, -127), 127);
 }
+
+// SiLU with the quotient from the fast reciprocal (2 ulp): the result is rounded to E4M3 next, and an
+// error of this size is below the spread the accumulation order already gives g and u.  For g < -88 the
+// denominator is infinite and the quotient 0, the limit of SiLU.
+__device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.f + expf(-g)); }
 
 }  // namespace
 
@@ -135,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB0,
                         const __grid_constant__ CUtensorMap mapB1, GemmArgs g) {
     constexpr int S = kStages;
-    constexpr int NB = kGateUp ? 128 : 256;  // MMA N
+    constexpr int NB = 256;  // MMA N: gate/up = [128 rows of Wg; the same 128 rows of Wu], down = 256 rows of Wd
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     __shared__ __align__(8) uint64_t full[S], empty[S], done;
@@ -148,7 +152,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int expert = g.act_expert[aidx];
     const int nks = (g.K + 127) / 128;
     const bool ragged = (g.K % 128) != 0;
-    const int wrow0 = jn * NB;  // first weight row of this CTA
+    constexpr int kRowsN = kGateUp ? 128 : 256;  // weight rows per CTA (gate/up: the same rows of Wg and Wu)
+    const int wrow0 = jn * kRowsN;  // first weight row of this CTA
     // the second 128-row weight half exists (down: rows 128..255 of the 256-row tile; gate/up: always)
     const bool b1 = kGateUp || wrow0 + 128 < g.Nrows;
     const int ntW = (g.Nrows + 127) / 128;  // 128-row weight tiles (atoms)
@@ -217,18 +222,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 atom_to_tmem(sfa, sS + kOffAtA);
                 atom_to_tmem(sfb0, sS + kOffAtB0);
                 if (b1) atom_to_tmem(sfb1, sS + kOffAtB1);
-                const uint32_t aA = smem_u32(sS), aB0 = aA + kOffB0, aB1 = aA + kOffB1;
+                const uint32_t aA = smem_u32(sS), aB0 = aA + kOffB0;
                 const int nk = (ragged && i == nks - 1) ? 2 : 4;
+                // one N = 256 MMA over both weight halves (contiguous in smem), B scales in two atoms:
+                // gate/up accumulates g in columns 0..127 and u in 128..255
                 for (int kk = 0; kk < nk; ++kk) {
                     const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-                    if (kGateUp) {
-                        mma_mx(tbase, sw128_desc(aA + kk * 32), sw128_desc(aB0 + kk * 32), idesc, kk, sfa, sfb0, acc);
-                        mma_mx(tbase + 128, sw128_desc(aA + kk * 32), sw128_desc(aB1 + kk * 32), idesc, kk, sfa, sfb1,
-                               acc);
-                    } else {
-                        // one N = 256 MMA over both halves (contiguous in smem); B scales in two atoms
-                        mma_mx(tbase, sw128_desc(aA + kk * 32), sw128_desc(aB0 + kk * 32), idesc, kk, sfa, sfb0, acc);
-                    }
+                    mma_mx(tbase, sw128_desc(aA + kk * 32), sw128_desc(aB0 + kk * 32), idesc, kk, sfa, sfb0, acc);
                 }
                 mma_commit(&empty[st]);
             }
@@ -237,16 +237,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     }
 
-    // ---------------- epilogue: thread r owns route row r of the tile ----------------
-    const int r = warp * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    // ---------------- epilogue: row r = 32 (warp % 4) + lane (a warp reaches its own 32 lanes of tensor
+    // memory), column half warp / 4 ----------------
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const bool valid = r < nrows;
     const bool got = __all_sync(0xffffffffu, mbar_wait(&done, 0, g.err, kErrDone));
     tc_fence_after();
     const int pr = tile * 128 + r;  // padded route row
     if (kGateUp) {
-        // h = SiLU(g) u for 128 columns of I, one 32-column MXFP8 block at a time
-        for (int c = 0; c < 4; ++c) {
+        // h = SiLU(g) u for 64 of the tile's 128 columns of I, one 32-column MXFP8 block at a time
+        for (int c = 2 * half; c < 2 * half + 2; ++c) {
             float h[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) h[j] = 0.f;
@@ -257,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld8x2_sync(tbase + lane_off + 32 * c + 8 * q, gg, tbase + 128 + lane_off + 32 * c + 8 * q, uu);
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        h[8 * q + j] = valid ? silu(__uint_as_float(gg[j])) * __uint_as_float(uu[j]) : 0.f;
+                        h[8 * q + j] = valid ? silu_fast(__uint_as_float(gg[j])) * __uint_as_float(uu[j]) : 0.f;
                 }
             }
             float amax = 0.f;
@@ -281,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // y * w for 256 columns of H.  The tensor-memory loads are warp-aligned: every lane issues them,
         // rows past the tile's routes only skip the stores.
         const float w = valid ? g.hot_w[g.act_off[aidx] + (pr - g.poff[aidx])] : 0.f;
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 4 * half; c < 4 * half + 4; ++c) {
             const int col = wrow0 + 32 * c;
             if (col >= g.H) break;  // H % 32 == 0; the same for every lane
             float y[32];

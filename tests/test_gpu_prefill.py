@@ -69,6 +69,19 @@ def test_prefill_tiny_all_tokens(M):
     compare_values(got, ref, True, exclude=np.where(near_tie_tokens(logits, w.top_k))[0])
 
 
+def test_prefill_multi_tile_shape():
+    """H = 704, I = 320: gate/up spans three 128-row tiles of I (the last one ragged) over 5.5 steps of K
+    (the pipeline stages are reused, the last step is half empty); down spans a full 256-row tile of H
+    and a ragged one over 2.5 steps of K.  Every token and column."""
+    w = synth.Workload("prefill_h704_i320_e8k2", 1, 704, 320, 8, 2, 8, (16,), 1, bias_tau=0.25)
+    li = stack.LayerInputs(w, 0)
+    M = 300
+    x_bits = synth.activations(0, 0, 14, M, w.hidden)
+    got = run_prefill(li, x_bits, M)
+    ref, logits = prefill_reference(li, x_bits, w.top_k, w.hidden, w.inter, range(M))
+    compare_values(got, ref, True, exclude=np.where(near_tie_tokens(logits, w.top_k))[0])
+
+
 def test_prefill_tiny_bf16_out():
     w = _tiny()
     li = stack.LayerInputs(w, 0)
