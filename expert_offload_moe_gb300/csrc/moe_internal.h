@@ -37,7 +37,8 @@ struct RouteBuffers {
     int32_t *counts;      // [4] n_hot, n_cold, n_active, M
     unsigned *arrive;     // [1] grid arrival counter (reset by the last block)
     int32_t *blk_cnt;     // prefill: [ceil(max_tokens / kPfRouteTok)][E] routes per (token tile, expert)
-    int32_t *route_rank;  // prefill: [max_tokens * k] rank of a route among its tile's routes to its expert
+    int32_t *route_rank;  // prefill: [max_tokens * k] rank of a route among its tile's routes to its expert,
+                          // then (after the launch) the route's position in the hot list
 };
 
 struct RouteParams {
@@ -51,6 +52,9 @@ struct RouteParams {
     uint8_t *xq;         // tensor-core decode: x terms [16][Hpad] and their atoms, or nullptr
     uint8_t *xat;
     int Hpad;
+    // prefill tile plan (or nullptr): each active expert's routes padded to whole 128-row tiles
+    int32_t *pf_poff, *pf_e2a, *pf_tile_aidx, *pf_tile_nrows, *pf_ntiles;  // [E], [E], [cap], [cap], [1]
+    int pf_tiles_cap;
 };
 
 struct ExpertGeometry {
@@ -127,8 +131,9 @@ struct PrefillLaunch {
     int E, k, M, max_routes, tiles_cap, Hpad, Ipad;
     const uint16_t *x;
     const int32_t *counts, *act_expert, *act_off, *act_cnt, *hot_expert, *hot_token, *topk_ids;
+    const int32_t *route_pos;  // [M * k] hot-list position of each (token, j) route
     const float *hot_w;
-    int32_t *poff, *e2a, *tile_aidx, *tile_nrows, *ntiles;  // plan: [E], [E], [tiles_cap] x 2, [1]
+    const int32_t *poff, *e2a, *tile_aidx, *tile_nrows, *ntiles;  // tile plan from the route launch
     uint8_t *XP, *XA, *HP, *HA;  // MXFP8 x / h in route order (rows_cap x Hpad / Ipad) and their atoms
     float *YP;                   // weighted expert outputs in route order [rows_cap][H]
     int *err;

@@ -88,6 +88,7 @@ struct moe_layer {
     // call-order state
     const void *routed_x = nullptr;
     int32_t routed_M = 0;
+    bool routed_plan = false;  // the last route launch wrote the prefill tile plan
     int64_t route_seq = 0, policy_seq = 0;
     int fault = MOE_FAULT_NONE;
     int64_t stats[4] = {0, 0, 0, 0};
@@ -566,6 +567,15 @@ int moe_route(moe_layer *L, const void *x_dev, int32_t M, void *stream, moe_rout
         p.xat = L->xat;
         p.Hpad = L->Hpad;
     }
+    if (M > moe::kDecodeMaxTokens && L->pf) {  // the route launch also plans the prefill GEMM tiles
+        p.pf_poff = L->pf_poff;
+        p.pf_e2a = L->pf_e2a;
+        p.pf_tile_aidx = L->pf_tile_aidx;
+        p.pf_tile_nrows = L->pf_tile_nrows;
+        p.pf_ntiles = L->pf_ntiles;
+        p.pf_tiles_cap = moe::prefill_tiles_cap(M * k, E);
+    }
+    L->routed_plan = false;
     CUDA_TRY(prof_mark(L, 0, st));
     CUDA_TRY(moe::launch_route(p, st, L->num_sms));
     CUDA_TRY(prof_mark(L, 0, st));
@@ -583,6 +593,7 @@ int moe_route(moe_layer *L, const void *x_dev, int32_t M, void *stream, moe_rout
 
     L->routed_x = x_dev;
     L->routed_M = M;
+    L->routed_plan = p.pf_poff != nullptr;
     L->route_seq++;
     if (res) {
         res->M = M;
@@ -615,6 +626,7 @@ int moe_forward_slots(moe_layer *L, const void *x_dev, void *out_dev, int32_t M,
     if (!L || !x_dev || !out_dev) return fail(MOE_EINVAL, "layer, x_dev and out_dev are required");
     if (L->routed_M == 0 || L->routed_x != x_dev || L->routed_M != M)
         return fail(MOE_ESTATE, "moe_forward_slots needs the x_dev and M of the last moe_route");
+    if (reinterpret_cast<uintptr_t>(out_dev) % 16) return fail(MOE_EINVAL, "out_dev must be 16-byte aligned");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     moe::DecodeParams p{};
     p.geo = L->geo;
@@ -677,6 +689,8 @@ int moe_forward_slots(moe_layer *L, const void *x_dev, void *out_dev, int32_t M,
                         moe::kDecodeMaxTokens);
         if (!L->pf)
             return fail(MOE_ESTATE, "prefill needs hidden and inter of at least 128 (tensor-core tiles)");
+        if (!L->routed_plan)
+            return fail(MOE_ESTATE, "prefill needs a moe_route call made after the staging buffer was attached");
         moe::PrefillLaunch P{};
         P.bank = L->staging;
         P.atoms = L->stage_atoms;
@@ -696,6 +710,7 @@ int moe_forward_slots(moe_layer *L, const void *x_dev, void *out_dev, int32_t M,
         P.hot_expert = L->rb.hot_expert;
         P.hot_token = L->rb.hot_token;
         P.topk_ids = L->rb.topk_ids;
+        P.route_pos = L->rb.route_rank;
         P.hot_w = L->rb.hot_w;
         P.poff = L->pf_poff;
         P.e2a = L->pf_e2a;

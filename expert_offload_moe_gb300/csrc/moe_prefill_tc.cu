@@ -3,9 +3,9 @@
 // expert layer is staged and the GEMM runs on it; tinyserve README, batched prefill: routes are grouped by
 // expert so that each expert's weights are read once per batch).
 //
-// The route launch has already ordered the hot routes by (expert, token).  Then, on one stream:
-//   prefill_plan_kernel      pads each active expert's routes to whole 128-row tiles (a tile never mixes
-//                            experts) and records the tile list and the expert -> active-index map
+// The route launch has already ordered the hot routes by (expert, token), padded each active expert's
+// routes to whole 128-row tiles (a tile never mixes experts) and recorded the tile list, the expert ->
+// active-index map and each route's hot-list position.  Then, on one stream:
 //   prefill_quant_kernel     x of every route -> MXFP8 (E4M3 codes, one E8M0 scale per 32 columns, the
 //                            OCP MX v1.0 conversion rule), gathered into route order with scale atoms
 //   prefill_gemm_kernel<1>   per (route tile, 128 rows of I): Dg = x Wg^T, Du = x Wu^T on tcgen05
@@ -59,56 +59,50 @@ __device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.f +
 
 }  // namespace
 
-// ------------------------------------------------------------------ plan
-
-__global__ void __launch_bounds__(256) prefill_plan_kernel(const int32_t *counts, const int32_t *act_expert,
-                                                           const int32_t *act_cnt, int E, int32_t *poff,
-                                                           int32_t *e2a, int32_t *tile_aidx, int32_t *tile_nrows,
-                                                           int32_t *ntiles, int tiles_cap) {
-    for (int e = threadIdx.x; e < E; e += blockDim.x) e2a[e] = -1;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const int n_act = counts[2];
-        int pr = 0, nt = 0;
-        for (int a = 0; a < n_act; ++a) {
-            const int cnt = act_cnt[a];
-            poff[a] = pr;
-            e2a[act_expert[a]] = a;
-            for (int r = 0; r < cnt; r += 128) {
-                if (nt < tiles_cap) {
-                    tile_aidx[nt] = a;
-                    tile_nrows[nt] = min(128, cnt - r);
-                }
-                ++nt;
-            }
-            pr += (cnt + 127) / 128 * 128;
-        }
-        *ntiles = min(nt, tiles_cap);
-    }
-}
-
 // ------------------------------------------------------------------ x -> MXFP8, route order
 
-// One warp per (route, 32-column block): XP[pr][Hpad] codes, XA[tile][kstep][512] scales, pr = padded row.
+// One warp per route (the warps striding over the hot list): each lane converts 8 consecutive columns
+// of the route's token, four lanes make one 32-column MXFP8 block.  XP[pr][Hpad] codes,
+// XA[tile][kstep][512] scales, pr = the route's padded row.
 __global__ void __launch_bounds__(256) prefill_quant_kernel(const uint16_t *x, int H, const int32_t *counts,
                                                             const int32_t *hot_expert, const int32_t *hot_token,
                                                             const int32_t *act_off, const int32_t *e2a,
                                                             const int32_t *poff, uint8_t *XP, int Hpad,
                                                             uint8_t *XA, int nks) {
     const int lane = threadIdx.x & 31;
-    const int nb = H / 32;
-    const int task = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (task >= counts[0] * nb) return;
-    const int p = task / nb, b = task - p * nb;
-    const int a = e2a[hot_expert[p]];
-    const int pr = poff[a] + (p - act_off[a]);
-    const float v = __uint_as_float((uint32_t)x[(size_t)hot_token[p] * H + b * 32 + lane] << 16);
-    const int X = mxfp8_exponent(warp_max(fabsf(v)));
-    const float sv = v * e8m0_value(e8m0_byte(-X));  // exact: a power of two
-    const float other = __shfl_xor_sync(0xffffffffu, sv, 1);
-    const uint16_t pk = (lane & 1) ? f32x2_to_e4m3x2(other, sv) : f32x2_to_e4m3x2(sv, other);
-    XP[(size_t)pr * Hpad + b * 32 + lane] = (lane & 1) ? (uint8_t)(pk >> 8) : (uint8_t)(pk & 0xff);
-    if (lane == 0) XA[((size_t)(pr >> 7) * nks + (b >> 2)) * kAtom + atom_byte(pr & 127, b & 3)] = (uint8_t)(X + 127);
+    const int n_hot = counts[0];
+    const int nit = (H + 255) / 256;
+    for (int p = blockIdx.x * 8 + (threadIdx.x >> 5); p < n_hot; p += gridDim.x * 8) {
+        const int a = e2a[hot_expert[p]];
+        const int pr = poff[a] + (p - act_off[a]);
+        const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)hot_token[p] * H);
+        uint8_t *xp = XP + (size_t)pr * Hpad;
+        uint8_t *xa = XA + (size_t)(pr >> 7) * nks * kAtom;
+        for (int it = 0; it < nit; ++it) {
+            const int col = it * 256 + lane * 8;
+            const bool valid = col < H;  // H % 32 == 0: a 4-lane block is all valid or all past H
+            const uint4 v = valid ? __ldg(xr + col / 8) : make_uint4(0u, 0u, 0u, 0u);
+            float f[8];
+            f[0] = __uint_as_float(v.x << 16); f[1] = __uint_as_float(v.x & 0xffff0000u);
+            f[2] = __uint_as_float(v.y << 16); f[3] = __uint_as_float(v.y & 0xffff0000u);
+            f[4] = __uint_as_float(v.z << 16); f[5] = __uint_as_float(v.z & 0xffff0000u);
+            f[6] = __uint_as_float(v.w << 16); f[7] = __uint_as_float(v.w & 0xffff0000u);
+            float m = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(f[j]));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            const int X = mxfp8_exponent(m);
+            const float inv = e8m0_value(e8m0_byte(-X));  // exact: a power of two
+            const uint32_t lo = f32x2_to_e4m3x2(f[0] * inv, f[1] * inv) | (f32x2_to_e4m3x2(f[2] * inv, f[3] * inv) << 16);
+            const uint32_t hi = f32x2_to_e4m3x2(f[4] * inv, f[5] * inv) | (f32x2_to_e4m3x2(f[6] * inv, f[7] * inv) << 16);
+            if (valid) {
+                *reinterpret_cast<uint2 *>(xp + col) = make_uint2(lo, hi);
+                const int b = col / 32;
+                if ((lane & 3) == 0) xa[(size_t)(b >> 2) * kAtom + atom_byte(pr & 127, b & 3)] = (uint8_t)(X + 127);
+            }
+        }
+    }
 }
 
 // ------------------------------------------------------------------ grouped GEMM
@@ -316,44 +310,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ combine
 
-// One block per token: its routes in ascending expert order, each found by binary search among the
-// expert's tokens (ascending), summed into out.
+// One block per token: its routes in ascending expert order (each route's padded row from its hot-list
+// position), summed into out four columns per thread.
 __global__ void __launch_bounds__(256) prefill_combine_kernel(const int32_t *topk_ids, int k, const int32_t *e2a,
-                                                              const int32_t *act_off, const int32_t *act_cnt,
-                                                              const int32_t *hot_token, const int32_t *poff,
-                                                              const float *YP, int H, void *out, int out_f32) {
+                                                              const int32_t *act_off, const int32_t *route_pos,
+                                                              const int32_t *poff, const float *YP, int H,
+                                                              void *out, int out_f32) {
     __shared__ int s_pr[kMaxTopK];
     const int t = blockIdx.x;
-    if (threadIdx.x == 0) {
-        int ids[kMaxTopK];
-        for (int j = 0; j < k; ++j) {
-            const int e = topk_ids[(size_t)t * k + j];
-            int q = j;
-            while (q > 0 && ids[q - 1] > e) {
-                ids[q] = ids[q - 1];
-                --q;
-            }
-            ids[q] = e;
-        }
-        for (int j = 0; j < k; ++j) {
-            const int a = e2a[ids[j]];
-            int lo = act_off[a], hi = act_off[a] + act_cnt[a];  // hot_token ascending in [lo, hi)
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (hot_token[mid] < t) lo = mid + 1;
-                else hi = mid;
-            }
-            s_pr[j] = poff[a] + (lo - act_off[a]);
-        }
+    if (threadIdx.x < k) {
+        const int j = threadIdx.x, e = topk_ids[(size_t)t * k + j];
+        int rank = 0;  // the k experts of a token are distinct
+        for (int i = 0; i < k; ++i) rank += topk_ids[(size_t)t * k + i] < e;
+        const int a = e2a[e];
+        s_pr[rank] = poff[a] + (route_pos[(size_t)t * k + j] - act_off[a]);
     }
     __syncthreads();
-    for (int h = threadIdx.x; h < H; h += blockDim.x) {
-        float acc = 0.f;
-        for (int j = 0; j < k; ++j) acc += YP[(size_t)s_pr[j] * H + h];
-        if (out_f32)
-            reinterpret_cast<float *>(out)[(size_t)t * H + h] = acc;
-        else
-            reinterpret_cast<__nv_bfloat16 *>(out)[(size_t)t * H + h] = __float2bfloat16_rn(acc);
+    for (int h4 = threadIdx.x; h4 < H / 4; h4 += blockDim.x) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < k; ++j) {
+            const float4 y = __ldg(reinterpret_cast<const float4 *>(YP + (size_t)s_pr[j] * H) + h4);
+            acc.x += y.x;
+            acc.y += y.y;
+            acc.z += y.z;
+            acc.w += y.w;
+        }
+        if (out_f32) {
+            reinterpret_cast<float4 *>(out)[(size_t)t * (H / 4) + h4] = acc;
+        } else {
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+            uint2 v;
+            v.x = (uint32_t)__bfloat16_as_ushort(lo.x) | ((uint32_t)__bfloat16_as_ushort(lo.y) << 16);
+            v.y = (uint32_t)__bfloat16_as_ushort(hi.x) | ((uint32_t)__bfloat16_as_ushort(hi.y) << 16);
+            reinterpret_cast<uint2 *>(out)[(size_t)t * (H / 4) + h4] = v;
+        }
     }
 }
 
@@ -364,11 +354,7 @@ int prefill_tiles_cap(int max_routes, int E) { return (max_routes + 127) / 128 +
 cudaError_t launch_prefill(const PrefillLaunch &P, cudaStream_t s) {
     const ExpertGeometry &geo = P.geo;
     const TcAtomLayout l = tc_atom_layout(geo.H, geo.I);
-    prefill_plan_kernel<<<1, 256, 0, s>>>(P.counts, P.act_expert, P.act_cnt, P.E, P.poff, P.e2a, P.tile_aidx,
-                                          P.tile_nrows, P.ntiles, P.tiles_cap);
-    const int nb = geo.H / 32;
-    const long tasks = (long)P.max_routes * nb;
-    prefill_quant_kernel<<<(unsigned)((tasks + 7) / 8), 256, 0, s>>>(P.x, geo.H, P.counts, P.hot_expert, P.hot_token,
+    prefill_quant_kernel<<<(unsigned)((P.max_routes + 7) / 8), 256, 0, s>>>(P.x, geo.H, P.counts, P.hot_expert, P.hot_token,
                                                                       P.act_off, P.e2a, P.poff, P.XP, P.Hpad, P.XA,
                                                                       l.nks);
     static bool cfg = false;
@@ -420,8 +406,8 @@ cudaError_t launch_prefill(const PrefillLaunch &P, cudaStream_t s) {
     if (P.ev[2]) cudaEventRecord(P.ev[2], s);
     prefill_gemm_kernel<0><<<P.tiles_cap * g.nN, kThreads, kSmemBytes, s>>>(*P.mapHP, *P.mapD, *P.mapD, g);
     if (P.ev[3]) cudaEventRecord(P.ev[3], s);
-    prefill_combine_kernel<<<P.M, 256, 0, s>>>(P.topk_ids, P.k, P.e2a, P.act_off, P.act_cnt, P.hot_token, P.poff,
-                                               P.YP, geo.H, P.out, P.out_f32);
+    prefill_combine_kernel<<<P.M, 256, 0, s>>>(P.topk_ids, P.k, P.e2a, P.act_off, P.route_pos, P.poff, P.YP, geo.H,
+                                               P.out, P.out_f32);
     return cudaGetLastError();
 }
 

@@ -697,6 +697,31 @@ __global__ void __launch_bounds__(kThreads, 1) route_prefill_kernel(RouteParams 
         p.b.hot_expert[pos] = e;
         p.b.hot_token[pos] = t;
         p.b.hot_w[pos] = __ldcg(p.b.topk_w + r);
+        p.b.route_rank[r] = pos;  // only this thread reads or writes entry r
+    }
+
+    // tile plan for the grouped GEMMs: each active expert's routes padded to whole 128-row tiles, in
+    // expert order (a tile never mixes experts)
+    if (p.pf_poff) {
+        __shared__ int s_tiles[kMaxExperts];
+        for (int e = threadIdx.x; e < E; e += kThreads) s_tiles[e] = (s_cnt[e] + 127) / 128;
+        __syncthreads();
+        const int total = block_scan_array(s_tiles, E);
+        for (int e = threadIdx.x; e < E; e += kThreads) {
+            if (s_cnt[e] == 0) {
+                p.pf_e2a[e] = -1;
+                continue;
+            }
+            const int a = s_act[e], t0e = s_tiles[e], cnt = s_cnt[e];
+            p.pf_e2a[e] = a;
+            p.pf_poff[a] = 128 * t0e;
+            for (int i = 0; 128 * i < cnt; ++i) {
+                if (t0e + i >= p.pf_tiles_cap) break;
+                p.pf_tile_aidx[t0e + i] = a;
+                p.pf_tile_nrows[t0e + i] = min(128, cnt - 128 * i);
+            }
+        }
+        if (threadIdx.x == 0) *p.pf_ntiles = min(total, p.pf_tiles_cap);
     }
     if (threadIdx.x == 0) {
         p.b.counts[0] = nr;
@@ -723,7 +748,9 @@ __global__ void map_update_kernel(int32_t *e2s, MapUpdate u) {
 
 cudaError_t launch_route(const RouteParams &p, cudaStream_t s, int num_sms) {
     const size_t smem = PfSmem::bytes(p.H, p.E);
-    if (p.all_hot && p.M > kDecodeMaxTokens && p.b.blk_cnt && p.b.route_rank && smem <= 200 * 1024) {
+    const bool tiled = p.all_hot && p.M > kDecodeMaxTokens && p.b.blk_cnt && p.b.route_rank && smem <= 200 * 1024;
+    if (p.pf_poff && !tiled) return cudaErrorNotSupported;  // only the tiled launch plans the prefill GEMMs
+    if (tiled) {
         static size_t smem_set = 0;  // the kernel's dynamic shared memory limit raised so far
         if (smem > smem_set) {
             cudaError_t e = cudaFuncSetAttribute(route_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

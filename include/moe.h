@@ -156,9 +156,10 @@ int moe_route(moe_layer *layer, const void *x_dev, int32_t M, void *stream, moe_
  * where y is the expert FFN read from the expert's slot (fp32 accumulation);
  * tokens without hot routes get zeros.  x_dev and M must be those of the last
  * moe_route (MOE_ESTATE otherwise).  M <= 8: decode kernels over the slot
- * bank.  M > 8: prefill on the staging bank (MOE_ESTATE if none is attached
- * or it was not staged with moe_layer_stage_all).
- *  out_dev  [M, H] out_dtype, device, caller-owned
+ * bank.  M > 8: prefill on the staging bank (MOE_ESTATE if none is attached,
+ * it was not staged with moe_layer_stage_all, or the last moe_route was made
+ * before it was attached: that route launch also plans the prefill tiles).
+ *  out_dev  [M, H] out_dtype, device, caller-owned, 16-byte aligned
  * Asynchronous, capturable.  Errors: MOE_EINVAL, MOE_ESTATE, MOE_ECUDA. */
 int moe_forward_slots(moe_layer *layer, const void *x_dev, void *out_dev, int32_t M, void *stream);
 

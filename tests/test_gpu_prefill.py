@@ -159,3 +159,30 @@ def test_prefill_needs_staging():
             lay.forward_slots(x, out, M)
     finally:
         lay.close()
+
+
+def test_prefill_needs_a_route_after_staging():
+    """The route launch plans the prefill tiles only when the staging buffer is attached: routing first and
+    attaching afterwards is refused, and routing again makes it run."""
+    w = _tiny()
+    li = stack.LayerInputs(w, 0)
+    lay = li.make_layer(max_tokens=32, out_f32=True)
+    try:
+        M = 20
+        x_bits = synth.activations(0, 0, 15, M, w.hidden)
+        x = stack.bf16_tensor(x_bits)
+        out = torch.empty((M, w.hidden), dtype=torch.float32, device="cuda")
+        lay.route(x, M)
+        staging = torch.empty(w.experts * w.expert_bytes, dtype=torch.uint8, device="cuda")
+        lay.attach_staging(staging)
+        lay.stage_all()
+        with pytest.raises(Exception):
+            lay.forward_slots(x, out, M)
+        lay.route(x, M)
+        lay.forward_slots(x, out, M)
+        torch.cuda.synchronize()
+        lay.check_error()
+        ref, logits = prefill_reference(li, x_bits, w.top_k, w.hidden, w.inter, range(M))
+        compare_values(out.cpu().numpy(), ref, True, exclude=np.where(near_tie_tokens(logits, w.top_k))[0])
+    finally:
+        lay.close()
