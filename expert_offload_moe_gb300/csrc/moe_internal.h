@@ -15,7 +15,7 @@ constexpr int kMaxExperts = 512;
 constexpr int kMaxTokens = 4096;
 constexpr int kDecodeMaxTokens = 8;            // M <= 8 takes the decode kernels
 constexpr int kRouteChunk = 256;               // router columns per warp task
-constexpr int kPfRouteTok = 16;                // prefill routing: tokens per thread block
+constexpr int kPfRouteTok = 8;                 // prefill routing: tokens per thread block
 constexpr int kDecodeSmemLimit = 200 * 1024;   // decode activations staged in shared memory
 
 // Device scratch written by the route kernel.
@@ -44,6 +44,8 @@ struct RouteBuffers {
 struct RouteParams {
     const uint16_t *x;   // bf16 bits [M, H]
     const float *Wr;     // [E, H]
+    const float *WrT;    // prefill: [H, E32] (E rounded up to 32, zero rows), or nullptr
+    int E32;
     const float *bias;   // [E] or nullptr
     const int32_t *e2s;  // [E]; ignored when all_hot
     int M, H, E, k, nchunk;
@@ -128,7 +130,7 @@ cudaError_t launch_down_tc(const TcLaunch &L, cudaStream_t s);
 struct PrefillLaunch {
     const uint8_t *bank, *atoms;  // staged experts (slot = expert id) and their weight atoms
     ExpertGeometry geo;
-    int E, k, M, max_routes, tiles_cap, Hpad, Ipad;
+    int E, k, M, max_routes, tiles_cap, Hpad, Ipad, num_sms;
     const uint16_t *x;
     const int32_t *counts, *act_expert, *act_off, *act_cnt, *hot_expert, *hot_token, *topk_ids;
     const int32_t *route_pos;  // [M * k] hot-list position of each (token, j) route
@@ -148,6 +150,7 @@ void launch_build_weight_atoms_bank(const uint8_t *bank, int E, const ExpertGeom
                                     cudaStream_t s);
 
 cudaError_t launch_route(const RouteParams &p, cudaStream_t s, int num_sms);
+cudaError_t launch_router_transpose(const float *Wr, float *WrT, int E, int H, int E32, cudaStream_t s);
 void launch_gateup(const DecodeParams &p, int M, cudaStream_t s, int num_sms);
 void launch_down(const DecodeParams &p, int M, cudaStream_t s, int num_sms);
 void launch_map_update(int32_t *e2s, int n, const int32_t *experts, const int32_t *slots, cudaStream_t s);

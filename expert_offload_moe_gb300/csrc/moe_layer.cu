@@ -56,6 +56,7 @@ struct moe_layer {
 
     uint8_t *slots = nullptr;  // [S][expert_bytes]
     float *Wr = nullptr;       // [E][H]
+    float *WrT = nullptr;      // [H][E32], the router transposed for prefill routing
     float *bias = nullptr;     // [E]
     int32_t *e2s_dev = nullptr;
     const uint8_t *host_bank = nullptr;
@@ -130,6 +131,7 @@ void release(moe_layer *L) {
     if (L->d2h) cudaStreamSynchronize(L->d2h);
     cudaFree(L->slots);
     cudaFree(L->Wr);
+    cudaFree(L->WrT);
     cudaFree(L->bias);
     cudaFree(L->e2s_dev);
     cudaFree(L->dev_block);
@@ -453,6 +455,8 @@ int moe_layer_create(const moe_layer_desc *desc, const float *router_w_dev, cons
     const size_t eb = L->geo.expert_bytes;
     CREATE_TRY(cudaMalloc(&L->slots, (size_t)d.num_slots * eb));
     CREATE_TRY(cudaMalloc(&L->Wr, (size_t)E * H * sizeof(float)));
+    const int E32 = (E + 31) / 32 * 32;
+    CREATE_TRY(cudaMalloc(&L->WrT, (size_t)E32 * H * sizeof(float)));
     CREATE_TRY(cudaMalloc(&L->bias, (size_t)E * sizeof(float)));
     CREATE_TRY(cudaMalloc(&L->e2s_dev, (size_t)E * sizeof(int32_t)));
     CREATE_TRY(cudaMalloc(&L->h, (size_t)L->max_hot * I * sizeof(float)));
@@ -519,6 +523,7 @@ int moe_layer_create(const moe_layer_desc *desc, const float *router_w_dev, cons
     for (auto &e : L->ev_copy) CREATE_TRY(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
 
     CREATE_TRY(cudaMemcpyAsync(L->Wr, router_w_dev, (size_t)E * H * sizeof(float), cudaMemcpyDeviceToDevice, st));
+    CREATE_TRY(moe::launch_router_transpose(L->Wr, L->WrT, E, H, (E + 31) / 32 * 32, st));
     if (router_bias_dev)
         CREATE_TRY(cudaMemcpyAsync(L->bias, router_bias_dev, (size_t)E * sizeof(float), cudaMemcpyDeviceToDevice, st));
     else
@@ -553,6 +558,8 @@ int moe_route(moe_layer *L, const void *x_dev, int32_t M, void *stream, moe_rout
     moe::RouteParams p{};
     p.x = static_cast<const uint16_t *>(x_dev);
     p.Wr = L->Wr;
+    p.WrT = L->WrT;
+    p.E32 = (L->d.num_experts + 31) / 32 * 32;
     p.bias = L->bias;
     p.e2s = L->e2s_dev;
     p.M = M;
@@ -700,6 +707,7 @@ int moe_forward_slots(moe_layer *L, const void *x_dev, void *out_dev, int32_t M,
         P.M = M;
         P.max_routes = M * L->d.top_k;
         P.tiles_cap = moe::prefill_tiles_cap(P.max_routes, P.E);
+        P.num_sms = L->num_sms;
         P.Hpad = L->Hpad;
         P.Ipad = L->Ipad;
         P.x = p.x;

@@ -24,7 +24,8 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 256;             // warp 0: copies; warp 1 lane 0: MMAs; all 8 warps: epilogue
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;  // warp 0: copies; warp 1 lane 0: MMAs; warps 2..9: epilogue
 constexpr int kTileA = 128 * 128;         // one 128 x 128 operand tile in smem (one byte per element)
 constexpr int kTileActTx = 128 * 128;     // TMA bytes of an E4M3 activation tile
 constexpr int kTileWTx = 128 * 128 / 2;   // TMA bytes of an E2M1 weight tile (packed codes)
@@ -36,7 +37,9 @@ constexpr int kOffB0 = kTileA, kOffB1 = 2 * kTileA, kOffAtA = 3 * kTileA, kOffAt
 constexpr int kStage = 3 * kTileA + 3 * kAtom + 512;  // 50 KB
 static_assert(kStage % 1024 == 0, "stage alignment");
 constexpr int kSmemBytes = 1024 + kStages * kStage;
-// tensor memory: one 256-column accumulator (gate | up, or 256 rows of down), then 12 scale columns per stage
+// tensor memory: one 256-column accumulator (gate | up, or 256 rows of down), then 12 scale columns per stage.
+// The kernels are persistent (one CTA per SM walks the work items); the epilogue copies the accumulator to
+// registers and releases it, so the next item's MMAs overlap the previous item's epilogue.
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColSF = 256;
 static_assert(kColSF + 12 * kStages <= kTmemCols, "tensor memory layout");
@@ -134,25 +137,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap mapB1, GemmArgs g) {
     constexpr int S = kStages;
     constexpr int NB = 256;  // MMA N: gate/up = [128 rows of Wg; the same 128 rows of Wu], down = 256 rows of Wd
+    constexpr int kRowsN = kGateUp ? 128 : 256;  // weight rows per work item
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
-    __shared__ __align__(8) uint64_t full[S], empty[S], done;
+    __shared__ __align__(8) uint64_t full[S], empty[S], acc_full, acc_empty;
     __shared__ uint32_t tslot;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tile = blockIdx.x / g.nN, jn = blockIdx.x - tile * g.nN;
-    if (tile >= *g.ntiles) return;
-    const int aidx = g.tile_aidx[tile], nrows = g.tile_nrows[tile];
-    const int expert = g.act_expert[aidx];
+    const int nwork = *g.ntiles * g.nN;
     const int nks = (g.K + 127) / 128;
     const bool ragged = (g.K % 128) != 0;
-    constexpr int kRowsN = kGateUp ? 128 : 256;  // weight rows per CTA (gate/up: the same rows of Wg and Wu)
-    const int wrow0 = jn * kRowsN;  // first weight row of this CTA
-    // the second 128-row weight half exists (down: rows 128..255 of the 256-row tile; gate/up: always)
-    const bool b1 = kGateUp || wrow0 + 128 < g.Nrows;
     const int ntW = (g.Nrows + 127) / 128;  // 128-row weight tiles (atoms)
-    const uint8_t *ex = g.bank + (size_t)expert * g.expert_bytes;
-    const uint8_t *exat = g.atoms + (size_t)expert * g.atom_slot_bytes;
 
     if (warp == 1) tmem_alloc(&tslot, kTmemCols);
     if (threadIdx.x == 0) {
@@ -160,7 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(&done, 1);
+        mbar_init(&acc_full, 1);
+        mbar_init(&acc_empty, kEpiWarps);
         fence_barrier_init();
         tma_prefetch_desc(&mapA);
         tma_prefetch_desc(&mapB0);
@@ -172,130 +168,159 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tbase = tslot;
 
     if (warp == 0) {
+        // ---------------- operand copies: one ring of stages across all work items ----------------
         bool ok = true;
-        for (int i = 0; i < nks && ok; ++i) {
-            const int st = i % S;
-            if (lane == 0) ok = mbar_wait(&empty[st], ((i / S) & 1) ^ 1, g.err, kErrEmpty);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            uint8_t *sS = smem + st * kStage;
-            const bool tail = ragged && i == nks - 1;
-            // weight tile halves: gate/up -> (Wg rows, Wu rows) of one 128-row tile; down -> two 128-row tiles
-            const int r0 = kGateUp ? wrow0 : wrow0, r1 = kGateUp ? wrow0 : wrow0 + 128;
-            const size_t atom0 = g.atom_off_b0 + ((size_t)(r0 >> 7) * nks + i) * kAtom;
-            const size_t atom1 = g.atom_off_b1 + ((size_t)(r1 >> 7) * nks + i) * kAtom;
-            if (tail) {
-                load_tail_tile(sS + kOffB0, ex + g.off_b0_codes, g.Nrows, r0, g.K, i);
-                if (b1) load_tail_tile(sS + kOffB1, ex + g.off_b1_codes, g.Nrows, r1, g.K, i);
-            }
-            if (lane == 0) {
-                const uint32_t wtx = tail ? 0u : (uint32_t)kTileWTx;
-                mbar_expect_tx(&full[st], kTileActTx + wtx * (b1 ? 2u : 1u) + kAtom * (b1 ? 3u : 2u));
-                tma_load_3d(&mapA, &full[st], sS, i * 128, tile * 128, 0);
-                if (!tail) {
-                    tma_load_3d(&mapB0, &full[st], sS + kOffB0, i * 128, r0, expert);
-                    if (b1) tma_load_3d(&mapB1, &full[st], sS + kOffB1, i * 128, r1, expert);
+        uint32_t it = 0;
+        for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
+            const int tile = w / g.nN, jn = w - tile * g.nN;
+            const int expert = g.act_expert[g.tile_aidx[tile]];
+            const int wrow0 = jn * kRowsN;
+            const bool b1 = kGateUp || wrow0 + 128 < g.Nrows;
+            const int r0 = wrow0, r1 = kGateUp ? wrow0 : wrow0 + 128;
+            const uint8_t *ex = g.bank + (size_t)expert * g.expert_bytes;
+            const uint8_t *exat = g.atoms + (size_t)expert * g.atom_slot_bytes;
+            for (int i = 0; i < nks; ++i, ++it) {
+                const int st = it % S;
+                if (lane == 0) ok = mbar_wait(&empty[st], ((it / S) & 1) ^ 1, g.err, kErrEmpty);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                uint8_t *sS = smem + st * kStage;
+                const bool tail = ragged && i == nks - 1;
+                const size_t atom0 = g.atom_off_b0 + ((size_t)(r0 >> 7) * nks + i) * kAtom;
+                const size_t atom1 = g.atom_off_b1 + ((size_t)(r1 >> 7) * nks + i) * kAtom;
+                if (tail) {
+                    load_tail_tile(sS + kOffB0, ex + g.off_b0_codes, g.Nrows, r0, g.K, i);
+                    if (b1) load_tail_tile(sS + kOffB1, ex + g.off_b1_codes, g.Nrows, r1, g.K, i);
                 }
-                bulk_copy(sS + kOffAtA, g.Aat + ((size_t)tile * nks + i) * kAtom, kAtom, &full[st]);
-                bulk_copy(sS + kOffAtB0, exat + atom0, kAtom, &full[st]);
-                if (b1 && (kGateUp || (r1 >> 7) < ntW)) bulk_copy(sS + kOffAtB1, exat + atom1, kAtom, &full[st]);
+                if (lane == 0) {
+                    const uint32_t wtx = tail ? 0u : (uint32_t)kTileWTx;
+                    mbar_expect_tx(&full[st], kTileActTx + wtx * (b1 ? 2u : 1u) + kAtom * (b1 ? 3u : 2u));
+                    tma_load_3d(&mapA, &full[st], sS, i * 128, tile * 128, 0);
+                    if (!tail) {
+                        tma_load_3d(&mapB0, &full[st], sS + kOffB0, i * 128, r0, expert);
+                        if (b1) tma_load_3d(&mapB1, &full[st], sS + kOffB1, i * 128, r1, expert);
+                    }
+                    bulk_copy(sS + kOffAtA, g.Aat + ((size_t)tile * nks + i) * kAtom, kAtom, &full[st]);
+                    bulk_copy(sS + kOffAtB0, exat + atom0, kAtom, &full[st]);
+                    if (b1 && (kGateUp || (r1 >> 7) < ntW)) bulk_copy(sS + kOffAtB1, exat + atom1, kAtom, &full[st]);
+                }
+                __syncwarp();
             }
-            __syncwarp();
         }
     } else if (warp == 1) {
+        // ---------------- MMAs: one thread; the accumulator is reused once the epilogue has drained it ----
         if (lane == 0) {
             const uint32_t idesc = mx_idesc(kFmtE4M3, kFmtE2M1, NB);
             bool ok = true;
-            for (int i = 0; i < nks && ok; ++i) {
-                const int st = i % S;
-                ok = mbar_wait(&full[st], (i / S) & 1, g.err, kErrFull);
-                if (!ok) break;
-                tc_fence_after();
-                uint8_t *sS = smem + st * kStage;
-                const uint32_t sfa = tbase + kColSF + 12 * st, sfb0 = sfa + 4, sfb1 = sfa + 8;
-                atom_to_tmem(sfa, sS + kOffAtA);
-                atom_to_tmem(sfb0, sS + kOffAtB0);
-                if (b1) atom_to_tmem(sfb1, sS + kOffAtB1);
-                const uint32_t aA = smem_u32(sS), aB0 = aA + kOffB0;
-                const int nk = (ragged && i == nks - 1) ? 2 : 4;
-                // one N = 256 MMA over both weight halves (contiguous in smem), B scales in two atoms:
-                // gate/up accumulates g in columns 0..127 and u in 128..255
-                for (int kk = 0; kk < nk; ++kk) {
-                    const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-                    mma_mx(tbase, sw128_desc(aA + kk * 32), sw128_desc(aB0 + kk * 32), idesc, kk, sfa, sfb0, acc);
+            uint32_t it = 0;
+            int n = 0;
+            for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x, ++n) {
+                if (n > 0) {
+                    ok = mbar_wait(&acc_empty, (n - 1) & 1, g.err, kErrDone);
+                    if (!ok) break;
+                    tc_fence_after();
                 }
-                mma_commit(&empty[st]);
+                const int jn = w % g.nN;
+                const bool b1 = kGateUp || jn * kRowsN + 128 < g.Nrows;  // the second weight half exists
+                for (int i = 0; i < nks; ++i, ++it) {
+                    const int st = it % S;
+                    ok = mbar_wait(&full[st], (it / S) & 1, g.err, kErrFull);
+                    if (!ok) break;
+                    tc_fence_after();
+                    uint8_t *sS = smem + st * kStage;
+                    const uint32_t sfa = tbase + kColSF + 12 * st, sfb0 = sfa + 4, sfb1 = sfa + 8;
+                    atom_to_tmem(sfa, sS + kOffAtA);
+                    atom_to_tmem(sfb0, sS + kOffAtB0);
+                    if (b1) atom_to_tmem(sfb1, sS + kOffAtB1);
+                    const uint32_t aA = smem_u32(sS), aB0 = aA + kOffB0;
+                    const int nk = (ragged && i == nks - 1) ? 2 : 4;
+                    // one N = 256 MMA over both weight halves (contiguous in smem), B scales in two atoms:
+                    // gate/up accumulates g in columns 0..127 and u in 128..255
+                    for (int kk = 0; kk < nk; ++kk) {
+                        const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                        mma_mx(tbase, sw128_desc(aA + kk * 32), sw128_desc(aB0 + kk * 32), idesc, kk, sfa, sfb0, acc);
+                    }
+                    mma_commit(&empty[st]);
+                }
+                if (ok) mma_commit(&acc_full);
             }
-            mma_commit(&done);
         }
         __syncwarp();
-    }
-
-    // ---------------- epilogue: row r = 32 (warp % 4) + lane (a warp reaches its own 32 lanes of tensor
-    // memory), column half warp / 4 ----------------
-    const int quarter = warp & 3, half = warp >> 2;
-    const int r = quarter * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const bool valid = r < nrows;
-    const bool got = __all_sync(0xffffffffu, mbar_wait(&done, 0, g.err, kErrDone));
-    tc_fence_after();
-    const int pr = tile * 128 + r;  // padded route row
-    if (kGateUp) {
-        // h = SiLU(g) u for 64 of the tile's 128 columns of I, one 32-column MXFP8 block at a time
-        for (int c = 2 * half; c < 2 * half + 2; ++c) {
-            float h[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) h[j] = 0.f;
-            if (got) {
-                uint32_t gg[8], uu[8];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    tmem_ld8x2_sync(tbase + lane_off + 32 * c + 8 * q, gg, tbase + 128 + lane_off + 32 * c + 8 * q, uu);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        h[8 * q + j] = valid ? silu_fast(__uint_as_float(gg[j])) * __uint_as_float(uu[j]) : 0.f;
-                }
-            }
-            float amax = 0.f;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(h[j]));
-            const int X = mxfp8_exponent(amax);
-            const float inv = e8m0_value(e8m0_byte(-X));
-            uint32_t w[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t lo = f32x2_to_e4m3x2(h[4 * j] * inv, h[4 * j + 1] * inv);
-                const uint32_t hi = f32x2_to_e4m3x2(h[4 * j + 2] * inv, h[4 * j + 3] * inv);
-                w[j] = lo | (hi << 16);
-            }
-            uint4 *dst = reinterpret_cast<uint4 *>(g.HP + (size_t)pr * g.Ipad + jn * 128 + 32 * c);
-            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-            g.HA[((size_t)tile * g.nksI + jn) * kAtom + atom_byte(r, c)] = (uint8_t)(X + 127);
-        }
     } else {
-        // y * w for 256 columns of H.  The tensor-memory loads are warp-aligned: every lane issues them,
-        // rows past the tile's routes only skip the stores.
-        const float w = valid ? g.hot_w[g.act_off[aidx] + (pr - g.poff[aidx])] : 0.f;
-        for (int c = 4 * half; c < 4 * half + 4; ++c) {
-            const int col = wrow0 + 32 * c;
-            if (col >= g.H) break;  // H % 32 == 0; the same for every lane
-            float y[32];
+        // ---------------- epilogue: row r = 32 (warp % 4) + lane (a warp reaches its own 32 lanes of
+        // tensor memory); the two warps of a lane quarter take one half of the columns each ----------
+        const int quarter = warp & 3, half = (warp - 2) >> 2;
+        const int r = quarter * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        int n = 0;
+        for (int w = blockIdx.x; w < nwork; w += gridDim.x, ++n) {
+            const int tile = w / g.nN, jn = w - tile * g.nN;
+            const int aidx = g.tile_aidx[tile], nrows = g.tile_nrows[tile];
+            const bool valid = r < nrows;
+            const int pr = tile * 128 + r;  // padded route row
+            const bool got = __all_sync(0xffffffffu, mbar_wait(&acc_full, n & 1, g.err, kErrDone));
+            if (!got) break;
+            tc_fence_after();
+            // drain this warp's 128 accumulator columns, then hand the accumulator back to the MMA thread
+            uint32_t v[128];
+            if (kGateUp) {
+                tmem_ld32_sync(tbase + lane_off + half * 64, v);
+                tmem_ld32_sync(tbase + lane_off + half * 64 + 32, v + 32);
+                tmem_ld32_sync(tbase + lane_off + 128 + half * 64, v + 64);
+                tmem_ld32_sync(tbase + lane_off + 128 + half * 64 + 32, v + 96);
+            } else {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t rr[8];
-                if (got)
-                    tmem_ld8_sync(tbase + lane_off + 32 * c + 8 * q, rr);
-                else
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) rr[j] = 0u;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) y[8 * q + j] = w * __uint_as_float(rr[j]);
+                for (int c = 0; c < 4; ++c) tmem_ld32_sync(tbase + lane_off + half * 128 + 32 * c, v + 32 * c);
             }
-            if (valid) {
-                float4 *dst = reinterpret_cast<float4 *>(g.YP + (size_t)pr * g.H + col);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty);
+            if (kGateUp) {
+                // h = SiLU(g) u for 64 of the item's 128 columns of I, one 32-column MXFP8 block at a time
 #pragma unroll
-                for (int j = 0; j < 8; ++j) dst[j] = make_float4(y[4 * j], y[4 * j + 1], y[4 * j + 2], y[4 * j + 3]);
+                for (int cb = 0; cb < 2; ++cb) {
+                    float h[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        h[j] = valid ? silu_fast(__uint_as_float(v[32 * cb + j])) * __uint_as_float(v[64 + 32 * cb + j])
+                                     : 0.f;
+                    float amax = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(h[j]));
+                    const int X = mxfp8_exponent(amax);
+                    const float inv = e8m0_value(e8m0_byte(-X));
+                    uint32_t q[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t lo = f32x2_to_e4m3x2(h[4 * j] * inv, h[4 * j + 1] * inv);
+                        const uint32_t hi = f32x2_to_e4m3x2(h[4 * j + 2] * inv, h[4 * j + 3] * inv);
+                        q[j] = lo | (hi << 16);
+                    }
+                    const int c = 2 * half + cb;  // 32-column block of the item
+                    uint4 *dst = reinterpret_cast<uint4 *>(g.HP + (size_t)pr * g.Ipad + jn * 128 + 32 * c);
+                    dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+                    dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+                    g.HA[((size_t)tile * g.nksI + jn) * kAtom + atom_byte(r, c)] = (uint8_t)(X + 127);
+                }
+            } else {
+                // y * w for 128 of the item's 256 columns of H (rows past the tile's routes are not stored)
+                const int wrow0 = jn * kRowsN;
+                const float wt = valid ? g.hot_w[g.act_off[aidx] + (pr - g.poff[aidx])] : 0.f;
+                if (valid) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int col = wrow0 + half * 128 + 32 * c;
+                        if (col < g.H) {  // H % 32 == 0
+                            float4 *dst = reinterpret_cast<float4 *>(g.YP + (size_t)pr * g.H + col);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                dst[j] = make_float4(wt * __uint_as_float(v[32 * c + 4 * j]),
+                                                     wt * __uint_as_float(v[32 * c + 4 * j + 1]),
+                                                     wt * __uint_as_float(v[32 * c + 4 * j + 2]),
+                                                     wt * __uint_as_float(v[32 * c + 4 * j + 3]));
+                        }
+                    }
+                }
             }
         }
     }
@@ -392,7 +417,8 @@ cudaError_t launch_prefill(const PrefillLaunch &P, cudaStream_t s) {
     g.nN = l.ntI;
     g.Aat = P.XA;
     if (P.ev[0]) cudaEventRecord(P.ev[0], s);
-    prefill_gemm_kernel<1><<<P.tiles_cap * g.nN, kThreads, kSmemBytes, s>>>(*P.mapXP, *P.mapG, *P.mapU, g);
+    const int grid1 = P.tiles_cap * g.nN < P.num_sms ? P.tiles_cap * g.nN : P.num_sms;
+    prefill_gemm_kernel<1><<<grid1, kThreads, kSmemBytes, s>>>(*P.mapXP, *P.mapG, *P.mapU, g);
     if (P.ev[1]) cudaEventRecord(P.ev[1], s);
     // down: A = h (route order), B = Wd tiles of 256 rows of H
     g.off_b0_codes = geo.off_wd_codes;
@@ -404,7 +430,8 @@ cudaError_t launch_prefill(const PrefillLaunch &P, cudaStream_t s) {
     g.nN = (geo.H + 255) / 256;
     g.Aat = P.HA;
     if (P.ev[2]) cudaEventRecord(P.ev[2], s);
-    prefill_gemm_kernel<0><<<P.tiles_cap * g.nN, kThreads, kSmemBytes, s>>>(*P.mapHP, *P.mapD, *P.mapD, g);
+    const int grid0 = P.tiles_cap * g.nN < P.num_sms ? P.tiles_cap * g.nN : P.num_sms;
+    prefill_gemm_kernel<0><<<grid0, kThreads, kSmemBytes, s>>>(*P.mapHP, *P.mapD, *P.mapD, g);
     if (P.ev[3]) cudaEventRecord(P.ev[3], s);
     prefill_combine_kernel<<<P.M, 256, 0, s>>>(P.topk_ids, P.k, P.e2a, P.act_off, P.route_pos, P.poff, P.YP, geo.H,
                                                P.out, P.out_f32);

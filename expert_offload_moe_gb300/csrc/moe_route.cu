@@ -442,57 +442,122 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
 // ---------------------------------------------------------------------------
 // Prefill routing (M > 8; every expert is hot, slot = expert id).
 //
-// Block b owns tokens [16 b, 16 b + 16).  It stages its 16 rows of x in shared
-// memory and streams the router through shared memory 128 columns x 32
-// experts at a time (transposed so lane e reads expert e without bank
-// conflicts); warp w accumulates 4 tokens x 32 experts over one half of each
-// 128-column chunk, and the two halves are added at the end.  Each block then
-// takes top-k + softmax for its tokens (ties to the lower id, as in decode),
-// counts its routes per expert and ranks each route among the block's routes
-// to the same expert (token order).  The last block to arrive turns the
-// per-block counts into offsets and scatters every route to
-//   hot position = offset(expert) + routes to that expert in earlier blocks + rank,
-// i.e. the hot list ordered by (expert, token) -- a counting sort with no
-// serial pass over the routes.
-constexpr int kPfWc = 128;  // router columns per staged chunk
-constexpr int kPfTokWarp = 4;
+// Block b owns tokens [8 b, 8 b + 8).  The router, transposed once to
+// [H][E32] (E rounded up to 32, zero rows), and the block's x rows are
+// streamed through shared memory 128 columns at a time as fp32.  Warp w takes
+// 16 columns of every chunk; each lane accumulates a tile of 2 tokens x 4
+// experts (one 16-byte load of x per token and of the router per column feeds
+// 8 FMAs per column), and the 8 warp sums of a (token, expert) are added in
+// warp order at the end.  Each block then takes top-k + softmax for its
+// tokens (ties to the lower id, as in decode), counts its routes per expert
+// and ranks each route among the block's routes to the same expert (token
+// order).  The last block to arrive turns the per-block counts into
+//   offset(expert) + routes to that expert in earlier blocks,
+// writes hist, the active-expert lists and (when asked) the prefill GEMM tile
+// plan; a second launch then places every route at that offset plus its rank,
+// i.e. the hot list ordered by (expert, token) -- a counting sort.
+constexpr int kPfWc = 128;                  // columns per staged chunk
+constexpr int kPfWarpCols = kPfWc / kWarps; // columns per warp per chunk
+constexpr int kPfXs = kPfWc + 8;            // x row stride in smem (bf16): token rows on distinct banks
+constexpr int kPfStages = 4;                // chunks in flight: 3 ahead of the one being summed
+static_assert(kPfRouteTok == 8 && kWarps == 8, "lane tile: 4 token pairs x 8 expert quads");
 
 struct PfSmem {
-    static size_t bytes(int H, int E) {
-        return (size_t)kPfRouteTok * H * 2 + 2 * kPfWc * 32 * 4 + kPfRouteTok * 32 * 4 + (size_t)kPfRouteTok * E * 4;
-    }
+    static constexpr int kWB = kPfWc * 32 * 4;           // bytes of one router chunk [128 columns][32 experts]
+    static constexpr int kXB = kPfRouteTok * kPfXs * 2;  // bytes of one x chunk [8 tokens][136] bf16
+    static constexpr int kStageB = kWB + kXB;
+    static constexpr int kRedB = kWarps * kPfRouteTok * 32 * 4;
+    static constexpr int kFixedB = kPfStages * kStageB + kRedB;
+    __host__ __device__ static size_t bytes(int E) { return (size_t)kFixedB + (size_t)kPfRouteTok * E * 4; }
 };
+static_assert(PfSmem::kStageB % 16 == 0 && PfSmem::kWB % 16 == 0, "16-byte copies");
 
-__device__ __forceinline__ void pf_load_w(const RouteParams &p, int eg, int c, float4 (&r)[4]) {
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, bool valid) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
+    const int n = valid ? 16 : 0;  // 0: the 16 bytes are zero-filled
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Copies chunk c of expert group eg into a stage: the router block [128 columns][32 experts] of WrT and
+// the block's 8 x rows (bf16), zeros past H and M (the router rows past E are zero in WrT).
+__device__ __forceinline__ void pf_issue(const RouteParams &p, int t0, int eg, int c, unsigned char *stage) {
+    float *sW = reinterpret_cast<float *>(stage);
+    uint16_t *sX = reinterpret_cast<uint16_t *>(stage + PfSmem::kWB);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const int idx = threadIdx.x + i * kThreads, el = idx & 31, cg = idx >> 5;
-        const int e = eg * 32 + el, col = c * kPfWc + cg * 4;
-        r[i] = (e < p.E && col < p.H) ? __ldg(reinterpret_cast<const float4 *>(p.Wr + (size_t)e * p.H + col))
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        const int idx = threadIdx.x + i * kThreads, row = idx >> 3, f4 = idx & 7;
+        const int col = c * kPfWc + row;
+        const bool ok = col < p.H;
+        cp_async16(sW + idx * 4, p.WrT + (size_t)(ok ? col : 0) * p.E32 + eg * 32 + f4 * 4, ok);
+    }
+    if (threadIdx.x < kPfRouteTok * (kPfWc / 8)) {
+        const int t = threadIdx.x / (kPfWc / 8), c8 = threadIdx.x % (kPfWc / 8);
+        const int col = c * kPfWc + c8 * 8;
+        const bool ok = t0 + t < p.M && col < p.H;
+        cp_async16(sX + t * kPfXs + c8 * 8, p.x + (ok ? (size_t)(t0 + t) * p.H + col : 0), ok);
     }
 }
 
-__device__ __forceinline__ void pf_store_w(float *sW, const float4 (&r)[4]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int idx = threadIdx.x + i * kThreads, el = idx & 31, cg = idx >> 5;
-        sW[(cg * 4 + 0) * 32 + el] = r[i].x;
-        sW[(cg * 4 + 1) * 32 + el] = r[i].y;
-        sW[(cg * 4 + 2) * 32 + el] = r[i].z;
-        sW[(cg * 4 + 3) * 32 + el] = r[i].w;
-    }
+// Exclusive prefix over blocks of cnt[b][e] (row stride E) for every expert, in place; tot[e] = the sum.
+// Lanes take experts, warps take contiguous ranges of blocks; the loads of 8 blocks go out before their
+// stores (the compiler keeps a load behind a store to the same array).
+template <bool kGlobal>
+__device__ __forceinline__ int pf_ld(const int *a) {
+    if constexpr (kGlobal) return __ldcg(a);  // written by other blocks
+    else return *a;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) route_prefill_kernel(RouteParams p) {
-    extern __shared__ __align__(16) unsigned char pf_smem[];
+template <bool kGlobal>
+__device__ void pf_block_prefix(int *cnt, int nblk, int E, int *tot, int (*s_part)[32]) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int H = p.H, E = p.E, M = p.M, k = p.k;
+    const int per = (nblk + kWarps - 1) / kWarps, b0 = min(warp * per, nblk), b1 = min(b0 + per, nblk);
+    for (int eb = 0; eb < E; eb += 32) {
+        const int e = eb + lane;
+        int sum = 0;
+        if (e < E)
+            for (int bb = b0; bb < b1; bb += 8) {
+                int v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = bb + i < b1 ? pf_ld<kGlobal>(cnt + (size_t)(bb + i) * E + e) : 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) sum += v[i];
+            }
+        s_part[warp][lane] = sum;
+        __syncthreads();
+        int run = 0, total = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            const int v = s_part[w][lane];
+            run += w < warp ? v : 0;
+            total += v;
+        }
+        if (e < E) {
+            for (int bb = b0; bb < b1; bb += 8) {
+                int v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = bb + i < b1 ? pf_ld<kGlobal>(cnt + (size_t)(bb + i) * E + e) : 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (bb + i < b1) {
+                        cnt[(size_t)(bb + i) * E + e] = run;
+                        run += v[i];
+                    }
+            }
+            if (warp == 0) tot[e] = total;
+        }
+        __syncthreads();
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) route_prefill_kernel(RouteParams p) {
+    extern __shared__ __align__(16) unsigned char pf_raw[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int E = p.E, M = p.M, k = p.k;
     const int t0 = blockIdx.x * kPfRouteTok;
-    uint16_t *sX = reinterpret_cast<uint16_t *>(pf_smem);                       // [16][H]
-    float *sW = reinterpret_cast<float *>(pf_smem + (size_t)kPfRouteTok * H * 2);  // [2][128][32]
-    float *sRed = sW + 2 * kPfWc * 32;                                           // [16][32]
-    float *sL = sRed + kPfRouteTok * 32;                                         // [16][E]
+    float *sRed = reinterpret_cast<float *>(pf_raw + kPfStages * PfSmem::kStageB);  // [8 warps][8 tokens][32]
+    float *sL = sRed + kWarps * kPfRouteTok * 32;                                     // [8][E]
     __shared__ float s_bias[kMaxExperts];
     __shared__ int s_cnt[kMaxExperts];
     __shared__ int s_off[kMaxExperts];
@@ -501,9 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1) route_prefill_kernel(RouteParams 
     __shared__ int s_sel_id[kWarps][kMaxTopK];
     __shared__ float s_sel_l[kWarps][kMaxTopK];
 
-    const int nc = (H + kPfWc - 1) / kPfWc;
-    float4 wr[4];
-    pf_load_w(p, 0, 0, wr);  // the router is constant: read before waiting for the previous grid
+    const int nc = (p.H + kPfWc - 1) / kPfWc;
     for (int e = threadIdx.x; e < E; e += kThreads) {
         s_bias[e] = p.bias ? p.bias[e] : 0.f;
         s_cnt[e] = 0;
@@ -511,67 +574,67 @@ __global__ void __launch_bounds__(kThreads, 1) route_prefill_kernel(RouteParams 
     tc::pdl_wait();
     tc::pdl_trigger();
 
-    // x rows of the block (zeros past M)
-    const int hv = H / 8;
-    for (int q = threadIdx.x; q < kPfRouteTok * hv; q += kThreads) {
-        const int t = q / hv, c8 = q - t * hv;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (t0 + t < M) v = __ldg(reinterpret_cast<const uint4 *>(p.x + (size_t)(t0 + t) * H) + c8);
-        reinterpret_cast<uint4 *>(sX + (size_t)t * H)[c8] = v;
-    }
-
     // ---------------- logits: 32 experts at a time --------------------------
-    const int g = warp & 3, hh = warp >> 2;
+    const int tg = lane >> 3, eq = lane & 7;  // tokens 2 tg, 2 tg + 1; experts 4 eq .. 4 eq + 3 of the group
     const int neg = (E + 31) / 32;
     for (int eg = 0; eg < neg; ++eg) {
-        if (eg > 0) pf_load_w(p, eg, 0, wr);
-        pf_store_w(sW, wr);
-        __syncthreads();
-        float acc[kPfTokWarp] = {0.f, 0.f, 0.f, 0.f};
+        // one commit group per chunk (empty past the last), so "all but the newest 3" is always chunk c
+#pragma unroll
+        for (int c = 0; c < kPfStages - 1; ++c) {
+            if (c < nc) pf_issue(p, t0, eg, c, pf_raw + c * PfSmem::kStageB);
+            cp_async_commit();
+        }
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         for (int c = 0; c < nc; ++c) {
-            if (c + 1 < nc) pf_load_w(p, eg, c + 1, wr);
-            const float *w = sW + (c & 1) * kPfWc * 32;
-            const int col0 = c * kPfWc + hh * (kPfWc / 2);
-            if (col0 < H) {  // H % 64 == 0: a half chunk is all valid or all past H
-#pragma unroll 2
-                for (int j = 0; j < kPfWc / 2; j += 8) {
-                    float wv[8];
+            cp_async_wait<kPfStages - 2>();
+            __syncthreads();  // chunk c is in smem for every thread; stage (c - 1) % 4 is free
+            if (c + kPfStages - 1 < nc)
+                pf_issue(p, t0, eg, c + kPfStages - 1, pf_raw + ((c + kPfStages - 1) % kPfStages) * PfSmem::kStageB);
+            cp_async_commit();
+            const unsigned char *stage = pf_raw + (c % kPfStages) * PfSmem::kStageB;
+            const float *w = reinterpret_cast<const float *>(stage) + warp * kPfWarpCols * 32 + eq * 4;
+            const uint16_t *xs = reinterpret_cast<const uint16_t *>(stage + PfSmem::kWB) + 2 * tg * kPfXs +
+                                 warp * kPfWarpCols;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) wv[q] = w[(hh * (kPfWc / 2) + j + q) * 32 + lane];
+            for (int j = 0; j < kPfWarpCols; j += 4) {
+                const uint2 xa = *reinterpret_cast<const uint2 *>(xs + j);
+                const uint2 xb = *reinterpret_cast<const uint2 *>(xs + kPfXs + j);
+                const float xv0[4] = {bf16_lo(xa.x), bf16_hi(xa.x), bf16_lo(xa.y), bf16_hi(xa.y)};
+                const float xv1[4] = {bf16_lo(xb.x), bf16_hi(xb.x), bf16_lo(xb.y), bf16_hi(xb.y)};
 #pragma unroll
-                    for (int t = 0; t < kPfTokWarp; ++t) {
-                        const uint4 xv = *reinterpret_cast<const uint4 *>(sX + (size_t)(g * kPfTokWarp + t) * H + col0 + j);
-                        float a = acc[t];
-                        a = fmaf(bf16_lo(xv.x), wv[0], a);
-                        a = fmaf(bf16_hi(xv.x), wv[1], a);
-                        a = fmaf(bf16_lo(xv.y), wv[2], a);
-                        a = fmaf(bf16_hi(xv.y), wv[3], a);
-                        a = fmaf(bf16_lo(xv.z), wv[4], a);
-                        a = fmaf(bf16_hi(xv.z), wv[5], a);
-                        a = fmaf(bf16_lo(xv.w), wv[6], a);
-                        a = fmaf(bf16_hi(xv.w), wv[7], a);
-                        acc[t] = a;
-                    }
+                for (int q = 0; q < 4; ++q) {
+                    const float4 wq = *reinterpret_cast<const float4 *>(w + (j + q) * 32);
+                    acc[0][0] = fmaf(xv0[q], wq.x, acc[0][0]);
+                    acc[0][1] = fmaf(xv0[q], wq.y, acc[0][1]);
+                    acc[0][2] = fmaf(xv0[q], wq.z, acc[0][2]);
+                    acc[0][3] = fmaf(xv0[q], wq.w, acc[0][3]);
+                    acc[1][0] = fmaf(xv1[q], wq.x, acc[1][0]);
+                    acc[1][1] = fmaf(xv1[q], wq.y, acc[1][1]);
+                    acc[1][2] = fmaf(xv1[q], wq.z, acc[1][2]);
+                    acc[1][3] = fmaf(xv1[q], wq.w, acc[1][3]);
                 }
             }
-            if (c + 1 < nc) pf_store_w(sW + ((c + 1) & 1) * kPfWc * 32, wr);
-            __syncthreads();
         }
-        if (hh == 1)
+        cp_async_wait<0>();
 #pragma unroll
-            for (int t = 0; t < kPfTokWarp; ++t) sRed[(g * kPfTokWarp + t) * 32 + lane] = acc[t];
-        __syncthreads();
-        const int e = eg * 32 + lane;
-        if (hh == 0 && e < E)
+        for (int t = 0; t < 2; ++t)
+            *reinterpret_cast<float4 *>(sRed + (warp * kPfRouteTok + 2 * tg + t) * 32 + eq * 4) =
+                make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
+        __syncthreads();  // also: every stage is idle before the next expert group refills them
+        {  // one (token, expert) per thread: the warp sums in warp order, then the bias
+            const int tl = warp, e = eg * 32 + lane;
+            float v = 0.f;
 #pragma unroll
-            for (int t = 0; t < kPfTokWarp; ++t) {
-                const float v = acc[t] + sRed[(g * kPfTokWarp + t) * 32 + lane] + s_bias[e];
-                sL[(size_t)(g * kPfTokWarp + t) * E + e] = (v != v) ? -INFINITY : v;  // NaN marks a taken expert
+            for (int w2 = 0; w2 < kWarps; ++w2) v += sRed[(w2 * kPfRouteTok + tl) * 32 + lane];
+            if (e < E) {
+                v += s_bias[e];
+                sL[(size_t)tl * E + e] = (v != v) ? -INFINITY : v;  // NaN marks a taken expert below
             }
+        }
         __syncthreads();
     }
 
-    // ---------------- top-k + softmax: two tokens per warp -------------------
+    // ---------------- top-k + softmax: one token per warp --------------------
     for (int tl = warp; tl < kPfRouteTok; tl += kWarps) {
         const int t = t0 + tl;
         if (t >= M) continue;  // warp-uniform
@@ -617,8 +680,8 @@ __global__ void __launch_bounds__(kThreads, 1) route_prefill_kernel(RouteParams 
     }
     __syncthreads();
     // rank of each route among the block's earlier tokens routed to the same expert
-    for (int r = threadIdx.x; r < kPfRouteTok * k; r += kThreads) {
-        const int tl = r / k, j = r - tl * k;
+    for (int q = threadIdx.x; q < kPfRouteTok * k; q += kThreads) {
+        const int tl = q / k, j = q - tl * k;
         if (t0 + tl >= M) continue;
         const int e = s_ids[tl][j];
         int n = 0;
@@ -628,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1) route_prefill_kernel(RouteParams 
     }
     for (int e = threadIdx.x; e < E; e += kThreads) p.b.blk_cnt[(size_t)blockIdx.x * E + e] = s_cnt[e];
 
-    // ---------------- arrival: the last block scatters ----------------------
+    // ---------------- arrival: the last block makes the offsets -------------
     __shared__ int s_last;
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -640,46 +703,51 @@ __global__ void __launch_bounds__(kThreads, 1) route_prefill_kernel(RouteParams 
     __syncthreads();
     if (!s_last) return;
 
-    // per expert: exclusive prefix of the block counts (in place), tpe lanes per expert
-    const int nblk = gridDim.x;
-    int tpe = 1;  // a power of two <= 32, so an expert's lanes never straddle a warp
-    while (tpe < 32 && E * tpe * 2 <= kThreads) tpe *= 2;
-    for (int base = 0; base < E * tpe; base += kThreads) {
-        const int q = base + threadIdx.x;
-        const int e = q / tpe, part = q - e * tpe;  // tpe consecutive lanes share an expert
-        const int per = (nblk + tpe - 1) / tpe, b0 = min(part * per, nblk), b1 = min(b0 + per, nblk);
-        int sum = 0;
-        if (e < E) {
-#pragma unroll 4
-            for (int b = b0; b < b1; ++b) sum += __ldcg(p.b.blk_cnt + (size_t)b * E + e);
-        }
-        int x = sum;  // inclusive scan over the tpe lanes of this expert
-        for (int o = 1; o < tpe; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, o);
-            if (part >= o) x += y;
-        }
-        const int total = __shfl_sync(0xffffffffu, x, (lane | (tpe - 1)));
-        int run = x - sum;
-        if (e < E) {
-            for (int b = b0; b < b1; ++b) {
-                const int v = __ldcg(p.b.blk_cnt + (size_t)b * E + e);
-                p.b.blk_cnt[(size_t)b * E + e] = run;
-                run += v;
+    __shared__ int s_part[kWarps][32];
+    const int nblk = gridDim.x, ncnt = nblk * E;
+    const bool in_smem = (size_t)ncnt * 4 <= PfSmem::bytes(E);
+    int *sc = reinterpret_cast<int *>(pf_raw);  // the chunk buffers are free now
+    if (in_smem) {
+        for (int i0 = 0; i0 < ncnt; i0 += 8 * kThreads) {
+            int v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int idx = i0 + i * kThreads + threadIdx.x;
+                v[i] = idx < ncnt ? __ldcg(p.b.blk_cnt + idx) : 0;
             }
-            if (part == 0) {
-                p.b.hist[e] = total;
-                s_cnt[e] = total;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int idx = i0 + i * kThreads + threadIdx.x;
+                if (idx < ncnt) sc[idx] = v[i];
             }
         }
+        __syncthreads();
+        pf_block_prefix<false>(sc, nblk, E, s_cnt, s_part);
+    } else {
+        pf_block_prefix<true>(p.b.blk_cnt, nblk, E, s_cnt, s_part);
     }
-    __syncthreads();
     for (int e = threadIdx.x; e < E; e += kThreads) {
+        p.b.hist[e] = s_cnt[e];
         s_off[e] = s_cnt[e];
         s_act[e] = s_cnt[e] > 0;
     }
     __syncthreads();
     block_scan_array(s_off, E);
     const int n_act = block_scan_array(s_act, E);
+    // block offsets + expert offsets: the hot position of a route is this plus its rank
+    for (int i0 = 0; i0 < ncnt; i0 += 8 * kThreads) {
+        int v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int idx = i0 + i * kThreads + threadIdx.x;
+            v[i] = idx < ncnt ? (in_smem ? sc[idx] : __ldcg(p.b.blk_cnt + idx)) : 0;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int idx = i0 + i * kThreads + threadIdx.x;
+            if (idx < ncnt) p.b.blk_cnt[idx] = v[i] + s_off[idx % E];
+        }
+    }
     for (int e = threadIdx.x; e < E; e += kThreads) {
         if (s_cnt[e] == 0) continue;
         const int a = s_act[e];
@@ -689,16 +757,6 @@ __global__ void __launch_bounds__(kThreads, 1) route_prefill_kernel(RouteParams 
         p.b.act_cnt[a] = s_cnt[e];
     }
     const int nr = M * k;
-#pragma unroll 4
-    for (int r = threadIdx.x; r < nr; r += kThreads) {
-        const int t = r / k;
-        const int e = __ldcg(p.b.topk_ids + r);
-        const int pos = s_off[e] + __ldcg(p.b.blk_cnt + (size_t)(t / kPfRouteTok) * E + e) + __ldcg(p.b.route_rank + r);
-        p.b.hot_expert[pos] = e;
-        p.b.hot_token[pos] = t;
-        p.b.hot_w[pos] = __ldcg(p.b.topk_w + r);
-        p.b.route_rank[r] = pos;  // only this thread reads or writes entry r
-    }
 
     // tile plan for the grouped GEMMs: each active expert's routes padded to whole 128-row tiles, in
     // expert order (a tile never mixes experts)
@@ -731,6 +789,28 @@ __global__ void __launch_bounds__(kThreads, 1) route_prefill_kernel(RouteParams 
     }
 }
 
+// Second prefill routing launch: every route to its hot position (block offset from the first launch
+// plus its rank within its block).
+__global__ void __launch_bounds__(kThreads) route_scatter_kernel(RouteParams p) {
+    const int q = blockIdx.x * kThreads + threadIdx.x;
+    if (q >= p.M * p.k) return;
+    const int t = q / p.k, e = p.b.topk_ids[q];
+    const int pos = p.b.blk_cnt[(size_t)(t / kPfRouteTok) * p.E + e] + p.b.route_rank[q];
+    p.b.hot_expert[pos] = e;
+    p.b.hot_token[pos] = t;
+    p.b.hot_w[pos] = p.b.topk_w[q];
+    p.b.route_rank[q] = pos;
+}
+
+// Wr [E][H] -> WrT [H][E32] (experts past E are zero rows).
+__global__ void router_transpose_kernel(const float *Wr, float *WrT, int E, int H, int E32) {
+    const long n = (long)H * E32;
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+        const int col = (int)(i / E32), e = (int)(i - (long)col * E32);
+        WrT[i] = e < E ? Wr[(size_t)e * H + col] : 0.f;
+    }
+}
+
 constexpr int kMaxMapUpdates = 64;
 
 struct MapUpdate {
@@ -747,8 +827,8 @@ __global__ void map_update_kernel(int32_t *e2s, MapUpdate u) {
 }  // namespace
 
 cudaError_t launch_route(const RouteParams &p, cudaStream_t s, int num_sms) {
-    const size_t smem = PfSmem::bytes(p.H, p.E);
-    const bool tiled = p.all_hot && p.M > kDecodeMaxTokens && p.b.blk_cnt && p.b.route_rank && smem <= 200 * 1024;
+    const size_t smem = PfSmem::bytes(p.E);
+    const bool tiled = p.all_hot && p.M > kDecodeMaxTokens && p.b.blk_cnt && p.b.route_rank && p.WrT;
     if (p.pf_poff && !tiled) return cudaErrorNotSupported;  // only the tiled launch plans the prefill GEMMs
     if (tiled) {
         static size_t smem_set = 0;  // the kernel's dynamic shared memory limit raised so far
@@ -768,7 +848,10 @@ cudaError_t launch_route(const RouteParams &p, cudaStream_t s, int num_sms) {
         at[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = at;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, route_prefill_kernel, p);
+        cudaError_t e = cudaLaunchKernelEx(&cfg, route_prefill_kernel, p);
+        if (e != cudaSuccess) return e;
+        route_scatter_kernel<<<(p.M * p.k + kThreads - 1) / kThreads, kThreads, 0, s>>>(p);
+        return cudaGetLastError();
     }
     const int ntask = p.E * p.nchunk + (p.xq ? p.M * (p.H / 32) : 0);
     int grid = (ntask + kWarps - 1) / kWarps;
@@ -783,6 +866,11 @@ cudaError_t launch_route(const RouteParams &p, cudaStream_t s, int num_sms) {
     cfg.attrs = at;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, route_kernel, p);
+}
+
+cudaError_t launch_router_transpose(const float *Wr, float *WrT, int E, int H, int E32, cudaStream_t s) {
+    router_transpose_kernel<<<256, 256, 0, s>>>(Wr, WrT, E, H, E32);
+    return cudaGetLastError();
 }
 
 void launch_map_update(int32_t *e2s, int n, const int32_t *experts, const int32_t *slots, cudaStream_t s) {
