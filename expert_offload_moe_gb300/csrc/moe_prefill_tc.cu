@@ -60,6 +60,15 @@ __device__ __forceinline__ int mxfp8_exponent(float amax) {
 // denominator is infinite and the quotient 0, the limit of SiLU.
 __device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.f + expf(-g)); }
 
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+// One arrival on bar once all of this thread's earlier cp.async copies have landed (counted in the
+// barrier's expected arrivals, not added to them).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ x -> MXFP8, route order
@@ -152,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_alloc(&tslot, kTmemCols);
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], 1 + 32);  // the copy thread's expect_tx + the 32 lanes' atom copies
             mbar_init(&empty[s], 1);
         }
         mbar_init(&acc_full, 1);
@@ -194,16 +203,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (lane == 0) {
                     const uint32_t wtx = tail ? 0u : (uint32_t)kTileWTx;
-                    mbar_expect_tx(&full[st], kTileActTx + wtx * (b1 ? 2u : 1u) + kAtom * (b1 ? 3u : 2u));
+                    mbar_expect_tx(&full[st], kTileActTx + wtx * (b1 ? 2u : 1u));
                     tma_load_3d(&mapA, &full[st], sS, i * 128, tile * 128, 0);
                     if (!tail) {
                         tma_load_3d(&mapB0, &full[st], sS + kOffB0, i * 128, r0, expert);
                         if (b1) tma_load_3d(&mapB1, &full[st], sS + kOffB1, i * 128, r1, expert);
                     }
-                    bulk_copy(sS + kOffAtA, g.Aat + ((size_t)tile * nks + i) * kAtom, kAtom, &full[st]);
-                    bulk_copy(sS + kOffAtB0, exat + atom0, kAtom, &full[st]);
-                    if (b1 && (kGateUp || (r1 >> 7) < ntW)) bulk_copy(sS + kOffAtB1, exat + atom1, kAtom, &full[st]);
                 }
+                // the scale atoms (512 bytes each) by the lanes, 16 bytes apiece: small copies through the
+                // tensor-copy unit would each cost it a whole request
+                cp_async16(sS + kOffAtA + lane * 16, g.Aat + ((size_t)tile * nks + i) * kAtom + lane * 16);
+                cp_async16(sS + kOffAtB0 + lane * 16, exat + atom0 + lane * 16);
+                if (b1 && (kGateUp || (r1 >> 7) < ntW)) cp_async16(sS + kOffAtB1 + lane * 16, exat + atom1 + lane * 16);
+                cp_async_arrive_noinc(&full[st]);
                 __syncwarp();
             }
         }
@@ -227,6 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = mbar_wait(&full[st], (it / S) & 1, g.err, kErrFull);
                     if (!ok) break;
                     tc_fence_after();
+                    fence_proxy_async();  // the atoms came through the generic proxy (cp.async)
                     uint8_t *sS = smem + st * kStage;
                     const uint32_t sfa = tbase + kColSF + 12 * st, sfb0 = sfa + 4, sfb1 = sfa + 8;
                     atom_to_tmem(sfa, sS + kOffAtA);
