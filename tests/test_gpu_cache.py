@@ -10,7 +10,7 @@ import oracle  # noqa: E402
 from expert_offload_moe_gb300 import build as moe_build  # noqa: E402
 from expert_offload_moe_gb300 import moe, stack, synth  # noqa: E402
 
-from parity import compare_routing, compare_values, dev_bytes, route_arrays  # noqa: E402
+from parity import compare_routing, compare_values, dev_bytes, near_tie_tokens, route_arrays  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -135,3 +135,69 @@ def test_cache_update_needs_a_route():
         lay.cache_update()
     assert ei.value.code == moe.MOE_ESTATE
     lay.close()
+
+
+def test_c4_prefill_then_decode_churn_follows_oracle_replay():
+    """The gpt-oss-shaped prefill-then-decode workload: 16 of 32 slots, LFU, at most 2 refills per step,
+    popularity drifting from order A to order B.  Step 0 is the 2048-token prefill on the staged bank; its
+    routes count in the scores like any other.  Every decode step is checked against the oracle under the
+    map it saw, every map against the oracle's policy replay, and every refilled slot against the bank."""
+    w = synth.WORKLOADS["gptoss20b_prefill2048_s16_lfu_drift"]
+    steps = 24  # the 256-step drift compressed, so that refills happen within the test
+    li = stack.LayerInputs(w, 0)
+    M_pf = w.prefill_tokens
+    lay = li.make_layer(max_tokens=M_pf, out_f32=True, max_refills=2, score_decay=1.0,
+                        visibility=moe.MOE_VIS_DETERMINISTIC)
+    replay = oracle.CacheReplay(li.e2s, w.slots, decay=1.0, R=2)
+    refills = 0
+    try:
+        staging = torch.empty(w.experts * w.expert_bytes, dtype=torch.uint8, device="cuda")
+        lay.attach_staging(staging)
+        lay.stage_all()
+        # step 0: prefill
+        bias = synth.drifting_bias(0, 0, w.experts, w.bias_tau, 0, steps)
+        lay.set_bias(torch.from_numpy(bias).cuda())
+        x_bits = synth.activations(0, 0, 0, M_pf, w.hidden)
+        x = stack.bf16_tensor(x_bits)
+        out = torch.empty((M_pf, w.hidden), dtype=torch.float32, device="cuda")
+        res = lay.route(x, M_pf)
+        lay.forward_slots(x, out, M_pf)
+        g = route_arrays(res, w.experts, w.top_k)
+        logits = oracle.router_logits(x_bits, li.Wr, bias)
+        ids, _ = oracle.topk_softmax(logits, w.top_k)
+        tie = near_tie_tokens(logits, w.top_k)
+        same = np.array([set(g["ids"][t]) == set(ids[t]) for t in range(M_pf)])
+        assert np.all(same | tie)
+        if same.all():
+            assert np.array_equal(g["hist"], np.bincount(ids.ravel(), minlength=w.experts))
+        n = lay.cache_update()
+        pairs = replay.step(g["hist"], 0)
+        assert n == len(pairs) and np.array_equal(lay.get_map(), replay.e2s)
+        refills += n
+        del staging
+        # decode steps
+        out1 = torch.empty((1, w.hidden), dtype=torch.float32, device="cuda")
+        for st in range(1, steps):
+            bias = synth.drifting_bias(0, 0, w.experts, w.bias_tau, st, steps)
+            lay.set_bias(torch.from_numpy(bias).cuda())
+            e2s_seen = lay.get_map()
+            x_bits = synth.activations(0, 0, 1000 + st, 1, w.hidden)
+            x = stack.bf16_tensor(x_bits)
+            res = lay.route(x, 1)
+            lay.forward_slots(x, out1, 1)
+            g = route_arrays(res, w.experts, w.top_k)
+            o = oracle.moe_layer(x_bits, li.Wr, bias, li.bank.numpy(), e2s_seen, w.top_k, w.hidden, w.inter)
+            excl = compare_routing(g, o, o["logits"], w.top_k, e2s_seen)
+            compare_values(out1.cpu().numpy(), o["out_f32"], True, exclude=sorted(excl))
+            n = lay.cache_update()
+            pairs = replay.step(o["hist"], st)
+            assert n == len(pairs), st
+            assert np.array_equal(lay.get_map(), replay.e2s), st
+            torch.cuda.synchronize()
+            for e, slot, _victim in pairs:  # the refilled slots hold their new expert's bytes
+                got = dev_bytes(lay.slot_ptr(slot), w.expert_bytes)
+                assert np.array_equal(got, li.bank.numpy()[e]), (st, e, slot)
+            refills += n
+    finally:
+        lay.close()
+    assert refills > 0
