@@ -194,6 +194,122 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
     for (int e = threadIdx.x; e < E; e += kThreads) s_hist[e] = 0;
     __syncthreads();
 
+    if (M <= kWarps && E <= 32 && p.nchunk <= kMaxChunks) {
+        // Decode with at most 32 experts: warp t takes token t, lane e expert e.  The logit is summed from
+        // the chunk partials in chunk order (all loads first), the k winners are ranked in one pass (ties
+        // to the lower id, as the arg-max rounds below), then warp 0 writes the expert lists and the hot
+        // routes and warp 1 the cold routes.
+        if (warp < M) {
+            const int t = warp;
+            float v = -INFINITY;
+            if (lane < E) {
+                float pv[kMaxChunks];
+#pragma unroll
+                for (int c = 0; c < kMaxChunks; ++c)
+                    pv[c] = c < p.nchunk ? __ldcg(p.b.logit_part + ((size_t)c * M + t) * E + lane) : 0.f;
+                float a = 0.f;
+#pragma unroll
+                for (int c = 0; c < kMaxChunks; ++c)
+                    if (c < p.nchunk) a += pv[c];
+                a += s_bias[lane];
+                v = (a != a) ? -INFINITY : a;
+            }
+            int rank = 0;  // experts that come before this one: larger logit, or equal and lower id
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float o = __shfl_sync(0xffffffffu, v, j);
+                rank += (o > v) || (o == v && j < lane);
+            }
+            if (lane < E && rank < k) {
+                s_sel_id[warp][rank] = lane;
+                s_sel_l[warp][rank] = v;
+            }
+            __syncwarp();
+            if (lane < k) {
+                const float lmax = s_sel_l[warp][0];
+                float den = 0.f;
+                for (int j = 0; j < k; ++j) den += expf(s_sel_l[warp][j] - lmax);
+                const int id = s_sel_id[warp][lane];
+                const float wj = expf(s_sel_l[warp][lane] - lmax) / den;
+                p.b.topk_ids[(size_t)t * k + lane] = id;
+                p.b.topk_w[(size_t)t * k + lane] = wj;
+                s_ids[t * k + lane] = id;
+                s_w[t * k + lane] = wj;
+                atomicAdd(&s_hist[id], 1);
+            }
+        }
+        __syncthreads();
+        if (warp == 0) {
+            const int e = lane;
+            const int hist = e < E ? s_hist[e] : 0;
+            const int h = (e < E && s_e2s[e] >= 0) ? hist : 0, act = h > 0;
+            int xh = h, xa = act;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int yh = __shfl_up_sync(0xffffffffu, xh, o), ya = __shfl_up_sync(0xffffffffu, xa, o);
+                if (lane >= o) {
+                    xh += yh;
+                    xa += ya;
+                }
+            }
+            if (e < E) p.b.hist[e] = hist;
+            if (act) {
+                const int oa = xa - 1;
+                int pos = xh - h;
+                p.b.act_expert[oa] = e;
+                p.b.act_slot[oa] = s_e2s[e];
+                p.b.act_off[oa] = pos;
+                p.b.act_cnt[oa] = h;
+                for (int t = 0; t < M; ++t)
+                    for (int j = 0; j < k; ++j)
+                        if (s_ids[t * k + j] == e) {
+                            p.b.hot_expert[pos] = e;
+                            p.b.hot_token[pos] = t;
+                            p.b.hot_w[pos] = s_w[t * k + j];
+                            ++pos;
+                        }
+            }
+            if (lane == 31) {
+                p.b.counts[0] = xh;
+                p.b.counts[2] = xa;
+                p.b.counts[3] = M;
+            }
+        } else if (warp == 1) {
+            // cold routes of token `lane`, ascending expert id
+            int ce[kMaxTopK];
+            float cw[kMaxTopK];
+            int n = 0;
+            if (lane < M)
+                for (int j = 0; j < k; ++j) {
+                    const int e = s_ids[lane * k + j];
+                    if (s_e2s[e] >= 0) continue;
+                    const float wt = s_w[lane * k + j];
+                    int q = n++;  // insertion by expert id
+                    while (q > 0 && ce[q - 1] > e) {
+                        ce[q] = ce[q - 1];
+                        cw[q] = cw[q - 1];
+                        --q;
+                    }
+                    ce[q] = e;
+                    cw[q] = wt;
+                }
+            int x = n;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            const int base = x - n;
+            for (int q = 0; q < n; ++q) {
+                p.b.cold_token[base + q] = lane;
+                p.b.cold_expert[base + q] = ce[q];
+                p.b.cold_w[base + q] = cw[q];
+            }
+            if (lane == 31) p.b.counts[1] = x;
+        }
+        return;
+    }
+
     // Decode (M <= 8): every thread sums chunk partials for some (token, expert) pairs, all loads of a
     // pair issued before the sum (in chunk order), into row t of s_l; warp t then selects from its row.
     const bool rows_by_block = M <= kWarps && p.nchunk <= kMaxChunks;
