@@ -60,14 +60,6 @@ __device__ __forceinline__ int mxfp8_exponent(float amax) {
 // denominator is infinite and the quotient 0, the limit of SiLU.
 __device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.f + expf(-g)); }
 
-__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-// One arrival on bar once all of this thread's earlier cp.async copies have landed (counted in the
-// barrier's expected arrivals, not added to them).
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 
 }  // namespace
 

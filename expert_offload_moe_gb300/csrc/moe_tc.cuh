@@ -87,6 +87,28 @@ __device__ __forceinline__ void tma_load_3d(const CUtensorMap *map, uint64_t *ba
         : "memory");
 }
 
+// 16 bytes global -> shared by this thread (cp.async, generic proxy).
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+// One arrival on bar once all of this thread's earlier cp.async copies have landed (counted in the
+// barrier's expected arrivals, not added to them).  The consumer runs fence_proxy_async() after its wait
+// before the tensor cores read the copied bytes.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// The lanes of a warp copy a rows x 128-byte tile (row stride src_stride) into the 128-byte-swizzled K-major
+// layout the MMA descriptors read: 16-byte chunk c of row r lands at chunk c ^ (r % 8).
+__device__ __forceinline__ void cp_async_tile_sw128(uint8_t *dst, const uint8_t *src, size_t src_stride, int rows,
+                                                    int lane) {
+    for (int q = lane; q < rows * 8; q += 32) {
+        const int r = q >> 3, c = q & 7;
+        cp_async16(dst + r * 128 + ((c ^ (r & 7)) << 4), src + (size_t)r * src_stride + c * 16);
+    }
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
