@@ -330,6 +330,118 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
         __syncthreads();
     }
 
+    if (rows_by_block && E > 32) {
+        // Decode with more than 32 experts.  Top-k: warp t holds its token's logits in registers (expert
+        // lane + 32 i in v[i]) and takes k arg-max rounds over them -- the same rounds, order and ties as
+        // below, without going back to shared memory.
+        constexpr int kPer = kMaxExperts / 32;
+        for (int t = warp; t < M; t += kWarps) {
+            float v[kPer];
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                const int e = lane + 32 * i;
+                v[i] = e < E ? s_l[t][e] : __int_as_float(0x7fc00000);  // NaN: never a candidate
+            }
+            for (int j = 0; j < k; ++j) {
+                float bv = -INFINITY;
+                int be = 0x7fffffff;
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) {
+                    const int e = lane + 32 * i;
+                    if (v[i] > bv || (v[i] == bv && e < be)) {
+                        bv = v[i];
+                        be = e;
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                    const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                    if (ov > bv || (ov == bv && oe < be)) {
+                        bv = ov;
+                        be = oe;
+                    }
+                }
+                if (lane == 0) {
+                    s_sel_id[warp][j] = be;
+                    s_sel_l[warp][j] = bv;
+                }
+#pragma unroll
+                for (int i = 0; i < kPer; ++i)
+                    if (lane + 32 * i == be) v[i] = __int_as_float(0x7fc00000);
+            }
+            __syncwarp();
+            if (lane < k) {
+                const float lmax = s_sel_l[warp][0];
+                float den = 0.f;
+                for (int j = 0; j < k; ++j) den += expf(s_sel_l[warp][j] - lmax);
+                const int id = s_sel_id[warp][lane];
+                const float wj = expf(s_sel_l[warp][lane] - lmax) / den;
+                p.b.topk_ids[(size_t)t * k + lane] = id;
+                p.b.topk_w[(size_t)t * k + lane] = wj;
+                s_ids[t * k + lane] = id;
+                s_w[t * k + lane] = wj;
+                atomicAdd(&s_hist[id], 1);
+            }
+            __syncwarp();
+        }
+        __syncthreads();
+        // Lists, one thread per route (at most 8 x 16): each counts the routes that come before it --
+        // hot routes by (expert, token), cold routes by (token, expert) -- and the active experts below
+        // its own; the first route of an expert (lowest token) writes the active entry.
+        __shared__ unsigned char s_first[kDecodeMaxTokens * kMaxTopK];
+        const int nr = M * k, r = threadIdx.x;
+        const bool mine = r < nr;
+        const int e = mine ? s_ids[r] : 0, t = mine ? r / k : 0;
+        const bool hot = mine && s_e2s[e] >= 0;
+        if (mine) {
+            bool first = true;
+            for (int q = 0; q < nr; ++q)
+                if (s_ids[q] == e && q / k < t) first = false;
+            s_first[r] = hot && first;
+        }
+        __syncthreads();
+        if (mine) {
+            int pos = 0, aidx = 0;
+            for (int q = 0; q < nr; ++q) {
+                const int e2 = s_ids[q], t2 = q / k;
+                const bool hot2 = s_e2s[e2] >= 0;
+                if (hot) {
+                    pos += hot2 && (e2 < e || (e2 == e && t2 < t));
+                    aidx += s_first[q] && e2 < e;
+                } else {
+                    pos += !hot2 && (t2 < t || (t2 == t && e2 < e));
+                }
+            }
+            if (hot) {
+                p.b.hot_expert[pos] = e;
+                p.b.hot_token[pos] = t;
+                p.b.hot_w[pos] = s_w[r];
+                if (s_first[r]) {
+                    p.b.act_expert[aidx] = e;
+                    p.b.act_slot[aidx] = s_e2s[e];
+                    p.b.act_off[aidx] = pos;
+                    p.b.act_cnt[aidx] = s_hist[e];
+                }
+            } else {
+                p.b.cold_token[pos] = t;
+                p.b.cold_expert[pos] = e;
+                p.b.cold_w[pos] = s_w[r];
+            }
+        }
+        for (int x = threadIdx.x; x < E; x += kThreads) p.b.hist[x] = s_hist[x];
+        const int n_hot = __syncthreads_count(hot);
+        const int n_cold = __syncthreads_count(mine && !hot);
+        const int n_act = __syncthreads_count(mine && s_first[r]);
+        if (threadIdx.x == 0) {
+            p.b.counts[0] = n_hot;
+            p.b.counts[1] = n_cold;
+            p.b.counts[2] = n_act;
+            p.b.counts[3] = M;
+        }
+        return;
+    }
+
     for (int t = warp; t < M; t += kWarps) {
         if (!rows_by_block) {
             for (int e = lane; e < E; e += 32) {
