@@ -9,6 +9,7 @@
 // run in the background without stalling decode).
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdarg>
@@ -17,7 +18,24 @@
 #include <string>
 #include <vector>
 
+#include "moe_host.h"
 #include "moe_internal.h"
+
+namespace {
+
+// out[t, :] += y[t, :] for the first M tokens (bf16 outputs are rounded once more, to nearest even).
+__global__ void add_cold_kernel(void *out, const float *y, int n, int out_f32) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        if (out_f32) {
+            reinterpret_cast<float *>(out)[i] += y[i];
+        } else {
+            __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(out);
+            o[i] = __float2bfloat16_rn(__bfloat162float(o[i]) + y[i]);
+        }
+    }
+}
+
+}  // namespace
 
 namespace {
 
@@ -71,6 +89,11 @@ struct moe_layer {
     // page-locked mirror
     int32_t *m_counts = nullptr, *m_cold_token = nullptr, *m_cold_expert = nullptr, *m_hist = nullptr;
     float *m_cold_w = nullptr;
+    // cold routes on host threads (decode): x mirrored with the route, their sums and the device copy
+    uint16_t *m_x = nullptr;     // [dec_tokens][H] bf16, page-locked
+    float *m_ycold = nullptr;    // [dec_tokens][H] fp32, page-locked
+    float *d_ycold = nullptr;    // [dec_tokens][H] fp32
+    cudaEvent_t ev_cold = nullptr;  // the last copy of m_ycold to the device
     void *pinned_block = nullptr;
 
     cudaStream_t d2h = nullptr, h2d = nullptr;
@@ -132,6 +155,7 @@ void release(moe_layer *L) {
     cudaFree(L->slots);
     cudaFree(L->Wr);
     cudaFree(L->WrT);
+    cudaFree(L->d_ycold);
     cudaFree(L->bias);
     cudaFree(L->e2s_dev);
     cudaFree(L->dev_block);
@@ -141,7 +165,7 @@ void release(moe_layer *L) {
     cudaFree(L->pf_block);
     cudaFree(L->stage_atoms);
     if (L->pinned_block) cudaFreeHost(L->pinned_block);
-    for (auto e : {L->ev_fork, L->ev_route, L->ev_fence})
+    for (auto e : {L->ev_fork, L->ev_route, L->ev_fence, L->ev_cold})
         if (e) cudaEventDestroy(e);
     for (auto e : L->ev_copy) cudaEventDestroy(e);
     for (auto e : L->ev_pool) cudaEventDestroy(e);
@@ -498,8 +522,11 @@ int moe_layer_create(const moe_layer_desc *desc, const float *router_w_dev, cons
         }
     }
 
-    // page-locked mirror: counts[4], hist[E], cold token/expert/w [max_hot]
-    const size_t psz = align_up(16, 64) + align_up((size_t)E * 4, 64) + 3 * align_up(nh * 4, 64);
+    // page-locked mirror: counts[4], hist[E], cold token/expert/w [max_hot], then x and the cold sums of the
+    // decode tokens
+    const int dec = mt < moe::kDecodeMaxTokens ? mt : moe::kDecodeMaxTokens;
+    const size_t psz = align_up(16, 64) + align_up((size_t)E * 4, 64) + 3 * align_up(nh * 4, 64) +
+                       align_up((size_t)dec * H * 2, 64) + align_up((size_t)dec * H * 4, 64);
     CREATE_TRY(cudaHostAlloc(&L->pinned_block, psz, cudaHostAllocDefault));
     memset(L->pinned_block, 0, psz);
     {
@@ -513,10 +540,16 @@ int moe_layer_create(const moe_layer_desc *desc, const float *router_w_dev, cons
         L->m_cold_expert = (int32_t *)p;
         p += align_up(nh * 4, 64);
         L->m_cold_w = (float *)p;
+        p += align_up(nh * 4, 64);
+        L->m_x = (uint16_t *)p;
+        p += align_up((size_t)dec * H * 2, 64);
+        L->m_ycold = (float *)p;
     }
+    CREATE_TRY(cudaMalloc(&L->d_ycold, (size_t)dec * H * 4));
 
     CREATE_TRY(cudaStreamCreateWithFlags(&L->d2h, cudaStreamNonBlocking));
     CREATE_TRY(cudaStreamCreateWithFlags(&L->h2d, cudaStreamNonBlocking));
+    CREATE_TRY(cudaEventCreateWithFlags(&L->ev_cold, cudaEventDisableTiming));
     for (cudaEvent_t *e : {&L->ev_fork, &L->ev_route, &L->ev_fence})
         CREATE_TRY(cudaEventCreateWithFlags(e, cudaEventDisableTiming));
     L->ev_copy.resize(d.max_refills_per_step);
@@ -596,6 +629,8 @@ int moe_route(moe_layer *L, const void *x_dev, int32_t M, void *stream, moe_rout
     CUDA_TRY(cudaMemcpyAsync(L->m_cold_token, L->rb.cold_token, n * 4, cudaMemcpyDeviceToHost, L->d2h));
     CUDA_TRY(cudaMemcpyAsync(L->m_cold_expert, L->rb.cold_expert, n * 4, cudaMemcpyDeviceToHost, L->d2h));
     CUDA_TRY(cudaMemcpyAsync(L->m_cold_w, L->rb.cold_w, n * 4, cudaMemcpyDeviceToHost, L->d2h));
+    if (M <= moe::kDecodeMaxTokens)  // the host computes cold routes from this copy (moe_forward_cold)
+        CUDA_TRY(cudaMemcpyAsync(L->m_x, x_dev, (size_t)M * L->d.hidden * 2, cudaMemcpyDeviceToHost, L->d2h));
     CUDA_TRY(cudaEventRecord(L->ev_route, L->d2h));
 
     L->routed_x = x_dev;
@@ -745,6 +780,47 @@ int moe_forward_slots(moe_layer *L, const void *x_dev, void *out_dev, int32_t M,
         CUDA_TRY(moe::launch_prefill(P, st));
     }
     CUDA_TRY(cudaStreamWaitEvent(st, L->ev_route, 0));  // join the mirror copies
+    return MOE_OK;
+}
+
+int moe_forward_cold(moe_layer *L, const void *x_dev, void *out_dev, int32_t M, int32_t nthreads, void *stream) {
+    g_err.clear();
+    if (!L || !x_dev || !out_dev) return fail(MOE_EINVAL, "layer, x_dev and out_dev are required");
+    if (nthreads < 0) return fail(MOE_EINVAL, "nthreads must be >= 0 (0: every host core)");
+    if (L->routed_M == 0 || L->routed_x != x_dev || L->routed_M != M)
+        return fail(MOE_ESTATE, "moe_forward_cold needs the x_dev and M of the last moe_route");
+    if (M > moe::kDecodeMaxTokens) return MOE_OK;  // prefill: every route is hot
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    CUDA_TRY(cudaEventSynchronize(L->ev_cold));   // the previous sums have left m_ycold
+    CUDA_TRY(cudaEventSynchronize(L->ev_route));  // counts, cold triples and x are on the host
+    const int n_cold = L->m_counts[1];
+    if (n_cold == 0) return MOE_OK;
+    moe::host::ColdJob job{};
+    job.L = moe::host::record_layout(L->d.hidden, L->d.inter);
+    job.bank = L->host_bank;
+    job.x = L->m_x;
+    job.M = M;
+    job.n = n_cold;
+    job.token = L->m_cold_token;
+    job.expert = L->m_cold_expert;
+    job.w = L->m_cold_w;
+    job.y = L->m_ycold;
+    moe::host::run_cold(job, nthreads);
+    const size_t n = (size_t)M * L->d.hidden;
+    CUDA_TRY(cudaMemcpyAsync(L->d_ycold, L->m_ycold, n * 4, cudaMemcpyHostToDevice, st));
+    CUDA_TRY(cudaEventRecord(L->ev_cold, st));
+    add_cold_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(out_dev, L->d_ycold, (int)n,
+                                                                 L->d.out_dtype == MOE_OUT_F32);
+    CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+}
+
+int moe_host_expert_ffn(const uint8_t *record, int32_t H, int32_t I, const uint16_t *x_host, float *y_host) {
+    g_err.clear();
+    if (!record || !x_host || !y_host) return fail(MOE_EINVAL, "record, x_host and y_host are required");
+    if (H <= 0 || H % 64 || I <= 0 || I % 64) return fail(MOE_EINVAL, "H and I must be positive multiples of 64");
+    std::vector<float> h((size_t)I);
+    moe::host::expert_ffn(moe::host::record_layout(H, I), record, x_host, h.data(), y_host);
     return MOE_OK;
 }
 

@@ -21,7 +21,8 @@ EXPORTED = [
     "moe_layer_create", "moe_route", "moe_forward_slots", "moe_cache_update", "moe_destroy", "moe_last_error",
     "moe_layer_set_bias", "moe_layer_attach_staging", "moe_layer_stage_all", "moe_debug_get_map",
     "moe_debug_slot_ptr", "moe_debug_inject_fault", "moe_debug_stats", "moe_debug_profile",
-    "moe_debug_profile_read", "moe_debug_check_error", "moe_policy_step", "moe_route_noalloc",
+    "moe_debug_profile_read", "moe_debug_check_error", "moe_policy_step", "moe_route_noalloc", "moe_forward_cold",
+    "moe_host_expert_ffn",
 ]
 
 
@@ -69,6 +70,8 @@ def lib():
         L.moe_layer_create.argtypes = [ctypes.POINTER(LayerDesc), p, p, p, p, p, ctypes.POINTER(p)]
         L.moe_route.argtypes = [p, p, i32, p, ctypes.POINTER(RouteResult)]
         L.moe_forward_slots.argtypes = [p, p, p, i32, p]
+        L.moe_forward_cold.argtypes = [p, p, p, i32, i32, p]
+        L.moe_host_expert_ffn.argtypes = [p, i32, i32, p, p]
         L.moe_cache_update.argtypes = [p, p, ctypes.POINTER(i32)]
         L.moe_destroy.argtypes = [p]
         L.moe_last_error.argtypes = []
@@ -138,6 +141,10 @@ class Layer:
 
     def forward_slots(self, x, out, M, stream=None):
         check(lib().moe_forward_slots(self.h, _P(x.data_ptr()), _P(out.data_ptr()), M, stream_ptr(stream)))
+
+    def forward_cold(self, x, out, M, nthreads=0, stream=None):
+        """Cold routes of the last route on host threads, added to ``out`` (blocks the calling thread)."""
+        check(lib().moe_forward_cold(self.h, _P(x.data_ptr()), _P(out.data_ptr()), M, nthreads, stream_ptr(stream)))
 
     def cache_update(self, stream=None):
         n = ctypes.c_int32(0)
@@ -227,3 +234,14 @@ def policy_step(score, last, e2s, s2e, hist, step, decay, R, in_flight=None):
     if n < 0:
         raise MoeError(MOE_EINVAL, "moe_policy_step rejected its arguments")
     return [(int(pe[i]), int(ps[i]), int(pv[i])) for i in range(n)]
+
+
+def host_expert_ffn(record, H, I, x_bits):
+    """The library's host expert FFN (the one its cold-route workers run) on one record: fp32 [H]."""
+    import numpy as np
+
+    rec = np.ascontiguousarray(record, dtype=np.uint8)
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    y = np.empty(H, dtype=np.float32)
+    check(lib().moe_host_expert_ffn(rec.ctypes.data_as(_P), H, I, x.ctypes.data_as(_P), y.ctypes.data_as(_P)))
+    return y

@@ -163,6 +163,38 @@ int moe_route(moe_layer *layer, const void *x_dev, int32_t M, void *stream, moe_
  * Asynchronous, capturable.  Errors: MOE_EINVAL, MOE_ESTATE, MOE_ECUDA. */
 int moe_forward_slots(moe_layer *layer, const void *x_dev, void *out_dev, int32_t M, void *stream);
 
+/* Computes the cold routes of the last moe_route on host threads and adds them
+ * to out_dev (onnxruntime PR #33976 "Key Changes" and NInfer-Offload v0.4.0:
+ * routes to experts not on the GPU are computed by CPU workers while the GPU
+ * computes the resident ones).  Call it after moe_forward_slots on the same
+ * stream.
+ *  x_dev, M   those of the last moe_route (MOE_ESTATE otherwise); M > 8 is
+ *             prefill, where every route is hot: nothing to do
+ *  out_dev    the output moe_forward_slots wrote, [M, H] out_dtype
+ *  nthreads   host threads to use, the calling thread included; 0 = every
+ *             hardware thread
+ * The calling thread blocks: it waits for the route's page-locked mirror
+ * (counts, cold triples and x, copied by moe_route), then computes
+ *   y[t] = sum over t's cold routes, ascending expert, of w * FFN_e(x_t)
+ * from the page-locked host bank, in fp32 with h not rounded, on the
+ * library's worker pool.  Every sum has a fixed order, so y does not depend
+ * on the thread count.  Meanwhile the GPU works on the hot routes.
+ * Then, asynchronously on `stream`, y is copied to the device and added to
+ * out_dev.  Tokens with no cold route are unchanged.  With bf16 outputs the
+ * sum is rounded once more; the fp32 output mode keeps hot + cold exact in
+ * fp32.
+ * Errors: MOE_EINVAL, MOE_ESTATE, MOE_ECUDA. */
+int moe_forward_cold(moe_layer *layer, const void *x_dev, void *out_dev, int32_t M, int32_t nthreads,
+                     void *stream);
+
+/* The expert FFN used by moe_forward_cold, on one expert record (layout as
+ * in moe_layer_create's host bank), on the calling thread:
+ *   y = Wd (SiLU(Wg x) * (Wu x)), fp32, h not rounded.
+ *  record  host, expert_bytes(H, I) bytes
+ *  x_host  bf16 [H] host;  y_host fp32 [H] host
+ * No GPU is involved.  Errors: MOE_EINVAL. */
+int moe_host_expert_ffn(const uint8_t *record, int32_t H, int32_t I, const uint16_t *x_host, float *y_host);
+
 /* Host-side slot-cache step after a moe_route (waits for its `done` event).
  * Scores every expert (score = decay * score + routes this step), picks at
  * most R (candidate, victim) pairs, copies each candidate from the host bank
