@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=None, help="fewer layers (debug only; not a valid result)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-layers", type=int, default=1, help="layers per oracle step (reference arm sample)")
+    ap.add_argument("--cold-on-host", action="store_true",
+                    help="decode with the cold routes computed on the host cores (moe_forward_cold) as well")
     return ap.parse_args()
 
 
@@ -484,6 +486,73 @@ def cpu_prefill_baseline(w, n_tokens=4):
                       f"{t:.1f} s), time scaled to the {w.layers}-layer stack"}
 
 
+COLD_METRIC = "MoE-layer decode tokens/s (M=1), cold routes computed on the host cores"
+
+
+def run_cold_host(args):
+    """Decode where every route is computed: hot routes on the GPU, cold ones on the host cores meanwhile
+    (route, forward_slots, forward_cold per layer; the host thread blocks in forward_cold)."""
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    from expert_offload_moe_gb300 import build as moe_build
+    from expert_offload_moe_gb300 import moe, stack, synth
+
+    moe_build.build()
+    moe.lib()
+    w = synth.WORKLOADS[args.workload]
+    M = w.tokens[0]
+    n_inputs = 16
+    st = stack.DecodeStack(w, M=M, n_layers=args.layers, seed=rank, n_inputs=n_inputs, out_f32=True)
+    L = st.L
+    stream = torch.cuda.current_stream()
+    n_cold = []
+
+    def step(i, record=False):
+        st.load_inputs(i)
+        for l, lay in enumerate(st.layers):
+            res = lay.route(st.x_cur[l], M)
+            lay.forward_slots(st.x_cur[l], st.out[l], M)
+            lay.forward_cold(st.x_cur[l], st.out[l], M)
+            if record:
+                n_cold.append(int(stack.host_counts(res)[1]))
+
+    for i in range(args.warmup):
+        step(i, record=i == 0)
+    torch.cuda.synchronize()
+    clk = Clocks(local)
+    clk.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = clk.stop()
+    t_ms = e0.elapsed_time(e1)
+    value = args.steps * M / (t_ms / 1e3)
+    cold_flop_step = float(np.mean(n_cold)) * 2 * 3 * w.hidden * w.inter * L
+    line = {
+        "metric": COLD_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "mxfp4*e4m3->f32 (GPU), mxfp4*bf16->f32 (host)", "data": "synthetic",
+        "config": {"workload": w.name, "layers": L, "hidden": w.hidden, "inter": w.inter, "experts": w.experts,
+                   "top_k": w.top_k, "slots": w.slots, "tokens_per_step": M, "host_threads": os.cpu_count(),
+                   "mean_cold_routes_per_layer": float(np.mean(n_cold)),
+                   "host_gflops": cold_flop_step / (t_ms / args.steps * 1e-3) / 1e9,
+                   "timing": "eager launches; the host thread computes each layer's cold routes between them"},
+        "roofline": None,
+        "clocks": clocks,
+        "gpu_launches": int(args.steps * L * 4),
+        "e2e": None,
+    }
+    st.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     prefill = synth_workload(args.workload).prefill_tokens > 0
@@ -491,6 +560,8 @@ def main():
         run_reference(args, prefill)
     elif prefill:
         run_prefill(args)
+    elif args.cold_on_host:
+        run_cold_host(args)
     else:
         run_ours(args)
 
