@@ -35,6 +35,53 @@ __global__ void add_cold_kernel(void *out, const float *y, int n, int out_f32) {
     }
 }
 
+// The cold routes of a decode step (ordered by (token, expert), at most 128) grouped by expert for the
+// CUDA-core FFN kernels: routes ordered by (expert, token), and per expert its first route and count.
+__global__ void __launch_bounds__(128) cold_lists_kernel(const int32_t *counts, const int32_t *ctok,
+                                                         const int32_t *cexp, const float *cw, int32_t *act_expert,
+                                                         int32_t *act_off, int32_t *act_cnt, int32_t *tok, float *w,
+                                                         int32_t *c_counts) {
+    __shared__ int s_e[128], s_t[128];
+    __shared__ unsigned char s_first[128];
+    const int n = counts[1], r = threadIdx.x;
+    const bool mine = r < n;
+    const int e = mine ? cexp[r] : 0, t = mine ? ctok[r] : 0;
+    if (mine) {
+        s_e[r] = e;
+        s_t[r] = t;
+    }
+    __syncthreads();
+    if (mine) {
+        bool first = true;
+        for (int q = 0; q < n; ++q)
+            if (s_e[q] == e && s_t[q] < t) first = false;
+        s_first[r] = first;
+    }
+    __syncthreads();
+    if (mine) {
+        int pos = 0, aidx = 0, cnt = 0;
+        for (int q = 0; q < n; ++q) {
+            pos += s_e[q] < e || (s_e[q] == e && s_t[q] < t);
+            aidx += s_first[q] && s_e[q] < e;
+            cnt += s_e[q] == e;
+        }
+        tok[pos] = t;
+        w[pos] = cw[r];
+        if (s_first[r]) {
+            act_expert[aidx] = e;
+            act_off[aidx] = pos;
+            act_cnt[aidx] = cnt;
+        }
+    }
+    const int n_act = __syncthreads_count(mine && s_first[r]);
+    if (r == 0) {
+        c_counts[0] = n;
+        c_counts[1] = 0;
+        c_counts[2] = n_act;
+        c_counts[3] = 0;
+    }
+}
+
 }  // namespace
 
 namespace {
@@ -84,6 +131,12 @@ struct moe_layer {
 
     moe::RouteBuffers rb{};
     float *h = nullptr;  // [max_hot][I]
+    // cold routes on the GPU from the page-locked bank (moe_forward_cold_gpu)
+    const uint8_t *host_bank_dev = nullptr;  // the bank's device address, nullptr if the GPU cannot reach it
+    void *cold_block = nullptr;              // lists of the cold routes grouped by expert, and their h
+    int32_t *c_act_expert = nullptr, *c_act_off = nullptr, *c_act_cnt = nullptr, *c_token = nullptr,
+            *c_counts = nullptr;
+    float *c_w = nullptr, *c_h = nullptr;
     void *dev_block = nullptr;
 
     // page-locked mirror
@@ -160,6 +213,7 @@ void release(moe_layer *L) {
     cudaFree(L->e2s_dev);
     cudaFree(L->dev_block);
     cudaFree(L->h);
+    cudaFree(L->cold_block);
     cudaFree(L->tc_block);
     cudaFree(L->atoms);
     cudaFree(L->pf_block);
@@ -484,6 +538,26 @@ int moe_layer_create(const moe_layer_desc *desc, const float *router_w_dev, cons
     CREATE_TRY(cudaMalloc(&L->bias, (size_t)E * sizeof(float)));
     CREATE_TRY(cudaMalloc(&L->e2s_dev, (size_t)E * sizeof(int32_t)));
     CREATE_TRY(cudaMalloc(&L->h, (size_t)L->max_hot * I * sizeof(float)));
+    {  // the cold routes of a decode step, grouped by expert for the GPU (at most 8 * k of them)
+        const int dec = (mt < moe::kDecodeMaxTokens ? mt : moe::kDecodeMaxTokens) * k;
+        const size_t l = align_up((size_t)dec * 4, 256);
+        CREATE_TRY(cudaMalloc(&L->cold_block, 6 * l + 256 + align_up((size_t)dec * I * 4, 256)));
+        char *q = static_cast<char *>(L->cold_block);
+        L->c_act_expert = (int32_t *)q;
+        L->c_act_off = (int32_t *)(q + l);
+        L->c_act_cnt = (int32_t *)(q + 2 * l);
+        L->c_token = (int32_t *)(q + 3 * l);
+        L->c_w = (float *)(q + 4 * l);
+        L->c_counts = (int32_t *)(q + 5 * l);
+        L->c_h = (float *)(q + 5 * l + 256);
+    }
+    {  // the device address of the page-locked bank, when the GPU can read it in place
+        void *dp = nullptr;
+        if (cudaHostGetDevicePointer(&dp, const_cast<uint8_t *>(host_bank), 0) == cudaSuccess)
+            L->host_bank_dev = static_cast<const uint8_t *>(dp);
+        else
+            cudaGetLastError();  // not mappable: moe_forward_cold_gpu reports it
+    }
 
     // route scratch in one block
     const size_t nh = (size_t)L->max_hot;
@@ -809,6 +883,41 @@ int moe_forward_cold(moe_layer *L, const void *x_dev, void *out_dev, int32_t M, 
     const size_t n = (size_t)M * L->d.hidden;
     CUDA_TRY(cudaMemcpyAsync(L->d_ycold, L->m_ycold, n * 4, cudaMemcpyHostToDevice, st));
     CUDA_TRY(cudaEventRecord(L->ev_cold, st));
+    add_cold_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(out_dev, L->d_ycold, (int)n,
+                                                                 L->d.out_dtype == MOE_OUT_F32);
+    CUDA_TRY(cudaGetLastError());
+    return MOE_OK;
+}
+
+int moe_forward_cold_gpu(moe_layer *L, const void *x_dev, void *out_dev, int32_t M, void *stream) {
+    g_err.clear();
+    if (!L || !x_dev || !out_dev) return fail(MOE_EINVAL, "layer, x_dev and out_dev are required");
+    if (L->routed_M == 0 || L->routed_x != x_dev || L->routed_M != M)
+        return fail(MOE_ESTATE, "moe_forward_cold_gpu needs the x_dev and M of the last moe_route");
+    if (M > moe::kDecodeMaxTokens) return MOE_OK;  // prefill: every route is hot
+    if (!L->host_bank_dev)
+        return fail(MOE_ESTATE, "the GPU cannot address the host bank in place (cudaHostGetDevicePointer failed)");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cold_lists_kernel<<<1, 128, 0, st>>>(L->rb.counts, L->rb.cold_token, L->rb.cold_expert, L->rb.cold_w,
+                                         L->c_act_expert, L->c_act_off, L->c_act_cnt, L->c_token, L->c_w,
+                                         L->c_counts);
+    CUDA_TRY(cudaGetLastError());
+    moe::DecodeParams p{};
+    p.bank = L->host_bank_dev;  // "slot" = expert id: the bank is indexed by expert
+    p.geo = L->geo;
+    p.x = static_cast<const uint16_t *>(x_dev);
+    p.counts = L->c_counts;
+    p.act_slot = L->c_act_expert;
+    p.act_off = L->c_act_off;
+    p.act_cnt = L->c_act_cnt;
+    p.hot_token = L->c_token;
+    p.hot_w = L->c_w;
+    p.h = L->c_h;
+    p.out = L->d_ycold;
+    p.out_f32 = 1;
+    moe::launch_gateup(p, M, st, L->num_sms);
+    moe::launch_down(p, M, st, L->num_sms);
+    const size_t n = (size_t)M * L->d.hidden;
     add_cold_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(out_dev, L->d_ycold, (int)n,
                                                                  L->d.out_dtype == MOE_OUT_F32);
     CUDA_TRY(cudaGetLastError());

@@ -22,7 +22,7 @@ EXPORTED = [
     "moe_layer_set_bias", "moe_layer_attach_staging", "moe_layer_stage_all", "moe_debug_get_map",
     "moe_debug_slot_ptr", "moe_debug_inject_fault", "moe_debug_stats", "moe_debug_profile",
     "moe_debug_profile_read", "moe_debug_check_error", "moe_policy_step", "moe_route_noalloc", "moe_forward_cold",
-    "moe_host_expert_ffn",
+    "moe_forward_cold_gpu", "moe_host_expert_ffn",
 ]
 
 
@@ -71,6 +71,7 @@ def lib():
         L.moe_route.argtypes = [p, p, i32, p, ctypes.POINTER(RouteResult)]
         L.moe_forward_slots.argtypes = [p, p, p, i32, p]
         L.moe_forward_cold.argtypes = [p, p, p, i32, i32, p]
+        L.moe_forward_cold_gpu.argtypes = [p, p, p, i32, p]
         L.moe_host_expert_ffn.argtypes = [p, i32, i32, p, p]
         L.moe_cache_update.argtypes = [p, p, ctypes.POINTER(i32)]
         L.moe_destroy.argtypes = [p]
@@ -145,6 +146,10 @@ class Layer:
     def forward_cold(self, x, out, M, nthreads=0, stream=None):
         """Cold routes of the last route on host threads, added to ``out`` (blocks the calling thread)."""
         check(lib().moe_forward_cold(self.h, _P(x.data_ptr()), _P(out.data_ptr()), M, nthreads, stream_ptr(stream)))
+
+    def forward_cold_gpu(self, x, out, M, stream=None):
+        """Cold routes of the last route on the GPU, reading the host bank in place, added to ``out``."""
+        check(lib().moe_forward_cold_gpu(self.h, _P(x.data_ptr()), _P(out.data_ptr()), M, stream_ptr(stream)))
 
     def cache_update(self, stream=None):
         n = ctypes.c_int32(0)

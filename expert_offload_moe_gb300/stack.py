@@ -55,8 +55,10 @@ class DecodeStack:
     """L layers of one workload with M-token decode steps over resident inputs."""
 
     def __init__(self, w: synth.Workload, M: int = 1, n_layers: int | None = None, seed: int = 0,
-                 n_inputs: int = 1, out_f32: bool = False, max_tokens: int = 8):
+                 n_inputs: int = 1, out_f32: bool = False, max_tokens: int = 8, cold_on_gpu: bool = False):
+        """cold_on_gpu: each layer also computes its cold routes on the GPU from the host bank in place."""
         self.w, self.M, self.seed = w, M, seed
+        self.cold_on_gpu = cold_on_gpu
         self.L = w.layers if n_layers is None else n_layers
         self.inputs = [LayerInputs(w, l, seed) for l in range(self.L)]
         self.layers = [li.make_layer(max_tokens=max_tokens, out_f32=out_f32) for li in self.inputs]
@@ -76,6 +78,8 @@ class DecodeStack:
         for l, layer in enumerate(self.layers):
             layer.route(self.x_cur[l], self.M, stream)
             layer.forward_slots(self.x_cur[l], self.out[l], self.M, stream)
+            if self.cold_on_gpu:
+                layer.forward_cold_gpu(self.x_cur[l], self.out[l], self.M, stream)
 
     def load_inputs(self, i: int):
         self.x_cur.copy_(self.x_all[i % self.x_all.shape[0]], non_blocking=True)

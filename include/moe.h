@@ -187,6 +187,23 @@ int moe_forward_slots(moe_layer *layer, const void *x_dev, void *out_dev, int32_
 int moe_forward_cold(moe_layer *layer, const void *x_dev, void *out_dev, int32_t M, int32_t nthreads,
                      void *stream);
 
+/* The cold routes of the last moe_route computed on the GPU, reading the
+ * expert bytes in place from the page-locked host bank through its device
+ * address (NVLink-C2C on a Grace host, PCIe elsewhere), added to out_dev.
+ * xinfer docs "How it works" reads missed experts from device-mapped host
+ * memory; here the CUDA-core FFN kernels stream them directly, one pass per
+ * step, without refilling a slot.  Call it after moe_forward_slots on the
+ * same stream.
+ *  x_dev, M   those of the last moe_route (MOE_ESTATE otherwise); M > 8 is
+ *             prefill, where every route is hot: nothing to do
+ *  out_dev    the output moe_forward_slots wrote, [M, H] out_dtype
+ * Fully asynchronous and capturable: the cold lists never leave the device.
+ * The cold sum is formed in fp32 in ascending expert order per token and
+ * added to out_dev (bf16 outputs are rounded once more, as in
+ * moe_forward_cold).  MOE_ESTATE if the GPU cannot address the bank.
+ * Errors: MOE_EINVAL, MOE_ESTATE, MOE_ECUDA. */
+int moe_forward_cold_gpu(moe_layer *layer, const void *x_dev, void *out_dev, int32_t M, void *stream);
+
 /* The expert FFN used by moe_forward_cold, on one expert record (layout as
  * in moe_layer_create's host bank), on the calling thread:
  *   y = Wd (SiLU(Wg x) * (Wu x)), fp32, h not rounded.

@@ -27,7 +27,7 @@ def built():
     moe.lib()
 
 
-def hybrid(li, x_bits, out_f32=True, nthreads=0, lay=None):
+def hybrid(li, x_bits, out_f32=True, nthreads=0, lay=None, on_gpu=False):
     w = li.w
     M = x_bits.shape[0]
     own = lay is None
@@ -37,7 +37,10 @@ def hybrid(li, x_bits, out_f32=True, nthreads=0, lay=None):
         out = torch.empty((M, w.hidden), dtype=torch.float32 if out_f32 else torch.bfloat16, device="cuda")
         res = lay.route(x, M)
         lay.forward_slots(x, out, M)
-        lay.forward_cold(x, out, M, nthreads=nthreads)
+        if on_gpu:
+            lay.forward_cold_gpu(x, out, M)
+        else:
+            lay.forward_cold(x, out, M, nthreads=nthreads)
         torch.cuda.synchronize()
         n_cold = int(stack.host_counts(res)[1])
         got = out.float().cpu().numpy()
@@ -53,33 +56,36 @@ def all_resident(li, x_bits):
                             w.top_k, w.hidden, w.inter)
 
 
+@pytest.mark.parametrize("on_gpu", [False, True])
 @pytest.mark.parametrize("M", [1, 4, 8])
-def test_tiny_half_resident(M):
+def test_tiny_half_resident(M, on_gpu):
     e2s = np.full(TINY.experts, -1, dtype=np.int32)
     e2s[::2] = np.arange(TINY.experts // 2)  # even experts in slots, odd ones cold
     li = stack.LayerInputs(TINY, 0, e2s=e2s)
     x_bits = synth.activations(0, 0, 60 + M, M, TINY.hidden)
-    got, n_cold = hybrid(li, x_bits)
+    got, n_cold = hybrid(li, x_bits, on_gpu=on_gpu)
     o = all_resident(li, x_bits)
     assert n_cold > 0
     compare_values(got, o["out_f32"], True, exclude=np.where(near_tie_tokens(o["logits"], TINY.top_k))[0])
 
 
-def test_tiny_all_cold():
+@pytest.mark.parametrize("on_gpu", [False, True])
+def test_tiny_all_cold(on_gpu):
     li = stack.LayerInputs(TINY, 0, e2s=np.full(TINY.experts, -1, dtype=np.int32))
     x_bits = synth.activations(0, 0, 70, 4, TINY.hidden)
-    got, n_cold = hybrid(li, x_bits)
+    got, n_cold = hybrid(li, x_bits, on_gpu=on_gpu)
     assert n_cold == 4 * TINY.top_k
     o = all_resident(li, x_bits)
     compare_values(got, o["out_f32"], True, exclude=np.where(near_tie_tokens(o["logits"], TINY.top_k))[0])
 
 
-def test_e512_half_resident_m1():
+@pytest.mark.parametrize("on_gpu", [False, True])
+def test_e512_half_resident_m1(on_gpu):
     """The E=512 shape with its 256 slots by popularity rank: about a quarter of the routes are cold."""
     li = stack.LayerInputs(E512, 0)
     for s in range(3):
         x_bits = synth.activations(0, 0, 80 + s, 1, E512.hidden)
-        got, n_cold = hybrid(li, x_bits)
+        got, n_cold = hybrid(li, x_bits, on_gpu=on_gpu)
         o = all_resident(li, x_bits)
         compare_values(got, o["out_f32"], True, exclude=np.where(near_tie_tokens(o["logits"], E512.top_k))[0])
 
@@ -121,5 +127,48 @@ def test_cold_needs_the_last_route():
         out = torch.zeros((2, TINY.hidden), dtype=torch.float32, device="cuda")
         with pytest.raises(moe.MoeError):
             lay.forward_cold(x, out, 2)
+    finally:
+        lay.close()
+
+
+def test_gpu_cold_in_a_graph_matches_eager():
+    """route + forward_slots + forward_cold_gpu captured in a CUDA graph and replayed on new inputs gives
+    the eager result bit for bit (no host step in the GPU cold path)."""
+    e2s = np.full(TINY.experts, -1, dtype=np.int32)
+    e2s[::3] = np.arange(len(e2s[::3]))
+    li = stack.LayerInputs(TINY, 0, e2s=e2s)
+    lay = li.make_layer(max_tokens=8, out_f32=True)
+    try:
+        M = 4
+        x = torch.empty((M, TINY.hidden), dtype=torch.bfloat16, device="cuda")
+        out = torch.empty((M, TINY.hidden), dtype=torch.float32, device="cuda")
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+
+        def body():
+            lay.route(x, M, s)
+            lay.forward_slots(x, out, M, s)
+            lay.forward_cold_gpu(x, out, M, s)
+
+        x.copy_(stack.bf16_tensor(synth.activations(0, 0, 120, M, TINY.hidden)))
+        with torch.cuda.stream(s):
+            body()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            body()
+        for step in range(3):
+            xb = synth.activations(0, 0, 130 + step, M, TINY.hidden)
+            x.copy_(stack.bf16_tensor(xb))
+            torch.cuda.synchronize()
+            g.replay()
+            torch.cuda.synchronize()
+            replayed = out.cpu().numpy().copy()
+            with torch.cuda.stream(s):
+                body()
+            torch.cuda.synchronize()
+            assert np.array_equal(replayed, out.cpu().numpy())
+            o = all_resident(li, xb)
+            compare_values(replayed, o["out_f32"], True, exclude=np.where(near_tie_tokens(o["logits"], TINY.top_k))[0])
     finally:
         lay.close()
