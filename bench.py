@@ -14,6 +14,12 @@ clocks sampled during the timed region, and the kernel launch count.
 
 `--impl reference` times the CPU oracle instead (the slow, plain reference),
 on a bounded sample of the same workload.
+
+Other lines (not the default): `--workload gptoss20b_prefill2048_s16_lfu_drift`
+times the 2048-token prefill of every layer (tensor-core roofline of the
+gate/up GEMM); `--cold-on-gpu` / `--cold-on-host` time decode with the cold
+routes computed as well (on the GPU from the host bank in place, or on the
+host cores).
 """
 from __future__ import annotations
 
