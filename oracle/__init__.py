@@ -70,6 +70,9 @@ def _declare(L):
     L.oracle_moe_layer.restype = None
     L.oracle_cache_step.argtypes = [P, P, P, P, I32, I32, P, ctypes.c_int64, ctypes.c_double, I32, P, P, P, P]
     L.oracle_cache_step.restype = I32
+    L.oracle_cache_step_recency.argtypes = [I32, P, P, P, P, P, I32, I32, P, ctypes.c_int64, ctypes.c_double, I32,
+                                            P, P, P, P]
+    L.oracle_cache_step_recency.restype = I32
     L.oracle_mxfp8_block.argtypes = [P, I32, P]
     L.oracle_mxfp8_block.restype = ctypes.c_uint8
 
@@ -220,10 +223,14 @@ def moe_layer(x_bf16, Wr, bias, experts, e2s, k, H, I):
     return out
 
 
-class CacheReplay:
-    """Step-by-step replay of the slot cache policy for one layer."""
+POLICIES = {"freq": 0, "lru": 1, "fifo": 2}
 
-    def __init__(self, e2s, S, decay=1.0, R=2):
+
+class CacheReplay:
+    """Step-by-step replay of the slot cache policy for one layer.  policy: "freq" (decayed frequency:
+    LFU / LFRU), "lru" or "fifo"."""
+
+    def __init__(self, e2s, S, decay=1.0, R=2, policy="freq"):
         self.e2s = _c(e2s, np.int32).copy()
         self.E = self.e2s.shape[0]
         self.S = S
@@ -235,6 +242,8 @@ class CacheReplay:
         self.last = np.full(self.E, -1, dtype=np.int64)
         self.decay = float(decay)
         self.R = int(R)
+        self.policy = POLICIES[policy]
+        self.loaded = np.full(self.E, -1, dtype=np.int64)
 
     def step(self, hist, step, in_flight=None):
         hist = _c(hist, np.int32)
@@ -242,9 +251,14 @@ class CacheReplay:
         ps = np.zeros_like(pe)
         pv = np.zeros_like(pe)
         fl = None if in_flight is None else _c(in_flight, np.uint8)
-        n = lib().oracle_cache_step(_p(self.score), _p(self.last), _p(self.e2s), _p(self.s2e), self.E,
-                                    self.S, _p(hist), int(step), self.decay, self.R, _p(fl), _p(pe),
-                                    _p(ps), _p(pv))
+        if self.policy == 0:
+            n = lib().oracle_cache_step(_p(self.score), _p(self.last), _p(self.e2s), _p(self.s2e), self.E,
+                                        self.S, _p(hist), int(step), self.decay, self.R, _p(fl), _p(pe),
+                                        _p(ps), _p(pv))
+        else:
+            n = lib().oracle_cache_step_recency(self.policy, _p(self.score), _p(self.last), _p(self.loaded),
+                                                _p(self.e2s), _p(self.s2e), self.E, self.S, _p(hist), int(step),
+                                                self.decay, self.R, _p(fl), _p(pe), _p(ps), _p(pv))
         return [(int(pe[i]), int(ps[i]), int(pv[i])) for i in range(n)]
 
 

@@ -330,6 +330,65 @@ int oracle_cache_step(double *score, int64_t *last, int32_t *e2s, int32_t *s2e, 
     return n;
 }
 
+/* Recency and arrival policies (tinyserve README "How it works" 3 lists lru
+ * and fifo beside frequency-recency; NInfer-Offload v0.4.0: at most R
+ * refills per layer and step).  policy 1 = LRU, 2 = FIFO.
+ *   last[e]   : the last step that routed e (updated first, for both)
+ *   loaded[e] : the step e entered a slot (FIFO; -1 for the initial ones)
+ * Candidates: non-resident experts routed this step, most routes first,
+ * ties to the lower id.  Victims: LRU the resident expert routed longest
+ * ago, FIFO the one loaded earliest, ties to the lower slot.  LRU takes a
+ * pair only while the victim was not routed this step; FIFO always.
+ * Experts in flight are neither.  score keeps the decayed frequency for
+ * reference only.  Returns the number of (expert, slot, victim) pairs. */
+int oracle_cache_step_recency(int policy, double *score, int64_t *last, int64_t *loaded, int32_t *e2s,
+                              int32_t *s2e, int E, int S, const int32_t *hist, int64_t step, double decay,
+                              int R, const uint8_t *in_flight, int32_t *pair_expert, int32_t *pair_slot,
+                              int32_t *pair_victim) {
+    int e, s, p, n = 0;
+    char *used = (char *)calloc((size_t)E, 1);
+    for (e = 0; e < E; ++e) {
+        score[e] = decay * score[e] + (double)hist[e];
+        if (hist[e] > 0) last[e] = step;
+    }
+    for (p = 0; p < R; ++p) {
+        int cand = -1, vic = -1;
+        for (e = 0; e < E; ++e) {
+            if (e2s[e] >= 0 || used[e] || hist[e] <= 0 || (in_flight && in_flight[e])) continue;
+            if (cand < 0 || hist[e] > hist[cand]) cand = e; /* ascending e: ties keep the lower id */
+        }
+        if (cand < 0) break;
+        for (s = 0; s < S; ++s) { /* ascending slot: ties keep the lower slot */
+            int r = s2e[s];
+            int64_t key, best;
+            if (r < 0 || used[r] || (in_flight && in_flight[r])) continue;
+            if (vic < 0) {
+                vic = r;
+                continue;
+            }
+            key = policy == 2 ? loaded[r] : last[r];
+            best = policy == 2 ? loaded[vic] : last[vic];
+            if (key < best) vic = r;
+        }
+        if (vic < 0) break;
+        if (policy == 1 && last[vic] >= step) break; /* LRU never evicts an expert this step used */
+        used[cand] = 1;
+        used[vic] = 1;
+        pair_expert[n] = cand;
+        pair_slot[n] = e2s[vic];
+        pair_victim[n] = vic;
+        ++n;
+    }
+    for (p = 0; p < n; ++p) {
+        e2s[pair_victim[p]] = -1;
+        e2s[pair_expert[p]] = pair_slot[p];
+        s2e[pair_slot[p]] = pair_expert[p];
+        if (loaded) loaded[pair_expert[p]] = step;
+    }
+    free(used);
+    return n;
+}
+
 /* ------------------------------------------------ prefill activation format */
 
 /* E4M3 element (OCP MX v1.0 / OFP8): sign bit 7, exponent bits 6..3 (bias 7),

@@ -357,6 +357,7 @@ def _read_trace(name):
     lines = [l.split() for l in open(os.path.join(GOLDEN, name)) if l.strip() and l[0] != "#"]
     hdr = lines[0]
     E, S, R, decay = int(hdr[1]), int(hdr[3]), int(hdr[5]), float(hdr[7])
+    policy = hdr[9] if len(hdr) > 9 else "freq"
     init = [int(v) for v in lines[1][1:]]
     steps = []
     for l in lines[2:]:
@@ -366,13 +367,14 @@ def _read_trace(name):
         pairs = [tuple(int(q) for q in p.split(":")) for p in l[i_p + 1:i_m]]
         mp = [int(v) for v in l[i_m + 1:]]
         steps.append((st, hist, pairs, mp))
-    return E, S, R, decay, init, steps
+    return E, S, R, decay, init, steps, policy
 
 
-@pytest.mark.parametrize("trace", ["cache_lfu_trace.txt", "cache_lfru_trace.txt"])
+@pytest.mark.parametrize("trace", ["cache_lfu_trace.txt", "cache_lfru_trace.txt", "cache_lru_trace.txt",
+                                   "cache_fifo_trace.txt"])
 def test_cache_policy_hand_worked_trace(oracle_lib, trace):
-    E, S, R, decay, init, steps = _read_trace(trace)
-    rp = oracle_lib.CacheReplay(np.array(init, dtype=np.int32), S, decay=decay, R=R)
+    E, S, R, decay, init, steps, policy = _read_trace(trace)
+    rp = oracle_lib.CacheReplay(np.array(init, dtype=np.int32), S, decay=decay, R=R, policy=policy)
     for st, hist, pairs, mp in steps:
         got = rp.step(np.array(hist, dtype=np.int32), st)
         assert got == pairs, (trace, st)
@@ -390,6 +392,31 @@ def test_cache_policy_never_exceeds_budget_and_keeps_map_injective(oracle_lib):
         res = rp.e2s[rp.e2s >= 0]
         assert len(res) == S and len(set(res.tolist())) == S
         assert all(rp.s2e[rp.e2s[e]] == e for e in range(E) if rp.e2s[e] >= 0)
+
+
+@pytest.mark.parametrize("policy", ["lru", "fifo"])
+def test_recency_policies_keep_budget_and_map(oracle_lib, policy):
+    rng = np.random.default_rng(13)
+    E, S, R = 32, 16, 2
+    rp = oracle_lib.CacheReplay(np.where(np.arange(E) < S, np.arange(E), -1).astype(np.int32), S, R=R,
+                                policy=policy)
+    for st in range(200):
+        hist = np.bincount(rng.choice(E, 4, replace=False), minlength=E).astype(np.int32)
+        pairs = rp.step(hist, st)
+        assert len(pairs) <= R
+        res = rp.e2s[rp.e2s >= 0]
+        assert len(res) == S and len(set(res.tolist())) == S
+        for e, _slot, v in pairs:
+            assert hist[e] > 0  # only experts this step routed come in
+            if policy == "lru":
+                assert hist[v] == 0  # LRU never evicts an expert this step routed
+
+
+def test_lru_with_every_resident_routed_takes_no_pair(oracle_lib):
+    rp = oracle_lib.CacheReplay(np.array([0, 1, -1], dtype=np.int32), 2, R=2, policy="lru")
+    assert rp.step(np.array([1, 1, 1], dtype=np.int32), 0) == []
+    rp = oracle_lib.CacheReplay(np.array([0, 1, -1], dtype=np.int32), 2, R=2, policy="fifo")
+    assert rp.step(np.array([1, 1, 1], dtype=np.int32), 0) == [(2, 0, 0)]
 
 
 def test_cache_in_flight_experts_are_skipped(oracle_lib):
