@@ -158,6 +158,8 @@ struct moe_layer {
     // host policy state
     std::vector<int32_t> e2s, s2e, e2s_visible;
     std::vector<double> score;
+    int policy = MOE_POLICY_FREQ;
+    std::vector<int64_t> loaded;  // FIFO: the step each expert entered its slot
     std::vector<int64_t> last;
     std::vector<uint8_t> in_flight;
     int64_t step = 0;
@@ -509,6 +511,7 @@ int moe_layer_create(const moe_layer_desc *desc, const float *router_w_dev, cons
     L->s2e = s2e;
     L->score.assign(d.num_experts, 0.0);
     L->last.assign(d.num_experts, -1);
+    L->loaded.assign(d.num_experts, -1);
     L->in_flight.assign(d.num_experts, 0);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
@@ -857,6 +860,15 @@ int moe_forward_slots(moe_layer *L, const void *x_dev, void *out_dev, int32_t M,
     return MOE_OK;
 }
 
+int moe_layer_set_policy(moe_layer *L, int32_t policy) {
+    g_err.clear();
+    if (!L) return fail(MOE_EINVAL, "layer is NULL");
+    if (policy != MOE_POLICY_FREQ && policy != MOE_POLICY_LRU && policy != MOE_POLICY_FIFO)
+        return fail(MOE_EINVAL, "unknown policy %d", policy);
+    L->policy = policy;
+    return MOE_OK;
+}
+
 int moe_forward_cold(moe_layer *L, const void *x_dev, void *out_dev, int32_t M, int32_t nthreads, void *stream) {
     g_err.clear();
     if (!L || !x_dev || !out_dev) return fail(MOE_EINVAL, "layer, x_dev and out_dev are required");
@@ -971,10 +983,15 @@ int moe_cache_update(moe_layer *L, void *stream, int32_t *n_refills_out) {
     std::vector<int32_t> pe(R > 0 ? R : 1), ps(pe.size()), pv(pe.size());
     // the decision runs on copies so that an injected fault leaves the state unchanged
     std::vector<double> score = L->score;
-    std::vector<int64_t> last = L->last;
+    std::vector<int64_t> last = L->last, loaded = L->loaded;
     std::vector<int32_t> e2s = L->e2s, s2e = L->s2e;
-    const int n = moe_policy_step(score.data(), last.data(), e2s.data(), s2e.data(), E, S, L->m_hist, L->step,
-                                  (double)L->d.score_decay, R, L->in_flight.data(), pe.data(), ps.data(), pv.data());
+    const int n =
+        L->policy == MOE_POLICY_FREQ
+            ? moe_policy_step(score.data(), last.data(), e2s.data(), s2e.data(), E, S, L->m_hist, L->step,
+                              (double)L->d.score_decay, R, L->in_flight.data(), pe.data(), ps.data(), pv.data())
+            : moe_policy_step_recency(L->policy, score.data(), last.data(), loaded.data(), e2s.data(), s2e.data(), E,
+                                      S, L->m_hist, L->step, (double)L->d.score_decay, R, L->in_flight.data(),
+                                      pe.data(), ps.data(), pv.data());
     if (n < 0) return fail(MOE_EINVAL, "policy rejected its arguments");
     if (n > 0 && L->fault == MOE_FAULT_COPY) {
         L->fault = MOE_FAULT_NONE;
@@ -982,6 +999,7 @@ int moe_cache_update(moe_layer *L, void *stream, int32_t *n_refills_out) {
     }
     L->score.swap(score);
     L->last.swap(last);
+    L->loaded.swap(loaded);
     L->e2s.swap(e2s);
     L->s2e.swap(s2e);
     L->step++;

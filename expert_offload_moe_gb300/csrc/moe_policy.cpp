@@ -11,6 +11,7 @@
 // (ties: least recently routed, then lower slot).  Pair i is taken while the
 // candidate's score is strictly greater than the victim's; at most R pairs.
 #include <cstdint>
+#include <algorithm>
 #include <vector>
 
 #include "../../include/moe.h"
@@ -62,6 +63,56 @@ extern "C" int moe_policy_step(double *score, int64_t *last, int32_t *e2s, int32
         e2s[pair_victim[i]] = -1;
         e2s[pair_expert[i]] = pair_slot[i];
         s2e[pair_slot[i]] = pair_expert[i];
+    }
+    return n;
+}
+
+// Recency and arrival policies (tinyserve README "How it works" 3 lists lru and fifo beside
+// frequency-recency).  policy MOE_POLICY_LRU: the victim is the resident expert routed longest ago, and
+// an expert this step routed is never evicted; MOE_POLICY_FIFO: the victim is the resident expert that
+// entered its slot first, whatever its use.  Candidates are the non-resident experts this step routed,
+// most routes first; ties go to the lower id (candidates) and the lower slot (victims).  score keeps the
+// decayed frequency for reference; loaded[e] (FIFO) is the step e entered a slot, -1 for the initial ones.
+extern "C" int moe_policy_step_recency(int32_t policy, double *score, int64_t *last, int64_t *loaded, int32_t *e2s,
+                                       int32_t *s2e, int32_t E, int32_t S, const int32_t *hist, int64_t step,
+                                       double decay, int32_t R, const uint8_t *in_flight, int32_t *pair_expert,
+                                       int32_t *pair_slot, int32_t *pair_victim) {
+    if ((policy != MOE_POLICY_LRU && policy != MOE_POLICY_FIFO) || !score || !last || !e2s || !s2e || !hist ||
+        E <= 0 || S <= 0 || S > E || R < 0 || (policy == MOE_POLICY_FIFO && !loaded) ||
+        (R > 0 && (!pair_expert || !pair_slot || !pair_victim)))
+        return -1;
+    for (int32_t e = 0; e < E; ++e) {
+        const double decayed = decay * score[e];
+        score[e] = decayed + static_cast<double>(hist[e]);
+        if (hist[e] > 0) last[e] = step;
+    }
+    auto busy = [&](int32_t e) { return in_flight && in_flight[e]; };
+    // candidates in order: routes descending, then id ascending
+    std::vector<int32_t> cand;
+    for (int32_t e = 0; e < E; ++e)
+        if (e2s[e] < 0 && hist[e] > 0 && !busy(e)) cand.push_back(e);
+    std::stable_sort(cand.begin(), cand.end(), [&](int32_t a, int32_t b) { return hist[a] > hist[b]; });
+    // victims in order: key ascending (last use, or load step), then slot ascending
+    std::vector<int32_t> vic;
+    for (int32_t s = 0; s < S; ++s)
+        if (s2e[s] >= 0 && !busy(s2e[s])) vic.push_back(s2e[s]);
+    auto key = [&](int32_t e) { return policy == MOE_POLICY_FIFO ? loaded[e] : last[e]; };
+    std::stable_sort(vic.begin(), vic.end(), [&](int32_t a, int32_t b) { return key(a) < key(b); });
+    int32_t n = 0;
+    const size_t np = std::min(cand.size(), vic.size());
+    for (size_t i = 0; i < np && n < R; ++i) {
+        const int32_t c = cand[i], v = vic[i];
+        if (policy == MOE_POLICY_LRU && last[v] >= step) break;
+        pair_expert[n] = c;
+        pair_slot[n] = e2s[v];
+        pair_victim[n] = v;
+        ++n;
+    }
+    for (int32_t i = 0; i < n; ++i) {
+        e2s[pair_victim[i]] = -1;
+        e2s[pair_expert[i]] = pair_slot[i];
+        s2e[pair_slot[i]] = pair_expert[i];
+        if (loaded) loaded[pair_expert[i]] = step;
     }
     return n;
 }

@@ -16,13 +16,14 @@ MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_ETIMEOUT, MOE_ESTATE = range(6)
 MOE_OUT_BF16, MOE_OUT_F32 = 0, 1
 MOE_VIS_DETERMINISTIC, MOE_VIS_POLLED = 0, 1
 MOE_FAULT_NONE, MOE_FAULT_COPY = 0, 1
+MOE_POLICY_FREQ, MOE_POLICY_LRU, MOE_POLICY_FIFO = 0, 1, 2
 
 EXPORTED = [
     "moe_layer_create", "moe_route", "moe_forward_slots", "moe_cache_update", "moe_destroy", "moe_last_error",
     "moe_layer_set_bias", "moe_layer_attach_staging", "moe_layer_stage_all", "moe_debug_get_map",
     "moe_debug_slot_ptr", "moe_debug_inject_fault", "moe_debug_stats", "moe_debug_profile",
     "moe_debug_profile_read", "moe_debug_check_error", "moe_policy_step", "moe_route_noalloc", "moe_forward_cold",
-    "moe_forward_cold_gpu", "moe_host_expert_ffn",
+    "moe_forward_cold_gpu", "moe_host_expert_ffn", "moe_policy_step_recency", "moe_layer_set_policy",
 ]
 
 
@@ -72,6 +73,9 @@ def lib():
         L.moe_forward_slots.argtypes = [p, p, p, i32, p]
         L.moe_forward_cold.argtypes = [p, p, p, i32, i32, p]
         L.moe_forward_cold_gpu.argtypes = [p, p, p, i32, p]
+        L.moe_policy_step_recency.argtypes = [i32, p, p, p, p, p, i32, i32, p, ctypes.c_int64, ctypes.c_double,
+                                              i32, p, p, p, p]
+        L.moe_layer_set_policy.argtypes = [p, i32]
         L.moe_host_expert_ffn.argtypes = [p, i32, i32, p, p]
         L.moe_cache_update.argtypes = [p, p, ctypes.POINTER(i32)]
         L.moe_destroy.argtypes = [p]
@@ -146,6 +150,10 @@ class Layer:
     def forward_cold(self, x, out, M, nthreads=0, stream=None):
         """Cold routes of the last route on host threads, added to ``out`` (blocks the calling thread)."""
         check(lib().moe_forward_cold(self.h, _P(x.data_ptr()), _P(out.data_ptr()), M, nthreads, stream_ptr(stream)))
+
+    def set_policy(self, policy):
+        """Slot policy for later cache updates: MOE_POLICY_FREQ (default), MOE_POLICY_LRU or MOE_POLICY_FIFO."""
+        check(lib().moe_layer_set_policy(self.h, int(policy)))
 
     def forward_cold_gpu(self, x, out, M, stream=None):
         """Cold routes of the last route on the GPU, reading the host bank in place, added to ``out``."""
@@ -238,6 +246,24 @@ def policy_step(score, last, e2s, s2e, hist, step, decay, R, in_flight=None):
                               pe.ctypes.data_as(_P), ps.ctypes.data_as(_P), pv.ctypes.data_as(_P))
     if n < 0:
         raise MoeError(MOE_EINVAL, "moe_policy_step rejected its arguments")
+    return [(int(pe[i]), int(ps[i]), int(pv[i])) for i in range(n)]
+
+
+def policy_step_recency(policy, score, last, loaded, e2s, s2e, hist, step, decay, R, in_flight=None):
+    """The library's LRU / FIFO slot decision on numpy arrays (updated in place)."""
+    import numpy as np
+
+    E, S = e2s.shape[0], s2e.shape[0]
+    pe, ps, pv = (np.zeros(max(R, 1), dtype=np.int32) for _ in range(3))
+    fl = None if in_flight is None else np.ascontiguousarray(in_flight, dtype=np.uint8)
+    hist = np.ascontiguousarray(hist, dtype=np.int32)
+    n = lib().moe_policy_step_recency(int(policy), score.ctypes.data_as(_P), last.ctypes.data_as(_P),
+                                      None if loaded is None else loaded.ctypes.data_as(_P), e2s.ctypes.data_as(_P),
+                                      s2e.ctypes.data_as(_P), E, S, hist.ctypes.data_as(_P), int(step), float(decay),
+                                      int(R), None if fl is None else fl.ctypes.data_as(_P), pe.ctypes.data_as(_P),
+                                      ps.ctypes.data_as(_P), pv.ctypes.data_as(_P))
+    if n < 0:
+        raise MoeError(MOE_EINVAL, "moe_policy_step_recency rejected its arguments")
     return [(int(pe[i]), int(ps[i]), int(pv[i])) for i in range(n)]
 
 

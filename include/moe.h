@@ -80,6 +80,17 @@ enum { MOE_OUT_BF16 = 0, MOE_OUT_F32 = 1 };
  *                 timing (the NInfer-Offload v0.4.0 behaviour). */
 enum { MOE_VIS_DETERMINISTIC = 0, MOE_VIS_POLLED = 1 };
 
+/* Slot policies (tinyserve README "How it works" 3 lists lfu, lru and fifo
+ * among its eviction policies, with frequency-recency as its default):
+ *  MOE_POLICY_FREQ  decayed route counts, score_decay = 1 LFU, < 1 LFRU (the
+ *                   default; moe_policy_step)
+ *  MOE_POLICY_LRU   evict the resident expert routed longest ago, never one
+ *                   this step routed
+ *  MOE_POLICY_FIFO  evict the resident expert that entered its slot first
+ * In every policy the candidates for a slot are non-resident experts,
+ * at most max_refills_per_step per step. */
+enum { MOE_POLICY_FREQ = 0, MOE_POLICY_LRU = 1, MOE_POLICY_FIFO = 2 };
+
 typedef struct moe_layer moe_layer;
 
 typedef struct {
@@ -339,6 +350,24 @@ int moe_debug_profile_read(moe_layer *layer, double out[4]);
 int moe_policy_step(double *score, int64_t *last, int32_t *e2s, int32_t *s2e, int32_t E, int32_t S,
                     const int32_t *hist, int64_t step, double decay, int32_t R, const uint8_t *in_flight,
                     int32_t *pair_expert, int32_t *pair_slot, int32_t *pair_victim);
+
+/* The same for MOE_POLICY_LRU and MOE_POLICY_FIFO.  Candidates: the
+ * non-resident experts this step routed, most routes first (ties: lower id).
+ * Victims: LRU the resident expert with the oldest last[e] (the last step
+ * that routed it), taken only while it was not routed this step; FIFO the
+ * one with the oldest loaded[e] (the step it entered a slot, -1 for experts
+ * placed at creation), taken whatever its use; ties: lower slot.  Experts in
+ * flight are neither.  last[] (and for FIFO loaded[], required) are updated
+ * in place; score[] keeps the decayed frequency for reference.  Returns the
+ * number of pairs, or -1 on bad arguments. */
+int moe_policy_step_recency(int32_t policy, double *score, int64_t *last, int64_t *loaded, int32_t *e2s,
+                            int32_t *s2e, int32_t E, int32_t S, const int32_t *hist, int64_t step, double decay,
+                            int32_t R, const uint8_t *in_flight, int32_t *pair_expert, int32_t *pair_slot,
+                            int32_t *pair_victim);
+
+/* Selects the slot policy of a layer (MOE_POLICY_*, default MOE_POLICY_FREQ)
+ * for its later moe_cache_update calls.  Errors: MOE_EINVAL. */
+int moe_layer_set_policy(moe_layer *layer, int32_t policy);
 
 #ifdef __cplusplus
 }

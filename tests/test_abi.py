@@ -113,3 +113,55 @@ def test_policy_rejects_bad_arguments(lib):
     with pytest.raises(moe.MoeError):
         moe.policy_step(np.zeros(4), np.zeros(4, dtype=np.int64), np.zeros(4, dtype=np.int32),
                         np.zeros(8, dtype=np.int32), np.zeros(4, dtype=np.int32), 0, 1.0, 1)
+
+
+@pytest.mark.parametrize("policy,R,E,S", [("lru", 2, 32, 16), ("fifo", 2, 32, 16), ("lru", 1, 16, 4),
+                                          ("fifo", 4, 64, 48)])
+def test_library_recency_policies_match_oracle_replay(lib, oracle_lib, policy, R, E, S):
+    rng = np.random.default_rng(len(policy) * 7 + R)
+    e2s0 = np.full(E, -1, dtype=np.int32)
+    e2s0[rng.choice(E, S, replace=False)] = rng.permutation(S)
+    rp = oracle_lib.CacheReplay(e2s0, S, R=R, policy=policy)
+    code = {"lru": moe.MOE_POLICY_LRU, "fifo": moe.MOE_POLICY_FIFO}[policy]
+    score, last, loaded = np.zeros(E), np.full(E, -1, dtype=np.int64), np.full(E, -1, dtype=np.int64)
+    e2s = e2s0.copy()
+    s2e = np.full(S, -1, dtype=np.int32)
+    s2e[e2s[e2s >= 0]] = np.nonzero(e2s >= 0)[0]
+    n_pairs = 0
+    for st, hist in _random_trace(rng, E, 4, 300, drift=True):
+        fl = (rng.random(E) < 0.1).astype(np.uint8)
+        a = moe.policy_step_recency(code, score, last, loaded, e2s, s2e, hist, st, 1.0, R, in_flight=fl)
+        b = rp.step(hist, st, fl)
+        assert a == b, st
+        assert np.array_equal(e2s, rp.e2s) and np.array_equal(s2e, rp.s2e)
+        n_pairs += len(a)
+    assert n_pairs > 0
+
+
+@pytest.mark.parametrize("name,code", [("cache_lru_trace.txt", 1), ("cache_fifo_trace.txt", 2)])
+def test_library_recency_golden_traces(lib, name, code):
+    lines = [l.split() for l in open(os.path.join(ROOT, "tests", "golden", name)) if l.strip() and l[0] != "#"]
+    E, S, R = int(lines[0][1]), int(lines[0][3]), int(lines[0][5])
+    e2s = np.array([int(v) for v in lines[1][1:]], dtype=np.int32)
+    s2e = np.full(S, -1, dtype=np.int32)
+    s2e[e2s[e2s >= 0]] = np.nonzero(e2s >= 0)[0]
+    score, last, loaded = np.zeros(E), np.full(E, -1, dtype=np.int64), np.full(E, -1, dtype=np.int64)
+    for l in lines[2:]:
+        st = int(l[1])
+        i_p, i_m = l.index("pairs"), l.index("map")
+        hist = np.array([int(v) for v in l[3:i_p]], dtype=np.int32)
+        want = [tuple(int(q) for q in p.split(":")) for p in l[i_p + 1:i_m]]
+        assert moe.policy_step_recency(code, score, last, loaded, e2s, s2e, hist, st, 1.0, R) == want, st
+        assert list(e2s) == [int(v) for v in l[i_m + 1:]]
+
+
+def test_recency_policy_rejects_bad_arguments(lib):
+    E, S = 4, 2
+    with pytest.raises(moe.MoeError):  # FIFO needs loaded[]
+        moe.policy_step_recency(moe.MOE_POLICY_FIFO, np.zeros(E), np.zeros(E, dtype=np.int64), None,
+                                np.array([0, 1, -1, -1], dtype=np.int32), np.array([0, 1], dtype=np.int32),
+                                np.zeros(E, dtype=np.int32), 0, 1.0, 1)
+    with pytest.raises(moe.MoeError):  # not a recency policy
+        moe.policy_step_recency(moe.MOE_POLICY_FREQ, np.zeros(E), np.zeros(E, dtype=np.int64),
+                                np.zeros(E, dtype=np.int64), np.array([0, 1, -1, -1], dtype=np.int32),
+                                np.array([0, 1], dtype=np.int32), np.zeros(E, dtype=np.int32), 0, 1.0, 1)

@@ -38,11 +38,12 @@ def least_popular_placement(seed, E, S):
     return np.where(rank >= E - S, rank - (E - S), -1).astype(np.int32)
 
 
-def drive(visibility, decay, steps, M, R=2, seed=0):
+def drive(visibility, decay, steps, M, R=2, seed=0, policy="freq"):
     w = SMALL
     li = stack.LayerInputs(w, 0, seed=seed, e2s=least_popular_placement(seed, w.experts, w.slots))
     lay = li.make_layer(max_tokens=8, out_f32=True, max_refills=R, score_decay=decay, visibility=visibility)
-    replay = oracle.CacheReplay(li.e2s, w.slots, decay=decay, R=R)
+    lay.set_policy({"freq": moe.MOE_POLICY_FREQ, "lru": moe.MOE_POLICY_LRU, "fifo": moe.MOE_POLICY_FIFO}[policy])
+    replay = oracle.CacheReplay(li.e2s, w.slots, decay=decay, R=R, policy=policy)
     refills = 0
     for st in range(steps):
         bias = synth.drifting_bias(seed, 0, w.experts, w.bias_tau, st, steps)
@@ -74,6 +75,28 @@ def test_deterministic_refills_follow_oracle_replay():
         slots_match_bank(lay, li, lay.get_map())
         st_ = lay.stats()
         assert st_[1] == st_[0] * SMALL.expert_bytes
+
+
+@pytest.mark.parametrize("policy", ["lru", "fifo"])
+def test_recency_policies_follow_oracle_replay(policy):
+    """LRU and FIFO slots on the GPU: each step's refills and map equal the oracle's replay, and every
+    refilled slot holds its expert's bytes."""
+    for st, lay, li, replay, o, n, _ in drive(moe.MOE_VIS_DETERMINISTIC, 1.0, 40, 2, policy=policy):
+        pairs = replay.step(o["hist"], st)
+        assert n == len(pairs), st
+        assert np.array_equal(lay.get_map(), replay.e2s), st
+        torch.cuda.synchronize()
+        slots_match_bank(lay, li, lay.get_map())
+
+
+def test_set_policy_rejects_unknown():
+    li = stack.LayerInputs(SMALL, 0)
+    lay = li.make_layer(max_tokens=8)
+    try:
+        with pytest.raises(moe.MoeError):
+            lay.set_policy(7)
+    finally:
+        lay.close()
 
 
 def test_deterministic_lfru_decay_batches():
