@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--ref-layers", type=int, default=1, help="layers per oracle step (reference arm sample)")
     ap.add_argument("--cold-on-host", action="store_true",
                     help="decode with the cold routes computed on the host cores (moe_forward_cold) as well")
+    ap.add_argument("--policy-sweep", action="store_true",
+                    help="hot-route hit rate and refills of each slot policy on the drifting decode workload")
     ap.add_argument("--cold-on-gpu", action="store_true",
                     help="decode with the cold routes computed on the GPU from the host bank in place as well")
     return ap.parse_args()
@@ -578,8 +580,81 @@ def run_cold_host(args):
         print(json.dumps(line), flush=True)
 
 
+SWEEP = [("LFU", "freq", 1.0), ("LFRU decay 0.9", "freq", 0.9), ("LFRU decay 0.7", "freq", 0.7),
+         ("LRU", "lru", 1.0), ("FIFO", "fifo", 1.0)]
+
+
+def run_policy_sweep(args):
+    """The decode phase of the prefill-then-decode workload under each slot policy: every layer routes,
+    computes its hot routes and updates its slots each step while the routing drifts between two
+    popularity orders.  Reports the share of routes that found their expert in a slot, the refills and
+    the decode rate with the cache updates (eager launches, one host decision per layer and step)."""
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    from expert_offload_moe_gb300 import build as moe_build
+    from expert_offload_moe_gb300 import moe, stack, synth
+
+    moe_build.build()
+    moe.lib()
+    w = synth.WORKLOADS[args.workload]
+    L = w.layers if args.layers is None else args.layers
+    steps = w.steps
+    inputs = [stack.LayerInputs(w, l) for l in range(L)]
+    codes = {"freq": moe.MOE_POLICY_FREQ, "lru": moe.MOE_POLICY_LRU, "fifo": moe.MOE_POLICY_FIFO}
+    x = torch.empty((L, 1, w.hidden), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((L, 1, w.hidden), dtype=torch.bfloat16, device="cuda")
+    biases = [[torch.from_numpy(synth.drifting_bias(0, l, w.experts, w.bias_tau, t, steps)).cuda()
+               for t in range(steps)] for l in range(L)]
+    xs = torch.from_numpy(np.stack([np.stack([synth.activations(0, l, 2000 + t, 1, w.hidden)[0] for l in range(L)])
+                                    for t in range(steps)]).view(np.int16)).view(torch.bfloat16).cuda()
+    rows = []
+    for name, pol, decay in SWEEP:
+        layers = [li.make_layer(max_tokens=8, max_refills=2, score_decay=decay) for li in inputs]
+        for lay in layers:
+            lay.set_policy(codes[pol])
+        hot = cold = refills = 0
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for t in range(steps):
+            x.copy_(xs[t].unsqueeze(1))
+            for l, lay in enumerate(layers):
+                lay.set_bias(biases[l][t])
+                res = lay.route(x[l], 1)
+                lay.forward_slots(x[l], out[l], 1)
+                refills += lay.cache_update()
+                c = stack.host_counts(res)  # cache_update waited for the route's mirror
+                hot += int(c[0])
+                cold += int(c[1])
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        for lay in layers:
+            lay.close()
+        rows.append({"policy": name, "hit_rate": hot / max(hot + cold, 1),
+                     "refills_per_layer_step": refills / (L * steps),
+                     "refill_gb": refills * w.expert_bytes / 1e9, "tokens_per_s": steps / dt})
+    best = max(rows, key=lambda r: r["hit_rate"])
+    line = {
+        "metric": "slot-cache hot-route hit rate, decode with drifting routing (LFU)", "value": rows[0]["hit_rate"],
+        "unit": "fraction of routes", "n_gpus": world, "steps": steps, "warmup": 0, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4*e4m3->f32", "data": "synthetic",
+        "config": {"workload": w.name, "layers": L, "experts": w.experts, "top_k": w.top_k, "slots": w.slots,
+                   "max_refills_per_step": 2, "drift": "bias from popularity order A to order B over the steps",
+                   "sweep": rows, "best": best["policy"],
+                   "timing": "wall clock, eager launches, one host policy decision per layer and step"},
+        "roofline": None, "clocks": None, "gpu_launches": int(len(SWEEP) * steps * L * 3), "e2e": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
+    if args.policy_sweep:
+        run_policy_sweep(args)
+        return
     prefill = synth_workload(args.workload).prefill_tokens > 0
     if args.impl == "reference":
         run_reference(args, prefill)
