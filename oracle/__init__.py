@@ -73,6 +73,8 @@ def _declare(L):
     L.oracle_cache_step_recency.argtypes = [I32, P, P, P, P, P, I32, I32, P, ctypes.c_int64, ctypes.c_double, I32,
                                             P, P, P, P]
     L.oracle_cache_step_recency.restype = I32
+    L.oracle_demand_lru_step.argtypes = [P, P, P, I32, I32, P, ctypes.c_int64, P, P]
+    L.oracle_demand_lru_step.restype = I32
     L.oracle_mxfp8_block.argtypes = [P, I32, P]
     L.oracle_mxfp8_block.restype = ctypes.c_uint8
 
@@ -260,6 +262,32 @@ class CacheReplay:
                                                 _p(self.e2s), _p(self.s2e), self.E, self.S, _p(hist), int(step),
                                                 self.decay, self.R, _p(fl), _p(pe), _p(ps), _p(pv))
         return [(int(pe[i]), int(ps[i]), int(pv[i])) for i in range(n)]
+
+
+class DemandLRUReplay:
+    """Step-by-step replay of the demand-filled LRU slot table (xinfer docs "How it works", Decode): every
+    routed expert without a slot is given the least-recently-used slot that this step did not route, in
+    the same step.  ``step(hist)`` returns the fills as (expert, slot) pairs; the step clock starts at 0."""
+
+    def __init__(self, e2s, S):
+        self.e2s = _c(e2s, np.int32).copy()
+        self.E = self.e2s.shape[0]
+        self.S = S
+        self.s2e = np.full(S, -1, dtype=np.int32)
+        for e, s in enumerate(self.e2s):
+            if s >= 0:
+                self.s2e[s] = e
+        self.stamp = np.full(S, -1, dtype=np.int64)
+        self.clock = 0
+
+    def step(self, hist):
+        hist = _c(hist, np.int32)
+        fe = np.zeros(max(self.S, 1), dtype=np.int32)
+        fs = np.zeros_like(fe)
+        n = lib().oracle_demand_lru_step(_p(self.e2s), _p(self.s2e), _p(self.stamp), self.E, self.S, _p(hist),
+                                         self.clock, _p(fe), _p(fs))
+        self.clock += 1
+        return [(int(fe[i]), int(fs[i])) for i in range(n)]
 
 
 def mxfp8_block(v):

@@ -389,6 +389,67 @@ int oracle_cache_step_recency(int policy, double *score, int64_t *last, int64_t 
     return n;
 }
 
+/* Demand-filled LRU slot table (xinfer docs "How it works", Decode: before
+ * the expert GEMMs, a kernel looks the routed experts up in a per-layer LRU
+ * table kept on the GPU, gives least-recently-used slots to the misses and
+ * rewrites expert ids to slot ids; a second kernel copies the missing
+ * experts from device-mapped page-locked host memory into their slots; the
+ * step then computes every route from a slot).  The page gives no tie or
+ * order rules; readings:
+ *   stamp[s] : the last step slot s was used, i.e. its expert was routed
+ *              while resident (a hit) or it was filled; -1 at creation.
+ *              Hits are stamped before any slot is chosen.
+ *   misses   : routed experts without a slot, most routes first, ties to
+ *              the lower id.
+ *   victims  : slots whose expert this step did not route; empty slots
+ *              first (ascending slot), then the oldest stamp, ties to the
+ *              lower slot.
+ * The i-th miss takes the i-th victim.  A miss left without a victim (the
+ * step routes more distinct experts than there are slots) stays cold for
+ * this step.  No refill budget: every miss that can be served is.  Writes
+ * the fills as (expert, slot) in that order and returns their number. */
+int oracle_demand_lru_step(int32_t *e2s, int32_t *s2e, int64_t *stamp, int E, int S, const int32_t *hist,
+                           int64_t step, int32_t *fill_expert, int32_t *fill_slot) {
+    int e, s, n = 0;
+    char *took_e = (char *)calloc((size_t)E, 1), *took_s = (char *)calloc((size_t)S, 1);
+    for (e = 0; e < E; ++e)
+        if (hist[e] > 0 && e2s[e] >= 0) stamp[e2s[e]] = step;
+    for (;;) {
+        int cand = -1, vic = -1;
+        for (e = 0; e < E; ++e) {
+            if (hist[e] <= 0 || e2s[e] >= 0 || took_e[e]) continue;
+            if (cand < 0 || hist[e] > hist[cand]) cand = e; /* ascending e: ties keep the lower id */
+        }
+        if (cand < 0) break;
+        for (s = 0; s < S; ++s) { /* ascending s: ties keep the lower slot */
+            int r = s2e[s];
+            if (took_s[s] || (r >= 0 && hist[r] > 0)) continue;
+            if (vic < 0) {
+                vic = s;
+                continue;
+            }
+            if (s2e[vic] < 0) continue; /* an empty slot comes first */
+            if (r < 0 || stamp[s] < stamp[vic]) vic = s;
+        }
+        if (vic < 0) break;
+        took_e[cand] = 1;
+        took_s[vic] = 1;
+        fill_expert[n] = cand;
+        fill_slot[n] = vic;
+        ++n;
+    }
+    for (int i = 0; i < n; ++i) {
+        int v = fill_slot[i], old = s2e[v];
+        if (old >= 0) e2s[old] = -1;
+        e2s[fill_expert[i]] = v;
+        s2e[v] = fill_expert[i];
+        stamp[v] = step;
+    }
+    free(took_e);
+    free(took_s);
+    return n;
+}
+
 /* ------------------------------------------------ prefill activation format */
 
 /* E4M3 element (OCP MX v1.0 / OFP8): sign bit 7, exponent bits 6..3 (bias 7),

@@ -476,3 +476,93 @@ def test_mxfp8_block_rule(oracle_lib):
     # zeros
     sc, codes = oracle_lib.mxfp8_block(np.zeros(32, dtype=np.float32))
     assert sc == 0 and np.all(codes == 0)
+
+
+# ---------------------------------------------------------------- demand-filled LRU slot table
+
+def _read_demand_trace(name):
+    lines = [l.split() for l in open(os.path.join(GOLDEN, name)) if l.strip() and l[0] != "#"]
+    E, S = int(lines[0][1]), int(lines[0][3])
+    init = [int(v) for v in lines[1][1:]]
+    steps = []
+    for l in lines[2:]:
+        i_f, i_m = l.index("fills"), l.index("map")
+        steps.append(([int(v) for v in l[3:i_f]], [tuple(int(q) for q in p.split(":")) for p in l[i_f + 1:i_m]],
+                      [int(v) for v in l[i_m + 1:]]))
+    return E, S, init, steps
+
+
+def test_demand_lru_hand_worked_trace(oracle_lib):
+    E, S, init, steps = _read_demand_trace("cache_demand_lru_trace.txt")
+    rp = oracle_lib.DemandLRUReplay(np.array(init, dtype=np.int32), S)
+    for i, (hist, fills, mp) in enumerate(steps):
+        assert rp.step(np.array(hist, dtype=np.int32)) == fills, i
+        assert list(rp.e2s) == mp, i
+
+
+@pytest.mark.parametrize("S,init_fill", [(4, 4), (8, 3), (1, 1)])
+def test_demand_lru_one_expert_per_step_is_a_textbook_lru_cache(oracle_lib, S, init_fill):
+    # With one routed expert per step there are no ties within a step: the resident set must follow a
+    # textbook LRU cache of capacity S (least recently used first out; initial experts in slot order count as
+    # used before any step, the lower slot earlier), and the fills must be exactly its misses.
+    from collections import OrderedDict
+    rng = np.random.default_rng(21)
+    E = 12
+    init = np.full(E, -1, dtype=np.int32)
+    init[:init_fill] = np.arange(init_fill)
+    rp = oracle_lib.DemandLRUReplay(init, S)
+    book = OrderedDict((e, None) for e in range(init_fill))
+    for st in range(400):
+        e = int(rng.zipf(1.3) - 1) % E
+        hist = np.zeros(E, dtype=np.int32)
+        hist[e] = 1 + int(rng.integers(0, 3))
+        fills = rp.step(hist)
+        miss = e not in book
+        if miss:
+            if len(book) == S:
+                book.popitem(last=False)
+            book[e] = None
+        else:
+            book.move_to_end(e)
+        assert [f[0] for f in fills] == ([e] if miss else []), st
+        assert set(np.nonzero(rp.e2s >= 0)[0].tolist()) == set(book), st
+
+
+def test_demand_lru_invariants_on_random_steps(oracle_lib):
+    rng = np.random.default_rng(23)
+    E, S = 40, 12
+    init = np.where(np.arange(E) < 10, np.arange(E), -1).astype(np.int32)  # two slots start empty
+    rp = oracle_lib.DemandLRUReplay(init, S)
+    for st in range(300):
+        M, k = int(rng.integers(1, 5)), 4
+        hist = np.zeros(E, dtype=np.int32)
+        for _ in range(M):
+            hist[rng.choice(E, k, replace=False)] += 1
+        e2s0, s2e0, stamp0 = rp.e2s.copy(), rp.s2e.copy(), rp.stamp.copy()
+        fills = rp.step(hist)
+        routed = set(np.nonzero(hist)[0].tolist())
+        hits = {e for e in routed if e2s0[e] >= 0}
+        misses = routed - hits
+        # every miss that can be served is, and only those
+        free = [s for s in range(S) if s2e0[s] < 0 or hist[s2e0[s]] == 0]
+        assert len(fills) == min(len(misses), len(free)), st
+        assert {f[0] for f in fills} <= misses and len({f[1] for f in fills}) == len(fills), st
+        # served misses: most routes first; victims: slots this step did not route, empty first, oldest stamp
+        served = [f[0] for f in fills]
+        assert all(hist[a] >= hist[b] for a, b in zip(served, served[1:])), st
+        if len(fills) < len(misses):
+            assert min(hist[e] for e in served) >= max(hist[e] for e in misses - set(served)), st
+        key = {s: (-2 if s2e0[s] < 0 else stamp0[s]) for s in free}
+        used = [f[1] for f in fills]
+        assert all(s in key for s in used), st
+        assert max((key[s] for s in used), default=-3) <= min((key[s] for s in free if s not in used),
+                                                               default=1 << 40), st
+        # map: injective, s2e its inverse, every hit unchanged, every routed expert resident when it fits
+        res = rp.e2s[rp.e2s >= 0]
+        assert len(set(res.tolist())) == len(res)
+        assert all(rp.s2e[rp.e2s[e]] == e for e in range(E) if rp.e2s[e] >= 0)
+        assert all(rp.e2s[e] == e2s0[e] for e in hits), st
+        if len(routed) <= S:
+            assert all(rp.e2s[e] >= 0 for e in routed), st
+        # stamps: every slot used this step carries the step
+        assert all(rp.stamp[rp.e2s[e]] == st for e in routed if rp.e2s[e] >= 0), st
