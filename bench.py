@@ -635,6 +635,7 @@ def run_policy_sweep(args):
         rows.append({"policy": name, "hit_rate": hot / max(hot + cold, 1),
                      "refills_per_layer_step": refills / (L * steps),
                      "refill_gb": refills * w.expert_bytes / 1e9, "tokens_per_s": steps / dt})
+    rows += device_table_rows(w, L, steps, inputs, xs, biases)
     best = max(rows, key=lambda r: r["hit_rate"])
     line = {
         "metric": "slot-cache hot-route hit rate, decode with drifting routing (LFU)", "value": rows[0]["hit_rate"],
@@ -648,6 +649,65 @@ def run_policy_sweep(args):
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def device_table_rows(w, L, steps, inputs, xs, biases):
+    """The same decode phase with the slot table on the GPU (xinfer docs "How it works", Decode): every
+    miss is filled in its own step, so every route is computed from a slot.  Timed twice: eager launches
+    like the host policies, and as one CUDA graph per step (route with the table step, fill, gate/up and
+    down of every layer; no host decision left)."""
+    import numpy as np
+    import torch
+
+    from expert_offload_moe_gb300 import stack
+
+    rows = []
+    for mode in ("eager", "graph"):
+        layers = [li.make_layer(max_tokens=8) for li in inputs]
+        for lay in layers:
+            lay.set_device_cache(True)
+        x = torch.empty((L, 1, w.hidden), dtype=torch.bfloat16, device="cuda")
+        out = torch.empty((L, 1, w.hidden), dtype=torch.bfloat16, device="cuda")
+        bias = torch.empty((L, w.experts), dtype=torch.float32, device="cuda")
+        bias_all = torch.stack([torch.stack([biases[l][t] for l in range(L)]) for t in range(steps)])
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+
+        def body():
+            for l, lay in enumerate(layers):
+                lay.set_bias(bias[l], s)
+                lay.route(x[l], 1, s)
+                lay.forward_slots(x[l], out[l], 1, s)
+
+        g = None
+        if mode == "graph":
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                body()
+            for lay in layers:  # capture ran nothing; start the counters from the same state as eager
+                lay.set_device_cache(False)
+                lay.set_device_cache(True)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(s):
+            for t in range(steps):
+                x.copy_(xs[t].unsqueeze(1))
+                bias.copy_(bias_all[t])
+                if g is None:
+                    body()
+                else:
+                    g.replay()
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        st = np.sum([lay.device_cache_stats() for lay in layers], axis=0)
+        for lay in layers:
+            lay.close()
+        routes = L * steps * w.top_k
+        rows.append({"policy": f"device LRU, demand fill ({mode})", "hit_rate": float(st[2]) / routes,
+                     "refills_per_layer_step": float(st[1]) / (L * steps),
+                     "refill_gb": float(st[1]) * w.expert_bytes / 1e9, "tokens_per_s": steps / dt,
+                     "routes_computed": "all (misses filled in the step)"})
+    return rows
 
 
 def main():

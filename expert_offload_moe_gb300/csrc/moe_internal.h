@@ -41,6 +41,20 @@ struct RouteBuffers {
                           // then (after the launch) the route's position in the hot list
 };
 
+// Device-resident slot table (demand-filled LRU), written only by the route kernel's last block.
+struct LruTable {
+    int32_t *e2s;          // [E] expert -> slot, the same array as RouteParams::e2s
+    int32_t *s2e;          // [S] slot -> expert, -1 empty
+    int32_t *stamp;        // [S] last step the slot was used, -1 never
+    int32_t *clock;        // [1] step counter
+    int32_t *fill_expert;  // [<= kMaxFill] this step's fills, in fill order
+    int32_t *fill_slot;
+    int32_t *n_fill;       // [1]
+    unsigned long long *stats;  // [4] steps, fills, hit experts, misses left cold
+    int S;                 // 0: no table
+};
+constexpr int kMaxFill = kDecodeMaxTokens * kMaxTopK;  // distinct experts of a decode step
+
 struct RouteParams {
     const uint16_t *x;   // bf16 bits [M, H]
     const float *Wr;     // [E, H]
@@ -57,6 +71,7 @@ struct RouteParams {
     // prefill tile plan (or nullptr): each active expert's routes padded to whole 128-row tiles
     int32_t *pf_poff, *pf_e2a, *pf_tile_aidx, *pf_tile_nrows, *pf_ntiles;  // [E], [E], [cap], [cap], [1]
     int pf_tiles_cap;
+    LruTable lru;        // decode with the device slot table (lru.S > 0): slots assigned before compaction
 };
 
 struct ExpertGeometry {
@@ -148,6 +163,19 @@ int prefill_tiles_cap(int max_routes, int E);  // 128-row route tiles the buffer
 cudaError_t launch_prefill(const PrefillLaunch &P, cudaStream_t s);
 void launch_build_weight_atoms_bank(const uint8_t *bank, int E, const ExpertGeometry &g, uint8_t *atoms,
                                     cudaStream_t s);
+
+// Miss-copy kernel of the device slot table (moe_fill.cu): copies this step's fills from the host bank's
+// device address into their slots and builds their scale atoms.
+struct FillLaunch {
+    const uint8_t *bank;  // device address of the page-locked bank, 16-byte aligned
+    uint8_t *slots;
+    uint8_t *atoms;       // weight atoms of every slot, or nullptr
+    ExpertGeometry geo;
+    const int32_t *fill_expert, *fill_slot, *n_fill;
+    int grid;
+};
+size_t slot_fill_smem(int H, int I);
+cudaError_t launch_slot_fill(const FillLaunch &F, cudaStream_t s);
 
 cudaError_t launch_route(const RouteParams &p, cudaStream_t s, int num_sms);
 cudaError_t launch_router_transpose(const float *Wr, float *WrT, int E, int H, int E32, cudaStream_t s);

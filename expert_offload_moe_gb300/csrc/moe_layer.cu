@@ -193,6 +193,12 @@ struct moe_layer {
     int32_t *pf_poff = nullptr, *pf_e2a = nullptr, *pf_tile_aidx = nullptr, *pf_tile_nrows = nullptr, *pf_ntiles = nullptr;
     CUtensorMap mapXP{}, mapHP{}, mapSG{}, mapSU{}, mapSD{};
 
+    // device-resident slot table (moe_layer_set_device_cache): the route kernel runs a demand-filled LRU
+    // step and the fill kernel copies the misses from the bank's device address, all in stream order
+    bool dev_cache = false;
+    void *lru_block = nullptr;
+    moe::LruTable lru{};
+
     // optional per-kernel timing: event pairs around route, gate/up and down launches
     bool prof = false;
     std::vector<cudaEvent_t> prof_ev[3];
@@ -220,6 +226,7 @@ void release(moe_layer *L) {
     cudaFree(L->atoms);
     cudaFree(L->pf_block);
     cudaFree(L->stage_atoms);
+    cudaFree(L->lru_block);
     if (L->pinned_block) cudaFreeHost(L->pinned_block);
     for (auto e : {L->ev_fork, L->ev_route, L->ev_fence, L->ev_cold})
         if (e) cudaEventDestroy(e);
@@ -692,9 +699,23 @@ int moe_route(moe_layer *L, const void *x_dev, int32_t M, void *stream, moe_rout
         p.pf_ntiles = L->pf_ntiles;
         p.pf_tiles_cap = moe::prefill_tiles_cap(M * k, E);
     }
+    const bool table = L->dev_cache && M <= moe::kDecodeMaxTokens;
+    if (table) p.lru = L->lru;  // the route launch assigns slots to this step's misses
     L->routed_plan = false;
     CUDA_TRY(prof_mark(L, 0, st));
     CUDA_TRY(moe::launch_route(p, st, L->num_sms));
+    if (table) {  // and the fill kernel copies them in before anything later on the stream runs
+        moe::FillLaunch F{};
+        F.bank = L->host_bank_dev;
+        F.slots = L->slots;
+        F.atoms = L->tc ? L->atoms : nullptr;
+        F.geo = L->geo;
+        F.fill_expert = L->lru.fill_expert;
+        F.fill_slot = L->lru.fill_slot;
+        F.n_fill = L->lru.n_fill;
+        F.grid = 2 * L->num_sms;
+        CUDA_TRY(moe::launch_slot_fill(F, st));
+    }
     CUDA_TRY(prof_mark(L, 0, st));
 
     // mirror counts, histogram and cold triples to page-locked memory off the compute chain
@@ -860,6 +881,57 @@ int moe_forward_slots(moe_layer *L, const void *x_dev, void *out_dev, int32_t M,
     return MOE_OK;
 }
 
+int moe_layer_set_device_cache(moe_layer *L, int32_t enable) {
+    g_err.clear();
+    if (!L) return fail(MOE_EINVAL, "layer is NULL");
+    const int E = L->d.num_experts, S = L->d.num_slots;
+    if (enable && !L->dev_cache) {
+        if (!L->host_bank_dev) return fail(MOE_ESTATE, "the GPU cannot address the host bank in place");
+        if (reinterpret_cast<uintptr_t>(L->host_bank_dev) % 16)
+            return fail(MOE_EINVAL, "the host bank must be 16-byte aligned for the device slot table");
+        // every copy the host policy issued has landed once the device is idle: its map is the slots' content
+        CUDA_TRY(cudaDeviceSynchronize());
+        for (auto &pc : L->pending) {
+            L->in_flight[pc.expert] = 0;
+            L->ev_pool.push_back(pc.ev);
+        }
+        L->pending.clear();
+        const size_t l = align_up((size_t)S * 4, 256), f = align_up((size_t)moe::kMaxFill * 4, 256);
+        if (!L->lru_block) {
+            CUDA_TRY(cudaMalloc(&L->lru_block, 2 * l + 2 * f + 512));
+            char *q = static_cast<char *>(L->lru_block);
+            L->lru.e2s = L->e2s_dev;
+            L->lru.s2e = (int32_t *)q;
+            L->lru.stamp = (int32_t *)(q + l);
+            L->lru.fill_expert = (int32_t *)(q + 2 * l);
+            L->lru.fill_slot = (int32_t *)(q + 2 * l + f);
+            L->lru.clock = (int32_t *)(q + 2 * l + 2 * f);
+            L->lru.n_fill = (int32_t *)(q + 2 * l + 2 * f + 4);
+            L->lru.stats = (unsigned long long *)(q + 2 * l + 2 * f + 256);
+            L->lru.S = S;
+        }
+        std::vector<int32_t> stamp((size_t)S, -1);
+        const int32_t zero2[2] = {0, 0};
+        const unsigned long long zero4[4] = {0, 0, 0, 0};
+        CUDA_TRY(cudaMemcpy(L->e2s_dev, L->e2s.data(), (size_t)E * 4, cudaMemcpyHostToDevice));
+        CUDA_TRY(cudaMemcpy(L->lru.s2e, L->s2e.data(), (size_t)S * 4, cudaMemcpyHostToDevice));
+        CUDA_TRY(cudaMemcpy(L->lru.stamp, stamp.data(), (size_t)S * 4, cudaMemcpyHostToDevice));
+        CUDA_TRY(cudaMemcpy(L->lru.clock, zero2, sizeof(zero2), cudaMemcpyHostToDevice));
+        CUDA_TRY(cudaMemcpy(L->lru.stats, zero4, sizeof(zero4), cudaMemcpyHostToDevice));
+        L->e2s_visible = L->e2s;
+        L->dev_cache = true;
+    } else if (!enable && L->dev_cache) {
+        // the host policy takes over the device's map
+        CUDA_TRY(cudaDeviceSynchronize());
+        CUDA_TRY(cudaMemcpy(L->e2s.data(), L->e2s_dev, (size_t)E * 4, cudaMemcpyDeviceToHost));
+        CUDA_TRY(cudaMemcpy(L->s2e.data(), L->lru.s2e, (size_t)S * 4, cudaMemcpyDeviceToHost));
+        L->e2s_visible = L->e2s;
+        L->policy_seq = L->route_seq;  // the last route's decision was the device's
+        L->dev_cache = false;
+    }
+    return MOE_OK;
+}
+
 int moe_layer_set_policy(moe_layer *L, int32_t policy) {
     g_err.clear();
     if (!L) return fail(MOE_EINVAL, "layer is NULL");
@@ -950,6 +1022,7 @@ int moe_cache_update(moe_layer *L, void *stream, int32_t *n_refills_out) {
     if (n_refills_out) *n_refills_out = 0;
     if (!L) return fail(MOE_EINVAL, "layer is NULL");
     const int E = L->d.num_experts, S = L->d.num_slots;
+    if (L->dev_cache) return fail(MOE_ESTATE, "the device slot table owns the slots (moe_layer_set_device_cache)");
     if (S >= E) return MOE_OK;  // every expert resident: nothing to refill
     if (L->route_seq == L->policy_seq)
         return fail(MOE_ESTATE, "moe_cache_update needs a moe_route since the last update");
@@ -1104,7 +1177,23 @@ int moe_layer_stage_all(moe_layer *L, void *stream) {
 
 int moe_debug_get_map(const moe_layer *L, int32_t *out) {
     if (!L || !out) return fail(MOE_EINVAL, "layer and out are required");
+    if (L->dev_cache) {  // the device owns the map: read it after everything enqueued
+        CUDA_TRY(cudaDeviceSynchronize());
+        CUDA_TRY(cudaMemcpy(out, L->e2s_dev, (size_t)L->d.num_experts * sizeof(int32_t), cudaMemcpyDeviceToHost));
+        return MOE_OK;
+    }
     memcpy(out, L->e2s_visible.data(), L->e2s_visible.size() * sizeof(int32_t));
+    return MOE_OK;
+}
+
+int moe_debug_device_cache(const moe_layer *L, int64_t out[4]) {
+    if (!L || !out) return fail(MOE_EINVAL, "layer and out are required");
+    for (int i = 0; i < 4; ++i) out[i] = 0;
+    if (!L->lru_block) return MOE_OK;
+    unsigned long long v[4];
+    CUDA_TRY(cudaDeviceSynchronize());
+    CUDA_TRY(cudaMemcpy(v, L->lru.stats, sizeof(v), cudaMemcpyDeviceToHost));
+    for (int i = 0; i < 4; ++i) out[i] = (int64_t)v[i];
     return MOE_OK;
 }
 

@@ -25,6 +25,8 @@
 // The kernel is launched with programmatic serialization: the router weights,
 // bias and expert_to_slot map are read before it waits for the previous grid
 // in the stream, x and all outputs after.
+#include <climits>
+
 #include "moe_internal.h"
 #include "moe_tc.cuh"
 
@@ -89,6 +91,96 @@ __device__ int block_scan_array(int *a, int n) {
     }
     __syncthreads();
     return total;
+}
+
+// Demand-filled LRU slot table (xinfer docs "How it works", Decode: the routed experts are looked up in a
+// per-layer LRU table kept on the GPU, misses get least-recently-used slots, expert ids become slot ids).
+// The whole last block runs it once top-k has filled s_hist and before the compaction, which then reads
+// the new map from s_e2s.
+//   - slots whose expert this step routed (hits) get the step's clock as their stamp;
+//   - misses (routed, no slot) are served most routes first, ties to the lower id;
+//   - victims are the slots this step did not route: empty first, then oldest stamp, ties to the lower
+//     slot; the i-th miss takes the i-th victim, and misses left over stay cold for this step.
+// The fills go to a device list that the fill kernel reads.  scr: 3 * kMaxExperts + 2 * kMaxFill ints of
+// shared scratch that is dead at this point.
+__device__ void lru_table_step(const RouteParams &p, int *s_e2s, const int *s_hist, int *scr) {
+    const LruTable &T = p.lru;
+    const int E = p.E, S = T.S;
+    int *s_s2e = scr, *s_key = scr + kMaxExperts, *s_off = scr + 2 * kMaxExperts;
+    int *s_cand = scr + 3 * kMaxExperts, *s_vict = s_cand + kMaxFill;
+    __shared__ int s_clock, s_hits, s_elig;
+    if (threadIdx.x == 0) {
+        s_clock = *T.clock;
+        s_hits = 0;
+        s_elig = 0;
+    }
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+        const int s = T.e2s[e];  // the previous step's last block wrote it; this launch has not
+        s_e2s[e] = s;
+        s_off[e] = (s_hist[e] > 0 && s < 0) ? 1 : 0;
+    }
+    for (int s = threadIdx.x; s < S; s += kThreads) s_s2e[s] = T.s2e[s];
+    __syncthreads();
+    const int clock = s_clock;
+    int hits = 0, elig = 0;
+    for (int s = threadIdx.x; s < S; s += kThreads) {
+        const int o = s_s2e[s];
+        const bool routed = o >= 0 && s_hist[o] > 0;
+        if (routed) T.stamp[s] = clock;
+        s_key[s] = routed ? INT_MAX : (o < 0 ? -2 : T.stamp[s]);
+        hits += routed;
+        elig += !routed;
+    }
+    if (hits) atomicAdd(&s_hits, hits);
+    if (elig) atomicAdd(&s_elig, elig);
+    const int n_cand = block_scan_array(s_off, E);  // misses, listed by ascending id
+    for (int e = threadIdx.x; e < E; e += kThreads)
+        if (s_hist[e] > 0 && s_e2s[e] < 0) s_cand[s_off[e]] = e;
+    const int n_fill = min(n_cand, s_elig);
+    if (n_cand > 0) {
+        // victim ranks by (key, slot); only the first n_fill are taken
+        for (int s = threadIdx.x; s < S; s += kThreads) {
+            const int key = s_key[s];
+            if (key == INT_MAX) continue;
+            int rank = 0;
+            for (int q = 0; q < S && rank < n_fill; ++q) {
+                const int kq = s_key[q];
+                rank += kq < key || (kq == key && q < s);
+            }
+            if (rank < n_fill) s_vict[rank] = s;
+        }
+        __syncthreads();
+        // miss ranks by (routes descending, id ascending); the list is in id order
+        for (int i = threadIdx.x; i < n_cand; i += kThreads) {
+            const int e = s_cand[i], h = s_hist[e];
+            int rank = 0;
+            for (int j = 0; j < n_cand; ++j) {
+                const int hj = s_hist[s_cand[j]];
+                rank += hj > h || (hj == h && j < i);
+            }
+            if (rank >= n_fill) continue;  // stays cold this step
+            const int v = s_vict[rank], old = s_s2e[v];
+            if (old >= 0) {
+                T.e2s[old] = -1;
+                s_e2s[old] = -1;
+            }
+            T.e2s[e] = v;
+            s_e2s[e] = v;
+            T.s2e[v] = e;
+            T.stamp[v] = clock;
+            T.fill_expert[rank] = e;
+            T.fill_slot[rank] = v;
+        }
+    }
+    if (threadIdx.x == 0) {
+        *T.n_fill = n_fill;
+        *T.clock = clock + 1;
+        T.stats[0] += 1;
+        T.stats[1] += (unsigned long long)n_fill;
+        T.stats[2] += (unsigned long long)s_hits;
+        T.stats[3] += (unsigned long long)(n_cand - n_fill);
+    }
+    __syncthreads();
 }
 
 __device__ __forceinline__ void load_router_row(const RouteParams &p, int task, int lane, float (&w8)[8]) {
@@ -239,6 +331,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
             }
         }
         __syncthreads();
+        if (p.lru.S) lru_table_step(p, s_e2s, s_hist, reinterpret_cast<int *>(s_union));
         if (warp == 0) {
             const int e = lane;
             const int hist = e < E ? s_hist[e] : 0;
@@ -386,6 +479,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
             __syncwarp();
         }
         __syncthreads();
+        if (p.lru.S) lru_table_step(p, s_e2s, s_hist, reinterpret_cast<int *>(s_union));
         // Lists, one thread per route (at most 8 x 16): each counts the routes that come before it --
         // hot routes by (expert, token), cold routes by (token, expert) -- and the active experts below
         // its own; the first route of an expert (lowest token) writes the active entry.
@@ -501,6 +595,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
     __syncthreads();
 
     if (M <= kWarps) {
+        if (p.lru.S) lru_table_step(p, s_e2s, s_hist, reinterpret_cast<int *>(s_union));
         // Decode: warp 0 scans the experts (each lane a run of consecutive ids), warp 1 the tokens.
         __shared__ int s_n[3];
         if (warp == 0) {

@@ -24,6 +24,7 @@ EXPORTED = [
     "moe_debug_slot_ptr", "moe_debug_inject_fault", "moe_debug_stats", "moe_debug_profile",
     "moe_debug_profile_read", "moe_debug_check_error", "moe_policy_step", "moe_route_noalloc", "moe_forward_cold",
     "moe_forward_cold_gpu", "moe_host_expert_ffn", "moe_policy_step_recency", "moe_layer_set_policy",
+    "moe_layer_set_device_cache", "moe_debug_device_cache",
 ]
 
 
@@ -76,6 +77,8 @@ def lib():
         L.moe_policy_step_recency.argtypes = [i32, p, p, p, p, p, i32, i32, p, ctypes.c_int64, ctypes.c_double,
                                               i32, p, p, p, p]
         L.moe_layer_set_policy.argtypes = [p, i32]
+        L.moe_layer_set_device_cache.argtypes = [p, i32]
+        L.moe_debug_device_cache.argtypes = [p, p]
         L.moe_host_expert_ffn.argtypes = [p, i32, i32, p, p]
         L.moe_cache_update.argtypes = [p, p, ctypes.POINTER(i32)]
         L.moe_destroy.argtypes = [p]
@@ -154,6 +157,19 @@ class Layer:
     def set_policy(self, policy):
         """Slot policy for later cache updates: MOE_POLICY_FREQ (default), MOE_POLICY_LRU or MOE_POLICY_FIFO."""
         check(lib().moe_layer_set_policy(self.h, int(policy)))
+
+    def set_device_cache(self, enable=True):
+        """Decode calls keep and run the slot table on the GPU (demand-filled LRU, misses copied in by a kernel
+        in the same step), or hand it back to the host policy.  Synchronises the device."""
+        check(lib().moe_layer_set_device_cache(self.h, 1 if enable else 0))
+
+    def device_cache_stats(self):
+        """[steps, experts filled, hit experts, misses left cold] of the device slot table (synchronises)."""
+        import numpy as np
+
+        s = np.zeros(4, dtype=np.int64)
+        check(lib().moe_debug_device_cache(self.h, s.ctypes.data_as(_P)))
+        return s
 
     def forward_cold_gpu(self, x, out, M, stream=None):
         """Cold routes of the last route on the GPU, reading the host bank in place, added to ``out``."""

@@ -369,6 +369,49 @@ int moe_policy_step_recency(int32_t policy, double *score, int64_t *last, int64_
  * for its later moe_cache_update calls.  Errors: MOE_EINVAL. */
 int moe_layer_set_policy(moe_layer *layer, int32_t policy);
 
+/* ------------------------------------------------ device-resident slot table */
+
+/* Switches the layer's decode calls (M <= 8) to a slot table kept and run on
+ * the GPU (xinfer docs "How it works", Decode: before the expert GEMMs a
+ * kernel looks the routed experts up in a per-layer LRU table on the GPU,
+ * gives least-recently-used slots to the misses and rewrites expert ids to
+ * slot ids; a second kernel copies the missing experts from device-mapped
+ * page-locked host memory into their slots; both have fixed launch shapes and
+ * read the miss count from device memory, so decode stays inside CUDA graphs).
+ *
+ * With the table on, moe_route does both in stream order after top-k:
+ *   - slots whose expert the step routed (hits) are stamped with the step;
+ *   - each routed expert without a slot (a miss; most routes first, ties to
+ *     the lower id) takes a slot the step did not route: empty slots first
+ *     (ascending), then the oldest stamp (ties: lower slot); expert_to_slot
+ *     and the route lists use the new map;
+ *   - a fill kernel copies those experts from the host bank's device address
+ *     into their slots (with their tensor-core scale atoms) before any later
+ *     work on the stream.
+ * Every route of the step is then hot, except for misses left without a slot
+ * (only when a step routes more distinct experts than num_slots), which stay
+ * cold for the step and are listed as usual.  There is no refill budget:
+ * max_refills_per_step and the host policy do not apply, and
+ * moe_cache_update returns MOE_ESTATE while the table is on.  Prefill calls
+ * (M > 8) do not touch the table.  Routes to the same experts give the same
+ * output whatever slots they sit in (expert-order accumulation).
+ *
+ * enable != 0: the table starts from the layer's current map (after every
+ * copy the host policy issued has landed), every stamp -1.  enable == 0: the
+ * host policy takes over the table's map.  Both synchronise the device; not
+ * capturable.  The host bank must have a device address (page-locked memory
+ * on a GPU that can map it: MOE_ESTATE otherwise) and be 16-byte aligned
+ * (MOE_EINVAL).  While on, moe_debug_get_map reads the device's map
+ * (synchronising).  In profiling mode (moe_debug_profile) the fill kernel is
+ * timed with the route.  Errors: MOE_EINVAL, MOE_ESTATE, MOE_ECUDA. */
+int moe_layer_set_device_cache(moe_layer *layer, int32_t enable);
+
+/* Cumulative counters of the device slot table since it was last switched
+ * on (synchronises the device): [0] decode steps, [1] experts filled,
+ * [2] hits (routed experts already resident, counted once per step),
+ * [3] misses left cold.  All zero if the table was never on. */
+int moe_debug_device_cache(const moe_layer *layer, int64_t out[4]);
+
 #ifdef __cplusplus
 }
 #endif
