@@ -57,6 +57,9 @@ def parse():
                     help="hot-route hit rate and refills of each slot policy on the drifting decode workload")
     ap.add_argument("--cold-on-gpu", action="store_true",
                     help="decode with the cold routes computed on the GPU from the host bank in place as well")
+    ap.add_argument("--one-launch", action="store_true",
+                    help="M = 1 decode with gate/up, SiLU and down in one launch (then a combine launch) instead of "
+                         "the separate gate/up and down launches")
     return ap.parse_args()
 
 
@@ -213,9 +216,9 @@ def run_reference(args, prefill=False):
     print(json.dumps(line), flush=True)
 
 
-def traffic_for(kernel_src):
+def traffic_for(kernel_src, summary):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
-    summ = os.path.join(ROOT, "profiles", "gateup_tc_gptoss20b_traffic.txt")
+    summ = os.path.join(ROOT, "profiles", summary)
     if not os.path.exists(summ):
         return None
     sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
@@ -252,6 +255,9 @@ def run_ours(args):
     st = stack.DecodeStack(w, M=M, n_layers=args.layers, seed=rank, n_inputs=n_inputs,
                            cold_on_gpu=args.cold_on_gpu)
     L = st.L
+    if args.one_launch:
+        for lay in st.layers:
+            lay.decode_fusion(True)
     st.capture()
     stream = torch.cuda.current_stream()
 
@@ -316,8 +322,16 @@ def run_ours(args):
     route_us, gateup_us, down_us = (1e3 * prof[i] / launches for i in range(3))
     pk, pk_src = peaks()
     hbm_peak = pk.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"])
-    achieved = gateup_bytes / (gateup_us * 1e-6) / 1e9
-    traffic = traffic_for(os.path.join(ROOT, "expert_offload_moe_gb300", "csrc", "moe_decode_tc.cu"))
+    src = os.path.join(ROOT, "expert_offload_moe_gb300", "csrc", "moe_decode_tc.cu")
+    if down_us == 0.0:  # one launch per layer: gate/up, SiLU, down and combine (every expert byte read)
+        kernel, kbytes = "ffn_tc_kernel", mean_act * w.expert_bytes
+        kernel_us = {"route": route_us, "ffn": gateup_us}
+        traffic = traffic_for(src, "ffn_tc_gptoss20b_traffic.txt")
+    else:
+        kernel, kbytes = "gateup_tc_kernel", gateup_bytes
+        kernel_us = {"route": route_us, "gateup": gateup_us, "down": down_us}
+        traffic = traffic_for(src, "gateup_tc_gptoss20b_traffic.txt")
+    achieved = kbytes / (gateup_us * 1e-6) / 1e9
 
     # ---------------- e2e: host inputs in, outputs back, every step ------------
     x_host = torch.empty((n_inputs, L, M, w.hidden), dtype=torch.bfloat16, pin_memory=True)
@@ -354,14 +368,14 @@ def run_ours(args):
                    "expert_gbs": expert_bytes_step / (t_ms / args.steps * 1e-3) / 1e9,
                    "router_gbs": router_bytes_step / (t_ms / args.steps * 1e-3) / 1e9,
                    "mean_active_experts": mean_act,
-                   "kernel_us": {"route": route_us, "gateup": gateup_us, "down": down_us}},
-        "roofline": {"bound": "hbm", "kernel": "gateup_tc_kernel", "achieved": achieved, "peak": hbm_peak,
+                   "kernel_us": kernel_us},
+        "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm_peak,
                      "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
-                     "bytes_per_launch": gateup_bytes, "avg_launch_us": gateup_us,
+                     "bytes_per_launch": kbytes, "avg_launch_us": gateup_us,
                      "peak_source": "measured hbm_gbs (MEASURED_PEAKS.json)" if pk_src == "measured"
                      else "fallback 6.8 TB/s"},
         "clocks": clocks,
-        "gpu_launches": int(args.steps * L * (7 if args.cold_on_gpu else 3)),
+        "gpu_launches": int(args.steps * L * (3 + (4 if args.cold_on_gpu else 0))),
         "e2e": e2e,
     }
     if args.cold_on_gpu:

@@ -570,6 +570,360 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_sync();  // no CTA leaves while another still reads its shared memory
 }
 
+// ------------------------------------------------------------------ one launch for M = 1
+
+constexpr int kFfnThreads = 192;  // warps 0-3: epilogue (TMEM lane quadrant = warp); warp 4: copies; warp 5: MMAs
+constexpr int kFfnNB = 16;        // B columns of the down MMA: 4 w*h terms of the one token, 12 zero columns
+constexpr int kErrHReady = 4, kErrAccFull = 5, kErrAccEmpty = 6;
+
+struct FfnArgs {
+    const uint8_t *bank, *atoms;
+    size_t expert_bytes, atom_slot_bytes, off_g_codes, off_u_codes, off_d_codes, atom_off_g, atom_off_u, atom_off_d;
+    int H, I, KS, Ucap;
+    const int32_t *counts, *act_slot, *act_off, *act_cnt, *hot_token;
+    const float *hot_w;
+    const uint8_t *xat;
+    float *part;      // [ntH][Ucap][128] down partial of each (active expert, I tile) unit
+    int *err;
+};
+
+// The whole expert FFN of a one-token decode step in one launch.  grid: (active expert, 128-row tile j of I,
+// K split), the K splits of a tile being one cluster.  Each cluster
+//   1. computes g, u for its I tile as gate/up does (K split over the CTAs, partials summed in rank order),
+//   2. forms h = w SiLU(g) u for the tile's 128 rows in every CTA and splits it into four E4M3 terms held in
+//      shared memory (the B operand of the down MMA, never written to global memory),
+//   3. multiplies the tile's column slice of Wd (all H rows, 128 columns) by it: CTA r takes H tiles
+//      r, r + KS, ...; its copy warp streams those weight tiles into the pipeline right behind the gate/up
+//      tiles (two per stage), so they load while the gate/up MMAs and step 2 run,
+//   4. stores a fp32 partial per (unit, H tile); ffn_combine_kernel, launched right behind, sums them.
+// Shared memory is the gate/up pipeline's: down tiles use a stage's two A slots and two atom slots; the
+// K-split partials, h terms and h atom live in the stages' x-term slots, which down tiles never touch.
+__global__ void __launch_bounds__(kFfnThreads, 2)
+    ffn_tc_kernel(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ CUtensorMap mapU,
+                  const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapD, FfnArgs a) {
+    constexpr int S = kGateStages;
+    constexpr int kB = NBX * 128;
+    constexpr uint32_t kTxFull = 2 * kTileATx + kB + 3 * kAtom, kTxTail = kB + 3 * kAtom;
+    constexpr int T = kHTerms;
+    constexpr int kAtomSlot = 2 * kTileA + kB;  // first atom slot of a stage
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    __shared__ __align__(8) uint64_t full[S], empty[S], done, hready, acc_full[2], acc_empty[2];
+    __shared__ uint32_t tslot;
+    __shared__ float s_w;
+    __shared__ int s_routed;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ntile = (a.I + 127) / 128, nks = (a.H + 127) / 128, nksI = ntile, ntH = (a.H + 127) / 128;
+    const int KS = a.KS;
+    const int unit = blockIdx.x / KS, ks = blockIdx.x - unit * KS;
+    const int aidx = unit / ntile, jt = unit - aidx * ntile;
+    const int k0 = ks * nks / KS, k1 = (ks + 1) * nks / KS, ngu = k1 - k0;
+    const bool raggedH = (a.H % 128) != 0, raggedI = (a.I % 128) != 0;
+    const bool tailI = raggedI && jt == nksI - 1;
+    const int row0 = jt * 128;
+    const int nd = (ntH - ks + KS - 1) / KS;  // H tiles of this CTA: ks, ks + KS, ...
+    const int nds = (nd + 1) / 2;             // pipeline stages they take, two tiles each
+
+    uint8_t *red = smem + kTileA * 2;               // stage 0 x-term slot: K-split partials [4][128] fp32
+    uint8_t *hB = smem + kGateStage + kTileA * 2;   // stage 1 x-term slot: h terms, 16 rows x 128 bytes
+    uint8_t *hAt = smem + 2 * kGateStage + kTileA * 2;  // stage 2 x-term slot: h atom
+
+    if (warp == 5) tmem_alloc(&tslot, kGateTmem);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(&done, 1);
+        mbar_init(&hready, 128);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 128);
+        }
+        fence_barrier_init();
+        tma_prefetch_desc(&mapG);
+        tma_prefetch_desc(&mapU);
+        tma_prefetch_desc(&mapX);
+        tma_prefetch_desc(&mapD);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = tslot;
+    pdl_wait();  // routing and x terms are complete
+    pdl_trigger();
+    const int n_act = a.counts[2];
+    if (aidx >= n_act) {  // the whole cluster (one unit) leaves together
+        __syncthreads();
+        if (warp == 5) tmem_dealloc(tbase, kGateTmem);
+        return;
+    }
+    const int slot = a.act_slot[aidx];
+    const uint8_t *expert = a.bank + (size_t)slot * a.expert_bytes;
+    const uint8_t *slot_atoms = a.atoms + (size_t)slot * a.atom_slot_bytes;
+    const uint8_t *gat = slot_atoms + a.atom_off_g + (size_t)jt * nks * kAtom;
+    const uint8_t *uat = slot_atoms + a.atom_off_u + (size_t)jt * nks * kAtom;
+    // columns: gate accumulator [16], up accumulator [16] (both reused as the two down accumulators once
+    // drained), 12 scale columns per stage, then the h atom
+    const uint32_t tDg = tbase, tDu = tbase + NBX, tSF = tbase + 2 * NBX, tHat = tSF + 12 * S;
+
+    if (warp == 4) {
+        // ---------------- copies ----------------
+        bool ok = true;
+        auto issue = [&](int i) {
+            const int st = i % S;
+            if (lane == 0) ok = mbar_wait(&empty[st], ((i / S) & 1) ^ 1, a.err, kErrEmpty);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) return;
+            uint8_t *sA = smem + st * kGateStage;
+            uint8_t *sAt = sA + kAtomSlot;
+            if (i < ngu) {  // gate/up k-step
+                const int kstep = k0 + i;
+                const bool tail = raggedH && kstep == nks - 1;
+                if (tail) {
+                    load_tail_tile(sA, expert + a.off_g_codes, a.I, row0, a.H, kstep);
+                    load_tail_tile(sA + kTileA, expert + a.off_u_codes, a.I, row0, a.H, kstep);
+                }
+                if (lane == 0) {
+                    mbar_expect_tx(&full[st], tail ? kTxTail : kTxFull);
+                    if (!tail) {
+                        tma_load_3d(&mapG, &full[st], sA, kstep * 128, row0, slot);
+                        tma_load_3d(&mapU, &full[st], sA + kTileA, kstep * 128, row0, slot);
+                    }
+                    tma_load_3d(&mapX, &full[st], sA + 2 * kTileA, kstep * 128, 0, 0);
+                    bulk_copy(sAt, gat + (size_t)kstep * kAtom, kAtom, &full[st]);
+                    bulk_copy(sAt + kAtom, uat + (size_t)kstep * kAtom, kAtom, &full[st]);
+                    bulk_copy(sAt + 2 * kAtom, a.xat + (size_t)kstep * kAtom, kAtom, &full[st]);
+                }
+            } else {  // two down tiles: Wd rows of H tile hr, columns of I tile jt
+                const int d0 = 2 * (i - ngu), nt = nd - d0 < 2 ? nd - d0 : 2;
+                if (tailI)
+                    for (int q = 0; q < nt; ++q)
+                        load_tail_tile(sA + q * kTileA, expert + a.off_d_codes, a.H, (ks + KS * (d0 + q)) * 128, a.I,
+                                       jt);
+                if (lane == 0) {
+                    mbar_expect_tx(&full[st], (uint32_t)nt * ((tailI ? 0u : (uint32_t)kTileATx) + kAtom));
+                    for (int q = 0; q < nt; ++q) {
+                        const int hr = ks + KS * (d0 + q);
+                        if (!tailI) tma_load_3d(&mapD, &full[st], sA + q * kTileA, jt * 128, hr * 128, slot);
+                        bulk_copy(sAt + q * kAtom, slot_atoms + a.atom_off_d + ((size_t)hr * nksI + jt) * kAtom, kAtom,
+                                  &full[st]);
+                    }
+                }
+            }
+            __syncwarp();
+        };
+        // a stage whose last user was a gate/up step frees without step 2; later ones wait for the down MMAs,
+        // which wait for h, which waits for every CTA of the cluster to arrive here
+        const int early = ngu + (nds < S ? nds : S);
+        for (int i = 0; i < early && ok; ++i) issue(i);
+        __syncwarp();
+        if (KS > 1) cluster_arrive_relaxed();
+        for (int i = early; i < ngu + nds && ok; ++i) issue(i);
+        __syncwarp();
+        if (KS > 1) {
+            cluster_wait();
+            cluster_arrive_relaxed();
+            cluster_wait();
+        }
+    } else if (warp == 5) {
+        // ---------------- MMAs ----------------
+        if (lane == 0) {
+            const uint32_t idesc = mx_idesc(kFmtE2M1, kFmtE4M3, NBX);
+            bool ok = true;
+            for (int i = 0; i < ngu && ok; ++i) {
+                const int st = i % S;
+                ok = mbar_wait(&full[st], (i / S) & 1, a.err, kErrFull);
+                if (!ok) break;
+                tc_fence_after();
+                uint8_t *sA = smem + st * kGateStage;
+                uint8_t *sAt = sA + kAtomSlot;
+                const uint32_t sfg = tSF + 12 * st, sfu = sfg + 4, sfb = sfg + 8;
+                atom_to_tmem(sfg, sAt);
+                atom_to_tmem(sfu, sAt + kAtom);
+                atom_to_tmem(sfb, sAt + 2 * kAtom);
+                const uint32_t aG = smem_u32(sA), aU = aG + kTileA, aB = aG + 2 * kTileA;
+                const int nk = (raggedH && (k0 + i) == nks - 1) ? 2 : 4;
+                for (int kk = 0; kk < nk; ++kk) {
+                    const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                    mma_mx(tDg, sw128_desc(aG + kk * 32), sw128_desc(aB + kk * 32), idesc, kk, sfg, sfb, acc);
+                    mma_mx(tDu, sw128_desc(aU + kk * 32), sw128_desc(aB + kk * 32), idesc, kk, sfu, sfb, acc);
+                }
+                mma_commit(&empty[st]);
+            }
+            mma_commit(&done);
+        }
+        __syncwarp();
+        if (KS > 1) cluster_arrive_relaxed();
+        if (lane == 0) {
+            const uint32_t idesc = mx_idesc(kFmtE2M1, kFmtE4M3, kFfnNB);
+            bool ok = mbar_wait(&hready, 0, a.err, kErrHReady);
+            tc_fence_after();
+            if (ok) atom_to_tmem(tHat, hAt);
+            const uint32_t aH = smem_u32(hB);
+            for (int ds = 0; ds < nds && ok; ++ds) {
+                const int i = ngu + ds, st = i % S;
+                ok = mbar_wait(&full[st], (i / S) & 1, a.err, kErrFull);
+                if (!ok) break;
+                tc_fence_after();
+                uint8_t *sA = smem + st * kGateStage;
+                const int d0 = 2 * ds, nt = nd - d0 < 2 ? nd - d0 : 2;
+                for (int q = 0; q < nt && ok; ++q) {
+                    const int ti = d0 + q, buf = ti & 1;
+                    if (ti >= 2) ok = mbar_wait(&acc_empty[buf], ((ti >> 1) - 1) & 1, a.err, kErrAccEmpty);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t sfa = tSF + 12 * st + 4 * q;
+                    atom_to_tmem(sfa, sA + kAtomSlot + q * kAtom);
+                    const uint32_t aA = smem_u32(sA + q * kTileA);
+                    const int nk = tailI ? 2 : 4;
+                    for (int kk = 0; kk < nk; ++kk)
+                        mma_mx(tbase + NBX * buf, sw128_desc(aA + kk * 32), sw128_desc(aH + kk * 32), idesc, kk, sfa,
+                               tHat, kk > 0 ? 1u : 0u);
+                    mma_commit(&acc_full[buf]);
+                }
+                mma_commit(&empty[st]);
+            }
+        }
+        __syncwarp();
+        if (KS > 1) {
+            cluster_wait();
+            cluster_arrive_relaxed();
+            cluster_wait();
+        }
+    } else {
+        // ---------------- epilogue: thread = row rloc of the I tile, then of each H tile ----------------
+        const int rloc = threadIdx.x;  // warps 0-3
+        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        if (threadIdx.x == 0) {  // routing weight of the token for this expert
+            const int off = a.act_off[aidx], cnt = a.act_cnt[aidx];
+            s_routed = cnt > 0 && a.hot_token[off] == 0;
+            s_w = s_routed ? a.hot_w[off] : 0.f;
+        }
+        float g[2] = {0.f, 0.f}, u[2] = {0.f, 0.f};
+        bool got = __all_sync(0xffffffffu, mbar_wait(&done, 0, a.err, kErrDone));
+        tc_fence_after();
+        if (got) {
+            uint32_t rg[8], ru[8];
+            tmem_ld8x2_sync(tDg + lane_off, rg, tDu + lane_off, ru);
+            g[0] = __uint_as_float(rg[0]);
+            g[1] = __uint_as_float(rg[1]);
+            u[0] = __uint_as_float(ru[0]);
+            u[1] = __uint_as_float(ru[1]);
+        }
+        tc_fence_before();
+        named_barrier(1, 128);  // s_w is set
+        if (KS > 1) {
+            float *rf = reinterpret_cast<float *>(red);
+            rf[0 * 128 + rloc] = g[0];
+            rf[1 * 128 + rloc] = g[1];
+            rf[2 * 128 + rloc] = u[0];
+            rf[3 * 128 + rloc] = u[1];
+            __syncwarp();
+            cluster_arrive();
+            cluster_wait();
+            // every rank's four partials are loaded before any is added (one round trip), then summed in rank order
+            float pv[kMaxCluster][4];
+#pragma unroll
+            for (int r = 0; r < kMaxCluster; ++r)
+                if (r < KS) {
+                    const uint32_t base = dsmem_addr(red, (uint32_t)r);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) pv[r][c] = ld_dsmem(base + 4u * (c * 128 + rloc));
+                }
+            g[0] = g[1] = u[0] = u[1] = 0.f;
+#pragma unroll
+            for (int r = 0; r < kMaxCluster; ++r)
+                if (r < KS) {
+                    g[0] += pv[r][0];
+                    g[1] += pv[r][1];
+                    u[0] += pv[r][2];
+                    u[1] += pv[r][3];
+                }
+            __syncwarp();
+            cluster_arrive();  // done reading the other CTAs' partials (waited for before leaving)
+        }
+        // h of this row: w SiLU(g) u, split into T E4M3 terms with one scale per 32-row block (= this warp)
+        {
+            const float gg = g[0] + g[1], uu = u[0] + u[1];
+            float res = s_routed ? s_w * (silu(gg) * uu) : 0.f;
+#pragma unroll
+            for (int term = 0; term < T; ++term) {
+                uint32_t sb;
+                const uint8_t code = split_term(res, sb);
+                st_shared_u8(hB + term * 128 + ((((rloc >> 4) ^ (term & 7)) << 4) | (rloc & 15)), code);
+                if (lane == 0) st_shared_u8(hAt + term * 16 + warp, sb);
+            }
+            if (rloc < (kFfnNB - T) * 8) st_shared_zero16(hB + T * 128 + rloc * 16);  // rows T..15: zero
+            if (rloc < 32 - T) st_shared_fill16(hAt + (T + rloc) * 16, 0x7f7f7f7fu);  // their scales: 2^0
+            fence_proxy_async();
+            mbar_arrive(&hready);
+        }
+        // down partials of this CTA's H tiles
+        float *part = a.part + (size_t)unit * 128;
+        for (int ti = 0; ti < nd; ++ti) {
+            const int buf = ti & 1, hr = ks + KS * ti;
+            got = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (ti >> 1) & 1, a.err, kErrAccFull));
+            tc_fence_after();
+            float v = 0.f;
+            if (got) {
+                uint32_t rr[8];
+                tmem_ld8_sync(tbase + NBX * buf + lane_off, rr);
+#pragma unroll
+                for (int term = 0; term < T; ++term) v += __uint_as_float(rr[term]);
+            }
+            tc_fence_before();
+            mbar_arrive(&acc_empty[buf]);
+            part[(size_t)hr * a.Ucap * 128 + rloc] = v;
+        }
+        __syncwarp();
+        if (KS > 1) cluster_wait();  // no CTA leaves while another still reads its shared memory
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) tmem_dealloc(tbase, kGateTmem);
+}
+
+constexpr int kCombineRows = 32;  // output rows per combine CTA; its 4 warps take a quarter of the units each
+
+// out[row] = sum over the units (active expert, I tile), in that order, of the one-launch FFN's partials:
+// warp q sums units [q U / 4, (q + 1) U / 4) for 32 rows with every load in flight, then the four sums are
+// added in warp order, so the result does not depend on timing or on which slots hold the experts.
+// Launched with programmatic serialization after ffn_tc_kernel; with no active unit the output is zero.
+__global__ void __launch_bounds__(128) ffn_combine_kernel(const float *part, const int32_t *counts, int ntI, int Ucap,
+                                                          int H, void *out, int out_f32) {
+    __shared__ float s_sum[4][kCombineRows];
+    pdl_wait();
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kCombineRows + lane, hr = row >> 7, rl = row & 127;
+    const int U = counts[2] * ntI;
+    const int u0 = warp * U / 4, u1 = (warp + 1) * U / 4;
+    float v = 0.f;
+    if (row < H) {
+        const float *p = part + (size_t)hr * Ucap * 128 + rl;
+        constexpr int kBatch = 32;
+        for (int ub = u0; ub < u1; ub += kBatch) {
+            float pv[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) pv[j] = ub + j < u1 ? __ldcg(p + (size_t)(ub + j) * 128) : 0.f;
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+                if (ub + j < u1) v += pv[j];
+        }
+    }
+    s_sum[warp][lane] = v;
+    __syncthreads();
+    if (warp == 0 && row < H) {
+        const float r = ((s_sum[0][lane] + s_sum[1][lane]) + s_sum[2][lane]) + s_sum[3][lane];
+        if (out_f32)
+            reinterpret_cast<float *>(out)[row] = r;
+        else
+            reinterpret_cast<__nv_bfloat16 *>(out)[row] = __float2bfloat16_rn(r);
+    }
+}
+
 template <typename K>
 void set_smem(K kernel, int bytes) {
     cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -577,10 +931,10 @@ void set_smem(K kernel, int bytes) {
 
 // Launch with the K splits of a tile as one cluster and programmatic serialization after the previous grid.
 template <typename K, typename... Args>
-cudaError_t launch_ex(K kernel, int grid, int cluster, int smem, cudaStream_t s, Args... args) {
+cudaError_t launch_ex_n(K kernel, int grid, int threads, int cluster, int smem, cudaStream_t s, Args... args) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute at[2];
@@ -598,6 +952,11 @@ cudaError_t launch_ex(K kernel, int grid, int cluster, int smem, cudaStream_t s,
     cfg.attrs = at;
     cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+template <typename K, typename... Args>
+cudaError_t launch_ex(K kernel, int grid, int cluster, int smem, cudaStream_t s, Args... args) {
+    return launch_ex_n(kernel, grid, kThreads, cluster, smem, s, args...);
 }
 
 }  // namespace
@@ -687,6 +1046,48 @@ cudaError_t launch_down_tc(const TcLaunch &L, cudaStream_t s) {
     static bool cfg = false;
     if (!cfg) set_smem(down_tc_kernel, tc_down_smem()), cfg = true;
     return launch_ex(down_tc_kernel, grid, a.KS, tc_down_smem(), s, *L.mapD, *L.mapH, a);
+}
+
+}  // namespace moe
+
+namespace moe {
+
+cudaError_t launch_ffn_tc(const TcLaunch &L, cudaStream_t s) {
+    const TcAtomLayout l = tc_atom_layout(L.geo.H, L.geo.I);
+    FfnArgs a{};
+    a.bank = L.bank;
+    a.atoms = L.atoms;
+    a.expert_bytes = L.geo.expert_bytes;
+    a.atom_slot_bytes = l.slot_bytes;
+    a.off_g_codes = L.geo.off_wg_codes;
+    a.off_u_codes = L.geo.off_wu_codes;
+    a.off_d_codes = L.geo.off_wd_codes;
+    a.atom_off_g = l.off_g;
+    a.atom_off_u = l.off_u;
+    a.atom_off_d = l.off_d;
+    a.H = L.geo.H;
+    a.I = L.geo.I;
+    a.KS = L.ks_gateup;
+    a.Ucap = L.n_act_max * l.ntI;
+    a.counts = L.counts;
+    a.act_slot = L.act_slot;
+    a.act_off = L.act_off;
+    a.act_cnt = L.act_cnt;
+    a.hot_token = L.hot_token;
+    a.hot_w = L.hot_w;
+    a.xat = L.xat;
+    a.part = L.part;
+    a.err = L.err;
+    if (L.M != 1 || a.KS < 1 || a.KS > kMaxCluster)
+        return cudaErrorInvalidValue;
+    const int grid = L.n_act_max * l.ntI * a.KS;
+    static bool cfg = false;
+    if (!cfg) set_smem(ffn_tc_kernel, tc_gateup_smem()), cfg = true;
+    cudaError_t e = launch_ex_n(ffn_tc_kernel, grid, kFfnThreads, a.KS, tc_gateup_smem(), s, *L.mapG, *L.mapU,
+                                *L.mapX, *L.mapD, a);
+    if (e != cudaSuccess) return e;
+    return launch_ex_n(ffn_combine_kernel, (a.H + kCombineRows - 1) / kCombineRows, 128, 1, 0, s,
+                       (const float *)L.part, L.counts, l.ntI, a.Ucap, a.H, L.out, L.out_f32);
 }
 
 }  // namespace moe

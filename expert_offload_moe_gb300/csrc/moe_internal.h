@@ -65,6 +65,7 @@ struct RouteParams {
     int M, H, E, k, nchunk;
     int all_hot;         // prefill: every expert is hot, slot = expert id
     RouteBuffers b;
+    uint16_t *xmir;      // decode: x copied here by the x-term tasks (the host mirror's source), or nullptr
     uint8_t *xq;         // tensor-core decode: x terms [16][Hpad] and their atoms, or nullptr
     uint8_t *xat;
     int Hpad;
@@ -133,6 +134,7 @@ struct TcLaunch {
     void *out;
     int out_f32;
     const CUtensorMap *mapG, *mapU, *mapX, *mapD, *mapH;
+    float *part;                  // one-launch FFN: down partials [ntH][n_act_max * ntI][128]
 };
 
 int tc_max_splits();  // K splits of a tile run as one thread-block cluster: at most this many
@@ -140,6 +142,9 @@ void launch_build_weight_atoms(const uint8_t *expert, const ExpertGeometry &g, u
 // Both launched with programmatic serialization after the previous grid in the stream.
 cudaError_t launch_gateup_tc(const TcLaunch &L, cudaStream_t s);
 cudaError_t launch_down_tc(const TcLaunch &L, cudaStream_t s);
+// M = 1: gate/up, SiLU and down in one launch, then the fixed-order combine of its partials (both with
+// programmatic serialization after the previous grid).
+cudaError_t launch_ffn_tc(const TcLaunch &L, cudaStream_t s);
 
 // Prefill (M > 8) on the tensor cores over the staged bank (moe_prefill_tc.cu).
 struct PrefillLaunch {

@@ -148,6 +148,14 @@ struct moe_layer {
     float *d_ycold = nullptr;    // [dec_tokens][H] fp32
     cudaEvent_t ev_cold = nullptr;  // the last copy of m_ycold to the device
     void *pinned_block = nullptr;
+    // what moe_route mirrors to the host, laid out identically on the device and in pinned_block, so that
+    // one copy moves it: counts[4], hist[E], cold token/expert/w [dec k] each, x [dec][H] (decode)
+    void *mir_block = nullptr;
+    size_t mir_off_cold = 0, mir_off_x = 0;
+    // under stream capture the mirror copy is a leaf node of the graph; the next moe_route of the layer in the
+    // same capture depends on it (it must have read the route buffers before they are rewritten)
+    cudaGraphNode_t cap_mirror = nullptr;
+    unsigned long long cap_id = 0;
 
     cudaStream_t d2h = nullptr, h2d = nullptr;
     cudaEvent_t ev_fork = nullptr, ev_route = nullptr, ev_fence = nullptr;
@@ -180,6 +188,8 @@ struct moe_layer {
     uint8_t *atoms = nullptr;  // weight scale atoms of every slot [S][atl.slot_bytes]
     uint8_t *xq = nullptr, *xat = nullptr, *hq = nullptr, *hat = nullptr;
     int *err = nullptr;
+    float *part = nullptr;      // one-launch FFN (M = 1): down partials [ntH][n_act(1) ntI][128]
+    bool ffn1 = false;          // M = 1 takes the one-launch FFN (moe_debug_decode_fusion)
     void *tc_block = nullptr;
     CUtensorMap mapG{}, mapU{}, mapD{}, mapX{}, mapH{};
 
@@ -220,6 +230,7 @@ void release(moe_layer *L) {
     cudaFree(L->bias);
     cudaFree(L->e2s_dev);
     cudaFree(L->dev_block);
+    cudaFree(L->mir_block);
     cudaFree(L->h);
     cudaFree(L->cold_block);
     cudaFree(L->tc_block);
@@ -343,11 +354,13 @@ int tc_setup(moe_layer *L, cudaStream_t st) {
     L->Hpad = (H + 127) / 128 * 128;
     L->Ipad = (I + 127) / 128 * 128;
     L->atl = moe::tc_atom_layout(H, I);
+    const size_t ucap1 = (size_t)act_cap(L, 1) * L->atl.ntI;  // units of the one-launch FFN
     const size_t sz[] = {(size_t)moe::kTcXRows * L->Hpad,
                          (size_t)L->atl.nks * moe::kTcAtomBytes,
                          (size_t)L->n_act_cap * moe::kTcHRows * L->Ipad,
                          (size_t)L->n_act_cap * L->atl.nksI * moe::kTcAtomBytes,
-                         sizeof(int)};
+                         sizeof(int),
+                         (size_t)L->atl.ntH * ucap1 * 128 * sizeof(float)};
     size_t total = 0;
     for (size_t s : sz) total += align_up(s, 256);
     cudaError_t e = cudaMalloc(&L->tc_block, total);
@@ -358,7 +371,8 @@ int tc_setup(moe_layer *L, cudaStream_t st) {
                     cudaGetErrorString(e));
     }
     char *p = static_cast<char *>(L->tc_block);
-    void **dst[] = {(void **)&L->xq, (void **)&L->xat, (void **)&L->hq, (void **)&L->hat, (void **)&L->err};
+    void **dst[] = {(void **)&L->xq,  (void **)&L->xat,  (void **)&L->hq,  (void **)&L->hat,
+                    (void **)&L->err, (void **)&L->part};
     for (size_t i = 0; i < sizeof(sz) / sizeof(sz[0]); ++i) {
         *dst[i] = p;
         p += align_up(sz[i], 256);
@@ -576,8 +590,7 @@ int moe_layer_create(const moe_layer_desc *desc, const float *router_w_dev, cons
         (size_t)mt * k * 4, (size_t)mt * k * 4,  // topk ids, w
         nh * 4, nh * 4, nh * 4,                  // hot expert/token/w
         nh * 4, nh * 4, nh * 4, nh * 4,          // act expert/slot/off/cnt
-        nh * 4, nh * 4, nh * 4,                  // cold token/expert/w
-        (size_t)E * 4, 16, 16,                   // hist, counts, arrive
+        16,                                      // arrive
         (size_t)((mt + moe::kPfRouteTok - 1) / moe::kPfRouteTok) * E * 4,  // blk_cnt
         (size_t)mt * k * 4};                     // route_rank
     size_t total = 0;
@@ -588,15 +601,31 @@ int moe_layer_create(const moe_layer_desc *desc, const float *router_w_dev, cons
         void **dst[] = {(void **)&L->rb.logit_part, (void **)&L->rb.topk_ids, (void **)&L->rb.topk_w,
                         (void **)&L->rb.hot_expert, (void **)&L->rb.hot_token, (void **)&L->rb.hot_w,
                         (void **)&L->rb.act_expert, (void **)&L->rb.act_slot, (void **)&L->rb.act_off,
-                        (void **)&L->rb.act_cnt, (void **)&L->rb.cold_token, (void **)&L->rb.cold_expert,
-                        (void **)&L->rb.cold_w, (void **)&L->rb.hist, (void **)&L->rb.counts,
-                        (void **)&L->rb.arrive, (void **)&L->rb.blk_cnt, (void **)&L->rb.route_rank};
+                        (void **)&L->rb.act_cnt, (void **)&L->rb.arrive, (void **)&L->rb.blk_cnt,
+                        (void **)&L->rb.route_rank};
         for (size_t i = 0; i < sizeof(sizes) / sizeof(sizes[0]); ++i) {
             *dst[i] = p;
             p += align_up(sizes[i], 256);
         }
     }
     CREATE_TRY(cudaMemsetAsync(L->dev_block, 0, total, st));
+    // The mirrored arrays: cold routes exist only in decode calls (M <= 8; prefill routes are all hot), so
+    // the cold lists hold dec k entries.
+    const int dec = mt < moe::kDecodeMaxTokens ? mt : moe::kDecodeMaxTokens;
+    const size_t nc = (size_t)dec * k;
+    L->mir_off_cold = align_up(16 + (size_t)E * 4, 16);
+    L->mir_off_x = L->mir_off_cold + 3 * align_up(nc * 4, 16);
+    const size_t mir_bytes = L->mir_off_x + align_up((size_t)dec * H * 2, 16);
+    CREATE_TRY(cudaMalloc(&L->mir_block, mir_bytes));
+    CREATE_TRY(cudaMemsetAsync(L->mir_block, 0, mir_bytes, st));
+    {
+        char *p = static_cast<char *>(L->mir_block);
+        L->rb.counts = (int32_t *)p;
+        L->rb.hist = (int32_t *)(p + 16);
+        L->rb.cold_token = (int32_t *)(p + L->mir_off_cold);
+        L->rb.cold_expert = (int32_t *)(p + L->mir_off_cold + align_up(nc * 4, 16));
+        L->rb.cold_w = (float *)(p + L->mir_off_cold + 2 * align_up(nc * 4, 16));
+    }
     // decode on the tensor cores wherever a full 128-column tile exists along H and I
     if (d.hidden >= 128 && d.inter >= 128) {
         const int rc = tc_setup(L, st);
@@ -606,28 +635,19 @@ int moe_layer_create(const moe_layer_desc *desc, const float *router_w_dev, cons
         }
     }
 
-    // page-locked mirror: counts[4], hist[E], cold token/expert/w [max_hot], then x and the cold sums of the
-    // decode tokens
-    const int dec = mt < moe::kDecodeMaxTokens ? mt : moe::kDecodeMaxTokens;
-    const size_t psz = align_up(16, 64) + align_up((size_t)E * 4, 64) + 3 * align_up(nh * 4, 64) +
-                       align_up((size_t)dec * H * 2, 64) + align_up((size_t)dec * H * 4, 64);
+    // page-locked mirror: the device mirror block's layout, then the cold sums of the decode tokens
+    const size_t psz = align_up(mir_bytes, 64) + align_up((size_t)dec * H * 4, 64);
     CREATE_TRY(cudaHostAlloc(&L->pinned_block, psz, cudaHostAllocDefault));
     memset(L->pinned_block, 0, psz);
     {
         char *p = static_cast<char *>(L->pinned_block);
         L->m_counts = (int32_t *)p;
-        p += align_up(16, 64);
-        L->m_hist = (int32_t *)p;
-        p += align_up((size_t)E * 4, 64);
-        L->m_cold_token = (int32_t *)p;
-        p += align_up(nh * 4, 64);
-        L->m_cold_expert = (int32_t *)p;
-        p += align_up(nh * 4, 64);
-        L->m_cold_w = (float *)p;
-        p += align_up(nh * 4, 64);
-        L->m_x = (uint16_t *)p;
-        p += align_up((size_t)dec * H * 2, 64);
-        L->m_ycold = (float *)p;
+        L->m_hist = (int32_t *)(p + 16);
+        L->m_cold_token = (int32_t *)(p + L->mir_off_cold);
+        L->m_cold_expert = (int32_t *)(p + L->mir_off_cold + align_up(nc * 4, 16));
+        L->m_cold_w = (float *)(p + L->mir_off_cold + 2 * align_up(nc * 4, 16));
+        L->m_x = (uint16_t *)(p + L->mir_off_x);
+        L->m_ycold = (float *)(p + align_up(mir_bytes, 64));
     }
     CREATE_TRY(cudaMalloc(&L->d_ycold, (size_t)dec * H * 4));
 
@@ -672,6 +692,16 @@ int moe_route(moe_layer *L, const void *x_dev, int32_t M, void *stream, moe_rout
     if (reinterpret_cast<uintptr_t>(x_dev) % 16) return fail(MOE_EINVAL, "x_dev must be 16-byte aligned");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int E = L->d.num_experts, k = L->d.top_k;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    unsigned long long cid = 0;
+    CUDA_TRY(cudaStreamGetCaptureInfo(st, &cs, &cid));
+    const bool capturing = cs == cudaStreamCaptureStatusActive;
+    // the previous mirror copy of this layer has read the route buffers before this launch rewrites them
+    if (!capturing) {
+        CUDA_TRY(cudaStreamWaitEvent(st, L->ev_route, 0));
+    } else if (L->cap_mirror && L->cap_id == cid) {
+        CUDA_TRY(cudaStreamUpdateCaptureDependencies(st, &L->cap_mirror, nullptr, 1, cudaStreamAddCaptureDependencies));
+    }
     moe::RouteParams p{};
     p.x = static_cast<const uint16_t *>(x_dev);
     p.Wr = L->Wr;
@@ -690,6 +720,7 @@ int moe_route(moe_layer *L, const void *x_dev, int32_t M, void *stream, moe_rout
         p.xq = L->xq;
         p.xat = L->xat;
         p.Hpad = L->Hpad;
+        p.xmir = reinterpret_cast<uint16_t *>(static_cast<char *>(L->mir_block) + L->mir_off_x);  // and copies x
     }
     if (M > moe::kDecodeMaxTokens && L->pf) {  // the route launch also plans the prefill GEMM tiles
         p.pf_poff = L->pf_poff;
@@ -718,18 +749,38 @@ int moe_route(moe_layer *L, const void *x_dev, int32_t M, void *stream, moe_rout
     }
     CUDA_TRY(prof_mark(L, 0, st));
 
-    // mirror counts, histogram and cold triples to page-locked memory off the compute chain
-    const size_t n = (size_t)M * k;
-    CUDA_TRY(cudaEventRecord(L->ev_fork, st));
-    CUDA_TRY(cudaStreamWaitEvent(L->d2h, L->ev_fork, 0));
-    CUDA_TRY(cudaMemcpyAsync(L->m_counts, L->rb.counts, 16, cudaMemcpyDeviceToHost, L->d2h));
-    CUDA_TRY(cudaMemcpyAsync(L->m_hist, L->rb.hist, (size_t)E * 4, cudaMemcpyDeviceToHost, L->d2h));
-    CUDA_TRY(cudaMemcpyAsync(L->m_cold_token, L->rb.cold_token, n * 4, cudaMemcpyDeviceToHost, L->d2h));
-    CUDA_TRY(cudaMemcpyAsync(L->m_cold_expert, L->rb.cold_expert, n * 4, cudaMemcpyDeviceToHost, L->d2h));
-    CUDA_TRY(cudaMemcpyAsync(L->m_cold_w, L->rb.cold_w, n * 4, cudaMemcpyDeviceToHost, L->d2h));
-    if (M <= moe::kDecodeMaxTokens)  // the host computes cold routes from this copy (moe_forward_cold)
-        CUDA_TRY(cudaMemcpyAsync(L->m_x, x_dev, (size_t)M * L->d.hidden * 2, cudaMemcpyDeviceToHost, L->d2h));
-    CUDA_TRY(cudaEventRecord(L->ev_route, L->d2h));
+    // mirror counts, histogram, cold triples and (decode) x to page-locked memory off the compute chain, in
+    // one copy of the mirror block: a prefill call has only counts and histogram (every route is hot); the
+    // route launch copied x into the block when it wrote the x terms, else x is copied on its own
+    // Nothing on `stream` waits for the copy: the compute chain of the next calls stays kernel after kernel.
+    const bool dec_call = M <= moe::kDecodeMaxTokens;
+    const size_t mbytes = !dec_call ? 16 + (size_t)E * 4 : p.xmir ? L->mir_off_x + (size_t)M * L->d.hidden * 2
+                                                                  : L->mir_off_x;
+    const bool copy_x = dec_call && !p.xmir;  // the host computes cold routes from this copy (moe_forward_cold)
+    if (capturing) {
+        cudaGraph_t g = nullptr;
+        const cudaGraphNode_t *deps = nullptr;
+        const cudaGraphEdgeData *edges = nullptr;
+        size_t nd = 0;
+        CUDA_TRY(cudaStreamGetCaptureInfo(st, &cs, &cid, &g, &deps, &edges, &nd));
+        cudaGraphNode_t node = nullptr;
+        CUDA_TRY(cudaGraphAddMemcpyNode1D(&node, g, deps, nd, L->pinned_block, L->mir_block, mbytes,
+                                          cudaMemcpyDeviceToHost));
+        if (copy_x) {
+            cudaGraphNode_t xn = nullptr;
+            CUDA_TRY(cudaGraphAddMemcpyNode1D(&xn, g, &node, 1, L->m_x, x_dev, (size_t)M * L->d.hidden * 2,
+                                              cudaMemcpyDeviceToHost));
+            node = xn;
+        }
+        L->cap_mirror = node;
+        L->cap_id = cid;
+    } else {
+        CUDA_TRY(cudaEventRecord(L->ev_fork, st));
+        CUDA_TRY(cudaStreamWaitEvent(L->d2h, L->ev_fork, 0));
+        CUDA_TRY(cudaMemcpyAsync(L->pinned_block, L->mir_block, mbytes, cudaMemcpyDeviceToHost, L->d2h));
+        if (copy_x) CUDA_TRY(cudaMemcpyAsync(L->m_x, x_dev, (size_t)M * L->d.hidden * 2, cudaMemcpyDeviceToHost, L->d2h));
+        CUDA_TRY(cudaEventRecord(L->ev_route, L->d2h));
+    }
 
     L->routed_x = x_dev;
     L->routed_M = M;
@@ -807,12 +858,19 @@ int moe_forward_slots(moe_layer *L, const void *x_dev, void *out_dev, int32_t M,
         t.mapX = &L->mapX;
         t.mapD = &L->mapD;
         t.mapH = &L->mapH;
-        CUDA_TRY(prof_mark(L, 1, st));
-        CUDA_TRY(moe::launch_gateup_tc(t, st));
-        CUDA_TRY(prof_mark(L, 1, st));
-        CUDA_TRY(prof_mark(L, 2, st));
-        CUDA_TRY(moe::launch_down_tc(t, st));
-        CUDA_TRY(prof_mark(L, 2, st));
+        t.part = L->part;
+        if (M == 1 && L->ffn1) {  // gate/up, SiLU and down in one launch, then the combine
+            CUDA_TRY(prof_mark(L, 1, st));
+            CUDA_TRY(moe::launch_ffn_tc(t, st));
+            CUDA_TRY(prof_mark(L, 1, st));
+        } else {
+            CUDA_TRY(prof_mark(L, 1, st));
+            CUDA_TRY(moe::launch_gateup_tc(t, st));
+            CUDA_TRY(prof_mark(L, 1, st));
+            CUDA_TRY(prof_mark(L, 2, st));
+            CUDA_TRY(moe::launch_down_tc(t, st));
+            CUDA_TRY(prof_mark(L, 2, st));
+        }
     } else if (M <= moe::kDecodeMaxTokens) {
         p.bank = L->slots;
         CUDA_TRY(prof_mark(L, 1, st));
@@ -877,7 +935,6 @@ int moe_forward_slots(moe_layer *L, const void *x_dev, void *out_dev, int32_t M,
         P.ev[3] = prof_next(L, 2);
         CUDA_TRY(moe::launch_prefill(P, st));
     }
-    CUDA_TRY(cudaStreamWaitEvent(st, L->ev_route, 0));  // join the mirror copies
     return MOE_OK;
 }
 
@@ -1225,6 +1282,12 @@ int moe_debug_check_error(moe_layer *L, int32_t *code) {
     }
     if (code) *code = v;
     return v ? fail(MOE_ETIMEOUT, "a tensor-core kernel gave up a bounded wait (code %d)", v) : MOE_OK;
+}
+
+int moe_debug_decode_fusion(moe_layer *L, int32_t enable) {
+    if (!L) return fail(MOE_EINVAL, "layer is NULL");
+    L->ffn1 = enable != 0;
+    return MOE_OK;
 }
 
 int moe_debug_profile(moe_layer *L, int32_t enable) {

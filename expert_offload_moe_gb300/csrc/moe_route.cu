@@ -220,7 +220,9 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
     for (bool first = true; task < ntask + nq; task += gridDim.x * kWarps, first = false) {
         if (task >= ntask) {
             const int q = task - ntask, nb = H / 32, t = q / nb, b = q - t * nb;
-            float res = __uint_as_float((uint32_t)p.x[(size_t)t * H + b * 32 + lane] << 16);
+            const uint16_t xb = p.x[(size_t)t * H + b * 32 + lane];
+            if (p.xmir) p.xmir[(size_t)t * H + b * 32 + lane] = xb;
+            float res = __uint_as_float((uint32_t)xb << 16);
 #pragma unroll
             for (int term = 0; term < 2; ++term) {
                 uint32_t sb;

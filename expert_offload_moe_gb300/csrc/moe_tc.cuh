@@ -129,6 +129,9 @@ __device__ __forceinline__ void st_shared_u8(void *p, uint32_t v) {
 __device__ __forceinline__ void st_shared_zero16(void *p) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(smem_u32(p)), "r"(0u) : "memory");
 }
+__device__ __forceinline__ void st_shared_fill16(void *p, uint32_t v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
 
 // ------------------------------------------------ thread-block clusters
 

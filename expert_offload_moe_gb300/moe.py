@@ -24,7 +24,7 @@ EXPORTED = [
     "moe_debug_slot_ptr", "moe_debug_inject_fault", "moe_debug_stats", "moe_debug_profile",
     "moe_debug_profile_read", "moe_debug_check_error", "moe_policy_step", "moe_route_noalloc", "moe_forward_cold",
     "moe_forward_cold_gpu", "moe_host_expert_ffn", "moe_policy_step_recency", "moe_layer_set_policy",
-    "moe_layer_set_device_cache", "moe_debug_device_cache",
+    "moe_layer_set_device_cache", "moe_debug_device_cache", "moe_debug_decode_fusion",
 ]
 
 
@@ -92,6 +92,7 @@ def lib():
         L.moe_debug_inject_fault.argtypes = [p, i32]
         L.moe_debug_stats.argtypes = [p, p]
         L.moe_debug_profile.argtypes = [p, i32]
+        L.moe_debug_decode_fusion.argtypes = [p, i32]
         L.moe_debug_profile_read.argtypes = [p, p]
         L.moe_debug_check_error.argtypes = [p, ctypes.POINTER(i32)]
         L.moe_route_noalloc.argtypes = [p, i32, i32, p, p, i32, i32, p, ctypes.POINTER(RouteBuffers), p]
@@ -216,6 +217,9 @@ class Layer:
         """Raises MoeError(MOE_ETIMEOUT) if a tensor-core kernel gave up a bounded wait since the last check."""
         code = ctypes.c_int32(0)
         check(lib().moe_debug_check_error(self.h, ctypes.byref(code)))
+
+    def decode_fusion(self, enable):
+        check(lib().moe_debug_decode_fusion(self.h, 1 if enable else 0))
 
     def profile(self, enable):
         check(lib().moe_debug_profile(self.h, 1 if enable else 0))

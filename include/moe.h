@@ -108,7 +108,8 @@ typedef struct {
 
 /* Result of moe_route.  Device arrays are owned by the layer and stay valid
  * until the next moe_route on the same layer; host arrays are a page-locked
- * mirror, valid once `done` (a cudaEvent_t) has completed. */
+ * mirror, valid once `done` (a cudaEvent_t) has completed (eager calls), or
+ * once the launch of a graph captured from the calls has completed. */
 typedef struct {
     int32_t M;
     /* device */
@@ -132,7 +133,7 @@ typedef struct {
     const int32_t *h_cold_expert;
     const float *h_cold_w;
     const int32_t *h_hist;
-    void *done; /* cudaEvent_t recorded after the mirror copies */
+    void *done; /* cudaEvent_t recorded after the mirror copy (eager calls) */
 } moe_route_result;
 
 /* Creates a layer on the current CUDA device.
@@ -153,8 +154,12 @@ int moe_layer_create(const moe_layer_desc *desc, const float *router_w_dev, cons
 
 /* Routes M tokens: router GEMV, top-k + softmax, slot lookup and compaction,
  * all on `stream` (asynchronous, no host synchronisation, fixed launch
- * shapes: capturable in a CUDA graph).  The mirror copies run on an internal
- * stream forked from `stream`; moe_forward_slots joins it back.
+ * shapes: capturable in a CUDA graph).  One copy moves the host mirror; later
+ * work on `stream` does not wait for it.  Eager calls run it on an internal
+ * stream forked from `stream` (`done` marks its end) and the layer's next
+ * moe_route waits for it.  Under stream capture it becomes a leaf node of the
+ * graph after the route launch, and the layer's next moe_route in the same
+ * capture depends on it.
  *  x_dev  bf16 [M, H] device;  1 <= M <= max_tokens
  *  res    filled with the pointers above (may be NULL)
  * With M > 8 (prefill) every expert is treated as resident in the staging
@@ -328,8 +333,9 @@ int moe_debug_stats(const moe_layer *layer, int64_t stats[4]);
 
 /* Reads and clears the layer's device error word (synchronises the device):
  * 0 = no error; otherwise a tensor-core kernel gave up a bounded wait
- * (1: operand copy, 2: stage release, 3: accumulator) and its output is not
- * valid.  Returns MOE_ETIMEOUT when the word was set, MOE_OK otherwise. */
+ * (1: operand copy, 2: stage release, 3: accumulator; in the one-launch
+ * M = 1 FFN also 4: h operand, 5: down accumulator full, 6: down accumulator
+ * drained) and its output is not valid.  Returns MOE_ETIMEOUT when the word was set, MOE_OK otherwise. */
 int moe_debug_check_error(moe_layer *layer, int32_t *code);
 
 /* Kernel timing for benchmarks: with enable != 0, later route and forward
@@ -337,8 +343,22 @@ int moe_debug_check_error(moe_layer *layer, int32_t *code);
  * the caller's stream (synchronises the device; resets the sums). */
 int moe_debug_profile(moe_layer *layer, int32_t enable);
 
+/* One-token decode (M = 1) on the tensor-core path runs gate/up, SiLU·up
+ * and down of every active expert (tinyserve README "How it works" 2: fused
+ * dequantise-and-multiply, gate / up / down) as ONE kernel launch, followed
+ * by a small launch that adds the weighted per-expert results in a fixed
+ * order, when enable != 0 (off by default: on GB300 the separate gate/up
+ * and down launches finish the step sooner).  Both give
+ * results within the same tolerance of the oracle; they sum the experts'
+ * contributions in different orders, so they are not bit-identical to each
+ * other.  Takes effect at the next moe_forward_slots; no device work.
+ * Errors: MOE_EINVAL (NULL layer). */
+int moe_debug_decode_fusion(moe_layer *layer, int32_t enable);
+
 /* Sums of the timed kernels since moe_debug_profile: out[0] route ms,
- * out[1] gate/up ms, out[2] down ms, out[3] forward calls (waits for the events). */
+ * out[1] gate/up ms (the one-launch FFN and its combine when M = 1 takes
+ * them), out[2] down ms (0 for one-launch calls), out[3] forward calls
+ * (waits for the events). */
 int moe_debug_profile_read(moe_layer *layer, double out[4]);
 
 /* The slot-cache decision on host arrays, as moe_cache_update runs it
