@@ -57,9 +57,8 @@ def parse():
                     help="hot-route hit rate and refills of each slot policy on the drifting decode workload")
     ap.add_argument("--cold-on-gpu", action="store_true",
                     help="decode with the cold routes computed on the GPU from the host bank in place as well")
-    ap.add_argument("--one-launch", action="store_true",
-                    help="M = 1 decode with gate/up, SiLU and down in one launch (then a combine launch) instead of "
-                         "the separate gate/up and down launches")
+    ap.add_argument("--two-launch", action="store_true",
+                    help="M = 1 decode with separate gate/up and down launches instead of the one-launch FFN")
     return ap.parse_args()
 
 
@@ -255,9 +254,9 @@ def run_ours(args):
     st = stack.DecodeStack(w, M=M, n_layers=args.layers, seed=rank, n_inputs=n_inputs,
                            cold_on_gpu=args.cold_on_gpu)
     L = st.L
-    if args.one_launch:
+    if args.two_launch:
         for lay in st.layers:
-            lay.decode_fusion(True)
+            lay.decode_fusion(False)
     st.capture()
     stream = torch.cuda.current_stream()
 

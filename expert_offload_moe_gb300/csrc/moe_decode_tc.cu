@@ -173,9 +173,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t *sA = smem + st * kGateStage;
             uint8_t *sAt = sA + 2 * kTileA + kB;
             const bool tail = ragged && kstep == nks - 1;
-            if (tail) {
-                load_tail_tile(sA, expert + a.off_g_codes, a.I, row0, a.H, kstep);
-                load_tail_tile(sA + kTileA, expert + a.off_u_codes, a.I, row0, a.H, kstep);
+            if (tail) {  // copied without blocking this warp; completion counted on the stage barrier
+                cp_async_tail_tile(sA, expert + a.off_g_codes, a.I, row0, a.H, kstep);
+                cp_async_tail_tile(sA + kTileA, expert + a.off_u_codes, a.I, row0, a.H, kstep);
+                fence_proxy_async();
+                cp_async_arrive(&full[st]);
+                __syncwarp();
             }
             if (lane == 0) {
                 mbar_expect_tx(&full[st], tail ? kTxTail : kTxFull);
@@ -208,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 atom_to_tmem(sfb, sAt + 2 * kAtom);
                 const uint32_t aG = smem_u32(sA), aU = aG + kTileA, aB = aG + 2 * kTileA;
                 const bool tail = ragged && (k0 + i) == nks - 1;
+                if (tail) fence_proxy_async();  // the tail tiles came by cp.async
                 const int nk = tail ? 2 : 4;
                 for (int kk = 0; kk < nk; ++kk) {
                     const int q = kk % kAcc;
@@ -409,7 +413,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t *sA = smem + i * kDownStage;
             const int slot = s_slot[e];
             const bool tail = ragged && s == nksI - 1;
-            if (tail) load_tail_tile(sA, a.bank + (size_t)slot * a.expert_bytes + a.off_d_codes, a.H, row0, a.I, s);
+            if (tail) {
+                cp_async_tail_tile(sA, a.bank + (size_t)slot * a.expert_bytes + a.off_d_codes, a.H, row0, a.I, s);
+                fence_proxy_async();
+                cp_async_arrive(&full[i]);
+                __syncwarp();
+            }
             if (lane == 0) {
                 mbar_expect_tx(&full[i], tail ? kTxTail : kTxFull);
                 if (!tail) tma_load_3d(&mapD, &full[i], sA, s * 128, row0, slot);
@@ -440,7 +449,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t *sAt = sA + kTileA + kB;
             const int slot = s_slot[e];
             const bool tail = ragged && s == nksI - 1;
-            if (tail) load_tail_tile(sA, a.bank + (size_t)slot * a.expert_bytes + a.off_d_codes, a.H, row0, a.I, s);
+            if (tail) {
+                cp_async_tail_tile(sA, a.bank + (size_t)slot * a.expert_bytes + a.off_d_codes, a.H, row0, a.I, s);
+                fence_proxy_async();
+                cp_async_arrive(&full[st]);
+                __syncwarp();
+            }
             if (lane == 0) {
                 mbar_expect_tx(&full[st], tail ? kTxTail : kTxFull);
                 if (!tail) tma_load_3d(&mapD, &full[st], sA, s * 128, row0, slot);
@@ -472,6 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     atom_to_tmem(sfb, sAt + kAtom);
                     const int s = (g0 + i) % nksI;
                     const uint32_t aA = smem_u32(sA), aB = aA + kTileA;
+                    if (ragged && s == nksI - 1) fence_proxy_async();  // the tail tile came by cp.async
                     const int nk = (ragged && s == nksI - 1) ? 2 : 4;
                     for (int kk = 0; kk < nk; ++kk) {
                         const int q = kk % kAcc;
@@ -681,9 +696,12 @@ __global__ void __launch_bounds__(kFfnThreads, 2)
             if (i < ngu) {  // gate/up k-step
                 const int kstep = k0 + i;
                 const bool tail = raggedH && kstep == nks - 1;
-                if (tail) {
-                    load_tail_tile(sA, expert + a.off_g_codes, a.I, row0, a.H, kstep);
-                    load_tail_tile(sA + kTileA, expert + a.off_u_codes, a.I, row0, a.H, kstep);
+                if (tail) {  // copied without blocking this warp; completion counted on the stage barrier
+                    cp_async_tail_tile(sA, expert + a.off_g_codes, a.I, row0, a.H, kstep);
+                    cp_async_tail_tile(sA + kTileA, expert + a.off_u_codes, a.I, row0, a.H, kstep);
+                    fence_proxy_async();
+                    cp_async_arrive(&full[st]);
+                    __syncwarp();
                 }
                 if (lane == 0) {
                     mbar_expect_tx(&full[st], tail ? kTxTail : kTxFull);
@@ -698,10 +716,14 @@ __global__ void __launch_bounds__(kFfnThreads, 2)
                 }
             } else {  // two down tiles: Wd rows of H tile hr, columns of I tile jt
                 const int d0 = 2 * (i - ngu), nt = nd - d0 < 2 ? nd - d0 : 2;
-                if (tailI)
+                if (tailI) {
                     for (int q = 0; q < nt; ++q)
-                        load_tail_tile(sA + q * kTileA, expert + a.off_d_codes, a.H, (ks + KS * (d0 + q)) * 128, a.I,
-                                       jt);
+                        cp_async_tail_tile(sA + q * kTileA, expert + a.off_d_codes, a.H, (ks + KS * (d0 + q)) * 128,
+                                           a.I, jt);
+                    fence_proxy_async();
+                    cp_async_arrive(&full[st]);
+                    __syncwarp();
+                }
                 if (lane == 0) {
                     mbar_expect_tx(&full[st], (uint32_t)nt * ((tailI ? 0u : (uint32_t)kTileATx) + kAtom));
                     for (int q = 0; q < nt; ++q) {
@@ -745,6 +767,7 @@ __global__ void __launch_bounds__(kFfnThreads, 2)
                 atom_to_tmem(sfb, sAt + 2 * kAtom);
                 const uint32_t aG = smem_u32(sA), aU = aG + kTileA, aB = aG + 2 * kTileA;
                 const int nk = (raggedH && (k0 + i) == nks - 1) ? 2 : 4;
+                if (nk == 2) fence_proxy_async();  // the tail tiles came by cp.async
                 for (int kk = 0; kk < nk; ++kk) {
                     const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
                     mma_mx(tDg, sw128_desc(aG + kk * 32), sw128_desc(aB + kk * 32), idesc, kk, sfg, sfb, acc);
@@ -769,6 +792,7 @@ __global__ void __launch_bounds__(kFfnThreads, 2)
                 tc_fence_after();
                 uint8_t *sA = smem + st * kGateStage;
                 const int d0 = 2 * ds, nt = nd - d0 < 2 ? nd - d0 : 2;
+                if (tailI) fence_proxy_async();  // the tail tiles came by cp.async
                 for (int q = 0; q < nt && ok; ++q) {
                     const int ti = d0 + q, buf = ti & 1;
                     if (ti >= 2) ok = mbar_wait(&acc_empty[buf], ((ti >> 1) - 1) & 1, a.err, kErrAccEmpty);

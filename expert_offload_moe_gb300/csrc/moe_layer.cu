@@ -189,7 +189,7 @@ struct moe_layer {
     uint8_t *xq = nullptr, *xat = nullptr, *hq = nullptr, *hat = nullptr;
     int *err = nullptr;
     float *part = nullptr;      // one-launch FFN (M = 1): down partials [ntH][n_act(1) ntI][128]
-    bool ffn1 = false;          // M = 1 takes the one-launch FFN (moe_debug_decode_fusion)
+    bool ffn1 = true;           // M = 1 takes the one-launch FFN (moe_debug_decode_fusion)
     void *tc_block = nullptr;
     CUtensorMap mapG{}, mapU{}, mapD{}, mapX{}, mapH{};
 

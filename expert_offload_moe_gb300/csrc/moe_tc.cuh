@@ -391,5 +391,37 @@ __device__ __forceinline__ void load_tail_tile(uint8_t *dst, const uint8_t *code
     __syncwarp();
 }
 
+// 8 bytes global -> shared by this thread (cp.async, generic proxy); both addresses 8-byte aligned.
+__device__ __forceinline__ void cp_async8(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+// One arrival on bar once all of this thread's earlier cp.async copies have landed.  The barrier's pending
+// count is raised by one when this is issued, so a barrier initialised for its other arrivals needs no
+// change; issue it before the arrival that could otherwise complete the phase.
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// load_tail_tile without waiting for the loads: the 8 code bytes of unit u of row r go to 16-byte chunk
+// u ^ (r % 8) by cp.async, the chunk's other 8 bytes (and whole chunks of rows past the matrix) are zeroed
+// by stores.  The caller then runs fence_proxy_async() and cp_async_arrive() on the stage barrier in every
+// lane; the consumer runs fence_proxy_async() after its wait, before the tensor cores read the tile.
+__device__ __forceinline__ void cp_async_tail_tile(uint8_t *dst, const uint8_t *codes, int rows, int row0, int K,
+                                                   int kstep) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int i = lane + 32 * j, r = i / 4, u = i % 4;
+        uint8_t *d = dst + r * 128 + ((u ^ (r & 7)) * 16);
+        if (row0 + r < rows) {
+            cp_async8(d, codes + (size_t)(row0 + r) * (K / 2) + kstep * 64 + u * 8);
+            asm volatile("st.shared.v2.u32 [%0], {%1, %1};" ::"r"(smem_u32(d + 8)), "r"(0u) : "memory");
+        } else {
+            st_shared_zero16(d);
+        }
+    }
+}
+
 }  // namespace tc
 }  // namespace moe

@@ -347,8 +347,8 @@ int moe_debug_profile(moe_layer *layer, int32_t enable);
  * and down of every active expert (tinyserve README "How it works" 2: fused
  * dequantise-and-multiply, gate / up / down) as ONE kernel launch, followed
  * by a small launch that adds the weighted per-expert results in a fixed
- * order, when enable != 0 (off by default: on GB300 the separate gate/up
- * and down launches finish the step sooner).  Both give
+ * order (on by default); enable == 0 makes moe_forward_slots use the
+ * separate gate/up and down launches instead (for comparison).  Both give
  * results within the same tolerance of the oracle; they sum the experts'
  * contributions in different orders, so they are not bit-identical to each
  * other.  Takes effect at the next moe_forward_slots; no device work.
