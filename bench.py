@@ -322,9 +322,9 @@ def run_ours(args):
     pk, pk_src = peaks()
     hbm_peak = pk.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"])
     src = os.path.join(ROOT, "expert_offload_moe_gb300", "csrc", "moe_decode_tc.cu")
-    if down_us == 0.0:  # one launch per layer: gate/up, SiLU, down and combine (every expert byte read)
+    if M == 1 and not args.two_launch:  # gate/up, SiLU and down in one launch (every expert byte), then combine
         kernel, kbytes = "ffn_tc_kernel", mean_act * w.expert_bytes
-        kernel_us = {"route": route_us, "ffn": gateup_us}
+        kernel_us = {"route": route_us, "ffn": gateup_us, "combine": down_us}
         traffic = traffic_for(src, "ffn_tc_gptoss20b_traffic.txt")
     else:
         kernel, kbytes = "gateup_tc_kernel", gateup_bytes

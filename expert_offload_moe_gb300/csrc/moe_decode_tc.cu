@@ -1107,11 +1107,14 @@ cudaError_t launch_ffn_tc(const TcLaunch &L, cudaStream_t s) {
     const int grid = L.n_act_max * l.ntI * a.KS;
     static bool cfg = false;
     if (!cfg) set_smem(ffn_tc_kernel, tc_gateup_smem()), cfg = true;
-    cudaError_t e = launch_ex_n(ffn_tc_kernel, grid, kFfnThreads, a.KS, tc_gateup_smem(), s, *L.mapG, *L.mapU,
-                                *L.mapX, *L.mapD, a);
-    if (e != cudaSuccess) return e;
-    return launch_ex_n(ffn_combine_kernel, (a.H + kCombineRows - 1) / kCombineRows, 128, 1, 0, s,
-                       (const float *)L.part, L.counts, l.ntI, a.Ucap, a.H, L.out, L.out_f32);
+    return launch_ex_n(ffn_tc_kernel, grid, kFfnThreads, a.KS, tc_gateup_smem(), s, *L.mapG, *L.mapU, *L.mapX,
+                       *L.mapD, a);
+}
+
+cudaError_t launch_ffn_combine(const TcLaunch &L, cudaStream_t s) {
+    const TcAtomLayout l = tc_atom_layout(L.geo.H, L.geo.I);
+    return launch_ex_n(ffn_combine_kernel, (L.geo.H + kCombineRows - 1) / kCombineRows, 128, 1, 0, s,
+                       (const float *)L.part, L.counts, l.ntI, L.n_act_max * l.ntI, L.geo.H, L.out, L.out_f32);
 }
 
 }  // namespace moe

@@ -142,9 +142,10 @@ void launch_build_weight_atoms(const uint8_t *expert, const ExpertGeometry &g, u
 // Both launched with programmatic serialization after the previous grid in the stream.
 cudaError_t launch_gateup_tc(const TcLaunch &L, cudaStream_t s);
 cudaError_t launch_down_tc(const TcLaunch &L, cudaStream_t s);
-// M = 1: gate/up, SiLU and down in one launch, then the fixed-order combine of its partials (both with
-// programmatic serialization after the previous grid).
+// M = 1: gate/up, SiLU and down in one launch (launch_ffn_tc), then the fixed-order combine of its partials
+// (launch_ffn_combine), both with programmatic serialization after the previous grid.
 cudaError_t launch_ffn_tc(const TcLaunch &L, cudaStream_t s);
+cudaError_t launch_ffn_combine(const TcLaunch &L, cudaStream_t s);
 
 // Prefill (M > 8) on the tensor cores over the staged bank (moe_prefill_tc.cu).
 struct PrefillLaunch {

@@ -863,6 +863,9 @@ int moe_forward_slots(moe_layer *L, const void *x_dev, void *out_dev, int32_t M,
             CUDA_TRY(prof_mark(L, 1, st));
             CUDA_TRY(moe::launch_ffn_tc(t, st));
             CUDA_TRY(prof_mark(L, 1, st));
+            CUDA_TRY(prof_mark(L, 2, st));
+            CUDA_TRY(moe::launch_ffn_combine(t, st));
+            CUDA_TRY(prof_mark(L, 2, st));
         } else {
             CUDA_TRY(prof_mark(L, 1, st));
             CUDA_TRY(moe::launch_gateup_tc(t, st));

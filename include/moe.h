@@ -356,9 +356,9 @@ int moe_debug_profile(moe_layer *layer, int32_t enable);
 int moe_debug_decode_fusion(moe_layer *layer, int32_t enable);
 
 /* Sums of the timed kernels since moe_debug_profile: out[0] route ms,
- * out[1] gate/up ms (the one-launch FFN and its combine when M = 1 takes
- * them), out[2] down ms (0 for one-launch calls), out[3] forward calls
- * (waits for the events). */
+ * out[1] gate/up ms (the one-launch FFN when M = 1 takes it), out[2] down
+ * ms (its combine launch for one-launch calls), out[3] forward calls (waits
+ * for the events). */
 int moe_debug_profile_read(moe_layer *layer, double out[4]);
 
 /* The slot-cache decision on host arrays, as moe_cache_update runs it
