@@ -29,6 +29,11 @@ Codes are row-major; byte ``c`` of a row holds column ``2c`` in its low nibble
 and column ``2c+1`` in its high nibble.  Scale byte ``b`` of a row covers
 columns ``[32b, 32b+32)``.
 
+NVFP4 records (``weight_format=1``) have the same codes and one E4M3 scale byte
+per 16 columns (``expert_bytes = 3 * I * H * 9 / 16``); scale bytes are
+positive normal E4M3 values with exponent field uniform over {1, ..., 7} and
+mantissa uniform, i.e. between 2^-6 and 1.875, a range like the MXFP4 scales'.
+
 Seeds follow ``SeedSequence([seed, layer, tensor_id, step])``.
 """
 from __future__ import annotations
@@ -57,10 +62,11 @@ class Workload:
     bias_tau: float = 0.0
     prefill_tokens: int = 0
     drift: bool = False  # bias drifts between two popularity orders over the steps
+    weight_format: int = 0  # 0 = MXFP4, 1 = NVFP4
 
     @property
     def expert_bytes(self) -> int:
-        return expert_bytes(self.hidden, self.inter)
+        return expert_bytes(self.hidden, self.inter, self.weight_format)
 
 
 WORKLOADS = {
@@ -77,18 +83,24 @@ WORKLOADS = {
         # gpt-oss shape: 2048-token prefill, then decode with 16 of 32 slots and LFU refill
         Workload("gptoss20b_prefill2048_s16_lfu_drift", 24, 2880, 2880, 32, 4, 16, (1,), 256,
                  bias_tau=0.25, prefill_tokens=2048, drift=True),
+        # the gpt-oss decode stack with NVFP4 experts (16-element E4M3 scales)
+        Workload("gptoss20b_h2880_e32k4_resident_m1_nvfp4", 24, 2880, 2880, 32, 4, 32, (1,), 512, weight_format=1),
     ]
 }
 
 
-def expert_bytes(hidden: int, inter: int) -> int:
-    return 3 * inter * hidden * 17 // 32
+def scale_block(weight_format: int = 0) -> int:
+    return 16 if weight_format == 1 else 32
 
 
-def section_offsets(hidden: int, inter: int) -> dict:
+def expert_bytes(hidden: int, inter: int, weight_format: int = 0) -> int:
+    return 3 * inter * hidden // 2 + 3 * inter * hidden // scale_block(weight_format)
+
+
+def section_offsets(hidden: int, inter: int, weight_format: int = 0) -> dict:
     """Byte offsets of the six sections of one expert record."""
     gc = inter * hidden // 2
-    gs = inter * hidden // 32
+    gs = inter * hidden // scale_block(weight_format)
     off = {}
     o = 0
     for name, size in (("wg_codes", gc), ("wg_scales", gs), ("wu_codes", gc), ("wu_scales", gs),
@@ -162,11 +174,12 @@ def expert_to_slot_by_rank(seed: int, layer: int, E: int, S: int, order: int = 0
     return np.where(rank < S, rank, -1).astype(np.int32)
 
 
-def fill_expert_records(out: np.ndarray, seed: int, layer: int, H: int, I: int, first: int = 0) -> None:
+def fill_expert_records(out: np.ndarray, seed: int, layer: int, H: int, I: int, first: int = 0,
+                        weight_format: int = 0) -> None:
     """Fill ``out`` ([n, expert_bytes] uint8) with experts first..first+n-1 of a layer."""
-    eb = expert_bytes(H, I)
+    eb = expert_bytes(H, I, weight_format)
     assert out.ndim == 2 and out.shape[1] == eb and out.dtype == np.uint8
-    offs = section_offsets(H, I)
+    offs = section_offsets(H, I, weight_format)
     for j in range(out.shape[0]):
         e = first + j
         raw = _bits(seed, layer, T_EXPERTS, e).random_raw((eb + 7) // 8).view(np.uint8)[:eb]
@@ -174,15 +187,18 @@ def fill_expert_records(out: np.ndarray, seed: int, layer: int, H: int, I: int, 
         rec[:] = raw
         for name in ("wg_scales", "wu_scales", "wd_scales"):
             o, n = offs[name]
-            rec[o:o + n] = (rec[o:o + n] & 7) + 120
+            if weight_format == 1:  # E4M3: exponent field 1..7, any mantissa, sign 0
+                rec[o:o + n] = (((rec[o:o + n] >> 3) % 7 + 1) << 3) | (rec[o:o + n] & 7)
+            else:
+                rec[o:o + n] = (rec[o:o + n] & 7) + 120
 
 
-def expert_records(seed: int, layer: int, E: int, H: int, I: int, experts=None) -> np.ndarray:
+def expert_records(seed: int, layer: int, E: int, H: int, I: int, experts=None, weight_format: int = 0) -> np.ndarray:
     """[n, expert_bytes] uint8 records for the listed experts (default: all E)."""
     ids = list(range(E)) if experts is None else list(experts)
-    out = np.empty((len(ids), expert_bytes(H, I)), dtype=np.uint8)
+    out = np.empty((len(ids), expert_bytes(H, I, weight_format)), dtype=np.uint8)
     for j, e in enumerate(ids):
-        fill_expert_records(out[j:j + 1], seed, layer, H, I, first=e)
+        fill_expert_records(out[j:j + 1], seed, layer, H, I, first=e, weight_format=weight_format)
     return out
 
 
@@ -194,7 +210,7 @@ def zipf_expected_hit_rate(E: int, S: int, tau: float) -> float:
 
 
 __all__ = [
-    "Workload", "WORKLOADS", "expert_bytes", "section_offsets", "bf16_bits_rne", "activations",
+    "Workload", "WORKLOADS", "scale_block", "expert_bytes", "section_offsets", "bf16_bits_rne", "activations",
     "router_weights", "popularity_rank", "router_bias", "drifting_bias", "expert_to_slot_by_rank",
     "fill_expert_records", "expert_records", "zipf_log_popularity", "zipf_expected_hit_rate",
 ]

@@ -52,6 +52,13 @@ def _declare(L):
     L.oracle_f32_to_bf16.argtypes, L.oracle_f32_to_bf16.restype = [F32], ctypes.c_uint16
     L.oracle_mxfp4_dequant.argtypes = [P, P, I32, I32, P]
     L.oracle_mxfp4_dequant.restype = None
+    L.oracle_nvfp4_dequant.argtypes = [P, P, I32, I32, P]
+    L.oracle_nvfp4_dequant.restype = None
+    L.oracle_expert_bytes_fmt.argtypes, L.oracle_expert_bytes_fmt.restype = [I32, I32, I32], ctypes.c_size_t
+    L.oracle_expert_ffn_fmt.argtypes = [P, I32, I32, I32, P, P]
+    L.oracle_expert_ffn_fmt.restype = None
+    L.oracle_moe_layer_fmt.argtypes = [P, I32, I32, I32, I32, I32, I32, P, P, P, P, P, P] + [P] * 16
+    L.oracle_moe_layer_fmt.restype = None
     L.oracle_router_logits.argtypes = [P, I32, I32, P, P, I32, P]
     L.oracle_router_logits.restype = None
     L.oracle_topk_softmax.argtypes = [P, I32, I32, I32, P, P]
@@ -112,6 +119,20 @@ def mxfp4_dequant(codes, scales, R, C):
     W = np.empty((R, C), dtype=np.float32)
     lib().oracle_mxfp4_dequant(_p(codes), _p(scales), R, C, _p(W))
     return W
+
+
+def nvfp4_dequant(codes, scales, R, C):
+    codes, scales = _c(codes, np.uint8), _c(scales, np.uint8)
+    W = np.empty((R, C), dtype=np.float32)
+    lib().oracle_nvfp4_dequant(_p(codes), _p(scales), R, C, _p(W))
+    return W
+
+
+FORMATS = {"mxfp4": 0, "nvfp4": 1}
+
+
+def expert_bytes(H, I, fmt="mxfp4"):
+    return int(lib().oracle_expert_bytes_fmt(H, I, FORMATS[fmt]))
 
 
 def router_logits(x_bf16, Wr, bias=None):
@@ -179,10 +200,10 @@ def expert_down(rec, H, I, h):
     return y
 
 
-def expert_ffn(rec, H, I, x_row):
+def expert_ffn(rec, H, I, x_row, fmt="mxfp4"):
     rec, x = _c(rec, np.uint8), _c(x_row, np.uint16)
     y = np.empty(H, dtype=np.float32)
-    lib().oracle_expert_ffn(_p(rec), H, I, _p(x), _p(y))
+    lib().oracle_expert_ffn_fmt(_p(rec), H, I, FORMATS[fmt], _p(x), _p(y))
     return y
 
 
@@ -193,8 +214,8 @@ def expert_ffn_mxfp8(rec, H, I, x_row):
     return y
 
 
-def moe_layer(x_bf16, Wr, bias, experts, e2s, k, H, I):
-    """Whole layer.  ``experts``: [E, expert_bytes] uint8 indexed by expert id."""
+def moe_layer(x_bf16, Wr, bias, experts, e2s, k, H, I, fmt="mxfp4"):
+    """Whole layer.  ``experts``: [E, expert_bytes] uint8 indexed by expert id; ``fmt``: "mxfp4" / "nvfp4"."""
     x = _c(x_bf16, np.uint16)
     Wr = _c(Wr, np.float32)
     b = None if bias is None else _c(bias, np.float32)
@@ -215,7 +236,7 @@ def moe_layer(x_bf16, Wr, bias, experts, e2s, k, H, I):
     r["cold_w"] = np.zeros(n, dtype=np.float32)
     r["hist"] = np.zeros(E, dtype=np.int32)
     counts = np.zeros(3, dtype=np.int32)
-    lib().oracle_moe_layer(_p(x), M, H, I, E, k, _p(Wr), _p(b), _p(experts), _p(e2s), _p(out_f32),
+    lib().oracle_moe_layer_fmt(_p(x), M, H, I, E, k, FORMATS[fmt], _p(Wr), _p(b), _p(experts), _p(e2s), _p(out_f32),
                            _p(out_bf16), _p(ids), _p(w), _p(r["hot_expert"]), _p(r["hot_slot"]),
                            _p(r["hot_token"]), _p(r["hot_w"]), _p(r["act_expert"]), _p(r["act_slot"]),
                            _p(r["act_off"]), _p(r["act_cnt"]), _p(r["cold_token"]), _p(r["cold_expert"]),

@@ -22,6 +22,10 @@
  *    the pages (xinfer "Supported": FusedMoeMxfp4; tinyserve README: native
  *    MXFP4) but not defined there; the OCP Microscaling Formats (MX) v1.0
  *    definition is used.
+ *  - NVFP4 is named by the pages (xinfer docs: NVFP4 checkpoints, "NVFP4 on
+ *    SM100+" not supported there) but not defined; NVIDIA's block format is
+ *    used: the same E2M1 elements with one E4M3 scale per 16 elements.  The
+ *    pages give no per-tensor scale, so none is applied (a factor of 1).
  *  - The pages define no router or FFN formula.  The plain reading used here:
  *    logits = x.Wr^T + b; the k largest logits (ties to the lower expert id);
  *    softmax over the k selected logits; expert FFN
@@ -81,17 +85,43 @@ float oracle_mxfp4_element(const uint8_t *codes, const uint8_t *scales, int C, i
     return oracle_e2m1(code) * oracle_e8m0(sc);
 }
 
+/* One NVFP4 matrix [R, C]: codes [R, C/2] as in MXFP4, scales [R, C/16], each
+ * an E4M3 byte (oracle_e4m3, below) for 16 consecutive columns. */
+float oracle_e4m3(uint8_t code);
+float oracle_nvfp4_element(const uint8_t *codes, const uint8_t *scales, int C, int r, int c) {
+    uint8_t byte = codes[(size_t)r * (C / 2) + c / 2];
+    uint8_t code = (c & 1) ? (byte >> 4) : (byte & 15);
+    uint8_t sc = scales[(size_t)r * (C / 16) + c / 16];
+    return oracle_e2m1(code) * oracle_e4m3(sc);
+}
+
+void oracle_nvfp4_dequant(const uint8_t *codes, const uint8_t *scales, int R, int C, float *W) {
+    for (int r = 0; r < R; ++r)
+        for (int c = 0; c < C; ++c) W[(size_t)r * C + c] = oracle_nvfp4_element(codes, scales, C, r, c);
+}
+
 void oracle_mxfp4_dequant(const uint8_t *codes, const uint8_t *scales, int R, int C, float *W) {
     for (int r = 0; r < R; ++r)
         for (int c = 0; c < C; ++c) W[(size_t)r * C + c] = oracle_mxfp4_element(codes, scales, C, r, c);
 }
 
-/* Expert record: [Wg codes, Wg scales, Wu codes, Wu scales, Wd codes, Wd scales]. */
-size_t oracle_expert_bytes(int H, int I) { return (size_t)3 * I * H * 17 / 32; }
+/* Expert record: [Wg codes, Wg scales, Wu codes, Wu scales, Wd codes, Wd scales].
+ * fmt 0 = MXFP4 (a scale per 32 elements), 1 = NVFP4 (a scale per 16). */
+static int scale_block(int fmt) { return fmt == 1 ? 16 : 32; }
 
-static void expert_sections(const uint8_t *rec, int H, int I, const uint8_t **gc, const uint8_t **gs,
+size_t oracle_expert_bytes_fmt(int H, int I, int fmt) {
+    return (size_t)3 * I * H / 2 + (size_t)3 * I * H / scale_block(fmt);
+}
+
+size_t oracle_expert_bytes(int H, int I) { return oracle_expert_bytes_fmt(H, I, 0); }
+
+static float element(int fmt, const uint8_t *codes, const uint8_t *scales, int C, int r, int c) {
+    return fmt == 1 ? oracle_nvfp4_element(codes, scales, C, r, c) : oracle_mxfp4_element(codes, scales, C, r, c);
+}
+
+static void expert_sections(const uint8_t *rec, int H, int I, int fmt, const uint8_t **gc, const uint8_t **gs,
                             const uint8_t **uc, const uint8_t **us, const uint8_t **dc, const uint8_t **ds) {
-    size_t c = (size_t)I * H / 2, s = (size_t)I * H / 32;
+    size_t c = (size_t)I * H / 2, s = (size_t)I * H / scale_block(fmt);
     *gc = rec;
     *gs = rec + c;
     *uc = rec + c + s;
@@ -198,36 +228,48 @@ void oracle_compact(const int32_t *ids, const float *w, int M, int k, const int3
 static float silu(float g) { return g / (1.0f + expf(-g)); }
 
 /* h[i] = SiLU(sum_c Wg[i,c] x[c]) * (sum_c Wu[i,c] x[c]), fp32, ascending c. */
-void oracle_expert_gate_up(const uint8_t *rec, int H, int I, const uint16_t *x, float *h) {
+void oracle_expert_gate_up_fmt(const uint8_t *rec, int H, int I, int fmt, const uint16_t *x, float *h) {
     const uint8_t *gc, *gs, *uc, *us, *dc, *ds;
-    expert_sections(rec, H, I, &gc, &gs, &uc, &us, &dc, &ds);
+    expert_sections(rec, H, I, fmt, &gc, &gs, &uc, &us, &dc, &ds);
     for (int i = 0; i < I; ++i) {
         float g = 0.0f, u = 0.0f;
         for (int c = 0; c < H; ++c) {
             float xc = oracle_bf16_to_f32(x[c]);
-            g = g + oracle_mxfp4_element(gc, gs, H, i, c) * xc;
-            u = u + oracle_mxfp4_element(uc, us, H, i, c) * xc;
+            g = g + element(fmt, gc, gs, H, i, c) * xc;
+            u = u + element(fmt, uc, us, H, i, c) * xc;
         }
         h[i] = silu(g) * u;
     }
 }
 
 /* y[r] = sum_i Wd[r,i] h[i], fp32, ascending i. */
-void oracle_expert_down(const uint8_t *rec, int H, int I, const float *h, float *y) {
+void oracle_expert_down_fmt(const uint8_t *rec, int H, int I, int fmt, const float *h, float *y) {
     const uint8_t *gc, *gs, *uc, *us, *dc, *ds;
-    expert_sections(rec, H, I, &gc, &gs, &uc, &us, &dc, &ds);
+    expert_sections(rec, H, I, fmt, &gc, &gs, &uc, &us, &dc, &ds);
     for (int r = 0; r < H; ++r) {
         float acc = 0.0f;
-        for (int i = 0; i < I; ++i) acc = acc + oracle_mxfp4_element(dc, ds, I, r, i) * h[i];
+        for (int i = 0; i < I; ++i) acc = acc + element(fmt, dc, ds, I, r, i) * h[i];
         y[r] = acc;
     }
 }
 
-void oracle_expert_ffn(const uint8_t *rec, int H, int I, const uint16_t *x, float *y) {
+void oracle_expert_ffn_fmt(const uint8_t *rec, int H, int I, int fmt, const uint16_t *x, float *y) {
     float *h = (float *)malloc(sizeof(float) * (size_t)I);
-    oracle_expert_gate_up(rec, H, I, x, h);
-    oracle_expert_down(rec, H, I, h, y);
+    oracle_expert_gate_up_fmt(rec, H, I, fmt, x, h);
+    oracle_expert_down_fmt(rec, H, I, fmt, h, y);
     free(h);
+}
+
+void oracle_expert_gate_up(const uint8_t *rec, int H, int I, const uint16_t *x, float *h) {
+    oracle_expert_gate_up_fmt(rec, H, I, 0, x, h);
+}
+
+void oracle_expert_down(const uint8_t *rec, int H, int I, const float *h, float *y) {
+    oracle_expert_down_fmt(rec, H, I, 0, h, y);
+}
+
+void oracle_expert_ffn(const uint8_t *rec, int H, int I, const uint16_t *x, float *y) {
+    oracle_expert_ffn_fmt(rec, H, I, 0, x, y);
 }
 
 /* ------------------------------------------------------------ whole layer */
@@ -238,13 +280,13 @@ void oracle_expert_ffn(const uint8_t *rec, int H, int I, const uint16_t *x, floa
  * out_f32[t, :] = sum over t's hot routes, ascending expert, of w * y;
  * a token without hot routes gets zeros.  Also returns the routing and the
  * compaction (arrays sized M*k, E, and 3 for counts). */
-void oracle_moe_layer(const uint16_t *x, int M, int H, int I, int E, int k, const float *Wr,
-                      const float *bias, const uint8_t *experts, const int32_t *e2s, float *out_f32,
-                      uint16_t *out_bf16, int32_t *ids, float *w, int32_t *hot_expert, int32_t *hot_slot,
-                      int32_t *hot_token, float *hot_w, int32_t *act_expert, int32_t *act_slot,
-                      int32_t *act_off, int32_t *act_cnt, int32_t *cold_token, int32_t *cold_expert,
-                      float *cold_w, int32_t *hist, int32_t *counts, float *logits_out) {
-    size_t eb = oracle_expert_bytes(H, I);
+void oracle_moe_layer_fmt(const uint16_t *x, int M, int H, int I, int E, int k, int fmt, const float *Wr,
+                          const float *bias, const uint8_t *experts, const int32_t *e2s, float *out_f32,
+                          uint16_t *out_bf16, int32_t *ids, float *w, int32_t *hot_expert, int32_t *hot_slot,
+                          int32_t *hot_token, float *hot_w, int32_t *act_expert, int32_t *act_slot,
+                          int32_t *act_off, int32_t *act_cnt, int32_t *cold_token, int32_t *cold_expert,
+                          float *cold_w, int32_t *hist, int32_t *counts, float *logits_out) {
+    size_t eb = oracle_expert_bytes_fmt(H, I, fmt);
     float *logits = (float *)malloc(sizeof(float) * (size_t)M * E);
     oracle_router_logits(x, M, H, Wr, bias, E, logits);
     if (logits_out) memcpy(logits_out, logits, sizeof(float) * (size_t)M * E);
@@ -255,13 +297,24 @@ void oracle_moe_layer(const uint16_t *x, int M, int H, int I, int E, int k, cons
     float *y = (float *)malloc(sizeof(float) * (size_t)H);
     for (int r = 0; r < counts[0]; ++r) {
         int t = hot_token[r];
-        oracle_expert_ffn(experts + (size_t)hot_expert[r] * eb, H, I, x + (size_t)t * H, y);
+        oracle_expert_ffn_fmt(experts + (size_t)hot_expert[r] * eb, H, I, fmt, x + (size_t)t * H, y);
         for (int c = 0; c < H; ++c) out_f32[(size_t)t * H + c] = out_f32[(size_t)t * H + c] + hot_w[r] * y[c];
     }
     if (out_bf16)
         for (size_t i = 0; i < (size_t)M * H; ++i) out_bf16[i] = oracle_f32_to_bf16(out_f32[i]);
     free(y);
     free(logits);
+}
+
+void oracle_moe_layer(const uint16_t *x, int M, int H, int I, int E, int k, const float *Wr,
+                      const float *bias, const uint8_t *experts, const int32_t *e2s, float *out_f32,
+                      uint16_t *out_bf16, int32_t *ids, float *w, int32_t *hot_expert, int32_t *hot_slot,
+                      int32_t *hot_token, float *hot_w, int32_t *act_expert, int32_t *act_slot,
+                      int32_t *act_off, int32_t *act_cnt, int32_t *cold_token, int32_t *cold_expert,
+                      float *cold_w, int32_t *hist, int32_t *counts, float *logits_out) {
+    oracle_moe_layer_fmt(x, M, H, I, E, k, 0, Wr, bias, experts, e2s, out_f32, out_bf16, ids, w, hot_expert,
+                         hot_slot, hot_token, hot_w, act_expert, act_slot, act_off, act_cnt, cold_token,
+                         cold_expert, cold_w, hist, counts, logits_out);
 }
 
 /* --------------------------------------------------------------- slot cache */
@@ -512,7 +565,7 @@ uint8_t oracle_mxfp8_block(const float *v, int n, uint8_t *codes) {
  * the products of two decoded values are exact and summed in fp32. */
 void oracle_expert_ffn_mxfp8(const uint8_t *rec, int H, int I, const uint16_t *x, float *y) {
     const uint8_t *gc, *gs, *uc, *us, *dc, *ds;
-    expert_sections(rec, H, I, &gc, &gs, &uc, &us, &dc, &ds);
+    expert_sections(rec, H, I, 0, &gc, &gs, &uc, &us, &dc, &ds);
     float *xq = (float *)malloc(sizeof(float) * (size_t)H);
     float *h = (float *)malloc(sizeof(float) * (size_t)I);
     float *hq = (float *)malloc(sizeof(float) * (size_t)I);

@@ -566,3 +566,85 @@ def test_demand_lru_invariants_on_random_steps(oracle_lib):
             assert all(rp.e2s[e] >= 0 for e in routed), st
         # stamps: every slot used this step carries the step
         assert all(rp.stamp[rp.e2s[e]] == st for e in routed if rp.e2s[e] >= 0), st
+
+
+# --------------------------------------------------------------------- NVFP4
+
+
+def decode_nvfp4_np(codes, scales, R, C):
+    """float64 decode of an NVFP4 matrix from bit fields: E2M1 codes (low nibble first), one E4M3 scale per
+    16 columns, both decoded by this file's bit-field decoders (pinned to the OCP fixtures above)."""
+    codes = codes.reshape(R, C // 2)
+    q = np.empty((R, C), dtype=np.int64)
+    q[:, 0::2] = codes & 15
+    q[:, 1::2] = codes >> 4
+    mag = np.vectorize(e2m1_from_bits)(q)
+    sc = np.vectorize(e4m3_from_bits)(scales.reshape(R, C // 16).astype(np.int64))
+    return mag * np.repeat(sc, 16, axis=1)
+
+
+def test_nvfp4_exhaustive_codes_times_e4m3_scales(oracle_lib):
+    # every (code, scale byte) pair: element = E2M1(code) * E4M3(scale), NaN scales give NaN
+    codes = np.array([(2 * j) | ((2 * j + 1) << 4) for j in range(8)], dtype=np.uint8)  # codes 0..15, one row
+    for sb in range(256):
+        scales = np.array([sb], dtype=np.uint8)
+        W = oracle_lib.nvfp4_dequant(codes, scales, 1, 16)[0]
+        for c in range(16):
+            ref = e2m1_from_bits(c) * e4m3_from_bits(sb)
+            assert (math.isnan(ref) and math.isnan(W[c])) or W[c] == ref, (c, sb)
+
+
+def test_nvfp4_sixteen_column_blocks_and_nibble_order(oracle_lib):
+    # a scale per 16 columns (not 32) and rows not transposed: distinct scales on every block of a 3 x 64 matrix
+    rng = np.random.default_rng(7)
+    R, C = 3, 64
+    codes = rng.integers(0, 256, R * C // 2, dtype=np.uint8)
+    scales = np.array([0x30 + 3 * i for i in range(R * C // 16)], dtype=np.uint8)
+    W = oracle_lib.nvfp4_dequant(codes, scales, R, C).astype(np.float64)
+    assert np.array_equal(W, decode_nvfp4_np(codes, scales, R, C))
+
+
+def test_nvfp4_record_size(oracle_lib):
+    for H, I in [(256, 128), (2880, 2880), (2048, 512)]:
+        assert oracle_lib.expert_bytes(H, I, "nvfp4") == 3 * I * H * 9 // 16 == synth.expert_bytes(H, I, 1)
+        assert oracle_lib.expert_bytes(H, I) == 3 * I * H * 17 // 32 == synth.expert_bytes(H, I)
+
+
+def test_nvfp4_ffn_within_fp32_bound(oracle_lib):
+    H, I = 256, 128
+    rec = synth.expert_records(0, 0, 16, H, I, experts=[2], weight_format=1)[0]
+    x = synth.activations(0, 0, 5, 1, H)[0]
+    y = oracle_lib.expert_ffn(rec, H, I, x, "nvfp4").astype(np.float64)
+    offs = synth.section_offsets(H, I, 1)
+    sec = {k: rec[o:o + n] for k, (o, n) in offs.items()}
+    Wg = decode_nvfp4_np(sec["wg_codes"], sec["wg_scales"], I, H)
+    Wu = decode_nvfp4_np(sec["wu_codes"], sec["wu_scales"], I, H)
+    Wd = decode_nvfp4_np(sec["wd_codes"], sec["wd_scales"], H, I)
+    xf = bf16_to_f64(x)
+    g, u = Wg @ xf, Wu @ xf
+    h = g / (1.0 + np.exp(-g)) * u
+    ref = Wd @ h
+    # fp32 sums of H and I terms: a loose but sure bound, relative to the sum of magnitudes
+    dh = 4 * (H + 8) * U32 * ((np.abs(Wg) @ np.abs(xf)) * np.abs(u) + np.abs(g) * (np.abs(Wu) @ np.abs(xf)))
+    bound = (I + 8) * U32 * (np.abs(Wd) @ np.abs(h)) + np.abs(Wd) @ dh + 1e-30
+    assert np.all(np.abs(y - ref) <= bound)
+
+
+def test_nvfp4_unit_scales_equal_mxfp4_unit_scales(oracle_lib):
+    # with every scale 1 (E4M3 0x38, E8M0 127) the two formats hold the same matrices: same layer output, bit for bit
+    H, I, E, k = 256, 128, 8, 2
+    mx = synth.expert_records(0, 1, E, H, I)
+    nv = np.empty((E, synth.expert_bytes(H, I, 1)), dtype=np.uint8)
+    om, on = synth.section_offsets(H, I), synth.section_offsets(H, I, 1)
+    for name in ("wg", "wu", "wd"):
+        (o1, n1), (o2, n2) = om[name + "_codes"], on[name + "_codes"]
+        nv[:, o2:o2 + n2] = mx[:, o1:o1 + n1]
+        (s1, l1), (s2, l2) = om[name + "_scales"], on[name + "_scales"]
+        mx[:, s1:s1 + l1] = 127
+        nv[:, s2:s2 + l2] = 0x38
+    x = synth.activations(0, 1, 9, 3, H)
+    Wr = synth.router_weights(0, 1, E, H)
+    e2s = np.arange(E, dtype=np.int32)
+    a = oracle_lib.moe_layer(x, Wr, None, mx, e2s, k, H, I)
+    b = oracle_lib.moe_layer(x, Wr, None, nv, e2s, k, H, I, fmt="nvfp4")
+    assert np.array_equal(a["out_f32"], b["out_f32"]) and np.abs(a["out_f32"]).max() > 0
