@@ -130,11 +130,11 @@ def oracle_token_seconds(w, n_layers, seed=0):
     for l in range(n_layers):
         Wr = synth.router_weights(seed, l, w.experts, w.hidden)
         b = synth.router_bias(seed, l, w.experts, w.bias_tau)
-        ex = synth.expert_records(seed, l, w.experts, w.hidden, w.inter)
+        ex = synth.expert_records(seed, l, w.experts, w.hidden, w.inter, weight_format=w.weight_format)
         e2s = synth.expert_to_slot_by_rank(seed, l, w.experts, w.slots)
         x = synth.activations(seed, l, 0, 1, w.hidden)
         t0 = time.perf_counter()
-        oracle.moe_layer(x, Wr, b, ex, e2s, w.top_k, w.hidden, w.inter)
+        oracle.moe_layer(x, Wr, b, ex, e2s, w.top_k, w.hidden, w.inter, fmt="nvfp4" if w.weight_format else "mxfp4")
         t_total += time.perf_counter() - t0
         del ex
     return t_total
@@ -158,13 +158,13 @@ def _oracle_layer_worker(args):
     oracle.build()
     Wr = synth.router_weights(0, layer, w.experts, w.hidden)
     b = synth.router_bias(0, layer, w.experts, w.bias_tau)
-    ex = synth.expert_records(0, layer, w.experts, w.hidden, w.inter)
+    ex = synth.expert_records(0, layer, w.experts, w.hidden, w.inter, weight_format=w.weight_format)
     e2s = synth.expert_to_slot_by_rank(0, layer, w.experts, w.slots)
     x = synth.activations(0, layer, 0, 1, w.hidden)
     while time.time() < start_at:
         time.sleep(0.001)
     t0 = time.time()
-    oracle.moe_layer(x, Wr, b, ex, e2s, w.top_k, w.hidden, w.inter)
+    oracle.moe_layer(x, Wr, b, ex, e2s, w.top_k, w.hidden, w.inter, fmt="nvfp4" if w.weight_format else "mxfp4")
     return t0, time.time()
 
 
@@ -302,7 +302,8 @@ def run_ours(args):
                                                          ctypes.POINTER(ctypes.c_int32)), (int(c[1]),))
                 n_cold_e.append(len(set(cold.tolist())))
     mean_act = float(np.mean(n_act))
-    gateup_bytes = mean_act * 2 * w.inter * w.hidden * 17 / 32
+    code_scale_bytes = 0.5 + 1.0 / synth.scale_block(w.weight_format)  # bytes per weight: code + its share of a scale
+    gateup_bytes = mean_act * 2 * w.inter * w.hidden * code_scale_bytes
     expert_bytes_step = mean_act * w.expert_bytes * L
     router_bytes_step = w.experts * w.hidden * 4 * L
 
@@ -322,7 +323,11 @@ def run_ours(args):
     pk, pk_src = peaks()
     hbm_peak = pk.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"])
     src = os.path.join(ROOT, "expert_offload_moe_gb300", "csrc", "moe_decode_tc.cu")
-    if M == 1 and not args.two_launch:  # gate/up, SiLU and down in one launch (every expert byte), then combine
+    if w.weight_format != 0:  # NVFP4: CUDA-core decode kernels (the tensor-core path is MXFP4 only)
+        kernel, kbytes = "gateup_kernel", gateup_bytes
+        kernel_us = {"route": route_us, "gateup": gateup_us, "down": down_us}
+        traffic = None
+    elif M == 1 and not args.two_launch:  # gate/up, SiLU and down in one launch (every expert byte), then combine
         kernel, kbytes = "ffn_tc_kernel", mean_act * w.expert_bytes
         kernel_us = {"route": route_us, "ffn": gateup_us, "combine": down_us}
         traffic = traffic_for(src, "ffn_tc_gptoss20b_traffic.txt")
@@ -358,10 +363,11 @@ def run_ours(args):
     line = {
         "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4*e4m3->f32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "nvfp4*bf16->f32" if w.weight_format else "mxfp4*e4m3->f32", "data": "synthetic",
         "config": {"workload": w.name, "layers": L, "hidden": w.hidden, "inter": w.inter, "experts": w.experts,
                    "top_k": w.top_k, "slots": w.slots, "tokens_per_step": M, "parallelism": f"replicas{world}",
-                   "weights": "mxfp4 experts, fp32 router, fp32 accumulation",
+                   "weights": ("nvfp4" if w.weight_format else "mxfp4") + " experts, fp32 router, fp32 accumulation",
                    "l2": "inputs larger than L2: each step reads %.2f GB of distinct expert weights"
                          % (expert_bytes_step / 1e9),
                    "expert_gbs": expert_bytes_step / (t_ms / args.steps * 1e-3) / 1e9,

@@ -77,15 +77,17 @@ struct RouteParams {
 
 struct ExpertGeometry {
     int H, I;
+    int sblk;  // columns per scale byte: 32 (MXFP4, E8M0 scales) or 16 (NVFP4, E4M3 scales)
     size_t expert_bytes;
     size_t off_wg_codes, off_wg_scales, off_wu_codes, off_wu_scales, off_wd_codes, off_wd_scales;
 };
 
-inline ExpertGeometry make_geometry(int H, int I) {
+inline ExpertGeometry make_geometry(int H, int I, int sblk = 32) {
     ExpertGeometry g;
     g.H = H;
     g.I = I;
-    size_t c = (size_t)I * H / 2, s = (size_t)I * H / 32;
+    g.sblk = sblk;
+    size_t c = (size_t)I * H / 2, s = (size_t)I * H / sblk;
     g.off_wg_codes = 0;
     g.off_wg_scales = c;
     g.off_wu_codes = c + s;

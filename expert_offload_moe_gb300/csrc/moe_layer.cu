@@ -501,6 +501,8 @@ int moe_layer_create(const moe_layer_desc *desc, const float *router_w_dev, cons
     if (!(d.score_decay > 0.f && d.score_decay <= 1.f)) return fail(MOE_EINVAL, "score_decay must be in (0, 1]");
     if (d.visibility != MOE_VIS_DETERMINISTIC && d.visibility != MOE_VIS_POLLED)
         return fail(MOE_EINVAL, "bad visibility");
+    if (d.weight_format != MOE_FMT_MXFP4 && d.weight_format != MOE_FMT_NVFP4)
+        return fail(MOE_EINVAL, "bad weight_format %d", d.weight_format);
     const int dec_tokens = d.max_tokens < moe::kDecodeMaxTokens ? d.max_tokens : moe::kDecodeMaxTokens;
     if ((size_t)dec_tokens * d.hidden * sizeof(float) > (size_t)moe::kDecodeSmemLimit)
         return fail(MOE_EINVAL, "hidden %d too large for the decode kernels", d.hidden);
@@ -524,7 +526,7 @@ int moe_layer_create(const moe_layer_desc *desc, const float *router_w_dev, cons
     moe_layer *L = new moe_layer();
     L->d = d;
     L->host_bank = host_bank;
-    L->geo = moe::make_geometry(d.hidden, d.inter);
+    L->geo = moe::make_geometry(d.hidden, d.inter, d.weight_format == MOE_FMT_NVFP4 ? 16 : 32);
     L->nchunk = (d.hidden + moe::kRouteChunk - 1) / moe::kRouteChunk;
     L->max_hot = d.max_tokens * d.top_k;
     L->e2s = e2s;
@@ -627,7 +629,7 @@ int moe_layer_create(const moe_layer_desc *desc, const float *router_w_dev, cons
         L->rb.cold_w = (float *)(p + L->mir_off_cold + 2 * align_up(nc * 4, 16));
     }
     // decode on the tensor cores wherever a full 128-column tile exists along H and I
-    if (d.hidden >= 128 && d.inter >= 128) {
+    if (d.hidden >= 128 && d.inter >= 128 && d.weight_format == MOE_FMT_MXFP4) {
         const int rc = tc_setup(L, st);
         if (rc) {
             release(L);
@@ -945,6 +947,7 @@ int moe_layer_set_device_cache(moe_layer *L, int32_t enable) {
     g_err.clear();
     if (!L) return fail(MOE_EINVAL, "layer is NULL");
     const int E = L->d.num_experts, S = L->d.num_slots;
+    if (enable && L->d.weight_format != MOE_FMT_MXFP4) return fail(MOE_EINVAL, "the device slot table is MXFP4 only");
     if (enable && !L->dev_cache) {
         if (!L->host_bank_dev) return fail(MOE_ESTATE, "the GPU cannot address the host bank in place");
         if (reinterpret_cast<uintptr_t>(L->host_bank_dev) % 16)
@@ -1005,6 +1008,7 @@ int moe_forward_cold(moe_layer *L, const void *x_dev, void *out_dev, int32_t M, 
     g_err.clear();
     if (!L || !x_dev || !out_dev) return fail(MOE_EINVAL, "layer, x_dev and out_dev are required");
     if (nthreads < 0) return fail(MOE_EINVAL, "nthreads must be >= 0 (0: every host core)");
+    if (L->d.weight_format != MOE_FMT_MXFP4) return fail(MOE_EINVAL, "moe_forward_cold is MXFP4 only");
     if (L->routed_M == 0 || L->routed_x != x_dev || L->routed_M != M)
         return fail(MOE_ESTATE, "moe_forward_cold needs the x_dev and M of the last moe_route");
     if (M > moe::kDecodeMaxTokens) return MOE_OK;  // prefill: every route is hot
@@ -1038,6 +1042,7 @@ int moe_forward_cold_gpu(moe_layer *L, const void *x_dev, void *out_dev, int32_t
     if (!L || !x_dev || !out_dev) return fail(MOE_EINVAL, "layer, x_dev and out_dev are required");
     if (L->routed_M == 0 || L->routed_x != x_dev || L->routed_M != M)
         return fail(MOE_ESTATE, "moe_forward_cold_gpu needs the x_dev and M of the last moe_route");
+    if (L->d.weight_format != MOE_FMT_MXFP4) return fail(MOE_EINVAL, "moe_forward_cold_gpu is MXFP4 only");
     if (M > moe::kDecodeMaxTokens) return MOE_OK;  // prefill: every route is hot
     if (!L->host_bank_dev)
         return fail(MOE_ESTATE, "the GPU cannot address the host bank in place (cudaHostGetDevicePointer failed)");
@@ -1211,6 +1216,7 @@ int moe_layer_set_bias(moe_layer *L, const float *bias_dev, void *stream) {
 int moe_layer_attach_staging(moe_layer *L, void *staging_dev, size_t bytes) {
     g_err.clear();
     if (!L) return fail(MOE_EINVAL, "layer is NULL");
+    if (staging_dev && L->d.weight_format != MOE_FMT_MXFP4) return fail(MOE_EINVAL, "prefill is MXFP4 only");
     if (staging_dev && bytes < (size_t)L->d.num_experts * L->geo.expert_bytes)
         return fail(MOE_EINVAL, "staging buffer needs %zu bytes, got %zu",
                     (size_t)L->d.num_experts * L->geo.expert_bytes, bytes);

@@ -17,6 +17,7 @@ MOE_OUT_BF16, MOE_OUT_F32 = 0, 1
 MOE_VIS_DETERMINISTIC, MOE_VIS_POLLED = 0, 1
 MOE_FAULT_NONE, MOE_FAULT_COPY = 0, 1
 MOE_POLICY_FREQ, MOE_POLICY_LRU, MOE_POLICY_FIFO = 0, 1, 2
+MOE_FMT_MXFP4, MOE_FMT_NVFP4 = 0, 1
 
 EXPORTED = [
     "moe_layer_create", "moe_route", "moe_forward_slots", "moe_cache_update", "moe_destroy", "moe_last_error",
@@ -38,7 +39,7 @@ class LayerDesc(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("inter", ctypes.c_int32), ("num_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("num_slots", ctypes.c_int32), ("max_tokens", ctypes.c_int32),
                 ("out_dtype", ctypes.c_int32), ("max_refills_per_step", ctypes.c_int32),
-                ("score_decay", ctypes.c_float), ("visibility", ctypes.c_int32)]
+                ("score_decay", ctypes.c_float), ("visibility", ctypes.c_int32), ("weight_format", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -128,12 +129,13 @@ class Layer:
 
     def __init__(self, hidden, inter, num_experts, top_k, num_slots, max_tokens, router_w, router_bias,
                  host_bank, expert_to_slot, out_f32=False, max_refills=2, score_decay=1.0,
-                 visibility=MOE_VIS_DETERMINISTIC, stream=None):
+                 visibility=MOE_VIS_DETERMINISTIC, stream=None, weight_format=0):
         import numpy as np
 
         self.h = None
         self.desc = LayerDesc(hidden, inter, num_experts, top_k, num_slots, max_tokens,
-                              MOE_OUT_F32 if out_f32 else MOE_OUT_BF16, max_refills, score_decay, visibility)
+                              MOE_OUT_F32 if out_f32 else MOE_OUT_BF16, max_refills, score_decay, visibility,
+                              weight_format)
         self._host_bank = host_bank  # keep the borrowed bank alive
         self._e2s = np.ascontiguousarray(np.asarray(expert_to_slot, dtype=np.int32))
         h = _P()

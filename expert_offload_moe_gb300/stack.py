@@ -21,10 +21,10 @@ def bf16_tensor(bits: np.ndarray, device="cuda") -> torch.Tensor:
     return t.to(device) if device != "cpu" else t
 
 
-def pinned_bank(seed: int, layer: int, E: int, H: int, I: int) -> torch.Tensor:
-    eb = synth.expert_bytes(H, I)
+def pinned_bank(seed: int, layer: int, E: int, H: int, I: int, weight_format: int = 0) -> torch.Tensor:
+    eb = synth.expert_bytes(H, I, weight_format)
     bank = torch.empty((E, eb), dtype=torch.uint8, pin_memory=True)
-    synth.fill_expert_records(bank.numpy(), seed, layer, H, I, first=0)
+    synth.fill_expert_records(bank.numpy(), seed, layer, H, I, first=0, weight_format=weight_format)
     return bank
 
 
@@ -42,13 +42,13 @@ class LayerInputs:
         self.Wr = synth.router_weights(seed, layer, E, H)
         self.bias = synth.router_bias(seed, layer, E, w.bias_tau, bias_order)
         self.e2s = synth.expert_to_slot_by_rank(seed, layer, E, w.slots) if e2s is None else np.asarray(e2s, np.int32)
-        self.bank = pinned_bank(seed, layer, E, H, I)
+        self.bank = pinned_bank(seed, layer, E, H, I, w.weight_format)
 
     def make_layer(self, max_tokens=8, out_f32=False, **kw) -> moe.Layer:
         w = self.w
         return moe.Layer(w.hidden, w.inter, w.experts, w.top_k, w.slots, max_tokens,
                          torch.from_numpy(self.Wr).cuda(), torch.from_numpy(self.bias).cuda(), self.bank,
-                         self.e2s, out_f32=out_f32, **kw)
+                         self.e2s, out_f32=out_f32, weight_format=w.weight_format, **kw)
 
 
 class DecodeStack:

@@ -80,6 +80,21 @@ enum { MOE_OUT_BF16 = 0, MOE_OUT_F32 = 1 };
  *                 timing (the NInfer-Offload v0.4.0 behaviour). */
 enum { MOE_VIS_DETERMINISTIC = 0, MOE_VIS_POLLED = 1 };
 
+/* Expert weight formats.  Both hold E2M1 codes [R, C/2] (column 2c in the
+ * low nibble of byte c) per matrix, followed by its block scales:
+ *  MOE_FMT_MXFP4: one E8M0 byte per 32 columns (OCP MX v1.0), record
+ *                 3*I*H*17/32 bytes;
+ *  MOE_FMT_NVFP4: one E4M3 byte per 16 columns (NVIDIA's NVFP4 block scale;
+ *                 the pages name NVFP4 -- xinfer docs -- without defining it,
+ *                 and no per-tensor scale is applied), record 3*I*H*9/16
+ *                 bytes.
+ * NVFP4 layers run decode (M <= 8) on CUDA-core kernels that decode the codes
+ * and scales in registers; the tensor-core decode, prefill (staging), the
+ * cold-route computations (moe_forward_cold, moe_forward_cold_gpu) and the
+ * device slot table are MXFP4 only and return MOE_EINVAL for them.  Routing,
+ * the miss list and the host slot policy are the same for both. */
+enum { MOE_FMT_MXFP4 = 0, MOE_FMT_NVFP4 = 1 };
+
 /* Slot policies (tinyserve README "How it works" 3 lists lfu, lru and fifo
  * among its eviction policies, with frequency-recency as its default):
  *  MOE_POLICY_FREQ  decayed route counts, score_decay = 1 LFU, < 1 LFRU (the
@@ -104,6 +119,7 @@ typedef struct {
     int32_t max_refills_per_step; /* R, refills per moe_cache_update (NInfer: 2) */
     float score_decay;            /* 1.0 = LFU; in (0,1) = decayed frequency (LFRU) */
     int32_t visibility;           /* MOE_VIS_DETERMINISTIC or MOE_VIS_POLLED */
+    int32_t weight_format;        /* MOE_FMT_MXFP4 (0) or MOE_FMT_NVFP4 */
 } moe_layer_desc;
 
 /* Result of moe_route.  Device arrays are owned by the layer and stay valid
