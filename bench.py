@@ -57,6 +57,8 @@ def parse():
                     help="hot-route hit rate and refills of each slot policy on the drifting decode workload")
     ap.add_argument("--cold-on-gpu", action="store_true",
                     help="decode with the cold routes computed on the GPU from the host bank in place as well")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="decode batch M (default: the workload's first; e.g. 8 for the M=8 speculative-verify line)")
     ap.add_argument("--two-launch", action="store_true",
                     help="M = 1 decode with separate gate/up and down launches instead of the one-launch FFN")
     return ap.parse_args()
@@ -249,7 +251,7 @@ def run_ours(args):
     moe_build.build()
     moe.lib()
     w = synth.WORKLOADS[args.workload]
-    M = w.tokens[0]
+    M = args.tokens or w.tokens[0]
     n_inputs = 64
     st = stack.DecodeStack(w, M=M, n_layers=args.layers, seed=rank, n_inputs=n_inputs,
                            cold_on_gpu=args.cold_on_gpu)

@@ -64,6 +64,7 @@ struct RouteParams {
     const int32_t *e2s;  // [E]; ignored when all_hot
     int M, H, E, k, nchunk;
     int all_hot;         // prefill: every expert is hot, slot = expert id
+    int rowtask;         // set by launch_route: one warp per whole router row (decode, E > 32), logits final
     RouteBuffers b;
     uint16_t *xmir;      // decode: x copied here by the x-term tasks (the host mirror's source), or nullptr
     uint8_t *xq;         // tensor-core decode: x terms [16][Hpad] and their atoms, or nullptr

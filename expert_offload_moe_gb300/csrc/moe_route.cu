@@ -37,6 +37,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kSmemRoutes = 1024;
 constexpr int kMaxChunks = 16;  // router chunks summed with all loads in flight (H <= 4096)
+constexpr size_t kRowTaskSmem = 48 * 1024;  // x of a decode call staged per block by row tasks (M H bf16)
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -197,6 +198,7 @@ __device__ __forceinline__ void load_router_row(const RouteParams &p, int task, 
     }
 }
 
+template <bool kRow>
 __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int H = p.H, E = p.E, M = p.M, k = p.k;
@@ -204,17 +206,38 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
     __shared__ float s_bias[kMaxExperts];
 
     // ---------------- before the previous grid has finished: constant inputs ----
-    const int ntask = E * p.nchunk;
+    const int ntask = kRow ? E : E * p.nchunk;  // whole router rows, or 256-column chunks of them
     const int nq = p.xq ? M * (H / 32) : 0;  // x-term tasks, one 32-element block each
     int task = blockIdx.x * kWarps + warp;
     float w8[8];
-    load_router_row(p, task, lane, w8);
+    float wrow[kRow ? kMaxChunks : 1][8];  // row tasks: the task's whole router row, chunk c in wrow[c]
+    if constexpr (kRow) {
+#pragma unroll
+        for (int c = 0; c < kMaxChunks; ++c) {
+            const int col = c * kRouteChunk + lane * 8;
+            const bool ok = task < E && c < p.nchunk && col < H;
+            const float4 a = ok ? __ldg(reinterpret_cast<const float4 *>(p.Wr + (size_t)task * H + col))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 b = ok ? __ldg(reinterpret_cast<const float4 *>(p.Wr + (size_t)task * H + col + 4))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+            wrow[c][0] = a.x; wrow[c][1] = a.y; wrow[c][2] = a.z; wrow[c][3] = a.w;
+            wrow[c][4] = b.x; wrow[c][5] = b.y; wrow[c][6] = b.z; wrow[c][7] = b.w;
+        }
+    } else {
+        load_router_row(p, task, lane, w8);
+    }
     for (int e = threadIdx.x; e < E; e += kThreads) {
         s_e2s[e] = p.all_hot ? e : p.e2s[e];
         s_bias[e] = p.bias ? p.bias[e] : 0.f;
     }
     tc::pdl_wait();
     tc::pdl_trigger();
+    extern __shared__ __align__(16) uint16_t s_xrow[];  // row tasks: x [M][H] staged once per block
+    if (kRow) {
+        for (int i = threadIdx.x; i < M * H / 8; i += kThreads)
+            reinterpret_cast<uint4 *>(s_xrow)[i] = __ldg(reinterpret_cast<const uint4 *>(p.x) + i);
+        __syncthreads();
+    }
 
     // ---------------- phase 1: partial logits; x terms -----------------------
     for (bool first = true; task < ntask + nq; task += gridDim.x * kWarps, first = false) {
@@ -231,6 +254,37 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
                 p.xq[(size_t)n * p.Hpad + b * 32 + lane] = code;
                 if (lane == 0) p.xat[(size_t)(b / 4) * kTcAtomBytes + n * 16 + (b % 4)] = (uint8_t)sb;
             }
+            continue;
+        }
+        if constexpr (kRow) {  // the logit of expert `task` for every token, summed per lane over the chunks
+            float acc[kWarps];
+#pragma unroll
+            for (int t = 0; t < kWarps; ++t) acc[t] = 0.f;
+#pragma unroll
+            for (int c = 0; c < kMaxChunks; ++c) {
+                const int col = c * kRouteChunk + lane * 8;
+                if (c < p.nchunk && col < H) {
+#pragma unroll
+                    for (int t = 0; t < kWarps; ++t)
+                        if (t < M) {
+                            const uint4 xv = *reinterpret_cast<const uint4 *>(s_xrow + (size_t)t * H + col);
+                            acc[t] = fmaf(bf16_lo(xv.x), wrow[c][0], acc[t]);
+                            acc[t] = fmaf(bf16_hi(xv.x), wrow[c][1], acc[t]);
+                            acc[t] = fmaf(bf16_lo(xv.y), wrow[c][2], acc[t]);
+                            acc[t] = fmaf(bf16_hi(xv.y), wrow[c][3], acc[t]);
+                            acc[t] = fmaf(bf16_lo(xv.z), wrow[c][4], acc[t]);
+                            acc[t] = fmaf(bf16_hi(xv.z), wrow[c][5], acc[t]);
+                            acc[t] = fmaf(bf16_lo(xv.w), wrow[c][6], acc[t]);
+                            acc[t] = fmaf(bf16_hi(xv.w), wrow[c][7], acc[t]);
+                        }
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < kWarps; ++t)
+                if (t < M) {
+                    const float v = warp_sum(acc[t]);
+                    if (lane == 0) p.b.logit_part[(size_t)t * E + task] = v;
+                }
             continue;
         }
         if (!first) load_router_row(p, task, lane, w8);
@@ -408,7 +462,28 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
     // Decode (M <= 8): every thread sums chunk partials for some (token, expert) pairs, all loads of a
     // pair issued before the sum (in chunk order), into row t of s_l; warp t then selects from its row.
     const bool rows_by_block = M <= kWarps && p.nchunk <= kMaxChunks;
-    if (rows_by_block) {
+    if (rows_by_block && kRow) {
+        // whole-row logits: one load per (token, expert), eight per thread in flight
+        constexpr int kPer = 8;
+        for (int q0 = threadIdx.x; q0 < M * E; q0 += kPer * kThreads) {
+            float lv[kPer];
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const int q = q0 + u * kThreads;
+                lv[u] = q < M * E ? __ldcg(p.b.logit_part + q) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const int q = q0 + u * kThreads;
+                if (q < M * E) {
+                    const int t = q / E, e = q - t * E;
+                    const float v = lv[u] + s_bias[e];
+                    s_l[t][e] = (v != v) ? -INFINITY : v;  // NaN marks a taken expert below
+                }
+            }
+        }
+        __syncthreads();
+    } else if (rows_by_block) {
         for (int q = threadIdx.x; q < M * E; q += kThreads) {
             const int t = q / E, e = q - t * E;
             float pv[kMaxChunks];
@@ -438,16 +513,25 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
                 v[i] = e < E ? s_l[t][e] : __int_as_float(0x7fc00000);  // NaN: never a candidate
             }
             for (int j = 0; j < k; ++j) {
-                float bv = -INFINITY;
-                int be = 0x7fffffff;
+                // this lane's best by a 4-level tree (larger value, equal values to the lower id; NaN never
+                // wins), instead of one dependent chain over the kPer values
+                float tv[kPer];
+                int te[kPer];
 #pragma unroll
                 for (int i = 0; i < kPer; ++i) {
-                    const int e = lane + 32 * i;
-                    if (v[i] > bv || (v[i] == bv && e < be)) {
-                        bv = v[i];
-                        be = e;
-                    }
+                    tv[i] = v[i] == v[i] ? v[i] : -INFINITY;
+                    te[i] = v[i] == v[i] ? lane + 32 * i : 0x7fffffff;
                 }
+#pragma unroll
+                for (int w = kPer / 2; w > 0; w >>= 1)
+#pragma unroll
+                    for (int i = 0; i < w; ++i)
+                        if (tv[i + w] > tv[i] || (tv[i + w] == tv[i] && te[i + w] < te[i])) {
+                            tv[i] = tv[i + w];
+                            te[i] = te[i + w];
+                        }
+                float bv = tv[0];
+                int be = te[0];
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) {
                     const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -486,29 +570,32 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
         // hot routes by (expert, token), cold routes by (token, expert) -- and the active experts below
         // its own; the first route of an expert (lowest token) writes the active entry.
         __shared__ unsigned char s_first[kDecodeMaxTokens * kMaxTopK];
+        __shared__ unsigned char s_hotr[kDecodeMaxTokens * kMaxTopK];  // route q is hot
         const int nr = M * k, r = threadIdx.x;
         const bool mine = r < nr;
         const int e = mine ? s_ids[r] : 0, t = mine ? r / k : 0;
         const bool hot = mine && s_e2s[e] >= 0;
         if (mine) {
-            bool first = true;
-            for (int q = 0; q < nr; ++q)
-                if (s_ids[q] == e && q / k < t) first = false;
+            bool first = true;  // no earlier token routes to e (tokens before t; a token picks e once)
+            for (int t2 = 0; t2 < t; ++t2)
+                for (int j = 0; j < k; ++j) first &= s_ids[t2 * k + j] != e;
             s_first[r] = hot && first;
+            s_hotr[r] = hot;
         }
         __syncthreads();
         if (mine) {
             int pos = 0, aidx = 0;
-            for (int q = 0; q < nr; ++q) {
-                const int e2 = s_ids[q], t2 = q / k;
-                const bool hot2 = s_e2s[e2] >= 0;
-                if (hot) {
-                    pos += hot2 && (e2 < e || (e2 == e && t2 < t));
-                    aidx += s_first[q] && e2 < e;
-                } else {
-                    pos += !hot2 && (t2 < t || (t2 == t && e2 < e));
+            for (int t2 = 0, q = 0; t2 < M; ++t2)
+                for (int j = 0; j < k; ++j, ++q) {
+                    const int e2 = s_ids[q];
+                    const bool hot2 = s_hotr[q];
+                    if (hot) {
+                        pos += hot2 && (e2 < e || (e2 == e && t2 < t));
+                        aidx += s_first[q] && e2 < e;
+                    } else {
+                        pos += !hot2 && (t2 < t || (t2 == t && e2 < e));
+                    }
                 }
-            }
             if (hot) {
                 p.b.hot_expert[pos] = e;
                 p.b.hot_token[pos] = t;
@@ -1178,19 +1265,33 @@ cudaError_t launch_route(const RouteParams &p, cudaStream_t s, int num_sms) {
         route_scatter_kernel<<<(p.M * p.k + kThreads - 1) / kThreads, kThreads, 0, s>>>(p);
         return cudaGetLastError();
     }
-    const int ntask = p.E * p.nchunk + (p.xq ? p.M * (p.H / 32) : 0);
+    // decode of 4-8 tokens with more than 32 experts: one warp per whole router row, x staged once per block
+    // (the last block then reads finished logits instead of summing chunk partials, which grows with M; with
+    // fewer tokens the chunk tasks, spread over more SMs, finish sooner)
+    RouteParams q = p;
+    q.rowtask = !p.all_hot && p.E > 32 && p.M >= 4 && p.M <= kWarps && p.nchunk <= kMaxChunks &&
+                (size_t)p.M * p.H * 2 <= kRowTaskSmem;
+    const int ntask = (q.rowtask ? p.E : p.E * p.nchunk) + (p.xq ? p.M * (p.H / 32) : 0);
     int grid = (ntask + kWarps - 1) / kWarps;
     grid = grid < 1 ? 1 : (grid > 8 * num_sms ? 8 * num_sms : grid);
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = q.rowtask ? (size_t)p.M * p.H * 2 : 0;
+    static bool row_smem_set = false;  // static + dynamic shared memory of the row-task form passes 48 KB
+    if (q.rowtask && !row_smem_set) {
+        cudaError_t e = cudaFuncSetAttribute(route_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kRowTaskSmem);
+        if (e != cudaSuccess) return e;
+        row_smem_set = true;
+    }
     cfg.stream = s;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, route_kernel, p);
+    return q.rowtask ? cudaLaunchKernelEx(&cfg, route_kernel<true>, q) : cudaLaunchKernelEx(&cfg, route_kernel<false>, q);
 }
 
 cudaError_t launch_router_transpose(const float *Wr, float *WrT, int E, int H, int E32, cudaStream_t s) {
