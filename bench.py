@@ -236,6 +236,26 @@ def traffic_for(kernel_src, summary):
         return None
 
 
+def job_time(t_local, world, device):
+    """The job's time: the largest of every rank's time for the same steps (an all-reduce MAX over the
+    process group; the value on one rank is its own).  device: where the reduction tensor lives."""
+    if world == 1:
+        return float(t_local)
+    import torch
+    import torch.distributed as dist
+
+    tt = torch.tensor([float(t_local)], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_rate(units_per_rank, t_local_ms, world, device):
+    """Whole-job throughput: the units every rank processed over the slowest rank's time (weak scaling,
+    independent replicas)."""
+    t_ms = job_time(t_local_ms, world, device)
+    return units_per_rank * world / (t_ms / 1e3), t_ms
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -268,11 +288,7 @@ def run_ours(args):
         torch.cuda.synchronize()
 
     def max_over_ranks(v):
-        if world == 1:
-            return v
-        tt = torch.tensor([v], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        return float(tt.item())
+        return job_time(v, world, "cuda")
 
     # ---------------- timed region: graph replay, inputs resident in HBM -------
     for i in range(args.warmup):
