@@ -82,6 +82,8 @@ def _declare(L):
     L.oracle_cache_step_recency.restype = I32
     L.oracle_demand_lru_step.argtypes = [P, P, P, I32, I32, P, ctypes.c_int64, P, P]
     L.oracle_demand_lru_step.restype = I32
+    L.oracle_prefetch_step.argtypes = [P, P, P, P, I32, I32, P, I32, P, P, P, P]
+    L.oracle_prefetch_step.restype = I32
     L.oracle_mxfp8_block.argtypes = [P, I32, P]
     L.oracle_mxfp8_block.restype = ctypes.c_uint8
 
@@ -316,3 +318,22 @@ def mxfp8_block(v):
     codes = np.empty(v.shape[0], dtype=np.uint8)
     sc = lib().oracle_mxfp8_block(_p(v), v.shape[0], _p(codes))
     return int(sc), codes
+
+
+def prefetch_step(score, last, e2s, S, pred, R, in_flight=None):
+    """One next-layer prefetch decision (see oracle_prefetch_step).  Returns (pairs, new e2s); the inputs
+    are not modified."""
+    score, last = _c(score, np.float64), _c(last, np.int64)
+    e2s = _c(e2s, np.int32).copy()
+    E = e2s.shape[0]
+    s2e = np.full(S, -1, dtype=np.int32)
+    for e, s in enumerate(e2s):
+        if s >= 0:
+            s2e[s] = e
+    pred = _c(pred, np.int32)
+    fl = None if in_flight is None else _c(in_flight, np.uint8)
+    pe = np.zeros(max(R, 1), dtype=np.int32)
+    ps, pv = np.zeros_like(pe), np.zeros_like(pe)
+    n = lib().oracle_prefetch_step(_p(score), _p(last), _p(e2s), _p(s2e), E, S, _p(pred), int(R), _p(fl), _p(pe),
+                                   _p(ps), _p(pv))
+    return [(int(pe[i]), int(ps[i]), int(pv[i])) for i in range(n)], e2s

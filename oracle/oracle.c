@@ -503,6 +503,58 @@ int oracle_demand_lru_step(int32_t *e2s, int32_t *s2e, int64_t *stamp, int E, in
     return n;
 }
 
+/* Next-layer prefetch (tinyserve README "How it works" 4, FATE: the current
+ * layer's activations predict the next layer's experts, and their copies to
+ * the GPU overlap the current layer's work).  The prediction is the next
+ * layer's own routing applied to the current layer's input; pred[e] counts
+ * the predicted routes of expert e.  One prefetch step of the next layer:
+ *  candidates: predicted experts (pred > 0) neither resident nor in flight,
+ *              most predicted routes first, then higher score, then lower id
+ *  victims:    resident experts not in flight and not predicted, lowest score
+ *              first, then least recently routed, then lower slot
+ *  the i-th candidate takes the i-th victim's slot, at most R pairs.
+ * Scores and recency are not touched (the layer's own step does that when it
+ * routes); e2s/s2e are updated as if the copies had landed.  Returns the
+ * number of pairs written to pair_expert/pair_slot/pair_victim. */
+int oracle_prefetch_step(const double *score, const int64_t *last, int32_t *e2s, int32_t *s2e, int E, int S,
+                         const int32_t *pred, int R, const uint8_t *in_flight, int32_t *pair_expert,
+                         int32_t *pair_slot, int32_t *pair_victim) {
+    int n = 0;
+    char *used = (char *)calloc((size_t)E, 1);
+    for (int p = 0; p < R; ++p) {
+        /* best remaining candidate */
+        int cand = -1;
+        for (int e = 0; e < E; ++e) {
+            if (pred[e] <= 0 || e2s[e] >= 0 || used[e] || (in_flight && in_flight[e])) continue;
+            if (cand < 0 || pred[e] > pred[cand] || (pred[e] == pred[cand] && score[e] > score[cand])) cand = e;
+        }
+        if (cand < 0) break;
+        /* best remaining victim, scanned by slot so that ties go to the lower slot */
+        int vic = -1, vslot = -1;
+        for (int s = 0; s < S; ++s) {
+            int e = s2e[s];
+            if (e < 0 || used[e] || pred[e] > 0 || (in_flight && in_flight[e])) continue;
+            if (vic < 0 || score[e] < score[vic] || (score[e] == score[vic] && last[e] < last[vic])) {
+                vic = e;
+                vslot = s;
+            }
+        }
+        if (vic < 0) break;
+        used[cand] = used[vic] = 1;
+        pair_expert[n] = cand;
+        pair_slot[n] = vslot;
+        pair_victim[n] = vic;
+        ++n;
+    }
+    for (int i = 0; i < n; ++i) {
+        e2s[pair_victim[i]] = -1;
+        e2s[pair_expert[i]] = pair_slot[i];
+        s2e[pair_slot[i]] = pair_expert[i];
+    }
+    free(used);
+    return n;
+}
+
 /* ------------------------------------------------ prefill activation format */
 
 /* E4M3 element (OCP MX v1.0 / OFP8): sign bit 7, exponent bits 6..3 (bias 7),

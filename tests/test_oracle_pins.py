@@ -648,3 +648,63 @@ def test_nvfp4_unit_scales_equal_mxfp4_unit_scales(oracle_lib):
     a = oracle_lib.moe_layer(x, Wr, None, mx, e2s, k, H, I)
     b = oracle_lib.moe_layer(x, Wr, None, nv, e2s, k, H, I, fmt="nvfp4")
     assert np.array_equal(a["out_f32"], b["out_f32"]) and np.abs(a["out_f32"]).max() > 0
+
+
+# ------------------------------------------------------------ next-layer prefetch
+
+
+def test_prefetch_hand_worked_cases(oracle_lib):
+    # E = 6, S = 3, experts 0, 1, 2 in slots 0, 1, 2
+    e2s = [0, 1, 2, -1, -1, -1]
+    zero, never = np.zeros(6), np.full(6, -1, dtype=np.int64)
+    # predicted: 2 (resident), 3 twice, 4 once -> 3 then 4 come in; victims 0 then 1 (ties: lower slot)
+    pairs, m = oracle_lib.prefetch_step(zero, never, e2s, 3, [0, 0, 1, 2, 1, 0], 2)
+    assert pairs == [(3, 0, 0), (4, 1, 1)] and list(m) == [-1, -1, 2, 0, 1, -1]
+    # R = 1 keeps the most predicted; the victim is the lowest score (expert 1), not the lowest slot
+    pairs, _ = oracle_lib.prefetch_step([5.0, 1.0, 3.0, 0, 0, 0], never, e2s, 3, [0, 0, 0, 1, 3, 1], 1)
+    assert pairs == [(4, 1, 1)]
+    # equal predictions: higher score first, then lower id; equal scores: least recently routed victim
+    pairs, _ = oracle_lib.prefetch_step([2.0, 2.0, 2.0, 1.0, 4.0, 1.0], [7, 3, 5, -1, -1, -1], e2s, 3,
+                                        [0, 0, 0, 1, 1, 1], 3)
+    assert pairs == [(4, 1, 1), (3, 2, 2), (5, 0, 0)]
+    # an expert in flight is neither a candidate nor a victim; predicted residents are never victims
+    pairs, _ = oracle_lib.prefetch_step(zero, never, e2s, 3, [1, 0, 1, 1, 1, 0], 3,
+                                        in_flight=np.array([0, 0, 0, 1, 0, 0], dtype=np.uint8))
+    assert pairs == [(4, 1, 1)]
+
+
+def test_prefetch_invariants_on_random_steps(oracle_lib):
+    rng = np.random.default_rng(11)
+    for _ in range(300):
+        E = int(rng.integers(4, 40))
+        S = int(rng.integers(1, E + 1))
+        e2s = np.full(E, -1, dtype=np.int32)
+        e2s[rng.choice(E, S, replace=False)] = rng.permutation(S)
+        score = rng.integers(0, 5, E).astype(np.float64)
+        last = rng.integers(-1, 6, E).astype(np.int64)
+        pred = np.where(rng.random(E) < 0.3, rng.integers(1, 4, E), 0).astype(np.int32)
+        fl = (rng.random(E) < 0.1).astype(np.uint8)
+        R = int(rng.integers(0, 5))
+        pairs, m = oracle_lib.prefetch_step(score, last, e2s, S, pred, R, in_flight=fl)
+        cands = [e for e in range(E) if pred[e] > 0 and e2s[e] < 0 and not fl[e]]
+        vics = [e for e in range(E) if e2s[e] >= 0 and pred[e] == 0 and not fl[e]]
+        assert len(pairs) == min(R, len(cands), len(vics))
+        for ce, sl, ve in pairs:
+            assert ce in cands and ve in vics and e2s[ve] == sl and m[ce] == sl and m[ve] == -1
+        assert all(m[e] == e2s[e] for e in range(E) if pred[e] > 0 and e2s[e] >= 0)  # predicted residents stay
+        slots = m[m >= 0]
+        assert len(slots) == len(set(slots.tolist())) == S  # injective, every slot still used
+
+
+def test_prefetching_the_exact_routes_makes_them_resident(oracle_lib):
+    # when the prediction is the step's routing and R covers the misses, the step then finds every route hot
+    rng = np.random.default_rng(5)
+    for _ in range(50):
+        E, S, k = 16, 8, 3
+        e2s = np.full(E, -1, dtype=np.int32)
+        e2s[rng.choice(E, S, replace=False)] = rng.permutation(S)
+        routed = rng.choice(E, k, replace=False)
+        pred = np.zeros(E, dtype=np.int32)
+        pred[routed] = 1
+        _, m = oracle_lib.prefetch_step(np.zeros(E), np.full(E, -1, dtype=np.int64), e2s, S, pred, k)
+        assert all(m[e] >= 0 for e in routed)
