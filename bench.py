@@ -673,6 +673,7 @@ def run_policy_sweep(args):
                      "refills_per_layer_step": refills / (L * steps),
                      "refill_gb": refills * w.expert_bytes / 1e9, "tokens_per_s": steps / dt})
     rows += device_table_rows(w, L, steps, inputs, xs, biases)
+    fate = fate_rows(w, L, steps, inputs, biases)
     best = max(rows, key=lambda r: r["hit_rate"])
     line = {
         "metric": "slot-cache hot-route hit rate, decode with drifting routing (LFU)", "value": rows[0]["hit_rate"],
@@ -680,12 +681,57 @@ def run_policy_sweep(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4*e4m3->f32", "data": "synthetic",
         "config": {"workload": w.name, "layers": L, "experts": w.experts, "top_k": w.top_k, "slots": w.slots,
                    "max_refills_per_step": 2, "drift": "bias from popularity order A to order B over the steps",
-                   "sweep": rows, "best": best["policy"],
+                   "sweep": rows, "best": best["policy"], "next_layer_prefetch": fate,
                    "timing": "wall clock, eager launches, one host policy decision per layer and step"},
         "roofline": None, "clocks": None, "gpu_launches": int(len(SWEEP) * steps * L * 3), "e2e": None,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+FATE_RHO = 0.9  # correlation of consecutive layers' inputs in the residual-stream stand-in
+
+
+def fate_rows(w, L, steps, inputs, biases):
+    """LFU with and without next-layer prefetch (tinyserve README "How it works" 4, FATE) on inputs whose layers
+    are correlated like a residual stream (x_l = rho x_(l-1) + sqrt(1 - rho^2) e_l): after layer l's kernels are
+    issued and its slots updated, layer l + 1 predicts its experts from x_l and copies the missing ones in."""
+    import numpy as np
+    import torch
+
+    from expert_offload_moe_gb300 import stack, synth
+
+    xs = torch.from_numpy(np.stack([synth.activations_residual(0, t, L, 1, w.hidden, FATE_RHO)
+                                    for t in range(steps)]).view(np.int16)).view(torch.bfloat16).cuda()
+    x = torch.empty((L, 1, w.hidden), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((L, 1, w.hidden), dtype=torch.bfloat16, device="cuda")
+    rows = []
+    for prefetch in (False, True):
+        layers = [li.make_layer(max_tokens=8, max_refills=2) for li in inputs]
+        hot = cold = refills = fetched = 0
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for t in range(steps):
+            x.copy_(xs[t])
+            for l, lay in enumerate(layers):
+                lay.set_bias(biases[l][t])
+                res = lay.route(x[l], 1)
+                lay.forward_slots(x[l], out[l], 1)
+                refills += lay.cache_update()
+                c = stack.host_counts(res)
+                hot += int(c[0])
+                cold += int(c[1])
+                if prefetch and l + 1 < L:
+                    fetched += layers[l + 1].prefetch(x[l], 1)
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        for lay in layers:
+            lay.close()
+        rows.append({"policy": "LFU + next-layer prefetch" if prefetch else "LFU", "inputs": f"residual rho={FATE_RHO}",
+                     "hit_rate": hot / max(hot + cold, 1), "refills_per_layer_step": refills / (L * steps),
+                     "prefetches_per_layer_step": fetched / (L * steps),
+                     "copy_gb": (refills + fetched) * w.expert_bytes / 1e9, "tokens_per_s": steps / dt})
+    return rows
 
 
 def device_table_rows(w, L, steps, inputs, xs, biases):

@@ -157,6 +157,13 @@ struct moe_layer {
     cudaGraphNode_t cap_mirror = nullptr;
     unsigned long long cap_id = 0;
 
+    // next-layer prefetch (moe_prefetch): route scratch of its own, so that a prediction never touches the
+    // buffers of the layer's last moe_route, and the predicted histogram in page-locked memory
+    moe::RouteBuffers prb{};
+    void *pred_block = nullptr;
+    int32_t *m_pred = nullptr;
+    cudaEvent_t ev_pred = nullptr, ev_pfork = nullptr;
+
     cudaStream_t d2h = nullptr, h2d = nullptr;
     cudaEvent_t ev_fork = nullptr, ev_route = nullptr, ev_fence = nullptr;
     std::vector<cudaEvent_t> ev_copy;  // deterministic mode, one per pair
@@ -231,6 +238,10 @@ void release(moe_layer *L) {
     cudaFree(L->e2s_dev);
     cudaFree(L->dev_block);
     cudaFree(L->mir_block);
+    cudaFree(L->pred_block);
+    if (L->m_pred) cudaFreeHost(L->m_pred);
+    if (L->ev_pred) cudaEventDestroy(L->ev_pred);
+    if (L->ev_pfork) cudaEventDestroy(L->ev_pfork);
     cudaFree(L->h);
     cudaFree(L->cold_block);
     cudaFree(L->tc_block);
@@ -1082,6 +1093,60 @@ int moe_host_expert_ffn(const uint8_t *record, int32_t H, int32_t I, const uint1
     return MOE_OK;
 }
 
+// Copies pairs (expert pe[i] into slot ps[i], replacing pv[i]) from the host bank on the side stream and
+// makes them visible as the layer's visibility mode says (shared by the slot policy and the prefetch).
+static int issue_refills(moe_layer *L, int n, const int32_t *pe, const int32_t *ps, const int32_t *pv,
+                         cudaStream_t st) {
+    if (n == 0) return MOE_OK;
+    const size_t eb = L->geo.expert_bytes;
+    std::vector<int32_t> unmap_e, unmap_s, map_e, map_s;
+    for (int i = 0; i < n; ++i) {
+        unmap_e.push_back(pv[i]);
+        unmap_s.push_back(-1);
+    }
+    if (L->d.visibility == MOE_VIS_POLLED) {
+        // victims leave the map in stream order before their slots are overwritten
+        int rc = enqueue_map(L, unmap_e, unmap_s, st);
+        if (rc) return rc;
+    }
+    // everything already on the compute stream (including reads of the victims' slots) precedes the copies
+    CUDA_TRY(cudaEventRecord(L->ev_fence, st));
+    CUDA_TRY(cudaStreamWaitEvent(L->h2d, L->ev_fence, 0));
+    for (int i = 0; i < n; ++i) {
+        CUDA_TRY(cudaMemcpyAsync(L->slots + (size_t)ps[i] * eb, L->host_bank + (size_t)pe[i] * eb, eb,
+                                 cudaMemcpyHostToDevice, L->h2d));
+        if (int rc = build_slot_atoms(L, ps[i], L->h2d)) return rc;
+        L->stats[0] += 1;
+        L->stats[1] += (int64_t)eb;
+        if (L->d.visibility == MOE_VIS_DETERMINISTIC) {
+            CUDA_TRY(cudaEventRecord(L->ev_copy[i], L->h2d));
+            CUDA_TRY(cudaStreamWaitEvent(st, L->ev_copy[i], 0));
+        } else {
+            cudaEvent_t ev;
+            if (L->ev_pool.empty()) {
+                CUDA_TRY(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+            } else {
+                ev = L->ev_pool.back();
+                L->ev_pool.pop_back();
+            }
+            CUDA_TRY(cudaEventRecord(ev, L->h2d));
+            L->pending.push_back({pe[i], ps[i], ev});
+            L->in_flight[pe[i]] = 1;
+        }
+    }
+    if (L->d.visibility == MOE_VIS_DETERMINISTIC) {
+        map_e = unmap_e;
+        map_s = unmap_s;
+        for (int i = 0; i < n; ++i) {
+            map_e.push_back(pe[i]);
+            map_s.push_back(ps[i]);
+        }
+        int rc = enqueue_map(L, map_e, map_s, st);
+        if (rc) return rc;
+    }
+    return MOE_OK;
+}
+
 int moe_cache_update(moe_layer *L, void *stream, int32_t *n_refills_out) {
     g_err.clear();
     if (n_refills_out) *n_refills_out = 0;
@@ -1144,53 +1209,94 @@ int moe_cache_update(moe_layer *L, void *stream, int32_t *n_refills_out) {
     L->stats[2] += (int64_t)L->routed_M * L->d.top_k;
     L->stats[3] += L->m_counts[0];
 
-    if (n == 0) return MOE_OK;
-    const size_t eb = L->geo.expert_bytes;
-    std::vector<int32_t> unmap_e, unmap_s, map_e, map_s;
-    for (int i = 0; i < n; ++i) {
-        unmap_e.push_back(pv[i]);
-        unmap_s.push_back(-1);
+    if (int rc = issue_refills(L, n, pe.data(), ps.data(), pv.data(), st)) return rc;
+    if (n_refills_out) *n_refills_out = n;
+    return MOE_OK;
+}
+
+// Scratch of the prediction launch, allocated at the first moe_prefetch of a layer.
+static int prefetch_setup(moe_layer *L) {
+    const int E = L->d.num_experts, k = L->d.top_k, dec = moe::kDecodeMaxTokens;
+    const size_t nh = (size_t)dec * k;
+    const size_t sizes[] = {(size_t)L->nchunk * dec * E * 4,     // logit_part
+                            nh * 4, nh * 4,                     // topk ids, w
+                            nh * 4, nh * 4, nh * 4,             // hot expert/token/w
+                            nh * 4, nh * 4, nh * 4, nh * 4,     // act expert/slot/off/cnt
+                            nh * 4, nh * 4, nh * 4,             // cold token/expert/w
+                            (size_t)E * 4, 16, 16};             // hist, counts, arrive
+    size_t total = 0;
+    for (size_t z : sizes) total += align_up(z, 256);
+    cudaError_t e = cudaMalloc(&L->pred_block, total);
+    if (e == cudaSuccess) e = cudaMemset(L->pred_block, 0, total);
+    if (e == cudaSuccess) e = cudaHostAlloc(&L->m_pred, (size_t)E * 4, cudaHostAllocDefault);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&L->ev_pred, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&L->ev_pfork, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(e == cudaErrorMemoryAllocation ? MOE_ENOMEM : MOE_ECUDA, "prefetch scratch: %s",
+                    cudaGetErrorString(e));
     }
-    if (L->d.visibility == MOE_VIS_POLLED) {
-        // victims leave the map in stream order before their slots are overwritten
-        int rc = enqueue_map(L, unmap_e, unmap_s, st);
-        if (rc) return rc;
+    char *q = static_cast<char *>(L->pred_block);
+    void **dst[] = {(void **)&L->prb.logit_part, (void **)&L->prb.topk_ids, (void **)&L->prb.topk_w,
+                    (void **)&L->prb.hot_expert, (void **)&L->prb.hot_token, (void **)&L->prb.hot_w,
+                    (void **)&L->prb.act_expert, (void **)&L->prb.act_slot, (void **)&L->prb.act_off,
+                    (void **)&L->prb.act_cnt, (void **)&L->prb.cold_token, (void **)&L->prb.cold_expert,
+                    (void **)&L->prb.cold_w, (void **)&L->prb.hist, (void **)&L->prb.counts, (void **)&L->prb.arrive};
+    for (size_t i = 0; i < sizeof(sizes) / sizeof(sizes[0]); ++i) {
+        *dst[i] = q;
+        q += align_up(sizes[i], 256);
     }
-    // everything already on the compute stream (including reads of the victims' slots) precedes the copies
-    CUDA_TRY(cudaEventRecord(L->ev_fence, st));
-    CUDA_TRY(cudaStreamWaitEvent(L->h2d, L->ev_fence, 0));
-    for (int i = 0; i < n; ++i) {
-        CUDA_TRY(cudaMemcpyAsync(L->slots + (size_t)ps[i] * eb, L->host_bank + (size_t)pe[i] * eb, eb,
-                                 cudaMemcpyHostToDevice, L->h2d));
-        if (int rc = build_slot_atoms(L, ps[i], L->h2d)) return rc;
-        L->stats[0] += 1;
-        L->stats[1] += (int64_t)eb;
-        if (L->d.visibility == MOE_VIS_DETERMINISTIC) {
-            CUDA_TRY(cudaEventRecord(L->ev_copy[i], L->h2d));
-            CUDA_TRY(cudaStreamWaitEvent(st, L->ev_copy[i], 0));
-        } else {
-            cudaEvent_t ev;
-            if (L->ev_pool.empty()) {
-                CUDA_TRY(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
-            } else {
-                ev = L->ev_pool.back();
-                L->ev_pool.pop_back();
-            }
-            CUDA_TRY(cudaEventRecord(ev, L->h2d));
-            L->pending.push_back({pe[i], ps[i], ev});
-            L->in_flight[pe[i]] = 1;
-        }
+    return MOE_OK;
+}
+
+int moe_prefetch(moe_layer *L, const void *x_dev, int32_t M, void *stream, int32_t *n_refills_out) {
+    g_err.clear();
+    if (n_refills_out) *n_refills_out = 0;
+    if (!L || !x_dev) return fail(MOE_EINVAL, "layer and x_dev are required");
+    const int dec = L->d.max_tokens < moe::kDecodeMaxTokens ? L->d.max_tokens : moe::kDecodeMaxTokens;
+    if (M < 1 || M > dec) return fail(MOE_EINVAL, "M = %d outside [1, %d] (decode calls)", M, dec);
+    if (reinterpret_cast<uintptr_t>(x_dev) % 16) return fail(MOE_EINVAL, "x_dev must be 16-byte aligned");
+    if (L->dev_cache) return fail(MOE_ESTATE, "the device slot table owns the slots (moe_layer_set_device_cache)");
+    const int E = L->d.num_experts, S = L->d.num_slots;
+    if (S >= E) return MOE_OK;  // every expert resident: nothing to prefetch
+    if (!L->pred_block)
+        if (int rc = prefetch_setup(L)) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    // the prediction: this layer's routing of x, on the side stream (the compute stream goes on meanwhile)
+    moe::RouteParams p{};
+    p.x = static_cast<const uint16_t *>(x_dev);
+    p.Wr = L->Wr;
+    p.WrT = L->WrT;
+    p.E32 = (E + 31) / 32 * 32;
+    p.bias = L->bias;
+    p.e2s = L->e2s_dev;
+    p.M = M;
+    p.H = L->d.hidden;
+    p.E = E;
+    p.k = L->d.top_k;
+    p.nchunk = L->nchunk;
+    p.b = L->prb;
+    CUDA_TRY(cudaEventRecord(L->ev_pfork, st));
+    CUDA_TRY(cudaStreamWaitEvent(L->d2h, L->ev_pfork, 0));
+    CUDA_TRY(moe::launch_route(p, L->d2h, L->num_sms));
+    CUDA_TRY(cudaMemcpyAsync(L->m_pred, L->prb.hist, (size_t)E * 4, cudaMemcpyDeviceToHost, L->d2h));
+    CUDA_TRY(cudaEventRecord(L->ev_pred, L->d2h));
+    CUDA_TRY(cudaEventSynchronize(L->ev_pred));
+
+    const int R = L->d.max_refills_per_step;
+    std::vector<int32_t> pe(R > 0 ? R : 1), ps(pe.size()), pv(pe.size());
+    std::vector<int32_t> e2s = L->e2s, s2e = L->s2e;
+    const int n = moe_prefetch_step(L->score.data(), L->last.data(), e2s.data(), s2e.data(), E, S, L->m_pred, R,
+                                    L->in_flight.data(), pe.data(), ps.data(), pv.data());
+    if (n < 0) return fail(MOE_EINVAL, "prefetch policy rejected its arguments");
+    if (n > 0 && L->fault == MOE_FAULT_COPY) {
+        L->fault = MOE_FAULT_NONE;
+        return fail(MOE_ECUDA, "injected refill copy failure (no copy issued, map unchanged)");
     }
-    if (L->d.visibility == MOE_VIS_DETERMINISTIC) {
-        map_e = unmap_e;
-        map_s = unmap_s;
-        for (int i = 0; i < n; ++i) {
-            map_e.push_back(pe[i]);
-            map_s.push_back(ps[i]);
-        }
-        int rc = enqueue_map(L, map_e, map_s, st);
-        if (rc) return rc;
-    }
+    L->e2s.swap(e2s);
+    L->s2e.swap(s2e);
+    if (int rc = issue_refills(L, n, pe.data(), ps.data(), pv.data(), st)) return rc;
     if (n_refills_out) *n_refills_out = n;
     return MOE_OK;
 }

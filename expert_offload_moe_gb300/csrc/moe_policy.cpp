@@ -116,3 +116,44 @@ extern "C" int moe_policy_step_recency(int32_t policy, double *score, int64_t *l
     }
     return n;
 }
+
+// Next-layer prefetch (tinyserve README "How it works" 4, FATE: the current layer's activations predict the
+// next layer's experts; their copies overlap the current layer's work).  pred[e] counts the predicted routes
+// of expert e (the next layer's routing applied to the current layer's input).  Candidates: predicted experts
+// neither resident nor in flight, most predicted routes first, then higher score, then lower id.  Victims:
+// resident experts neither predicted nor in flight, lowest score first, then least recently routed, then
+// lower slot.  Candidate i takes victim i's slot, at most R pairs.  Scores and recency are left alone: the
+// layer's own step counts the routes when they happen.
+extern "C" int moe_prefetch_step(const double *score, const int64_t *last, int32_t *e2s, int32_t *s2e, int32_t E,
+                                 int32_t S, const int32_t *pred, int32_t R, const uint8_t *in_flight,
+                                 int32_t *pair_expert, int32_t *pair_slot, int32_t *pair_victim) {
+    if (!score || !last || !e2s || !s2e || !pred || E <= 0 || S <= 0 || S > E || R < 0 ||
+        (R > 0 && (!pair_expert || !pair_slot || !pair_victim)))
+        return -1;
+    auto busy = [&](int32_t e) { return in_flight && in_flight[e]; };
+    std::vector<int32_t> cand, vic;
+    for (int32_t e = 0; e < E; ++e)
+        if (pred[e] > 0 && e2s[e] < 0 && !busy(e)) cand.push_back(e);
+    std::stable_sort(cand.begin(), cand.end(), [&](int32_t a, int32_t b) {
+        return pred[a] != pred[b] ? pred[a] > pred[b] : score[a] > score[b];
+    });
+    for (int32_t s = 0; s < S; ++s) {
+        const int32_t e = s2e[s];
+        if (e >= 0 && pred[e] <= 0 && !busy(e)) vic.push_back(e);
+    }
+    std::stable_sort(vic.begin(), vic.end(), [&](int32_t a, int32_t b) {
+        return score[a] != score[b] ? score[a] < score[b] : last[a] < last[b];
+    });
+    const int32_t n = static_cast<int32_t>(std::min<size_t>({cand.size(), vic.size(), static_cast<size_t>(R)}));
+    for (int32_t i = 0; i < n; ++i) {
+        pair_expert[i] = cand[i];
+        pair_slot[i] = e2s[vic[i]];
+        pair_victim[i] = vic[i];
+    }
+    for (int32_t i = 0; i < n; ++i) {
+        e2s[pair_victim[i]] = -1;
+        e2s[pair_expert[i]] = pair_slot[i];
+        s2e[pair_slot[i]] = pair_expert[i];
+    }
+    return n;
+}

@@ -25,7 +25,8 @@ EXPORTED = [
     "moe_debug_slot_ptr", "moe_debug_inject_fault", "moe_debug_stats", "moe_debug_profile",
     "moe_debug_profile_read", "moe_debug_check_error", "moe_policy_step", "moe_route_noalloc", "moe_forward_cold",
     "moe_forward_cold_gpu", "moe_host_expert_ffn", "moe_policy_step_recency", "moe_layer_set_policy",
-    "moe_layer_set_device_cache", "moe_debug_device_cache", "moe_debug_decode_fusion",
+    "moe_layer_set_device_cache", "moe_debug_device_cache", "moe_debug_decode_fusion", "moe_prefetch_step",
+    "moe_prefetch",
 ]
 
 
@@ -94,6 +95,8 @@ def lib():
         L.moe_debug_stats.argtypes = [p, p]
         L.moe_debug_profile.argtypes = [p, i32]
         L.moe_debug_decode_fusion.argtypes = [p, i32]
+        L.moe_prefetch_step.argtypes = [p, p, p, p, i32, i32, p, i32, p, p, p, p]
+        L.moe_prefetch.argtypes = [p, p, i32, p, ctypes.POINTER(i32)]
         L.moe_debug_profile_read.argtypes = [p, p]
         L.moe_debug_check_error.argtypes = [p, ctypes.POINTER(i32)]
         L.moe_route_noalloc.argtypes = [p, i32, i32, p, p, i32, i32, p, ctypes.POINTER(RouteBuffers), p]
@@ -220,6 +223,13 @@ class Layer:
         code = ctypes.c_int32(0)
         check(lib().moe_debug_check_error(self.h, ctypes.byref(code)))
 
+    def prefetch(self, x, M, stream=None):
+        """Next-layer prefetch: this layer's router predicts its experts from ``x`` (the current layer's input)
+        and the predicted experts missing from its slots are copied in now.  Returns the refills issued."""
+        n = ctypes.c_int32(0)
+        check(lib().moe_prefetch(self.h, _P(x.data_ptr()), M, stream_ptr(stream), ctypes.byref(n)))
+        return n.value
+
     def decode_fusion(self, enable):
         check(lib().moe_debug_decode_fusion(self.h, 1 if enable else 0))
 
@@ -286,6 +296,23 @@ def policy_step_recency(policy, score, last, loaded, e2s, s2e, hist, step, decay
                                       ps.ctypes.data_as(_P), pv.ctypes.data_as(_P))
     if n < 0:
         raise MoeError(MOE_EINVAL, "moe_policy_step_recency rejected its arguments")
+    return [(int(pe[i]), int(ps[i]), int(pv[i])) for i in range(n)]
+
+
+def prefetch_step(score, last, e2s, s2e, pred, R, in_flight=None):
+    """The library's next-layer prefetch decision on numpy arrays (e2s / s2e updated in place)."""
+    import numpy as np
+
+    E, S = e2s.shape[0], s2e.shape[0]
+    pe, ps, pv = (np.zeros(max(R, 1), dtype=np.int32) for _ in range(3))
+    fl = None if in_flight is None else np.ascontiguousarray(in_flight, dtype=np.uint8)
+    pred = np.ascontiguousarray(pred, dtype=np.int32)
+    n = lib().moe_prefetch_step(score.ctypes.data_as(_P), last.ctypes.data_as(_P), e2s.ctypes.data_as(_P),
+                                s2e.ctypes.data_as(_P), E, S, pred.ctypes.data_as(_P), int(R),
+                                None if fl is None else fl.ctypes.data_as(_P), pe.ctypes.data_as(_P),
+                                ps.ctypes.data_as(_P), pv.ctypes.data_as(_P))
+    if n < 0:
+        raise MoeError(MOE_EINVAL, "moe_prefetch_step rejected its arguments")
     return [(int(pe[i]), int(ps[i]), int(pv[i])) for i in range(n)]
 
 

@@ -43,7 +43,7 @@ import dataclasses
 import numpy as np
 
 # tensor ids inside a SeedSequence key
-T_X, T_ROUTER, T_RANK, T_EXPERTS, T_RANK_B = 1, 2, 3, 4, 5
+T_X, T_ROUTER, T_RANK, T_EXPERTS, T_RANK_B, T_X_RESID = 1, 2, 3, 4, 5, 6
 
 
 @dataclasses.dataclass(frozen=True)
@@ -131,6 +131,19 @@ def activations(seed: int, layer: int, step: int, M: int, H: int) -> np.ndarray:
     return bf16_bits_rne(g)
 
 
+def activations_residual(seed: int, step: int, L: int, M: int, H: int, rho: float) -> np.ndarray:
+    """[L, M, H] bf16 bits whose layers are correlated like a residual stream:
+    x_0 ~ N(0, 1), x_l = rho x_(l-1) + sqrt(1 - rho^2) e_l with fresh e_l ~ N(0, 1) (float64, then RNE)."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 0, T_X_RESID, step]))
+    x = rng.standard_normal((M, H))
+    out = np.empty((L, M, H), dtype=np.uint16)
+    for l in range(L):
+        if l:
+            x = rho * x + np.sqrt(1.0 - rho * rho) * rng.standard_normal((M, H))
+        out[l] = bf16_bits_rne(x.astype(np.float32))
+    return out
+
+
 def router_weights(seed: int, layer: int, E: int, H: int) -> np.ndarray:
     return (_rng(seed, layer, T_ROUTER).standard_normal((E, H), dtype=np.float32) * np.float32(0.02)).astype(np.float32)
 
@@ -211,6 +224,6 @@ def zipf_expected_hit_rate(E: int, S: int, tau: float) -> float:
 
 __all__ = [
     "Workload", "WORKLOADS", "scale_block", "expert_bytes", "section_offsets", "bf16_bits_rne", "activations",
-    "router_weights", "popularity_rank", "router_bias", "drifting_bias", "expert_to_slot_by_rank",
+    "activations_residual", "router_weights", "popularity_rank", "router_bias", "drifting_bias", "expert_to_slot_by_rank",
     "fill_expert_records", "expert_records", "zipf_log_popularity", "zipf_expected_hit_rate",
 ]

@@ -377,6 +377,40 @@ int moe_debug_decode_fusion(moe_layer *layer, int32_t enable);
  * for the events). */
 int moe_debug_profile_read(moe_layer *layer, double out[4]);
 
+/* Next-layer prefetch (tinyserve README "How it works" 4, FATE: the
+ * current layer's activations predict the next layer's experts, and the
+ * copies overlap the current layer's work).  Call it on the NEXT layer with
+ * the CURRENT layer's input x_dev [M, H] (1 <= M <= min(8, max_tokens)),
+ * after the current layer's moe_forward_slots has been issued:
+ *  1. the layer's own router, top-k and softmax run on x_dev (its routing of
+ *     x_dev, i.e. the prediction) on an internal stream forked from `stream`,
+ *     into scratch of their own (the last moe_route's results stay valid);
+ *  2. the calling thread waits for the predicted per-expert route counts;
+ *  3. moe_prefetch_step picks up to max_refills_per_step predicted,
+ *     non-resident experts and the unpredicted resident experts they replace;
+ *  4. their copies from the host bank are issued on the layer's copy stream
+ *     and become visible as moe_cache_update's do (MOE_VIS_DETERMINISTIC:
+ *     later work on `stream` waits for them; MOE_VIS_POLLED: they join the map
+ *     once landed).
+ * Scores and recency are not changed (the layer's own moe_cache_update counts
+ * the routes when they happen).  Does nothing when every expert is resident.
+ * *n_refills (may be NULL) receives the number of copies issued.  Not
+ * capturable (the host waits for the prediction).  Errors: MOE_EINVAL,
+ * MOE_ESTATE (device slot table on), MOE_ENOMEM, MOE_ECUDA. */
+int moe_prefetch(moe_layer *layer, const void *x_dev, int32_t M, void *stream, int32_t *n_refills);
+
+/* The prefetch decision on host arrays, as moe_prefetch runs it.
+ *  pred[E]: predicted routes per expert.  Candidates: predicted experts
+ *  neither resident nor in flight, most predicted routes first, then higher
+ *  score[e], then lower id.  Victims: resident experts neither predicted nor
+ *  in flight, lowest score first, then the oldest last[e], then lower slot.
+ *  Candidate i takes victim i's slot; at most R pairs.  e2s[E] and s2e[S]
+ *  are updated in place, score[] and last[] are only read.  Returns the
+ *  number of pairs, or -1 on bad arguments. */
+int moe_prefetch_step(const double *score, const int64_t *last, int32_t *e2s, int32_t *s2e, int32_t E, int32_t S,
+                      const int32_t *pred, int32_t R, const uint8_t *in_flight, int32_t *pair_expert,
+                      int32_t *pair_slot, int32_t *pair_victim);
+
 /* The slot-cache decision on host arrays, as moe_cache_update runs it
  * (exported so that the policy can be checked without a GPU).
  *  score[E], last[E], e2s[E], s2e[S] are updated in place; in_flight[E]

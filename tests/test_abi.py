@@ -165,3 +165,21 @@ def test_recency_policy_rejects_bad_arguments(lib):
         moe.policy_step_recency(moe.MOE_POLICY_FREQ, np.zeros(E), np.zeros(E, dtype=np.int64),
                                 np.zeros(E, dtype=np.int64), np.array([0, 1, -1, -1], dtype=np.int32),
                                 np.array([0, 1], dtype=np.int32), np.zeros(E, dtype=np.int32), 0, 1.0, 1)
+
+
+@pytest.mark.parametrize("R,E,S", [(2, 32, 16), (1, 16, 4), (4, 64, 48), (3, 8, 8)])
+def test_library_prefetch_step_matches_oracle(lib, oracle_lib, R, E, S):
+    rng = np.random.default_rng(R * 100 + E)
+    for _ in range(200):
+        e2s = np.full(E, -1, dtype=np.int32)
+        e2s[rng.choice(E, S, replace=False)] = rng.permutation(S)
+        s2e = np.full(S, -1, dtype=np.int32)
+        s2e[e2s[e2s >= 0]] = np.nonzero(e2s >= 0)[0]
+        score = rng.integers(0, 4, E).astype(np.float64)
+        last = rng.integers(-1, 5, E).astype(np.int64)
+        pred = np.where(rng.random(E) < 0.25, rng.integers(1, 4, E), 0).astype(np.int32)
+        fl = (rng.random(E) < 0.1).astype(np.uint8)
+        want, want_map = oracle_lib.prefetch_step(score, last, e2s, S, pred, R, in_flight=fl)
+        got = moe.prefetch_step(score, last, e2s, s2e, pred, R, in_flight=fl)
+        assert got == want and np.array_equal(e2s, want_map)
+        assert all(s2e[e2s[e]] == e for e in range(E) if e2s[e] >= 0)
