@@ -26,13 +26,16 @@
 // operand (w h), so the down MMA accumulates the sum over experts of w Wd h in
 // tensor memory, in ascending expert order: the combine happens there.
 //
-// quantize_x_kernel  x -> x terms + x atoms (B operand of gate/up)
+// The x terms and their atoms (B operand of gate/up) are written by the route launch.
 // gateup_tc_kernel   one CTA per (active expert, 128-row tile of I, K split):
 //                    Dg = Wg x, Du = Wu x; then h = SiLU(g) u, w h -> h terms
 // down_tc_kernel     one CTA per (128-row tile of H, K split over the
 //                    concatenated (expert, k-step) sequence): out = sum_e Wd_e (w h)
-// K splits write fp32 partials; the last CTA of a tile (arrival counter, no
-// waiting) sums them in split order, so results do not depend on timing.
+// ffn_tc_kernel      (M = 1) both in one launch per (active expert, I tile, K split):
+//                    gate/up, h in shared memory, then the tile's column slice of Wd
+//                    into fp32 partials; ffn_combine_kernel sums them in a fixed order
+// The K splits of a tile form a thread-block cluster; their partials meet in distributed
+// shared memory and are summed in rank order, so results do not depend on timing.
 #include <cuda_bf16.h>
 
 #include "moe_internal.h"
