@@ -44,6 +44,8 @@ def test_null_arguments_are_rejected_without_a_gpu(lib):
     assert lib.moe_route(None, None, 1, None, None) == moe.MOE_EINVAL
     assert lib.moe_forward_slots(None, None, None, 1, None) == moe.MOE_EINVAL
     assert lib.moe_cache_update(None, None, None) == moe.MOE_EINVAL
+    assert lib.moe_prefetch(None, None, 1, None, None) == moe.MOE_EINVAL
+    assert lib.moe_debug_decode_fusion(None, 1) == moe.MOE_EINVAL
     assert lib.moe_destroy(None) == moe.MOE_OK
 
 
@@ -183,3 +185,15 @@ def test_library_prefetch_step_matches_oracle(lib, oracle_lib, R, E, S):
         got = moe.prefetch_step(score, last, e2s, s2e, pred, R, in_flight=fl)
         assert got == want and np.array_equal(e2s, want_map)
         assert all(s2e[e2s[e]] == e for e in range(E) if e2s[e] >= 0)
+
+
+def test_prefetch_step_rejects_bad_arguments(lib):
+    E, S = 4, 2
+    e2s = np.array([0, 1, -1, -1], dtype=np.int32)
+    s2e = np.array([0, 1], dtype=np.int32)
+    with pytest.raises(moe.MoeError):  # R < 0
+        moe.prefetch_step(np.zeros(E), np.zeros(E, dtype=np.int64), e2s, s2e, np.ones(E, dtype=np.int32), -1)
+    with pytest.raises(moe.MoeError):  # more slots than experts
+        moe.prefetch_step(np.zeros(E), np.zeros(E, dtype=np.int64), e2s, np.zeros(8, dtype=np.int32),
+                          np.ones(E, dtype=np.int32), 1)
+    assert moe.prefetch_step(np.zeros(E), np.zeros(E, dtype=np.int64), e2s, s2e, np.zeros(E, dtype=np.int32), 2) == []

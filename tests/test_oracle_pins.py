@@ -708,3 +708,16 @@ def test_prefetching_the_exact_routes_makes_them_resident(oracle_lib):
         pred[routed] = 1
         _, m = oracle_lib.prefetch_step(np.zeros(E), np.full(E, -1, dtype=np.int64), e2s, S, pred, k)
         assert all(m[e] >= 0 for e in routed)
+
+
+
+def test_residual_stream_inputs_are_seeded_and_correlated():
+    # the next-layer prefetch line's stand-in for a residual stream: x_l = rho x_(l-1) + sqrt(1 - rho^2) e_l
+    a = synth.activations_residual(0, 3, 6, 2, 2048, 0.9)
+    assert np.array_equal(a, synth.activations_residual(0, 3, 6, 2, 2048, 0.9))
+    x = bf16_to_f64(a)
+    for l in range(1, 6):
+        c = np.corrcoef(x[l - 1].ravel(), x[l].ravel())[0, 1]
+        assert abs(c - 0.9) < 0.02
+        assert abs(np.std(x[l]) - 1.0) < 0.05
+    assert abs(np.corrcoef(x[0].ravel(), x[5].ravel())[0, 1] - 0.9 ** 5) < 0.03
