@@ -43,7 +43,22 @@ namespace {
 constexpr float kE2M1[16] = {0.f,  0.5f,  1.f,  1.5f,  2.f,  3.f,  4.f,  6.f,
                              -0.f, -0.5f, -1.f, -1.5f, -2.f, -3.f, -4.f, -6.f};
 
-inline float e8m0(uint8_t s) { return std::ldexp(1.0f, (int)s - 127); }
+// Decode tables built once: both elements of a code byte (low nibble first), and 2^(s - 127) for every
+// E8M0 byte (the same values as ldexp: s = 0 is the subnormal 2^-127, s = 255 overflows to infinity).
+struct Tables {
+    float pair[256][2];
+    float scale[256];
+    Tables() {
+        for (int b = 0; b < 256; ++b) {
+            pair[b][0] = kE2M1[b & 15];
+            pair[b][1] = kE2M1[b >> 4];
+            scale[b] = std::ldexp(1.0f, b - 127);
+        }
+    }
+};
+const Tables kTables;
+
+inline float e8m0(uint8_t s) { return kTables.scale[s]; }
 
 inline float bf16_to_f32(uint16_t b) {
     const uint32_t u = (uint32_t)b << 16;
@@ -59,8 +74,8 @@ inline float mxfp4_row_dot(const uint8_t *codes, const uint8_t *scales, int C, c
         float e[32];
         const uint8_t *cb = codes + b * 16;
         for (int j = 0; j < 16; ++j) {
-            e[2 * j] = kE2M1[cb[j] & 15];
-            e[2 * j + 1] = kE2M1[cb[j] >> 4];
+            e[2 * j] = kTables.pair[cb[j]][0];
+            e[2 * j + 1] = kTables.pair[cb[j]][1];
         }
         const float *vb = v + b * 32;
         float p[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
