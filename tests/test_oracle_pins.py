@@ -478,6 +478,169 @@ def test_mxfp8_block_rule(oracle_lib):
     assert sc == 0 and np.all(codes == 0)
 
 
+
+# ------------------------------------------------- prefill expert FFN (MXFP8 activations)
+
+
+def e4m3_rne_np(s):
+    """Round float64 values to the E4M3 grid, nearest with ties to an even mantissa, saturating at
+    +-448; computed from the format's spacing (3 mantissa bits, normal from 2^-6, subnormal step
+    2^-9), not from a code table."""
+    s = np.asarray(s, dtype=np.float64)
+    a = np.abs(s)
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    step = np.where(a >= 2.0 ** -6, np.ldexp(1.0, (np.maximum(e, -6) - 3).astype(np.int64)), 2.0 ** -9)
+    q = np.round(a / step) * step  # numpy rounds halves to even: the even integer is the even mantissa
+    return np.sign(s) * np.minimum(q, 448.0)
+
+
+def mxfp8_quant_np(v):
+    """OCP MX v1.0 MXFP8 conversion of a float64 vector in blocks of 32: shared exponent
+    X = floor(log2 max|v|) - 8 (8 = E4M3's largest exponent), X = -127 for a zero block,
+    elements E4M3(v / 2^X).  Returns the dequantised values and X per block."""
+    v = np.asarray(v, dtype=np.float64).reshape(-1, 32)
+    amax = np.abs(v).max(axis=1)
+    _, ex = np.frexp(np.where(amax > 0, amax, 1.0))
+    X = np.where(amax > 0, np.clip(ex - 1 - 8, -127, 127), -127)
+    sc = np.ldexp(1.0, X)[:, None]
+    return (e4m3_rne_np(v / sc) * sc).reshape(-1), X
+
+
+def test_mxfp8_quantiser_restatement_agrees_with_the_oracle_block_rule(oracle_lib):
+    # the numpy quantiser used below against the oracle's block rule, on bf16-exact blocks of many
+    # magnitudes (any disagreement here would make the FFN pin below meaningless)
+    rng = np.random.default_rng(7)
+    for t in range(200):
+        v = (rng.standard_normal(32) * 2.0 ** rng.integers(-20, 20, size=32)).astype(np.float32)
+        if t % 5 == 0:
+            v[rng.integers(0, 32)] = 0
+        sc, codes = oracle_lib.mxfp8_block(v)
+        back = np.array([e4m3_from_bits(int(c)) for c in codes]) * 2.0 ** (int(sc) - 127)
+        ref, X = mxfp8_quant_np(v.astype(np.float64))
+        assert int(sc) - 127 == X[0]
+        assert np.array_equal(back, ref)
+
+
+def _ffn_mxfp8_reference(rec, H, I, x):
+    """float64 restatement of the prefill reading of the expert FFN from independent decoders:
+    xq = MXFP8(x) in 32-element blocks along H; g = Wg xq, u = Wu xq; h = SiLU(g) u;
+    hq = MXFP8(h) in 32-element blocks along I; y = Wd hq.
+
+    The oracle forms h in fp32, so an element of h that lies within the fp32 error bound of an E4M3
+    rounding boundary may legitimately round either way.  Returns y for the float64 h, the bound
+    on |y_oracle - y| (fp32 summation of both contractions plus the spread of those ambiguous
+    elements), and the number of ambiguous elements."""
+    Wg, Wu, Wd = _expert_f64(rec, H, I)
+    xf = bf16_to_f64(x)
+    xq, _ = mxfp8_quant_np(xf)
+    g, u = Wg @ xq, Wu @ xq
+    dg = (H + 1) * U32 * (np.abs(Wg) @ np.abs(xq))
+    du = (H + 1) * U32 * (np.abs(Wu) @ np.abs(xq))
+    sig = 1.0 / (1.0 + np.exp(-g))
+    silu = g * sig
+    h = silu * u
+    # mean value theorem: |SiLU(g') - SiLU(g)| <= (|SiLU'(g)| + 1/2 |g' - g|) |g' - g|, as |SiLU''| <= 1/2
+    dsilu = (np.abs(sig * (1.0 + g * (1.0 - sig))) + 0.5 * dg) * dg
+    dh = dsilu * (np.abs(u) + du) + np.abs(silu) * du + 16 * U32 * np.abs(h) + 1e-30
+    hq, X = mxfp8_quant_np(h)
+    lo, Xlo = mxfp8_quant_np(h - dh)
+    hi, Xhi = mxfp8_quant_np(h + dh)
+    amax_lo = np.maximum(np.abs(h) - dh, 0).reshape(-1, 32).max(axis=1)
+    amax_hi = (np.abs(h) + dh).reshape(-1, 32).max(axis=1)
+    _, e_lo = np.frexp(amax_lo)
+    _, e_hi = np.frexp(amax_hi)
+    assert np.array_equal(e_lo, e_hi), "a block scale of h is ambiguous at this seed"
+    # the quantiser is monotone within a fixed block scale, so every admissible hq lies in [qlo, qhi]
+    qlo = np.minimum(lo, hi)
+    qhi = np.maximum(lo, hi)
+    spread = qhi - qlo
+    y = Wd @ hq
+    bound = (I + 1) * U32 * (np.abs(Wd) @ np.maximum(np.abs(qlo), np.abs(qhi))) + np.abs(Wd) @ spread + 1e-30
+    return y, bound, int(np.count_nonzero(spread)), h, hq
+
+
+@pytest.mark.parametrize("H,I", [(256, 128), (128, 256), (320, 96)])
+def test_ffn_mxfp8_against_float64_restatement(oracle_lib, H, I):
+    # H != I both ways: a block axis or a transposed operand taken the wrong way cannot pass
+    rec = synth.expert_records(3, 1, 8, H, I, experts=[6])[0]
+    x = synth.activations(3, 1, 0, 1, H)[0]
+    y = oracle_lib.expert_ffn_mxfp8(rec, H, I, x).astype(np.float64)
+    ref, bound, n_amb, h, hq = _ffn_mxfp8_reference(rec, H, I, x)
+    assert n_amb <= I // 16
+    assert np.all(np.abs(y - ref) <= bound)
+    # the bound is tight enough to tell the readings apart: leaving h unquantised, or quantising
+    # x per element instead of per block, moves y far outside it
+    Wg, Wu, Wd = _expert_f64(rec, H, I)
+    assert np.mean(np.abs(Wd @ h - ref) > bound) > 0.5
+    xf = bf16_to_f64(x)
+    x_elem = np.concatenate([mxfp8_quant_np(np.repeat(v, 32))[0][:1] for v in xf])
+    g2, u2 = Wg @ x_elem, Wu @ x_elem
+    y2 = Wd @ mxfp8_quant_np(g2 / (1 + np.exp(-g2)) * u2)[0]
+    assert np.mean(np.abs(y2 - ref) > bound) > 0.5
+
+
+def test_ffn_mxfp8_gate_and_up_scales_are_their_own(oracle_lib):
+    # Wg and Wu identical in codes but with different block scales: taking one section's scales
+    # for the other changes h by a power of two per block
+    H, I = 128, 64
+    rec = synth.expert_records(5, 0, 4, H, I, experts=[1])[0].copy()
+    s = sections(rec, H, I)
+    s["wu_codes"][:] = s["wg_codes"]
+    s["wu_scales"][:] = 120 + (s["wg_scales"].astype(np.int64) - 120 + 3) % 8
+    x = synth.activations(5, 0, 0, 1, H)[0]
+    y = oracle_lib.expert_ffn_mxfp8(rec, H, I, x).astype(np.float64)
+    ref, bound, _, _, _ = _ffn_mxfp8_reference(rec, H, I, x)
+    assert np.all(np.abs(y - ref) <= bound)
+
+
+def _mxfp8_exact_token(rng, H):
+    """bf16 values that MXFP8 represents exactly: each 32-block holds one +-3 (so X = 1 - 8 = -7) and
+    other values m/8 * 2^e with m in 8..15, e in [-6, 1] (inside E4M3's normal range at that scale)."""
+    v = (rng.integers(8, 16, size=H) / 8.0) * np.ldexp(1.0, rng.integers(-6, 2, size=H))
+    v *= np.where(rng.random(H) < 0.5, -1.0, 1.0)
+    v[::32] = np.where(rng.random(H // 32) < 0.5, -3.0, 3.0)
+    bits = synth.bf16_bits_rne(v.astype(np.float32))
+    assert np.array_equal(bf16_to_f64(bits), v)
+    return bits
+
+
+def test_ffn_mxfp8_equals_decode_ffn_on_mxfp8_exact_values(oracle_lib):
+    # x exactly MXFP8-representable and h exactly MXFP8-representable: the prefill reading must give
+    # the decode FFN's result bit for bit (quantisation is the identity there).
+    # Wg row i picks 6 * 2^a_i * x_0 with x_0 = 3, so g_i = 18 * 2^a_i >= 18 and SiLU(g_i) = g_i in
+    # fp32 (exp(-18) < 2^-25); Wu row i picks +-2^b_i * x_j for an x_j that is a power of two, so
+    # h_i = g_i u_i has at most 4 significant bits.  Within each 32-block of h the exponents span
+    # 5 binades, inside E4M3's range below the block maximum.
+    H, I = 128, 96
+    rng = np.random.default_rng(11)
+    x = _mxfp8_exact_token(rng, H)
+    x[0] = 0x4040  # x_0 = +3
+    xf = bf16_to_f64(x)
+    pow2 = [c for c in range(H) if c % 32 and np.log2(abs(xf[c])) == np.round(np.log2(abs(xf[c])))]
+    assert len(pow2) >= 4
+    rec = synth.expert_records(9, 0, 4, H, I, experts=[2])[0].copy()
+    s = sections(rec, H, I)
+    gc = s["wg_codes"].reshape(I, H // 2)
+    uc = s["wu_codes"].reshape(I, H // 2)
+    gs = s["wg_scales"].reshape(I, H // 32)
+    us = s["wu_scales"].reshape(I, H // 32)
+    gc[:] = 0
+    uc[:] = 0
+    for i in range(I):
+        gc[i, 0] = 7  # code 7 = 6.0 in the low nibble: column 0
+        gs[i, 0] = 127 + rng.integers(0, 3)
+        c = pow2[rng.integers(0, len(pow2))]
+        uc[i, c // 2] = (2 | (8 if rng.random() < 0.5 else 0)) << (4 * (c & 1))  # +-1.0
+        us[i, c // 32] = 127 - rng.integers(0, 3)
+    h = oracle_lib.expert_gate_up(rec, H, I, x).astype(np.float64)
+    hq, _ = mxfp8_quant_np(h)
+    assert np.array_equal(hq, h)  # the construction really is MXFP8-exact
+    y8 = oracle_lib.expert_ffn_mxfp8(rec, H, I, x)
+    y = oracle_lib.expert_ffn(rec, H, I, x)
+    assert np.array_equal(y8.view(np.uint32), y.view(np.uint32))
+
+
 # ---------------------------------------------------------------- demand-filled LRU slot table
 
 def _read_demand_trace(name):
