@@ -281,7 +281,12 @@ cudaError_t prof_mark(moe_layer *L, int which, cudaStream_t s) {
         if (rc != cudaSuccess) return rc;
         v.push_back(e);
     }
-    return cudaEventRecord(v[n++], s);
+    // under stream capture the mark becomes an event-record node of the graph, so replays record times
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t rc = cudaStreamIsCapturing(s, &cs);
+    if (rc != cudaSuccess) return rc;
+    return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(v[n++], s, cudaEventRecordExternal)
+                                               : cudaEventRecord(v[n++], s);
 }
 
 // The next event of timed kernel `which` for a caller that records it itself (nullptr when not profiling).

@@ -26,7 +26,7 @@ EXPORTED = [
     "moe_debug_profile_read", "moe_debug_check_error", "moe_policy_step", "moe_route_noalloc", "moe_forward_cold",
     "moe_forward_cold_gpu", "moe_host_expert_ffn", "moe_policy_step_recency", "moe_layer_set_policy",
     "moe_layer_set_device_cache", "moe_debug_device_cache", "moe_debug_decode_fusion", "moe_prefetch_step",
-    "moe_prefetch",
+    "moe_prefetch", "moe_debug_stream_read",
 ]
 
 
@@ -99,6 +99,7 @@ def lib():
         L.moe_prefetch.argtypes = [p, p, i32, p, ctypes.POINTER(i32)]
         L.moe_debug_profile_read.argtypes = [p, p]
         L.moe_debug_check_error.argtypes = [p, ctypes.POINTER(i32)]
+        L.moe_debug_stream_read.argtypes = [p, ctypes.c_size_t, p, i32, p]
         L.moe_route_noalloc.argtypes = [p, i32, i32, p, p, i32, i32, p, ctypes.POINTER(RouteBuffers), p]
         L.moe_policy_step.argtypes = [p, p, p, p, i32, i32, p, ctypes.c_int64, ctypes.c_double, i32, p, p, p, p]
         for name in EXPORTED:
@@ -325,3 +326,8 @@ def host_expert_ffn(record, H, I, x_bits):
     y = np.empty(H, dtype=np.float32)
     check(lib().moe_host_expert_ffn(rec.ctypes.data_as(_P), H, I, x.ctypes.data_as(_P), y.ctypes.data_as(_P)))
     return y
+
+
+def stream_read(src, nbytes, sink, stream=None, nblocks=0):
+    """One launch of the library's streaming-read probe over ``nbytes`` bytes at device pointer ``src``."""
+    check(lib().moe_debug_stream_read(_P(int(src)), nbytes, _P(int(sink)), nblocks, stream_ptr(stream)))

@@ -371,6 +371,17 @@ int moe_debug_profile(moe_layer *layer, int32_t enable);
  * Errors: MOE_EINVAL (NULL layer). */
 int moe_debug_decode_fusion(moe_layer *layer, int32_t enable);
 
+/* Streaming-read probe for benchmarks (no counterpart on the pages; it does
+ * none of the layer's arithmetic): one launch on `stream` that reads `bytes`
+ * bytes of device memory at src_dev with 128-bit loads, the floor against
+ * which a weight-streaming kernel of the same byte count is measured.
+ * src_dev and bytes must be multiples of 16; sink_dev (4 bytes, device,
+ * caller-owned) is written only in the unlikely case the xor of all words
+ * read equals 0x9E3779B9.  nblocks = 0 picks four 512-thread blocks per SM.
+ * Asynchronous; nothing is allocated.  Errors: MOE_EINVAL (NULL or unaligned
+ * pointers, bytes not a multiple of 16, nblocks < 0), MOE_ECUDA. */
+int moe_debug_stream_read(const void *src_dev, size_t bytes, void *sink_dev, int32_t nblocks, void *stream);
+
 /* Sums of the timed kernels since moe_debug_profile: out[0] route ms,
  * out[1] gate/up ms (the one-launch FFN when M = 1 takes it), out[2] down
  * ms (its combine launch for one-launch calls), out[3] forward calls (waits
