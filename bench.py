@@ -673,7 +673,7 @@ def run_cold_host(args):
 
 
 SWEEP = [("LFU", "freq", 1.0), ("LFRU decay 0.9", "freq", 0.9), ("LFRU decay 0.7", "freq", 0.7),
-         ("LRU", "lru", 1.0), ("FIFO", "fifo", 1.0)]
+         ("LRU", "lru", 1.0), ("FIFO", "fifo", 1.0), ("SLRU", "slru", 1.0)]
 
 
 def run_policy_sweep(args):
@@ -695,7 +695,8 @@ def run_policy_sweep(args):
     L = w.layers if args.layers is None else args.layers
     steps = w.steps
     inputs = [stack.LayerInputs(w, l) for l in range(L)]
-    codes = {"freq": moe.MOE_POLICY_FREQ, "lru": moe.MOE_POLICY_LRU, "fifo": moe.MOE_POLICY_FIFO}
+    codes = {"freq": moe.MOE_POLICY_FREQ, "lru": moe.MOE_POLICY_LRU, "fifo": moe.MOE_POLICY_FIFO,
+             "slru": moe.MOE_POLICY_SLRU}
     x = torch.empty((L, 1, w.hidden), dtype=torch.bfloat16, device="cuda")
     out = torch.empty((L, 1, w.hidden), dtype=torch.bfloat16, device="cuda")
     biases = [[torch.from_numpy(synth.drifting_bias(0, l, w.experts, w.bias_tau, t, steps)).cuda()

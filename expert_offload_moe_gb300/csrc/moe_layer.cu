@@ -175,6 +175,7 @@ struct moe_layer {
     std::vector<double> score;
     int policy = MOE_POLICY_FREQ;
     std::vector<int64_t> loaded;  // FIFO: the step each expert entered its slot
+    std::vector<uint8_t> seg;     // SLRU: 1 while the expert is in the protected segment
     std::vector<int64_t> last;
     std::vector<uint8_t> in_flight;
     int64_t step = 0;
@@ -551,6 +552,7 @@ int moe_layer_create(const moe_layer_desc *desc, const float *router_w_dev, cons
     L->score.assign(d.num_experts, 0.0);
     L->last.assign(d.num_experts, -1);
     L->loaded.assign(d.num_experts, -1);
+    L->seg.assign(d.num_experts, 0);
     L->in_flight.assign(d.num_experts, 0);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
@@ -1005,6 +1007,7 @@ int moe_layer_set_device_cache(moe_layer *L, int32_t enable) {
         CUDA_TRY(cudaMemcpy(L->e2s.data(), L->e2s_dev, (size_t)E * 4, cudaMemcpyDeviceToHost));
         CUDA_TRY(cudaMemcpy(L->s2e.data(), L->lru.s2e, (size_t)S * 4, cudaMemcpyDeviceToHost));
         L->e2s_visible = L->e2s;
+        L->seg.assign(E, 0);  // SLRU segments start over from the device's map
         L->policy_seq = L->route_seq;  // the last route's decision was the device's
         L->dev_cache = false;
     }
@@ -1014,7 +1017,8 @@ int moe_layer_set_device_cache(moe_layer *L, int32_t enable) {
 int moe_layer_set_policy(moe_layer *L, int32_t policy) {
     g_err.clear();
     if (!L) return fail(MOE_EINVAL, "layer is NULL");
-    if (policy != MOE_POLICY_FREQ && policy != MOE_POLICY_LRU && policy != MOE_POLICY_FIFO)
+    if (policy != MOE_POLICY_FREQ && policy != MOE_POLICY_LRU && policy != MOE_POLICY_FIFO &&
+        policy != MOE_POLICY_SLRU)
         return fail(MOE_EINVAL, "unknown policy %d", policy);
     L->policy = policy;
     return MOE_OK;
@@ -1192,11 +1196,16 @@ int moe_cache_update(moe_layer *L, void *stream, int32_t *n_refills_out) {
     // the decision runs on copies so that an injected fault leaves the state unchanged
     std::vector<double> score = L->score;
     std::vector<int64_t> last = L->last, loaded = L->loaded;
+    std::vector<uint8_t> seg = L->seg;
     std::vector<int32_t> e2s = L->e2s, s2e = L->s2e;
     const int n =
         L->policy == MOE_POLICY_FREQ
             ? moe_policy_step(score.data(), last.data(), e2s.data(), s2e.data(), E, S, L->m_hist, L->step,
                               (double)L->d.score_decay, R, L->in_flight.data(), pe.data(), ps.data(), pv.data())
+        : L->policy == MOE_POLICY_SLRU
+            ? moe_policy_step_slru(score.data(), last.data(), seg.data(), e2s.data(), s2e.data(), E, S, L->m_hist,
+                                   L->step, (double)L->d.score_decay, R, (4 * S) / 5, L->in_flight.data(), pe.data(),
+                                   ps.data(), pv.data())
             : moe_policy_step_recency(L->policy, score.data(), last.data(), loaded.data(), e2s.data(), s2e.data(), E,
                                       S, L->m_hist, L->step, (double)L->d.score_decay, R, L->in_flight.data(),
                                       pe.data(), ps.data(), pv.data());
@@ -1208,6 +1217,7 @@ int moe_cache_update(moe_layer *L, void *stream, int32_t *n_refills_out) {
     L->score.swap(score);
     L->last.swap(last);
     L->loaded.swap(loaded);
+    L->seg.swap(seg);
     L->e2s.swap(e2s);
     L->s2e.swap(s2e);
     L->step++;
@@ -1301,6 +1311,7 @@ int moe_prefetch(moe_layer *L, const void *x_dev, int32_t M, void *stream, int32
     }
     L->e2s.swap(e2s);
     L->s2e.swap(s2e);
+    for (int i = 0; i < n; ++i) L->seg[pe[i]] = L->seg[pv[i]] = 0;  // SLRU: prefetched experts are probationary
     if (int rc = issue_refills(L, n, pe.data(), ps.data(), pv.data(), st)) return rc;
     if (n_refills_out) *n_refills_out = n;
     return MOE_OK;

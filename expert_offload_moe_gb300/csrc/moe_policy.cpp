@@ -117,6 +117,65 @@ extern "C" int moe_policy_step_recency(int32_t policy, double *score, int64_t *l
     return n;
 }
 
+// Segmented LRU (tinyserve README "Configuration" lists slru among the cache policies): hits are promoted
+// to a protected segment of at most pcap residents, its least recently routed members fall back to the
+// probationary segment, and victims come from the probationary segment before the protected one.
+extern "C" int moe_policy_step_slru(double *score, int64_t *last, uint8_t *seg, int32_t *e2s, int32_t *s2e,
+                                    int32_t E, int32_t S, const int32_t *hist, int64_t step, double decay,
+                                    int32_t R, int32_t pcap, const uint8_t *in_flight, int32_t *pair_expert,
+                                    int32_t *pair_slot, int32_t *pair_victim) {
+    if (!score || !last || !seg || !e2s || !s2e || !hist || E <= 0 || S <= 0 || S > E || R < 0 || pcap < 0 ||
+        pcap > S || (R > 0 && (!pair_expert || !pair_slot || !pair_victim)))
+        return -1;
+    for (int32_t e = 0; e < E; ++e) {
+        const double decayed = decay * score[e];
+        score[e] = decayed + static_cast<double>(hist[e]);
+        if (hist[e] > 0) last[e] = step;
+        if (hist[e] > 0 && e2s[e] >= 0) seg[e] = 1;
+    }
+    // residents by (last use, slot): the order of both demotion and eviction within a segment
+    std::vector<int32_t> order;
+    for (int32_t s = 0; s < S; ++s)
+        if (s2e[s] >= 0) order.push_back(s2e[s]);
+    std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return last[a] < last[b]; });
+    int32_t nprot = 0;
+    for (int32_t e : order) nprot += seg[e] ? 1 : 0;
+    for (int32_t e : order) {
+        if (nprot <= pcap) break;
+        if (seg[e]) {
+            seg[e] = 0;
+            --nprot;
+        }
+    }
+    auto busy = [&](int32_t e) { return in_flight && in_flight[e]; };
+    std::vector<int32_t> cand;
+    for (int32_t e = 0; e < E; ++e)
+        if (e2s[e] < 0 && hist[e] > 0 && !busy(e)) cand.push_back(e);
+    std::stable_sort(cand.begin(), cand.end(), [&](int32_t a, int32_t b) { return hist[a] > hist[b]; });
+    std::vector<int32_t> vic;
+    for (int32_t e : order)
+        if (!seg[e] && !busy(e)) vic.push_back(e);
+    for (int32_t e : order)
+        if (seg[e] && !busy(e)) vic.push_back(e);
+    int32_t n = 0;
+    const size_t np = std::min(cand.size(), vic.size());
+    for (size_t i = 0; i < np && n < R; ++i) {
+        if (last[vic[i]] >= step) break;
+        pair_expert[n] = cand[i];
+        pair_slot[n] = e2s[vic[i]];
+        pair_victim[n] = vic[i];
+        ++n;
+    }
+    for (int32_t i = 0; i < n; ++i) {
+        e2s[pair_victim[i]] = -1;
+        seg[pair_victim[i]] = 0;
+        e2s[pair_expert[i]] = pair_slot[i];
+        s2e[pair_slot[i]] = pair_expert[i];
+        seg[pair_expert[i]] = 0;
+    }
+    return n;
+}
+
 // Next-layer prefetch (tinyserve README "How it works" 4, FATE: the current layer's activations predict the
 // next layer's experts; their copies overlap the current layer's work).  pred[e] counts the predicted routes
 // of expert e (the next layer's routing applied to the current layer's input).  Candidates: predicted experts

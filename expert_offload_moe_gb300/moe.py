@@ -16,7 +16,7 @@ MOE_OK, MOE_EINVAL, MOE_ENOMEM, MOE_ECUDA, MOE_ETIMEOUT, MOE_ESTATE = range(6)
 MOE_OUT_BF16, MOE_OUT_F32 = 0, 1
 MOE_VIS_DETERMINISTIC, MOE_VIS_POLLED = 0, 1
 MOE_FAULT_NONE, MOE_FAULT_COPY = 0, 1
-MOE_POLICY_FREQ, MOE_POLICY_LRU, MOE_POLICY_FIFO = 0, 1, 2
+MOE_POLICY_FREQ, MOE_POLICY_LRU, MOE_POLICY_FIFO, MOE_POLICY_SLRU = 0, 1, 2, 3
 MOE_FMT_MXFP4, MOE_FMT_NVFP4 = 0, 1
 
 EXPORTED = [
@@ -26,7 +26,7 @@ EXPORTED = [
     "moe_debug_profile_read", "moe_debug_check_error", "moe_policy_step", "moe_route_noalloc", "moe_forward_cold",
     "moe_forward_cold_gpu", "moe_host_expert_ffn", "moe_policy_step_recency", "moe_layer_set_policy",
     "moe_layer_set_device_cache", "moe_debug_device_cache", "moe_debug_decode_fusion", "moe_prefetch_step",
-    "moe_prefetch", "moe_debug_stream_read",
+    "moe_prefetch", "moe_debug_stream_read", "moe_policy_step_slru",
 ]
 
 
@@ -79,6 +79,8 @@ def lib():
         L.moe_policy_step_recency.argtypes = [i32, p, p, p, p, p, i32, i32, p, ctypes.c_int64, ctypes.c_double,
                                               i32, p, p, p, p]
         L.moe_layer_set_policy.argtypes = [p, i32]
+        L.moe_policy_step_slru.argtypes = [p, p, p, p, p, i32, i32, p, ctypes.c_int64, ctypes.c_double, i32, i32,
+                                           p, p, p, p]
         L.moe_layer_set_device_cache.argtypes = [p, i32]
         L.moe_debug_device_cache.argtypes = [p, p]
         L.moe_host_expert_ffn.argtypes = [p, i32, i32, p, p]
@@ -297,6 +299,24 @@ def policy_step_recency(policy, score, last, loaded, e2s, s2e, hist, step, decay
                                       ps.ctypes.data_as(_P), pv.ctypes.data_as(_P))
     if n < 0:
         raise MoeError(MOE_EINVAL, "moe_policy_step_recency rejected its arguments")
+    return [(int(pe[i]), int(ps[i]), int(pv[i])) for i in range(n)]
+
+
+def policy_step_slru(score, last, seg, e2s, s2e, hist, step, decay, R, pcap, in_flight=None):
+    """The library's segmented-LRU slot decision on numpy arrays (updated in place)."""
+    import numpy as np
+
+    E, S = e2s.shape[0], s2e.shape[0]
+    pe, ps, pv = (np.zeros(max(R, 1), dtype=np.int32) for _ in range(3))
+    fl = None if in_flight is None else np.ascontiguousarray(in_flight, dtype=np.uint8)
+    hist = np.ascontiguousarray(hist, dtype=np.int32)
+    n = lib().moe_policy_step_slru(score.ctypes.data_as(_P), last.ctypes.data_as(_P), seg.ctypes.data_as(_P),
+                                   e2s.ctypes.data_as(_P), s2e.ctypes.data_as(_P), E, S, hist.ctypes.data_as(_P),
+                                   int(step), float(decay), int(R), int(pcap),
+                                   None if fl is None else fl.ctypes.data_as(_P), pe.ctypes.data_as(_P),
+                                   ps.ctypes.data_as(_P), pv.ctypes.data_as(_P))
+    if n < 0:
+        raise MoeError(MOE_EINVAL, "moe_policy_step_slru rejected its arguments")
     return [(int(pe[i]), int(ps[i]), int(pv[i])) for i in range(n)]
 
 

@@ -102,9 +102,14 @@ enum { MOE_FMT_MXFP4 = 0, MOE_FMT_NVFP4 = 1 };
  *  MOE_POLICY_LRU   evict the resident expert routed longest ago, never one
  *                   this step routed
  *  MOE_POLICY_FIFO  evict the resident expert that entered its slot first
+ *  MOE_POLICY_SLRU  segmented LRU (tinyserve README "Configuration" lists
+ *                   slru): a probationary and a protected segment of four
+ *                   fifths of the slots; a hit is protected, new experts
+ *                   are probationary and probationary ones are evicted first
+ *                   (moe_policy_step_slru)
  * In every policy the candidates for a slot are non-resident experts,
  * at most max_refills_per_step per step. */
-enum { MOE_POLICY_FREQ = 0, MOE_POLICY_LRU = 1, MOE_POLICY_FIFO = 2 };
+enum { MOE_POLICY_FREQ = 0, MOE_POLICY_LRU = 1, MOE_POLICY_FIFO = 2, MOE_POLICY_SLRU = 3 };
 
 typedef struct moe_layer moe_layer;
 
@@ -445,6 +450,29 @@ int moe_policy_step_recency(int32_t policy, double *score, int64_t *last, int64_
                             int32_t *s2e, int32_t E, int32_t S, const int32_t *hist, int64_t step, double decay,
                             int32_t R, const uint8_t *in_flight, int32_t *pair_expert, int32_t *pair_slot,
                             int32_t *pair_victim);
+
+/* Segmented LRU (MOE_POLICY_SLRU; tinyserve README "Configuration" names slru
+ * among its cache policies and gives no details, so the textbook two-segment
+ * scheme is used).  seg[e] is 1 while resident expert e is in the protected
+ * segment, 0 otherwise; at most pcap residents are protected (layers use
+ * pcap = 4 S / 5, rounded down).  One step:
+ *   1. last[e] = step for every expert this step routed (score[] keeps the
+ *      decayed frequency for reference);
+ *   2. every routed resident expert becomes protected;
+ *   3. while more than pcap residents are protected, the protected one with
+ *      the oldest last[e] (ties: lower slot) returns to probationary;
+ *   4. candidates: non-resident experts this step routed, most routes first
+ *      (ties: lower id); victims: probationary residents by oldest last[e],
+ *      then protected ones by oldest last[e] (ties: lower slot); experts in
+ *      flight are neither; candidate i replaces victim i while that victim
+ *      was not routed this step, at most R pairs; new experts enter the
+ *      probationary segment.
+ * score[], last[], seg[], e2s[E] and s2e[S] are updated in place.  Returns
+ * the number of (expert, slot, victim) pairs, or -1 on bad arguments
+ * (NULL arrays, E, S or R out of range, pcap < 0 or > S). */
+int moe_policy_step_slru(double *score, int64_t *last, uint8_t *seg, int32_t *e2s, int32_t *s2e, int32_t E, int32_t S,
+                         const int32_t *hist, int64_t step, double decay, int32_t R, int32_t pcap,
+                         const uint8_t *in_flight, int32_t *pair_expert, int32_t *pair_slot, int32_t *pair_victim);
 
 /* Selects the slot policy of a layer (MOE_POLICY_*, default MOE_POLICY_FREQ)
  * for its later moe_cache_update calls.  Errors: MOE_EINVAL. */

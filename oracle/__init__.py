@@ -80,6 +80,9 @@ def _declare(L):
     L.oracle_cache_step_recency.argtypes = [I32, P, P, P, P, P, I32, I32, P, ctypes.c_int64, ctypes.c_double, I32,
                                             P, P, P, P]
     L.oracle_cache_step_recency.restype = I32
+    L.oracle_cache_step_slru.argtypes = [P, P, P, P, P, I32, I32, P, ctypes.c_int64, ctypes.c_double, I32, I32, P,
+                                         P, P, P]
+    L.oracle_cache_step_slru.restype = I32
     L.oracle_demand_lru_step.argtypes = [P, P, P, I32, I32, P, ctypes.c_int64, P, P]
     L.oracle_demand_lru_step.restype = I32
     L.oracle_prefetch_step.argtypes = [P, P, P, P, I32, I32, P, I32, P, P, P, P]
@@ -248,14 +251,19 @@ def moe_layer(x_bf16, Wr, bias, experts, e2s, k, H, I, fmt="mxfp4"):
     return out
 
 
-POLICIES = {"freq": 0, "lru": 1, "fifo": 2}
+POLICIES = {"freq": 0, "lru": 1, "fifo": 2, "slru": 3}
+
+
+def slru_protected_cap(S):
+    """Protected segment of the SLRU reading: four fifths of the slots (rounded down)."""
+    return (4 * S) // 5
 
 
 class CacheReplay:
     """Step-by-step replay of the slot cache policy for one layer.  policy: "freq" (decayed frequency:
-    LFU / LFRU), "lru" or "fifo"."""
+    LFU / LFRU), "lru", "fifo" or "slru" (segmented LRU; ``pcap`` protected slots, default four fifths)."""
 
-    def __init__(self, e2s, S, decay=1.0, R=2, policy="freq"):
+    def __init__(self, e2s, S, decay=1.0, R=2, policy="freq", pcap=None):
         self.e2s = _c(e2s, np.int32).copy()
         self.E = self.e2s.shape[0]
         self.S = S
@@ -269,6 +277,8 @@ class CacheReplay:
         self.R = int(R)
         self.policy = POLICIES[policy]
         self.loaded = np.full(self.E, -1, dtype=np.int64)
+        self.seg = np.zeros(self.E, dtype=np.uint8)  # SLRU: 1 = protected segment
+        self.pcap = slru_protected_cap(S) if pcap is None else int(pcap)
 
     def step(self, hist, step, in_flight=None):
         hist = _c(hist, np.int32)
@@ -280,6 +290,10 @@ class CacheReplay:
             n = lib().oracle_cache_step(_p(self.score), _p(self.last), _p(self.e2s), _p(self.s2e), self.E,
                                         self.S, _p(hist), int(step), self.decay, self.R, _p(fl), _p(pe),
                                         _p(ps), _p(pv))
+        elif self.policy == 3:
+            n = lib().oracle_cache_step_slru(_p(self.score), _p(self.last), _p(self.seg), _p(self.e2s),
+                                             _p(self.s2e), self.E, self.S, _p(hist), int(step), self.decay, self.R,
+                                             self.pcap, _p(fl), _p(pe), _p(ps), _p(pv))
         else:
             n = lib().oracle_cache_step_recency(self.policy, _p(self.score), _p(self.last), _p(self.loaded),
                                                 _p(self.e2s), _p(self.s2e), self.E, self.S, _p(hist), int(step),

@@ -442,6 +442,79 @@ int oracle_cache_step_recency(int policy, double *score, int64_t *last, int64_t 
     return n;
 }
 
+/* Segmented LRU (tinyserve README "Configuration" lists slru among its cache
+ * policies beside lru, lfru, lfu and fifo; "How it works" 3).  The pages
+ * give no details; this follows the textbook two-segment scheme.  Resident
+ * experts are either probationary (seg 0) or protected (seg 1); at most
+ * pcap of them are protected.  Per step:
+ *   1. last[e] = step for every routed expert; score keeps the decayed
+ *      frequency for reference only.
+ *   2. a routed resident expert that is probationary becomes protected;
+ *   3. while more than pcap residents are protected, the protected one
+ *      routed longest ago (ties: lower slot) goes back to probationary;
+ *   4. candidates: non-resident experts routed this step, most routes
+ *      first (ties: lower id); victims: the probationary residents, routed
+ *      longest ago first (ties: lower slot), then the protected ones in the
+ *      same order; experts in flight are neither.  Candidate i replaces
+ *      victim i while that victim was not routed this step, at most R pairs;
+ *      a new expert enters probationary.
+ * Returns the number of (expert, slot, victim) pairs. */
+int oracle_cache_step_slru(double *score, int64_t *last, uint8_t *seg, int32_t *e2s, int32_t *s2e, int E, int S,
+                           const int32_t *hist, int64_t step, double decay, int R, int pcap,
+                           const uint8_t *in_flight, int32_t *pair_expert, int32_t *pair_slot,
+                           int32_t *pair_victim) {
+    int e, s, p, n = 0;
+    char *used = (char *)calloc((size_t)E, 1);
+    for (e = 0; e < E; ++e) {
+        score[e] = decay * score[e] + (double)hist[e];
+        if (hist[e] > 0) last[e] = step;
+    }
+    /* promotion of this step's hits */
+    for (e = 0; e < E; ++e)
+        if (e2s[e] >= 0 && hist[e] > 0) seg[e] = 1;
+    /* demotion down to the protected capacity */
+    for (;;) {
+        int nprot = 0, worst = -1;
+        for (s = 0; s < S; ++s) {
+            int r = s2e[s];
+            if (r < 0 || !seg[r]) continue;
+            ++nprot;
+            if (worst < 0 || last[r] < last[worst]) worst = r; /* ascending slot: ties keep the lower slot */
+        }
+        if (nprot <= pcap) break;
+        seg[worst] = 0;
+    }
+    for (p = 0; p < R; ++p) {
+        int cand = -1, vic = -1;
+        for (e = 0; e < E; ++e) {
+            if (e2s[e] >= 0 || used[e] || hist[e] <= 0 || (in_flight && in_flight[e])) continue;
+            if (cand < 0 || hist[e] > hist[cand]) cand = e;
+        }
+        if (cand < 0) break;
+        for (s = 0; s < S; ++s) {
+            int r = s2e[s];
+            if (r < 0 || used[r] || (in_flight && in_flight[r])) continue;
+            if (vic < 0 || seg[r] < seg[vic] || (seg[r] == seg[vic] && last[r] < last[vic])) vic = r;
+        }
+        if (vic < 0 || last[vic] >= step) break; /* never evicts an expert this step routed */
+        used[cand] = 1;
+        used[vic] = 1;
+        pair_expert[n] = cand;
+        pair_slot[n] = e2s[vic];
+        pair_victim[n] = vic;
+        ++n;
+    }
+    for (p = 0; p < n; ++p) {
+        e2s[pair_victim[p]] = -1;
+        seg[pair_victim[p]] = 0;
+        e2s[pair_expert[p]] = pair_slot[p];
+        s2e[pair_slot[p]] = pair_expert[p];
+        seg[pair_expert[p]] = 0;
+    }
+    free(used);
+    return n;
+}
+
 /* Demand-filled LRU slot table (xinfer docs "How it works", Decode: before
  * the expert GEMMs, a kernel looks the routed experts up in a per-layer LRU
  * table kept on the GPU, gives least-recently-used slots to the misses and

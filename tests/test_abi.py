@@ -170,6 +170,57 @@ def test_recency_policy_rejects_bad_arguments(lib):
                                 np.array([0, 1], dtype=np.int32), np.zeros(E, dtype=np.int32), 0, 1.0, 1)
 
 
+@pytest.mark.parametrize("R,E,S,pcap", [(2, 32, 16, None), (1, 16, 4, None), (4, 64, 48, None), (2, 32, 16, 0),
+                                         (2, 32, 16, 16), (3, 12, 5, 2)])
+def test_library_slru_matches_oracle_replay(lib, oracle_lib, R, E, S, pcap):
+    rng = np.random.default_rng(R * 31 + E + S)
+    e2s0 = np.full(E, -1, dtype=np.int32)
+    e2s0[rng.choice(E, S, replace=False)] = rng.permutation(S)
+    rp = oracle_lib.CacheReplay(e2s0, S, R=R, policy="slru", pcap=pcap)
+    score, last = np.zeros(E), np.full(E, -1, dtype=np.int64)
+    seg = np.zeros(E, dtype=np.uint8)
+    e2s = e2s0.copy()
+    s2e = np.full(S, -1, dtype=np.int32)
+    s2e[e2s[e2s >= 0]] = np.nonzero(e2s >= 0)[0]
+    n_pairs = 0
+    for st, hist in _random_trace(rng, E, 4, 300, drift=True):
+        fl = (rng.random(E) < 0.1).astype(np.uint8)
+        a = moe.policy_step_slru(score, last, seg, e2s, s2e, hist, st, 1.0, R, rp.pcap, in_flight=fl)
+        b = rp.step(hist, st, fl)
+        assert a == b, st
+        assert np.array_equal(e2s, rp.e2s) and np.array_equal(s2e, rp.s2e) and np.array_equal(seg, rp.seg)
+        n_pairs += len(a)
+    assert n_pairs > 0
+
+
+def test_library_slru_golden_trace(lib):
+    lines = [l.split() for l in open(os.path.join(ROOT, "tests", "golden", "cache_slru_trace.txt"))
+             if l.strip() and l[0] != "#"]
+    E, S, R = int(lines[0][1]), int(lines[0][3]), int(lines[0][5])
+    e2s = np.array([int(v) for v in lines[1][1:]], dtype=np.int32)
+    s2e = np.full(S, -1, dtype=np.int32)
+    s2e[e2s[e2s >= 0]] = np.nonzero(e2s >= 0)[0]
+    score, last, seg = np.zeros(E), np.full(E, -1, dtype=np.int64), np.zeros(E, dtype=np.uint8)
+    for l in lines[2:]:
+        st = int(l[1])
+        i_p, i_m = l.index("pairs"), l.index("map")
+        hist = np.array([int(v) for v in l[3:i_p]], dtype=np.int32)
+        want = [tuple(int(q) for q in p.split(":")) for p in l[i_p + 1:i_m]]
+        assert moe.policy_step_slru(score, last, seg, e2s, s2e, hist, st, 1.0, R, (4 * S) // 5) == want, st
+        assert list(e2s) == [int(v) for v in l[i_m + 1:]]
+
+
+def test_slru_rejects_bad_arguments(lib):
+    E, S = 4, 2
+    args = (np.zeros(E), np.zeros(E, dtype=np.int64), np.zeros(E, dtype=np.uint8),
+            np.array([0, 1, -1, -1], dtype=np.int32), np.array([0, 1], dtype=np.int32), np.zeros(E, dtype=np.int32),
+            0, 1.0, 1)
+    for pcap in (-1, S + 1):
+        with pytest.raises(moe.MoeError):
+            moe.policy_step_slru(*args, pcap)
+    assert lib.moe_layer_set_policy(None, moe.MOE_POLICY_SLRU) == moe.MOE_EINVAL
+
+
 @pytest.mark.parametrize("R,E,S", [(2, 32, 16), (1, 16, 4), (4, 64, 48), (3, 8, 8)])
 def test_library_prefetch_step_matches_oracle(lib, oracle_lib, R, E, S):
     rng = np.random.default_rng(R * 100 + E)

@@ -42,7 +42,8 @@ def drive(visibility, decay, steps, M, R=2, seed=0, policy="freq"):
     w = SMALL
     li = stack.LayerInputs(w, 0, seed=seed, e2s=least_popular_placement(seed, w.experts, w.slots))
     lay = li.make_layer(max_tokens=8, out_f32=True, max_refills=R, score_decay=decay, visibility=visibility)
-    lay.set_policy({"freq": moe.MOE_POLICY_FREQ, "lru": moe.MOE_POLICY_LRU, "fifo": moe.MOE_POLICY_FIFO}[policy])
+    lay.set_policy({"freq": moe.MOE_POLICY_FREQ, "lru": moe.MOE_POLICY_LRU, "fifo": moe.MOE_POLICY_FIFO,
+                    "slru": moe.MOE_POLICY_SLRU}[policy])
     replay = oracle.CacheReplay(li.e2s, w.slots, decay=decay, R=R, policy=policy)
     refills = 0
     for st in range(steps):
@@ -77,9 +78,9 @@ def test_deterministic_refills_follow_oracle_replay():
         assert st_[1] == st_[0] * SMALL.expert_bytes
 
 
-@pytest.mark.parametrize("policy", ["lru", "fifo"])
+@pytest.mark.parametrize("policy", ["lru", "fifo", "slru"])
 def test_recency_policies_follow_oracle_replay(policy):
-    """LRU and FIFO slots on the GPU: each step's refills and map equal the oracle's replay, and every
+    """LRU, FIFO and SLRU slots on the GPU: each step's refills and map equal the oracle's replay, and every
     refilled slot holds its expert's bytes."""
     for st, lay, li, replay, o, n, _ in drive(moe.MOE_VIS_DETERMINISTIC, 1.0, 40, 2, policy=policy):
         pairs = replay.step(o["hist"], st)

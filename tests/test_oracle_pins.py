@@ -371,7 +371,7 @@ def _read_trace(name):
 
 
 @pytest.mark.parametrize("trace", ["cache_lfu_trace.txt", "cache_lfru_trace.txt", "cache_lru_trace.txt",
-                                   "cache_fifo_trace.txt"])
+                                   "cache_fifo_trace.txt", "cache_slru_trace.txt"])
 def test_cache_policy_hand_worked_trace(oracle_lib, trace):
     E, S, R, decay, init, steps, policy = _read_trace(trace)
     rp = oracle_lib.CacheReplay(np.array(init, dtype=np.int32), S, decay=decay, R=R, policy=policy)
@@ -410,6 +410,42 @@ def test_recency_policies_keep_budget_and_map(oracle_lib, policy):
             assert hist[e] > 0  # only experts this step routed come in
             if policy == "lru":
                 assert hist[v] == 0  # LRU never evicts an expert this step routed
+
+
+def test_slru_segments_keep_capacity_budget_and_map(oracle_lib):
+    rng = np.random.default_rng(17)
+    E, S, R = 32, 16, 2
+    rp = oracle_lib.CacheReplay(np.where(np.arange(E) < S, np.arange(E), -1).astype(np.int32), S, R=R,
+                                policy="slru")
+    assert rp.pcap == 12
+    for st in range(300):
+        hist = np.bincount(rng.choice(E, 4, replace=False), minlength=E).astype(np.int32)
+        before = rp.e2s.copy()
+        pairs = rp.step(hist, st)
+        assert len(pairs) <= R
+        res = np.flatnonzero(rp.e2s >= 0)
+        assert len(res) == S and len(set(rp.e2s[res].tolist())) == S
+        assert int(rp.seg[res].sum()) <= rp.pcap and not rp.seg[rp.e2s < 0].any()
+        for e, _slot, v in pairs:
+            assert hist[e] > 0 and hist[v] == 0 and before[e] < 0 and rp.seg[e] == 0
+        for e in np.flatnonzero((hist > 0) & (before >= 0)):
+            # a hit is protected after the step unless demoted for the capacity, which only happens when
+            # every protected expert was routed this step
+            if not rp.seg[e]:
+                assert all(hist[p] > 0 for p in np.flatnonzero(rp.seg))
+
+
+def test_slru_without_a_protected_segment_is_lru(oracle_lib):
+    # pcap = 0: no protected segment, victims by recency alone = the LRU replay, step for step
+    rng = np.random.default_rng(19)
+    E, S, R = 12, 5, 2
+    init = np.where(np.arange(E) < S, np.arange(E), -1).astype(np.int32)
+    a = oracle_lib.CacheReplay(init, S, R=R, policy="slru", pcap=0)
+    b = oracle_lib.CacheReplay(init, S, R=R, policy="lru")
+    for st in range(200):
+        hist = np.bincount(rng.choice(E, 3, replace=False), minlength=E).astype(np.int32)
+        assert a.step(hist, st) == b.step(hist, st)
+        assert np.array_equal(a.e2s, b.e2s)
 
 
 def test_lru_with_every_resident_routed_takes_no_pair(oracle_lib):
