@@ -237,11 +237,7 @@ __global__ void __launch_bounds__(kThreads) down_kernel(DecodeParams p, int M) {
 // 1, 2, 4, 8 that covers M (a slot never serves more tokens than M).
 template <int kM, bool kNv>
 void gateup_launch(const DecodeParams &p, int M, cudaStream_t s, int num_sms) {
-    static bool configured = false;
-    if (!configured) {
-        cudaFuncSetAttribute(gateup_kernel<kM, kNv>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmemLimit);
-        configured = true;
-    }
+    ensure_dyn_smem(reinterpret_cast<const void *>(gateup_kernel<kM, kNv>), kDecodeSmemLimit);
     gateup_kernel<kM, kNv><<<num_sms * 4, kThreads, (size_t)M * p.geo.H * sizeof(float), s>>>(p, M);
 }
 

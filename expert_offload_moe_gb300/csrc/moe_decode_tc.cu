@@ -20,7 +20,9 @@
 // The activation operand must be 8-bit, so each value is split exactly into
 // E4M3 terms with one E8M0 scale per 32-element block along K: x (bf16, 8-bit
 // significand) = 2 terms, reproduced exactly for every element within 2^14 of
-// its block's largest magnitude; w h (fp32) = 4 terms (16 significant bits).
+// its block's largest magnitude; w h (fp32) = 8 terms, each taking 4 more
+// significant bits of the block's largest residual (32 bits below the block's
+// largest magnitude: h may span a wide range within 32 consecutive rows).
 // Each term is one more column of the B operand, and the columns of a token
 // are summed after the MMA.  The routing weight is folded into the down
 // operand (w h), so the down MMA accumulates the sum over experts of w Wd h in
@@ -51,12 +53,12 @@ constexpr int kTileA = 128 * 128;       // one 128 x 128 E2M1 tile, one byte per
 constexpr int kTileATx = 128 * 128 / 2; // bytes a TMA copy of that tile moves (the packed codes)
 constexpr int kAtom = kTcAtomBytes;
 constexpr int NBX = kTcXRows;           // B columns of gate/up: 2 x terms x <= 8 tokens
-constexpr int NBH = kTcHRows;           // B columns of down: 4 w*h terms x <= 8 tokens
-constexpr int kHTerms = 4;
+constexpr int NBH = kTcHRows;           // B columns of down: 8 w*h terms x <= 8 tokens
+constexpr int kHTerms = 8;
 constexpr int kGateStages = 3, kDownStages = 4;
 // stage layout: [A tiles][B tile][atoms], 1024-aligned for the 128-byte swizzle
 constexpr int kGateStage = 2 * kTileA + NBX * 128 + 3 * kAtom + 512;   // 36 KB
-constexpr int kDownStage = kTileA + NBH * 128 + 2 * kAtom + 1024;       // 22 KB
+constexpr int kDownStage = kTileA + NBH * 128 + 2 * kAtom + 1024;       // 26 KB
 static_assert(kGateStage % 1024 == 0 && kDownStage % 1024 == 0, "stage alignment");
 // Accumulators per operand: MMA slice kk of a k-step accumulates into kk % kAcc (summed in the epilogue).
 // More than one did not shorten a k-step on GB300 (the MMA chain is not the bottleneck), so one.
@@ -104,7 +106,7 @@ struct GateUpArgs {
     const int32_t *counts, *act_slot, *act_off, *act_cnt, *hot_token;
     const float *hot_w;
     const uint8_t *xat;  // x atoms [nks][512]
-    uint8_t *hq, *hat;   // w*h terms [n_act_cap][32][Ipad], atoms [n_act_cap][nksI][512]
+    uint8_t *hq, *hat;   // w*h terms [n_act_cap][64][Ipad], atoms [n_act_cap][nksI][512]
     int Ipad;
     int *err;
 };
@@ -341,7 +343,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint8_t code = split_term(res, sb);
                     const int n = t * T + term;
                     hq[(size_t)n * a.Ipad + row] = code;
-                    if (lane == 0) hat[(size_t)(kblock / 4) * kAtom + n * 16 + (kblock % 4)] = (uint8_t)sb;
+                    // B-operand scale of column n: lane n % 32, column n / 32 of the atom
+                    if (lane == 0)
+                        hat[(size_t)(kblock / 4) * kAtom + (n & 31) * 16 + (n >> 5) * 4 + (kblock % 4)] = (uint8_t)sb;
                 }
             }
         }
@@ -591,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------ one launch for M = 1
 
 constexpr int kFfnThreads = 192;  // warps 0-3: epilogue (TMEM lane quadrant = warp); warp 4: copies; warp 5: MMAs
-constexpr int kFfnNB = 16;        // B columns of the down MMA: 4 w*h terms of the one token, 12 zero columns
+constexpr int kFfnNB = 16;        // B columns of the down MMA: 8 w*h terms of the one token, 8 zero columns
 constexpr int kErrHReady = 4, kErrAccFull = 5, kErrAccEmpty = 6;
 
 struct FfnArgs {
@@ -608,7 +612,7 @@ struct FfnArgs {
 // The whole expert FFN of a one-token decode step in one launch.  grid: (active expert, 128-row tile j of I,
 // K split), the K splits of a tile being one cluster.  Each cluster
 //   1. computes g, u for its I tile as gate/up does (K split over the CTAs, partials summed in rank order),
-//   2. forms h = w SiLU(g) u for the tile's 128 rows in every CTA and splits it into four E4M3 terms held in
+//   2. forms h = w SiLU(g) u for the tile's 128 rows in every CTA and splits it into eight E4M3 terms held in
 //      shared memory (the B operand of the down MMA, never written to global memory),
 //   3. multiplies the tile's column slice of Wd (all H rows, 128 columns) by it: CTA r takes H tiles
 //      r, r + KS, ...; its copy warp streams those weight tiles into the pipeline right behind the gate/up
@@ -952,8 +956,8 @@ __global__ void __launch_bounds__(128) ffn_combine_kernel(const float *part, con
 }
 
 template <typename K>
-void set_smem(K kernel, int bytes) {
-    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+cudaError_t set_smem(K kernel, int bytes) {
+    return ensure_dyn_smem(reinterpret_cast<const void *>(kernel), (size_t)bytes);
 }
 
 // Launch with the K splits of a tile as one cluster and programmatic serialization after the previous grid.
@@ -1044,8 +1048,7 @@ cudaError_t launch_gateup_tc(const TcLaunch &L, cudaStream_t s) {
     a.err = L.err;
     if (a.KS < 1 || a.KS > kMaxCluster) return cudaErrorInvalidValue;
     const int grid = L.n_act_max * l.ntI * a.KS;
-    static bool cfg = false;
-    if (!cfg) set_smem(gateup_tc_kernel, tc_gateup_smem()), cfg = true;
+    if (cudaError_t e = set_smem(gateup_tc_kernel, tc_gateup_smem())) return e;
     return launch_ex(gateup_tc_kernel, grid, a.KS, tc_gateup_smem(), s, *L.mapG, *L.mapU, *L.mapX, a);
 }
 
@@ -1070,8 +1073,7 @@ cudaError_t launch_down_tc(const TcLaunch &L, cudaStream_t s) {
     a.err = L.err;
     if (a.KS < 1 || a.KS > kMaxCluster) return cudaErrorInvalidValue;
     const int grid = l.ntH * a.KS;
-    static bool cfg = false;
-    if (!cfg) set_smem(down_tc_kernel, tc_down_smem()), cfg = true;
+    if (cudaError_t e = set_smem(down_tc_kernel, tc_down_smem())) return e;
     return launch_ex(down_tc_kernel, grid, a.KS, tc_down_smem(), s, *L.mapD, *L.mapH, a);
 }
 
@@ -1108,8 +1110,7 @@ cudaError_t launch_ffn_tc(const TcLaunch &L, cudaStream_t s) {
     if (L.M != 1 || a.KS < 1 || a.KS > kMaxCluster)
         return cudaErrorInvalidValue;
     const int grid = L.n_act_max * l.ntI * a.KS;
-    static bool cfg = false;
-    if (!cfg) set_smem(ffn_tc_kernel, tc_gateup_smem()), cfg = true;
+    if (cudaError_t e = set_smem(ffn_tc_kernel, tc_gateup_smem())) return e;
     return launch_ex_n(ffn_tc_kernel, grid, kFfnThreads, a.KS, tc_gateup_smem(), s, *L.mapG, *L.mapU, *L.mapX,
                        *L.mapD, a);
 }

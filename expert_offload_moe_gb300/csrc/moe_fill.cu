@@ -157,11 +157,9 @@ cudaError_t launch_slot_fill(const FillLaunch &F, cudaStream_t s) {
     a.n_fill = F.n_fill;
 
     const size_t smem = slot_fill_smem(g.H, g.I);
-    static size_t smem_set = 0;  // the kernel's dynamic shared memory limit raised so far
-    if (smem > 48 * 1024 && smem > smem_set) {
-        cudaError_t e = cudaFuncSetAttribute(slot_fill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (smem > 48 * 1024) {
+        cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void *>(slot_fill_kernel), smem);
         if (e != cudaSuccess) return e;
-        smem_set = smem;
     }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(F.grid);

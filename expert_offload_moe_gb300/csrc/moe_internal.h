@@ -115,7 +115,7 @@ struct DecodeParams {
 // Tensor-core decode path (moe_decode_tc.cu).
 constexpr int kTcAtomBytes = 512;   // block scales of a 128-row tile x 128-column k-step
 constexpr int kTcXRows = 16;        // rows of the x-term operand: 2 terms x 8 tokens
-constexpr int kTcHRows = 32;        // rows of the w*h-term operand: 4 terms x 8 tokens
+constexpr int kTcHRows = 64;        // rows of the w*h-term operand: 8 terms x 8 tokens
 
 // Weight scale atoms of one slot: gate [ntI][nks], up [ntI][nks], down [ntH][nksI], 512 bytes each.
 struct TcAtomLayout {
@@ -131,7 +131,7 @@ struct TcLaunch {
     const int32_t *counts, *act_slot, *act_off, *act_cnt, *hot_token;
     const float *hot_w;
     const uint8_t *xat;           // x-term atoms [nks][512]
-    uint8_t *hq, *hat;            // w*h terms [n_act_cap][32][Ipad], atoms [n_act_cap][nksI][512]
+    uint8_t *hq, *hat;            // w*h terms [n_act_cap][64][Ipad], atoms [n_act_cap][nksI][512]
     int Ipad;
     int *err;
     void *out;
@@ -194,5 +194,9 @@ void launch_map_update(int32_t *e2s, int n, const int32_t *experts, const int32_
 
 // Sets the thread-local message returned by moe_last_error().
 void set_last_error(const char *msg);
+
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the current device.  Function
+// attributes belong to a device's context, so the limit is tracked per (device, kernel); thread-safe.
+cudaError_t ensure_dyn_smem(const void *func, size_t bytes);
 
 }  // namespace moe

@@ -106,7 +106,10 @@ extern "C" int moe_route_noalloc(const void *x_dev, int32_t M, int32_t H, const 
     if (rc) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     unsigned char *base = static_cast<unsigned char *>(s.scratch);
-    // the arrival counter must start at zero
+    // The arrival counter must start at zero.  The route kernel's last block returns it to zero, so calls
+    // ordered on one stream would find it so; the memset is kept because calls that overlap on the GPU
+    // (documented as racing) can leave it elsewhere, and no later call would then ever find a last block.
+    // It costs the route launch its programmatic overlap with the kernel before it.
     cudaError_t e = cudaMemsetAsync(base, 0, sizeof(unsigned), st);
     if (e != cudaSuccess) return noalloc_fail(MOE_ECUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
 

@@ -387,12 +387,8 @@ cudaError_t launch_prefill(const PrefillLaunch &P, cudaStream_t s) {
     prefill_quant_kernel<<<(unsigned)((P.max_routes + 7) / 8), 256, 0, s>>>(P.x, geo.H, P.counts, P.hot_expert, P.hot_token,
                                                                       P.act_off, P.e2a, P.poff, P.XP, P.Hpad, P.XA,
                                                                       l.nks);
-    static bool cfg = false;
-    if (!cfg) {
-        cudaFuncSetAttribute(prefill_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        cudaFuncSetAttribute(prefill_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        cfg = true;
-    }
+    ensure_dyn_smem(reinterpret_cast<const void *>(prefill_gemm_kernel<1>), kSmemBytes);
+    ensure_dyn_smem(reinterpret_cast<const void *>(prefill_gemm_kernel<0>), kSmemBytes);
     GemmArgs g{};
     g.bank = P.bank;
     g.atoms = P.atoms;

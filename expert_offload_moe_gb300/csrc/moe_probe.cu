@@ -7,6 +7,9 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "moe.h"
 #include "moe_internal.h"
@@ -53,6 +56,26 @@ int probe_fail(int code, const char *fmt, ...) {
 }
 
 }  // namespace
+
+namespace moe {
+
+cudaError_t ensure_dyn_smem(const void *func, size_t bytes) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void *>, size_t> raised;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    size_t &have = raised[{dev, func}];
+    if (bytes > have) {
+        e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        if (e != cudaSuccess) return e;
+        have = bytes;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace moe
 
 extern "C" int moe_debug_stream_read(const void *src_dev, size_t bytes, void *sink_dev, int32_t nblocks,
                                      void *stream) {

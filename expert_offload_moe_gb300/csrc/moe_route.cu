@@ -1243,12 +1243,9 @@ cudaError_t launch_route(const RouteParams &p, cudaStream_t s, int num_sms) {
     const bool tiled = p.all_hot && p.M > kDecodeMaxTokens && p.b.blk_cnt && p.b.route_rank && p.WrT;
     if (p.pf_poff && !tiled) return cudaErrorNotSupported;  // only the tiled launch plans the prefill GEMMs
     if (tiled) {
-        static size_t smem_set = 0;  // the kernel's dynamic shared memory limit raised so far
-        if (smem > smem_set) {
-            cudaError_t e = cudaFuncSetAttribute(route_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)smem);
+        {
+            cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void *>(route_prefill_kernel), smem);
             if (e != cudaSuccess) return e;
-            smem_set = smem;
         }
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3((p.M + kPfRouteTok - 1) / kPfRouteTok);
@@ -1278,12 +1275,9 @@ cudaError_t launch_route(const RouteParams &p, cudaStream_t s, int num_sms) {
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = q.rowtask ? (size_t)p.M * p.H * 2 : 0;
-    static bool row_smem_set = false;  // static + dynamic shared memory of the row-task form passes 48 KB
-    if (q.rowtask && !row_smem_set) {
-        cudaError_t e = cudaFuncSetAttribute(route_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kRowTaskSmem);
+    if (q.rowtask) {  // static + dynamic shared memory of the row-task form passes 48 KB
+        cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void *>(route_kernel<true>), kRowTaskSmem);
         if (e != cudaSuccess) return e;
-        row_smem_set = true;
     }
     cfg.stream = s;
     cudaLaunchAttribute at[1];

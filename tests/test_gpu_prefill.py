@@ -13,27 +13,36 @@ import torch
 import oracle
 from expert_offload_moe_gb300 import stack, synth
 
-from parity import compare_routing, compare_values, near_tie_tokens, route_arrays
+from parity import (compare_routing, compare_values, near_tie_tokens, oracle_ffn_mxfp8_task, outlier_tokens,
+                    route_arrays, spawn_pool)
 
 pytestmark = pytest.mark.gpu
 
 
-def prefill_reference(li, x_bits, k, H, I, tokens):
-    """The oracle's prefill output for the listed tokens: fp32, experts summed in ascending order."""
+def prefill_reference(li, x_bits, k, H, I, tokens, pool=None):
+    """The oracle's prefill output for the listed tokens: fp32, experts summed in ascending order.  With a
+    process pool the expert FFNs run in its workers (same function, records regenerated from the seed)."""
     logits = oracle.router_logits(x_bits, li.Wr, li.bias)
     ids, w = oracle.topk_softmax(logits, k)
-    bank = li.bank.numpy()
+    order = [(t, j) for t in tokens for j in np.argsort(ids[t], kind="stable")]
+    if pool is None:
+        bank = li.bank.numpy()
+        ys = [oracle.expert_ffn_mxfp8(bank[ids[t][j]], H, I, x_bits[t]) for t, j in order]
+    else:
+        ys = pool.map(oracle_ffn_mxfp8_task, [(li.seed, li.layer, li.w.experts, H, I, int(ids[t][j]), x_bits[t])
+                                             for t, j in order])
     out = np.zeros((len(tokens), H), dtype=np.float32)
+    it = iter(zip(order, ys))
     for i, t in enumerate(tokens):
         acc = np.zeros(H, dtype=np.float32)
-        for j in np.argsort(ids[t], kind="stable"):
-            y = oracle.expert_ffn_mxfp8(bank[ids[t][j]], H, I, x_bits[t])
+        for _ in range(k):
+            (_, j), y = next(it)
             acc = (acc + np.float32(w[t][j]) * y).astype(np.float32)
         out[i] = acc
     return out, logits
 
 
-def run_prefill(li, x_bits, M, out_f32=True, max_tokens=None):
+def run_prefill(li, x_bits, M, out_f32=True, max_tokens=None, routes=False):
     w = li.w
     lay = li.make_layer(max_tokens=max_tokens or M, out_f32=out_f32)
     try:
@@ -42,14 +51,36 @@ def run_prefill(li, x_bits, M, out_f32=True, max_tokens=None):
         lay.stage_all()
         x = stack.bf16_tensor(x_bits)
         out = torch.empty((M, w.hidden), dtype=torch.float32 if out_f32 else torch.bfloat16, device="cuda")
-        lay.route(x, M)
+        res = lay.route(x, M)
         lay.forward_slots(x, out, M)
         torch.cuda.synchronize()
         lay.check_error()
         got = out.float().cpu().numpy()
+        g = route_arrays(res, w.experts, w.top_k) if routes else None
     finally:
         lay.close()
-    return got
+    return (got, g) if routes else got
+
+
+def tokens_covering_every_route_tile(g, tile=128):
+    """A set of tokens that has a route in every (expert, 128-route tile) of the grouped GEMMs: the hot
+    list is ordered by (expert, token) and each expert's routes are padded to whole tiles, so route r of
+    expert e's segment lies in tile r // 128.  Greedy: the first token of each tile not yet covered."""
+    covered, tokens = set(), []
+    tiles_of = {}
+    for e, off, cnt in zip(g["act_expert"], g["act_off"], g["act_cnt"]):
+        for r in range(cnt):
+            tiles_of.setdefault(int(g["hot_token"][off + r]), []).append((int(e), r // tile))
+    for e, off, cnt in zip(g["act_expert"], g["act_off"], g["act_cnt"]):
+        for r0 in range(0, cnt, tile):
+            if (int(e), r0 // tile) in covered:
+                continue
+            t = int(g["hot_token"][off + r0])
+            tokens.append(t)
+            covered.update(tiles_of[t])
+    n_tiles = sum((int(c) + tile - 1) // tile for c in g["act_cnt"])
+    assert len(covered) == n_tiles
+    return sorted(tokens), n_tiles
 
 
 def _tiny():
@@ -92,19 +123,37 @@ def test_prefill_tiny_bf16_out():
     compare_values(got, ref, False, exclude=np.where(near_tie_tokens(logits, w.top_k))[0])
 
 
-def test_prefill_gptoss_shape_sampled():
-    """The gpt-oss-20B-shaped prefill batch (2048 tokens, 32 experts, k = 4; ragged H = I = 2880), checked
-    on sampled tokens the oracle computes one by one."""
+def test_prefill_gptoss_shape_every_route_tile():
+    """The gpt-oss-20B-shaped prefill batch (2048 tokens, 32 experts, k = 4; ragged H = I = 2880) in the
+    launch configuration the benchmark times, checked on a set of tokens that has a route in every
+    (expert, 128-route tile) work item of the grouped GEMMs (plus the first and last token), every column,
+    the oracle computing each token's experts one by one."""
     w = synth.WORKLOADS["gptoss20b_prefill2048_s16_lfu_drift"]
     li = stack.LayerInputs(w, 0)
     M = w.prefill_tokens
     x_bits = synth.activations(0, 0, 0, M, w.hidden)
-    got = run_prefill(li, x_bits, M)
-    tokens = [0, 1, 777, 1500, M - 1]
-    ref, logits = prefill_reference(li, x_bits, w.top_k, w.hidden, w.inter, tokens)
+    got, g = run_prefill(li, x_bits, M, routes=True)
+    tokens, n_tiles = tokens_covering_every_route_tile(g)
+    assert n_tiles >= 64  # about 256 routes per expert: two or three tiles each
+    tokens = sorted(set(tokens) | {0, M - 1})
+    with spawn_pool() as pool:
+        ref, logits = prefill_reference(li, x_bits, w.top_k, w.hidden, w.inter, tokens, pool=pool)
     tie = near_tie_tokens(logits, w.top_k)
     keep = [i for i, t in enumerate(tokens) if not tie[t]]
     compare_values(got[tokens][keep], ref[keep], True)
+
+
+@pytest.mark.parametrize("out_f32", [True, False])
+def test_prefill_outlier_blocks(out_f32):
+    """Activations with outliers inside their 32-element blocks: MXFP8 keeps 3 mantissa bits relative to
+    each block's scale on both sides, and h spans a wide range within its blocks; every token and column."""
+    w = _tiny()
+    li = stack.LayerInputs(w, 0)
+    M = 60
+    x_bits = outlier_tokens(5, M, w.hidden)
+    got = run_prefill(li, x_bits, M, out_f32=out_f32)
+    ref, logits = prefill_reference(li, x_bits, w.top_k, w.hidden, w.inter, range(M))
+    compare_values(got, ref, out_f32, exclude=np.where(near_tie_tokens(logits, w.top_k))[0])
 
 
 def _route_case(w, M, seed_step, layer=0):

@@ -5,9 +5,10 @@ decode loop must not take cudaMalloc's implicit synchronisation, routes with
 moe_route_noalloc into buffers it owns; the call's only scratch is a built-in
 device array.  These tests call it through the C ABI and check, on two calls in
 a row (the array keeps the previous call's contents), that it returns what
-moe_route returns for the same inputs, and that sizes beyond the built-in
-array are refused with a clear error.  The file is named so that pytest
-collects it last.
+moe_route returns for the same inputs, that batches of more than 8 tokens
+(which no layer call routes with a partial map) give the oracle's routing and
+compaction bit for bit, and that sizes beyond the built-in array are refused
+with a clear error.  The file is named so that pytest collects it last.
 """
 import numpy as np
 import pytest
@@ -17,7 +18,7 @@ torch = pytest.importorskip("torch")
 from expert_offload_moe_gb300 import build as moe_build  # noqa: E402
 from expert_offload_moe_gb300 import moe, stack, synth  # noqa: E402
 
-from parity import W_ATOL, W_RTOL, route_arrays  # noqa: E402
+from parity import W_ATOL, W_RTOL, compare_routing, route_arrays  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -86,6 +87,50 @@ def test_noalloc_route_matches_moe_route_twice_in_a_row(name, placement):
         torch.cuda.synchronize()
         check_same(bufs, ref, E, k)
     lay.close()
+
+
+def read_buffers(bufs, k, E):
+    counts = bufs["counts"].cpu().numpy()
+    n_hot, n_cold, n_act, M = (int(c) for c in counts)
+    h = {name: t.cpu().numpy() for name, t in bufs.items()}
+    return {"counts": counts, "ids": h["topk_ids"][:M * k].reshape(M, k), "w": h["topk_w"][:M * k].reshape(M, k),
+            "hot_expert": h["hot_expert"][:n_hot], "hot_token": h["hot_token"][:n_hot], "hot_w": h["hot_w"][:n_hot],
+            "act_expert": h["act_expert"][:n_act], "act_slot": h["act_slot"][:n_act],
+            "act_off": h["act_off"][:n_act], "act_cnt": h["act_cnt"][:n_act],
+            "cold_token": h["cold_token"][:n_cold], "cold_expert": h["cold_expert"][:n_cold],
+            "cold_w": h["cold_w"][:n_cold], "hist": h["hist"]}
+
+
+@pytest.mark.parametrize("E,k,H,Ms,tau", [(16, 2, 256, (16, 600), 0.0), (512, 10, 2048, (16, 40), 0.25),
+                                          (64, 10, 256, (128, 9), 0.0)])
+def test_noalloc_route_batches_above_eight_tokens_match_the_oracle(E, k, H, Ms, tau):
+    """Batches of more than 8 tokens take the route kernel's general compaction (route lists kept in
+    global memory once M * k > 1024), which no layer call reaches with a partial map: top-k ids,
+    hot / active / cold lists and counts must equal the oracle's bit for bit (near-tie tokens aside),
+    with half the experts cold, on two calls in a row."""
+    import oracle
+
+    Wr_h = synth.router_weights(5, 1, E, H)
+    b_h = synth.router_bias(5, 1, E, tau)
+    e2s = np.full(E, -1, dtype=np.int32)
+    e2s[1::2] = np.random.default_rng(E).permutation(E // 2)  # odd experts in shuffled slots
+    Wr = torch.from_numpy(Wr_h).cuda()
+    bias = torch.from_numpy(b_h).cuda()
+    e2s_dev = torch.from_numpy(e2s).cuda()
+    for call, M in enumerate(Ms):
+        xb = synth.activations(5, 1, 300 + call, M, H)
+        bufs = new_buffers(M, k, E)
+        moe.route_noalloc(stack.bf16_tensor(xb), M, Wr, bias, E, k, e2s_dev, bufs)
+        torch.cuda.synchronize()
+        g = read_buffers(bufs, k, E)
+        logits = oracle.router_logits(xb, Wr_h, b_h)
+        ids, w = oracle.topk_softmax(logits, k)
+        o = oracle.compact(ids, w, e2s)
+        o.update(ids=ids, w=w)
+        assert int(g["counts"][3]) == M
+        excluded = compare_routing(g, o, logits, k, e2s)
+        assert len(excluded) <= max(1, M // 50)
+        assert g["counts"][0] > 0 and g["counts"][1] > 0  # both hot and cold routes were exercised
 
 
 def test_noalloc_route_refuses_sizes_beyond_its_scratch():
