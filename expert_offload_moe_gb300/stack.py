@@ -115,6 +115,49 @@ class DecodeStack:
         self.layers = []
 
 
+class EPShard:
+    """One rank's shard of an expert-parallel layer (xinfer docs "Options": each rank loads and offloads its own
+    expert shard; NCCL combines the rank-local MoE results).  The router is replicated; the layer holds only
+    the rank's contiguous range of experts (moe_ep_local_map), computes the routes to them and returns the
+    rest as its cold list; ``forward`` then sums the ranks' fp32 outputs with one all-reduce."""
+
+    def __init__(self, inputs: LayerInputs, world: int, rank: int, max_tokens: int = 8):
+        w = inputs.w
+        self.world, self.rank = world, rank
+        self.e2s, self.first, self.count = moe.ep_local_map(w.experts, world, rank)
+        self.layer = moe.Layer(w.hidden, w.inter, w.experts, w.top_k, self.count, max_tokens,
+                               torch.from_numpy(inputs.Wr).cuda(), torch.from_numpy(inputs.bias).cuda(), inputs.bank,
+                               self.e2s, out_f32=True, weight_format=w.weight_format)
+
+    def forward(self, x: torch.Tensor, M: int, out: torch.Tensor, group=None, stream=None, reduce: bool = True):
+        """Routes and computes this rank's routes into ``out`` (fp32 [M, H]), then (reduce, world > 1) all-reduces
+        it over the ranks.  Returns the route result (its cold list = the other ranks' routes)."""
+        res = self.layer.route(x, M, stream)
+        self.layer.forward_slots(x, out, M, stream)
+        if reduce and self.world > 1:
+            torch.distributed.all_reduce(out, group=group)
+        return res
+
+    def close(self):
+        self.layer.close()
+
+
+def ep_host_partial(bank: np.ndarray, e2s_local: np.ndarray, ids: np.ndarray, w: np.ndarray, x_bits: np.ndarray,
+                    H: int, I: int) -> np.ndarray:
+    """A rank's share of an expert-parallel layer on the host: for each token, the fp32 sum in ascending expert
+    order of w * FFN_e(x) over its routes to the experts this rank holds (e2s_local[e] >= 0), each FFN run by
+    the library's host expert FFN (the one its cold-route workers use).  [M, H] fp32."""
+    M, k = ids.shape
+    out = np.zeros((M, H), dtype=np.float32)
+    for t in range(M):
+        for j in np.argsort(ids[t], kind="stable"):
+            e = int(ids[t][j])
+            if e2s_local[e] >= 0:
+                y = moe.host_expert_ffn(bank[e], H, I, x_bits[t])
+                out[t] = (out[t] + np.float32(w[t][j]) * y).astype(np.float32)
+    return out
+
+
 class PrefillStack:
     """L layers of one workload with the whole expert bank staged on the device, and the M-token prefill
     step over it (route + forward of every layer on the tensor cores)."""

@@ -271,6 +271,26 @@ const char *moe_last_error(void);
  * between steps.  Errors: MOE_EINVAL, MOE_ECUDA. */
 int moe_layer_set_bias(moe_layer *layer, const float *bias_dev, void *stream);
 
+/* ------------------------------------------------ expert-parallel sharding */
+
+/* Expert parallelism over `world` ranks, one GPU each (xinfer docs "Options":
+ * each rank loads and offloads its own expert shard, and NCCL combines the
+ * rank-local MoE results).  The router is replicated on every rank; the E
+ * experts are split into `world` contiguous ranges, the first E % world
+ * ranks taking one more, and rank r owns [first, first + count).  Writes the
+ * rank's expert_to_slot[E]: its own experts in slots 0..count-1 in ascending
+ * id order, every other expert -1.  A layer created with this map (and
+ * num_slots >= count) routes every token like the whole layer, computes the
+ * routes to this rank's experts as its hot routes (moe_forward_slots) and
+ * returns the routes to the other ranks' experts as its cold list; one sum
+ * all-reduce of the ranks' fp32 outputs out[M, H] gives the whole layer (the
+ * experts' contributions summed within each rank in ascending order, then
+ * over the ranks in rank order).  first and count may be NULL.  Host only.
+ * Errors: MOE_EINVAL (E < 1, world < 1 or > E, rank outside [0, world),
+ * NULL map). */
+int moe_ep_local_map(int32_t E, int32_t world, int32_t rank, int32_t *expert_to_slot, int32_t *first,
+                     int32_t *count);
+
 /* ------------------------------------------------ routing without allocation */
 
 /* Caller-owned device buffers that receive a routing result; sizes as in
