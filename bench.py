@@ -370,7 +370,11 @@ def run_ours(args):
     pk, pk_src = peaks()
     hbm_peak = pk.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"])
     src = os.path.join(ROOT, "expert_offload_moe_gb300", "csrc", "moe_decode_tc.cu")
-    if w.weight_format != 0:  # NVFP4: CUDA-core decode kernels (the tensor-core path is MXFP4 only)
+    if w.weight_format != 0 and M == 1 and not args.two_launch:  # NVFP4 one-token FFN on the tensor cores
+        kernel, kbytes = "ffn_nv_kernel", mean_act * w.expert_bytes
+        kernel_us = {"route": route_us, "ffn": gateup_us, "combine": down_us}
+        traffic = None
+    elif w.weight_format != 0:  # NVFP4 batches: CUDA-core decode kernels
         kernel, kbytes = "gateup_kernel", gateup_bytes
         kernel_us = {"route": route_us, "gateup": gateup_us, "down": down_us}
         traffic = None

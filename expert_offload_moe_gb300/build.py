@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["moe_route.cu", "moe_decode.cu", "moe_decode_tc.cu", "moe_prefill_tc.cu", "moe_fill.cu", "moe_layer.cu",
+SOURCES = ["moe_route.cu", "moe_decode.cu", "moe_decode_tc.cu", "moe_decode_nv.cu", "moe_prefill_tc.cu", "moe_fill.cu", "moe_layer.cu",
            "moe_policy.cpp", "moe_cold.cpp", "moe_noalloc.cu", "moe_probe.cu", "moe_ep.cpp"]
 
 

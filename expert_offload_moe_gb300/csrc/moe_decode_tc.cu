@@ -336,6 +336,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int t = 0; t < kDecodeMaxTokens; ++t) {
                 if (t >= M) break;
+                if (!((routed >> t) & 1u)) {  // w h = 0 (warp-uniform): zero codes, the zero block's scale byte
+#pragma unroll
+                    for (int term = 0; term < T; ++term) {
+                        const int n = t * T + term;
+                        hq[(size_t)n * a.Ipad + row] = 0;
+                        if (lane == 0) hat[(size_t)(kblock / 4) * kAtom + (n & 31) * 16 + (n >> 5) * 4 + (kblock % 4)] = 0;
+                    }
+                    continue;
+                }
                 float res = vt[t];
 #pragma unroll
                 for (int term = 0; term < T; ++term) {

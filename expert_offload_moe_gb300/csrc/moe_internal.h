@@ -70,6 +70,11 @@ struct RouteParams {
     uint8_t *xq;         // tensor-core decode: x terms [16][Hpad] and their atoms, or nullptr
     uint8_t *xat;
     int Hpad;
+    // NVFP4 one-token decode on the tensor cores: x as kNvTerms E2M1 terms instead (xq [kNvTerms][Hpad4 / 2]
+    // packed, xat [nks4][4][512] UE4M3 scale atoms), the power-of-two factor of each term in xg [kNvTerms]
+    int xnv;
+    float *xg;
+    int Hpad4;
     // prefill tile plan (or nullptr): each active expert's routes padded to whole 128-row tiles
     int32_t *pf_poff, *pf_e2a, *pf_tile_aidx, *pf_tile_nrows, *pf_ntiles;  // [E], [E], [cap], [cap], [1]
     int pf_tiles_cap;
@@ -116,6 +121,33 @@ struct DecodeParams {
 constexpr int kTcAtomBytes = 512;   // block scales of a 128-row tile x 128-column k-step
 constexpr int kTcXRows = 16;        // rows of the x-term operand: 2 terms x 8 tokens
 constexpr int kTcHRows = 64;        // rows of the w*h-term operand: 8 terms x 8 tokens
+
+// NVFP4 decode on the tensor cores (moe_decode_nv.cu): packed E2M1 x packed E2M1 with UE4M3 scales per 16
+// elements; activations and h enter as kNvTerms E2M1 terms, one B column each, term j scaled by its own
+// power of two (applied when the accumulator column is read).
+constexpr int kNvTerms = 16;
+
+struct NvAtomLayout {       // UE4M3 scale atoms of one slot (512 bytes: one MMA of 64 K elements, 128 rows)
+    int ntI, ntH, nks4;     // 128-row tiles of I and H; 256-element k-steps of H
+    size_t off_g, off_u, off_d, slot_bytes;  // gate/up [ntI][nks4][4], down [ntH][ntI][2]
+};
+NvAtomLayout nv_atom_layout(int H, int I);
+
+struct NvLaunch {
+    const uint8_t *bank, *atoms;
+    ExpertGeometry geo;
+    int n_act_max, ks;
+    const int32_t *counts, *act_slot, *act_off, *act_cnt, *hot_token;
+    const float *hot_w;
+    const uint8_t *xat;
+    const float *xg;
+    float *part;
+    int *err;
+    const CUtensorMap *mapG, *mapU, *mapX, *mapD;
+};
+void launch_build_weight_atoms_nv(const uint8_t *expert, const ExpertGeometry &g, uint8_t *atoms, cudaStream_t s);
+cudaError_t launch_ffn_nv(const NvLaunch &L, cudaStream_t s);
+int nv_ffn_smem();
 
 // Weight scale atoms of one slot: gate [ntI][nks], up [ntI][nks], down [ntH][nksI], 512 bytes each.
 struct TcAtomLayout {

@@ -200,6 +200,13 @@ struct moe_layer {
     bool ffn1 = true;           // M = 1 takes the one-launch FFN (moe_debug_decode_fusion)
     void *tc_block = nullptr;
     CUtensorMap mapG{}, mapU{}, mapD{}, mapX{}, mapH{};
+    // NVFP4 one-token decode on the tensor cores (the buffers above are shared with it: xq, xat, atoms, err,
+    // part, tc_block): x terms as packed E2M1, their per-term powers of two, UE4M3 scale atoms, packed maps
+    bool tcnv = false;
+    moe::NvAtomLayout nvl{};
+    float *nv_xg = nullptr;
+    int Hpad4 = 0;
+    CUtensorMap mapGn{}, mapUn{}, mapDn{}, mapXn{};
 
     // tensor-core prefill over the staged bank: scratch allocated when staging is attached
     bool pf = false;
@@ -357,6 +364,12 @@ int tc_splits_down(const moe_layer *L, int M) {
 
 // Weight scale atoms of one slot, rebuilt whenever an expert lands in it (stream-ordered after the copy).
 int build_slot_atoms(moe_layer *L, int slot, cudaStream_t st) {
+    if (L->tcnv) {
+        moe::launch_build_weight_atoms_nv(L->slots + (size_t)slot * L->geo.expert_bytes, L->geo,
+                                          L->atoms + (size_t)slot * L->nvl.slot_bytes, st);
+        CUDA_TRY(cudaGetLastError());
+        return MOE_OK;
+    }
     if (!L->tc) return MOE_OK;
     moe::launch_build_weight_atoms(L->slots + (size_t)slot * L->geo.expert_bytes, L->geo,
                                    L->atoms + (size_t)slot * L->atl.slot_bytes, st);
@@ -419,6 +432,56 @@ int tc_setup(moe_layer *L, cudaStream_t st) {
                          L->Ipad, (uint64_t)moe::kTcHRows * L->Ipad, 128, moe::kTcHRows, "h terms")))
         return rc;
     L->tc = true;
+    return MOE_OK;
+}
+
+// Buffers and tensor maps of the NVFP4 one-token decode on the tensor cores (packed E2M1 operands).
+int nv_setup(moe_layer *L, cudaStream_t st) {
+    const int H = L->d.hidden, I = L->d.inter;
+    L->Hpad4 = (H + 255) / 256 * 256;
+    L->nvl = moe::nv_atom_layout(H, I);
+    const size_t ucap1 = (size_t)act_cap(L, 1) * L->nvl.ntI;
+    const size_t xrow = (size_t)L->Hpad4 / 2;
+    const size_t sz[] = {(size_t)moe::kNvTerms * xrow, (size_t)L->nvl.nks4 * 4 * moe::kTcAtomBytes,
+                         (size_t)moe::kNvTerms * sizeof(float), sizeof(int),
+                         (size_t)L->nvl.ntH * ucap1 * 128 * sizeof(float)};
+    size_t total = 0;
+    for (size_t s : sz) total += align_up(s, 256);
+    cudaError_t e = cudaMalloc(&L->tc_block, total);
+    if (e == cudaSuccess) e = cudaMalloc(&L->atoms, (size_t)L->d.num_slots * L->nvl.slot_bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(e == cudaErrorMemoryAllocation ? MOE_ENOMEM : MOE_ECUDA, "NVFP4 tensor-core buffers: %s",
+                    cudaGetErrorString(e));
+    }
+    char *p = static_cast<char *>(L->tc_block);
+    void **dst[] = {(void **)&L->xq, (void **)&L->xat, (void **)&L->nv_xg, (void **)&L->err, (void **)&L->part};
+    for (size_t i = 0; i < sizeof(sz) / sizeof(sz[0]); ++i) {
+        *dst[i] = p;
+        p += align_up(sz[i], 256);
+    }
+    // x codes past H stay zero; scale bytes never written (blocks past H, columns past the terms) stay 1.0
+    CUDA_TRY(cudaMemsetAsync(L->tc_block, 0, total, st));
+    CUDA_TRY(cudaMemsetAsync(L->xat, 0x38, sz[1], st));
+    CUDA_TRY(cudaMemsetAsync(L->atoms, 0x38, (size_t)L->d.num_slots * L->nvl.slot_bytes, st));
+    const moe::ExpertGeometry &g = L->geo;
+    const int S = L->d.num_slots;
+    int rc;
+    // codes as bytes: 128 rows x 128 bytes (256 codes) per gate/up box, 128 rows x 64 bytes per down box; the
+    // boxes at the ragged ends of H and I are zero-filled past the matrix
+    if ((rc = encode_map(&L->mapGn, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->slots + g.off_wg_codes, H / 2, I, S, H / 2,
+                         g.expert_bytes, 128, 128, "gate codes (NVFP4)")))
+        return rc;
+    if ((rc = encode_map(&L->mapUn, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->slots + g.off_wu_codes, H / 2, I, S, H / 2,
+                         g.expert_bytes, 128, 128, "up codes (NVFP4)")))
+        return rc;
+    if ((rc = encode_map(&L->mapDn, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->slots + g.off_wd_codes, I / 2, H, S, I / 2,
+                         g.expert_bytes, 64, 128, "down codes (NVFP4)")))
+        return rc;
+    if ((rc = encode_map(&L->mapXn, CU_TENSOR_MAP_DATA_TYPE_UINT8, L->xq, xrow, moe::kNvTerms, 1, xrow,
+                         (uint64_t)moe::kNvTerms * xrow, 128, moe::kNvTerms, "x terms (NVFP4)")))
+        return rc;
+    L->tcnv = true;
     return MOE_OK;
 }
 
@@ -653,6 +716,13 @@ int moe_layer_create(const moe_layer_desc *desc, const float *router_w_dev, cons
             release(L);
             return rc;
         }
+    } else if (d.hidden >= 256 && d.inter >= 128 && d.hidden % 64 == 0 && d.inter % 64 == 0 &&
+               d.weight_format == MOE_FMT_NVFP4) {  // NVFP4: one-token decode on the tensor cores
+        const int rc = nv_setup(L, st);
+        if (rc) {
+            release(L);
+            return rc;
+        }
     }
 
     // page-locked mirror: the device mirror block's layout, then the cold sums of the decode tokens
@@ -741,6 +811,14 @@ int moe_route(moe_layer *L, const void *x_dev, int32_t M, void *stream, moe_rout
         p.xat = L->xat;
         p.Hpad = L->Hpad;
         p.xmir = reinterpret_cast<uint16_t *>(static_cast<char *>(L->mir_block) + L->mir_off_x);  // and copies x
+    }
+    if (L->tcnv && M == 1 && L->ffn1) {  // NVFP4: x as E2M1 terms for the one-token tensor-core FFN
+        p.xq = L->xq;
+        p.xat = L->xat;
+        p.xnv = 1;
+        p.xg = L->nv_xg;
+        p.Hpad4 = L->Hpad4;
+        p.xmir = reinterpret_cast<uint16_t *>(static_cast<char *>(L->mir_block) + L->mir_off_x);
     }
     if (M > moe::kDecodeMaxTokens && L->pf) {  // the route launch also plans the prefill GEMM tiles
         p.pf_poff = L->pf_poff;
@@ -851,7 +929,41 @@ int moe_forward_slots(moe_layer *L, const void *x_dev, void *out_dev, int32_t M,
     p.h = L->h;
     p.out = out_dev;
     p.out_f32 = L->d.out_dtype == MOE_OUT_F32;
-    if (M <= moe::kDecodeMaxTokens && L->tc) {
+    if (M == 1 && L->tcnv && L->ffn1) {  // NVFP4: gate/up, SiLU and down in one launch, then the combine
+        moe::NvLaunch n{};
+        n.bank = L->slots;
+        n.atoms = L->atoms;
+        n.geo = L->geo;
+        n.n_act_max = act_cap(L, 1);
+        n.ks = choose_splits(n.n_act_max * L->nvl.ntI, L->nvl.nks4, L->num_sms);
+        n.counts = L->rb.counts;
+        n.act_slot = L->rb.act_slot;
+        n.act_off = L->rb.act_off;
+        n.act_cnt = L->rb.act_cnt;
+        n.hot_token = L->rb.hot_token;
+        n.hot_w = L->rb.hot_w;
+        n.xat = L->xat;
+        n.xg = L->nv_xg;
+        n.part = L->part;
+        n.err = L->err;
+        n.mapG = &L->mapGn;
+        n.mapU = &L->mapUn;
+        n.mapX = &L->mapXn;
+        n.mapD = &L->mapDn;
+        moe::TcLaunch t{};  // the combine's arguments
+        t.geo = L->geo;
+        t.n_act_max = n.n_act_max;
+        t.counts = L->rb.counts;
+        t.part = L->part;
+        t.out = out_dev;
+        t.out_f32 = p.out_f32;
+        CUDA_TRY(prof_mark(L, 1, st));
+        CUDA_TRY(moe::launch_ffn_nv(n, st));
+        CUDA_TRY(prof_mark(L, 1, st));
+        CUDA_TRY(prof_mark(L, 2, st));
+        CUDA_TRY(moe::launch_ffn_combine(t, st));
+        CUDA_TRY(prof_mark(L, 2, st));
+    } else if (M <= moe::kDecodeMaxTokens && L->tc) {
         moe::TcLaunch t{};
         t.bank = L->slots;
         t.geo = L->geo;

@@ -241,6 +241,36 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
 
     // ---------------- phase 1: partial logits; x terms -----------------------
     for (bool first = true; task < ntask + nq; task += gridDim.x * kWarps, first = false) {
+        if (task >= ntask && p.xnv) {
+            // NVFP4 one-token decode: x as kNvTerms E2M1 terms, UE4M3 scale per 16 values, term j scaled by
+            // G_j = 2^(E0 - 2 j) with 2^E0 <= max|x| / 128 (every block's scale stays below 448 and each term
+            // shrinks the residual at least 5-fold, so G never outruns it)
+            const int q = task - ntask, b = q;  // M == 1: token 0, 32-value block b
+            const uint16_t xb = p.x[b * 32 + lane];
+            if (p.xmir) p.xmir[b * 32 + lane] = xb;
+            float am = 0.f;
+            for (int i = lane; i < H / 8; i += 32) {
+                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.x) + i);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    am = fmaxf(am, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xffff0000u))));
+            }
+            am = tc::warp_max(am);
+            const int e0 = am > 0.f ? tc::floor_log2(am) - 7 : 0;
+            float res = __uint_as_float((uint32_t)xb << 16);
+            const int e = b * 32 + lane, ks = e / 256, kk = (e % 256) / 64, b16 = (e % 64) / 16;
+            const size_t row_bytes = (size_t)p.Hpad4 / 2;
+            for (int j = 0; j < kNvTerms; ++j) {
+                const float G = am > 0.f ? tc::pow2f(e0 - 2 * j) : 0.f;
+                uint32_t sb;
+                const uint32_t byte = tc::split_term_e2m1(res, G, sb);
+                if (!(lane & 1)) p.xq[(size_t)j * row_bytes + e / 2] = (uint8_t)byte;
+                if ((lane & 15) == 0) p.xat[(size_t)(ks * 4 + kk) * kTcAtomBytes + j * 16 + b16] = (uint8_t)sb;
+                if (b == 0 && lane == 0) p.xg[j] = G;
+            }
+            continue;
+        }
         if (task >= ntask) {
             const int q = task - ntask, nb = H / 32, t = q / nb, b = q - t * nb;
             const uint16_t xb = p.x[(size_t)t * H + b * 32 + lane];

@@ -350,6 +350,68 @@ __device__ __forceinline__ uint8_t split_term(float &res, uint32_t &scale_byte) 
     return code;
 }
 
+// ------------------------------------------------ E2M1 terms with UE4M3 scales per 16 values (NVFP4 path)
+
+// Two fp32 values to one byte of E2M1 codes (round to nearest even, saturating at +-6): hi in the high nibble.
+__device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float lo, float hi) {
+    uint16_t r;
+    asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u16.u8 %0, t; }" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// The two E2M1 codes of a byte back to fp32 (exact): low nibble -> lo, high nibble -> hi.
+__device__ __forceinline__ void e2m1x2_to_f32x2(uint32_t byte, float &lo, float &hi) {
+    asm("{\n\t.reg .b32 t;\n\t.reg .b16 a, b, c;\n\t.reg .b8 q;\n\t"
+        "cvt.u16.u32 c, %2;\n\t"
+        "cvt.u8.u16 q, c;\n\t"
+        "cvt.rn.f16x2.e2m1x2 t, q;\n\t"
+        "mov.b32 {a, b}, t;\n\t"
+        "cvt.f32.f16 %0, a;\n\t"
+        "cvt.f32.f16 %1, b;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(byte));
+}
+
+// The smallest UE4M3 value >= s (s > 0, s <= 448) as its byte, and that value.
+__device__ __forceinline__ uint32_t ue4m3_ceil(float s, float &v) {
+    const uint16_t pk = f32x2_to_e4m3x2(s, s);
+    uint32_t c = pk & 0xff;
+    float lo, hi;
+    e4m3x2_to_f32x2((uint16_t)(c | (c << 8)), lo, hi);
+    if (lo < s && c < 0x7e) {
+        ++c;
+        e4m3x2_to_f32x2((uint16_t)(c | (c << 8)), lo, hi);
+    }
+    v = lo;
+    return c;
+}
+
+// 2^e as fp32 for e in [-126, 127], 0 below.
+__device__ __forceinline__ float pow2f(int e) { return e < -126 ? 0.f : __uint_as_float((uint32_t)(e + 127) << 23); }
+
+// One E2M1 term of 16-value blocks held one value per lane (a half-warp per block): the block's scale
+// s = the smallest UE4M3 >= max|res| / (6 G), codes RNE(res / (s G)); res loses the term exactly.  Returns the
+// byte holding this lane's code with its pair lane's (even lane low nibble), and the block's scale byte
+// (0 for an all-zero block or G == 0: codes 0).
+__device__ __forceinline__ uint32_t split_term_e2m1(float &res, float G, uint32_t &scale_byte) {
+    float bmax = fabsf(res);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, o));
+    const int lane = threadIdx.x & 31;
+    float f = 0.f, sv = 0.f;
+    scale_byte = 0;
+    if (bmax > 0.f && G > 0.f) {
+        scale_byte = ue4m3_ceil(bmax / (6.f * G), sv);
+        f = res / (sv * G);
+    }
+    const float other = __shfl_xor_sync(0xffffffffu, f, 1);
+    const uint32_t byte = (lane & 1) ? f32x2_to_e2m1x2(other, f) : f32x2_to_e2m1x2(f, other);
+    float lo, hi;
+    e2m1x2_to_f32x2(byte, lo, hi);
+    if (sv > 0.f) res = res - ((lane & 1) ? hi : lo) * sv * G;
+    return byte;
+}
+
 // ------------------------------------------------ operand tiles shared by the decode and prefill kernels
 
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {

@@ -10,7 +10,8 @@ import oracle  # noqa: E402
 from expert_offload_moe_gb300 import build as moe_build  # noqa: E402
 from expert_offload_moe_gb300 import moe, stack, synth  # noqa: E402
 
-from parity import compare_routing, compare_values, dev_bytes, route_arrays  # noqa: E402
+from parity import (combine_with_weights, compare_routing, compare_values, dev_bytes, outlier_tokens,  # noqa: E402
+                    route_arrays, route_weight_rtol)
 
 pytestmark = pytest.mark.gpu
 
@@ -58,6 +59,49 @@ def test_gptoss_shape_nvfp4(M):
     li = stack.LayerInputs(GPTOSS_NV, 3)
     g, _ = run_and_compare(li, synth.activations(0, 3, 210 + M, M, GPTOSS_NV.hidden), M == 8)
     assert g["counts"][2] > 0
+
+
+@pytest.mark.parametrize("shape", [TINY_NV, GPTOSS_NV])
+@pytest.mark.parametrize("fusion", [True, False])
+def test_one_token_tensor_core_and_cuda_core_paths(shape, fusion):
+    """M = 1 runs the one-launch tensor-core FFN (packed E2M1 x E2M1, UE4M3 scales per 16, x and h as 16 E2M1
+    terms each); with decode fusion off the CUDA-core kernels.  Both against the oracle, both output types."""
+    li = stack.LayerInputs(shape, 1)
+    for out_f32 in (False, True):
+        lay = li.make_layer(max_tokens=8, out_f32=out_f32)
+        lay.decode_fusion(fusion)
+        try:
+            run_and_compare(li, synth.activations(0, 1, 240 + out_f32, 1, shape.hidden), out_f32, layer=lay)
+        finally:
+            lay.close()
+
+
+@pytest.mark.parametrize("shape", [TINY_NV, GPTOSS_NV])
+def test_one_token_outlier_activations(shape):
+    """Outliers inside the 16-element blocks of x (and so a wide range within h's blocks) on the tensor-core
+    path: routing weights within each token's own summation bound, outputs against the oracle's expert
+    outputs combined with the GPU's weights, at the same 2e-3 metric."""
+    li = stack.LayerInputs(shape, 2)
+    w = li.w
+    for seed in (3, 4, 5):
+        x = outlier_tokens(seed, 3, w.hidden)[seed % 3:seed % 3 + 1]
+        lay = li.make_layer(max_tokens=8, out_f32=True)
+        try:
+            xt = stack.bf16_tensor(x)
+            out = torch.empty((1, w.hidden), dtype=torch.float32, device="cuda")
+            res = lay.route(xt, 1)
+            lay.forward_slots(xt, out, 1)
+            torch.cuda.synchronize()
+            lay.check_error()
+            g = route_arrays(res, w.experts, w.top_k)
+        finally:
+            lay.close()
+        o = oracle.moe_layer(x, li.Wr, li.bias, li.bank.numpy(), li.e2s, w.top_k, w.hidden, w.inter, fmt="nvfp4")
+        excl = compare_routing(g, o, o["logits"], w.top_k, li.e2s, w_rtol=route_weight_rtol(x, li.Wr, li.bias))
+        bank = li.bank.numpy()
+        ys = np.stack([np.stack([oracle.expert_ffn(bank[e], w.hidden, w.inter, x[0], fmt="nvfp4")
+                                 for e in g["ids"][0]])])
+        compare_values(out.cpu().numpy(), combine_with_weights(g["ids"], g["w"], ys), True, exclude=excl)
 
 
 def test_nvfp4_partial_map_cache_refills():
