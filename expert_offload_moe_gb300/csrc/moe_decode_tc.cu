@@ -605,6 +605,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 constexpr int kFfnThreads = 192;  // warps 0-3: epilogue (TMEM lane quadrant = warp); warp 4: copies; warp 5: MMAs
 constexpr int kFfnNB = 16;        // B columns of the down MMA: 8 w*h terms of the one token, 8 zero columns
+constexpr int kFfnDownAcc = 8;    // down accumulators (16 columns each) in a ring: a tile's MMAs rarely wait for a drain
+constexpr uint32_t kFfnTmem = 256;  // gate/up accumulators and scales in columns 0..127, the down ring in 128..255
 constexpr int kErrHReady = 4, kErrAccFull = 5, kErrAccEmpty = 6;
 
 struct FfnArgs {
@@ -639,7 +641,7 @@ __global__ void __launch_bounds__(kFfnThreads, 2)
     constexpr int kAtomSlot = 2 * kTileA + kB;  // first atom slot of a stage
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
-    __shared__ __align__(8) uint64_t full[S], empty[S], done, hready, acc_full[2], acc_empty[2];
+    __shared__ __align__(8) uint64_t full[S], empty[S], done, hready, acc_full[kFfnDownAcc], acc_empty[kFfnDownAcc];
     __shared__ uint32_t tslot;
     __shared__ float s_w;
     __shared__ int s_routed;
@@ -660,7 +662,7 @@ __global__ void __launch_bounds__(kFfnThreads, 2)
     uint8_t *hB = smem + kGateStage + kTileA * 2;   // stage 1 x-term slot: h terms, 16 rows x 128 bytes
     uint8_t *hAt = smem + 2 * kGateStage + kTileA * 2;  // stage 2 x-term slot: h atom
 
-    if (warp == 5) tmem_alloc(&tslot, kGateTmem);
+    if (warp == 5) tmem_alloc(&tslot, kFfnTmem);
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
@@ -668,7 +670,7 @@ __global__ void __launch_bounds__(kFfnThreads, 2)
         }
         mbar_init(&done, 1);
         mbar_init(&hready, 128);
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kFfnDownAcc; ++b) {
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], 128);
         }
@@ -687,7 +689,7 @@ __global__ void __launch_bounds__(kFfnThreads, 2)
     const int n_act = a.counts[2];
     if (aidx >= n_act) {  // the whole cluster (one unit) leaves together
         __syncthreads();
-        if (warp == 5) tmem_dealloc(tbase, kGateTmem);
+        if (warp == 5) tmem_dealloc(tbase, kFfnTmem);
         return;
     }
     const int slot = a.act_slot[aidx];
@@ -695,9 +697,9 @@ __global__ void __launch_bounds__(kFfnThreads, 2)
     const uint8_t *slot_atoms = a.atoms + (size_t)slot * a.atom_slot_bytes;
     const uint8_t *gat = slot_atoms + a.atom_off_g + (size_t)jt * nks * kAtom;
     const uint8_t *uat = slot_atoms + a.atom_off_u + (size_t)jt * nks * kAtom;
-    // columns: gate accumulator [16], up accumulator [16] (both reused as the two down accumulators once
-    // drained), 12 scale columns per stage, then the h atom
-    const uint32_t tDg = tbase, tDu = tbase + NBX, tSF = tbase + 2 * NBX, tHat = tSF + 12 * S;
+    // columns: gate accumulator [16], up accumulator [16], 12 scale columns per stage, the h atom; the ring of
+    // down accumulators from column 128
+    const uint32_t tDg = tbase, tDu = tbase + NBX, tSF = tbase + 2 * NBX, tHat = tSF + 12 * S, tDown = tbase + 128;
 
     if (warp == 4) {
         // ---------------- copies ----------------
@@ -810,8 +812,9 @@ __global__ void __launch_bounds__(kFfnThreads, 2)
                 const int d0 = 2 * ds, nt = nd - d0 < 2 ? nd - d0 : 2;
                 if (tailI) fence_proxy_async();  // the tail tiles came by cp.async
                 for (int q = 0; q < nt && ok; ++q) {
-                    const int ti = d0 + q, buf = ti & 1;
-                    if (ti >= 2) ok = mbar_wait(&acc_empty[buf], ((ti >> 1) - 1) & 1, a.err, kErrAccEmpty);
+                    const int ti = d0 + q, buf = ti % kFfnDownAcc;
+                    if (ti >= kFfnDownAcc)
+                        ok = mbar_wait(&acc_empty[buf], ((ti / kFfnDownAcc) - 1) & 1, a.err, kErrAccEmpty);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t sfa = tSF + 12 * st + 4 * q;
@@ -819,7 +822,7 @@ __global__ void __launch_bounds__(kFfnThreads, 2)
                     const uint32_t aA = smem_u32(sA + q * kTileA);
                     const int nk = tailI ? 2 : 4;
                     for (int kk = 0; kk < nk; ++kk)
-                        mma_mx(tbase + NBX * buf, sw128_desc(aA + kk * 32), sw128_desc(aH + kk * 32), idesc, kk, sfa,
+                        mma_mx(tDown + NBX * buf, sw128_desc(aA + kk * 32), sw128_desc(aH + kk * 32), idesc, kk, sfa,
                                tHat, kk > 0 ? 1u : 0u);
                     mma_commit(&acc_full[buf]);
                 }
@@ -903,13 +906,13 @@ __global__ void __launch_bounds__(kFfnThreads, 2)
         // down partials of this CTA's H tiles
         float *part = a.part + (size_t)unit * 128;
         for (int ti = 0; ti < nd; ++ti) {
-            const int buf = ti & 1, hr = ks + KS * ti;
-            got = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (ti >> 1) & 1, a.err, kErrAccFull));
+            const int buf = ti % kFfnDownAcc, hr = ks + KS * ti;
+            got = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (ti / kFfnDownAcc) & 1, a.err, kErrAccFull));
             tc_fence_after();
             float v = 0.f;
             if (got) {
                 uint32_t rr[8];
-                tmem_ld8_sync(tbase + NBX * buf + lane_off, rr);
+                tmem_ld8_sync(tDown + NBX * buf + lane_off, rr);
 #pragma unroll
                 for (int term = 0; term < T; ++term) v += __uint_as_float(rr[term]);
             }
@@ -922,7 +925,7 @@ __global__ void __launch_bounds__(kFfnThreads, 2)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) tmem_dealloc(tbase, kGateTmem);
+    if (warp == 5) tmem_dealloc(tbase, kFfnTmem);
 }
 
 constexpr int kCombineRows = 32;  // output rows per combine CTA; its 4 warps take a quarter of the units each

@@ -199,7 +199,7 @@ __device__ __forceinline__ void load_router_row(const RouteParams &p, int task, 
 }
 
 template <bool kRow>
-__global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
+__global__ void __launch_bounds__(kThreads, kRow ? 1 : 4) route_kernel(RouteParams p) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int H = p.H, E = p.E, M = p.M, k = p.k;
     __shared__ int s_e2s[kMaxExperts];
@@ -514,141 +514,227 @@ __global__ void __launch_bounds__(kThreads) route_kernel(RouteParams p) {
         }
         __syncthreads();
     } else if (rows_by_block) {
-        for (int q = threadIdx.x; q < M * E; q += kThreads) {
-            const int t = q / E, e = q - t * E;
-            float pv[kMaxChunks];
+        // two (token, expert) pairs per thread and iteration, the loads of both issued before either sum
+        for (int q0 = threadIdx.x; q0 < M * E; q0 += 2 * kThreads) {
+            float pv[2][kMaxChunks];
 #pragma unroll
-            for (int c = 0; c < kMaxChunks; ++c)
-                pv[c] = c < p.nchunk ? __ldcg(p.b.logit_part + ((size_t)c * M + t) * E + e) : 0.f;
-            float v = 0.f;
+            for (int u = 0; u < 2; ++u) {
+                const int q = q0 + u * kThreads, t = q / E, e = q - t * E;
 #pragma unroll
-            for (int c = 0; c < kMaxChunks; ++c)
-                if (c < p.nchunk) v += pv[c];
-            v += s_bias[e];
-            s_l[t][e] = (v != v) ? -INFINITY : v;  // NaN marks a taken expert below
+                for (int c = 0; c < kMaxChunks; ++c)
+                    pv[u][c] = (q < M * E && c < p.nchunk) ? __ldcg(p.b.logit_part + ((size_t)c * M + t) * E + e) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int q = q0 + u * kThreads, t = q / E, e = q - t * E;
+                if (q >= M * E) continue;
+                float v = 0.f;
+#pragma unroll
+                for (int c = 0; c < kMaxChunks; ++c)
+                    if (c < p.nchunk) v += pv[u][c];
+                v += s_bias[e];
+                s_l[t][e] = (v != v) ? -INFINITY : v;  // NaN marks a taken expert below
+            }
         }
         __syncthreads();
     }
 
     if (rows_by_block && E > 32) {
-        // Decode with more than 32 experts.  Top-k: warp t holds its token's logits in registers (expert
-        // lane + 32 i in v[i]) and takes k arg-max rounds over them -- the same rounds, order and ties as
-        // below, without going back to shared memory.
+        // Decode with more than 32 experts.  Top-k of token t by warp t: the k-th largest of the 32 lane maxima
+        // bounds the k-th largest logit from below, so the k winners are among the logits at or above it (a
+        // few more than k, as a rule); those candidates are ranked in one pass of shuffles -- larger first,
+        // equal ones by lower id, the order and ties of k arg-max rounds.  With more than 32 candidates (wide
+        // ties) the warp takes the k arg-max rounds over its row instead.
         constexpr int kPer = kMaxExperts / 32;
+        __shared__ float s_cv[kWarps][32];
+        __shared__ int s_ce[kWarps][32];
+        __shared__ unsigned s_mask[kMaxExperts];  // bit t: token t routed to the expert
+        __shared__ int s_tok_cold[kDecodeMaxTokens];
+        for (int e = threadIdx.x; e < E; e += kThreads) s_mask[e] = 0u;
+        if (threadIdx.x < kDecodeMaxTokens) s_tok_cold[threadIdx.x] = 0;
+        __syncthreads();
         for (int t = warp; t < M; t += kWarps) {
             float v[kPer];
+            float lm = -INFINITY;
 #pragma unroll
             for (int i = 0; i < kPer; ++i) {
                 const int e = lane + 32 * i;
-                v[i] = e < E ? s_l[t][e] : __int_as_float(0x7fc00000);  // NaN: never a candidate
+                v[i] = e < E ? s_l[t][e] : -INFINITY;
+                lm = fmaxf(lm, v[i]);
             }
-            for (int j = 0; j < k; ++j) {
-                // this lane's best by a 4-level tree (larger value, equal values to the lower id; NaN never
-                // wins), instead of one dependent chain over the kPer values
-                float tv[kPer];
-                int te[kPer];
+            int r = 0;  // rank of this lane's maximum among the 32 (larger first, ties by lane)
 #pragma unroll
-                for (int i = 0; i < kPer; ++i) {
-                    tv[i] = v[i] == v[i] ? v[i] : -INFINITY;
-                    te[i] = v[i] == v[i] ? lane + 32 * i : 0x7fffffff;
-                }
+            for (int j = 0; j < 32; ++j) {
+                const float o = __shfl_sync(0xffffffffu, lm, j);
+                r += (o > lm) || (o == lm && j < lane);
+            }
+            const float tau = __shfl_sync(0xffffffffu, lm, __ffs(__ballot_sync(0xffffffffu, r == k - 1)) - 1);
+            int c = 0;
 #pragma unroll
-                for (int w = kPer / 2; w > 0; w >>= 1)
+            for (int i = 0; i < kPer; ++i) c += (v[i] >= tau) && (lane + 32 * i < E);
+            int x = c;
 #pragma unroll
-                    for (int i = 0; i < w; ++i)
-                        if (tv[i + w] > tv[i] || (tv[i + w] == tv[i] && te[i + w] < te[i])) {
-                            tv[i] = tv[i + w];
-                            te[i] = te[i + w];
-                        }
-                float bv = tv[0];
-                int be = te[0];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                    const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                    if (ov > bv || (ov == bv && oe < be)) {
-                        bv = ov;
-                        be = oe;
-                    }
-                }
-                if (lane == 0) {
-                    s_sel_id[warp][j] = be;
-                    s_sel_l[warp][j] = bv;
-                }
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            const int C = __shfl_sync(0xffffffffu, x, 31);
+            if (C <= 32 && tau > -INFINITY) {
+                int pos = x - c;
 #pragma unroll
                 for (int i = 0; i < kPer; ++i)
-                    if (lane + 32 * i == be) v[i] = __int_as_float(0x7fc00000);
+                    if (v[i] >= tau && lane + 32 * i < E) {
+                        s_cv[warp][pos] = v[i];
+                        s_ce[warp][pos] = lane + 32 * i;
+                        ++pos;
+                    }
+                __syncwarp();
+                const float cv = lane < C ? s_cv[warp][lane] : -INFINITY;
+                const int ce = lane < C ? s_ce[warp][lane] : 0x7fffffff;
+                int rk = 0;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float ov = __shfl_sync(0xffffffffu, cv, j);
+                    const int oe = __shfl_sync(0xffffffffu, ce, j);
+                    rk += (ov > cv) || (ov == cv && oe < ce);
+                }
+                if (lane < C && rk < k) {
+                    s_sel_id[warp][rk] = ce;
+                    s_sel_l[warp][rk] = cv;
+                }
+            } else {
+                // k arg-max rounds over the row (larger value, equal values to the lower id); NaN marks taken
+#pragma unroll
+                for (int i = 0; i < kPer; ++i)
+                    if (lane + 32 * i >= E) v[i] = __int_as_float(0x7fc00000);
+                for (int j = 0; j < k; ++j) {
+                    float bv = -INFINITY;
+                    int be = 0x7fffffff;
+#pragma unroll
+                    for (int i = 0; i < kPer; ++i)
+                        if (v[i] == v[i] && (v[i] > bv || (v[i] == bv && lane + 32 * i < be))) {
+                            bv = v[i];
+                            be = lane + 32 * i;
+                        }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                        if (ov > bv || (ov == bv && oe < be)) {
+                            bv = ov;
+                            be = oe;
+                        }
+                    }
+                    if (lane == 0) {
+                        s_sel_id[warp][j] = be;
+                        s_sel_l[warp][j] = bv;
+                    }
+#pragma unroll
+                    for (int i = 0; i < kPer; ++i)
+                        if (lane + 32 * i == be) v[i] = __int_as_float(0x7fc00000);
+                }
             }
             __syncwarp();
-            if (lane < k) {
+            {
+                // softmax over the k selected logits: one exp per lane, the denominator summed in selection order
                 const float lmax = s_sel_l[warp][0];
+                const float ej = lane < k ? expf(s_sel_l[warp][lane] - lmax) : 0.f;
                 float den = 0.f;
-                for (int j = 0; j < k; ++j) den += expf(s_sel_l[warp][j] - lmax);
-                const int id = s_sel_id[warp][lane];
-                const float wj = expf(s_sel_l[warp][lane] - lmax) / den;
-                p.b.topk_ids[(size_t)t * k + lane] = id;
-                p.b.topk_w[(size_t)t * k + lane] = wj;
-                s_ids[t * k + lane] = id;
-                s_w[t * k + lane] = wj;
-                atomicAdd(&s_hist[id], 1);
+                for (int j = 0; j < k; ++j) den += __shfl_sync(0xffffffffu, ej, j);
+                if (lane < k) {
+                    const int id = s_sel_id[warp][lane];
+                    const float wj = ej / den;
+                    p.b.topk_ids[(size_t)t * k + lane] = id;
+                    p.b.topk_w[(size_t)t * k + lane] = wj;
+                    s_ids[t * k + lane] = id;
+                    s_w[t * k + lane] = wj;
+                    atomicAdd(&s_hist[id], 1);
+                    atomicOr(&s_mask[id], 1u << t);
+                }
             }
             __syncwarp();
         }
         __syncthreads();
         if (p.lru.S) lru_table_step(p, s_e2s, s_hist, reinterpret_cast<int *>(s_union));
-        // Lists, one thread per route (at most 8 x 16): each counts the routes that come before it --
-        // hot routes by (expert, token), cold routes by (token, expert) -- and the active experts below
-        // its own; the first route of an expert (lowest token) writes the active entry.
-        __shared__ unsigned char s_first[kDecodeMaxTokens * kMaxTopK];
-        __shared__ unsigned char s_hotr[kDecodeMaxTokens * kMaxTopK];  // route q is hot
+        // Lists: hot routes by (expert, token) at the expert's offset (a block scan of the hot counts) plus the
+        // number of earlier tokens in its token mask; active experts at their index (a scan of the active
+        // flags); cold routes by (token, expert) at the cold routes of earlier tokens plus the token's cold
+        // routes to lower ids.
+        __shared__ int s_wsum[kWarps][2];
+        const int e0 = 2 * threadIdx.x;  // E <= 2 kThreads
+        int hc[2], ac[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int e = e0 + u;
+            hc[u] = (e < E && s_e2s[e] >= 0) ? s_hist[e] : 0;
+            ac[u] = hc[u] > 0;
+            if (e < E) p.b.hist[e] = s_hist[e];
+        }
+        int xh = hc[0] + hc[1], xa = ac[0] + ac[1];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int yh = __shfl_up_sync(0xffffffffu, xh, o), ya = __shfl_up_sync(0xffffffffu, xa, o);
+            if (lane >= o) {
+                xh += yh;
+                xa += ya;
+            }
+        }
+        if (lane == 31) {
+            s_wsum[warp][0] = xh;
+            s_wsum[warp][1] = xa;
+        }
         const int nr = M * k, r = threadIdx.x;
         const bool mine = r < nr;
         const int e = mine ? s_ids[r] : 0, t = mine ? r / k : 0;
         const bool hot = mine && s_e2s[e] >= 0;
-        if (mine) {
-            bool first = true;  // no earlier token routes to e (tokens before t; a token picks e once)
-            for (int t2 = 0; t2 < t; ++t2)
-                for (int j = 0; j < k; ++j) first &= s_ids[t2 * k + j] != e;
-            s_first[r] = hot && first;
-            s_hotr[r] = hot;
+        if (mine && !hot) atomicAdd(&s_tok_cold[t], 1);
+        __syncthreads();
+        int oh = 0, oa = 0, n_hot = 0, n_act = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            oh += w < warp ? s_wsum[w][0] : 0;
+            oa += w < warp ? s_wsum[w][1] : 0;
+            n_hot += s_wsum[w][0];
+            n_act += s_wsum[w][1];
+        }
+        if (e0 < E) {
+            s_hot_off[e0] = oh + xh - hc[0] - hc[1];
+            s_act_pos[e0] = oa + xa - ac[0] - ac[1];
+        }
+        if (e0 + 1 < E) {
+            s_hot_off[e0 + 1] = oh + xh - hc[1];
+            s_act_pos[e0 + 1] = oa + xa - ac[1];
         }
         __syncthreads();
         if (mine) {
-            int pos = 0, aidx = 0;
-            for (int t2 = 0, q = 0; t2 < M; ++t2)
-                for (int j = 0; j < k; ++j, ++q) {
-                    const int e2 = s_ids[q];
-                    const bool hot2 = s_hotr[q];
-                    if (hot) {
-                        pos += hot2 && (e2 < e || (e2 == e && t2 < t));
-                        aidx += s_first[q] && e2 < e;
-                    } else {
-                        pos += !hot2 && (t2 < t || (t2 == t && e2 < e));
-                    }
-                }
+            const unsigned below = s_mask[e] & ((1u << t) - 1u);
             if (hot) {
+                const int pos = s_hot_off[e] + __popc(below);
                 p.b.hot_expert[pos] = e;
                 p.b.hot_token[pos] = t;
                 p.b.hot_w[pos] = s_w[r];
-                if (s_first[r]) {
-                    p.b.act_expert[aidx] = e;
-                    p.b.act_slot[aidx] = s_e2s[e];
-                    p.b.act_off[aidx] = pos;
-                    p.b.act_cnt[aidx] = s_hist[e];
+                if (below == 0u) {  // the expert's first token writes its active entry
+                    const int ai = s_act_pos[e];
+                    p.b.act_expert[ai] = e;
+                    p.b.act_slot[ai] = s_e2s[e];
+                    p.b.act_off[ai] = s_hot_off[e];
+                    p.b.act_cnt[ai] = s_hist[e];
                 }
             } else {
+                int pos = 0;
+                for (int t2 = 0; t2 < t; ++t2) pos += s_tok_cold[t2];
+                for (int j = 0; j < k; ++j) {
+                    const int e2 = s_ids[t * k + j];
+                    pos += s_e2s[e2] < 0 && e2 < e;
+                }
                 p.b.cold_token[pos] = t;
                 p.b.cold_expert[pos] = e;
                 p.b.cold_w[pos] = s_w[r];
             }
         }
-        for (int x = threadIdx.x; x < E; x += kThreads) p.b.hist[x] = s_hist[x];
-        const int n_hot = __syncthreads_count(hot);
-        const int n_cold = __syncthreads_count(mine && !hot);
-        const int n_act = __syncthreads_count(mine && s_first[r]);
         if (threadIdx.x == 0) {
             p.b.counts[0] = n_hot;
-            p.b.counts[1] = n_cold;
+            p.b.counts[1] = nr - n_hot;
             p.b.counts[2] = n_act;
             p.b.counts[3] = M;
         }
