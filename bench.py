@@ -552,9 +552,12 @@ def run_prefill(args):
     gateup_flop = 2.0 * routes * 2 * w.inter * w.hidden
     down_flop = 2.0 * routes * w.hidden * w.inter
     pk, pk_src = peaks()
-    bf16 = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops", PEAKS_FALLBACK["bf16_tflops"]))
+    # the GEMMs are event-timed inside a step of a few ms: the burst figure is the denominator
+    bf16 = pk.get("bf16_tflops", PEAKS_FALLBACK["bf16_tflops"])
+    bf16_sus = pk.get("bf16_tflops_sustained", bf16)
     peak = bf16 * FP8_OVER_BF16
     achieved = gateup_flop / (gateup_us * 1e-6) / 1e12
+    mma_probe = mma_probe_tflops(moe, torch)
 
     # e2e: the step's activations copied in from pinned host memory and the outputs read back, every step
     x_host = torch.empty(st.x_all.shape[1:], dtype=torch.bfloat16, pin_memory=True)
@@ -590,8 +593,15 @@ def run_prefill(args):
         "roofline": {"bound": "tensor", "kernel": "prefill_gemm_kernel<1> (gate/up)", "achieved": achieved,
                      "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
                      "flop_per_launch": gateup_flop, "avg_launch_us": gateup_us,
-                     "peak_source": ("measured bf16_tflops_sustained (MEASURED_PEAKS.json)" if pk_src == "measured"
-                                     else "fallback 1.9 PFLOP/s bf16") + " x 2 (nominal 8-bit / bf16 ratio)"},
+                     "peak_source": ("measured bf16_tflops burst (MEASURED_PEAKS.json)" if pk_src == "measured"
+                                     else "fallback 1.9 PFLOP/s bf16") + " x 2 (nominal 8-bit / bf16 ratio)",
+                     "frac_of_sustained_x2": achieved / (bf16_sus * FP8_OVER_BF16),
+                     "mma_probe_tflops": mma_probe, "frac_of_mma_probe": achieved / mma_probe,
+                     "mma_probe": "moe_debug_mma_peak: one CTA per SM issuing the GEMM's M=128 N=256 K=32 "
+                                  "block-scaled MMAs from operands resident in shared memory, event-timed",
+                     "down": {"flop_per_launch": down_flop, "avg_launch_us": down_us,
+                              "achieved": down_flop / (down_us * 1e-6) / 1e12,
+                              "frac": down_flop / (down_us * 1e-6) / 1e12 / peak}},
         "clocks": clocks,
         "gpu_launches": int(args.steps * L * 6),
         "e2e": e2e,
@@ -601,6 +611,25 @@ def run_prefill(args):
     st.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def mma_probe_tflops(moe, torch, iters=4096, reps=5):
+    """Median rate of the block-scaled MMA probe over `reps` event-timed launches (after one warm-up)."""
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    moe.mma_peak(iters, err.data_ptr(), stream)
+    times = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        moe.mma_peak(iters, err.data_ptr(), stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    if int(err.item()) != 0:
+        raise RuntimeError("the MMA probe's completion wait ran out")
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return moe.mma_peak_flops(iters, sms) / (sorted(times)[reps // 2] * 1e-3) / 1e12
 
 
 def oracle_prefill_seconds(w, n_tokens, seed=0):

@@ -168,13 +168,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t tbase = tslot;
     pdl_wait();  // routing and x terms are complete
     pdl_trigger();
-    const int n_act = a.counts[2];
-    if (aidx >= n_act) {  // the whole cluster (one unit) leaves together
+    const int slot = a.act_slot[aidx];  // -1 past the active experts
+    if (slot < 0) {  // the whole cluster (one unit) leaves together
         __syncthreads();
         if (warp == 5) tmem_dealloc(tbase, kTmemCols);
         return;
     }
-    const int slot = a.act_slot[aidx];
     const uint8_t *slot_atoms = a.atoms + (size_t)slot * a.atom_slot_bytes;
     const uint8_t *gat = slot_atoms + a.atom_off_g + (size_t)jt * nks * 4 * kAtom;
     const uint8_t *uat = slot_atoms + a.atom_off_u + (size_t)jt * nks * 4 * kAtom;

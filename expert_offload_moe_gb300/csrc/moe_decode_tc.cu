@@ -156,12 +156,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tbase = tslot;
     pdl_wait();  // routing and x terms are complete
     pdl_trigger();
-    const int n_act = a.counts[2];
-    if (aidx >= n_act) {  // the whole cluster (one tile) leaves together
+    const int slot = a.act_slot[aidx];  // -1 past the active experts
+    if (slot < 0) {  // the whole cluster (one tile) leaves together
         if (warp == 1) tmem_dealloc(tbase, kGateTmem);
         return;
     }
-    const int slot = a.act_slot[aidx];
     const uint8_t *expert = a.bank + (size_t)slot * a.expert_bytes;
     const uint8_t *gat = a.atoms + (size_t)slot * a.atom_slot_bytes + a.atom_off_g + (size_t)tile * nks * kAtom;
     const uint8_t *uat = a.atoms + (size_t)slot * a.atom_slot_bytes + a.atom_off_u + (size_t)tile * nks * kAtom;
@@ -686,13 +685,12 @@ __global__ void __launch_bounds__(kFfnThreads, 2)
     const uint32_t tbase = tslot;
     pdl_wait();  // routing and x terms are complete
     pdl_trigger();
-    const int n_act = a.counts[2];
-    if (aidx >= n_act) {  // the whole cluster (one unit) leaves together
+    const int slot = a.act_slot[aidx];  // -1 past the active experts
+    if (slot < 0) {  // the whole cluster (one unit) leaves together
         __syncthreads();
         if (warp == 5) tmem_dealloc(tbase, kFfnTmem);
         return;
     }
-    const int slot = a.act_slot[aidx];
     const uint8_t *expert = a.bank + (size_t)slot * a.expert_bytes;
     const uint8_t *slot_atoms = a.atoms + (size_t)slot * a.atom_slot_bytes;
     const uint8_t *gat = slot_atoms + a.atom_off_g + (size_t)jt * nks * kAtom;

@@ -63,6 +63,7 @@ struct RouteParams {
     const float *bias;   // [E] or nullptr
     const int32_t *e2s;  // [E]; ignored when all_hot
     int M, H, E, k, nchunk;
+    int act_pad;         // decode: act_slot[n_active .. act_pad) are set to -1 (the expert kernels read one word)
     int all_hot;         // prefill: every expert is hot, slot = expert id
     int rowtask;         // set by launch_route: one warp per whole router row (decode, E > 32), logits final
     RouteBuffers b;

@@ -805,6 +805,7 @@ int moe_route(moe_layer *L, const void *x_dev, int32_t M, void *stream, moe_rout
     p.k = k;
     p.nchunk = L->nchunk;
     p.all_hot = M > moe::kDecodeMaxTokens;
+    p.act_pad = M <= moe::kDecodeMaxTokens ? act_cap(L, M) : 0;
     p.b = L->rb;
     if (L->tc && M <= moe::kDecodeMaxTokens) {  // the route launch also writes the gate/up B operand
         p.xq = L->xq;

@@ -453,6 +453,7 @@ __global__ void __launch_bounds__(kThreads, kRow ? 1 : 4) route_kernel(RoutePara
                 p.b.counts[2] = xa;
                 p.b.counts[3] = M;
             }
+            for (int i = __shfl_sync(0xffffffffu, xa, 31) + lane; i < p.act_pad; i += 32) p.b.act_slot[i] = -1;
         } else if (warp == 1) {
             // cold routes of token `lane`, ascending expert id
             int ce[kMaxTopK];
@@ -732,6 +733,7 @@ __global__ void __launch_bounds__(kThreads, kRow ? 1 : 4) route_kernel(RoutePara
                 p.b.cold_w[pos] = s_w[r];
             }
         }
+        for (int i = n_act + threadIdx.x; i < p.act_pad; i += kThreads) p.b.act_slot[i] = -1;
         if (threadIdx.x == 0) {
             p.b.counts[0] = n_hot;
             p.b.counts[1] = nr - n_hot;
@@ -838,6 +840,7 @@ __global__ void __launch_bounds__(kThreads, kRow ? 1 : 4) route_kernel(RoutePara
                 s_n[0] = xh;
                 s_n[1] = xa;
             }
+            for (int i = __shfl_sync(0xffffffffu, xa, 31) + lane; i < p.act_pad; i += 32) p.b.act_slot[i] = -1;
         } else if (warp == 1) {
             // cold routes of token `lane`, ascending expert id
             int ce[kMaxTopK];

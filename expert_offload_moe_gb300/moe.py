@@ -26,7 +26,7 @@ EXPORTED = [
     "moe_debug_profile_read", "moe_debug_check_error", "moe_policy_step", "moe_route_noalloc", "moe_forward_cold",
     "moe_forward_cold_gpu", "moe_host_expert_ffn", "moe_policy_step_recency", "moe_layer_set_policy",
     "moe_layer_set_device_cache", "moe_debug_device_cache", "moe_debug_decode_fusion", "moe_prefetch_step",
-    "moe_prefetch", "moe_debug_stream_read", "moe_policy_step_slru", "moe_ep_local_map",
+    "moe_prefetch", "moe_debug_stream_read", "moe_debug_mma_peak", "moe_policy_step_slru", "moe_ep_local_map",
 ]
 
 
@@ -102,6 +102,7 @@ def lib():
         L.moe_debug_profile_read.argtypes = [p, p]
         L.moe_debug_check_error.argtypes = [p, ctypes.POINTER(i32)]
         L.moe_debug_stream_read.argtypes = [p, ctypes.c_size_t, p, i32, p]
+        L.moe_debug_mma_peak.argtypes = [i32, i32, p, p]
         L.moe_ep_local_map.argtypes = [i32, i32, i32, p, ctypes.POINTER(i32), ctypes.POINTER(i32)]
         L.moe_route_noalloc.argtypes = [p, i32, i32, p, p, i32, i32, p, ctypes.POINTER(RouteBuffers), p]
         L.moe_policy_step.argtypes = [p, p, p, p, i32, i32, p, ctypes.c_int64, ctypes.c_double, i32, p, p, p, p]
@@ -352,6 +353,15 @@ def host_expert_ffn(record, H, I, x_bits):
 def stream_read(src, nbytes, sink, stream=None, nblocks=0):
     """One launch of the library's streaming-read probe over ``nbytes`` bytes at device pointer ``src``."""
     check(lib().moe_debug_stream_read(_P(int(src)), nbytes, _P(int(sink)), nblocks, stream_ptr(stream)))
+
+
+def mma_peak(iters, err, stream=None, nblocks=0):
+    """One launch of the library's block-scaled MMA probe (nblocks x iters x 4 MMAs of 128 x 256 x 32)."""
+    check(lib().moe_debug_mma_peak(iters, nblocks, _P(int(err)), stream_ptr(stream)))
+
+
+def mma_peak_flops(iters, nblocks):
+    return float(nblocks) * iters * 4 * 2 * 128 * 256 * 32
 
 
 def ep_local_map(E, world, rank):

@@ -140,7 +140,7 @@ typedef struct {
     const int32_t *hot_token;
     const float *hot_w;
     const int32_t *act_expert; /* [<= min(S, M*k)] experts with hot routes, ascending */
-    const int32_t *act_slot;   /* their slots */
+    const int32_t *act_slot;   /* their slots; after a decode call (M <= 8) entries n_active..min(S, M*k)-1 are -1 */
     const int32_t *act_off;    /* first index of each in the hot arrays */
     const int32_t *act_cnt;    /* number of hot routes of each */
     const int32_t *cold_token; /* [<= M*k] cold routes ordered by (token, expert) */
@@ -389,11 +389,11 @@ int moe_debug_profile(moe_layer *layer, int32_t enable);
  * dequantise-and-multiply, gate / up / down) as ONE kernel launch, followed
  * by a small launch that adds the weighted per-expert results in a fixed
  * order (on by default); enable == 0 makes moe_forward_slots use the
- * separate gate/up and down launches instead (for comparison).  Both give
- * results within the same tolerance of the oracle; they sum the experts'
- * contributions in different orders, so they are not bit-identical to each
- * other.  Takes effect at the next moe_forward_slots; no device work.
- * Errors: MOE_EINVAL (NULL layer). */
+ * separate gate/up and down launches instead (for comparison; with NVFP4
+ * layers, the CUDA-core kernels).  Both give results within the same
+ * tolerance of the oracle; they sum the experts' contributions in different
+ * orders, so they are not bit-identical to each other.  Takes effect at the
+ * next moe_forward_slots; no device work.  Errors: MOE_EINVAL (NULL layer). */
 int moe_debug_decode_fusion(moe_layer *layer, int32_t enable);
 
 /* Streaming-read probe for benchmarks (no counterpart on the pages; it does
@@ -406,6 +406,20 @@ int moe_debug_decode_fusion(moe_layer *layer, int32_t enable);
  * Asynchronous; nothing is allocated.  Errors: MOE_EINVAL (NULL or unaligned
  * pointers, bytes not a multiple of 16, nblocks < 0), MOE_ECUDA. */
 int moe_debug_stream_read(const void *src_dev, size_t bytes, void *sink_dev, int32_t nblocks, void *stream);
+
+/* Block-scaled tensor-core probe for benchmarks (no counterpart on the
+ * pages; none of the layer's data): one launch on `stream`, one CTA per SM
+ * (nblocks = 0: the device's SM count), each issuing `iters` steps of four
+ * tcgen05.mma kind::mxf8f6f4 block_scale MMAs of M = 128, N = 256, K = 32
+ * (E4M3 A x E2M1 B, UE8M0 scales, fp32 accumulator in tensor memory) on
+ * operand tiles held in shared memory, the shape the prefill GEMMs issue per
+ * 128-column step.  The launch does nblocks * iters * 4 * 2 * 128 * 256 * 32
+ * flops; its event-timed duration gives the ceiling of that MMA stream with
+ * no operand traffic.  err_dev (4 bytes, device, caller-owned, set to 0 by
+ * the caller) receives a nonzero code if the final completion wait ran out.
+ * Asynchronous; nothing is allocated.  Errors: MOE_EINVAL (NULL or unaligned
+ * err_dev, iters outside 1..65536, nblocks < 0), MOE_ECUDA. */
+int moe_debug_mma_peak(int32_t iters, int32_t nblocks, void *err_dev, void *stream);
 
 /* Sums of the timed kernels since moe_debug_profile: out[0] route ms,
  * out[1] gate/up ms (the one-launch FFN when M = 1 takes it), out[2] down

@@ -47,6 +47,7 @@ def test_null_arguments_are_rejected_without_a_gpu(lib):
     assert lib.moe_prefetch(None, None, 1, None, None) == moe.MOE_EINVAL
     assert lib.moe_debug_decode_fusion(None, 1) == moe.MOE_EINVAL
     assert lib.moe_debug_stream_read(None, 16, None, 0, None) == moe.MOE_EINVAL
+    assert lib.moe_debug_mma_peak(8, 0, None, None) == moe.MOE_EINVAL
     assert lib.moe_destroy(None) == moe.MOE_OK
 
 

@@ -132,3 +132,29 @@ def test_one_launch_placement_gives_bit_identical_output():
         outs.append(forward(lay, x, True)[1])
         lay.close()
     assert np.array_equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_decode_route_pads_the_active_slots_with_minus_one(M):
+    """A decode route writes act_slot[n_active .. min(S, M k)) = -1 (the expert kernels launched for up to
+    min(S, M k) experts take an entry of -1 as 'no expert here'), on every call: a call with more active
+    experts followed by one with fewer leaves no stale slot behind."""
+    from parity import dev_i32
+
+    w = synth.WORKLOADS["e512k10_h2048_i512_s256_m1"]
+    li = stack.LayerInputs(w, 1)
+    lay = li.make_layer(max_tokens=8)
+    try:
+        cap = min(w.slots, M * w.top_k)
+        n_seen = set()
+        for c in range(6):
+            res = lay.route(stack.bf16_tensor(synth.activations(0, 1, 400 + c, M, w.hidden)), M)
+            g = route_arrays(res, w.experts, w.top_k)
+            n_act = int(g["counts"][2])
+            n_seen.add(n_act)
+            slots = dev_i32(res.act_slot, cap)
+            assert np.array_equal(slots[:n_act], g["act_slot"])
+            assert (slots[:n_act] >= 0).all() and (slots[n_act:] == -1).all()
+        assert len(n_seen) > 1  # the calls had different numbers of active experts
+    finally:
+        lay.close()
