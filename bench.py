@@ -219,8 +219,20 @@ def run_reference(args, prefill=False):
     print(json.dumps(line), flush=True)
 
 
-def traffic_for(kernel_src, summary):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel source."""
+# committed ncu traffic summaries: (kernel, workload, tokens per step) -> file under profiles/
+TRAFFIC_SUMMARIES = {
+    ("ffn_tc_kernel", "gptoss20b_h2880_e32k4_resident_m1", 1): "ffn_tc_gptoss20b_traffic.txt",
+    ("ffn_tc_kernel", "e512k10_h2048_i512_s256_m1", 1): "ffn_tc_e512k10_s256_traffic.txt",
+    ("gateup_tc_kernel", "e512k10_h2048_i512_s384_m4m8", 8): "gateup_tc_e512k10_s384_m8_traffic.txt",
+}
+
+
+def traffic_for(kernel_src, kernel, workload, M):
+    """DRAM bytes per launch from the committed ncu summary of this kernel on this workload, if it was taken
+    on this kernel source."""
+    summary = TRAFFIC_SUMMARIES.get((kernel, workload, M))
+    if summary is None:
+        return None
     summ = os.path.join(ROOT, "profiles", summary)
     if not os.path.exists(summ):
         return None
@@ -381,11 +393,11 @@ def run_ours(args):
     elif M == 1 and not args.two_launch:  # gate/up, SiLU and down in one launch (every expert byte), then combine
         kernel, kbytes = "ffn_tc_kernel", mean_act * w.expert_bytes
         kernel_us = {"route": route_us, "ffn": gateup_us, "combine": down_us}
-        traffic = traffic_for(src, "ffn_tc_gptoss20b_traffic.txt")
+        traffic = traffic_for(src, kernel, w.name, M)
     else:
         kernel, kbytes = "gateup_tc_kernel", gateup_bytes
         kernel_us = {"route": route_us, "gateup": gateup_us, "down": down_us}
-        traffic = traffic_for(src, "gateup_tc_gptoss20b_traffic.txt")
+        traffic = traffic_for(src, kernel, w.name, M)
     achieved = kbytes / (gateup_us * 1e-6) / 1e9
 
     # ---------------- floor: a plain read of the same bytes, timed the same way -----

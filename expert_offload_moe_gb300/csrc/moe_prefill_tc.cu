@@ -25,7 +25,9 @@ namespace {
 using namespace tc;
 
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + 32 * kEpiWarps;  // warp 0: copies; warp 1 lane 0: MMAs; warps 2..9: epilogue
+// warp 0: copies; warp 1 lane 0: MMAs; warps 2..9: epilogue; warp 10 lane 0: the proxy fence of each stage
+constexpr int kThreads = 96 + 32 * kEpiWarps;
+constexpr int kProxyWarp = 2 + kEpiWarps;
 constexpr int kTileA = 128 * 128;         // one 128 x 128 operand tile in smem (one byte per element)
 constexpr int kTileActTx = 128 * 128;     // TMA bytes of an E4M3 activation tile
 constexpr int kTileWTx = 128 * 128 / 2;   // TMA bytes of an E2M1 weight tile (packed codes)
@@ -132,6 +134,73 @@ struct GemmArgs {
     int *err;
 };
 
+// Before a copy warp leaves: the copies of its last stages (issued, perhaps never consumed when a wait ran
+// out) have landed, so nothing is written into the CTA's shared memory after it exits.  Lane 0 waits on the
+// last min(it, S) stage barriers (bounded); a stage whose copies were consumed completed long ago.
+__device__ __forceinline__ void drain_copies(uint64_t *full, int S, uint32_t it, int *err) {
+    if ((threadIdx.x & 31) == 0)
+        for (uint32_t j = it > (uint32_t)S ? it - S : 0u; j < it; ++j)
+            if (!mbar_wait(&full[j % S], (j / S) & 1, err, kErrFull)) break;
+    __syncwarp();
+}
+
+// The epilogue of one work item for accumulator row r (route row pr of the tile, valid if a real route)
+// and this warp's half of the 256 columns, v = those columns as fp32 bits:
+//   gate/up: h = SiLU(g) u for 64 of the item's 128 columns of I, stored as MXFP8 with its scale atom;
+//   down: w y for 128 of the item's 256 columns of H.
+template <int kGateUp>
+__device__ __forceinline__ void epilogue_item(const GemmArgs &g, const uint32_t (&v)[128], int tile, int jn, int r,
+                                              int half, int aidx, bool valid, int pr) {
+    constexpr int kRowsN = kGateUp ? 128 : 256;
+    if (kGateUp) {
+        // h = SiLU(g) u for 64 of the item's 128 columns of I, one 32-column MXFP8 block at a time
+#pragma unroll
+        for (int cb = 0; cb < 2; ++cb) {
+            float h[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                h[j] = valid ? silu_fast(__uint_as_float(v[32 * cb + j])) * __uint_as_float(v[64 + 32 * cb + j])
+                             : 0.f;
+            float amax = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(h[j]));
+            const int X = mxfp8_exponent(amax);
+            const float inv = e8m0_value(e8m0_byte(-X));
+            uint32_t q[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t lo = f32x2_to_e4m3x2(h[4 * j] * inv, h[4 * j + 1] * inv);
+                const uint32_t hi = f32x2_to_e4m3x2(h[4 * j + 2] * inv, h[4 * j + 3] * inv);
+                q[j] = lo | (hi << 16);
+            }
+            const int c = 2 * half + cb;  // 32-column block of the item
+            uint4 *dst = reinterpret_cast<uint4 *>(g.HP + (size_t)pr * g.Ipad + jn * 128 + 32 * c);
+            dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+            dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+            g.HA[((size_t)tile * g.nksI + jn) * kAtom + atom_byte(r, c)] = (uint8_t)(X + 127);
+        }
+    } else {
+        // y * w for 128 of the item's 256 columns of H (rows past the tile's routes are not stored)
+        const int wrow0 = jn * kRowsN;
+        const float wt = valid ? g.hot_w[g.act_off[aidx] + (pr - g.poff[aidx])] : 0.f;
+        if (valid) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int col = wrow0 + half * 128 + 32 * c;
+                if (col < g.H) {  // H % 32 == 0
+                    float4 *dst = reinterpret_cast<float4 *>(g.YP + (size_t)pr * g.H + col);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        dst[j] = make_float4(wt * __uint_as_float(v[32 * c + 4 * j]),
+                                             wt * __uint_as_float(v[32 * c + 4 * j + 1]),
+                                             wt * __uint_as_float(v[32 * c + 4 * j + 2]),
+                                             wt * __uint_as_float(v[32 * c + 4 * j + 3]));
+                }
+            }
+        }
+    }
+}
+
 template <int kGateUp>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB0,
@@ -141,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kRowsN = kGateUp ? 128 : 256;  // weight rows per work item
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
-    __shared__ __align__(8) uint64_t full[S], empty[S], acc_full, acc_empty;
+    __shared__ __align__(8) uint64_t full[S], ready[S], empty[S], acc_full, acc_empty, drain;
     __shared__ uint32_t tslot;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -154,10 +223,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1 + 32);  // the copy thread's expect_tx + the 32 lanes' atom copies
+            mbar_init(&ready[s], 1);      // the proxy warp, after its fence
             mbar_init(&empty[s], 1);
         }
         mbar_init(&acc_full, 1);
         mbar_init(&acc_empty, kEpiWarps);
+        mbar_init(&drain, 1);
         fence_barrier_init();
         tma_prefetch_desc(&mapA);
         tma_prefetch_desc(&mapB0);
@@ -211,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
             }
         }
+        drain_copies(full, S, it, g.err);
     } else if (warp == 1) {
         // ---------------- MMAs: one thread; the accumulator is reused once the epilogue has drained it ----
         if (lane == 0) {
@@ -228,10 +300,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool b1 = kGateUp || jn * kRowsN + 128 < g.Nrows;  // the second weight half exists
                 for (int i = 0; i < nks; ++i, ++it) {
                     const int st = it % S;
-                    ok = mbar_wait(&full[st], (it / S) & 1, g.err, kErrFull);
+                    ok = mbar_wait(&ready[st], (it / S) & 1, g.err, kErrFull);
                     if (!ok) break;
                     tc_fence_after();
-                    fence_proxy_async();  // the atoms came through the generic proxy (cp.async)
                     uint8_t *sS = smem + st * kStage;
                     const uint32_t sfa = tbase + kColSF + 12 * st, sfb0 = sfa + 4, sfb1 = sfa + 8;
                     atom_to_tmem(sfa, sS + kOffAtA);
@@ -249,6 +320,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (ok) mma_commit(&acc_full);
             }
+            // every MMA issued has finished before the CTA can leave, also when a wait ran out
+            mma_commit(&drain);
+            mbar_wait(&drain, 0, g.err, kErrDone);
+        }
+        __syncwarp();
+    } else if (warp == kProxyWarp) {
+        // ---------------- proxy fence: the atoms (and ragged tail tiles) of each stage came through the
+        // generic proxy; this warp waits for the stage, fences, and hands it to the MMA thread, which then
+        // issues no fence of its own ----------------
+        if (lane == 0) {
+            bool ok = true;
+            uint32_t it = 0;
+            for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x)
+                for (int i = 0; i < nks; ++i, ++it) {
+                    const int st = it % S;
+                    ok = mbar_wait(&full[st], (it / S) & 1, g.err, kErrFull);
+                    if (!ok) break;
+                    fence_proxy_async();
+                    mbar_arrive(&ready[st]);
+                }
         }
         __syncwarp();
     } else {
@@ -280,53 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty);
-            if (kGateUp) {
-                // h = SiLU(g) u for 64 of the item's 128 columns of I, one 32-column MXFP8 block at a time
-#pragma unroll
-                for (int cb = 0; cb < 2; ++cb) {
-                    float h[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        h[j] = valid ? silu_fast(__uint_as_float(v[32 * cb + j])) * __uint_as_float(v[64 + 32 * cb + j])
-                                     : 0.f;
-                    float amax = 0.f;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(h[j]));
-                    const int X = mxfp8_exponent(amax);
-                    const float inv = e8m0_value(e8m0_byte(-X));
-                    uint32_t q[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint32_t lo = f32x2_to_e4m3x2(h[4 * j] * inv, h[4 * j + 1] * inv);
-                        const uint32_t hi = f32x2_to_e4m3x2(h[4 * j + 2] * inv, h[4 * j + 3] * inv);
-                        q[j] = lo | (hi << 16);
-                    }
-                    const int c = 2 * half + cb;  // 32-column block of the item
-                    uint4 *dst = reinterpret_cast<uint4 *>(g.HP + (size_t)pr * g.Ipad + jn * 128 + 32 * c);
-                    dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
-                    dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
-                    g.HA[((size_t)tile * g.nksI + jn) * kAtom + atom_byte(r, c)] = (uint8_t)(X + 127);
-                }
-            } else {
-                // y * w for 128 of the item's 256 columns of H (rows past the tile's routes are not stored)
-                const int wrow0 = jn * kRowsN;
-                const float wt = valid ? g.hot_w[g.act_off[aidx] + (pr - g.poff[aidx])] : 0.f;
-                if (valid) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int col = wrow0 + half * 128 + 32 * c;
-                        if (col < g.H) {  // H % 32 == 0
-                            float4 *dst = reinterpret_cast<float4 *>(g.YP + (size_t)pr * g.H + col);
-#pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                dst[j] = make_float4(wt * __uint_as_float(v[32 * c + 4 * j]),
-                                                     wt * __uint_as_float(v[32 * c + 4 * j + 1]),
-                                                     wt * __uint_as_float(v[32 * c + 4 * j + 2]),
-                                                     wt * __uint_as_float(v[32 * c + 4 * j + 3]));
-                        }
-                    }
-                }
-            }
+            epilogue_item<kGateUp>(g, v, tile, jn, r, half, aidx, valid, pr);
         }
     }
     tc_fence_before();
@@ -335,6 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tbase, kTmemCols);
 }
+
 
 }  // namespace
 
