@@ -494,49 +494,56 @@ __global__ void __launch_bounds__(kThreads, kRow ? 1 : 4) route_kernel(RoutePara
     // pair issued before the sum (in chunk order), into row t of s_l; warp t then selects from its row.
     const bool rows_by_block = M <= kWarps && p.nchunk <= kMaxChunks;
     if (rows_by_block && kRow) {
-        // whole-row logits: one load per (token, expert), eight per thread in flight
-        constexpr int kPer = 8;
-        for (int q0 = threadIdx.x; q0 < M * E; q0 += kPer * kThreads) {
-            float lv[kPer];
+        // whole-row logits: one load per (token, expert), all of a thread's loads (up to 16) in flight; the
+        // loop runs over tokens and experts directly (a division per element made the code that the
+        // finishing block fetches cold larger: 2430 -> 2518 tokens/s at E = 512, M = 8)
+        for (int e0 = threadIdx.x; e0 < E; e0 += 2 * kThreads) {
+            float lv[kWarps][2];
 #pragma unroll
-            for (int u = 0; u < kPer; ++u) {
-                const int q = q0 + u * kThreads;
-                lv[u] = q < M * E ? __ldcg(p.b.logit_part + q) : 0.f;
-            }
+            for (int t = 0; t < kWarps; ++t)
 #pragma unroll
-            for (int u = 0; u < kPer; ++u) {
-                const int q = q0 + u * kThreads;
-                if (q < M * E) {
-                    const int t = q / E, e = q - t * E;
-                    const float v = lv[u] + s_bias[e];
-                    s_l[t][e] = (v != v) ? -INFINITY : v;  // NaN marks a taken expert below
+                for (int u = 0; u < 2; ++u) {
+                    const int e = e0 + u * kThreads;
+                    lv[t][u] = (t < M && e < E) ? __ldcg(p.b.logit_part + (size_t)t * E + e) : 0.f;
                 }
-            }
+#pragma unroll
+            for (int t = 0; t < kWarps; ++t)
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int e = e0 + u * kThreads;
+                    if (t < M && e < E) {
+                        const float v = lv[t][u] + s_bias[e];
+                        s_l[t][e] = (v != v) ? -INFINITY : v;
+                    }
+                }
         }
         __syncthreads();
     } else if (rows_by_block) {
-        // two (token, expert) pairs per thread and iteration, the loads of both issued before either sum
-        for (int q0 = threadIdx.x; q0 < M * E; q0 += 2 * kThreads) {
-            float pv[2][kMaxChunks];
+        // two experts of a token per thread and iteration, the loads of both issued before either sum (the
+        // loop runs over tokens and experts directly: 866 -> 898 tokens/s at E = 512, M = 1, against a
+        // division per element)
+        for (int t = 0; t < M; ++t)
+            for (int e0 = threadIdx.x; e0 < E; e0 += 2 * kThreads) {
+                float pv[2][kMaxChunks];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int q = q0 + u * kThreads, t = q / E, e = q - t * E;
+                for (int u = 0; u < 2; ++u) {
+                    const int e = e0 + u * kThreads;
 #pragma unroll
-                for (int c = 0; c < kMaxChunks; ++c)
-                    pv[u][c] = (q < M * E && c < p.nchunk) ? __ldcg(p.b.logit_part + ((size_t)c * M + t) * E + e) : 0.f;
+                    for (int c = 0; c < kMaxChunks; ++c)
+                        pv[u][c] = (e < E && c < p.nchunk) ? __ldcg(p.b.logit_part + ((size_t)c * M + t) * E + e) : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int e = e0 + u * kThreads;
+                    if (e >= E) continue;
+                    float v = 0.f;
+#pragma unroll
+                    for (int c = 0; c < kMaxChunks; ++c)
+                        if (c < p.nchunk) v += pv[u][c];
+                    v += s_bias[e];
+                    s_l[t][e] = (v != v) ? -INFINITY : v;  // NaN marks a taken expert below
+                }
             }
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int q = q0 + u * kThreads, t = q / E, e = q - t * E;
-                if (q >= M * E) continue;
-                float v = 0.f;
-#pragma unroll
-                for (int c = 0; c < kMaxChunks; ++c)
-                    if (c < p.nchunk) v += pv[u][c];
-                v += s_bias[e];
-                s_l[t][e] = (v != v) ? -INFINITY : v;  // NaN marks a taken expert below
-            }
-        }
         __syncthreads();
     }
 
