@@ -53,7 +53,11 @@ __global__ void __launch_bounds__(512) stream_read_kernel(const uint4 *src, size
 // their one-byte-per-element shared-memory form), every scale 2^0.  Thread 0 issues iters x 4 MMAs into one
 // 256-column accumulator, then one commit; the CTA waits for it (bounded) and frees tensor memory.
 constexpr int kPkTileA = 128 * 128, kPkTileB = 256 * 128, kPkAtom = 512;
-constexpr int kPkSmem = 1024 + kPkTileA + kPkTileB + 3 * kPkAtom;
+constexpr int kPkUsed = 1024 + kPkTileA + kPkTileB + 3 * kPkAtom;
+// Launched with more shared memory than it uses, so that no SM takes two CTAs (each holds all 512 tensor-memory
+// columns; a second one on the same SM would wait for the first and halve the measured rate).
+constexpr int kPkSmem = 120 * 1024;
+static_assert(kPkUsed <= kPkSmem, "probe shared memory");
 
 __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int *err) {
     using namespace moe::tc;
