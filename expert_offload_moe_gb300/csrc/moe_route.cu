@@ -403,12 +403,13 @@ __global__ void __launch_bounds__(kThreads, kRow ? 1 : 4) route_kernel(RoutePara
                 s_sel_l[warp][rank] = v;
             }
             __syncwarp();
+            const float lmax = s_sel_l[warp][0];
+            const float ej = lane < k ? expf(s_sel_l[warp][lane] - lmax) : 0.f;
+            float den = 0.f;
+            for (int j = 0; j < k; ++j) den += __shfl_sync(0xffffffffu, ej, j);
             if (lane < k) {
-                const float lmax = s_sel_l[warp][0];
-                float den = 0.f;
-                for (int j = 0; j < k; ++j) den += expf(s_sel_l[warp][j] - lmax);
                 const int id = s_sel_id[warp][lane];
-                const float wj = expf(s_sel_l[warp][lane] - lmax) / den;
+                const float wj = ej / den;
                 p.b.topk_ids[(size_t)t * k + lane] = id;
                 p.b.topk_w[(size_t)t * k + lane] = wj;
                 s_ids[t * k + lane] = id;
