@@ -49,3 +49,18 @@ def test_one_rank_is_its_own_time():
     import bench
 
     assert bench.job_rate(100, 25.0, 1, "cpu") == (100 / 0.025, 25.0)
+
+
+def test_traffic_summaries_match_their_kernel_sources():
+    """Every committed ncu traffic summary that the benchmark reads names a kernel source whose current
+    sha256 it was taken on (a stale summary would report no traffic), and the lookup is keyed by kernel,
+    workload and batch: another workload or batch of the same kernel gets none."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    src = os.path.join(ROOT, "expert_offload_moe_gb300", "csrc", "moe_decode_tc.cu")
+    for (kernel, workload, M), fname in bench.TRAFFIC_SUMMARIES.items():
+        got = bench.traffic_for(src, kernel, workload, M)
+        assert got is not None and got > 0, fname
+    assert bench.traffic_for(src, "ffn_tc_kernel", "gptoss20b_h2880_e32k4_resident_m1", 8) is None
+    assert bench.traffic_for(src, "gateup_tc_kernel", "gptoss20b_h2880_e32k4_resident_m1", 1) is None
